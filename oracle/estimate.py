@@ -1,0 +1,118 @@
+"""Inner-product estimator and the three consumers of it (oracle side, fp64).
+
+Estimator ([cnyes] 1 bit 掃尾 / 高精度的那一側「兜住了」; [xujun] 第二步; [suzuke]
+第三步: score = approximation + residual-correction term).  A full-precision
+query q is rotated and sketched once, q' = Pi q and q'' = S q', and a
+compressed key (n, yhat, gamma, sigma) scores
+
+    est(q, x) = n * ( <q', yhat> + gamma * sqrt(pi/2) / m * <q'', sigma> ),
+
+sigma in {-1, +1}^m.  For Gaussian S, E[sign(<s, r>) <s, v>] =
+sqrt(2/pi) <r, v> / ||r||, so E_S[est] = n <q', y> = <q, x> (unbiased); without
+the QJL term an MSE quantizer shrinks inner products ([xujun] 第二步: the 2/pi
+bias of an MSE-optimal 1-bit quantizer).
+
+Consumers:
+* ``logits``  raw estimates for every (query head, cached key), GQA groups of
+  G = Hq / Hkv query heads share one kv head;
+* ``attention`` softmax(scale * logits) over the first seq_len keys, then the
+  weighted sum of MSE-dequantized values, accumulated in the rotated domain and
+  rotated back once: o = Pi_v^T sum_t p_t n_v,t yhat_v,t;
+* ``search`` top-k database rows by estimated inner product, sorted by
+  decreasing score, ties to the smaller id.
+"""
+import numpy as np
+
+
+def prep_query(cb, q):
+    """(q', q'') for query rows q [Q, d_in], zero-padded to d."""
+    q = np.asarray(q, dtype=np.float64)
+    if q.shape[1] < cb.d:
+        q = np.concatenate([q, np.zeros((q.shape[0], cb.d - q.shape[1]))], axis=1)
+    q1 = q @ cb.Pi.T
+    q2 = q1 @ cb.S.T if cb.kind == "prod" else None
+    return q1, q2
+
+
+def estimate(cb, q, code, rows=None, use_fp16_norms=True, qjl=True):
+    """est(q, x) for query rows q [Q, d_in] against coded rows -> [Q, N]."""
+    q1, q2 = prep_query(cb, q)
+    sel = slice(None) if rows is None else rows
+    n = (code["n16"].astype(np.float64) if use_fp16_norms else code["n"])[sel]
+    out = q1 @ code["yhat"][sel].T
+    if cb.kind == "prod" and qjl:
+        g = (code["g16"].astype(np.float64) if use_fp16_norms else code["gamma"])[sel]
+        sgn = np.where(code["sigma"][sel], 1.0, -1.0)
+        out = out + (q2 @ sgn.T) * (g * cb.qjl_const)[None, :]
+    return out * n[None, :]
+
+
+def logits(cb_k, kcode, q, seq_lens, Hkv, capacity):
+    """Raw estimates [B, Hq, capacity]; entries t >= seq_len[b] are NaN.
+
+    ``kcode`` holds rows indexed (b * Hkv + kvh) * capacity + t.
+    """
+    B, Hq, _ = q.shape
+    G = Hq // Hkv
+    out = np.full((B, Hq, capacity), np.nan)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for kvh in range(Hkv):
+            base = (b * Hkv + kvh) * capacity
+            rows = np.arange(base, base + L)
+            out[b, kvh * G:(kvh + 1) * G, :L] = estimate(cb_k, q[b, kvh * G:(kvh + 1) * G], kcode, rows)
+    return out
+
+
+def attention(cb_k, cb_v, kcode, vcode, q, seq_lens, Hkv, capacity, scale, chunk=1 << 16):
+    """Decode attention output [B, Hq, d] (fp64), chunked over tokens."""
+    B, Hq, d = q.shape
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        for kvh in range(Hkv):
+            base = (b * Hkv + kvh) * capacity
+            qs = q[b, kvh * G:(kvh + 1) * G]
+            s = np.concatenate([
+                scale * estimate(cb_k, qs, kcode, np.arange(base + a, base + min(a + chunk, L)))
+                for a in range(0, L, chunk)], axis=1)
+            mx = s.max(axis=1, keepdims=True)
+            p = np.exp(s - mx)
+            den = p.sum(axis=1)
+            acc = np.zeros((G, d))
+            for a in range(0, L, chunk):
+                rows = np.arange(base + a, base + min(a + chunk, L))
+                nv = vcode["n16"][rows].astype(np.float64)
+                acc += (p[:, a:a + len(rows)] * nv[None, :]) @ vcode["yhat"][rows]
+            out[b, kvh * G:(kvh + 1) * G] = (acc / den[:, None]) @ cb_v.Pi
+    return out
+
+
+def topk(scores, k):
+    """Row-wise top-k of ``scores`` [Q, N]: decreasing score, ties to smaller id."""
+    ids = np.argsort(-scores, axis=1, kind="stable")[:, :k]
+    return ids, np.take_along_axis(scores, ids, axis=1)
+
+
+def search(cb, dbcode, q, k, block=1 << 15):
+    """Top-k (ids int64 [Q, k], scores fp64 [Q, k]) over all coded DB rows."""
+    N = dbcode["idx"].shape[0]
+    best_s = np.full((q.shape[0], 0), -np.inf)
+    best_i = np.zeros((q.shape[0], 0), dtype=np.int64)
+    for a in range(0, N, block):
+        rows = np.arange(a, min(a + block, N))
+        s = estimate(cb, q, dbcode, rows)
+        cand_s = np.concatenate([best_s, s], axis=1)
+        cand_i = np.concatenate([best_i, np.broadcast_to(rows, s.shape)], axis=1)
+        order = np.lexsort((cand_i, -cand_s), axis=1)[:, :k]
+        best_s = np.take_along_axis(cand_s, order, axis=1)
+        best_i = np.take_along_axis(cand_i, order, axis=1)
+    return best_i, best_s
+
+
+def recall_1_at_k(true_top1, ids, ks=(1, 2, 4, 8, 10)):
+    """Fraction of queries whose exact top-1 lies among the first k returned ids."""
+    return {k: float(np.mean([t in row[:k] for t, row in zip(true_top1, ids)])) for k in ks}
