@@ -1,0 +1,482 @@
+// C ABI of the TurboQuant hot path: codebook setup, argument validation and
+// kernel launches.  Every declaration is documented in include/tq.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "tq.h"
+#include "tq_internal.cuh"
+#include "tq_math.h"
+
+
+struct tq_codebook {
+  tq::Dev dev;
+  tq_codebook_desc desc;
+  int device;
+  std::vector<float> cent, bound;
+  std::vector<double> pi;
+  std::vector<float> s;
+  std::vector<void*> allocs;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+tq_status fail(tq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+tq_status ok() {
+  g_err.clear();
+  return TQ_OK;
+}
+
+tq_status launched(const char* what, cudaError_t e) {
+  if (e != cudaSuccess) return fail(TQ_ECUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
+constexpr int kTargetCtas = 148 * 4;
+
+template <class T>
+tq_status upload(tq_codebook* cb, const std::vector<T>& h, const T** out) {
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, h.size() * sizeof(T));
+  if (e != cudaSuccess) return fail(TQ_ENOMEM, "cudaMalloc(%zu) failed: %s", h.size() * sizeof(T), cudaGetErrorString(e));
+  cb->allocs.push_back(p);
+  e = cudaMemcpy(p, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(TQ_ECUDA, "cudaMemcpy failed: %s", cudaGetErrorString(e));
+  *out = static_cast<const T*>(p);
+  return TQ_OK;
+}
+
+uint16_t bf16_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+  return (uint16_t)u;
+}
+
+float bf16_value(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+void chunking(int B, int Hkv, int64_t capacity, int* nchunks, int* tiles_per_cta) {
+  const int64_t tiles = (capacity + 15) / 16;
+  if (tiles <= 0) {
+    *nchunks = 1;
+    *tiles_per_cta = 4;
+    return;
+  }
+  const int64_t units = (int64_t)B * Hkv;
+  const int64_t want = std::max<int64_t>(1, (kTargetCtas + units - 1) / units);
+  int64_t tpc = std::max<int64_t>(4, (tiles + want - 1) / want);
+  *tiles_per_cta = (int)tpc;
+  *nchunks = (int)((tiles + tpc - 1) / tpc);
+}
+
+tq_status check_scoring_codebook(const tq_codebook* cb, int kind, const char* what) {
+  if (!cb) return fail(TQ_EINVAL, "%s: codebook is NULL", what);
+  if (cb->dev.kind != kind) return fail(TQ_EINVAL, "%s: codebook has the wrong kind", what);
+  if (cb->dev.d != 128) return fail(TQ_EUNSUPPORTED, "%s: only d = 128 is implemented", what);
+  if (cb->dev.extra != 0) return fail(TQ_EUNSUPPORTED, "%s: mixed-bit caches are not scored yet", what);
+  if (cb->dev.mode != TQ_MODE_SCALAR) return fail(TQ_EUNSUPPORTED, "%s: polar-mode scoring is not implemented", what);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_last_error(void) { return g_err.c_str(); }
+
+static tq_status check_desc(const tq_codebook_desc* desc, const char* what) {
+  const tq_codebook_desc& D = *desc;
+  if (D.d != 128 && D.d != 256) return fail(TQ_EINVAL, "%s: d must be 128 or 256 (got %d)", what, D.d);
+  if (D.kind != TQ_KIND_PROD && D.kind != TQ_KIND_MSE) return fail(TQ_EINVAL, "%s: bad kind %d", what, D.kind);
+  if (D.mode != TQ_MODE_SCALAR && D.mode != TQ_MODE_POLAR) return fail(TQ_EINVAL, "%s: bad mode %d", what, D.mode);
+  const int b1 = D.kind == TQ_KIND_PROD ? D.bits - 1 : D.bits;
+  if (b1 < 1 || b1 > 4 || (D.kind == TQ_KIND_PROD && b1 > 3))
+    return fail(TQ_EINVAL, "%s: bits %d out of range for this kind", what, D.bits);
+  if (D.kind == TQ_KIND_PROD && D.m != D.d) return fail(TQ_EINVAL, "%s: m must equal d", what);
+  if (D.extra != 0 && D.extra != D.d / 4 && D.extra != D.d / 2)
+    return fail(TQ_EINVAL, "%s: extra must be 0, d/4 or d/2", what);
+  if (D.extra != 0 && (D.mode != TQ_MODE_SCALAR || b1 + 1 > 4))
+    return fail(TQ_EINVAL, "%s: extra bits need scalar mode and b' <= 3", what);
+  return TQ_OK;
+}
+
+tq_status tq_host_tables(const tq_codebook_desc* desc, int32_t level, float* centroids, float* boundaries,
+                         double* pi, float* s) {
+  if (!desc) return fail(TQ_EINVAL, "tq_host_tables: NULL descriptor");
+  tq_status st = check_desc(desc, "tq_host_tables");
+  if (st != TQ_OK) return st;
+  const tq_codebook_desc& D = *desc;
+  const int d = D.d;
+  const int b1 = D.kind == TQ_KIND_PROD ? D.bits - 1 : D.bits;
+  const int L = 1 << b1;
+  const int logd = d == 128 ? 7 : 8;
+  if (D.mode == TQ_MODE_SCALAR) {
+    const tqm::Quantizer q = tqm::lloyd_max_beta(d, L);
+    for (int k = 0; k < L && centroids; ++k) centroids[k] = (float)q.c[k];
+    for (int k = 0; k < L - 1 && boundaries; ++k) boundaries[k] = (float)q.t[k];
+  } else {
+    if (level < 1 || level > logd) return fail(TQ_EINVAL, "tq_host_tables: level %d out of 1..%d", level, logd);
+    if (level == 1) {
+      for (int k = 0; k < L && centroids; ++k) centroids[k] = (float)((2.0 * k + 1.0) * M_PI / L);
+      for (int k = 0; k < L - 1 && boundaries; ++k) boundaries[k] = (float)(2.0 * M_PI * (k + 1) / L);
+    } else {
+      const tqm::Quantizer q = tqm::lloyd_max_polar(1 << (level - 1), L);
+      for (int k = 0; k < L && centroids; ++k) centroids[k] = (float)q.c[k];
+      for (int k = 0; k < L - 1 && boundaries; ++k) boundaries[k] = (float)q.t[k];
+    }
+  }
+  if (pi) {
+    const std::vector<double> P = D.pi ? std::vector<double>(D.pi, D.pi + (size_t)d * d) : tqm::haar_rotation(d, D.seed_pi);
+    std::memcpy(pi, P.data(), P.size() * sizeof(double));
+  }
+  if (s && D.kind == TQ_KIND_PROD) {
+    const std::vector<double> g = tqm::gaussians(D.seed_s, (size_t)D.m * d);
+    for (size_t e = 0; e < g.size(); ++e) s[e] = D.s ? D.s[e] : tqm::round_bf16(g[e]);
+  }
+  return ok();
+}
+
+tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
+  if (!desc || !out) return fail(TQ_EINVAL, "tq_make_codebook: NULL argument");
+  *out = nullptr;
+  const tq_codebook_desc& D = *desc;
+  {
+    tq_status st0 = check_desc(desc, "tq_make_codebook");
+    if (st0 != TQ_OK) return st0;
+  }
+  const int b1 = D.kind == TQ_KIND_PROD ? D.bits - 1 : D.bits;
+
+  int device = -1;
+  {
+    const cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return fail(TQ_ECUDA, "tq_make_codebook: no CUDA device: %s", cudaGetErrorString(e));
+  }
+  tq_codebook* cb = new tq_codebook();
+  cb->desc = D;
+  cb->desc.pi = nullptr;
+  cb->desc.s = nullptr;
+  cb->device = device;
+  tq::Dev& dv = cb->dev;
+  std::memset(&dv, 0, sizeof(dv));
+  const int d = D.d;
+  dv.d = d;
+  dv.m = D.kind == TQ_KIND_PROD ? D.m : 0;
+  dv.b1 = b1;
+  dv.kind = D.kind;
+  dv.mode = D.mode;
+  dv.extra = D.extra;
+  dv.P = b1 + (D.kind == TQ_KIND_PROD ? 1 : 0);
+  dv.W = (d / 32) * dv.P + D.extra / 32;
+  dv.nb = D.kind == TQ_KIND_PROD ? 4 : 2;
+  dv.qjl_const = (float)(std::sqrt(M_PI / 2.0) / d);
+  const int L = 1 << b1;
+
+  if (D.mode == TQ_MODE_SCALAR) {
+    const tqm::Quantizer q = tqm::lloyd_max_beta(d, L);
+    cb->cent.resize(L);
+    cb->bound.resize(L - 1);
+    for (int k = 0; k < L; ++k) cb->cent[k] = dv.cent[k] = (float)q.c[k];
+    for (int k = 0; k < L - 1; ++k) cb->bound[k] = dv.bound[k] = (float)q.t[k];
+    if (D.extra) {
+      const tqm::Quantizer qx = tqm::lloyd_max_beta(d, 2 * L);
+      for (int k = 0; k < 2 * L; ++k) dv.cent_x[k] = (float)qx.c[k];
+      for (int k = 0; k < 2 * L - 1; ++k) dv.bound_x[k] = (float)qx.t[k];
+    }
+    // Walsh-Hadamard expansion of the centroid table over the +-1 planes
+    // s'_p = (-1)^(bit p of idx), plane 0 = most significant bit.
+    dv.nv = L / 2;
+    for (int v = 0; v < dv.nv; ++v) {
+      const uint32_t mask = kOddMaskHost[v];
+      double a = 0.0;
+      for (int idx = 0; idx < L; ++idx) {
+        int par = 0;
+        for (int p = 0; p < b1; ++p)
+          if (mask >> p & 1u) par ^= (idx >> (b1 - 1 - p)) & 1;
+        a += (par ? -1.0 : 1.0) * (double)dv.cent[idx];
+      }
+      dv.vmask[v] = mask;
+      dv.vcoef[v] = (float)(a / L);
+    }
+    // the expansion must reproduce every centroid (even subsets vanish for a
+    // symmetric table)
+    for (int idx = 0; idx < L; ++idx) {
+      double r = 0.0;
+      for (int v = 0; v < dv.nv; ++v) {
+        int par = 0;
+        for (int p = 0; p < b1; ++p)
+          if (dv.vmask[v] >> p & 1u) par ^= (idx >> (b1 - 1 - p)) & 1;
+        r += (par ? -1.0 : 1.0) * dv.vcoef[v];
+      }
+      if (std::fabs(r - dv.cent[idx]) > 1e-6 * std::fabs(dv.cent[L - 1])) {
+        delete cb;
+        return fail(TQ_EINVAL, "tq_make_codebook: centroid table is not symmetric");
+      }
+    }
+  } else {
+    const int logd = d == 128 ? 7 : 8;
+    // level 1: uniform quantizer on [0, 2 pi); boundaries inside the first quadrant
+    for (int j = 1; j < L / 4; ++j) {
+      const double t = (double)(float)(2.0 * M_PI * j / L);
+      dv.pb_cos[1][j - 1] = (float)std::cos(t);
+      dv.pb_sin[1][j - 1] = (float)std::sin(t);
+    }
+    for (int k = 0; k < L; ++k) {
+      const double c = (double)(float)((2.0 * k + 1.0) * M_PI / L);
+      dv.pc_cos[1][k] = (float)std::cos(c);
+      dv.pc_sin[1][k] = (float)std::sin(c);
+    }
+    for (int lev = 2; lev <= logd; ++lev) {
+      const tqm::Quantizer q = tqm::lloyd_max_polar(1 << (lev - 1), L);
+      for (int k = 0; k < L - 1; ++k) {
+        const double t = (double)(float)q.t[k];
+        dv.pb_cos[lev][k] = (float)std::cos(t);
+        dv.pb_sin[lev][k] = (float)std::sin(t);
+      }
+      for (int k = 0; k < L; ++k) {
+        const double c = (double)(float)q.c[k];
+        dv.pc_cos[lev][k] = (float)std::cos(c);
+        dv.pc_sin[lev][k] = (float)std::sin(c);
+      }
+      if (lev == 2) {
+        cb->cent.resize(L);
+        cb->bound.resize(L - 1);
+        for (int k = 0; k < L; ++k) cb->cent[k] = (float)q.c[k];
+        for (int k = 0; k < L - 1; ++k) cb->bound[k] = (float)q.t[k];
+      }
+    }
+    dv.nv = 0;
+  }
+
+  // rotation
+  if (D.pi) {
+    cb->pi.assign(D.pi, D.pi + (size_t)d * d);
+  } else {
+    cb->pi = tqm::haar_rotation(d, D.seed_pi);
+  }
+  std::vector<float> pi32((size_t)d * d), piT((size_t)d * d);
+  std::vector<uint16_t> pi_hi((size_t)d * d), pi_lo((size_t)d * d);
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) {
+      const float v = (float)cb->pi[(size_t)i * d + j];
+      pi32[(size_t)i * d + j] = v;
+      piT[(size_t)j * d + i] = v;
+      const uint16_t h = bf16_bits(v);
+      pi_hi[(size_t)i * d + j] = h;
+      pi_lo[(size_t)i * d + j] = bf16_bits(v - bf16_value(h));
+    }
+  tq_status st;
+  if ((st = upload(cb, pi32, &dv.Pi)) != TQ_OK || (st = upload(cb, piT, &dv.PiT)) != TQ_OK ||
+      (st = upload(cb, pi_hi, &dv.Pi_hi)) != TQ_OK || (st = upload(cb, pi_lo, &dv.Pi_lo)) != TQ_OK) {
+    tq_free_codebook(cb);
+    return st;
+  }
+  if (D.kind == TQ_KIND_PROD) {
+    const int m = D.m;
+    cb->s.resize((size_t)m * d);
+    if (D.s) {
+      for (size_t e = 0; e < cb->s.size(); ++e) {
+        if (tqm::round_bf16(D.s[e]) != D.s[e]) {
+          tq_free_codebook(cb);
+          return fail(TQ_EINVAL, "tq_make_codebook: S entries must be bf16-exact");
+        }
+        cb->s[e] = D.s[e];
+      }
+    } else {
+      const std::vector<double> g = tqm::gaussians(D.seed_s, (size_t)m * d);
+      for (size_t e = 0; e < cb->s.size(); ++e) cb->s[e] = tqm::round_bf16(g[e]);
+    }
+    std::vector<float> sT((size_t)d * m);
+    std::vector<uint16_t> sbf((size_t)m * d);
+    for (int j = 0; j < m; ++j)
+      for (int i = 0; i < d; ++i) {
+        sT[(size_t)i * m + j] = cb->s[(size_t)j * d + i];
+        sbf[(size_t)j * d + i] = bf16_bits(cb->s[(size_t)j * d + i]);
+      }
+    if ((st = upload(cb, sT, &dv.ST)) != TQ_OK || (st = upload(cb, sbf, &dv.S_bf)) != TQ_OK) {
+      tq_free_codebook(cb);
+      return st;
+    }
+  }
+  *out = cb;
+  return ok();
+}
+
+void tq_free_codebook(tq_codebook* cb) {
+  if (!cb) return;
+  for (void* p : cb->allocs) cudaFree(p);
+  delete cb;
+}
+
+tq_status tq_codebook_tables(const tq_codebook* cb, float* centroids, float* boundaries, double* pi, float* s) {
+  if (!cb) return fail(TQ_EINVAL, "tq_codebook_tables: NULL codebook");
+  if (centroids) std::memcpy(centroids, cb->cent.data(), cb->cent.size() * sizeof(float));
+  if (boundaries) std::memcpy(boundaries, cb->bound.data(), cb->bound.size() * sizeof(float));
+  if (pi) std::memcpy(pi, cb->pi.data(), cb->pi.size() * sizeof(double));
+  if (s && !cb->s.empty()) std::memcpy(s, cb->s.data(), cb->s.size() * sizeof(float));
+  return ok();
+}
+
+size_t tq_record_bytes(const tq_codebook* cb) { return cb ? (size_t)cb->dev.W * 4 : 0; }
+
+size_t tq_cache_bytes(const tq_codebook* cb, int64_t rows) {
+  if (!cb || rows < 0) return 0;
+  return (size_t)(tq::norm_offset(cb->dev, rows) + rows * cb->dev.nb);
+}
+
+static tq_status quantize_common(const char* what, const tq_codebook* cb, void* cache, int64_t cache_rows,
+                                 const void* x, int32_t x_dtype, int64_t n, int32_t d_in, const float* y,
+                                 const float* norms, const int64_t* dst_rows, void* stream) {
+  if (!cb) return fail(TQ_EINVAL, "%s: codebook is NULL", what);
+  if (n < 0 || cache_rows < 0) return fail(TQ_EINVAL, "%s: negative size", what);
+  if (n == 0) return ok();
+  if (!cache || !aligned16(cache)) return fail(TQ_EINVAL, "%s: cache must be a 16-byte aligned device pointer", what);
+  if (!dst_rows && n > cache_rows) return fail(TQ_EINVAL, "%s: n = %lld rows exceed cache_rows = %lld", what, (long long)n, (long long)cache_rows);
+  if (!y) {
+    if (!x) return fail(TQ_EINVAL, "%s: x is NULL", what);
+    if (x_dtype != TQ_F32 && x_dtype != TQ_BF16) return fail(TQ_EINVAL, "%s: bad dtype %d", what, x_dtype);
+    if (d_in < 1 || d_in > cb->dev.d) return fail(TQ_EINVAL, "%s: d_in = %d must be in 1..%d", what, d_in, cb->dev.d);
+  } else if (!norms) {
+    return fail(TQ_EINVAL, "%s: norms is NULL", what);
+  }
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return launched(what, tq::launch_quantize_simt(cb->dev, static_cast<uint8_t*>(cache), cache_rows, x, x_dtype, n,
+                                                 d_in, y, norms, dst_rows, s));
+}
+
+tq_status tq_quantize(const tq_codebook* cb, void* cache, int64_t cache_rows, const void* x, int32_t x_dtype,
+                      int64_t n, int32_t d_in, const int64_t* dst_rows, void* stream) {
+  return quantize_common("tq_quantize", cb, cache, cache_rows, x, x_dtype, n, d_in, nullptr, nullptr, dst_rows,
+                         stream);
+}
+
+tq_status tq_quantize_rotated(const tq_codebook* cb, void* cache, int64_t cache_rows, const float* y,
+                              const float* norms, int64_t n, const int64_t* dst_rows, void* stream) {
+  if (n > 0 && !y) return fail(TQ_EINVAL, "tq_quantize_rotated: y is NULL");
+  return quantize_common("tq_quantize_rotated", cb, cache, cache_rows, nullptr, TQ_F32, n, cb ? cb->dev.d : 0, y,
+                         norms, dst_rows, stream);
+}
+
+size_t tq_logits_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv) {
+  (void)Hq;
+  if (!kcb || B <= 0 || Hkv <= 0) return 0;
+  return (size_t)tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d));
+}
+
+static tq_status check_heads(const char* what, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || capacity < 0) return fail(TQ_EINVAL, "%s: bad sizes", what);
+  if (Hq % Hkv) return fail(TQ_EINVAL, "%s: Hq = %d is not a multiple of Hkv = %d", what, Hq, Hkv);
+  if (Hq / Hkv > 4) return fail(TQ_EUNSUPPORTED, "%s: GQA groups larger than 4 are not implemented", what);
+  if (B > 65535 || Hkv > 65535 || Hq > 65535) return fail(TQ_EINVAL, "%s: too many heads or sequences", what);
+  return TQ_OK;
+}
+
+tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
+                    const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  tq_status st;
+  if ((st = check_scoring_codebook(kcb, TQ_KIND_PROD, "tq_logits")) != TQ_OK) return st;
+  if ((st = check_heads("tq_logits", B, Hq, Hkv, capacity)) != TQ_OK) return st;
+  if (capacity == 0) return ok();
+  if (!kcache || !seq_lens || !q || !logits || !workspace)
+    return fail(TQ_EINVAL, "tq_logits: NULL device pointer");
+  if (!aligned16(kcache) || !aligned16(q) || !aligned16(logits) || !aligned16(workspace))
+    return fail(TQ_EINVAL, "tq_logits: device pointers must be 16-byte aligned");
+  if (ws_bytes < tq_logits_workspace(kcb, B, Hq, Hkv)) return fail(TQ_ENOMEM, "tq_logits: workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* prep = static_cast<uint8_t*>(workspace);
+  if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+  int nchunks, tpc;
+  chunking(B, Hkv, capacity, &nchunks, &tpc);
+  const int64_t rows = (int64_t)B * Hkv * capacity;
+  return launched("tq_logits", tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
+                                                 rows, seq_lens, prep, logits, nchunks, tpc, s));
+}
+
+size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
+  if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
+  int nchunks, tpc;
+  chunking(B, Hkv, capacity, &nchunks, &tpc);
+  const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d));
+  const int64_t parts = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d) * 4;
+  (void)Hq;
+  return (size_t)(prep + parts);
+}
+
+tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache, const void* vcache,
+                              int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
+                              const float* q, float scale, float* out, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  tq_status st;
+  if ((st = check_scoring_codebook(kcb, TQ_KIND_PROD, "tq_decode_attention(keys)")) != TQ_OK) return st;
+  if ((st = check_scoring_codebook(vcb, TQ_KIND_MSE, "tq_decode_attention(values)")) != TQ_OK) return st;
+  if ((st = check_heads("tq_decode_attention", B, Hq, Hkv, capacity)) != TQ_OK) return st;
+  if (!kcache || !vcache || !seq_lens || !q || !out || !workspace)
+    return fail(TQ_EINVAL, "tq_decode_attention: NULL device pointer");
+  if (!aligned16(kcache) || !aligned16(vcache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
+    return fail(TQ_EINVAL, "tq_decode_attention: device pointers must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(TQ_EINVAL, "tq_decode_attention: scale must be finite");
+  if (ws_bytes < tq_decode_attention_workspace(kcb, B, Hq, Hkv, capacity))
+    return fail(TQ_ENOMEM, "tq_decode_attention: workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* prep = static_cast<uint8_t*>(workspace);
+  float* parts = reinterpret_cast<float*>(
+      prep + tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d)));
+  if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
+    return st;
+  int nchunks, tpc;
+  chunking(B, Hkv, capacity, &nchunks, &tpc);
+  const int64_t rows = (int64_t)B * Hkv * capacity;
+  const float sl2 = scale * 1.4426950408889634f;
+  if ((st = launched("tq_decode_attention",
+                     tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                     static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens, prep,
+                                     sl2, parts, nchunks, tpc, s))) != TQ_OK)
+    return st;
+  return launched("tq_decode_attention/merge",
+                  tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
+}
+
+size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k) {
+  (void)cb; (void)n_db; (void)nq; (void)k;
+  return 0;
+}
+
+tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, const float* q, int32_t nq,
+                    int32_t d_in, int32_t k, int32_t* ids, float* scores, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  (void)cb; (void)db_cache; (void)n_db; (void)q; (void)nq; (void)d_in; (void)k; (void)ids; (void)scores;
+  (void)workspace; (void)ws_bytes; (void)stream;
+  return fail(TQ_EUNSUPPORTED, "tq_search: not implemented yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Internal definitions shared by the CUDA kernels and the C-ABI layer.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tq {
+
+constexpr int kMaxL = 16;        // largest stage-1 cell count (4 bits)
+constexpr int kMaxLevels = 9;    // polar levels for d <= 256
+
+// Codebook as the kernels see it; passed by value as a kernel parameter.
+struct Dev {
+  int d, m, b1, kind, mode, extra;
+  int P;            // stored planes per 32-coordinate word column
+  int W;            // 32-bit words per record
+  int nb;           // norm bytes per row (4 prod, 2 mse)
+  int nv;           // stage-1 virtual planes (odd subsets of the code planes)
+  uint32_t vmask[kMaxL];  // plane p in subset <=> bit p set
+  float vcoef[kMaxL];     // yhat = sum_v vcoef[v] * (-1)^(xor of the subset's bits)
+  float cent[kMaxL], bound[kMaxL];
+  float cent_x[2 * kMaxL], bound_x[2 * kMaxL];
+  float qjl_const;        // sqrt(pi/2) / m
+  // polar mode, per level l = 1..D (index l): boundary and centroid (cos, sin)
+  float pb_cos[kMaxLevels][kMaxL], pb_sin[kMaxLevels][kMaxL];
+  float pc_cos[kMaxLevels][kMaxL], pc_sin[kMaxLevels][kMaxL];
+  // device tables
+  const float* Pi;        // [d][d] row-major, y = Pi x
+  const float* PiT;       // [d][d], PiT[j*d + i] = Pi[i][j]
+  const float* ST;        // [d][m], ST[i*m + j] = S[j][i]
+  const uint16_t* Pi_hi;  // bf16 split of Pi (row-major): Pi ~ hi + lo
+  const uint16_t* Pi_lo;
+  const uint16_t* S_bf;   // bf16 S (exact), row-major [m][d]
+};
+
+inline __host__ __device__ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Byte offset of the norm region of a cache holding `rows` rows.
+inline __host__ __device__ int64_t norm_offset(const Dev& cb, int64_t rows) {
+  return align256(rows * cb.W * 4);
+}
+
+// Per-(sequence, kv head) block of query data prepared once per step.
+//   header: float scale1[4], scale2[4]  (power-of-two scales per head slot)
+//   fragments: [nv + 1][d/16][32 lanes] uint2   (last plane = QJL)
+constexpr int kPrepHeader = 64;
+inline __host__ __device__ int64_t prep_block_bytes(int nv, int d) {
+  return kPrepHeader + (int64_t)(nv + 1) * (d / 16) * 32 * 8;
+}
+
+// Split-KV partial of one warp: per head slot (4): m, l, acc[d].
+inline __host__ __device__ int64_t partial_floats(int d) { return 4 * (2 + d); }
+
+constexpr int kAttnWarps = 4;     // warps per attention / logits CTA
+
+// Host-side launchers (one per kernel family); each returns the launch error.
+cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int x_dtype,
+                                 int64_t n, int d_in, const float* y, const float* norms, const int64_t* dst_rows,
+                                 cudaStream_t s);
+cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s);
+cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
+                          int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
+                          int nchunks, int tiles_per_cta, cudaStream_t s);
+cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache, int B, int Hq,
+                        int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep,
+                        float scale_log2, float* partials, int nchunks, int tiles_per_cta, cudaStream_t s);
+cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts, float* out,
+                              cudaStream_t s);
+
+}  // namespace tq

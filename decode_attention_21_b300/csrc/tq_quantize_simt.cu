@@ -1,0 +1,289 @@
+// Row-wise compression on the CUDA cores (fp32): rotation, stage 1 (scalar
+// Lloyd-Max or recursive polar), QJL sign sketch of the residual, bit-plane
+// packing and fp16 norms.  One warp per row.  Used for fp32 inputs, for
+// already-rotated inputs and for the polar mode; bf16 batches in scalar mode
+// take the tensor-core kernel.
+//
+// [suzuke] "TurboQuant: compressing AI consciousness", 技術上怎麼做到的:
+//   第一步 rotate, 第二步 code at b-1 bits (polar angles, Max-Lloyd),
+//   第三步 1-bit sign of the projected residual.
+// [xujun] note-189244, 第一步 (recursive polar pairing), 第二步 (QJL).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Exact sign of rb*c - ra*s >= 0 for fp32 inputs: the products are exact in
+// fp64 and the sign of their difference is exact.
+__device__ __forceinline__ int ge_exact(float rb, float ra, float c, float s) {
+  const double v = (double)rb * (double)c - (double)ra * (double)s;
+  return v >= 0.0 ? 1 : 0;
+}
+
+// fp32 radius with separately rounded products, sum and square root.
+__device__ __forceinline__ float radius_rn(float a, float b) {
+  return __fsqrt_rn(__fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b)));
+}
+
+// Slot (32*word + bit) of angle j of level `lev` (see the polar layout in tq.h).
+__device__ __forceinline__ int polar_slot(int lev, int j, int logd) {
+  if (lev <= 5) {
+    const int per = 32 >> lev;             // 16, 8, 4, 2, 1 angles per subtree
+    const int base = 32 - (64 >> lev);     // 0, 16, 24, 28, 30
+    return 32 * (j / per) + base + (j % per);
+  }
+  const int heap = ((1 << (logd - lev)) - 1) + j;
+  return 32 * heap + 31;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __restrict__ cache,
+                                                       int64_t cache_rows, const void* __restrict__ x,
+                                                       int x_dtype, int64_t n, int d_in,
+                                                       const float* __restrict__ y_in,
+                                                       const float* __restrict__ n_in,
+                                                       const int64_t* __restrict__ dst_rows) {
+  constexpr int K = D / 32;
+  constexpr int LOGD = D == 128 ? 7 : 8;
+  __shared__ float s_y[8][D];
+  __shared__ float s_a[8][D];
+  __shared__ float s_b[8][D];
+  __shared__ unsigned char s_code[8][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* buf = s_y[warp];
+  uint32_t* recs = reinterpret_cast<uint32_t*>(cache);
+  unsigned char* norms = cache + norm_offset(cb, cache_rows);
+  const int b1 = cb.b1, P = cb.P, W = cb.W;
+  const bool prod = cb.kind == 0;
+  const int64_t stride = (int64_t)gridDim.x * 8;
+
+  for (int64_t row = (int64_t)blockIdx.x * 8 + warp; row < n; row += stride) {
+    float y[K];
+    float nrm;
+    if (y_in) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) y[k] = y_in[row * D + lane + 32 * k];
+      nrm = n_in[row];
+    } else {
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int j = lane + 32 * k;
+        float v = 0.f;
+        if (j < d_in) {
+          if (x_dtype == 0)
+            v = static_cast<const float*>(x)[row * d_in + j];
+          else
+            v = __bfloat162float(static_cast<const __nv_bfloat16*>(x)[row * d_in + j]);
+        }
+        buf[j] = v;
+        y[k] = 0.f;
+      }
+      __syncwarp();
+      for (int j = 0; j < D; ++j) {
+        const float xj = buf[j];
+        const float* prow = cb.PiT + (size_t)j * D + lane;
+#pragma unroll
+        for (int k = 0; k < K; ++k) y[k] = fmaf(__ldg(prow + 32 * k), xj, y[k]);
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < K; ++k) ss = fmaf(y[k], y[k], ss);
+      ss = warp_sum(ss);
+      nrm = sqrtf(ss);
+      const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
+#pragma unroll
+      for (int k = 0; k < K; ++k) y[k] *= inv;
+      __syncwarp();
+    }
+
+    // ---- stage 1
+    int idx[K];
+    float r[K];
+    if (cb.mode == 0) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int i = lane + 32 * k;
+        const float v = y[k];
+        int c = 0;
+        if (i < cb.extra) {
+          const int nbd = (2 << b1) - 1;
+          for (int t = 0; t < nbd; ++t) c += (v >= cb.bound_x[t]) ? 1 : 0;
+          r[k] = v - cb.cent_x[c];
+        } else {
+          const int nbd = (1 << b1) - 1;
+          for (int t = 0; t < nbd; ++t) c += (v >= cb.bound[t]) ? 1 : 0;
+          r[k] = v - cb.cent[c];
+        }
+        idx[k] = c;
+      }
+    } else {
+      // recursive polar: level 1 pairs (y[2a], y[2a+1]), then pairs of radii
+      float* ya = s_a[warp];
+      float* yb = s_b[warp];
+      unsigned char* code = s_code[warp];
+#pragma unroll
+      for (int k = 0; k < K; ++k) buf[lane + 32 * k] = y[k];
+      __syncwarp();
+      const int L = 1 << b1;
+      for (int a = lane; a < D / 2; a += 32) {
+        const float p = buf[2 * a], q = buf[2 * a + 1];
+        int Q = 0;
+        if (p <= 0.f && q > 0.f) Q = 1;
+        else if (p < 0.f && q <= 0.f) Q = 2;
+        else if (p >= 0.f && q < 0.f) Q = 3;
+        const float ar = Q == 0 ? p : (Q == 1 ? q : (Q == 2 ? -p : -q));
+        const float br = Q == 0 ? q : (Q == 1 ? -p : (Q == 2 ? -q : p));
+        int c;
+        if (L == 2) c = Q >> 1;
+        else if (L == 4) c = Q;
+        else {
+          const int per = L / 4;
+          int cnt = 0;
+          for (int j = 0; j < per - 1; ++j) cnt += ge_exact(br, ar, cb.pb_cos[1][j], cb.pb_sin[1][j]);
+          c = Q * per + cnt;
+        }
+        code[polar_slot(1, a, LOGD)] = (unsigned char)c;
+        ya[a] = radius_rn(p, q);
+      }
+      __syncwarp();
+      float* rin = ya;
+      float* rout = yb;
+      for (int lev = 2; lev <= LOGD; ++lev) {
+        const int cnt_ang = D >> lev;
+        for (int j = lane; j < cnt_ang; j += 32) {
+          const float ra = rin[2 * j], rb = rin[2 * j + 1];
+          int c = 0;
+          for (int t = 0; t < L - 1; ++t) c += ge_exact(rb, ra, cb.pb_cos[lev][t], cb.pb_sin[lev][t]);
+          code[polar_slot(lev, j, LOGD)] = (unsigned char)c;
+          rout[j] = radius_rn(ra, rb);
+        }
+        __syncwarp();
+        float* tmp = rin;
+        rin = rout;
+        rout = tmp;
+      }
+      // decode the reproduction, root radius 1
+      if (lane == 0) rin[0] = 1.f;
+      __syncwarp();
+      for (int lev = LOGD; lev >= 2; --lev) {
+        const int cnt_ang = D >> lev;
+        for (int j = lane; j < cnt_ang; j += 32) {
+          const int c = code[polar_slot(lev, j, LOGD)];
+          const float rho = rin[j];
+          rout[2 * j] = rho * cb.pc_cos[lev][c];
+          rout[2 * j + 1] = rho * cb.pc_sin[lev][c];
+        }
+        __syncwarp();
+        float* tmp = rin;
+        rin = rout;
+        rout = tmp;
+      }
+      for (int a = lane; a < D / 2; a += 32) {
+        const int c = code[polar_slot(1, a, LOGD)];
+        rout[2 * a] = rin[a] * cb.pc_cos[1][c];
+        rout[2 * a + 1] = rin[a] * cb.pc_sin[1][c];
+      }
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int i = lane + 32 * k;
+        r[k] = y[k] - rout[i];
+        idx[k] = (i == D - 1) ? 0 : code[i];   // slot view; the last slot is padding
+      }
+      __syncwarp();
+    }
+
+    // ---- pack code planes (bit j of word c <-> coordinate / slot 32c + j)
+    uint32_t mine0 = 0, mine1 = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = lane + 32 * k;
+      const int top = (i < cb.extra) ? (idx[k] >> 1) : idx[k];
+      for (int p = 0; p < b1; ++p) {
+        const uint32_t w = __ballot_sync(kFull, (top >> (b1 - 1 - p)) & 1);
+        const int wi = k * P + p;
+        if ((wi & 31) == lane) {
+          if (wi < 32) mine0 = w; else mine1 = w;
+        }
+      }
+    }
+    for (int k = 0; k < cb.extra / 32; ++k) {
+      const uint32_t w = __ballot_sync(kFull, idx[k] & 1);
+      const int wi = (D / 32) * P + k;
+      if ((wi & 31) == lane) {
+        if (wi < 32) mine0 = w; else mine1 = w;
+      }
+    }
+
+    // ---- QJL: gamma = ||r||, signs of S r
+    float gamma = 0.f;
+    if (prod) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < K; ++k) ss = fmaf(r[k], r[k], ss);
+      gamma = sqrtf(warp_sum(ss));
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < K; ++k) buf[lane + 32 * k] = r[k];
+      __syncwarp();
+      float z[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) z[k] = 0.f;
+      for (int i = 0; i < D; ++i) {
+        const float ri = buf[i];
+        const float* srow = cb.ST + (size_t)i * D + lane;
+#pragma unroll
+        for (int k = 0; k < K; ++k) z[k] = fmaf(__ldg(srow + 32 * k), ri, z[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const uint32_t w = __ballot_sync(kFull, z[k] >= 0.f);
+        const int wi = k * P + b1;
+        if ((wi & 31) == lane) {
+          if (wi < 32) mine0 = w; else mine1 = w;
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- store
+    const int64_t dst = dst_rows ? dst_rows[row] : row;
+    uint32_t* rec = recs + dst * W;
+    if (lane < W) rec[lane] = mine0;
+    if (lane + 32 < W) rec[lane + 32] = mine1;
+    if (lane == 0) {
+      if (prod)
+        reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
+      else
+        reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+    }
+  }
+}
+
+cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int x_dtype,
+                                 int64_t n, int d_in, const float* y, const float* norms, const int64_t* dst_rows,
+                                 cudaStream_t s) {
+  const int64_t blocks64 = (n + 7) / 8;
+  const int blocks = (int)(blocks64 < 148 * 16 ? (blocks64 > 0 ? blocks64 : 1) : 148 * 16);
+  if (cb.d == 128)
+    k_quantize_simt<128><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+  else
+    k_quantize_simt<256><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

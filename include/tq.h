@@ -1,0 +1,185 @@
+/*
+ * tq.h -- C ABI of the TurboQuant hot path on one NVIDIA B300 (sm_103a).
+ *
+ * TurboQuant compresses key/value-cache and search-database vectors online and
+ * without data: a seeded random rotation Pi, a per-coordinate Lloyd-Max code
+ * at b-1 bits (or a recursive-polar code), and a 1-bit QJL sign sketch of the
+ * residual with its norm; compressed keys are scored against full-precision
+ * queries with an unbiased inner-product estimator.  Sources (web pages on
+ * Google Research's TurboQuant, arXiv 2504.19874):
+ *   [xujun]  xujun.org note-189244, sections "第一步：PolarQuant",
+ *            "第二步：QJL", "性能数据";
+ *   [suzuke] suzuke.github.io "TurboQuant: compressing AI consciousness",
+ *            section "技術上怎麼做到的" (第一步, 第二步, 第三步);
+ *   [cnyes]  hao.cnyes.com "TurboQuant", sections "極坐標的妙用", "1 bit 掃尾".
+ *
+ * Conventions for every entry point below
+ *   - Pointers marked "device" are CUDA device pointers on the current device;
+ *     "host" pointers are ordinary CPU memory.  The caller owns all of them.
+ *   - ``stream`` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Hot calls only enqueue work on it: they never allocate memory
+ *     and never synchronise.
+ *   - Arguments are validated on the host before any launch; a bad argument
+ *     returns TQ_EINVAL (or TQ_EUNSUPPORTED for a valid but unimplemented
+ *     shape) and enqueues nothing.  A failed launch returns TQ_ECUDA.
+ *     Errors of work already enqueued surface on a later call or sync.
+ *     tq_last_error() gives a message for the calling thread.
+ *   - All device buffers must be 16-byte aligned.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_EINVAL = 1,        /* invalid argument                                  */
+  TQ_ENOMEM = 2,        /* codebook allocation failed / workspace too small  */
+  TQ_ECUDA = 3,         /* a CUDA runtime call or launch failed              */
+  TQ_ETIMEOUT = 4,      /* a bounded device-side wait gave up                */
+  TQ_EUNSUPPORTED = 5   /* valid request outside the implemented shapes     */
+} tq_status;
+
+typedef enum { TQ_MODE_SCALAR = 0, TQ_MODE_POLAR = 1 } tq_mode;
+
+/* PROD: (b-1)-bit stage 1 + 1-bit QJL sketch; keys and database rows.
+ * MSE:  b-bit stage 1 only; values.                                          */
+typedef enum { TQ_KIND_PROD = 0, TQ_KIND_MSE = 1 } tq_kind;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
+
+/* Everything the method fixes before the first vector arrives.
+ * [suzuke] 第一步 (seeded orthogonal rotation), 第二步 (Max-Lloyd codes at
+ * b-1 bits), 第三步 (1-bit QJL); [xujun] 第一步 (Beta law after rotation).   */
+typedef struct {
+  int32_t d;          /* vector dimension after padding: 128 or 256          */
+  int32_t bits;       /* total bits per coordinate: PROD 2..4, MSE 1..4       */
+  int32_t m;          /* QJL sketch rows; must equal d (ignored for MSE)      */
+  int32_t mode;       /* tq_mode                                             */
+  int32_t kind;       /* tq_kind                                             */
+  int32_t extra;      /* scalar mode: the first `extra` rotated coordinates
+                         get one more stage-1 bit; 0, d/4 or d/2             */
+  uint64_t seed_pi;   /* splitmix64 stream of the Gaussian matrix behind Pi  */
+  uint64_t seed_s;    /* splitmix64 stream of S                               */
+  const double* pi;   /* host, optional: d*d row-major Pi overriding seed_pi */
+  const float* s;     /* host, optional: m*d row-major S (bf16-exact values)
+                         overriding seed_s                                   */
+} tq_codebook_desc;
+
+typedef struct tq_codebook tq_codebook;   /* opaque; immutable once built */
+
+/* Solve the Lloyd-Max tables on the rotated-coordinate law (Beta_d, or the
+ * polar angle laws), draw Pi (Householder QR of a seeded Gaussian matrix,
+ * positive-diagonal R) and S (Gaussian rounded to fp32 then bf16), and upload
+ * them to the current device.  Setup only: allocates device memory and
+ * synchronises.  *out receives the codebook; free it with tq_free_codebook.
+ * Errors: TQ_EINVAL (bad field), TQ_ENOMEM, TQ_ECUDA.                       */
+tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out);
+void tq_free_codebook(tq_codebook* cb);
+
+/* Host copies of the fp32 tables the kernels use, for inspection and tests.
+ * centroids: 2^b' floats, boundaries: 2^b' - 1 floats (b' = stage-1 bits;
+ * scalar mode; polar mode returns the level-2 angle tables).  pi: d*d fp64
+ * row-major, s: m*d fp32 (PROD only).  Any output pointer may be NULL.       */
+tq_status tq_codebook_tables(const tq_codebook* cb, float* centroids, float* boundaries,
+                             double* pi, float* s);
+
+/* Host-only: the tables tq_make_codebook would build for `desc`, computed on
+ * the CPU without touching a device (for inspection and cross-checks).
+ * Scalar mode: centroids 2^b' floats and boundaries 2^b' - 1 floats of the
+ * stage-1 quantizer (level is ignored).  Polar mode: the angle quantizer of
+ * tree level `level` (1 = first pairing of coordinates, up to log2 d).
+ * pi: d*d fp64 row-major; s: m*d fp32 (PROD).  Outputs may be NULL.
+ * Errors: TQ_EINVAL for a bad descriptor or level.                          */
+tq_status tq_host_tables(const tq_codebook_desc* desc, int32_t level, float* centroids, float* boundaries,
+                         double* pi, float* s);
+
+/* Bytes of one packed row record (code planes + sign plane + extra words). */
+size_t tq_record_bytes(const tq_codebook* cb);
+
+/* Bytes of a cache holding `rows` rows: the records, padding to 256 bytes,
+ * then one norm entry per row (PROD: fp16 ||x|| and fp16 ||r||; MSE: fp16
+ * ||x||).  Record layout: word (c, p) at word offset c*P + p (P planes, plane
+ * 0 = most significant stage-1 bit, last plane of PROD = QJL signs), bit j of
+ * word c <-> coordinate 32c + j.                                             */
+size_t tq_cache_bytes(const tq_codebook* cb, int64_t rows);
+
+/* Append / overwrite rows of a packed cache (online per-token compression:
+ * [suzuke] 為什麼這個方法特別聰明, no calibration, no offline pass).
+ *   cache      device, tq_cache_bytes(cb, cache_rows) bytes
+ *   x          device, n x d_in row-major, dtype TQ_F32 or TQ_BF16; d_in <= d
+ *              and columns d_in..d-1 are taken as zero
+ *   dst_rows   device int64[n] target rows (each < cache_rows, distinct), or
+ *              NULL for rows 0..n-1
+ * Each row: n = ||x||, y = Pi x / n, stage-1 codes, r = y - yhat, gamma =
+ * ||r||, sign(S r); n and gamma stored as fp16 (round to nearest even).    */
+tq_status tq_quantize(const tq_codebook* cb, void* cache, int64_t cache_rows,
+                      const void* x, int32_t x_dtype, int64_t n, int32_t d_in,
+                      const int64_t* dst_rows, void* stream);
+
+/* As tq_quantize but from already rotated unit rows: y device fp32 [n, d],
+ * norms device fp32 [n] (stored as ||x||).  The stage-1 codes depend only on
+ * fp32 comparisons of y, so they are reproducible bit for bit.              */
+tq_status tq_quantize_rotated(const tq_codebook* cb, void* cache, int64_t cache_rows,
+                              const float* y, const float* norms, int64_t n,
+                              const int64_t* dst_rows, void* stream);
+
+/* Workspace bytes tq_logits / tq_decode_attention need for B sequences and Hq
+ * query heads (per-step query rotation and sketch, plus split partials).    */
+size_t tq_logits_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv);
+
+/* Attention logits of full-precision queries against compressed keys
+ * ([cnyes] 1 bit 掃尾; [xujun] 第二步 unbiased estimator):
+ *   logits[b, h, t] = n_t ( <Pi q, yhat_t> + gamma_t sqrt(pi/2)/m <S Pi q, sigma_t> )
+ * for t < seq_lens[b]; entries t >= seq_lens[b] are left untouched.
+ *   kcache     device, rows (b*Hkv + kvh)*capacity + t, PROD kind
+ *   seq_lens   device int32[B], each <= capacity
+ *   q          device fp32 [B, Hq, d] (Hq = G*Hkv, G <= 4; head h uses kv
+ *              head h / G)
+ *   logits     device fp32 [B, Hq, capacity]
+ *   workspace  device, >= tq_logits_workspace(kcb, B, Hq, Hkv) bytes        */
+tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq,
+                    int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q,
+                    float* logits, void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of tq_decode_attention. */
+size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq,
+                                     int32_t Hkv, int64_t capacity);
+
+/* Fused decode attention over compressed keys (PROD) and values (MSE):
+ *   s_t = scale * logits[b, h, t], p = softmax over t < seq_lens[b],
+ *   out[b, h] = Pi_v^T sum_t p_t n_v,t yhat_v,t
+ * (weighted sum in the rotated domain, rotated back once per head; fp32
+ * throughout).  seq_lens[b] == 0 gives a zero row.  Split-KV partials live
+ * in the caller's workspace and are merged by a second kernel.              */
+tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb,
+                              const void* kcache, const void* vcache, int32_t B, int32_t Hq,
+                              int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
+                              const float* q, float scale, float* out, void* workspace,
+                              size_t ws_bytes, void* stream);
+
+/* Workspace bytes of tq_search. */
+size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k);
+
+/* Top-k inner-product search over a compressed database ([xujun] 常见问题,
+ * vector search; [cnyes]): score(q, x_i) is the estimator above; returns, per
+ * query, the k best rows by decreasing score, ties to the smaller id.
+ *   db_cache   device, rows 0..n_db-1, PROD kind
+ *   q          device fp32 [nq, d_in], d_in <= d (zero-padded)
+ *   ids        device int32 [nq, k];  scores  device fp32 [nq, k]           */
+tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, const float* q,
+                    int32_t nq, int32_t d_in, int32_t k, int32_t* ids, float* scores,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* tq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H_ */

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the oracle on
+the same seeded inputs.
+
+* quantize from identical rotated fp32 rows: stage-1 codes bit-exact; QJL
+  signs bit-exact except near-ties |z| < 1e-5 * gamma * ||s_j||; fp16 norms
+  exact (n) or within one ulp (gamma, fp32 vs fp64 accumulation);
+* quantize end to end (fp32 and bf16 inputs): <= 0.1% differing code or sign
+  bits, each differing code within 1e-4 / sqrt(d) of a boundary;
+* logits / attention: the GPU scores the oracle's own packed cache; per
+  (sequence, head) row max |diff| <= 1e-3 * max |oracle|, median relative
+  error <= 1e-4 (fp32 accumulation vs fp64).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_21_b300 import tq
+from decode_attention_21_b300 import workloads as wl
+from oracle import estimate, layout, quant
+
+pytestmark = pytest.mark.gpu
+
+KIND = {"prod": tq.KIND_PROD, "mse": tq.KIND_MSE}
+MODE = {"scalar": tq.MODE_SCALAR, "polar": tq.MODE_POLAR}
+
+
+def pair(d, bits, kind="prod", mode="scalar", extra=0, seed_pi=1, seed_s=2):
+    ocb = quant.Codebook(d, bits, kind=kind, mode=mode, extra=extra, seed_pi=seed_pi, seed_s=seed_s)
+    gcb = tq.Codebook(d, bits, KIND[kind], MODE[mode], seed_pi, seed_s, extra=extra)
+    return ocb, gcb
+
+
+def gpu_cache(gcb, rows):
+    return torch.zeros(tq.cache_bytes(gcb, rows), dtype=torch.uint8, device="cuda")
+
+
+def read_back(ocb, rows, buf):
+    return layout.read_cache(ocb, rows, buf.cpu().numpy())
+
+
+def sign_ties(ocb, code, rows=None):
+    """Mask of QJL sign bits whose oracle projection is a near-tie."""
+    z = code["z"] if rows is None else code["z"][rows]
+    g = code["gamma"] if rows is None else code["gamma"][rows]
+    sn = np.linalg.norm(ocb.S, axis=1)
+    return np.abs(z) < 1e-5 * g[:, None] * sn[None, :]
+
+
+CASES = [(128, 2, "prod", "scalar", 0), (128, 3, "prod", "scalar", 0), (128, 4, "prod", "scalar", 0),
+         (128, 1, "mse", "scalar", 0), (128, 3, "mse", "scalar", 0), (128, 4, "mse", "scalar", 0),
+         (128, 3, "prod", "scalar", 32), (128, 2, "prod", "scalar", 64), (256, 2, "prod", "scalar", 0),
+         (256, 4, "prod", "scalar", 0), (128, 3, "prod", "polar", 0), (128, 3, "mse", "polar", 0),
+         (128, 4, "mse", "polar", 0), (256, 3, "prod", "polar", 0)]
+
+
+@pytest.mark.parametrize("d,bits,kind,mode,extra", CASES)
+def test_quantize_rotated_bit_exact(d, bits, kind, mode, extra):
+    ocb, gcb = pair(d, bits, kind, mode, extra)
+    n = 1000 + 37
+    x = np.random.default_rng(d * 10 + bits).standard_normal((n, d)) * 3.0
+    y, nrm = quant.rotate(ocb, x)
+    y32 = y.astype(np.float32)
+    n32 = nrm.astype(np.float32)
+    code = quant.encode_rotated(ocb, y32.astype(np.float64), n32.astype(np.float64))
+    rows = n + 5
+    perm = np.random.default_rng(1).permutation(rows)[:n]
+    cache = gpu_cache(gcb, rows)
+    tq.tq_quantize_rotated(gcb, cache, rows, torch.from_numpy(y32).cuda(), torch.from_numpy(n32).cuda(), n,
+                           dst_rows=torch.from_numpy(perm.astype(np.int64)).cuda())
+    torch.cuda.synchronize()
+    got = read_back(ocb, rows, cache)
+    sel = np.argsort(perm)
+    inv = np.empty(n, dtype=np.int64)
+    inv[:] = perm
+    g_idx = got["idx"][inv]
+    assert np.array_equal(g_idx, code["idx"])
+    assert np.array_equal(got["n16"][inv], code["n16"])
+    if kind == "prod":
+        diff = got["sigma"][inv] != code["sigma"]
+        assert not np.any(diff & ~sign_ties(ocb, code))
+        g16 = got["g16"][inv].astype(np.float64)
+        assert np.all(np.abs(g16 - code["g16"].astype(np.float64)) <= np.spacing(code["g16"]).astype(np.float64) * 1.01)
+    del sel
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,bits,kind,mode,extra", [(128, 3, "prod", "scalar", 0), (128, 4, "prod", "scalar", 0),
+                                                    (128, 3, "mse", "scalar", 0), (128, 2, "prod", "scalar", 32),
+                                                    (256, 2, "prod", "scalar", 0), (128, 3, "prod", "polar", 0)])
+def test_quantize_end_to_end(dtype, d, bits, kind, mode, extra):
+    ocb, gcb = pair(d, bits, kind, mode, extra)
+    d_in = 200 if d == 256 else d
+    if dtype == "f32":
+        x = wl.gaussian_outlier_keys(4096, d_in)
+    else:
+        x = wl.llama_kv_slice(0, 1, 0, 4096, d_in)
+    code = quant.quantize(ocb, x.astype(np.float64))
+    cache = gpu_cache(gcb, len(x))
+    xt = torch.from_numpy(x).cuda()
+    if dtype == "bf16":
+        xt = xt.to(torch.bfloat16)
+    tq.tq_quantize(gcb, cache, len(x), xt, len(x), d_in)
+    torch.cuda.synchronize()
+    got = read_back(ocb, len(x), cache)
+    code_bits = (got["idx"] != code["idx"])
+    nbits = code["idx"].size * ocb.b1
+    flips = code_bits.sum()
+    if kind == "prod":
+        flips += (got["sigma"] != code["sigma"]).sum()
+        nbits += code["sigma"].size
+    assert flips <= 1e-3 * nbits
+    if mode == "scalar" and code_bits.any():
+        y, _ = quant.rotate(ocb, x.astype(np.float64))
+        t = ocb.t.astype(np.float64)
+        dist = np.min(np.abs(y[code_bits][:, None] - t[None, :]), axis=1)
+        assert np.all(dist < 1e-4 / math.sqrt(d))
+    n_ref = np.linalg.norm(x.astype(np.float64), axis=1)
+    assert np.allclose(got["n16"].astype(np.float64), n_ref, rtol=1e-3)
+
+
+def oracle_cache(ocb, rows, x):
+    code = quant.quantize(ocb, x)
+    return code, layout.write_cache(ocb, rows, code)
+
+
+def rowwise_ok(got, ref, tol=1e-3, med=1e-4):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.max(np.abs(ref), axis=-1, keepdims=True)
+    assert np.all(np.abs(got - ref) <= tol * scale + 1e-30), float(np.max(np.abs(got - ref) / scale))
+    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3 * scale)
+    assert np.median(rel) <= med, float(np.median(rel))
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 8, 2, 4096, [4096]), (2, 4, 1, 1000, [1000, 1]),
+                                               (3, 6, 3, 333, [333, 17, 0]), (1, 2, 2, 64, [49])])
+def test_logits_parity(bits, B, Hq, Hkv, cap, lens):
+    ocb, gcb = pair(128, bits)
+    rows = B * Hkv * cap
+    x = wl.gaussian_outlier_keys(rows, 128)
+    code, img = oracle_cache(ocb, rows, x.astype(np.float64))
+    q = wl.queries((B, Hq, 128), name="tiny_q")
+    ref = estimate.logits(ocb, code, q.astype(np.float64), lens, Hkv, cap)
+    kc = torch.from_numpy(img).cuda()
+    ws = torch.empty(tq.tq_logits_workspace(gcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    tq.tq_logits(gcb, kc, B, Hq, Hkv, cap, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                 torch.from_numpy(q).cuda(), out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        L = lens[b]
+        assert np.all(np.isnan(got[b, :, L:]))
+        if L:
+            rowwise_ok(got[b, :, :L], ref[b, :, :L])
+
+
+@pytest.mark.parametrize("kb,vb", [(3, 3), (4, 3), (2, 2), (3, 4), (3, 1)])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 300, [300, 1, 0]),
+                                               (1, 4, 4, 5000, [4999])])
+def test_attention_parity(kb, vb, B, Hq, Hkv, cap, lens):
+    okc, gkc = pair(128, kb, "prod")
+    ovc, gvc = pair(128, vb, "mse", seed_pi=1)
+    rows = B * Hkv * cap
+    K = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="keys") for h in range(B * Hkv)])
+    V = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="values") for h in range(B * Hkv)])
+    kcode, kimg = oracle_cache(okc, rows, K.astype(np.float64))
+    vcode, vimg = oracle_cache(ovc, rows, V.astype(np.float64))
+    q = wl.queries((B, Hq, 128))
+    scale = 1.0 / math.sqrt(128)
+    ref = estimate.attention(okc, ovc, kcode, vcode, q.astype(np.float64), lens, Hkv, cap, scale)
+    ws = torch.empty(tq.tq_decode_attention_workspace(gkc, B, Hq, Hkv, cap), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    tq.tq_decode_attention(gkc, gvc, torch.from_numpy(kimg).cuda(), torch.from_numpy(vimg).cuda(), B, Hq, Hkv, cap,
+                           torch.tensor(lens, dtype=torch.int32, device="cuda"), torch.from_numpy(q).cuda(), scale,
+                           out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        if lens[b] == 0:
+            assert np.all(got[b] == 0)
+        else:
+            rowwise_ok(got[b], ref[b])
+
+
+def test_invalid_arguments_return_status_without_launch():
+    _, gcb = pair(128, 3)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    kc = torch.zeros(tq.cache_bytes(gcb, 64), dtype=torch.uint8, device="cuda")
+    q = torch.zeros(1, 4, 128, device="cuda")
+    out = torch.zeros(1, 4, 64, device="cuda")
+    sl = torch.tensor([64], dtype=torch.int32, device="cuda")
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_logits(gcb, kc, 1, 4, 1, 64, sl, q, out, ws)       # workspace too small
+    assert e.value.status == tq.TQ_ENOMEM
+    ws = torch.empty(tq.tq_logits_workspace(gcb, 1, 4, 1), dtype=torch.uint8, device="cuda")
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_logits(gcb, kc, 1, 12, 1, 64, sl, q, out, ws)      # G = 12 > 4
+    assert e.value.status == tq.TQ_EUNSUPPORTED
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_logits(gcb, kc, 1, 6, 4, 64, sl, q, out, ws)       # Hq not a multiple of Hkv
+    assert e.value.status == tq.TQ_EINVAL
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_quantize(gcb, kc, 64, q.view(-1, 128), 4, 129)     # d_in > d
+    assert e.value.status == tq.TQ_EINVAL
+    _, vcb = pair(128, 3, "mse")
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_logits(vcb, kc, 1, 4, 1, 64, sl, q, out, ws)       # values codebook for keys
+    assert e.value.status == tq.TQ_EINVAL
+    torch.cuda.synchronize()
