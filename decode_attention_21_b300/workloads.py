@@ -92,3 +92,15 @@ def search_rows(n, which="db", n_centres=1000, d_in=200, sigma=0.3, seed=DATA_SE
         a, e = max(start, bi * block), min(start + n, (bi + 1) * block)
         out[a - start:e - start] = x[a - bi * block:e - bi * block]
     return out
+
+
+def llama_kv_torch(n, d, kv_head, seed=DATA_SEED, which="keys", device="cuda", generator_offset=0):
+    """Same recipe as ``llama_kv_slice`` drawn on the GPU with torch's Philox
+    generator (for benchmark-sized caches that are never checked row by row):
+    N(0,1) times the per-(kv-head, channel) scale, rounded to bf16."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + _NAMES[which] * 7919 + int(kv_head) * 104729 + int(generator_offset))
+    s = torch.from_numpy(llama_channel_scale(kv_head, d, seed, which)).to(device=device, dtype=torch.float32)
+    x = torch.randn(n, d, generator=g, device=device, dtype=torch.float32) * s
+    return x.to(torch.bfloat16)
