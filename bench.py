@@ -177,14 +177,18 @@ def timed(dist, fn):
 
 
 def per_call_ms(fn, n):
-    """Average device duration of fn() bracketed by events on the current stream."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    for i in range(n):
-        evs[i][0].record()
-        fn(i)
-        evs[i][1].record()
+    """Average device duration of one fn(i): n calls captured back to back in a
+    CUDA graph, timed with events around the replay on the launching stream
+    (host-side call overhead is excluded, inter-kernel gaps are included)."""
+    g = capture(fn, n)
+    g.replay()
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
 
 
 def cores():

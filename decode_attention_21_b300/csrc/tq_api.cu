@@ -51,7 +51,8 @@ tq_status launched(const char* what, cudaError_t e) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
-constexpr int kTargetCtas = 148 * 4;
+constexpr int kLogitsCtas = 148 * 3;   // resident CTAs of the logits kernel
+constexpr int kAttnCtas = 148 * 2;     // resident CTAs of the attention kernel
 
 template <class T>
 tq_status upload(tq_codebook* cb, const std::vector<T>& h, const T** out) {
@@ -79,7 +80,7 @@ float bf16_value(uint16_t b) {
   return f;
 }
 
-void chunking(int B, int Hkv, int64_t capacity, int* nchunks, int* tiles_per_cta) {
+void chunking(int B, int Hkv, int64_t capacity, int target, int* nchunks, int* tiles_per_cta) {
   const int64_t tiles = (capacity + 15) / 16;
   if (tiles <= 0) {
     *nchunks = 1;
@@ -87,7 +88,7 @@ void chunking(int B, int Hkv, int64_t capacity, int* nchunks, int* tiles_per_cta
     return;
   }
   const int64_t units = (int64_t)B * Hkv;
-  const int64_t want = std::max<int64_t>(1, (kTargetCtas + units - 1) / units);
+  const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
   int64_t tpc = std::max<int64_t>(4, (tiles + want - 1) / want);
   *tiles_per_cta = (int)tpc;
   *nchunks = (int)((tiles + tpc - 1) / tpc);
@@ -416,7 +417,7 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, &nchunks, &tpc);
+  chunking(B, Hkv, capacity, kLogitsCtas, &nchunks, &tpc);
   const int64_t rows = (int64_t)B * Hkv * capacity;
   return launched("tq_logits", tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
                                                  rows, seq_lens, prep, logits, nchunks, tpc, s));
@@ -425,7 +426,7 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
   if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, &nchunks, &tpc);
+  chunking(B, Hkv, capacity, kAttnCtas, &nchunks, &tpc);
   const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d));
   const int64_t parts = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d) * 4;
   (void)Hq;
@@ -454,7 +455,7 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
     return st;
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, &nchunks, &tpc);
+  chunking(B, Hkv, capacity, kAttnCtas, &nchunks, &tpc);
   const int64_t rows = (int64_t)B * Hkv * capacity;
   const float sl2 = scale * 1.4426950408889634f;
   if ((st = launched("tq_decode_attention",

@@ -9,15 +9,24 @@
 //
 // Both inner products are sums over +-1 patterns: sigma is one, and a
 // symmetric 2^b'-cell scalar codebook is exactly a weighted sum of the odd
-// XOR-products of its code planes, yhat = sum_v coef_v * s_v with
-// s_v = (-1)^(xor of the planes in subset v) (a Walsh-Hadamard expansion of
-// the centroid table).  Each +-1 pattern is expanded from a packed word into
-// fp16 tensor-core operands with one shift and one logic op per two
-// coordinates, and the query side (fp32 split into fp16 hi + lo, scaled by a
-// power of two) is the other operand, so the contraction runs on the tensor
-// cores with fp32 accumulation.  The G <= 4 query heads of a GQA group fill
-// the 8 columns of one m16n8k16 tile as (head, hi/lo) pairs.
+// XOR-products of its code planes, yhat = sum_v coef_v s_v with
+// s_v = (-1)^(xor of the planes in subset v) = 1 - 2 b_v (a Walsh-Hadamard
+// expansion of the centroid table).  So every score is a constant per query
+// head plus masked sums  sum_{i : b_v(i) = 1} x_i  of a query-side vector x.
+//
+// Those masked sums run on the tensor cores with the packed bits as the
+// operand: a bit at mantissa position p of a subnormal fp8 (e4m3) or fp16
+// element is the exact value 2^(p - 9) (fp8) or 2^(p - 24) (fp16), so a packed
+// word becomes tensor-core operands with one AND per 4 (fp8) or 2 (fp16)
+// coordinates and a shift per 3 or 4 bit positions; the factor 2^-p goes into
+// the query side (keys) or into a per-row scale (values).
+//   * QK: fp8 m16n8k32, A = key bits (16 keys x 32 coordinates), B = query
+//     side split into four e4m3 pieces (each 16x finer than the last), the
+//     G <= 4 heads x 4 pieces filling two n8 tiles; fp32 accumulation.
+//   * PV: fp16 m16n8k16, A = value bits (16 coordinates x 16 tokens), B =
+//     -2 coef_v p_t n_v,t split into fp16 hi + lo; fp32 accumulation.
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "tq_internal.cuh"
 
@@ -31,14 +40,17 @@ constexpr unsigned kFull = 0xffffffffu;
 // first 2^(b'-1) entries are exactly the odd subsets of b' planes.
 __device__ constexpr uint32_t kOddMask[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
 
-// +-1 fp16 pair from bits beta (low half) and beta + 16 (high half) of w:
-// bit set -> -1, clear -> +1.
-__device__ __forceinline__ uint32_t pm1(uint32_t w, int beta) {
-  return ((w << (15 - beta)) & 0x80008000u) | 0x3C003C00u;
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint2 b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
@@ -52,125 +64,212 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // fp16 piece of x: 0 -> round(x), 1 -> round(x - round(x)).
-__device__ __forceinline__ float piece(float x, int which) {
+__device__ __forceinline__ float piece16(float x, int which) {
   const float hi = __half2float(__float2half_rn(x));
   return which == 0 ? hi : x - hi;
 }
 
-__device__ __forceinline__ float pow2_ceil_scale(float amax) {
-  // power of two s with amax / s <= 64
+// The 8 fp8 operand registers of one packed word: register r holds bits
+// r, r+8, r+16, r+24 (one per byte) at mantissa position r mod 3.
+__device__ __forceinline__ void expand8(uint32_t w, uint32_t (&r)[8]) {
+  const uint32_t w3 = w >> 3, w6 = w >> 6;
+  r[0] = w & 0x01010101u;
+  r[1] = w & 0x02020202u;
+  r[2] = w & 0x04040404u;
+  r[3] = w3 & 0x01010101u;
+  r[4] = w3 & 0x02020202u;
+  r[5] = w3 & 0x04040404u;
+  r[6] = w6 & 0x01010101u;
+  r[7] = w6 & 0x02020202u;
+}
+
+// The 16 fp16 operand registers of one word whose low / high halves hold two
+// tokens' bits of 16 coordinates: register beta holds bits beta and beta+16
+// at mantissa position 6 + (beta mod 4).
+__device__ __forceinline__ void expand16(uint32_t w, uint32_t (&r)[16]) {
+  const uint32_t t0 = w << 6, t1 = w << 2, t2 = w >> 2, t3 = w >> 6;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t m = 0x00400040u << e;
+    r[e] = t0 & m;
+    r[4 + e] = t1 & m;
+    r[8 + e] = t2 & m;
+    r[12 + e] = t3 & m;
+  }
+}
+
+__device__ __forceinline__ float pow2_scale(float amax, float target) {
   if (!(amax > 0.f)) return 1.f;
   int e;
-  frexpf(amax / 64.f, &e);
+  frexpf(amax / target, &e);
   return ldexpf(1.f, e);
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float from_e4m3(uint8_t b) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// k-th e4m3 piece of x: pieces p_0, p_1, ... with x = sum_k p_k 16^-k to
+// within 2^-4 of the last piece's own size.
+__device__ __forceinline__ uint8_t e4m3_piece(float x, int k) {
+  uint8_t p = to_e4m3(x);
+  for (int j = 0; j < k; ++j) {
+    x = (x - from_e4m3(p)) * 16.f;
+    p = to_e4m3(x);
+  }
+  return p;
 }
 
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Query preparation: one CTA per (sequence b, kv head).  q' = Pi q,
-// q'' = S q', then the tensor-core B fragments of every virtual plane and of
-// the sign plane in register order.  MMA k-index 2c + 8h + e of k-block kb
-// maps to coordinate 32 (c + 4 (kb / 8)) + 2 (kb % 8) + h + 16 e.
+// Query preparation: one CTA per (kv head, head slot, sequence).  q' = Pi q,
+// q'' = S q', the per-slot constants and the fp8 B fragments of every stage-1
+// virtual plane and of the sign plane.
+//   header (floats): S1[4], S2[4], K1[4], K2[4]
+//   fragments: [plane][kb][tile][lane] uint2, plane nv = QJL, kb = 0..3,
+//   tile t holds pieces 2t, 2t+1 of the 4 head slots (column 2*slot + piece).
+// Element k = 4c + i (b0) / 4c + 16 + i (b1) of k-block kb is coordinate
+// 32c + 2kb + 8i (+1 for b1); its key bit sits at mantissa position
+// (2kb (+1)) mod 3, whose factor 2^-pos the query side absorbs.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
                                               uint8_t* __restrict__ prep) {
-  const int d = cb.d;
+  constexpr int d = 128;
   const int G = Hq / Hkv;
-  const int kvh = blockIdx.x, b = blockIdx.y;
-  __shared__ float sq[4][256];
-  __shared__ float sq1[4][256];
-  __shared__ float sq2[4][256];
-  __shared__ float sscale[8];
+  const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
+  const bool live = slot < G;
+  __shared__ float sq[d], sq1[d], sq2[d], part[2][d];
+  __shared__ float red[4];
   const int tid = threadIdx.x;
-  for (int e = tid; e < 4 * d; e += blockDim.x) {
-    const int h = e / d, i = e % d;
-    sq[h][i] = h < G ? q[((size_t)b * Hq + kvh * G + h) * d + i] : 0.f;
-  }
+  const int i = tid & 127, half = tid >> 7;
+  if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
-  for (int e = tid; e < 4 * d; e += blockDim.x) {
-    const int h = e / d, i = e % d;
+  {
     float acc = 0.f;
-    for (int j = 0; j < d; ++j) acc = fmaf(cb.PiT[(size_t)j * d + i], sq[h][j], acc);
-    sq1[h][i] = acc;
+    const float* col = cb.PiT + (size_t)(64 * half) * d + i;
+#pragma unroll 8
+    for (int j = 0; j < 64; ++j) acc = fmaf(__ldg(col + (size_t)j * d), sq[64 * half + j], acc);
+    part[half][i] = acc;
   }
   __syncthreads();
-  for (int e = tid; e < 4 * d; e += blockDim.x) {
-    const int h = e / d, j = e % d;
+  if (tid < d) sq1[tid] = part[0][tid] + part[1][tid];
+  __syncthreads();
+  {
     float acc = 0.f;
-    for (int i = 0; i < d; ++i) acc = fmaf(cb.ST[(size_t)i * d + j], sq1[h][i], acc);
-    sq2[h][j] = acc;
+    const float* col = cb.ST + (size_t)(64 * half) * d + i;
+#pragma unroll 8
+    for (int j = 0; j < 64; ++j) acc = fmaf(__ldg(col + (size_t)j * d), sq1[64 * half + j], acc);
+    part[half][i] = acc;
   }
   __syncthreads();
+  if (tid < d) sq2[tid] = part[0][tid] + part[1][tid];
+  __syncthreads();
+  // per-slot scales and constants
+  const int nv = cb.nv;
+  float cmax = 0.f, csum = 0.f;
+  for (int v = 0; v < nv; ++v) {
+    cmax = fmaxf(cmax, fabsf(cb.vcoef[v]));
+    csum += cb.vcoef[v];
+  }
   const int warp = tid >> 5, lane = tid & 31;
-  float cmax = 0.f;
-  for (int v = 0; v < cb.nv; ++v) cmax = fmaxf(cmax, fabsf(cb.vcoef[v]));
-  if (warp < 8) {
-    const int h = warp & 3;
-    const float* src = warp < 4 ? sq1[h] : sq2[h];
-    float m = 0.f;
-    for (int i = lane; i < d; i += 32) m = fmaxf(m, fabsf(src[i]));
+  if (warp < 4) {
+    // warp 0: max |stage-1 B|, 1: max |QJL B|, 2: sum q', 3: sum q''
+    float v = 0.f;
+    for (int k = lane; k < d; k += 32) {
+      const int r = k & 7;  // bit position of coordinate k within its byte
+      const float pf = (float)(512 >> (r % 3));  // 2^(9 - pos)
+      if (warp == 0) v = fmaxf(v, 2.f * cmax * fabsf(sq1[k]) * pf);
+      else if (warp == 1) v = fmaxf(v, 2.f * fabsf(sq2[k]) * pf);
+      else if (warp == 2) v += sq1[k];
+      else v += sq2[k];
+    }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    if (lane == 0) sscale[warp] = pow2_ceil_scale(warp < 4 ? m * cmax : m);
+    for (int o = 16; o; o >>= 1) {
+      const float u = __shfl_xor_sync(kFull, v, o);
+      v = warp < 2 ? fmaxf(v, u) : v + u;
+    }
+    if (lane == 0) red[warp] = v;
   }
   __syncthreads();
-  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(cb.nv, d);
+  const float S1 = pow2_scale(red[0], 224.f), S2 = pow2_scale(red[1], 224.f);
+  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(nv, d);
   float* hdr = reinterpret_cast<float*>(blk);
-  if (tid < 8) hdr[tid] = sscale[tid];
+  if (tid == 0) {
+    hdr[slot] = live ? S1 : 0.f;
+    hdr[4 + slot] = live ? S2 : 0.f;
+    hdr[8 + slot] = live ? csum * red[2] : 0.f;
+    hdr[12 + slot] = live ? -red[3] : 0.f;
+  }
+  // fragments of the lanes whose column belongs to this slot: g = 2*slot + (piece & 1)
   uint2* frag = reinterpret_cast<uint2*>(blk + kPrepHeader);
-  const int KB = d / 16;
-  const int total = (cb.nv + 1) * KB * 32;
+  const int total = (nv + 1) * 4 * 2 * 8;
   for (int e = tid; e < total; e += blockDim.x) {
-    const int ln = e & 31, kb = (e >> 5) % KB, v = (e >> 5) / KB;
-    const int g = ln >> 2, c = ln & 3;
-    const int head = g >> 1, pc = g & 1;
-    const int base = 32 * (c + 4 * (kb / 8)) + 2 * (kb % 8);
-    float vals[4] = {0.f, 0.f, 0.f, 0.f};
-    const int coords[4] = {base, base + 16, base + 1, base + 17};
-    if (head < G) {
-      for (int t = 0; t < 4; ++t) {
-        float x;
-        if (v < cb.nv)
-          x = cb.vcoef[v] * sq1[head][coords[t]] / sscale[head];
-        else
-          x = -sq2[head][coords[t]] / sscale[4 + head];
-        vals[t] = piece(x, pc);
+    const int sub = e & 7, t = (e >> 3) & 1, kb = (e >> 4) & 3, v = e >> 6;
+    const int g = 2 * slot + (sub >> 2), c = sub & 3;
+    const int lnum = g * 4 + c;
+    const int pc = 2 * t + (sub >> 2);
+    uint32_t w[2] = {0u, 0u};
+    if (live) {
+      for (int h = 0; h < 2; ++h) {
+        const int r = 2 * kb + h;
+        const float pf = (float)(512 >> (r % 3));
+        for (int bi = 0; bi < 4; ++bi) {
+          const int k = 32 * c + r + 8 * bi;
+          const float x = v < nv ? -2.f * cb.vcoef[v] * sq1[k] * pf / S1 : 2.f * sq2[k] * pf / S2;
+          w[h] |= (uint32_t)e4m3_piece(x, pc) << (8 * bi);
+        }
       }
     }
-    frag[e] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
+    frag[((v * 4 + kb) * 2 + t) * 32 + lnum] = make_uint2(w[0], w[1]);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Shared QK step for one 16-key tile: thread (g, c) returns the estimates of
-// keys t0+g and t0+g+8 for head slot c.
+// QK for one 16-key tile: thread (g, c) gets the estimates' inner products of
+// keys g and g+8 for head slot c.
 // ---------------------------------------------------------------------------
 template <int NV, int P>
-struct QK {
-  uint2 bq[NV][8];
-  uint2 bs[8];
-  float sc1, sc2;
+struct QK8 {
+  uint2 bq[NV + 1][4][2];
+  float S1, S2, K1, K2;
 
-  __device__ __forceinline__ void load(const Dev& cb, const uint8_t* blk, int lane) {
+  __device__ __forceinline__ void load(const uint8_t* blk, int lane) {
     const float* hdr = reinterpret_cast<const float*>(blk);
     const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
+    for (int v = 0; v <= NV; ++v)
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb) bq[v][kb] = frag[(v * 8 + kb) * 32 + lane];
+      for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-    for (int kb = 0; kb < 8; ++kb) bs[kb] = frag[(NV * 8 + kb) * 32 + lane];
+        for (int t = 0; t < 2; ++t) bq[v][kb][t] = frag[((v * 4 + kb) * 2 + t) * 32 + lane];
     const int c = lane & 3;
-    sc1 = hdr[c];
-    sc2 = hdr[4 + c];
+    S1 = hdr[c];
+    S2 = hdr[4 + c];
+    K1 = hdr[8 + c];
+    K2 = hdr[12 + c];
+  }
+
+  __device__ __forceinline__ void plane(uint32_t xa, uint32_t xb, int v, float (&acc)[2][4]) const {
+    uint32_t ra[8], rb[8];
+    expand8(xa, ra);
+    expand8(xb, rb);
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+      for (int t = 0; t < 2; ++t) mma_e4m3(acc[t], ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb][t]);
   }
 
   // wa, wb: the P plane words (column c) of keys g and g+8
   __device__ __forceinline__ void score(const uint32_t (&wa)[P], const uint32_t (&wb)[P], float& s1a, float& s1b,
                                         float& s2a, float& s2b) const {
-    float acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       uint32_t xa = 0, xb = 0;
@@ -180,19 +279,13 @@ struct QK {
           xa ^= wa[p];
           xb ^= wb[p];
         }
-#pragma unroll
-      for (int kb = 0; kb < 8; ++kb)
-        mma16816(acc1, pm1(xa, 2 * kb), pm1(xb, 2 * kb), pm1(xa, 2 * kb + 1), pm1(xb, 2 * kb + 1), bq[v][kb].x,
-                 bq[v][kb].y);
+      plane(xa, xb, v, acc1);
     }
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb)
-      mma16816(acc2, pm1(wa[P - 1], 2 * kb), pm1(wb[P - 1], 2 * kb), pm1(wa[P - 1], 2 * kb + 1),
-               pm1(wb[P - 1], 2 * kb + 1), bs[kb].x, bs[kb].y);
-    s1a = (acc1[0] + acc1[1]) * sc1;
-    s1b = (acc1[2] + acc1[3]) * sc1;
-    s2a = (acc2[0] + acc2[1]) * sc2;
-    s2b = (acc2[2] + acc2[3]) * sc2;
+    plane(wa[P - 1], wb[P - 1], NV, acc2);
+    s1a = fmaf(S1, acc1[0][0] + 0.0625f * acc1[0][1] + 0.00390625f * acc1[1][0] + 0.000244140625f * acc1[1][1], K1);
+    s1b = fmaf(S1, acc1[0][2] + 0.0625f * acc1[0][3] + 0.00390625f * acc1[1][2] + 0.000244140625f * acc1[1][3], K1);
+    s2a = fmaf(S2, acc2[0][0] + 0.0625f * acc2[0][1] + 0.00390625f * acc2[1][0] + 0.000244140625f * acc2[1][1], K2);
+    s2b = fmaf(S2, acc2[0][2] + 0.0625f * acc2[0][3] + 0.00390625f * acc2[1][2] + 0.000244140625f * acc2[1][3], K2);
   }
 };
 
@@ -211,11 +304,44 @@ __device__ __forceinline__ void load_words(const uint32_t* __restrict__ rec, int
   }
 }
 
+// Key words and norms of one 16-key tile for thread (g, c).
+template <int P>
+struct KTile {
+  uint32_t wa[P], wb[P];
+  uint32_t na, nb;
+  __device__ __forceinline__ void load(const uint32_t* recs, const uint32_t* nrm, int W, int64_t rowbase, int64_t ta,
+                                       int64_t L, int c) {
+    const int64_t tb = ta + 8;
+    if (ta < L) {
+      load_words<P>(recs + (rowbase + ta) * W, c, wa);
+      na = __ldg(nrm + rowbase + ta);
+    } else {
+#pragma unroll
+      for (int p = 0; p < P; ++p) wa[p] = 0;
+      na = 0;
+    }
+    if (tb < L) {
+      load_words<P>(recs + (rowbase + tb) * W, c, wb);
+      nb = __ldg(nrm + rowbase + tb);
+    } else {
+#pragma unroll
+      for (int p = 0; p < P; ++p) wb[p] = 0;
+      nb = 0;
+    }
+  }
+};
+
+__device__ __forceinline__ float est_from(uint32_t nrm_bits, float s1, float s2, float kq) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&nrm_bits);
+  return __low2float(h) * fmaf(__high2float(h) * kq, s2, s1);
+}
+
 // ---------------------------------------------------------------------------
-// Logits: grid (chunks, Hkv, B), 4 warps; each warp scores 16-key tiles.
+// Logits: grid (chunks, Hkv, B), 4 warps; each warp scores 16-key tiles,
+// prefetching its next tile while scoring the current one.
 // ---------------------------------------------------------------------------
 template <int NV, int P>
-__global__ void __launch_bounds__(128) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
+__global__ void __launch_bounds__(128, 3) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
                                                 int64_t capacity, int64_t cache_rows,
                                                 const int32_t* __restrict__ seq_lens,
                                                 const uint8_t* __restrict__ prep, float* __restrict__ logits,
@@ -227,56 +353,66 @@ __global__ void __launch_bounds__(128) k_logits(const Dev cb, const uint8_t* __r
   const int64_t L = seq_lens[b];
   const int64_t ntiles = (L + 15) / 16;
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
-  if (tile0 >= ntiles) return;
-  QK<NV, P> qk;
-  qk.load(cb, prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
+  const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
+  if (tile0 + warp >= tend) return;
+  QK8<NV, P> qk;
+  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
   const float kq = cb.qjl_const;
+  const int W = cb.W;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
-  const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
-  for (int64_t tile = tile0 + warp; tile < tend; tile += 4) {
-    const int64_t ta = tile * 16 + g, tb = ta + 8;
-    uint32_t wa[P], wb[P];
-    uint32_t na = 0, nb = 0;
-    if (ta < L) {
-      load_words<P>(recs + (rowbase + ta) * cb.W, c, wa);
-      na = __ldg(nrm + rowbase + ta);
-    } else {
-#pragma unroll
-      for (int p = 0; p < P; ++p) wa[p] = 0;
-    }
-    if (tb < L) {
-      load_words<P>(recs + (rowbase + tb) * cb.W, c, wb);
-      nb = __ldg(nrm + rowbase + tb);
-    } else {
-#pragma unroll
-      for (int p = 0; p < P; ++p) wb[p] = 0;
-    }
+  KTile<P> cur, nxt;
+  int64_t tile = tile0 + warp;
+  cur.load(recs, nrm, W, rowbase, tile * 16 + g, L, c);
+  for (; tile < tend; tile += 4) {
+    const int64_t tn = tile + 4;
+    if (tn < tend) nxt.load(recs, nrm, W, rowbase, tn * 16 + g, L, c);
     float s1a, s1b, s2a, s2b;
-    qk.score(wa, wb, s1a, s1b, s2a, s2b);
-    const __half2 ha = *reinterpret_cast<const __half2*>(&na);
-    const __half2 hb = *reinterpret_cast<const __half2*>(&nb);
-    const float la = __low2float(ha) * fmaf(__high2float(ha) * kq, s2a, s1a);
-    const float lb = __low2float(hb) * fmaf(__high2float(hb) * kq, s2b, s1b);
+    qk.score(cur.wa, cur.wb, s1a, s1b, s2a, s2b);
+    const int64_t ta = tile * 16 + g, tb = ta + 8;
     if (c < G) {
-      if (ta < L) out[ta] = la;
-      if (tb < L) out[tb] = lb;
+      if (ta < L) out[ta] = est_from(cur.na, s1a, s2a, kq);
+      if (tb < L) out[tb] = est_from(cur.nb, s1b, s2b, kq);
     }
+    cur = nxt;
   }
 }
 
 // ---------------------------------------------------------------------------
 // Fused decode attention: QK as above, online softmax per head slot, and the
 // weighted value sum  acc[i] = sum_t p_t n_v,t yhat_v,t[i]  in the rotated
-// domain, again on the tensor cores: A = value bit patterns (16 coordinates
-// x 16 tokens, two tokens per fp16 pair), B = p_t n_v,t (hi/lo) times the
-// value codebook's coefficients.  Thread (g, c) owns head slot c and
-// coordinates 16g .. 16g+15 of the accumulator.
+// domain on the tensor cores (A = value bits, 16 coordinates x 16 tokens, the
+// two tokens of a pair in the two fp16 halves; B = -2 coef_v p_t n_v,t).
+// Thread (g, c) owns head slot c and coordinates 16g .. 16g+15.
 // ---------------------------------------------------------------------------
+template <int PV>
+struct VTile {
+  uint32_t w[4][PV];
+  float vn0, vn1;
+  __device__ __forceinline__ void load(const uint32_t* vrec, const __half* vnrm, int VW, int64_t rowbase, int64_t t0,
+                                       int64_t L, int g, int c) {
+    const int vword = g >> 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t t = t0 + 2 * c + (j & 1) + 8 * (j >> 1);
+      if (t < L) {
+#pragma unroll
+        for (int p = 0; p < PV; ++p) w[j][p] = __ldg(vrec + (rowbase + t) * VW + vword * PV + p);
+      } else {
+#pragma unroll
+        for (int p = 0; p < PV; ++p) w[j][p] = 0;
+      }
+    }
+    const int64_t ta = t0 + g, tb = ta + 8;
+    vn0 = ta < L ? __half2float(vnrm[rowbase + ta]) : 0.f;
+    vn1 = tb < L ? __half2float(vnrm[rowbase + tb]) : 0.f;
+  }
+};
+
 template <int NVK, int PK, int NVV, int PV>
-__global__ void __launch_bounds__(128) k_attn(const Dev kcb, const Dev vcb, const uint8_t* __restrict__ kcache,
+__global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, const uint8_t* __restrict__ kcache,
                                               const uint8_t* __restrict__ vcache, int Hq, int Hkv, int64_t capacity,
                                               int64_t cache_rows, const int32_t* __restrict__ seq_lens,
                                               const uint8_t* __restrict__ prep, float scale_log2,
@@ -289,119 +425,107 @@ __global__ void __launch_bounds__(128) k_attn(const Dev kcb, const Dev vcb, cons
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
 
-  float m_run = -INFINITY, l_run = 0.f;
+  float m_run = -INFINITY, l_run = 0.f, wsum = 0.f;
   float acc[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
-  if (tile0 < ntiles) {
-    QK<NVK, PK> qk;
-    qk.load(kcb, prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NVK, 128), lane);
-    float vcoef[NVV];
+  if (tile0 + warp < tend) {
+    QK8<NVK, PK> qk;
+    qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NVK, 128), lane);
+    float vcn[NVV];
 #pragma unroll
-    for (int u = 0; u < NVV; ++u) vcoef[u] = vcb.vcoef[u];
+    for (int u = 0; u < NVV; ++u) vcn[u] = -2.f * vcb.vcoef[u];
     const uint32_t* krec = reinterpret_cast<const uint32_t*>(kcache);
     const uint32_t* knrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(kcb, cache_rows));
     const uint32_t* vrec = reinterpret_cast<const uint32_t*>(vcache);
     const __half* vnrm = reinterpret_cast<const __half*>(vcache + norm_offset(vcb, cache_rows));
     const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
     const float kq = kcb.qjl_const;
-    // value tokens used by this thread in a tile: 2c, 2c+1, 2c+8, 2c+9; word g/2
-    const int vword = g >> 1;
+    const int KW = kcb.W, VW = vcb.W;
     const uint32_t vsel = (g & 1) ? 0x7632u : 0x5410u;
     const int hh = g >> 1, pc = g & 1;    // B-fragment column: head slot, piece
     const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
 
-    for (int64_t tile = tile0 + warp; tile < tend; tile += 4) {
-      const int64_t t0 = tile * 16;
-      const int64_t ta = t0 + g, tb = ta + 8;
-      uint32_t wa[PK], wb[PK];
-      uint32_t na = 0, nb = 0;
-      if (ta < L) {
-        load_words<PK>(krec + (rowbase + ta) * kcb.W, c, wa);
-        na = __ldg(knrm + rowbase + ta);
-      } else {
-#pragma unroll
-        for (int p = 0; p < PK; ++p) wa[p] = 0;
+    KTile<PK> kcur, knxt;
+    VTile<PV> vcur, vnxt;
+    int64_t tile = tile0 + warp;
+    kcur.load(krec, knrm, KW, rowbase, tile * 16 + g, L, c);
+    vcur.load(vrec, vnrm, VW, rowbase, tile * 16, L, g, c);
+    for (; tile < tend; tile += 4) {
+      const int64_t tn = tile + 4;
+      if (tn < tend) {
+        knxt.load(krec, knrm, KW, rowbase, tn * 16 + g, L, c);
+        vnxt.load(vrec, vnrm, VW, rowbase, tn * 16, L, g, c);
       }
-      if (tb < L) {
-        load_words<PK>(krec + (rowbase + tb) * kcb.W, c, wb);
-        nb = __ldg(knrm + rowbase + tb);
-      } else {
-#pragma unroll
-        for (int p = 0; p < PK; ++p) wb[p] = 0;
-      }
-      // value words for this thread's four tokens
-      uint32_t vw[4][PV];
-      float vn[2] = {0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t t = t0 + 2 * c + (j & 1) + 8 * (j >> 1);
-        if (t < L) {
-#pragma unroll
-          for (int p = 0; p < PV; ++p) vw[j][p] = __ldg(vrec + (rowbase + t) * vcb.W + vword * PV + p);
-        } else {
-#pragma unroll
-          for (int p = 0; p < PV; ++p) vw[j][p] = 0;
-        }
-      }
-      if (ta < L) vn[0] = __half2float(vnrm[rowbase + ta]);
-      if (tb < L) vn[1] = __half2float(vnrm[rowbase + tb]);
-
+      const int64_t ta = tile * 16 + g, tb = ta + 8;
       float s1a, s1b, s2a, s2b;
-      qk.score(wa, wb, s1a, s1b, s2a, s2b);
-      const __half2 ha = *reinterpret_cast<const __half2*>(&na);
-      const __half2 hb = *reinterpret_cast<const __half2*>(&nb);
+      qk.score(kcur.wa, kcur.wb, s1a, s1b, s2a, s2b);
       // scores in log2 units
-      float sa = ta < L ? __low2float(ha) * fmaf(__high2float(ha) * kq, s2a, s1a) * scale_log2 : -INFINITY;
-      float sb = tb < L ? __low2float(hb) * fmaf(__high2float(hb) * kq, s2b, s1b) * scale_log2 : -INFINITY;
+      const float sa = ta < L ? est_from(kcur.na, s1a, s2a, kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L ? est_from(kcur.nb, s1b, s2b, kq) * scale_log2 : -INFINITY;
       float mx = fmaxf(sa, sb);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-      const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_new);
-      const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_new);
-      float ps = pa + pb;
+      if (__any_sync(kFull, mx > m_run)) {
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+        l_run *= alpha;
+        wsum *= alpha;
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) ps += __shfl_xor_sync(kFull, ps, o);
-      l_run = l_run * alpha + ps;
-      m_run = m_new;
+        for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+          for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        m_run = m_new;
+      }
+      const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
+      const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_run);
+      const float wA = pa * vcur.vn0, wB = pb * vcur.vn1;
+      float ps = pa + pb, ws = wA + wB;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
-      // weights of tokens g and g+8 for head slot c, gathered into B-fragment order
-      const float wA = pa * vn[0], wB = pb * vn[1];
+      for (int o = 4; o < 32; o <<= 1) {
+        ps += __shfl_xor_sync(kFull, ps, o);
+        ws += __shfl_xor_sync(kFull, ws, o);
+      }
+      l_run += ps;
+      wsum += ws;
+      // weights of tokens 2c, 2c+1, 2c+8, 2c+9 for head slot hh, in B-fragment order
       const float w0 = __shfl_sync(kFull, wA, src0);
       const float w1 = __shfl_sync(kFull, wA, src1);
       const float w8 = __shfl_sync(kFull, wB, src0);
       const float w9 = __shfl_sync(kFull, wB, src1);
 #pragma unroll
       for (int u = 0; u < NVV; ++u) {
-        const float cu = vcoef[u];
-        const uint32_t b0 = pack_half2(piece(cu * w0, pc), piece(cu * w1, pc));
-        const uint32_t b1 = pack_half2(piece(cu * w8, pc), piece(cu * w9, pc));
+        const float cu = vcn[u];
+        const uint32_t b0 = pack_half2(piece16(cu * w0, pc), piece16(cu * w1, pc));
+        const uint32_t b1 = pack_half2(piece16(cu * w8, pc), piece16(cu * w9, pc));
         uint32_t x[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t r = 0;
 #pragma unroll
           for (int p = 0; p < PV; ++p)
-            if (kOddMask[u] >> p & 1u) r ^= vw[j][p];
+            if (kOddMask[u] >> p & 1u) r ^= vcur.w[j][p];
           x[j] = r;
         }
-        const uint32_t w01 = __byte_perm(x[0], x[1], vsel);
-        const uint32_t w89 = __byte_perm(x[2], x[3], vsel);
+        uint32_t r01[16], r89[16];
+        expand16(__byte_perm(x[0], x[1], vsel), r01);
+        expand16(__byte_perm(x[2], x[3], vsel), r89);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
-          mma16816(acc[mt], pm1(w01, 2 * mt), pm1(w01, 2 * mt + 1), pm1(w89, 2 * mt), pm1(w89, 2 * mt + 1), b0, b1);
+          mma_f16(acc[mt], r01[2 * mt], r01[2 * mt + 1], r89[2 * mt], r89[2 * mt + 1], b0, b1);
       }
+      kcur = knxt;
+      vcur = vnxt;
     }
   }
-  // write this warp's partial: head slot c, coordinates 16g + 2mt (+1)
+  // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
+  // acc = C0 * wsum + 2^(24 - pos) * D with pos = 6 + (beta mod 4)
+  float c0 = 0.f;
+#pragma unroll
+  for (int u = 0; u < NVV; ++u) c0 += vcb.vcoef[u];
   const int nchunks = gridDim.x;
   float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
   float* ph = part + c * (2 + 128);
@@ -411,8 +535,10 @@ __global__ void __launch_bounds__(128) k_attn(const Dev kcb, const Dev vcb, cons
   }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    ph[2 + 16 * g + 2 * mt] = acc[mt][0] + acc[mt][1];
-    ph[2 + 16 * g + 2 * mt + 1] = acc[mt][2] + acc[mt][3];
+    const int b0 = 2 * mt, b1 = 2 * mt + 1;
+    const float f0 = (float)(1 << (18 - (b0 & 3))), f1 = (float)(1 << (18 - (b1 & 3)));
+    ph[2 + 16 * g + b0] = fmaf(f0, acc[mt][0] + acc[mt][1], c0 * wsum);
+    ph[2 + 16 * g + b1] = fmaf(f1, acc[mt][2] + acc[mt][3], c0 * wsum);
   }
 }
 
@@ -460,7 +586,7 @@ static void attn_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& 
 }
 
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s) {
-  k_prep<<<dim3(Hkv, B), 256, 0, s>>>(cb, q, Hq, Hkv, prep);
+  k_prep<<<dim3(Hkv * 4, B), 256, 0, s>>>(cb, q, Hq, Hkv, prep);
   return cudaGetLastError();
 }
 
