@@ -275,93 +275,120 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
 }
 
 // Latency path for short batches (a decode step appends one vector per kv
-// head): one CTA of D threads per row, thread i owning coordinate i, so each
-// row's two matrix-vector products run as D parallel dot products.  Scalar
-// mode only; same arithmetic and bit layout as k_quantize_simt.
+// head): one CTA per row, 4 threads per coordinate, so each row's two
+// matrix-vector products are 4 x D independent 32-term dot products whose
+// loads are all in flight at once.  Scalar mode only; same arithmetic and bit
+// layout as k_quantize_simt.
 template <int D>
-__global__ void __launch_bounds__(D) k_quantize_row(const Dev cb, uint8_t* __restrict__ cache, int64_t cache_rows,
-                                                    const void* __restrict__ x, int x_dtype, int64_t n, int d_in,
-                                                    const float* __restrict__ y_in, const float* __restrict__ n_in,
-                                                    const int64_t* __restrict__ dst_rows) {
+__device__ __forceinline__ float matvec_quarter(const float* __restrict__ MT, const float* xs, int i, int q) {
+  constexpr int J = D / 4;
+  const float* col = MT + (size_t)(q * J) * D + i;
+  float m[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) m[j] = __ldg(col + (size_t)j * D);
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < J; ++j) acc = fmaf(m[j], xs[q * J + j], acc);
+  return acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* __restrict__ cache, int64_t cache_rows,
+                                                        const void* __restrict__ x, int x_dtype, int64_t n, int d_in,
+                                                        const float* __restrict__ y_in, const float* __restrict__ n_in,
+                                                        const int64_t* __restrict__ dst_rows) {
   constexpr int NW = D / 32;
   __shared__ float xs[D];
+  __shared__ float part[4][D];
   __shared__ float red[NW];
   __shared__ uint32_t words[64];
-  const int i = threadIdx.x, lane = i & 31, w = i >> 5;
+  const int t = threadIdx.x, i = t % D, q = t / D;
+  const int lane = i & 31, w = i >> 5;
   const int b1 = cb.b1, P = cb.P;
   const bool prod = cb.kind == 0;
   uint32_t* recs = reinterpret_cast<uint32_t*>(cache);
   unsigned char* norms = cache + norm_offset(cb, cache_rows);
   for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
-    float y, nrm;
+    float y = 0.f, nrm = 0.f;
     if (y_in) {
-      y = y_in[row * D + i];
-      nrm = n_in[row];
-    } else {
-      float v = 0.f;
-      if (i < d_in) {
-        if (x_dtype == 0)
-          v = static_cast<const float*>(x)[row * d_in + i];
-        else
-          v = __bfloat162float(static_cast<const __nv_bfloat16*>(x)[row * d_in + i]);
+      if (q == 0) {
+        y = y_in[row * D + i];
+        nrm = n_in[row];
       }
-      xs[i] = v;
-      __syncthreads();
-      y = 0.f;
-      const float* col = cb.PiT + i;
-#pragma unroll 8
-      for (int j = 0; j < D; ++j) y = fmaf(__ldg(col + (size_t)j * D), xs[j], y);
-      float ss = warp_sum(y * y);
-      if (lane == 0) red[w] = ss;
-      __syncthreads();
-      ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < NW; ++k) ss += red[k];
-      nrm = sqrtf(ss);
-      y *= nrm > 0.f ? 1.f / nrm : 0.f;
-      __syncthreads();
-    }
-    int idx = 0;
-    float r;
-    if (i < cb.extra) {
-      const int nbd = (2 << b1) - 1;
-      for (int t = 0; t < nbd; ++t) idx += (y >= cb.bound_x[t]) ? 1 : 0;
-      r = y - cb.cent_x[idx];
     } else {
-      const int nbd = (1 << b1) - 1;
-      for (int t = 0; t < nbd; ++t) idx += (y >= cb.bound[t]) ? 1 : 0;
-      r = y - cb.cent[idx];
+      if (q == 0) {
+        float v = 0.f;
+        if (i < d_in) {
+          if (x_dtype == 0)
+            v = static_cast<const float*>(x)[row * d_in + i];
+          else
+            v = __bfloat162float(static_cast<const __nv_bfloat16*>(x)[row * d_in + i]);
+        }
+        xs[i] = v;
+      }
+      __syncthreads();
+      part[q][i] = matvec_quarter<D>(cb.PiT, xs, i, q);
+      __syncthreads();
+      if (q == 0) {
+        y = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
+        const float ss = warp_sum(y * y);
+        if (lane == 0) red[w] = ss;
+      }
+      __syncthreads();
+      if (q == 0) {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) ss += red[k];
+        nrm = sqrtf(ss);
+        y *= nrm > 0.f ? 1.f / nrm : 0.f;
+      }
     }
-    const int top = i < cb.extra ? idx >> 1 : idx;
-    for (int p = 0; p < b1; ++p) {
-      const uint32_t bw = __ballot_sync(kFull, (top >> (b1 - 1 - p)) & 1);
-      if (lane == 0) words[w * P + p] = bw;
+    float r = 0.f;
+    int idx = 0;
+    if (q == 0) {
+      if (i < cb.extra) {
+        const int nbd = (2 << b1) - 1;
+        for (int k = 0; k < nbd; ++k) idx += (y >= cb.bound_x[k]) ? 1 : 0;
+        r = y - cb.cent_x[idx];
+      } else {
+        const int nbd = (1 << b1) - 1;
+        for (int k = 0; k < nbd; ++k) idx += (y >= cb.bound[k]) ? 1 : 0;
+        r = y - cb.cent[idx];
+      }
+      const int top = i < cb.extra ? idx >> 1 : idx;
+      for (int p = 0; p < b1; ++p) {
+        const uint32_t bw = __ballot_sync(kFull, (top >> (b1 - 1 - p)) & 1);
+        if (lane == 0) words[w * P + p] = bw;
+      }
+      if (i < cb.extra) {
+        const uint32_t bw = __ballot_sync(kFull, idx & 1);
+        if (lane == 0) words[NW * P + w] = bw;
+      }
+      if (prod) {
+        xs[i] = r;
+        const float ss = warp_sum(r * r);
+        if (lane == 0) red[w] = ss;
+      }
     }
-    if (i < cb.extra) {
-      const uint32_t bw = __ballot_sync(kFull, idx & 1);
-      if (lane == 0) words[NW * P + w] = bw;
-    }
+    __syncthreads();
     float gamma = 0.f;
     if (prod) {
-      float ss = warp_sum(r * r);
-      if (lane == 0) red[w] = ss;
-      xs[i] = r;
+      part[q][i] = matvec_quarter<D>(cb.ST, xs, i, q);
       __syncthreads();
-      ss = 0.f;
+      if (q == 0) {
+        float ss = 0.f;
 #pragma unroll
-      for (int k = 0; k < NW; ++k) ss += red[k];
-      gamma = sqrtf(ss);
-      float z = 0.f;
-      const float* col = cb.ST + i;
-#pragma unroll 8
-      for (int j = 0; j < D; ++j) z = fmaf(__ldg(col + (size_t)j * D), xs[j], z);
-      const uint32_t bw = __ballot_sync(kFull, z >= 0.f);
-      if (lane == 0) words[w * P + b1] = bw;
+        for (int k = 0; k < NW; ++k) ss += red[k];
+        gamma = sqrtf(ss);
+        const float z = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
+        const uint32_t bw = __ballot_sync(kFull, z >= 0.f);
+        if (lane == 0) words[w * P + b1] = bw;
+      }
     }
     __syncthreads();
     const int64_t dst = dst_rows ? dst_rows[row] : row;
-    if (i < cb.W) recs[dst * cb.W + i] = words[i];
-    if (i == 0) {
+    if (t < cb.W) recs[dst * cb.W + t] = words[t];
+    if (t == 0) {
       if (prod)
         reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
       else
@@ -377,9 +404,9 @@ cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_ro
   if (cb.mode == 0 && n <= 16384) {
     const int blocks = (int)(n < 148 * 16 ? n : 148 * 16);
     if (cb.d == 128)
-      k_quantize_row<128><<<blocks, 128, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+      k_quantize_row<128><<<blocks, 512, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
     else
-      k_quantize_row<256><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+      k_quantize_row<256><<<blocks, 1024, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
     return cudaGetLastError();
   }
   const int64_t blocks64 = (n + 7) / 8;

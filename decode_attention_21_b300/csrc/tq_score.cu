@@ -14,19 +14,18 @@
 // expansion of the centroid table).  So every score is a constant per query
 // head plus masked sums  sum_{i : b_v(i) = 1} x_i  of a query-side vector x.
 //
-// Those masked sums run on the tensor cores with the packed bits as the
-// operand: a bit at mantissa position p of a subnormal fp8 (e4m3) or fp16
-// element is the exact value 2^(p - 9) (fp8) or 2^(p - 24) (fp16), so a packed
-// word becomes tensor-core operands with one AND per 4 (fp8) or 2 (fp16)
-// coordinates and a shift per 3 or 4 bit positions; the factor 2^-p goes into
-// the query side (keys) or into a per-row scale (values).
-//   * QK: fp8 m16n8k32, A = key bits (16 keys x 32 coordinates), B = query
-//     side split into four e4m3 pieces (each 16x finer than the last), the
-//     G <= 4 heads x 4 pieces filling two n8 tiles; fp32 accumulation.
-//   * PV: fp16 m16n8k16, A = value bits (16 coordinates x 16 tokens), B =
-//     -2 coef_v p_t n_v,t split into fp16 hi + lo; fp32 accumulation.
+// Those masked sums run on the tensor cores (fp16 m16n8k16, fp32
+// accumulation) with the packed bits as the operand: a bit at mantissa
+// position p of a subnormal fp16 element is the exact value 2^(p - 24), so a
+// packed word becomes operands with one AND per 2 coordinates and one shift
+// per 4 bit positions; the factor 2^-p goes into the query side (keys) or into
+// a per-row scale (values).
+//   * QK: A = key bits (16 keys x 16 coordinates), B = -2 coef_v q' (or 2 q'')
+//     times 2^(24 - p), split into fp16 hi + lo; the G <= 4 heads x (hi, lo)
+//     fill the 8 columns.
+//   * PV: A = value bits (16 coordinates x 16 tokens), B = -2 coef_v p_t n_v,t
+//     split into fp16 hi + lo.
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "tq_internal.cuh"
 
@@ -39,15 +38,6 @@ constexpr unsigned kFull = 0xffffffffu;
 // Odd subsets of the code planes (bit p <-> plane p) in increasing order; the
 // first 2^(b'-1) entries are exactly the odd subsets of b' planes.
 __device__ constexpr uint32_t kOddMask[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
-
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint2 b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
-}
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -69,23 +59,8 @@ __device__ __forceinline__ float piece16(float x, int which) {
   return which == 0 ? hi : x - hi;
 }
 
-// The 8 fp8 operand registers of one packed word: register r holds bits
-// r, r+8, r+16, r+24 (one per byte) at mantissa position r mod 3.
-__device__ __forceinline__ void expand8(uint32_t w, uint32_t (&r)[8]) {
-  const uint32_t w3 = w >> 3, w6 = w >> 6;
-  r[0] = w & 0x01010101u;
-  r[1] = w & 0x02020202u;
-  r[2] = w & 0x04040404u;
-  r[3] = w3 & 0x01010101u;
-  r[4] = w3 & 0x02020202u;
-  r[5] = w3 & 0x04040404u;
-  r[6] = w6 & 0x01010101u;
-  r[7] = w6 & 0x02020202u;
-}
-
-// The 16 fp16 operand registers of one word whose low / high halves hold two
-// tokens' bits of 16 coordinates: register beta holds bits beta and beta+16
-// at mantissa position 6 + (beta mod 4).
+// The 16 fp16 operand registers of one packed word: register beta holds bits
+// beta and beta+16 (low and high half) at mantissa position 6 + (beta mod 4).
 __device__ __forceinline__ void expand16(uint32_t w, uint32_t (&r)[16]) {
   const uint32_t t0 = w << 6, t1 = w << 2, t2 = w >> 2, t3 = w >> 6;
 #pragma unroll
@@ -105,72 +80,52 @@ __device__ __forceinline__ float pow2_scale(float amax, float target) {
   return ldexpf(1.f, e);
 }
 
-__device__ __forceinline__ uint8_t to_e4m3(float x) {
-  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ float from_e4m3(uint8_t b) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
-  return __half2float(__half(h));
-}
-
-// k-th e4m3 piece of x: pieces p_0, p_1, ... with x = sum_k p_k 16^-k to
-// within 2^-4 of the last piece's own size.
-__device__ __forceinline__ uint8_t e4m3_piece(float x, int k) {
-  uint8_t p = to_e4m3(x);
-  for (int j = 0; j < k; ++j) {
-    x = (x - from_e4m3(p)) * 16.f;
-    p = to_e4m3(x);
-  }
-  return p;
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // Query preparation: one CTA per (kv head, head slot, sequence).  q' = Pi q,
-// q'' = S q', the per-slot constants and the fp8 B fragments of every stage-1
-// virtual plane and of the sign plane.
+// q'' = S q', the per-slot constants and the fp16 B fragments of every
+// stage-1 virtual plane and of the sign plane.
 //   header (floats): S1[4], S2[4], K1[4], K2[4]
-//   fragments: [plane][kb][tile][lane] uint2, plane nv = QJL, kb = 0..3,
-//   tile t holds pieces 2t, 2t+1 of the 4 head slots (column 2*slot + piece).
-// Element k = 4c + i (b0) / 4c + 16 + i (b1) of k-block kb is coordinate
-// 32c + 2kb + 8i (+1 for b1); its key bit sits at mantissa position
-// (2kb (+1)) mod 3, whose factor 2^-pos the query side absorbs.
+//   fragments: [plane][kb][lane] uint2, plane nv = QJL, kb = 0..7, column
+//   2*slot + piece (piece 0 = hi, 1 = lo).
+// Element k = 2c + e (b0) / 2c + 8 + e (b1) of k-block kb is coordinate
+// 32c + beta + 16e with beta = 2kb (b0) or 2kb + 1 (b1); its key bit sits at
+// mantissa position 6 + (beta mod 4), whose factor 2^-(pos - 24) the query
+// side absorbs.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
+__device__ __forceinline__ float dot32(const float* __restrict__ MT, const float* xs, int i, int qt) {
+  constexpr int d = 128;
+  const float* col = MT + (size_t)(32 * qt) * d + i;
+  float m[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) m[j] = __ldg(col + (size_t)j * d);
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc = fmaf(m[j], xs[32 * qt + j], acc);
+  return acc;
+}
+
+__global__ void __launch_bounds__(512) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
                                               uint8_t* __restrict__ prep) {
   constexpr int d = 128;
   const int G = Hq / Hkv;
   const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
   const bool live = slot < G;
-  __shared__ float sq[d], sq1[d], sq2[d], part[2][d];
+  __shared__ float sq[d], sq1[d], sq2[d], part[4][d];
   __shared__ float red[4];
   const int tid = threadIdx.x;
-  const int i = tid & 127, half = tid >> 7;
+  const int i = tid & 127, qt = tid >> 7;
   if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
-  {
-    float acc = 0.f;
-    const float* col = cb.PiT + (size_t)(64 * half) * d + i;
-#pragma unroll 8
-    for (int j = 0; j < 64; ++j) acc = fmaf(__ldg(col + (size_t)j * d), sq[64 * half + j], acc);
-    part[half][i] = acc;
-  }
+  part[qt][i] = dot32(cb.PiT, sq, i, qt);
   __syncthreads();
-  if (tid < d) sq1[tid] = part[0][tid] + part[1][tid];
+  if (tid < d) sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
   __syncthreads();
-  {
-    float acc = 0.f;
-    const float* col = cb.ST + (size_t)(64 * half) * d + i;
-#pragma unroll 8
-    for (int j = 0; j < 64; ++j) acc = fmaf(__ldg(col + (size_t)j * d), sq1[64 * half + j], acc);
-    part[half][i] = acc;
-  }
+  part[qt][i] = dot32(cb.ST, sq1, i, qt);
   __syncthreads();
-  if (tid < d) sq2[tid] = part[0][tid] + part[1][tid];
+  if (tid < d) sq2[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
   __syncthreads();
-  // per-slot scales and constants
   const int nv = cb.nv;
   float cmax = 0.f, csum = 0.f;
   for (int v = 0; v < nv; ++v) {
@@ -179,13 +134,12 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   }
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < 4) {
-    // warp 0: max |stage-1 B|, 1: max |QJL B|, 2: sum q', 3: sum q''
+    // warp 0: max |stage-1 B|, 1: max |QJL B| (before the mantissa factor),
+    // 2: sum q', 3: sum q''
     float v = 0.f;
     for (int k = lane; k < d; k += 32) {
-      const int r = k & 7;  // bit position of coordinate k within its byte
-      const float pf = (float)(512 >> (r % 3));  // 2^(9 - pos)
-      if (warp == 0) v = fmaxf(v, 2.f * cmax * fabsf(sq1[k]) * pf);
-      else if (warp == 1) v = fmaxf(v, 2.f * fabsf(sq2[k]) * pf);
+      if (warp == 0) v = fmaxf(v, 2.f * cmax * fabsf(sq1[k]));
+      else if (warp == 1) v = fmaxf(v, 2.f * fabsf(sq2[k]));
       else if (warp == 2) v += sq1[k];
       else v += sq2[k];
     }
@@ -197,7 +151,8 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
     if (lane == 0) red[warp] = v;
   }
   __syncthreads();
-  const float S1 = pow2_scale(red[0], 224.f), S2 = pow2_scale(red[1], 224.f);
+  // largest mantissa factor 2^(24 - 6) = 2^18; keep |B| <= 2^14
+  const float S1 = pow2_scale(red[0] * 262144.f, 16384.f), S2 = pow2_scale(red[1] * 262144.f, 16384.f);
   uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(nv, d);
   float* hdr = reinterpret_cast<float*>(blk);
   if (tid == 0) {
@@ -206,37 +161,34 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
     hdr[8 + slot] = live ? csum * red[2] : 0.f;
     hdr[12 + slot] = live ? -red[3] : 0.f;
   }
-  // fragments of the lanes whose column belongs to this slot: g = 2*slot + (piece & 1)
+  // fragments of the 8 lanes whose column belongs to this slot (g = 2 slot + piece)
   uint2* frag = reinterpret_cast<uint2*>(blk + kPrepHeader);
-  const int total = (nv + 1) * 4 * 2 * 8;
+  const int total = (nv + 1) * 8 * 8;
   for (int e = tid; e < total; e += blockDim.x) {
-    const int sub = e & 7, t = (e >> 3) & 1, kb = (e >> 4) & 3, v = e >> 6;
-    const int g = 2 * slot + (sub >> 2), c = sub & 3;
-    const int lnum = g * 4 + c;
-    const int pc = 2 * t + (sub >> 2);
-    uint32_t w[2] = {0u, 0u};
+    const int sub = e & 7, kb = (e >> 3) & 7, v = e >> 6;
+    const int pc = sub >> 2, c = sub & 3;
+    const int g = 2 * slot + pc;
+    float vals[4] = {0.f, 0.f, 0.f, 0.f};
     if (live) {
-      for (int h = 0; h < 2; ++h) {
-        const int r = 2 * kb + h;
-        const float pf = (float)(512 >> (r % 3));
-        for (int bi = 0; bi < 4; ++bi) {
-          const int k = 32 * c + r + 8 * bi;
-          const float x = v < nv ? -2.f * cb.vcoef[v] * sq1[k] * pf / S1 : 2.f * sq2[k] * pf / S2;
-          w[h] |= (uint32_t)e4m3_piece(x, pc) << (8 * bi);
-        }
+      for (int t = 0; t < 4; ++t) {
+        const int beta = 2 * kb + (t >> 1);
+        const int k = 32 * c + beta + 16 * (t & 1);
+        const float pf = (float)(1 << (18 - (beta & 3)));
+        const float x = v < nv ? -2.f * cb.vcoef[v] * sq1[k] * pf / S1 : 2.f * sq2[k] * pf / S2;
+        vals[t] = piece16(x, pc);
       }
     }
-    frag[((v * 4 + kb) * 2 + t) * 32 + lnum] = make_uint2(w[0], w[1]);
+    frag[(v * 8 + kb) * 32 + g * 4 + c] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
   }
 }
 
 // ---------------------------------------------------------------------------
-// QK for one 16-key tile: thread (g, c) gets the estimates' inner products of
-// keys g and g+8 for head slot c.
+// QK for one 16-key tile: thread (g, c) gets the two inner products of keys
+// g and g+8 for head slot c.
 // ---------------------------------------------------------------------------
 template <int NV, int P>
-struct QK8 {
-  uint2 bq[NV + 1][4][2];
+struct QK16 {
+  uint2 bq[NV + 1][8];
   float S1, S2, K1, K2;
 
   __device__ __forceinline__ void load(const uint8_t* blk, int lane) {
@@ -245,9 +197,7 @@ struct QK8 {
 #pragma unroll
     for (int v = 0; v <= NV; ++v)
 #pragma unroll
-      for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) bq[v][kb][t] = frag[((v * 4 + kb) * 2 + t) * 32 + lane];
+      for (int kb = 0; kb < 8; ++kb) bq[v][kb] = frag[(v * 8 + kb) * 32 + lane];
     const int c = lane & 3;
     S1 = hdr[c];
     S2 = hdr[4 + c];
@@ -255,21 +205,20 @@ struct QK8 {
     K2 = hdr[12 + c];
   }
 
-  __device__ __forceinline__ void plane(uint32_t xa, uint32_t xb, int v, float (&acc)[2][4]) const {
-    uint32_t ra[8], rb[8];
-    expand8(xa, ra);
-    expand8(xb, rb);
+  __device__ __forceinline__ void plane(uint32_t xa, uint32_t xb, int v, float (&acc)[4]) const {
+    uint32_t ra[16], rb[16];
+    expand16(xa, ra);
+    expand16(xb, rb);
 #pragma unroll
-    for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-      for (int t = 0; t < 2; ++t) mma_e4m3(acc[t], ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb][t]);
+    for (int kb = 0; kb < 8; ++kb)
+      mma_f16(acc, ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
   }
 
   // wa, wb: the P plane words (column c) of keys g and g+8
   __device__ __forceinline__ void score(const uint32_t (&wa)[P], const uint32_t (&wb)[P], float& s1a, float& s1b,
                                         float& s2a, float& s2b) const {
-    float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       uint32_t xa = 0, xb = 0;
@@ -282,10 +231,10 @@ struct QK8 {
       plane(xa, xb, v, acc1);
     }
     plane(wa[P - 1], wb[P - 1], NV, acc2);
-    s1a = fmaf(S1, acc1[0][0] + 0.0625f * acc1[0][1] + 0.00390625f * acc1[1][0] + 0.000244140625f * acc1[1][1], K1);
-    s1b = fmaf(S1, acc1[0][2] + 0.0625f * acc1[0][3] + 0.00390625f * acc1[1][2] + 0.000244140625f * acc1[1][3], K1);
-    s2a = fmaf(S2, acc2[0][0] + 0.0625f * acc2[0][1] + 0.00390625f * acc2[1][0] + 0.000244140625f * acc2[1][1], K2);
-    s2b = fmaf(S2, acc2[0][2] + 0.0625f * acc2[0][3] + 0.00390625f * acc2[1][2] + 0.000244140625f * acc2[1][3], K2);
+    s1a = fmaf(S1, acc1[0] + acc1[1], K1);
+    s1b = fmaf(S1, acc1[2] + acc1[3], K1);
+    s2a = fmaf(S2, acc2[0] + acc2[1], K2);
+    s2b = fmaf(S2, acc2[2] + acc2[3], K2);
   }
 };
 
@@ -355,7 +304,7 @@ __global__ void __launch_bounds__(128, 3) k_logits(const Dev cb, const uint8_t* 
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
   if (tile0 + warp >= tend) return;
-  QK8<NV, P> qk;
+  QK16<NV, P> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
@@ -433,7 +382,7 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
   if (tile0 + warp < tend) {
-    QK8<NVK, PK> qk;
+    QK16<NVK, PK> qk;
     qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NVK, 128), lane);
     float vcn[NVV];
 #pragma unroll
@@ -586,7 +535,7 @@ static void attn_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& 
 }
 
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s) {
-  k_prep<<<dim3(Hkv * 4, B), 256, 0, s>>>(cb, q, Hq, Hkv, prep);
+  k_prep<<<dim3(Hkv * 4, B), 512, 0, s>>>(cb, q, Hq, Hkv, prep);
   return cudaGetLastError();
 }
 
