@@ -18,10 +18,14 @@ struct tq_codebook {
   tq::Dev dev;
   tq_codebook_desc desc;
   int device;
+  int sms;
   std::vector<float> cent, bound;
   std::vector<double> pi;
   std::vector<float> s;
   std::vector<void*> allocs;
+  bool tc_ready;                  // tensor maps of Pi_hi, Pi_lo, S built
+  CUtensorMap tm_pihi, tm_pilo, tm_s;
+  int* d_status;                  // device word set by a kernel whose bounded wait gave up
 };
 
 namespace {
@@ -49,6 +53,37 @@ tq_status launched(const char* what, cudaError_t e) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 row-major [rows, cols] matrix, 128-byte swizzled boxes of 64 columns x 128 rows.
+bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
 constexpr int kLogitsCtas = 148 * 3;   // resident CTAs of the logits kernel
@@ -325,7 +360,39 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
       return st;
     }
   }
+  {
+    std::vector<int> zero(4, 0);
+    const int* dst = nullptr;
+    if ((st = upload(cb, zero, &dst)) != TQ_OK) {
+      tq_free_codebook(cb);
+      return st;
+    }
+    cb->d_status = const_cast<int*>(dst);
+  }
+  cudaDeviceGetAttribute(&cb->sms, cudaDevAttrMultiProcessorCount, cb->device);
+  cb->tc_ready = false;
+  if (D.mode == TQ_MODE_SCALAR && d == 128) {
+    bool good = encode_bf16_rows(&cb->tm_pihi, dv.Pi_hi, d, d) && encode_bf16_rows(&cb->tm_pilo, dv.Pi_lo, d, d);
+    if (D.kind == TQ_KIND_PROD) good = good && encode_bf16_rows(&cb->tm_s, dv.S_bf, D.m, d);
+    else cb->tm_s = cb->tm_pihi;
+    cb->tc_ready = good;
+  }
   *out = cb;
+  return ok();
+}
+
+tq_status tq_check_device(const tq_codebook* cb) {
+  if (!cb) return fail(TQ_EINVAL, "tq_check_device: NULL codebook");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(TQ_ECUDA, "tq_check_device: %s", cudaGetErrorString(e));
+  int flag = 0;
+  e = cudaMemcpy(&flag, cb->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(TQ_ECUDA, "tq_check_device: %s", cudaGetErrorString(e));
+  if (flag) {
+    const int zero = 0;
+    cudaMemcpy(cb->d_status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return fail(TQ_ETIMEOUT, "tq_check_device: a kernel's bounded wait on its copies or MMAs gave up");
+  }
   return ok();
 }
 
@@ -370,6 +437,14 @@ static tq_status quantize_common(const char* what, const tq_codebook* cb, void* 
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // bf16 batches in scalar mode: tensor-core rotation and sketch
+  if (!y && x_dtype == TQ_BF16 && cb->tc_ready && n >= 2048 && d_in % 8 == 0 && aligned16(x) && n < (1ll << 31)) {
+    CUtensorMap tm_x;
+    if (encode_bf16_rows(&tm_x, x, n, d_in))
+      return launched(what, tq::launch_quantize_tc(tm_x, cb->tm_pihi, cb->tm_pilo, cb->tm_s, cb->dev,
+                                                   static_cast<uint8_t*>(cache), cache_rows, n, dst_rows,
+                                                   cb->d_status, cb->sms, s));
+  }
   return launched(what, tq::launch_quantize_simt(cb->dev, static_cast<uint8_t*>(cache), cache_rows, x, x_dtype, n,
                                                  d_in, y, norms, dst_rows, s));
 }

@@ -1,6 +1,7 @@
 // Internal definitions shared by the CUDA kernels and the C-ABI layer.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace tq {
@@ -56,6 +57,9 @@ constexpr int kAttnWarps = 4;     // warps per attention / logits CTA
 cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int x_dtype,
                                  int64_t n, int d_in, const float* y, const float* norms, const int64_t* dst_rows,
                                  cudaStream_t s);
+cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
+                               const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
+                               const int64_t* dst_rows, int* status, int sms, cudaStream_t s);
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s);
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,

@@ -1,0 +1,353 @@
+// Batch compression on the 5th-generation tensor cores (tcgen05 + TMEM, fed
+// by TMA): the two dense contractions of the method, the rotation
+// Y = X Pi^T and the QJL projection Z = R S^T, for 128-row tiles of bf16
+// input vectors (d = 128, scalar stage 1).
+//
+// [suzuke] "TurboQuant: compressing AI consciousness", 技術上怎麼做到的:
+//   第一步 multiply by the random orthogonal matrix, 第二步 Max-Lloyd code per
+//   coordinate, 第三步 1-bit sign of the projected residual.
+//
+// Per tile (persistent CTAs, 16 warps):
+//   TMA: X tile (128 x 128 bf16, 128B-swizzled, two 64-column blocks); Pi and
+//        S once per CTA.
+//   MMA (one thread): Y = X Pi_hi^T + X Pi_lo^T into TMEM columns 0..127
+//        (Pi = Pi_hi + Pi_lo, both bf16: fp32-accurate rotation of bf16 x).
+//   epilogue 1 (warp w: TMEM lanes 32 (w%4).., columns 32 (w/4)..): n = ||y||,
+//        codes by compare-count against the boundaries, code-plane words,
+//        residual r = y/n - yhat written to shared memory as bf16 hi + lo in
+//        the MMA's swizzled K-major layout.
+//   MMA: Z = R_hi S^T + R_lo S^T into TMEM columns 128..255.
+//   epilogue 2: sign words of Z, gamma = ||r||, record and fp16 norms.
+// Every wait on an mbarrier is bounded; on a timeout the kernel records an
+// error code, waits (bounded) for its own copies and MMAs, frees its TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kThreads = 512;
+constexpr uint32_t kBlockBytes = kRows * 128;          // 64 bf16 columns x 128 rows
+constexpr uint32_t kTileBytes = 2 * kBlockBytes;       // 128 columns
+// shared memory map (offsets from a 1024-aligned base)
+constexpr uint32_t kOffX = 0;                          // 2 stages x kTileBytes (R_hi reuses the stage)
+constexpr uint32_t kOffPiHi = 2 * kTileBytes;
+constexpr uint32_t kOffPiLo = kOffPiHi + kTileBytes;
+constexpr uint32_t kOffS = kOffPiLo + kTileBytes;
+constexpr uint32_t kOffRlo = kOffS + kTileBytes;
+constexpr uint32_t kOffRed = kOffRlo + kTileBytes;     // float red1[4][128], red2[4][128]
+constexpr uint32_t kOffBar = kOffRed + 2 * 4 * kRows * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 256;
+constexpr long long kSpinLimit = 1ll << 26;
+
+// kind::f16 instruction descriptor: D = F32, A = B = BF16, both K-major,
+// N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_quantize_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pihi,
+                  const __grid_constant__ CUtensorMap tm_pilo, const __grid_constant__ CUtensorMap tm_s, const Dev cb,
+                  uint8_t* __restrict__ cache, int64_t cache_rows, int64_t n, const int64_t* __restrict__ dst_rows,
+                  int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, cg = warp >> 2;
+  const int m = 32 * q + lane;                       // tile row = TMEM lane
+  float* red1 = reinterpret_cast<float*>(smem + kOffRed);
+  float* red2 = red1 + 4 * kRows;
+  const uint32_t bar_full0 = sbase + kOffBar, bar_const = bar_full0 + 16, bar_mma1 = bar_full0 + 24,
+                 bar_mma2 = bar_full0 + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 48);
+  const int64_t ntiles = (n + kRows - 1) / kRows;
+  const int b1 = cb.b1, P = cb.P, W = cb.W;
+  const bool prod = cb.kind == 0;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    mbar_init(bar_full0, 1);
+    mbar_init(bar_full0 + 8, 1);
+    mbar_init(bar_const, 1);
+    mbar_init(bar_mma1, 1);
+    mbar_init(bar_mma2, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_y = tmem, tm_z = tmem + 128;
+
+  bool ok = true;
+  int pending_stage = -1;  // stage with a TMA load in flight that nobody waited for
+  const int64_t first = blockIdx.x;
+  if (tid == 0 && first < ntiles) {
+    mbar_expect_tx(bar_const, (prod ? 3 : 2) * kTileBytes);
+    for (int kb = 0; kb < 2; ++kb) {
+      tma_load_2d(sbase + kOffPiHi + kb * kBlockBytes, &tm_pihi, 64 * kb, 0, bar_const);
+      tma_load_2d(sbase + kOffPiLo + kb * kBlockBytes, &tm_pilo, 64 * kb, 0, bar_const);
+      if (prod) tma_load_2d(sbase + kOffS + kb * kBlockBytes, &tm_s, 64 * kb, 0, bar_const);
+    }
+    mbar_expect_tx(bar_full0, kTileBytes);
+    for (int kb = 0; kb < 2; ++kb)
+      tma_load_2d(sbase + kOffX + kb * kBlockBytes, &tm_x, 64 * kb, (int)(first * kRows), bar_full0);
+  }
+  if (first < ntiles) pending_stage = 0;
+  if (first < ntiles) ok = __syncthreads_and(mbar_wait(bar_const, 0)) != 0;
+
+  int it = 0;
+  for (int64_t tile = first; tile < ntiles && ok; tile += gridDim.x, ++it) {
+    const int s = it & 1;
+    const uint32_t xs = sbase + kOffX + s * kTileBytes;
+    const int64_t next = tile + gridDim.x;
+    if (tid == 0 && next < ntiles) {
+      const uint32_t xn = sbase + kOffX + (s ^ 1) * kTileBytes;
+      mbar_expect_tx(bar_full0 + 8 * (s ^ 1), kTileBytes);
+      for (int kb = 0; kb < 2; ++kb) tma_load_2d(xn + kb * kBlockBytes, &tm_x, 64 * kb, (int)(next * kRows), bar_full0 + 8 * (s ^ 1));
+    }
+    // ---- rotation on the tensor cores
+    if (!__syncthreads_and(mbar_wait(bar_full0 + 8 * s, (it >> 1) & 1))) {
+      ok = false;
+      break;
+    }
+    pending_stage = next < ntiles ? (s ^ 1) : -1;
+    if (tid == 0) {
+      fence_after();
+      for (int kb = 0; kb < 2; ++kb)
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tm_y, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffPiHi + kb * kBlockBytes + 32 * ks),
+                   (kb | ks) != 0);
+      for (int kb = 0; kb < 2; ++kb)
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tm_y, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffPiLo + kb * kBlockBytes + 32 * ks), 1);
+      mma_commit(bar_mma1);
+    }
+    if (!__syncthreads_and(mbar_wait(bar_mma1, it & 1))) {
+      ok = false;
+      break;
+    }
+    fence_after();
+    // ---- epilogue 1: norm, codes, residual
+    float v[32];
+    tmem_ld32(tm_y + ((uint32_t)(32 * q) << 16) + 32 * cg, v);
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+    red1[cg * kRows + m] = ss;
+    __syncthreads();
+    const float tot = (red1[m] + red1[kRows + m]) + (red1[2 * kRows + m] + red1[3 * kRows + m]);
+    const float nrm = sqrtf(tot);
+    const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
+    const bool ext = 32 * cg < cb.extra;
+    const int nbd = ext ? (2 << b1) - 1 : (1 << b1) - 1;
+    const float* bnd = ext ? cb.bound_x : cb.bound;
+    const float* cen = ext ? cb.cent_x : cb.cent;
+    uint32_t word[5] = {0u, 0u, 0u, 0u, 0u};
+    uint32_t xword = 0u;
+    float gs = 0.f;
+    uint32_t rh[16], rl[16];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float y = v[j] * inv;
+      int idx = 0;
+      for (int t = 0; t < nbd; ++t) idx += (y >= bnd[t]) ? 1 : 0;
+      const float r = y - cen[idx];
+      gs = fmaf(r, r, gs);
+      const int top = ext ? idx >> 1 : idx;
+      for (int p = 0; p < b1; ++p) word[p] |= (uint32_t)((top >> (b1 - 1 - p)) & 1) << j;
+      if (ext) xword |= (uint32_t)(idx & 1) << j;
+      const uint32_t hb = bf16_bits(r);
+      const float hi = __uint_as_float(hb << 16);
+      const uint32_t lb = bf16_bits(r - hi);
+      if (j & 1) {
+        rh[j >> 1] |= hb << 16;
+        rl[j >> 1] |= lb << 16;
+      } else {
+        rh[j >> 1] = hb;
+        rl[j >> 1] = lb;
+      }
+    }
+    red2[cg * kRows + m] = gs;
+    if (prod) {
+      // residual rows into the swizzled K-major operand layout: coordinate
+      // block cg/2, 16-byte chunks (cg%2)*4 + c at chunk position ^ (m % 8)
+      const uint32_t blk = (uint32_t)(cg >> 1) * kBlockBytes + (uint32_t)m * 128;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const uint32_t chunk = (uint32_t)(((cg & 1) * 4 + c4) ^ (m & 7)) * 16;
+        uint8_t* ph = smem + (xs - sbase) + blk + chunk;
+        uint8_t* pl = smem + kOffRlo + blk + chunk;
+        *reinterpret_cast<uint4*>(ph) = make_uint4(rh[4 * c4], rh[4 * c4 + 1], rh[4 * c4 + 2], rh[4 * c4 + 3]);
+        *reinterpret_cast<uint4*>(pl) = make_uint4(rl[4 * c4], rl[4 * c4 + 1], rl[4 * c4 + 2], rl[4 * c4 + 3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    // ---- QJL projection on the tensor cores
+    uint32_t sword = 0u;
+    float gamma = 0.f;
+    if (prod) {
+      if (tid == 0) {
+        fence_after();
+        for (int kb = 0; kb < 2; ++kb)
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tm_z, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffS + kb * kBlockBytes + 32 * ks),
+                     (kb | ks) != 0);
+        for (int kb = 0; kb < 2; ++kb)
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tm_z, sw128_desc(sbase + kOffRlo + kb * kBlockBytes + 32 * ks),
+                     sw128_desc(sbase + kOffS + kb * kBlockBytes + 32 * ks), 1);
+        mma_commit(bar_mma2);
+      }
+      if (!__syncthreads_and(mbar_wait(bar_mma2, it & 1))) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      tmem_ld32(tm_z + ((uint32_t)(32 * q) << 16) + 32 * cg, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sword |= (v[j] >= 0.f ? 1u : 0u) << j;
+      gamma = sqrtf((red2[m] + red2[kRows + m]) + (red2[2 * kRows + m] + red2[3 * kRows + m]));
+    }
+    // ---- store
+    const int64_t row = tile * kRows + m;
+    if (row < n) {
+      const int64_t dst = dst_rows ? dst_rows[row] : row;
+      uint32_t* rec = reinterpret_cast<uint32_t*>(cache) + dst * W;
+      if (prod) word[b1] = sword;
+      for (int p = 0; p < P; ++p) rec[cg * P + p] = word[p];
+      if (ext) rec[(128 / 32) * P + cg] = xword;
+      if (cg == 0) {
+        uint8_t* norms = cache + norm_offset(cb, cache_rows);
+        if (prod)
+          reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
+        else
+          reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+      }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+  }
+  if (!ok) {
+    if (tid == 0) atomicExch(status, 1);
+    // let our own copies and MMAs drain (bounded waits) before freeing TMEM
+    if (pending_stage >= 0) mbar_wait(bar_full0 + 8 * pending_stage, ((it + 1) >> 1) & 1);
+    mbar_wait(bar_mma1, it & 1);
+    if (prod) mbar_wait(bar_mma2, it & 1);
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+uint32_t quantize_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
+                               const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
+                               const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t ntiles = (n + kRows - 1) / kRows;
+  const int grid = (int)(ntiles < sms ? ntiles : sms);
+  k_quantize_tc<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, n, dst_rows,
+                                                   status);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

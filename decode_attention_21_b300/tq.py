@@ -20,7 +20,7 @@ F32, BF16 = 0, 1
 EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_host_tables", "tq_record_bytes", "tq_cache_bytes",
            "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits",
            "tq_decode_attention_workspace", "tq_decode_attention", "tq_search_workspace", "tq_search",
-           "tq_last_error"]
+           "tq_check_device", "tq_last_error"]
 
 
 class TqError(RuntimeError):
@@ -67,6 +67,7 @@ def lib():
         L.tq_search_workspace.argtypes = [vp, i64, i32, i32]
         L.tq_search_workspace.restype = sz
         L.tq_search.argtypes = [vp, vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.tq_check_device.argtypes = [vp]
         L.tq_last_error.argtypes = []
         L.tq_last_error.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -202,6 +203,10 @@ def tq_search_workspace(cb, n_db, nq, k):
 def tq_search(cb, db_cache, n_db, q, nq, d_in, k, ids, scores, workspace, stream=None):
     _check(lib().tq_search(cb.handle, _ptr(db_cache), n_db, _ptr(q), nq, d_in, k, _ptr(ids), _ptr(scores),
                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_check_device(cb):
+    _check(lib().tq_check_device(cb.handle))
 
 
 def tq_last_error():

@@ -176,6 +176,11 @@ tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, c
                     int32_t nq, int32_t d_in, int32_t k, int32_t* ids, float* scores,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Synchronise the device and report whether any kernel of this codebook
+ * gave up a bounded wait on its own copies or tensor-core operations since
+ * the last check (TQ_ETIMEOUT, flag cleared), else TQ_OK.  Not a hot call.  */
+tq_status tq_check_device(const tq_codebook* cb);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* tq_last_error(void);
 

@@ -211,3 +211,32 @@ def test_invalid_arguments_return_status_without_launch():
         tq.tq_logits(vcb, kc, 1, 4, 1, 64, sl, q, out, ws)       # values codebook for keys
     assert e.value.status == tq.TQ_EINVAL
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bits,kind,extra", [(2, "prod", 0), (3, "prod", 0), (4, "prod", 0), (3, "mse", 0),
+                                             (4, "mse", 0), (3, "prod", 32), (2, "prod", 64)])
+@pytest.mark.parametrize("n", [2048, 5000 + 37])
+def test_quantize_tensor_core_path(bits, kind, extra, n):
+    """bf16 batches of >= 2048 rows take the tcgen05 kernel: <= 0.1% differing
+    bits against the oracle, scattered destination rows, ragged last tile."""
+    ocb, gcb = pair(128, bits, kind, "scalar", extra)
+    x = np.concatenate([wl.llama_kv_slice(0, h, 0, 4096) for h in range(2)])[:n]
+    code = quant.quantize(ocb, x.astype(np.float64))
+    rows = n + 100
+    perm = np.random.default_rng(n).permutation(rows)[:n]
+    cache = gpu_cache(gcb, rows)
+    tq.tq_quantize(gcb, cache, rows, torch.from_numpy(x).cuda().to(torch.bfloat16), n, 128,
+                   dst_rows=torch.from_numpy(perm.astype(np.int64)).cuda())
+    tq.tq_check_device(gcb)
+    got = read_back(ocb, rows, cache)
+    g_idx = got["idx"][perm]
+    flips = (g_idx != code["idx"]).sum()
+    nbits = code["idx"].size * ocb.b1
+    if kind == "prod":
+        flips += (got["sigma"][perm] != code["sigma"]).sum()
+        nbits += code["sigma"].size
+    assert flips <= 1e-3 * nbits, flips / nbits
+    n_ref = np.linalg.norm(x.astype(np.float64), axis=1)
+    assert np.allclose(got["n16"][perm].astype(np.float64), n_ref, rtol=1e-3)
+    if kind == "prod":
+        assert np.allclose(got["g16"][perm].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
