@@ -543,16 +543,32 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
 }
 
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k) {
-  (void)cb; (void)n_db; (void)nq; (void)k;
-  return 0;
+  (void)n_db;
+  (void)k;
+  if (!cb || nq <= 0) return 0;
+  return (size_t)tq::search_workspace_bytes(cb->dev, nq);
 }
 
 tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, const float* q, int32_t nq,
                     int32_t d_in, int32_t k, int32_t* ids, float* scores, void* workspace, size_t ws_bytes,
                     void* stream) {
-  (void)cb; (void)db_cache; (void)n_db; (void)q; (void)nq; (void)d_in; (void)k; (void)ids; (void)scores;
-  (void)workspace; (void)ws_bytes; (void)stream;
-  return fail(TQ_EUNSUPPORTED, "tq_search: not implemented yet");
+  if (!cb) return fail(TQ_EINVAL, "tq_search: codebook is NULL");
+  if (cb->dev.kind != TQ_KIND_PROD) return fail(TQ_EINVAL, "tq_search: the database codebook must be of kind PROD");
+  if (cb->dev.mode != TQ_MODE_SCALAR || cb->dev.extra != 0)
+    return fail(TQ_EUNSUPPORTED, "tq_search: only scalar-mode databases without extra bits are searched");
+  if (cb->dev.d != 256) return fail(TQ_EUNSUPPORTED, "tq_search: only d = 256 is implemented");
+  if (n_db <= 0 || n_db >= (1ll << 31) || nq <= 0 || d_in < 1 || d_in > cb->dev.d || k < 1 || k > 32)
+    return fail(TQ_EINVAL, "tq_search: bad sizes (n_db %lld, nq %d, d_in %d, k %d; k must be 1..32)",
+                (long long)n_db, nq, d_in, k);
+  if (!db_cache || !q || !ids || !scores || !workspace) return fail(TQ_EINVAL, "tq_search: NULL device pointer");
+  if (!aligned16(db_cache) || !aligned16(workspace)) return fail(TQ_EINVAL, "tq_search: buffers must be 16-byte aligned");
+  if (ws_bytes < tq_search_workspace(cb, n_db, nq, k)) return fail(TQ_ENOMEM, "tq_search: workspace too small");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != cb->device) return fail(TQ_EINVAL, "tq_search: codebook lives on another device");
+  return launched("tq_search", tq::launch_search(cb->dev, static_cast<const uint8_t*>(db_cache), n_db, q, nq, d_in, k,
+                                                ids, scores, static_cast<uint8_t*>(workspace),
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

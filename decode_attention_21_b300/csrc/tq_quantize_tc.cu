@@ -126,6 +126,7 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
 
 }  // namespace
 
+template <int B1, bool PROD, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_quantize_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pihi,
                   const __grid_constant__ CUtensorMap tm_pilo, const __grid_constant__ CUtensorMap tm_s, const Dev cb,
@@ -143,8 +144,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                  bar_mma2 = bar_full0 + 32;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 48);
   const int64_t ntiles = (n + kRows - 1) / kRows;
-  const int b1 = cb.b1, P = cb.P, W = cb.W;
-  const bool prod = cb.kind == 0;
+  constexpr int b1 = B1, P = B1 + (PROD ? 1 : 0);
+  constexpr bool prod = PROD;
+  constexpr int NB = (1 << B1) - 1, NBX = (2 << B1) - 1;
+  const int W = cb.W;
+  // stage-1 tables in registers (boundaries) and shared memory (centroids)
+  __shared__ float s_cent[16], s_centx[32];
+  float bnd[NB], bndx[EXT ? NBX : 1];
+#pragma unroll
+  for (int t = 0; t < NB; ++t) bnd[t] = cb.bound[t];
+#pragma unroll
+  for (int t = 0; t < (EXT ? NBX : 1); ++t) bndx[t] = EXT ? cb.bound_x[t] : 0.f;
+  if (tid < 16) s_cent[tid] = cb.cent[tid];
+  if (tid < 32) s_centx[tid] = cb.cent_x[tid];
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -225,11 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float tot = (red1[m] + red1[kRows + m]) + (red1[2 * kRows + m] + red1[3 * kRows + m]);
     const float nrm = sqrtf(tot);
     const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
-    const bool ext = 32 * cg < cb.extra;
-    const int nbd = ext ? (2 << b1) - 1 : (1 << b1) - 1;
-    const float* bnd = ext ? cb.bound_x : cb.bound;
-    const float* cen = ext ? cb.cent_x : cb.cent;
-    uint32_t word[5] = {0u, 0u, 0u, 0u, 0u};
+    const bool ext = EXT && (32 * cg < cb.extra);
+    uint32_t word[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) word[p] = 0u;
     uint32_t xword = 0u;
     float gs = 0.f;
     uint32_t rh[16], rl[16];
@@ -237,12 +248,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 32; ++j) {
       const float y = v[j] * inv;
       int idx = 0;
-      for (int t = 0; t < nbd; ++t) idx += (y >= bnd[t]) ? 1 : 0;
-      const float r = y - cen[idx];
+      float r;
+      if (EXT && ext) {
+#pragma unroll
+        for (int t = 0; t < (EXT ? NBX : 1); ++t) idx += (y >= bndx[t]) ? 1 : 0;
+        r = y - s_centx[idx];
+      } else {
+#pragma unroll
+        for (int t = 0; t < NB; ++t) idx += (y >= bnd[t]) ? 1 : 0;
+        r = y - s_cent[idx];
+      }
       gs = fmaf(r, r, gs);
-      const int top = ext ? idx >> 1 : idx;
+      const int top = (EXT && ext) ? idx >> 1 : idx;
+#pragma unroll
       for (int p = 0; p < b1; ++p) word[p] |= (uint32_t)((top >> (b1 - 1 - p)) & 1) << j;
-      if (ext) xword |= (uint32_t)(idx & 1) << j;
+      if (EXT && ext) xword |= (uint32_t)(idx & 1) << j;
       const uint32_t hb = bf16_bits(r);
       const float hi = __uint_as_float(hb << 16);
       const uint32_t lb = bf16_bits(r - hi);
@@ -302,9 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (row < n) {
       const int64_t dst = dst_rows ? dst_rows[row] : row;
       uint32_t* rec = reinterpret_cast<uint32_t*>(cache) + dst * W;
-      if (prod) word[b1] = sword;
-      for (int p = 0; p < P; ++p) rec[cg * P + p] = word[p];
-      if (ext) rec[(128 / 32) * P + cg] = xword;
+      if constexpr (PROD) word[b1] = sword;
+      if constexpr (P == 4 && !EXT) {
+        *reinterpret_cast<uint4*>(rec + cg * P) = make_uint4(word[0], word[1], word[2], word[3]);
+      } else if constexpr (P == 2 && !EXT) {
+        *reinterpret_cast<uint2*>(rec + cg * P) = make_uint2(word[0], word[1]);
+      } else {
+#pragma unroll
+        for (int p = 0; p < P; ++p) rec[cg * P + p] = word[p];
+      }
+      if (EXT && ext) rec[(128 / 32) * P + cg] = xword;
       if (cg == 0) {
         uint8_t* norms = cache + norm_offset(cb, cache_rows);
         if (prod)
@@ -332,22 +359,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-uint32_t quantize_tc_smem_bytes() { return kSmemBytes; }
-
-cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
+template <int B1, bool PROD, bool EXT>
+static cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
                                const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
                                const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_tc<B1, PROD, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t ntiles = (n + kRows - 1) / kRows;
   const int grid = (int)(ntiles < sms ? ntiles : sms);
-  k_quantize_tc<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, n, dst_rows,
-                                                   status);
+  k_quantize_tc<B1, PROD, EXT><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows,
+                                                                  n, dst_rows, status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
+                               const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
+                               const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
+#define TQ_TC(B, PR, EX) \
+  return launch_tc_t<B, PR, EX>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, n, dst_rows, status, sms, s)
+  const bool ext = cb.extra != 0;
+  if (cb.kind == 0) {
+    switch (cb.b1 * 2 + (ext ? 1 : 0)) {
+      case 2: TQ_TC(1, true, false);
+      case 3: TQ_TC(1, true, true);
+      case 4: TQ_TC(2, true, false);
+      case 5: TQ_TC(2, true, true);
+      case 6: TQ_TC(3, true, false);
+      default: TQ_TC(3, true, true);
+    }
+  }
+  switch (cb.b1 * 2 + (ext ? 1 : 0)) {
+    case 2: TQ_TC(1, false, false);
+    case 3: TQ_TC(1, false, true);
+    case 4: TQ_TC(2, false, false);
+    case 5: TQ_TC(2, false, true);
+    case 6: TQ_TC(3, false, false);
+    case 7: TQ_TC(3, false, true);
+    default: TQ_TC(4, false, false);
+  }
+#undef TQ_TC
 }
 
 }  // namespace tq

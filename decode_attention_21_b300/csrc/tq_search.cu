@@ -1,0 +1,316 @@
+// Top-k inner-product search over a compressed database ([xujun] note-189244,
+// 常见问题 on vector search; [cnyes] hao.cnyes.com "TurboQuant"): every query
+// scores every database row with the unbiased estimator
+//   est(q, x) = n ( <q', yhat> + gamma sqrt(pi/2)/m <q'', sigma> )
+// and keeps the k best rows (decreasing score, ties to the smaller id).
+//
+// Same operand scheme as the attention logits (tq_score.cu): the score is a
+// per-query constant plus masked sums of the query side over the database's
+// bit planes, computed on the tensor cores (fp16 m16n8k16, subnormal 0/1
+// operands from the packed words, query side split into fp16 hi + lo).
+//   * prep: one CTA per (group of 4 queries, query slot): q' = Pi q,
+//     q'' = S q' (d = 256), per-slot constants and B fragments.
+//   * scan: CTA = 4 query groups x 2 coordinate halves (8 warps).  Each warp
+//     keeps the B fragments of its group and half in registers and streams
+//     16-row database tiles; the two halves of a group add their partial
+//     accumulators through shared memory, and the first half updates a
+//     per-query top-k list in shared memory (a candidate enters only if it
+//     beats the current k-th score).
+#include <cuda_fp16.h>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kD = 256;
+constexpr int kMaxK = 32;
+__device__ constexpr uint32_t kOddMask[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float piece16(float x, int which) {
+  const float hi = __half2float(__float2half_rn(x));
+  return which == 0 ? hi : x - hi;
+}
+
+__device__ __forceinline__ void expand16(uint32_t w, uint32_t (&r)[16]) {
+  const uint32_t t0 = w << 6, t1 = w << 2, t2 = w >> 2, t3 = w >> 6;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t m = 0x00400040u << e;
+    r[e] = t0 & m;
+    r[4 + e] = t1 & m;
+    r[8 + e] = t2 & m;
+    r[12 + e] = t3 & m;
+  }
+}
+
+__device__ __forceinline__ float pow2_scale(float amax, float target) {
+  if (!(amax > 0.f)) return 1.f;
+  int e;
+  frexpf(amax / target, &e);
+  return ldexpf(1.f, e);
+}
+
+__device__ __forceinline__ float dot64(const float* __restrict__ MT, const float* xs, int i, int qt) {
+  const float* col = MT + (size_t)(64 * qt) * kD + i;
+  float m[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) m[j] = __ldg(col + (size_t)j * kD);
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) acc = fmaf(m[j], xs[64 * qt + j], acc);
+  return acc;
+}
+
+}  // namespace
+
+// Bytes of one query group's prep block (header + fragments).
+__host__ __device__ inline int64_t search_block_bytes(int nv) { return kPrepHeader + (int64_t)(nv + 1) * 16 * 32 * 8; }
+
+// Fragment layout: [plane][kb (16)][lane] uint2; k-block kb covers word
+// c + 4 (kb / 8) of thread c, bit positions beta = 2 (kb % 8) (+1 for b1).
+__global__ void __launch_bounds__(1024) k_search_prep(const Dev cb, const float* __restrict__ q, int nq, int d_in,
+                                                      uint8_t* __restrict__ prep) {
+  const int grp = blockIdx.x, slot = blockIdx.y;
+  const int qi = grp * 4 + slot;
+  const bool live = qi < nq;
+  __shared__ float sq[kD], sq1[kD], sq2[kD], part[4][kD];
+  __shared__ float red[4];
+  const int tid = threadIdx.x;
+  const int i = tid & 255, qt = tid >> 8;
+  if (tid < kD) sq[tid] = (live && tid < d_in) ? q[(size_t)qi * d_in + tid] : 0.f;
+  __syncthreads();
+  part[qt][i] = dot64(cb.PiT, sq, i, qt);
+  __syncthreads();
+  if (tid < kD) sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  __syncthreads();
+  part[qt][i] = dot64(cb.ST, sq1, i, qt);
+  __syncthreads();
+  if (tid < kD) sq2[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  __syncthreads();
+  const int nv = cb.nv;
+  float cmax = 0.f, csum = 0.f;
+  for (int v = 0; v < nv; ++v) {
+    cmax = fmaxf(cmax, fabsf(cb.vcoef[v]));
+    csum += cb.vcoef[v];
+  }
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 4) {
+    float v = 0.f;
+    for (int k = lane; k < kD; k += 32) {
+      if (warp == 0) v = fmaxf(v, 2.f * cmax * fabsf(sq1[k]));
+      else if (warp == 1) v = fmaxf(v, 2.f * fabsf(sq2[k]));
+      else if (warp == 2) v += sq1[k];
+      else v += sq2[k];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float u = __shfl_xor_sync(kFull, v, o);
+      v = warp < 2 ? fmaxf(v, u) : v + u;
+    }
+    if (lane == 0) red[warp] = v;
+  }
+  __syncthreads();
+  const float S1 = pow2_scale(red[0] * 262144.f, 16384.f), S2 = pow2_scale(red[1] * 262144.f, 16384.f);
+  uint8_t* blk = prep + (size_t)grp * search_block_bytes(nv);
+  float* hdr = reinterpret_cast<float*>(blk);
+  if (tid == 0) {
+    hdr[slot] = live ? S1 : 0.f;
+    hdr[4 + slot] = live ? S2 : 0.f;
+    hdr[8 + slot] = live ? csum * red[2] : 0.f;
+    hdr[12 + slot] = live ? -red[3] : 0.f;
+  }
+  uint2* frag = reinterpret_cast<uint2*>(blk + kPrepHeader);
+  const int total = (nv + 1) * 16 * 8;
+  for (int e = tid; e < total; e += blockDim.x) {
+    const int sub = e & 7, kb = (e >> 3) & 15, v = e >> 7;
+    const int pc = sub >> 2, c = sub & 3;
+    const int g = 2 * slot + pc;
+    float vals[4] = {0.f, 0.f, 0.f, 0.f};
+    if (live) {
+      for (int t = 0; t < 4; ++t) {
+        const int beta = 2 * (kb & 7) + (t >> 1);
+        const int k = 32 * (c + 4 * (kb >> 3)) + beta + 16 * (t & 1);
+        const float pf = (float)(1 << (18 - (beta & 3)));
+        const float x = v < nv ? -2.f * cb.vcoef[v] * sq1[k] * pf / S1 : 2.f * sq2[k] * pf / S2;
+        vals[t] = piece16(x, pc);
+      }
+    }
+    frag[(v * 16 + kb) * 32 + g * 4 + c] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
+  }
+}
+
+// Scan: 8 warps = 4 query groups x 2 coordinate halves.  Warp (grp_local,
+// half) holds the fragments of k-blocks 8 half .. 8 half + 7 (word c + 4 half).
+template <int NV, int P>
+__global__ void __launch_bounds__(256, 1) k_search(const Dev cb, const uint8_t* __restrict__ db, int64_t n_db,
+                                                   const uint8_t* __restrict__ prep, int nq, int k,
+                                                   int32_t* __restrict__ ids, float* __restrict__ scores) {
+  __shared__ float xch[4][4][32];             // [group][acc element][lane]
+  __shared__ float top_s[16][kMaxK];
+  __shared__ int32_t top_i[16][kMaxK];
+  __shared__ int top_n[16];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gl = warp >> 1, half = warp & 1;
+  const int grp = blockIdx.x * 4 + gl;
+  const int ngroups = (nq + 3) / 4;
+  const int g = lane >> 2, c = lane & 3;
+  const bool live = grp < ngroups;
+  if (threadIdx.x < 16) top_n[threadIdx.x] = 0;
+  uint2 bq[NV + 1][8];
+  float S1 = 0.f, S2 = 0.f, K1 = 0.f, K2 = 0.f;
+  if (live) {
+    const uint8_t* blk = prep + (size_t)grp * search_block_bytes(NV);
+    const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
+#pragma unroll
+    for (int v = 0; v <= NV; ++v)
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) bq[v][kb] = frag[(v * 16 + 8 * half + kb) * 32 + lane];
+    const float* hdr = reinterpret_cast<const float*>(blk);
+    S1 = hdr[c];
+    S2 = hdr[4 + c];
+    K1 = hdr[8 + c];
+    K2 = hdr[12 + c];
+  }
+  __syncthreads();
+  const uint32_t* recs = reinterpret_cast<const uint32_t*>(db);
+  const uint32_t* nrm = reinterpret_cast<const uint32_t*>(db + norm_offset(cb, n_db));
+  const int W = cb.W;
+  const float kq = cb.qjl_const;
+  const int word = c + 4 * half;
+  const int qslot = gl * 4 + c;               // this thread's query (shared-memory list index)
+  const int64_t ntiles = (n_db + 15) / 16;
+  for (int64_t tile = 0; tile < ntiles; ++tile) {
+    const int64_t ta = tile * 16 + g, tb = ta + 8;
+    float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    if (live) {
+      uint32_t wa[P], wb[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        wa[p] = ta < n_db ? __ldg(recs + ta * W + word * P + p) : 0u;
+        wb[p] = tb < n_db ? __ldg(recs + tb * W + word * P + p) : 0u;
+      }
+#pragma unroll
+      for (int v = 0; v <= NV; ++v) {
+        uint32_t xa = 0, xb = 0;
+        if (v < NV) {
+#pragma unroll
+          for (int p = 0; p < P - 1; ++p)
+            if (kOddMask[v] >> p & 1u) {
+              xa ^= wa[p];
+              xb ^= wb[p];
+            }
+        } else {
+          xa = wa[P - 1];
+          xb = wb[P - 1];
+        }
+        uint32_t ra[16], rb[16];
+        expand16(xa, ra);
+        expand16(xb, rb);
+        float(&acc)[4] = v < NV ? acc1 : acc2;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb)
+          mma_f16(acc, ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
+      }
+    }
+    // combine the two coordinate halves of the group
+    if (half == 1) {
+      xch[gl][0][lane] = (acc1[0] + acc1[1]);
+      xch[gl][1][lane] = (acc1[2] + acc1[3]);
+      xch[gl][2][lane] = (acc2[0] + acc2[1]);
+      xch[gl][3][lane] = (acc2[2] + acc2[3]);
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + gl));
+    if (half == 0 && live) {
+      const float m1a = (acc1[0] + acc1[1]) + xch[gl][0][lane];
+      const float m1b = (acc1[2] + acc1[3]) + xch[gl][1][lane];
+      const float m2a = (acc2[0] + acc2[1]) + xch[gl][2][lane];
+      const float m2b = (acc2[2] + acc2[3]) + xch[gl][3][lane];
+      const uint32_t na = ta < n_db ? __ldg(nrm + ta) : 0u, nb = tb < n_db ? __ldg(nrm + tb) : 0u;
+      const __half2 ha = *reinterpret_cast<const __half2*>(&na);
+      const __half2 hb = *reinterpret_cast<const __half2*>(&nb);
+      const float sa = __low2float(ha) * fmaf(__high2float(ha) * kq, fmaf(S2, m2a, K2), fmaf(S1, m1a, K1));
+      const float sb = __low2float(hb) * fmaf(__high2float(hb) * kq, fmaf(S2, m2b, K2), fmaf(S1, m1b, K1));
+      const bool qok = grp * 4 + c < nq;
+      // candidates: beat the current k-th score of their query
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float sc = h == 0 ? sa : sb;
+        const int64_t id = h == 0 ? ta : tb;
+        const int cnt = top_n[qslot];
+        const bool cand = qok && id < n_db && (cnt < k || sc > top_s[qslot][k - 1]);
+        unsigned mask = __ballot_sync(kFull, cand);
+        while (mask) {
+          const int src = __ffs(mask) - 1;
+          mask &= mask - 1;
+          const float s_new = __shfl_sync(kFull, sc, src);
+          const int id_new = (int)__shfl_sync(kFull, (int)id, src);
+          const int qs = __shfl_sync(kFull, qslot, src);
+          if (lane == 0) {
+            // insert into the sorted list of query qs (decreasing score, ties keep the earlier id first)
+            int n0 = top_n[qs];
+            if (n0 < k || s_new > top_s[qs][k - 1]) {
+              int pos = n0 < k ? n0 : k - 1;
+              while (pos > 0 && top_s[qs][pos - 1] < s_new) {
+                top_s[qs][pos] = top_s[qs][pos - 1];
+                top_i[qs][pos] = top_i[qs][pos - 1];
+                --pos;
+              }
+              top_s[qs][pos] = s_new;
+              top_i[qs][pos] = id_new;
+              if (n0 < k) top_n[qs] = n0 + 1;
+            }
+          }
+          __syncwarp();
+        }
+      }
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + gl));
+  }
+  __syncthreads();
+  if (half == 0 && live && lane < 4) {
+    const int qi = grp * 4 + lane;
+    if (qi < nq) {
+      const int qs = gl * 4 + lane;
+      for (int j = 0; j < k; ++j) {
+        ids[(size_t)qi * k + j] = j < top_n[qs] ? top_i[qs][j] : -1;
+        scores[(size_t)qi * k + j] = j < top_n[qs] ? top_s[qs][j] : -INFINITY;
+      }
+    }
+  }
+}
+
+int64_t search_workspace_bytes(const Dev& cb, int nq) { return align256((int64_t)((nq + 3) / 4) * search_block_bytes(cb.nv)); }
+
+cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
+                          int32_t* ids, float* scores, uint8_t* prep, cudaStream_t s) {
+  const int ngroups = (nq + 3) / 4;
+  k_search_prep<<<dim3(ngroups, 4), 1024, 0, s>>>(cb, q, nq, d_in, prep);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = (ngroups + 3) / 4;
+  switch (cb.b1) {
+    case 1: k_search<1, 2><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, ids, scores); break;
+    case 2: k_search<2, 3><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, ids, scores); break;
+    default: k_search<4, 4><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, ids, scores); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tq

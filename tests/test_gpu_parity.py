@@ -240,3 +240,39 @@ def test_quantize_tensor_core_path(bits, kind, extra, n):
     assert np.allclose(got["n16"][perm].astype(np.float64), n_ref, rtol=1e-3)
     if kind == "prod":
         assert np.allclose(got["g16"][perm].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("n_db,nq,k", [(20013, 37, 10), (7, 5, 10), (4096, 8, 1)])
+def test_search_parity(bits, n_db, nq, k):
+    """Top-k ids equal to the oracle's on the oracle's own packed database,
+    except swaps among near-tied scores (oracle scores within 1e-5 relative)."""
+    ocb, gcb = pair(256, bits)
+    x = wl.search_rows(n_db, "db")
+    q = wl.search_rows(nq, "search_q")
+    code = quant.quantize(ocb, x.astype(np.float64))
+    img = torch.from_numpy(layout.write_cache(ocb, n_db, code)).cuda()
+    ref_ids, ref_sc = estimate.search(ocb, code, q.astype(np.float64), min(k, n_db))
+    full = estimate.estimate(ocb, q.astype(np.float64), code)
+    ws = torch.empty(tq.tq_search_workspace(gcb, n_db, nq, k), dtype=torch.uint8, device="cuda")
+    ids = torch.full((nq, k), -7, dtype=torch.int32, device="cuda")
+    sc = torch.full((nq, k), float("nan"), device="cuda")
+    tq.tq_search(gcb, img, n_db, torch.from_numpy(q).cuda(), nq, q.shape[1], k, ids, sc, ws)
+    torch.cuda.synchronize()
+    gi, gs = ids.cpu().numpy(), sc.cpu().numpy()
+    kk = min(k, n_db)
+    assert np.all(gi[:, kk:] == -1)
+    scale = np.max(np.abs(full))
+    tol = 1e-5 * scale
+    for r in range(nq):
+        g_ids = gi[r, :kk]
+        assert len(set(g_ids.tolist())) == kk and np.all(g_ids >= 0) and np.all(g_ids < n_db)
+        # GPU scores are the estimator of the returned rows
+        assert np.all(np.abs(gs[r, :kk] - full[r, g_ids]) <= tol)
+        # a valid top-k: the oracle scores of the returned rows match the oracle's top-k scores
+        assert np.all(np.abs(np.sort(full[r, g_ids])[::-1] - ref_sc[r]) <= tol)
+        # identical ids except where the oracle's scores are near-tied
+        for j in np.nonzero(g_ids != ref_ids[r])[0]:
+            assert abs(full[r, g_ids[j]] - ref_sc[r, j]) <= tol
+        # sorted by decreasing score
+        assert np.all(np.diff(gs[r, :kk]) <= tol)
