@@ -143,6 +143,11 @@ tq_status check_scoring_codebook(const tq_codebook* cb, int kind, const char* wh
 
 }  // namespace
 
+namespace tq {
+// Records an error message for tq_last_error (used by entry points in other files).
+tq_status report_error(tq_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace tq
+
 extern "C" {
 
 const char* tq_last_error(void) { return g_err.c_str(); }

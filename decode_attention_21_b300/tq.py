@@ -19,7 +19,8 @@ F32, BF16 = 0, 1
 
 EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_host_tables", "tq_record_bytes", "tq_cache_bytes",
            "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits",
-           "tq_decode_attention_workspace", "tq_decode_attention", "tq_search_workspace", "tq_search",
+           "tq_decode_attention_workspace", "tq_decode_attention", "tq_decode_attention_static",
+           "tq_search_workspace", "tq_search",
            "tq_check_device", "tq_last_error"]
 
 
@@ -64,6 +65,8 @@ def lib():
         L.tq_decode_attention_workspace.argtypes = [vp, i32, i32, i32, i64]
         L.tq_decode_attention_workspace.restype = sz
         L.tq_decode_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i64, vp, vp, ctypes.c_float, vp, vp, sz, vp]
+        L.tq_decode_attention_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i64, vp, vp, ctypes.c_float, vp,
+                                                 vp]
         L.tq_search_workspace.argtypes = [vp, i64, i32, i32]
         L.tq_search_workspace.restype = sz
         L.tq_search.argtypes = [vp, vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp]
@@ -194,6 +197,14 @@ def tq_decode_attention(kcb, vcb, kcache, vcache, B, Hq, Hkv, capacity, seq_lens
     _check(lib().tq_decode_attention(kcb.handle, vcb.handle, _ptr(kcache), _ptr(vcache), B, Hq, Hkv, capacity,
                                      _ptr(seq_lens), _ptr(q), float(scale), _ptr(out), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_decode_attention_static(kcb, vcb, kcache, vcache, B, Hq, Hkv, capacity, seq_lens, q, scale, out,
+                               stream=None):
+    """Decode attention with the library's built-in scratch array (no workspace
+    argument, no allocation); see include/tq.h for its limit and sharing rules."""
+    _check(lib().tq_decode_attention_static(kcb.handle, vcb.handle, _ptr(kcache), _ptr(vcache), B, Hq, Hkv, capacity,
+                                            _ptr(seq_lens), _ptr(q), float(scale), _ptr(out), _stream(stream)))
 
 
 def tq_search_workspace(cb, n_db, nq, k):

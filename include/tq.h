@@ -163,6 +163,24 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb,
                               const float* q, float scale, float* out, void* workspace,
                               size_t ws_bytes, void* stream);
 
+/* tq_decode_attention without a workspace argument, for callers that cannot
+ * allocate device memory for this library (a plugin whose host framework owns
+ * all device memory, or a loop that must not call cudaMalloc).  The pages
+ * have no counterpart to this entry point.  Scratch comes from one 4 MiB
+ * array built into the library (reserved on every GPU that loads it, until
+ * exit); a call that would need more returns TQ_EINVAL with a message and
+ * launches nothing.  Arguments and results are those of tq_decode_attention.
+ * All calls share the array and it keeps the last call's contents (each call
+ * writes every byte it later reads, so nothing needs clearing); calls that
+ * overlap on the GPU race on it and must be serialised.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress with
+ * that device current); make that first call before any stream capture.
+ * This entry point itself allocates no memory.                              */
+tq_status tq_decode_attention_static(const tq_codebook* kcb, const tq_codebook* vcb,
+                                     const void* kcache, const void* vcache, int32_t B, int32_t Hq,
+                                     int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
+                                     const float* q, float scale, float* out, void* stream);
+
 /* Workspace bytes of tq_search. */
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k);
 
