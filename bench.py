@@ -79,8 +79,9 @@ def peaks():
     if os.path.exists(p):
         with open(p) as f:
             j = json.load(f)
-        return {"hbm_gbs": float(j["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j.get("bf16_tflops", 1800.0)),
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1800.0, "source": "fallback"}
 
 
 def profile_traffic(name, source_file):
@@ -438,6 +439,54 @@ def run_quantize(args, dist, rank, steps):
     return out
 
 
+# ----------------------------------------------------------- search (config)
+def run_search(args, dist, rank, steps):
+    """Top-10 inner-product search: 10^6 database rows (d 200 -> 256), 10^4
+    queries from a Gaussian mixture; recall@1@k against exact fp32 scores."""
+    from decode_attention_21_b300 import tq
+    from decode_attention_21_b300 import workloads as wl
+    n_db, nq, d_in, d, k = 1000000, 10000, 200, 256, 10
+    x = torch.from_numpy(wl.search_rows(n_db, "db")).cuda()
+    q = torch.from_numpy(wl.search_rows(nq, "search_q")).cuda()
+    # exact fp32 top-1 (reference for recall), in blocks
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    true1 = torch.empty(nq, dtype=torch.int64, device="cuda")
+    for a in range(0, nq, 1000):
+        true1[a:a + 1000] = torch.argmax(q[a:a + 1000] @ x.T, dim=1)
+    torch.backends.cuda.matmul.allow_tf32 = prev
+    pk = peaks()
+    out = {}
+    for bits in (2, 4):
+        cb = tq.Codebook(d, bits, tq.KIND_PROD)
+        db = torch.empty(tq.cache_bytes(cb, n_db), dtype=torch.uint8, device="cuda")
+        tq.tq_quantize(cb, db, n_db, x, n_db, d_in)
+        ws = torch.empty(tq.tq_search_workspace(cb, n_db, nq, k), dtype=torch.uint8, device="cuda")
+        ids = torch.empty(nq, k, dtype=torch.int32, device="cuda")
+        sc = torch.empty(nq, k, device="cuda")
+
+        def step(i, cb=cb, db=db, ws=ws, ids=ids, sc=sc):
+            tq.tq_search(cb, db, n_db, q, nq, d_in, k, ids, sc, ws)
+
+        step(0)
+        torch.cuda.synchronize()
+        ms = timed(dist, lambda: [step(i) for i in range(steps)])
+        hit = (ids.long() == true1[:, None])
+        recall = {str(kk): float(hit[:, :kk].any(dim=1).float().mean()) for kk in (1, 2, 4, 8, 10)}
+        nv = 1 << (bits - 2)
+        flops_legacy = 2.0 * nq * n_db * (nv + 1) * d * 2          # hi/lo query columns
+        flops_alg = 2.0 * nq * n_db * 2 * d                         # dense [q'; q''] . [yhat; sigma]
+        tf = steps * flops_alg / (ms / 1e3) / 1e12
+        out[f"b{bits}"] = {"queries_per_s": steps * nq * args.world / (ms / 1e3), "ms_per_call": ms / steps,
+                           "pair_scores_per_s": steps * nq * n_db / (ms / 1e3),
+                           "recall_1_at_k": recall, "db_bytes": n_db * (tq.record_bytes(cb) + 4),
+                           "roofline": {"bound": "tensor", "achieved": tf, "unit": "TFLOP/s",
+                                        "peak": pk.get("bf16_tflops"), "frac": (tf / pk["bf16_tflops"]) if pk.get("bf16_tflops") else None,
+                                        "algorithmic_flop_per_call": flops_alg,
+                                        "executed_mma_flop_per_call": flops_legacy}}
+    return {"workload": "top-10 search, 10^6 rows d 200->256, 10^4 queries, b = 2 and 4", **out}
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args, rank):
     """The CPU oracle as it stands, on a bounded sample of the headline step."""
@@ -469,7 +518,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "logits", "attention", "quantize"])
+    ap.add_argument("--workload", default="all", choices=["all", "logits", "attention", "quantize", "search"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -491,6 +540,8 @@ def main():
         secondary["attention"] = run_attention(args, dist, rank, sec_steps)
     if args.workload in ("all", "quantize"):
         secondary["quantize"] = run_quantize(args, dist, rank, sec_steps)
+    if args.workload in ("all", "search"):
+        secondary["search"] = run_search(args, dist, rank, 2)
     line = {"metric": res.get("metric", "secondary workloads only"), "value": res.get("value"),
             "unit": res.get("unit"), "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": res.get("ms_per_step"), "higher_is_better": True, "scaling": "weak",
