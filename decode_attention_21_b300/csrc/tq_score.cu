@@ -205,20 +205,24 @@ struct QK16 {
     K2 = hdr[12 + c];
   }
 
-  __device__ __forceinline__ void plane(uint32_t xa, uint32_t xb, int v, float (&acc)[4]) const {
+  // Accumulates into chains kb % 2 (two independent accumulator chains per
+  // call so consecutive MMAs do not wait on each other).
+  __device__ __forceinline__ void plane(uint32_t xa, uint32_t xb, int v, float (&acc)[2][4]) const {
     uint32_t ra[16], rb[16];
     expand16(xa, ra);
     expand16(xb, rb);
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb)
-      mma_f16(acc, ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
+      mma_f16(acc[kb & 1], ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
   }
 
   // wa, wb: the P plane words (column c) of keys g and g+8
   __device__ __forceinline__ void score(const uint32_t (&wa)[P], const uint32_t (&wb)[P], float& s1a, float& s1b,
                                         float& s2a, float& s2b) const {
-    float acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // sign plane first: its chain runs alongside the stage-1 planes
+    plane(wa[P - 1], wb[P - 1], NV, acc2);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       uint32_t xa = 0, xb = 0;
@@ -230,11 +234,10 @@ struct QK16 {
         }
       plane(xa, xb, v, acc1);
     }
-    plane(wa[P - 1], wb[P - 1], NV, acc2);
-    s1a = fmaf(S1, acc1[0] + acc1[1], K1);
-    s1b = fmaf(S1, acc1[2] + acc1[3], K1);
-    s2a = fmaf(S2, acc2[0] + acc2[1], K2);
-    s2b = fmaf(S2, acc2[2] + acc2[3], K2);
+    s1a = fmaf(S1, (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]), K1);
+    s1b = fmaf(S1, (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]), K1);
+    s2a = fmaf(S2, (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]), K2);
+    s2b = fmaf(S2, (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]), K2);
   }
 };
 
