@@ -134,7 +134,6 @@ tq_status check_scoring_codebook(const tq_codebook* cb, int kind, const char* wh
   if (cb->dev.kind != kind) return fail(TQ_EINVAL, "%s: codebook has the wrong kind", what);
   if (cb->dev.d != 128) return fail(TQ_EUNSUPPORTED, "%s: only d = 128 is implemented", what);
   if (cb->dev.extra != 0) return fail(TQ_EUNSUPPORTED, "%s: mixed-bit caches are not scored yet", what);
-  if (cb->dev.mode != TQ_MODE_SCALAR) return fail(TQ_EUNSUPPORTED, "%s: polar-mode scoring is not implemented", what);
   int dev = -1;
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
@@ -312,7 +311,7 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
         for (int k = 0; k < L - 1; ++k) cb->bound[k] = (float)q.t[k];
       }
     }
-    dv.nv = 0;
+    dv.nv = 1;   // one decoded stage-1 plane for the scoring kernels
   }
 
   // rotation
@@ -495,10 +494,15 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
   if (ws_bytes < tq_logits_workspace(kcb, B, Hq, Hkv)) return fail(TQ_ENOMEM, "tq_logits: workspace too small");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
-  if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
   int nchunks, tpc;
   chunking(B, Hkv, capacity, kLogitsCtas, &nchunks, &tpc);
   const int64_t rows = (int64_t)B * Hkv * capacity;
+  if (kcb->dev.mode == TQ_MODE_POLAR) {
+    if ((st = launched("tq_logits/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+    return launched("tq_logits", tq::launch_logits_polar(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                         capacity, rows, seq_lens, prep, logits, nchunks, tpc, s));
+  }
+  if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
   return launched("tq_logits", tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
                                                  rows, seq_lens, prep, logits, nchunks, tpc, s));
 }
@@ -532,12 +536,25 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   float* parts = reinterpret_cast<float*>(
       prep + tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d)));
-  if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
-    return st;
+  if (kcb->dev.mode != vcb->dev.mode)
+    return fail(TQ_EUNSUPPORTED, "tq_decode_attention: keys and values must use the same stage-1 mode");
   int nchunks, tpc;
   chunking(B, Hkv, capacity, kAttnCtas, &nchunks, &tpc);
   const int64_t rows = (int64_t)B * Hkv * capacity;
   const float sl2 = scale * 1.4426950408889634f;
+  if (kcb->dev.mode == TQ_MODE_POLAR) {
+    if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
+      return st;
+    if ((st = launched("tq_decode_attention",
+                       tq::launch_attn_polar(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                             static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
+                                             seq_lens, prep, sl2, parts, nchunks, tpc, s))) != TQ_OK)
+      return st;
+    return launched("tq_decode_attention/merge",
+                    tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
+  }
+  if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
+    return st;
   if ((st = launched("tq_decode_attention",
                      tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
                                      static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens, prep,

@@ -1,0 +1,469 @@
+// Scoring of recursive-polar caches ([xujun] note-189244, 第一步 recursive
+// pairing of radii; [suzuke] 第二步 polar coordinates + Max-Lloyd angles):
+// the stage-1 reproduction is a product of cosines and sines down the tree,
+// so it is decoded to fp32 per key (or value) and fed to the tensor cores as
+// fp16 hi + lo operands; the QJL term is the same sign-plane contraction as
+// in scalar mode.  d = 128, tree of 7 levels, subtrees of 32 leaves per
+// packed word (see the polar layout in tq.h).
+//
+//   logits: A = decoded keys (16 keys x 16 coordinates, hi then lo),
+//           B = q' (fp16 hi/lo columns of the G <= 4 heads);
+//   attention PV: A = decoded values (16 coordinates x 16 tokens, the two
+//           tokens of a pair in the two fp16 halves), B = p_t n_v,t.
+#include <cuda_fp16.h>
+
+#include "tq_internal.cuh"
+#include "tq_mma.cuh"
+
+namespace tq {
+
+using namespace mma;
+
+namespace {
+
+constexpr int kLevels = 7;   // log2(128)
+
+// (cos, sin) of the centroid of code k at tree level l, in shared memory.
+struct PolarTab {
+  float2 t[kLevels + 1][16];
+};
+
+__device__ __forceinline__ void load_tab(const Dev& cb, PolarTab& tab) {
+  for (int e = threadIdx.x; e < (kLevels + 1) * 16; e += blockDim.x) {
+    const int l = e >> 4, k = e & 15;
+    tab.t[l][k] = make_float2(cb.pc_cos[l][k], cb.pc_sin[l][k]);
+  }
+}
+
+// Code of the angle stored at bit `bit` of the B planes' words (plane 0 = MSB).
+template <int B>
+__device__ __forceinline__ int code_at(const uint32_t (&w)[B], int bit) {
+  int c = 0;
+#pragma unroll
+  for (int p = 0; p < B; ++p) c = (c << 1) | ((w[p] >> bit) & 1u);
+  return c;
+}
+
+// Radius of subtree s (32 leaves) of a unit row: root angle (bit 31 of word 0)
+// and the level-6 angle (bit 31 of word 1 + s/2).
+template <int B>
+__device__ __forceinline__ float subtree_radius(const PolarTab& tab, const uint32_t (&w0)[B],
+                                                const uint32_t (&w6)[B], int s) {
+  const float2 r7 = tab.t[7][code_at<B>(w0, 31)];
+  const float rho6 = (s >> 1) ? r7.y : r7.x;
+  const float2 r6 = tab.t[6][code_at<B>(w6, 31)];
+  return rho6 * ((s & 1) ? r6.y : r6.x);
+}
+
+// The 16 leaves of half h of subtree s, starting from the subtree radius.
+template <int B>
+__device__ __forceinline__ void decode_half(const PolarTab& tab, const uint32_t (&ws)[B], float rho5, int h,
+                                            float (&y)[16]) {
+  const float2 a5 = tab.t[5][code_at<B>(ws, 30)];
+  const float rho4 = rho5 * (h ? a5.y : a5.x);
+  const float2 a4 = tab.t[4][code_at<B>(ws, 28 + h)];
+  float r3[2] = {rho4 * a4.x, rho4 * a4.y};
+  float r2[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 a = tab.t[3][code_at<B>(ws, 24 + 2 * h + i)];
+    r2[2 * i] = r3[i] * a.x;
+    r2[2 * i + 1] = r3[i] * a.y;
+  }
+  float r1[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = tab.t[2][code_at<B>(ws, 16 + 4 * h + i)];
+    r1[2 * i] = r2[i] * a.x;
+    r1[2 * i + 1] = r2[i] * a.y;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 a = tab.t[1][code_at<B>(ws, 8 * h + i)];
+    y[2 * i] = r1[i] * a.x;
+    y[2 * i + 1] = r1[i] * a.y;
+  }
+}
+
+__device__ __forceinline__ float dot32p(const float* __restrict__ MT, const float* xs, int i, int qt) {
+  constexpr int d = 128;
+  const float* col = MT + (size_t)(32 * qt) * d + i;
+  float m[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) m[j] = __ldg(col + (size_t)j * d);
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc = fmaf(m[j], xs[32 * qt + j], acc);
+  return acc;
+}
+
+}  // namespace
+
+// Query preparation for polar keys: plane 0 = q' (plain fp16 hi/lo, the key
+// side is decoded to normal fp16 values), plane 1 = the QJL plane exactly as
+// in scalar mode.  Header: S1[4], S2[4], K1[4] = 0, K2[4] = -sum q''.
+__global__ void __launch_bounds__(512) k_prep_polar(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
+                                                    uint8_t* __restrict__ prep) {
+  constexpr int d = 128;
+  const int G = Hq / Hkv;
+  const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
+  const bool live = slot < G;
+  __shared__ float sq[d], sq1[d], sq2[d], part[4][d];
+  __shared__ float red[3];
+  const int tid = threadIdx.x;
+  const int i = tid & 127, qt = tid >> 7;
+  if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
+  __syncthreads();
+  part[qt][i] = dot32p(cb.PiT, sq, i, qt);
+  __syncthreads();
+  if (tid < d) sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  __syncthreads();
+  part[qt][i] = dot32p(cb.ST, sq1, i, qt);
+  __syncthreads();
+  if (tid < d) sq2[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 3) {
+    float v = 0.f;
+    for (int k = lane; k < d; k += 32) {
+      if (warp == 0) v = fmaxf(v, fabsf(sq1[k]));
+      else if (warp == 1) v = fmaxf(v, 2.f * fabsf(sq2[k]));
+      else v += sq2[k];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float u = __shfl_xor_sync(kFull, v, o);
+      v = warp < 2 ? fmaxf(v, u) : v + u;
+    }
+    if (lane == 0) red[warp] = v;
+  }
+  __syncthreads();
+  const float S1 = pow2_scale(red[0], 16384.f), S2 = pow2_scale(red[1] * 262144.f, 16384.f);
+  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(1, d);
+  float* hdr = reinterpret_cast<float*>(blk);
+  if (tid == 0) {
+    hdr[slot] = live ? S1 : 0.f;
+    hdr[4 + slot] = live ? S2 : 0.f;
+    hdr[8 + slot] = 0.f;
+    hdr[12 + slot] = live ? -red[2] : 0.f;
+  }
+  uint2* frag = reinterpret_cast<uint2*>(blk + kPrepHeader);
+  for (int e = tid; e < 2 * 8 * 8; e += blockDim.x) {
+    const int sub = e & 7, kb = (e >> 3) & 7, v = e >> 6;
+    const int pc = sub >> 2, c = sub & 3;
+    const int g = 2 * slot + pc;
+    float vals[4] = {0.f, 0.f, 0.f, 0.f};
+    if (live) {
+      for (int t = 0; t < 4; ++t) {
+        const int beta = 2 * kb + (t >> 1);
+        const int k = 32 * c + beta + 16 * (t & 1);
+        const float x = v == 0 ? sq1[k] / S1 : 2.f * sq2[k] * (float)(1 << (18 - (beta & 3))) / S2;
+        vals[t] = piece16(x, pc);
+      }
+    }
+    frag[(v * 8 + kb) * 32 + g * 4 + c] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
+  }
+}
+
+// Words of one key the thread needs: its own column c (all P planes) and
+// the top-path words 0 and 1 + c/2 of the B code planes.
+template <int B>
+struct PKey {
+  uint32_t ws[B + 1], w0[B], w6[B];
+  uint32_t nrm;
+  __device__ __forceinline__ void load(const uint32_t* rec, const uint32_t* nrm_p, int64_t row, int W, int c,
+                                       bool valid) {
+    constexpr int P = B + 1;
+    if (!valid) {
+#pragma unroll
+      for (int p = 0; p < P; ++p) ws[p] = 0;
+#pragma unroll
+      for (int p = 0; p < B; ++p) w0[p] = w6[p] = 0;
+      nrm = 0;
+      return;
+    }
+    const uint32_t* r = rec + row * W;
+#pragma unroll
+    for (int p = 0; p < P; ++p) ws[p] = __ldg(r + c * P + p);
+#pragma unroll
+    for (int p = 0; p < B; ++p) {
+      w0[p] = __ldg(r + p);
+      w6[p] = __ldg(r + (1 + (c >> 1)) * P + p);
+    }
+    nrm = __ldg(nrm_p + row);
+  }
+  // the 32 leaves of subtree c (unit row)
+  __device__ __forceinline__ void decode(const PolarTab& tab, int c, float (&y)[32]) const {
+    uint32_t cw[B];
+#pragma unroll
+    for (int p = 0; p < B; ++p) cw[p] = ws[p];
+    const float rho5 = subtree_radius<B>(tab, w0, w6, c);
+    float lo[16], hi[16];
+    decode_half<B>(tab, cw, rho5, 0, lo);
+    decode_half<B>(tab, cw, rho5, 1, hi);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      y[i] = lo[i];
+      y[16 + i] = hi[i];
+    }
+  }
+};
+
+// inner products (stage 1, QJL) of keys g and g+8 for head slot c
+template <int B>
+__device__ __forceinline__ void polar_qk(const PolarTab& tab, const uint2 (&bq)[2][8], const PKey<B>& ka,
+                                         const PKey<B>& kb_, int c, float& s1a, float& s1b, float& s2a,
+                                         float& s2b) {
+  float ya[32], yb[32];
+  ka.decode(tab, c, ya);
+  kb_.decode(tab, c, yb);
+  float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  {
+    uint32_t ra[16], rb[16];
+    expand16(ka.ws[B], ra);
+    expand16(kb_.ws[B], rb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      mma_f16(acc2[k & 1], ra[2 * k], rb[2 * k], ra[2 * k + 1], rb[2 * k + 1], bq[1][k].x, bq[1][k].y);
+  }
+#pragma unroll
+  for (int pc = 0; pc < 2; ++pc) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int be = 2 * k;
+      const uint32_t a0 = pack_half2(piece16(ya[be], pc), piece16(ya[be + 16], pc));
+      const uint32_t a1 = pack_half2(piece16(yb[be], pc), piece16(yb[be + 16], pc));
+      const uint32_t a2 = pack_half2(piece16(ya[be + 1], pc), piece16(ya[be + 17], pc));
+      const uint32_t a3 = pack_half2(piece16(yb[be + 1], pc), piece16(yb[be + 17], pc));
+      mma_f16(acc1[pc], a0, a1, a2, a3, bq[0][k].x, bq[0][k].y);
+    }
+  }
+  s1a = (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]);
+  s1b = (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]);
+  s2a = (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]);
+  s2b = (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]);
+}
+
+__device__ __forceinline__ float est_polar(uint32_t nrm_bits, float s1, float s2, float kq) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&nrm_bits);
+  return __low2float(h) * fmaf(__high2float(h) * kq, s2, s1);
+}
+
+template <int B>
+__global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
+                                                      int Hkv, int64_t capacity, int64_t cache_rows,
+                                                      const int32_t* __restrict__ seq_lens,
+                                                      const uint8_t* __restrict__ prep, float* __restrict__ logits,
+                                                      int tiles_per_cta) {
+  __shared__ PolarTab tab;
+  load_tab(cb, tab);
+  __syncthreads();
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int G = Hq / Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t L = seq_lens[b];
+  const int64_t ntiles = (L + 15) / 16;
+  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
+  if (tile0 + warp >= tend) return;
+  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(1, 128);
+  const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
+  uint2 bq[2][8];
+#pragma unroll
+  for (int v = 0; v < 2; ++v)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) bq[v][k] = frag[(v * 8 + k) * 32 + lane];
+  const float* hdr = reinterpret_cast<const float*>(blk);
+  const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
+  const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
+  const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
+  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
+  const float kq = cb.qjl_const;
+  float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
+  for (int64_t tile = tile0 + warp; tile < tend; tile += 4) {
+    const int64_t ta = tile * 16 + g, tb = ta + 8;
+    PKey<B> ka, kb_;
+    ka.load(recs, nrm, rowbase + ta, cb.W, c, ta < L);
+    kb_.load(recs, nrm, rowbase + tb, cb.W, c, tb < L);
+    float s1a, s1b, s2a, s2b;
+    polar_qk<B>(tab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
+    if (c < G) {
+      if (ta < L) out[ta] = est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq);
+      if (tb < L) out[tb] = est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq);
+    }
+  }
+}
+
+template <int BK, int BV>
+__global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev vcb, const uint8_t* __restrict__ kcache,
+                                                       const uint8_t* __restrict__ vcache, int Hq, int Hkv,
+                                                       int64_t capacity, int64_t cache_rows,
+                                                       const int32_t* __restrict__ seq_lens,
+                                                       const uint8_t* __restrict__ prep, float scale_log2,
+                                                       float* __restrict__ partials, int tiles_per_cta) {
+  __shared__ PolarTab ktab, vtab;
+  load_tab(kcb, ktab);
+  load_tab(vcb, vtab);
+  __syncthreads();
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t L = seq_lens[b];
+  const int64_t ntiles = (L + 15) / 16;
+  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  if (tile0 + warp < tend) {
+    const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(1, 128);
+    const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
+    uint2 bq[2][8];
+#pragma unroll
+    for (int v = 0; v < 2; ++v)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) bq[v][k] = frag[(v * 8 + k) * 32 + lane];
+    const float* hdr = reinterpret_cast<const float*>(blk);
+    const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
+    const uint32_t* krec = reinterpret_cast<const uint32_t*>(kcache);
+    const uint32_t* knrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(kcb, cache_rows));
+    const uint32_t* vrec = reinterpret_cast<const uint32_t*>(vcache);
+    const __half* vnrm = reinterpret_cast<const __half*>(vcache + norm_offset(vcb, cache_rows));
+    const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
+    const float kq = kcb.qjl_const;
+    const int hh = g >> 1, pc = g & 1;
+    const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
+    const int vs = g >> 1, vh = g & 1;   // value subtree and half of this thread's 16 coordinates
+    for (int64_t tile = tile0 + warp; tile < tend; tile += 4) {
+      const int64_t t0 = tile * 16, ta = t0 + g, tb = ta + 8;
+      PKey<BK> ka, kb_;
+      ka.load(krec, knrm, rowbase + ta, kcb.W, c, ta < L);
+      kb_.load(krec, knrm, rowbase + tb, kcb.W, c, tb < L);
+      float s1a, s1b, s2a, s2b;
+      polar_qk<BK>(ktab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
+      const float sa = ta < L ? est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L ? est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq) * scale_log2 : -INFINITY;
+      float mx = fmaxf(sa, sb);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (__any_sync(kFull, mx > m_run)) {
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+        l_run *= alpha;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        m_run = m_new;
+      }
+      const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
+      const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_run);
+      const float vn0 = ta < L ? __half2float(vnrm[rowbase + ta]) : 0.f;
+      const float vn1 = tb < L ? __half2float(vnrm[rowbase + tb]) : 0.f;
+      const float wA = pa * vn0, wB = pb * vn1;
+      float ps = pa + pb;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) ps += __shfl_xor_sync(kFull, ps, o);
+      l_run += ps;
+      const float w0 = __shfl_sync(kFull, wA, src0);
+      const float w1 = __shfl_sync(kFull, wA, src1);
+      const float w8 = __shfl_sync(kFull, wB, src0);
+      const float w9 = __shfl_sync(kFull, wB, src1);
+      const uint32_t b0 = pack_half2(piece16(w0, pc), piece16(w1, pc));
+      const uint32_t b1 = pack_half2(piece16(w8, pc), piece16(w9, pc));
+      // decode this thread's 16 value coordinates of tokens 2c, 2c+1, 2c+8, 2c+9
+      float yv[4][16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t t = t0 + 2 * c + (j & 1) + 8 * (j >> 1);
+        uint32_t wsv[BV], w0v[BV], w6v[BV];
+        if (t < L) {
+          const uint32_t* r = vrec + (rowbase + t) * vcb.W;
+#pragma unroll
+          for (int p = 0; p < BV; ++p) {
+            wsv[p] = __ldg(r + vs * BV + p);
+            w0v[p] = __ldg(r + p);
+            w6v[p] = __ldg(r + (1 + (vs >> 1)) * BV + p);
+          }
+          const float rho5 = subtree_radius<BV>(vtab, w0v, w6v, vs);
+          decode_half<BV>(vtab, wsv, rho5, vh, yv[j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) yv[j][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int pv = 0; pv < 2; ++pv) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int r0 = 2 * mt, r1 = 2 * mt + 1;
+          const uint32_t a0 = pack_half2(piece16(yv[0][r0], pv), piece16(yv[1][r0], pv));
+          const uint32_t a1 = pack_half2(piece16(yv[0][r1], pv), piece16(yv[1][r1], pv));
+          const uint32_t a2 = pack_half2(piece16(yv[2][r0], pv), piece16(yv[3][r0], pv));
+          const uint32_t a3 = pack_half2(piece16(yv[2][r1], pv), piece16(yv[3][r1], pv));
+          mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+    }
+  }
+  const int nchunks = gridDim.x;
+  float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
+  float* ph = part + c * (2 + 128);
+  if (g == 0) {
+    ph[0] = m_run;
+    ph[1] = l_run;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    ph[2 + 16 * g + 2 * mt] = acc[mt][0] + acc[mt][1];
+    ph[2 + 16 * g + 2 * mt + 1] = acc[mt][2] + acc[mt][3];
+  }
+}
+
+cudaError_t launch_prep_polar(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s) {
+  k_prep_polar<<<dim3(Hkv * 4, B), 512, 0, s>>>(cb, q, Hq, Hkv, prep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logits_polar(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
+                                int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks,
+                                int tpc, cudaStream_t s) {
+  const dim3 grid(nchunks, Hkv, B);
+  switch (cb.b1) {
+    case 1: k_logits_polar<1><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
+    case 2: k_logits_polar<2><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
+    default: k_logits_polar<3><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
+  }
+  return cudaGetLastError();
+}
+
+template <int BK>
+static void attn_polar_v(int bv, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
+                         const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const int32_t* sl,
+                         const uint8_t* prep, float sl2, float* parts, int tpc) {
+  switch (bv) {
+    case 1: k_attn_polar<BK, 1><<<grid, 128, 0, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc); break;
+    case 2: k_attn_polar<BK, 2><<<grid, 128, 0, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc); break;
+    case 3: k_attn_polar<BK, 3><<<grid, 128, 0, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc); break;
+    default: k_attn_polar<BK, 4><<<grid, 128, 0, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc); break;
+  }
+}
+
+cudaError_t launch_attn_polar(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq,
+                              int Hkv, int64_t capacity, int64_t rows, const int32_t* seq_lens, const uint8_t* prep,
+                              float scale_log2, float* parts, int nchunks, int tpc, cudaStream_t s) {
+  const dim3 grid(nchunks, Hkv, B);
+  switch (kcb.b1) {
+    case 1: attn_polar_v<1>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc); break;
+    case 2: attn_polar_v<2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc); break;
+    default: attn_polar_v<3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tq

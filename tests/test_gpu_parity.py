@@ -134,11 +134,12 @@ def rowwise_ok(got, ref, tol=1e-3, med=1e-4):
     assert np.median(rel) <= med, float(np.median(rel))
 
 
+@pytest.mark.parametrize("mode", ["scalar", "polar"])
 @pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 8, 2, 4096, [4096]), (2, 4, 1, 1000, [1000, 1]),
                                                (3, 6, 3, 333, [333, 17, 0]), (1, 2, 2, 64, [49])])
-def test_logits_parity(bits, B, Hq, Hkv, cap, lens):
-    ocb, gcb = pair(128, bits)
+def test_logits_parity(bits, B, Hq, Hkv, cap, lens, mode):
+    ocb, gcb = pair(128, bits, mode=mode)
     rows = B * Hkv * cap
     x = wl.gaussian_outlier_keys(rows, 128)
     code, img = oracle_cache(ocb, rows, x.astype(np.float64))
@@ -158,12 +159,13 @@ def test_logits_parity(bits, B, Hq, Hkv, cap, lens):
             rowwise_ok(got[b, :, :L], ref[b, :, :L])
 
 
-@pytest.mark.parametrize("kb,vb", [(3, 3), (4, 3), (2, 2), (3, 4), (3, 1)])
+@pytest.mark.parametrize("kb,vb,mode", [(3, 3, "scalar"), (4, 3, "scalar"), (2, 2, "scalar"), (3, 4, "scalar"),
+                                        (3, 1, "scalar"), (3, 3, "polar"), (4, 2, "polar"), (2, 4, "polar")])
 @pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 300, [300, 1, 0]),
                                                (1, 4, 4, 5000, [4999])])
-def test_attention_parity(kb, vb, B, Hq, Hkv, cap, lens):
-    okc, gkc = pair(128, kb, "prod")
-    ovc, gvc = pair(128, vb, "mse", seed_pi=1)
+def test_attention_parity(kb, vb, mode, B, Hq, Hkv, cap, lens):
+    okc, gkc = pair(128, kb, "prod", mode=mode)
+    ovc, gvc = pair(128, vb, "mse", mode=mode, seed_pi=1)
     rows = B * Hkv * cap
     K = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="keys") for h in range(B * Hkv)])
     V = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="values") for h in range(B * Hkv)])
