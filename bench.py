@@ -355,14 +355,15 @@ def run_logits(args, dist, rank):
 ATTN = dict(B=8, Hq=32, Hkv=8, d=128, T=131072, kbits=3, vbits=3)
 
 
-def run_attention(args, dist, rank, steps):
+def run_attention(args, dist, rank, steps, mode="scalar"):
     from decode_attention_21_b300 import tq
     from decode_attention_21_b300 import workloads as wl
     c = ATTN
     B, Hq, Hkv, d, T = c["B"], c["Hq"], c["Hkv"], c["d"], c["T"]
     rows = B * Hkv * T
-    kcb = tq.Codebook(d, c["kbits"], tq.KIND_PROD)
-    vcb = tq.Codebook(d, c["vbits"], tq.KIND_MSE)
+    md = tq.MODE_POLAR if mode == "polar" else tq.MODE_SCALAR
+    kcb = tq.Codebook(d, c["kbits"], tq.KIND_PROD, md)
+    vcb = tq.Codebook(d, c["vbits"], tq.KIND_MSE, md)
     kc = torch.empty(tq.cache_bytes(kcb, rows), dtype=torch.uint8, device="cuda")
     vc = torch.empty(tq.cache_bytes(vcb, rows), dtype=torch.uint8, device="cuda")
     chunk = 1 << 20
@@ -403,7 +404,8 @@ def run_attention(args, dist, rank, steps):
                        max(steps, 5))
     pk = peaks()
     achieved = packed / (k_ms / 1e3) / 1e9
-    return {"workload": "fused decode attention: batch 8, 32/8 heads, d 128, context 131072, keys 3-bit, values 3-bit",
+    return {"workload": f"fused decode attention ({mode} stage 1): batch 8, 32/8 heads, d 128, context 131072, "
+                        "keys 3-bit, values 3-bit",
             "keys_per_s": steps * rows * args.world / (ms / 1e3), "ms_per_step": ms / steps,
             "packed_bytes_per_step": packed,
             "roofline": {"kernel": "tq_decode_attention (prep + fused kernel + merge)", "bound": "hbm",
@@ -538,6 +540,7 @@ def main():
     sec_steps = max(3, args.steps // 5)
     if args.workload in ("all", "attention"):
         secondary["attention"] = run_attention(args, dist, rank, sec_steps)
+        secondary["attention_polar"] = run_attention(args, dist, rank, sec_steps, mode="polar")
     if args.workload in ("all", "quantize"):
         secondary["quantize"] = run_quantize(args, dist, rank, sec_steps)
     if args.workload in ("all", "search"):
