@@ -359,7 +359,16 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
         sT[(size_t)i * m + j] = cb->s[(size_t)j * d + i];
         sbf[(size_t)j * d + i] = bf16_bits(cb->s[(size_t)j * d + i]);
       }
-    if ((st = upload(cb, sT, &dv.ST)) != TQ_OK || (st = upload(cb, sbf, &dv.S_bf)) != TQ_OK) {
+    // (S Pi), accumulated in fp64, stored transposed
+    std::vector<float> spT((size_t)d * m);
+    for (int j = 0; j < m; ++j)
+      for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int k = 0; k < d; ++k) acc += (double)cb->s[(size_t)j * d + k] * cb->pi[(size_t)k * d + i];
+        spT[(size_t)i * m + j] = (float)acc;
+      }
+    if ((st = upload(cb, sT, &dv.ST)) != TQ_OK || (st = upload(cb, sbf, &dv.S_bf)) != TQ_OK ||
+        (st = upload(cb, spT, &dv.SPT)) != TQ_OK) {
       tq_free_codebook(cb);
       return st;
     }
@@ -503,6 +512,10 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
                                                          capacity, rows, seq_lens, prep, logits, nchunks, tpc, s));
   }
   if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+  if (capacity % 16 == 0 && tpc <= tq::logits_tma_max_tiles() && aligned16(kcache))
+    return launched("tq_logits", tq::launch_logits_tma(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                       capacity, rows, seq_lens, prep, logits, nchunks, tpc,
+                                                       kcb->d_status, s));
   return launched("tq_logits", tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
                                                  rows, seq_lens, prep, logits, nchunks, tpc, s));
 }

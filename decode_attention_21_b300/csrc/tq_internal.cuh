@@ -28,6 +28,7 @@ struct Dev {
   const float* Pi;        // [d][d] row-major, y = Pi x
   const float* PiT;       // [d][d], PiT[j*d + i] = Pi[i][j]
   const float* ST;        // [d][m], ST[i*m + j] = S[j][i]
+  const float* SPT;       // [d][m], SPT[i*m + j] = (S Pi)[j][i]: q'' = (S Pi) q in one pass
   const uint16_t* Pi_hi;  // bf16 split of Pi (row-major): Pi ~ hi + lo
   const uint16_t* Pi_lo;
   const uint16_t* S_bf;   // bf16 S (exact), row-major [m][d]
@@ -64,6 +65,10 @@ cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, u
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                           int nchunks, int tiles_per_cta, cudaStream_t s);
+int logits_tma_max_tiles();
+cudaError_t launch_logits_tma(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
+                              int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
+                              int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache, int B, int Hq,
                         int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep,
                         float scale_log2, float* partials, int nchunks, int tiles_per_cta, cudaStream_t s);

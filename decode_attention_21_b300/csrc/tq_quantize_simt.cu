@@ -280,17 +280,21 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
 // loads are all in flight at once.  Scalar mode only; same arithmetic and bit
 // layout as k_quantize_simt.
 template <int D>
-__device__ __forceinline__ float matvec_quarter(const float* __restrict__ MT, const float* xs, int i, int q) {
-  constexpr int J = D / 4;
-  const float* col = MT + (size_t)(q * J) * D + i;
-  float m[J];
+struct Quarter {
+  float m[D / 4];
+  // column slice i, rows q*D/4 .. (q+1)*D/4 - 1 of the transposed matrix MT
+  __device__ __forceinline__ void load(const float* __restrict__ MT, int i, int q) {
+    const float* col = MT + (size_t)(q * (D / 4)) * D + i;
 #pragma unroll
-  for (int j = 0; j < J; ++j) m[j] = __ldg(col + (size_t)j * D);
-  float acc = 0.f;
+    for (int j = 0; j < D / 4; ++j) m[j] = __ldg(col + (size_t)j * D);
+  }
+  __device__ __forceinline__ float dot(const float* xs, int q) const {
+    float acc = 0.f;
 #pragma unroll
-  for (int j = 0; j < J; ++j) acc = fmaf(m[j], xs[q * J + j], acc);
-  return acc;
-}
+    for (int j = 0; j < D / 4; ++j) acc = fmaf(m[j], xs[q * (D / 4) + j], acc);
+    return acc;
+  }
+};
 
 template <int D>
 __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* __restrict__ cache, int64_t cache_rows,
@@ -308,6 +312,12 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
   const bool prod = cb.kind == 0;
   uint32_t* recs = reinterpret_cast<uint32_t*>(cache);
   unsigned char* norms = cache + norm_offset(cb, cache_rows);
+  // at d = 128 both matrices' column slices stay in registers for every row
+  // of this CTA (one round trip to L2); the 1024-thread d = 256 CTA reloads them
+  constexpr bool kKeep = D == 128;
+  Quarter<kKeep ? D : 4> mpi, ms;
+  if (kKeep && !y_in) mpi.load(cb.PiT, i, q);
+  if (kKeep && prod) ms.load(cb.ST, i, q);
   for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
     float y = 0.f, nrm = 0.f;
     if (y_in) {
@@ -327,7 +337,13 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
         xs[i] = v;
       }
       __syncthreads();
-      part[q][i] = matvec_quarter<D>(cb.PiT, xs, i, q);
+      if constexpr (kKeep) {
+        part[q][i] = mpi.dot(xs, q);
+      } else {
+        Quarter<D> m1;
+        m1.load(cb.PiT, i, q);
+        part[q][i] = m1.dot(xs, q);
+      }
       __syncthreads();
       if (q == 0) {
         y = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
@@ -373,7 +389,13 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
     __syncthreads();
     float gamma = 0.f;
     if (prod) {
-      part[q][i] = matvec_quarter<D>(cb.ST, xs, i, q);
+      if constexpr (kKeep) {
+        part[q][i] = ms.dot(xs, q);
+      } else {
+        Quarter<D> m2;
+        m2.load(cb.ST, i, q);
+        part[q][i] = m2.dot(xs, q);
+      }
       __syncthreads();
       if (q == 0) {
         float ss = 0.f;

@@ -64,19 +64,20 @@ __global__ void __launch_bounds__(512) k_prep(const Dev cb, const float* __restr
   const int G = Hq / Hkv;
   const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
   const bool live = slot < G;
-  __shared__ float sq[d], sq1[d], sq2[d], part[4][d];
+  __shared__ float sq[d], sq1[d], sq2[d], part[4][d], part2[4][d];
   __shared__ float red[4];
   const int tid = threadIdx.x;
   const int i = tid & 127, qt = tid >> 7;
   if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
+  // q' = Pi q and q'' = (S Pi) q in the same pass
   part[qt][i] = dot32(cb.PiT, sq, i, qt);
+  part2[qt][i] = dot32(cb.SPT, sq, i, qt);
   __syncthreads();
-  if (tid < d) sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
-  __syncthreads();
-  part[qt][i] = dot32(cb.ST, sq1, i, qt);
-  __syncthreads();
-  if (tid < d) sq2[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  if (tid < d) {
+    sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+    sq2[tid] = (part2[0][tid] + part2[1][tid]) + (part2[2][tid] + part2[3][tid]);
+  }
   __syncthreads();
   const int nv = cb.nv;
   float cmax = 0.f, csum = 0.f;
@@ -283,6 +284,134 @@ __global__ void __launch_bounds__(128, 3) k_logits(const Dev cb, const uint8_t* 
     cur = nxt;
   }
 }
+
+// ---------------------------------------------------------------------------
+// Logits with bulk-copy staging: the CTA's whole chunk of key records and
+// norms (up to kStageTiles x kMaxStages tiles) is requested at once with
+// cp.async.bulk into shared memory, one mbarrier per stage of kStageTiles
+// tiles, and the warps score each stage as it lands.  Requires capacity to be
+// a multiple of 16 (every copied tile lies inside its sequence's rows).
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kStageTiles = 8;
+constexpr int kMaxStages = 8;
+constexpr long long kWaitLimit = 1ll << 26;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+}  // namespace
+
+template <int NV, int P>
+__global__ void __launch_bounds__(128) k_logits_tma(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
+                                                    int64_t capacity, int64_t cache_rows,
+                                                    const int32_t* __restrict__ seq_lens,
+                                                    const uint8_t* __restrict__ prep, float* __restrict__ logits,
+                                                    int tiles_per_cta, int* __restrict__ status) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ __align__(8) uint64_t bars[kMaxStages];
+  constexpr int RB = 16 * P;                 // record bytes at d = 128
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int G = Hq / Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t L = seq_lens[b];
+  const int64_t ntiles = (L + 15) / 16;
+  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
+  if (tile0 >= tend) return;
+  const int nt = (int)(tend - tile0);
+  const int nstages = (nt + kStageTiles - 1) / kStageTiles;
+  uint8_t* srec = sm;
+  uint8_t* snrm = sm + (size_t)tiles_per_cta * 16 * RB;
+  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
+  const uint8_t* grec = kcache + (rowbase + tile0 * 16) * RB;
+  const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows) + (rowbase + tile0 * 16) * 4;
+  if (tid == 0) {
+    for (int st = 0; st < nstages; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[st])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int st = 0; st < nstages; ++st) {
+      const int t_a = st * kStageTiles, t_n = min(kStageTiles, nt - t_a);
+      const uint32_t rb = (uint32_t)(t_n * 16 * RB), nb = (uint32_t)(t_n * 16 * 4);
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(&bars[st])), "r"(rb + nb)
+                   : "memory");
+      bulk_g2s(su32(srec + (size_t)t_a * 16 * RB), grec + (size_t)t_a * 16 * RB, rb, su32(&bars[st]));
+      bulk_g2s(su32(snrm + (size_t)t_a * 16 * 4), gnrm + (size_t)t_a * 16 * 4, nb, su32(&bars[st]));
+    }
+  }
+  QK16<NV, P> qk;
+  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
+  __syncthreads();
+  const float kq = cb.qjl_const;
+  float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
+  bool ok = true;
+  for (int st = 0; st < nstages && ok; ++st) {
+    if (!bar_wait(su32(&bars[st]), 0)) {
+      ok = false;
+      break;
+    }
+    const int t_a = st * kStageTiles, t_e = min(t_a + kStageTiles, nt);
+    for (int lt = t_a + warp; lt < t_e; lt += 4) {
+      const uint8_t* ra = srec + ((size_t)lt * 16 + g) * RB + c * P * 4;
+      const uint8_t* rbp = ra + 8 * RB;
+      uint32_t wa[P], wb[P];
+      if constexpr (P == 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(ra);
+        const uint4 y = *reinterpret_cast<const uint4*>(rbp);
+        wa[0] = x.x; wa[1] = x.y; wa[2] = x.z; wa[3] = x.w;
+        wb[0] = y.x; wb[1] = y.y; wb[2] = y.z; wb[3] = y.w;
+      } else {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          wa[p] = reinterpret_cast<const uint32_t*>(ra)[p];
+          wb[p] = reinterpret_cast<const uint32_t*>(rbp)[p];
+        }
+      }
+      const uint32_t na = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g];
+      const uint32_t nb = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g + 8];
+      const int64_t ta = (tile0 + lt) * 16 + g, tb = ta + 8;
+      if (ta >= L) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) wa[p] = 0;
+      }
+      if (tb >= L) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) wb[p] = 0;
+      }
+      float s1a, s1b, s2a, s2b;
+      qk.score(wa, wb, s1a, s1b, s2a, s2b);
+      if (c < G) {
+        if (ta < L) out[ta] = est_from(na, s1a, s2a, kq);
+        if (tb < L) out[tb] = est_from(nb, s1b, s2b, kq);
+      }
+    }
+  }
+  if (!ok) {
+    if (tid == 0) atomicExch(status, 2);
+    // let the remaining copies land (bounded) before the CTA's shared memory is released
+    for (int st = 0; st < nstages; ++st) bar_wait(su32(&bars[st]), 0);
+  }
+}
+
+int logits_tma_max_tiles() { return kStageTiles * kMaxStages; }
 
 // ---------------------------------------------------------------------------
 // Fused decode attention: QK as above, online softmax per head slot, and the
@@ -504,6 +633,33 @@ cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int H
     default: k_logits<4, 4><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
   }
   return cudaGetLastError();
+}
+
+template <int NV, int P>
+static cudaError_t logits_tma_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity, int64_t rows,
+                                const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks, int tpc,
+                                int* status, cudaStream_t s) {
+  const size_t smem = (size_t)tpc * 16 * (16 * P + 4);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_logits_tma<NV, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((size_t)logits_tma_max_tiles() * 16 * (16 * 4 + 4)));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k_logits_tma<NV, P><<<dim3(nchunks, Hkv, B), 128, smem, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits,
+                                                                tpc, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logits_tma(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity, int64_t rows,
+                              const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks, int tpc,
+                              int* status, cudaStream_t s) {
+  switch (cb.b1) {
+    case 1: return logits_tma_t<1, 2>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+    case 2: return logits_tma_t<2, 3>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+    default: return logits_tma_t<4, 4>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+  }
 }
 
 cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq, int Hkv,

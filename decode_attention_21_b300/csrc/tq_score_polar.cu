@@ -108,19 +108,20 @@ __global__ void __launch_bounds__(512) k_prep_polar(const Dev cb, const float* _
   const int G = Hq / Hkv;
   const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
   const bool live = slot < G;
-  __shared__ float sq[d], sq1[d], sq2[d], part[4][d];
+  __shared__ float sq[d], sq1[d], sq2[d], part[4][d], part2[4][d];
   __shared__ float red[3];
   const int tid = threadIdx.x;
   const int i = tid & 127, qt = tid >> 7;
   if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
+  // q' = Pi q and q'' = (S Pi) q in the same pass
   part[qt][i] = dot32p(cb.PiT, sq, i, qt);
+  part2[qt][i] = dot32p(cb.SPT, sq, i, qt);
   __syncthreads();
-  if (tid < d) sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
-  __syncthreads();
-  part[qt][i] = dot32p(cb.ST, sq1, i, qt);
-  __syncthreads();
-  if (tid < d) sq2[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  if (tid < d) {
+    sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+    sq2[tid] = (part2[0][tid] + part2[1][tid]) + (part2[2][tid] + part2[3][tid]);
+  }
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < 3) {

@@ -90,19 +90,19 @@ __global__ void __launch_bounds__(1024) k_search_prep(const Dev cb, const float*
   const int grp = blockIdx.x, slot = blockIdx.y;
   const int qi = grp * 4 + slot;
   const bool live = qi < nq;
-  __shared__ float sq[kD], sq1[kD], sq2[kD], part[4][kD];
+  __shared__ float sq[kD], sq1[kD], sq2[kD], part[4][kD], part2[4][kD];
   __shared__ float red[4];
   const int tid = threadIdx.x;
   const int i = tid & 255, qt = tid >> 8;
   if (tid < kD) sq[tid] = (live && tid < d_in) ? q[(size_t)qi * d_in + tid] : 0.f;
   __syncthreads();
   part[qt][i] = dot64(cb.PiT, sq, i, qt);
+  part2[qt][i] = dot64(cb.SPT, sq, i, qt);
   __syncthreads();
-  if (tid < kD) sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
-  __syncthreads();
-  part[qt][i] = dot64(cb.ST, sq1, i, qt);
-  __syncthreads();
-  if (tid < kD) sq2[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+  if (tid < kD) {
+    sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+    sq2[tid] = (part2[0][tid] + part2[1][tid]) + (part2[2][tid] + part2[3][tid]);
+  }
   __syncthreads();
   const int nv = cb.nv;
   float cmax = 0.f, csum = 0.f;
