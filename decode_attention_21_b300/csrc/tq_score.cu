@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(512) k_prep(const Dev cb, const float* __restr
   const int G = Hq / Hkv;
   const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
   const bool live = slot < G;
+  // The scoring kernel that follows may start now: it only reads the key
+  // cache (written before this kernel started) until it waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float sq[d], sq1[d], sq2[d], part[4][d], part2[4][d];
   __shared__ float red[4];
   const int tid = threadIdx.x;
@@ -191,6 +194,40 @@ struct QK16 {
     s1b = fmaf(S1, (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]), K1);
     s2a = fmaf(S2, (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]), K2);
     s2b = fmaf(S2, (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]), K2);
+  }
+
+  // Two 16-key tiles at once, plane by plane, so their MMA chains interleave.
+  __device__ __forceinline__ void score2(const uint32_t (&wa)[P], const uint32_t (&wb)[P], const uint32_t (&xa)[P],
+                                         const uint32_t (&xb)[P], float& s1a, float& s1b, float& s2a, float& s2b,
+                                         float& u1a, float& u1b, float& u2a, float& u2b) const {
+    float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float bcc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float bcc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    plane(wa[P - 1], wb[P - 1], NV, acc2);
+    plane(xa[P - 1], xb[P - 1], NV, bcc2);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      uint32_t pa = 0, pb = 0, qa = 0, qb = 0;
+#pragma unroll
+      for (int p = 0; p < P - 1; ++p)
+        if (kOddMask[v] >> p & 1u) {
+          pa ^= wa[p];
+          pb ^= wb[p];
+          qa ^= xa[p];
+          qb ^= xb[p];
+        }
+      plane(pa, pb, v, acc1);
+      plane(qa, qb, v, bcc1);
+    }
+    s1a = fmaf(S1, (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]), K1);
+    s1b = fmaf(S1, (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]), K1);
+    s2a = fmaf(S2, (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]), K2);
+    s2b = fmaf(S2, (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]), K2);
+    u1a = fmaf(S1, (bcc1[0][0] + bcc1[0][1]) + (bcc1[1][0] + bcc1[1][1]), K1);
+    u1b = fmaf(S1, (bcc1[0][2] + bcc1[0][3]) + (bcc1[1][2] + bcc1[1][3]), K1);
+    u2a = fmaf(S2, (bcc2[0][0] + bcc2[0][1]) + (bcc2[1][0] + bcc2[1][1]), K2);
+    u2b = fmaf(S2, (bcc2[0][2] + bcc2[0][3]) + (bcc2[1][2] + bcc2[1][3]), K2);
   }
 };
 
@@ -357,51 +394,71 @@ __global__ void __launch_bounds__(128) k_logits_tma(const Dev cb, const uint8_t*
       bulk_g2s(su32(snrm + (size_t)t_a * 16 * 4), gnrm + (size_t)t_a * 16 * 4, nb, su32(&bars[st]));
     }
   }
+  // query fragments come from the preceding prep grid (launched as its
+  // programmatic dependent): wait for it only now, after the copies are in flight
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   QK16<NV, P> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
   __syncthreads();
   const float kq = cb.qjl_const;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
   bool ok = true;
+  auto tile_words = [&](int lt, uint32_t(&wa)[P], uint32_t(&wb)[P], uint32_t& na, uint32_t& nb) {
+    const uint8_t* ra = srec + ((size_t)lt * 16 + g) * RB + c * P * 4;
+    const uint8_t* rbp = ra + 8 * RB;
+    if constexpr (P == 4) {
+      const uint4 x = *reinterpret_cast<const uint4*>(ra);
+      const uint4 y = *reinterpret_cast<const uint4*>(rbp);
+      wa[0] = x.x; wa[1] = x.y; wa[2] = x.z; wa[3] = x.w;
+      wb[0] = y.x; wb[1] = y.y; wb[2] = y.z; wb[3] = y.w;
+    } else {
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        wa[p] = reinterpret_cast<const uint32_t*>(ra)[p];
+        wb[p] = reinterpret_cast<const uint32_t*>(rbp)[p];
+      }
+    }
+    na = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g];
+    nb = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g + 8];
+    const int64_t ta = (tile0 + lt) * 16 + g;
+    if (ta >= L) {
+#pragma unroll
+      for (int p = 0; p < P; ++p) wa[p] = 0;
+    }
+    if (ta + 8 >= L) {
+#pragma unroll
+      for (int p = 0; p < P; ++p) wb[p] = 0;
+    }
+  };
+  auto emit = [&](int lt, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
+    const int64_t ta = (tile0 + lt) * 16 + g, tb = ta + 8;
+    if (c < G) {
+      if (ta < L) out[ta] = est_from(na, s1a, s2a, kq);
+      if (tb < L) out[tb] = est_from(nb, s1b, s2b, kq);
+    }
+  };
   for (int st = 0; st < nstages && ok; ++st) {
     if (!bar_wait(su32(&bars[st]), 0)) {
       ok = false;
       break;
     }
     const int t_a = st * kStageTiles, t_e = min(t_a + kStageTiles, nt);
-    for (int lt = t_a + warp; lt < t_e; lt += 4) {
-      const uint8_t* ra = srec + ((size_t)lt * 16 + g) * RB + c * P * 4;
-      const uint8_t* rbp = ra + 8 * RB;
-      uint32_t wa[P], wb[P];
-      if constexpr (P == 4) {
-        const uint4 x = *reinterpret_cast<const uint4*>(ra);
-        const uint4 y = *reinterpret_cast<const uint4*>(rbp);
-        wa[0] = x.x; wa[1] = x.y; wa[2] = x.z; wa[3] = x.w;
-        wb[0] = y.x; wb[1] = y.y; wb[2] = y.z; wb[3] = y.w;
+    // two tiles per iteration (warp, warp + 4) for independent MMA chains
+    for (int lt = t_a + warp; lt < t_e; lt += 8) {
+      const int lt2 = lt + 4;
+      uint32_t wa[P], wb[P], xa[P], xb[P], na, nb, ma = 0, mb = 0;
+      tile_words(lt, wa, wb, na, nb);
+      const bool two = lt2 < t_e;
+      if (two) {
+        tile_words(lt2, xa, xb, ma, mb);
       } else {
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-          wa[p] = reinterpret_cast<const uint32_t*>(ra)[p];
-          wb[p] = reinterpret_cast<const uint32_t*>(rbp)[p];
-        }
+        for (int p = 0; p < P; ++p) xa[p] = xb[p] = 0;
       }
-      const uint32_t na = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g];
-      const uint32_t nb = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g + 8];
-      const int64_t ta = (tile0 + lt) * 16 + g, tb = ta + 8;
-      if (ta >= L) {
-#pragma unroll
-        for (int p = 0; p < P; ++p) wa[p] = 0;
-      }
-      if (tb >= L) {
-#pragma unroll
-        for (int p = 0; p < P; ++p) wb[p] = 0;
-      }
-      float s1a, s1b, s2a, s2b;
-      qk.score(wa, wb, s1a, s1b, s2a, s2b);
-      if (c < G) {
-        if (ta < L) out[ta] = est_from(na, s1a, s2a, kq);
-        if (tb < L) out[tb] = est_from(nb, s1b, s2b, kq);
-      }
+      float s1a, s1b, s2a, s2b, u1a, u1b, u2a, u2b;
+      qk.score2(wa, wb, xa, xb, s1a, s1b, s2a, s2b, u1a, u1b, u2a, u2b);
+      emit(lt, na, nb, s1a, s1b, s2a, s2b);
+      if (two) emit(lt2, ma, mb, u1a, u1b, u2a, u2b);
     }
   }
   if (!ok) {
@@ -647,9 +704,18 @@ static cudaError_t logits_tma_t(const Dev& cb, const uint8_t* kc, int B, int Hq,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_logits_tma<NV, P><<<dim3(nchunks, Hkv, B), 128, smem, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits,
-                                                                tpc, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nchunks, Hkv, B);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_logits_tma<NV, P>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc,
+                            status);
 }
 
 cudaError_t launch_logits_tma(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity, int64_t rows,
