@@ -122,8 +122,10 @@ void chunking(int B, int Hkv, int64_t capacity, int target, int* nchunks, int* t
     *tiles_per_cta = 4;
     return;
   }
+  // as many chunks per unit as fit in one wave of `target` resident CTAs
+  // (rounding up would leave a few CTAs for a second wave)
   const int64_t units = (int64_t)B * Hkv;
-  const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
+  const int64_t want = std::max<int64_t>(1, target / units);
   int64_t tpc = std::max<int64_t>(4, (tiles + want - 1) / want);
   *tiles_per_cta = (int)tpc;
   *nchunks = (int)((tiles + tpc - 1) / tpc);
