@@ -86,7 +86,7 @@ bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t c
 }
 
 constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
-constexpr int kLogitsCtas = 148 * 3;   // resident CTAs of the logits kernel
+constexpr int kLogitsCtas = 148 * 4;   // resident CTAs of the logits kernel
 constexpr int kAttnCtas = 148 * 2;     // resident CTAs of the attention kernel
 
 template <class T>
@@ -480,7 +480,7 @@ tq_status tq_quantize_rotated(const tq_codebook* cb, void* cache, int64_t cache_
 size_t tq_logits_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv) {
   (void)Hq;
   if (!kcb || B <= 0 || Hkv <= 0) return 0;
-  return (size_t)tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d));
+  return (size_t)tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d));
 }
 
 static tq_status check_heads(const char* what, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
@@ -514,10 +514,10 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
                                                          capacity, rows, seq_lens, prep, logits, nchunks, tpc, s));
   }
   if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
-  if (capacity % 16 == 0 && tpc <= tq::logits_tma_max_tiles() && aligned16(kcache))
-    return launched("tq_logits", tq::launch_logits_tma(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
-                                                       capacity, rows, seq_lens, prep, logits, nchunks, tpc,
-                                                       kcb->d_status, s));
+  if (capacity % 16 == 0)
+    return launched("tq_logits", tq::launch_logits_staged(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                          capacity, rows, seq_lens, prep, logits, nchunks, tpc,
+                                                          kcb->d_status, s));
   return launched("tq_logits", tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
                                                  rows, seq_lens, prep, logits, nchunks, tpc, s));
 }
@@ -526,7 +526,7 @@ size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t 
   if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
   int nchunks, tpc;
   chunking(B, Hkv, capacity, kAttnCtas, &nchunks, &tpc);
-  const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d));
+  const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d));
   const int64_t parts = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d) * 4;
   (void)Hq;
   return (size_t)(prep + parts);
@@ -550,7 +550,7 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   float* parts = reinterpret_cast<float*>(
-      prep + tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.nv, kcb->dev.d)));
+      prep + tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d)));
   if (kcb->dev.mode != vcb->dev.mode)
     return fail(TQ_EUNSUPPORTED, "tq_decode_attention: keys and values must use the same stage-1 mode");
   int nchunks, tpc;

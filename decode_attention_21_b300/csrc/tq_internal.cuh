@@ -42,12 +42,10 @@ inline __host__ __device__ int64_t norm_offset(const Dev& cb, int64_t rows) {
 }
 
 // Per-(sequence, kv head) block of query data prepared once per step.
-//   header: float scale1[4], scale2[4]  (power-of-two scales per head slot)
-//   fragments: [nv + 1][d/16][32 lanes] uint2   (last plane = QJL)
+//   header: float S1[4], S2[4], K1[4], K2[4]  (per head slot)
+//   fragments: [2][d/16][32 lanes] uint2  (plane 0 = stage 1, plane 1 = QJL)
 constexpr int kPrepHeader = 64;
-inline __host__ __device__ int64_t prep_block_bytes(int nv, int d) {
-  return kPrepHeader + (int64_t)(nv + 1) * (d / 16) * 32 * 8;
-}
+inline __host__ __device__ int64_t prep_block_bytes(int d) { return kPrepHeader + (int64_t)2 * (d / 16) * 32 * 8; }
 
 // Split-KV partial of one warp: per head slot (4): m, l, acc[d].
 inline __host__ __device__ int64_t partial_floats(int d) { return 4 * (2 + d); }
@@ -65,10 +63,9 @@ cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, u
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                           int nchunks, int tiles_per_cta, cudaStream_t s);
-int logits_tma_max_tiles();
-cudaError_t launch_logits_tma(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
-                              int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
-                              int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
+cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
+                                 int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
+                                 int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache, int B, int Hq,
                         int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep,
                         float scale_log2, float* partials, int nchunks, int tiles_per_cta, cudaStream_t s);

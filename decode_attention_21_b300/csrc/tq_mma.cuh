@@ -35,18 +35,42 @@ __device__ __forceinline__ float piece16(float x, int which) {
   return which == 0 ? hi : x - hi;
 }
 
-// The 16 fp16 operand registers of one packed word: register beta holds bits
-// beta and beta+16 (low and high half) at mantissa position 6 + (beta mod 4).
+// Packed bits as fp16 tensor-core operands.  A half whose only set bit is
+// bit p <= 11 is exactly 2^(p - 24) (bits 0..9 are subnormal mantissa bits,
+// bits 10 and 11 the two lowest exponent bits).  Operand register beta holds
+// bits beta and beta + 16 of a word w: in place for beta < 12, from w >> 4
+// (so at position beta - 4) for beta >= 12.  The other side of the product
+// carries bit_factor(beta) = 1 / (value of the set bit).
+__host__ __device__ constexpr float bit_factor(int beta) {
+  return beta < 12 ? (float)(1u << (24 - beta)) : (float)(1u << (28 - beta));
+}
+constexpr float kMaxBitFactor = 16777216.f;  // bit_factor(0) = 2^24
+
+// Operand register beta of word w (w4 = w >> 4).
+__device__ __forceinline__ uint32_t bit_operand(uint32_t w, uint32_t w4, int beta) {
+  return beta < 12 ? (w & (0x00010001u << beta)) : (w4 & (0x00010001u << (beta - 4)));
+}
+
+// All 16 operand registers of one word.
 __device__ __forceinline__ void expand16(uint32_t w, uint32_t (&r)[16]) {
-  const uint32_t t0 = w << 6, t1 = w << 2, t2 = w >> 2, t3 = w >> 6;
+  const uint32_t w4 = w >> 4;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t m = 0x00400040u << e;
-    r[e] = t0 & m;
-    r[4 + e] = t1 & m;
-    r[8 + e] = t2 & m;
-    r[12 + e] = t3 & m;
-  }
+  for (int beta = 0; beta < 16; ++beta) r[beta] = bit_operand(w, w4, beta);
+}
+
+// Variant for operands multiplied by small values (softmax weights): chained
+// fp16 MMAs accumulate products of the deepest subnormals (bits 0..5) less
+// accurately, so bits 0..5 move up by 6 (from w << 6).  Every set bit is then
+// worth 2^-18 .. 2^-13 and value_factor(beta) = 1 / (value of the set bit).
+__host__ __device__ constexpr float value_factor(int beta) {
+  return beta < 6 ? (float)(1u << (18 - beta)) : bit_factor(beta);
+}
+
+__device__ __forceinline__ void expand16_v(uint32_t w, uint32_t (&r)[16]) {
+  const uint32_t w6 = w << 6, w4 = w >> 4;
+#pragma unroll
+  for (int beta = 0; beta < 16; ++beta)
+    r[beta] = beta < 6 ? (w6 & (0x00010001u << (beta + 6))) : bit_operand(w, w4, beta);
 }
 
 // Power of two s with amax / s <= target (1 for amax = 0).

@@ -36,198 +36,221 @@ using namespace mma;
 
 // ---------------------------------------------------------------------------
 // Query preparation: one CTA per (kv head, head slot, sequence).  q' = Pi q,
-// q'' = S q', the per-slot constants and the fp16 B fragments of every
-// stage-1 virtual plane and of the sign plane.
-//   header (floats): S1[4], S2[4], K1[4], K2[4]
-//   fragments: [plane][kb][lane] uint2, plane nv = QJL, kb = 0..7, column
-//   2*slot + piece (piece 0 = hi, 1 = lo).
+// q'' = S q', the per-slot constants and the fp16 B fragments of the two
+// query-side planes:
+//   plane 0 (stage 1): q'_k * bit_factor / S1, shared by every virtual plane
+//     (the kernels apply -2 coef_v S1 to each virtual plane's MMA sum);
+//   plane 1 (QJL):     2 q''_k * bit_factor / S2.
+//   header (floats): S1[4], S2[4], K1[4] = (sum coef) sum q', K2[4] = -sum q''
+//   fragments: [plane][kb][lane] uint2, column 2*slot + piece (piece 0 = hi,
+//   1 = lo).
 // Element k = 2c + e (b0) / 2c + 8 + e (b1) of k-block kb is coordinate
-// 32c + beta + 16e with beta = 2kb (b0) or 2kb + 1 (b1); its key bit sits at
-// mantissa position 6 + (beta mod 4), whose factor 2^-(pos - 24) the query
-// side absorbs.
+// 32c + beta + 16e with beta = 2kb (b0) or 2kb + 1 (b1); its key bit sits in
+// operand register beta, whose bit value 1 / bit_factor(beta) the query side
+// absorbs.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float dot32(const float* __restrict__ MT, const float* xs, int i, int qt) {
-  constexpr int d = 128;
-  const float* col = MT + (size_t)(32 * qt) * d + i;
-  float m[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) m[j] = __ldg(col + (size_t)j * d);
-  float acc = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) acc = fmaf(m[j], xs[32 * qt + j], acc);
-  return acc;
+//
+// One cluster of 4 CTAs per (kv head, head slot, sequence): CTA r computes
+// the 32 coordinates 32r .. 32r+31 (word column r), reading only that slice
+// of Pi and S Pi, and the cluster combines the per-CTA maxima and sums
+// through distributed shared memory.
+// ---------------------------------------------------------------------------
+namespace {
+// Store v at the address of p in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void cluster_st(float* p, uint32_t rank, float v) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
 }
 
-__global__ void __launch_bounds__(512) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+}  // namespace
+
+__global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
                                               uint8_t* __restrict__ prep) {
   constexpr int d = 128;
   const int G = Hq / Hkv;
-  const int kvh = blockIdx.x >> 2, slot = blockIdx.x & 3, b = blockIdx.y;
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  const int unit = blockIdx.x >> 2;               // kv head * 4 + slot
+  const int kvh = unit >> 2, slot = unit & 3, b = blockIdx.y;
   const bool live = slot < G;
   // The scoring kernel that follows may start now: it only reads the key
   // cache (written before this kernel started) until it waits for this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float sq[d], sq1[d], sq2[d], part[4][d], part2[4][d];
-  __shared__ float red[4];
+  __shared__ float sq[d], part[2][4][32], sv[2][32];
+  __shared__ float red[4][4];   // [source rank][max |q'|, max |2 q''|, sum q', sum q'']
   const int tid = threadIdx.x;
-  const int i = tid & 127, qt = tid >> 7;
+  const int mat = tid >> 7, qt = (tid >> 5) & 3, o = tid & 31;
+  // Pi^T (mat 0) or (S Pi)^T (mat 1): rows 32 qt .. 32 qt + 31, column 32 r + o;
+  // these loads do not depend on q, so they are issued before waiting for it
+  const float* col = (mat == 0 ? cb.PiT : cb.SPT) + (size_t)(32 * qt) * d + 32 * r + o;
+  float m[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) m[j] = __ldg(col + (size_t)j * d);
   if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
-  // q' = Pi q and q'' = (S Pi) q in the same pass
-  part[qt][i] = dot32(cb.PiT, sq, i, qt);
-  part2[qt][i] = dot32(cb.SPT, sq, i, qt);
-  __syncthreads();
-  if (tid < d) {
-    sq1[tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
-    sq2[tid] = (part2[0][tid] + part2[1][tid]) + (part2[2][tid] + part2[3][tid]);
-  }
-  __syncthreads();
-  const int nv = cb.nv;
-  float cmax = 0.f, csum = 0.f;
-  for (int v = 0; v < nv; ++v) {
-    cmax = fmaxf(cmax, fabsf(cb.vcoef[v]));
-    csum += cb.vcoef[v];
-  }
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp < 4) {
-    // warp 0: max |stage-1 B|, 1: max |QJL B| (before the mantissa factor),
-    // 2: sum q', 3: sum q''
-    float v = 0.f;
-    for (int k = lane; k < d; k += 32) {
-      if (warp == 0) v = fmaxf(v, 2.f * cmax * fabsf(sq1[k]));
-      else if (warp == 1) v = fmaxf(v, 2.f * fabsf(sq2[k]));
-      else if (warp == 2) v += sq1[k];
-      else v += sq2[k];
-    }
+  float acc = 0.f;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float u = __shfl_xor_sync(kFull, v, o);
-      v = warp < 2 ? fmaxf(v, u) : v + u;
-    }
-    if (lane == 0) red[warp] = v;
-  }
+  for (int j = 0; j < 32; ++j) acc = fmaf(m[j], sq[32 * qt + j], acc);
+  part[mat][qt][o] = acc;
   __syncthreads();
-  // largest mantissa factor 2^(24 - 6) = 2^18; keep |B| <= 2^14
-  const float S1 = pow2_scale(red[0] * 262144.f, 16384.f), S2 = pow2_scale(red[1] * 262144.f, 16384.f);
-  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(nv, d);
+  if (tid < 64) {
+    // warp 0: q'_{32r+o}; warp 1: q''_{32r+o}.  Local max |q'| (|2 q''|) and sum.
+    const int mm = tid >> 5;
+    const float v = (part[mm][0][o] + part[mm][1][o]) + (part[mm][2][o] + part[mm][3][o]);
+    sv[mm][o] = v;
+    float mx = mm == 0 ? fabsf(v) : 2.f * fabsf(v), sm = v;
+#pragma unroll
+    for (int k = 16; k; k >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, k));
+      sm += __shfl_xor_sync(kFull, sm, k);
+    }
+    // push this CTA's partials into slot r of every cluster CTA (itself included)
+    if (o < 4) {
+      cluster_st(&red[r][mm], (uint32_t)o, mx);
+      cluster_st(&red[r][2 + mm], (uint32_t)o, sm);
+    }
+  }
+  cluster_sync();
+  // every CTA combines the four partials in rank order (identical results)
+  float mx1 = 0.f, mx2 = 0.f, sm1 = 0.f, sm2 = 0.f;
+  for (int k = 0; k < 4; ++k) {
+    mx1 = fmaxf(mx1, red[k][0]);
+    mx2 = fmaxf(mx2, red[k][1]);
+    sm1 += red[k][2];
+    sm2 += red[k][3];
+  }
+  const int nv = cb.nv;
+  float csum = 0.f;
+  for (int v = 0; v < nv; ++v) csum += cb.vcoef[v];
+  // keep |B| <= 2^14 at the largest bit factor
+  const float S1 = pow2_scale(mx1 * kMaxBitFactor, 16384.f), S2 = pow2_scale(mx2 * kMaxBitFactor, 16384.f);
+  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(d);
   float* hdr = reinterpret_cast<float*>(blk);
-  if (tid == 0) {
+  if (r == 0 && tid == 0) {
     hdr[slot] = live ? S1 : 0.f;
     hdr[4 + slot] = live ? S2 : 0.f;
-    hdr[8 + slot] = live ? csum * red[2] : 0.f;
-    hdr[12 + slot] = live ? -red[3] : 0.f;
+    hdr[8 + slot] = live ? csum * sm1 : 0.f;
+    hdr[12 + slot] = live ? -sm2 : 0.f;
   }
-  // fragments of the 8 lanes whose column belongs to this slot (g = 2 slot + piece)
+  // fragments of this word column (c = r) for this slot's lanes g = 2 slot + piece
   uint2* frag = reinterpret_cast<uint2*>(blk + kPrepHeader);
-  const int total = (nv + 1) * 8 * 8;
-  for (int e = tid; e < total; e += blockDim.x) {
-    const int sub = e & 7, kb = (e >> 3) & 7, v = e >> 6;
-    const int pc = sub >> 2, c = sub & 3;
+  if (tid < 32) {
+    const int pc = tid & 1, kb = (tid >> 1) & 7, v = tid >> 4;
     const int g = 2 * slot + pc;
     float vals[4] = {0.f, 0.f, 0.f, 0.f};
     if (live) {
       for (int t = 0; t < 4; ++t) {
         const int beta = 2 * kb + (t >> 1);
-        const int k = 32 * c + beta + 16 * (t & 1);
-        const float pf = (float)(1 << (18 - (beta & 3)));
-        const float x = v < nv ? -2.f * cb.vcoef[v] * sq1[k] * pf / S1 : 2.f * sq2[k] * pf / S2;
+        const int k = beta + 16 * (t & 1);          // local coordinate (32 r + k)
+        const float x = v == 0 ? sv[0][k] * bit_factor(beta) / S1 : 2.f * sv[1][k] * bit_factor(beta) / S2;
         vals[t] = piece16(x, pc);
       }
     }
-    frag[(v * 8 + kb) * 32 + g * 4 + c] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
+    frag[(v * 8 + kb) * 32 + g * 4 + r] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
   }
 }
 
 // ---------------------------------------------------------------------------
-// QK for one 16-key tile: thread (g, c) gets the two inner products of keys
-// g and g+8 for head slot c.
+// QK for T 16-key tiles at once: thread (g, c) gets the inner products of
+// keys g and g+8 of each tile for head slot c.  The stage-1 virtual planes
+// (odd XOR-products of the code planes) share the query operand and keep one
+// accumulator each; the coefficients -2 coef_v S1 are applied to the sums.
 // ---------------------------------------------------------------------------
 template <int NV, int P>
 struct QK16 {
-  uint2 bq[NV + 1][8];
-  float S1, S2, K1, K2;
+  static constexpr int C1 = NV == 1 ? 2 : 1;   // accumulator chains per virtual plane
+  uint2 bq[2][8];
+  float S2, K1, K2;
+  float cv[NV];
 
-  __device__ __forceinline__ void load(const uint8_t* blk, int lane) {
+  __device__ __forceinline__ void load(const uint8_t* blk, int lane, const Dev& cb) {
     const float* hdr = reinterpret_cast<const float*>(blk);
     const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
 #pragma unroll
-    for (int v = 0; v <= NV; ++v)
+    for (int v = 0; v < 2; ++v)
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb) bq[v][kb] = frag[(v * 8 + kb) * 32 + lane];
     const int c = lane & 3;
-    S1 = hdr[c];
+    const float S1 = hdr[c];
     S2 = hdr[4 + c];
     K1 = hdr[8 + c];
     K2 = hdr[12 + c];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) cv[v] = -2.f * cb.vcoef[v] * S1;
   }
 
-  // Accumulates into chains kb % 2 (two independent accumulator chains per
-  // call so consecutive MMAs do not wait on each other).
-  __device__ __forceinline__ void plane(uint32_t xa, uint32_t xb, int v, float (&acc)[2][4]) const {
-    uint32_t ra[16], rb[16];
-    expand16(xa, ra);
-    expand16(xb, rb);
+  // wa[t], wb[t]: the P plane words (column c) of keys g and g+8 of tile t.
+  // s1[t][0/1], s2[t][0/1]: stage-1 and QJL inner products of keys g, g+8.
+  template <int T>
+  __device__ __forceinline__ void score(const uint32_t (&wa)[T][P], const uint32_t (&wb)[T][P], float (&s1)[T][2],
+                                        float (&s2)[T][2]) const {
+    float a1[T][NV][C1][4], a2[T][2][4];
+    uint32_t xa[T][NV + 1], xb[T][NV + 1], ya[T][NV + 1], yb[T][NV + 1];
 #pragma unroll
-    for (int kb = 0; kb < 8; ++kb)
-      mma_f16(acc[kb & 1], ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
-  }
-
-  // wa, wb: the P plane words (column c) of keys g and g+8
-  __device__ __forceinline__ void score(const uint32_t (&wa)[P], const uint32_t (&wb)[P], float& s1a, float& s1b,
-                                        float& s2a, float& s2b) const {
-    float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    // sign plane first: its chain runs alongside the stage-1 planes
-    plane(wa[P - 1], wb[P - 1], NV, acc2);
+    for (int t = 0; t < T; ++t) {
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      uint32_t xa = 0, xb = 0;
+      for (int v = 0; v < NV; ++v) {
+        uint32_t pa = 0, pb = 0;
 #pragma unroll
-      for (int p = 0; p < P - 1; ++p)
-        if (kOddMask[v] >> p & 1u) {
-          xa ^= wa[p];
-          xb ^= wb[p];
-        }
-      plane(xa, xb, v, acc1);
+        for (int p = 0; p < P - 1; ++p)
+          if (kOddMask[v] >> p & 1u) {
+            pa ^= wa[t][p];
+            pb ^= wb[t][p];
+          }
+        xa[t][v] = pa;
+        xb[t][v] = pb;
+#pragma unroll
+        for (int ch = 0; ch < C1; ++ch)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a1[t][v][ch][e] = 0.f;
+      }
+      xa[t][NV] = wa[t][P - 1];
+      xb[t][NV] = wb[t][P - 1];
+#pragma unroll
+      for (int v = 0; v <= NV; ++v) {
+        ya[t][v] = xa[t][v] >> 4;
+        yb[t][v] = xb[t][v] >> 4;
+      }
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a2[t][ch][e] = 0.f;
     }
-    s1a = fmaf(S1, (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]), K1);
-    s1b = fmaf(S1, (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]), K1);
-    s2a = fmaf(S2, (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]), K2);
-    s2b = fmaf(S2, (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]), K2);
-  }
-
-  // Two 16-key tiles at once, plane by plane, so their MMA chains interleave.
-  __device__ __forceinline__ void score2(const uint32_t (&wa)[P], const uint32_t (&wb)[P], const uint32_t (&xa)[P],
-                                         const uint32_t (&xb)[P], float& s1a, float& s1b, float& s2a, float& s2b,
-                                         float& u1a, float& u1b, float& u2a, float& u2b) const {
-    float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float bcc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float bcc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    plane(wa[P - 1], wb[P - 1], NV, acc2);
-    plane(xa[P - 1], xb[P - 1], NV, bcc2);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      uint32_t pa = 0, pb = 0, qa = 0, qb = 0;
+    for (int kb = 0; kb < 8; ++kb) {
+      const int b0 = 2 * kb, b1 = 2 * kb + 1;
 #pragma unroll
-      for (int p = 0; p < P - 1; ++p)
-        if (kOddMask[v] >> p & 1u) {
-          pa ^= wa[p];
-          pb ^= wb[p];
-          qa ^= xa[p];
-          qb ^= xb[p];
-        }
-      plane(pa, pb, v, acc1);
-      plane(qa, qb, v, bcc1);
+      for (int t = 0; t < T; ++t) {
+        mma_f16(a2[t][kb & 1], bit_operand(xa[t][NV], ya[t][NV], b0), bit_operand(xb[t][NV], yb[t][NV], b0),
+                bit_operand(xa[t][NV], ya[t][NV], b1), bit_operand(xb[t][NV], yb[t][NV], b1), bq[1][kb].x,
+                bq[1][kb].y);
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+          mma_f16(a1[t][v][kb % C1], bit_operand(xa[t][v], ya[t][v], b0), bit_operand(xb[t][v], yb[t][v], b0),
+                  bit_operand(xa[t][v], ya[t][v], b1), bit_operand(xb[t][v], yb[t][v], b1), bq[0][kb].x,
+                  bq[0][kb].y);
+      }
     }
-    s1a = fmaf(S1, (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]), K1);
-    s1b = fmaf(S1, (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]), K1);
-    s2a = fmaf(S2, (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]), K2);
-    s2b = fmaf(S2, (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]), K2);
-    u1a = fmaf(S1, (bcc1[0][0] + bcc1[0][1]) + (bcc1[1][0] + bcc1[1][1]), K1);
-    u1b = fmaf(S1, (bcc1[0][2] + bcc1[0][3]) + (bcc1[1][2] + bcc1[1][3]), K1);
-    u2a = fmaf(S2, (bcc2[0][0] + bcc2[0][1]) + (bcc2[1][0] + bcc2[1][1]), K2);
-    u2b = fmaf(S2, (bcc2[0][2] + bcc2[0][3]) + (bcc2[1][2] + bcc2[1][3]), K2);
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      float ra = K1, rb = K1;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int ch = 0; ch < C1; ++ch) {
+          ra = fmaf(cv[v], a1[t][v][ch][0] + a1[t][v][ch][1], ra);
+          rb = fmaf(cv[v], a1[t][v][ch][2] + a1[t][v][ch][3], rb);
+        }
+      s1[t][0] = ra;
+      s1[t][1] = rb;
+      s2[t][0] = fmaf(S2, (a2[t][0][0] + a2[t][0][1]) + (a2[t][1][0] + a2[t][1][1]), K2);
+      s2[t][1] = fmaf(S2, (a2[t][0][2] + a2[t][0][3]) + (a2[t][1][2] + a2[t][1][3]), K2);
+    }
   }
 };
 
@@ -283,7 +306,7 @@ __device__ __forceinline__ float est_from(uint32_t nrm_bits, float s1, float s2,
 // prefetching its next tile while scoring the current one.
 // ---------------------------------------------------------------------------
 template <int NV, int P>
-__global__ void __launch_bounds__(128, 3) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
+__global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
                                                 int64_t capacity, int64_t cache_rows,
                                                 const int32_t* __restrict__ seq_lens,
                                                 const uint8_t* __restrict__ prep, float* __restrict__ logits,
@@ -298,7 +321,7 @@ __global__ void __launch_bounds__(128, 3) k_logits(const Dev cb, const uint8_t* 
   const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
   if (tile0 + warp >= tend) return;
   QK16<NV, P> qk;
-  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
+  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, cb);
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
@@ -311,27 +334,40 @@ __global__ void __launch_bounds__(128, 3) k_logits(const Dev cb, const uint8_t* 
   for (; tile < tend; tile += 4) {
     const int64_t tn = tile + 4;
     if (tn < tend) nxt.load(recs, nrm, W, rowbase, tn * 16 + g, L, c);
-    float s1a, s1b, s2a, s2b;
-    qk.score(cur.wa, cur.wb, s1a, s1b, s2a, s2b);
+    uint32_t wa[1][P], wb[1][P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      wa[0][p] = cur.wa[p];
+      wb[0][p] = cur.wb[p];
+    }
+    float s1[1][2], s2[1][2];
+    qk.template score<1>(wa, wb, s1, s2);
     const int64_t ta = tile * 16 + g, tb = ta + 8;
     if (c < G) {
-      if (ta < L) out[ta] = est_from(cur.na, s1a, s2a, kq);
-      if (tb < L) out[tb] = est_from(cur.nb, s1b, s2b, kq);
+      if (ta < L) out[ta] = est_from(cur.na, s1[0][0], s2[0][0], kq);
+      if (tb < L) out[tb] = est_from(cur.nb, s1[0][1], s2[0][1], kq);
     }
     cur = nxt;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Logits with bulk-copy staging: the CTA's whole chunk of key records and
-// norms (up to kStageTiles x kMaxStages tiles) is requested at once with
-// cp.async.bulk into shared memory, one mbarrier per stage of kStageTiles
-// tiles, and the warps score each stage as it lands.  Requires capacity to be
-// a multiple of 16 (every copied tile lies inside its sequence's rows).
+// Logits with bulk-copy staging (capacity a multiple of 16), launched as the
+// programmatic dependent of the query prep.  Grid (chunks, Hkv, B); each CTA
+//   * requests the first stage of its chunk's key records and norms
+//     (cp.async.bulk into a ring of kRing stages of kStageTiles tiles, one
+//     mbarrier per stage) before the sequence length or the query arrive;
+//   * waits for the prep grid and loads the query fragments while only that
+//     first stage is in flight (a whole chunk in flight would queue these
+//     small loads behind it), then requests the next stages;
+//   * scores its tiles as the stages land, refilling each ring slot once all
+//     warps are done with it.
+// Every wait is bounded; on a timeout the CTA records an error, waits
+// (bounded) for its copies in flight and returns.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr int kStageTiles = 8;
-constexpr int kMaxStages = 8;
+constexpr int kRing = 4;
 constexpr long long kWaitLimit = 1ll << 26;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -357,54 +393,65 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
 }  // namespace
 
 template <int NV, int P>
-__global__ void __launch_bounds__(128) k_logits_tma(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
-                                                    int64_t capacity, int64_t cache_rows,
-                                                    const int32_t* __restrict__ seq_lens,
-                                                    const uint8_t* __restrict__ prep, float* __restrict__ logits,
-                                                    int tiles_per_cta, int* __restrict__ status) {
-  extern __shared__ __align__(16) uint8_t sm[];
-  __shared__ __align__(8) uint64_t bars[kMaxStages];
+__global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
+                                                       int Hkv, int64_t capacity, int64_t cache_rows,
+                                                       const int32_t* __restrict__ seq_lens,
+                                                       const uint8_t* __restrict__ prep, float* __restrict__ logits,
+                                                       int tiles_per_cta, int* __restrict__ status) {
   constexpr int RB = 16 * P;                 // record bytes at d = 128
+  constexpr int kStageRec = kStageTiles * 16 * RB, kStageNrm = kStageTiles * 16 * 4;
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ __align__(8) uint64_t bars[kRing];
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int G = Hq / Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t L = seq_lens[b];
-  const int64_t ntiles = (L + 15) / 16;
-  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
-  const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
-  if (tile0 >= tend) return;
-  const int nt = (int)(tend - tile0);
-  const int nstages = (nt + kStageTiles - 1) / kStageTiles;
   uint8_t* srec = sm;
-  uint8_t* snrm = sm + (size_t)tiles_per_cta * 16 * RB;
+  uint8_t* snrm = sm + (size_t)kRing * kStageRec;
+  // ---- chunk bounds; the first stage is requested before the length arrives
+  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
+  if (tile0 >= tcap) return;
+  const int nt_cap = (int)(tcap - tile0);
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
   const uint8_t* grec = kcache + (rowbase + tile0 * 16) * RB;
   const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows) + (rowbase + tile0 * 16) * 4;
+  // stage st (tiles st*kStageTiles ..) into ring slot st % kRing
+  auto request = [&](int st, int t_n) {
+    const int slot = st % kRing;
+    const int t_a = st * kStageTiles;
+    const uint32_t rb = (uint32_t)(t_n * 16 * RB), nb = (uint32_t)(t_n * 16 * 4);
+    const uint32_t bar = su32(&bars[slot]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(rb + nb) : "memory");
+    bulk_g2s(su32(srec + (size_t)slot * kStageRec), grec + (size_t)t_a * 16 * RB, rb, bar);
+    bulk_g2s(su32(snrm + (size_t)slot * kStageNrm), gnrm + (size_t)t_a * 16 * 4, nb, bar);
+  };
   if (tid == 0) {
-    for (int st = 0; st < nstages; ++st)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[st])));
+    for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (int st = 0; st < nstages; ++st) {
-      const int t_a = st * kStageTiles, t_n = min(kStageTiles, nt - t_a);
-      const uint32_t rb = (uint32_t)(t_n * 16 * RB), nb = (uint32_t)(t_n * 16 * 4);
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(&bars[st])), "r"(rb + nb)
-                   : "memory");
-      bulk_g2s(su32(srec + (size_t)t_a * 16 * RB), grec + (size_t)t_a * 16 * RB, rb, su32(&bars[st]));
-      bulk_g2s(su32(snrm + (size_t)t_a * 16 * 4), gnrm + (size_t)t_a * 16 * 4, nb, su32(&bars[st]));
-    }
+    request(0, min(kStageTiles, nt_cap));
   }
+  const int64_t L = seq_lens[b];
+  const int64_t tend = min(tcap, (L + 15) / 16);
+  const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
+  const int nst = (nt + kStageTiles - 1) / kStageTiles;
   // query fragments come from the preceding prep grid (launched as its
-  // programmatic dependent): wait for it only now, after the copies are in flight
+  // programmatic dependent): wait for it only now
   asm volatile("griddepcontrol.wait;" ::: "memory");
   QK16<NV, P> qk;
-  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NV, 128), lane);
-  __syncthreads();
+  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, cb);
+  __syncthreads();                           // the barriers are initialised; the fragments are in
+  if (tid == 0)
+    for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
+  int issued = max(1, min(nst, kRing));      // stages requested so far
+  // ---- scoring
   const float kq = cb.qjl_const;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
   bool ok = true;
-  auto tile_words = [&](int lt, uint32_t(&wa)[P], uint32_t(&wb)[P], uint32_t& na, uint32_t& nb) {
-    const uint8_t* ra = srec + ((size_t)lt * 16 + g) * RB + c * P * 4;
+  int pending_from = 0;                      // first stage whose copy may still be in flight
+  auto tile_words = [&](const uint8_t* rec, const uint8_t* nrm, int lt, int64_t tg, uint32_t(&wa)[P],
+                        uint32_t(&wb)[P], uint32_t& na, uint32_t& nb) {
+    const uint8_t* ra = rec + ((size_t)lt * 16 + g) * RB + c * P * 4;
     const uint8_t* rbp = ra + 8 * RB;
     if constexpr (P == 4) {
       const uint4 x = *reinterpret_cast<const uint4*>(ra);
@@ -418,9 +465,9 @@ __global__ void __launch_bounds__(128) k_logits_tma(const Dev cb, const uint8_t*
         wb[p] = reinterpret_cast<const uint32_t*>(rbp)[p];
       }
     }
-    na = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g];
-    nb = reinterpret_cast<const uint32_t*>(snrm)[lt * 16 + g + 8];
-    const int64_t ta = (tile0 + lt) * 16 + g;
+    na = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g];
+    nb = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g + 8];
+    const int64_t ta = tg * 16 + g;
     if (ta >= L) {
 #pragma unroll
       for (int p = 0; p < P; ++p) wa[p] = 0;
@@ -430,45 +477,58 @@ __global__ void __launch_bounds__(128) k_logits_tma(const Dev cb, const uint8_t*
       for (int p = 0; p < P; ++p) wb[p] = 0;
     }
   };
-  auto emit = [&](int lt, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
-    const int64_t ta = (tile0 + lt) * 16 + g, tb = ta + 8;
+  auto emit = [&](int64_t tg, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
+    const int64_t ta = tg * 16 + g, tb = ta + 8;
     if (c < G) {
       if (ta < L) out[ta] = est_from(na, s1a, s2a, kq);
       if (tb < L) out[tb] = est_from(nb, s1b, s2b, kq);
     }
   };
-  for (int st = 0; st < nstages && ok; ++st) {
-    if (!bar_wait(su32(&bars[st]), 0)) {
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kRing;
+    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1)))) {
       ok = false;
+      pending_from = st;
       break;
     }
-    const int t_a = st * kStageTiles, t_e = min(t_a + kStageTiles, nt);
-    // two tiles per iteration (warp, warp + 4) for independent MMA chains
-    for (int lt = t_a + warp; lt < t_e; lt += 8) {
+    const uint8_t* rec = srec + (size_t)slot * kStageRec;
+    const uint8_t* nrm = snrm + (size_t)slot * kStageNrm;
+    const int t_a = st * kStageTiles, n_here = min(kStageTiles, nt - t_a);
+    // two tiles per iteration (warp, warp + 4) for independent MMA chains;
+    // a lone last tile is scored on its own
+    for (int lt = warp; lt < n_here; lt += 8) {
       const int lt2 = lt + 4;
-      uint32_t wa[P], wb[P], xa[P], xb[P], na, nb, ma = 0, mb = 0;
-      tile_words(lt, wa, wb, na, nb);
-      const bool two = lt2 < t_e;
-      if (two) {
-        tile_words(lt2, xa, xb, ma, mb);
+      if (lt2 < n_here) {
+        uint32_t wa[2][P], wb[2][P], na, nb, ma, mb;
+        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb);
+        tile_words(rec, nrm, lt2, tile0 + t_a + lt2, wa[1], wb[1], ma, mb);
+        float s1[2][2], s2[2][2];
+        qk.template score<2>(wa, wb, s1, s2);
+        emit(tile0 + t_a + lt, na, nb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
+        emit(tile0 + t_a + lt2, ma, mb, s1[1][0], s1[1][1], s2[1][0], s2[1][1]);
       } else {
-#pragma unroll
-        for (int p = 0; p < P; ++p) xa[p] = xb[p] = 0;
+        uint32_t wa[1][P], wb[1][P], na, nb;
+        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb);
+        float s1[1][2], s2[1][2];
+        qk.template score<1>(wa, wb, s1, s2);
+        emit(tile0 + t_a + lt, na, nb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
       }
-      float s1a, s1b, s2a, s2b, u1a, u1b, u2a, u2b;
-      qk.score2(wa, wb, xa, xb, s1a, s1b, s2a, s2b, u1a, u1b, u2a, u2b);
-      emit(lt, na, nb, s1a, s1b, s2a, s2b);
-      if (two) emit(lt2, ma, mb, u1a, u1b, u2a, u2b);
+    }
+    // every warp is done with this ring slot: refill it with stage st + kRing
+    if (st + kRing < nst) {
+      __syncthreads();
+      if (tid == 0) request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
+      issued = st + kRing + 1;
     }
   }
   if (!ok) {
     if (tid == 0) atomicExch(status, 2);
-    // let the remaining copies land (bounded) before the CTA's shared memory is released
-    for (int st = 0; st < nstages; ++st) bar_wait(su32(&bars[st]), 0);
+    // let the copies still in flight land (bounded) before the shared memory is released
+    for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
+  } else if (nst == 0) {
+    bar_wait(su32(&bars[0]), 0);             // the speculative first stage
   }
 }
-
-int logits_tma_max_tiles() { return kStageTiles * kMaxStages; }
 
 // ---------------------------------------------------------------------------
 // Fused decode attention: QK as above, online softmax per head slot, and the
@@ -524,7 +584,7 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
 
   if (tile0 + warp < tend) {
     QK16<NVK, PK> qk;
-    qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(NVK, 128), lane);
+    qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, kcb);
     float vcn[NVV];
 #pragma unroll
     for (int u = 0; u < NVV; ++u) vcn[u] = -2.f * vcb.vcoef[u];
@@ -551,11 +611,17 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
         vnxt.load(vrec, vnrm, VW, rowbase, tn * 16, L, g, c);
       }
       const int64_t ta = tile * 16 + g, tb = ta + 8;
-      float s1a, s1b, s2a, s2b;
-      qk.score(kcur.wa, kcur.wb, s1a, s1b, s2a, s2b);
+      uint32_t wa[1][PK], wb[1][PK];
+#pragma unroll
+      for (int p = 0; p < PK; ++p) {
+        wa[0][p] = kcur.wa[p];
+        wb[0][p] = kcur.wb[p];
+      }
+      float s1[1][2], s2[1][2];
+      qk.template score<1>(wa, wb, s1, s2);
       // scores in log2 units
-      const float sa = ta < L ? est_from(kcur.na, s1a, s2a, kq) * scale_log2 : -INFINITY;
-      const float sb = tb < L ? est_from(kcur.nb, s1b, s2b, kq) * scale_log2 : -INFINITY;
+      const float sa = ta < L ? est_from(kcur.na, s1[0][0], s2[0][0], kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L ? est_from(kcur.nb, s1[0][1], s2[0][1], kq) * scale_log2 : -INFINITY;
       float mx = fmaxf(sa, sb);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
@@ -601,8 +667,8 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
           x[j] = r;
         }
         uint32_t r01[16], r89[16];
-        expand16(__byte_perm(x[0], x[1], vsel), r01);
-        expand16(__byte_perm(x[2], x[3], vsel), r89);
+        expand16_v(__byte_perm(x[0], x[1], vsel), r01);
+        expand16_v(__byte_perm(x[2], x[3], vsel), r89);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
           mma_f16(acc[mt], r01[2 * mt], r01[2 * mt + 1], r89[2 * mt], r89[2 * mt + 1], b0, b1);
@@ -612,7 +678,7 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
     }
   }
   // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
-  // acc = C0 * wsum + 2^(24 - pos) * D with pos = 6 + (beta mod 4)
+  // acc = C0 * wsum + value_factor(beta) * D
   float c0 = 0.f;
 #pragma unroll
   for (int u = 0; u < NVV; ++u) c0 += vcb.vcoef[u];
@@ -626,7 +692,7 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const int b0 = 2 * mt, b1 = 2 * mt + 1;
-    const float f0 = (float)(1 << (18 - (b0 & 3))), f1 = (float)(1 << (18 - (b1 & 3)));
+    const float f0 = value_factor(b0), f1 = value_factor(b1);
     ph[2 + 16 * g + b0] = fmaf(f0, acc[mt][0] + acc[mt][1], c0 * wsum);
     ph[2 + 16 * g + b1] = fmaf(f1, acc[mt][2] + acc[mt][3], c0 * wsum);
   }
@@ -675,9 +741,28 @@ static void attn_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& 
   }
 }
 
+// The query prep, the scoring kernels and the cache append share SMs while
+// their grids overlap; an SM only hosts CTAs of kernels with the same
+// shared-memory carveout, so all of them ask for the largest one.
+cudaError_t prefer_max_shared(const void* fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s) {
-  k_prep<<<dim3(Hkv * 4, B), 512, 0, s>>>(cb, q, Hq, Hkv, prep);
-  return cudaGetLastError();
+  static cudaError_t configured = prefer_max_shared(reinterpret_cast<const void*>(k_prep));
+  if (configured != cudaSuccess) return configured;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Hkv * 16, B);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_prep, cb, q, Hq, Hkv, prep);
 }
 
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
@@ -693,17 +778,16 @@ cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int H
 }
 
 template <int NV, int P>
-static cudaError_t logits_tma_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity, int64_t rows,
-                                const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks, int tpc,
-                                int* status, cudaStream_t s) {
-  const size_t smem = (size_t)tpc * 16 * (16 * P + 4);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_tma<NV, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((size_t)logits_tma_max_tiles() * 16 * (16 * 4 + 4)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
+                                   int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
+                                   int nchunks, int tpc, int* status, cudaStream_t s) {
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + 4);
+  static cudaError_t configured = [] {
+    cudaError_t e = cudaFuncSetAttribute(k_logits_staged<NV, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_logits_staged<NV, P>));
+    return e;
+  }();
+  if (configured != cudaSuccess) return configured;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nchunks, Hkv, B);
   cfg.blockDim = dim3(128);
@@ -714,17 +798,17 @@ static cudaError_t logits_tma_t(const Dev& cb, const uint8_t* kc, int B, int Hq,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_logits_tma<NV, P>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc,
+  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc,
                             status);
 }
 
-cudaError_t launch_logits_tma(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity, int64_t rows,
-                              const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks, int tpc,
-                              int* status, cudaStream_t s) {
+cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
+                                 int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
+                                 int nchunks, int tpc, int* status, cudaStream_t s) {
   switch (cb.b1) {
-    case 1: return logits_tma_t<1, 2>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
-    case 2: return logits_tma_t<2, 3>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
-    default: return logits_tma_t<4, 4>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+    case 1: return logits_staged_t<1, 2>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+    case 2: return logits_staged_t<2, 3>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+    default: return logits_staged_t<4, 4>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
   }
 }
 

@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(512) k_prep_polar(const Dev cb, const float* _
     if (lane == 0) red[warp] = v;
   }
   __syncthreads();
-  const float S1 = pow2_scale(red[0], 16384.f), S2 = pow2_scale(red[1] * 262144.f, 16384.f);
-  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(1, d);
+  const float S1 = pow2_scale(red[0], 16384.f), S2 = pow2_scale(red[1] * kMaxBitFactor, 16384.f);
+  uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(d);
   float* hdr = reinterpret_cast<float*>(blk);
   if (tid == 0) {
     hdr[slot] = live ? S1 : 0.f;
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(512) k_prep_polar(const Dev cb, const float* _
       for (int t = 0; t < 4; ++t) {
         const int beta = 2 * kb + (t >> 1);
         const int k = 32 * c + beta + 16 * (t & 1);
-        const float x = v == 0 ? sq1[k] / S1 : 2.f * sq2[k] * (float)(1 << (18 - (beta & 3))) / S2;
+        const float x = v == 0 ? sq1[k] / S1 : 2.f * sq2[k] * bit_factor(beta) / S2;
         vals[t] = piece16(x, pc);
       }
     }
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
   if (tile0 + warp >= tend) return;
-  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(1, 128);
+  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
   const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
   uint2 bq[2][8];
 #pragma unroll
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
   if (tile0 + warp < tend) {
-    const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(1, 128);
+    const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
     const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
     uint2 bq[2][8];
 #pragma unroll

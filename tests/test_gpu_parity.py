@@ -159,6 +159,43 @@ def test_logits_parity(bits, B, Hq, Hkv, cap, lens, mode):
             rowwise_ok(got[b, :, :L], ref[b, :, :L])
 
 
+def tiled_code(code, reps):
+    """The oracle's code arrays repeated ``reps`` times along the rows."""
+    n = code["n"].shape[0]
+    return {k: (np.tile(v, (reps,) + (1,) * (v.ndim - 1)) if isinstance(v, np.ndarray) and v.shape[:1] == (n,) else v)
+            for k, v in code.items()}
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_logits_long_context_every_position(bits):
+    """Context 131072 for 2 sequences x 2 kv heads: chunks of more tiles than
+    the staging ring holds, so stages are refilled.  The cache repeats 4096
+    oracle-coded keys, so every one of the 2 x 8 x 131072 outputs has an
+    oracle value (that of its source key)."""
+    B, Hq, Hkv, cap, lens = 2, 8, 2, 131072, [131072, 100003]
+    ocb, gcb = pair(128, bits)
+    x = wl.gaussian_outlier_keys(4096, 128)
+    code = quant.quantize(ocb, x.astype(np.float64))
+    reps = B * Hkv * cap // 4096
+    img = layout.write_cache(ocb, B * Hkv * cap, tiled_code(code, reps))
+    q = wl.queries((B, Hq, 128), name="tiny_q")
+    G = Hq // Hkv
+    ref = np.stack([estimate.estimate(ocb, q[b].astype(np.float64), code) for b in range(B)])   # [B, Hq, 4096]
+    ws = torch.empty(tq.tq_logits_workspace(gcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    tq.tq_logits(gcb, torch.from_numpy(img).cuda(), B, Hq, Hkv, cap, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                 torch.from_numpy(q).cuda(), out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        L = lens[b]
+        assert np.all(np.isnan(got[b, :, L:]))
+        for h in range(Hq):
+            # rows of (b, kv head h // G) start at a multiple of 4096: position t holds key t mod 4096
+            want = np.tile(ref[b, h], cap // 4096)[:L]
+            rowwise_ok(got[b, h, :L][None], want[None])
+
+
 @pytest.mark.parametrize("kb,vb,mode", [(3, 3, "scalar"), (4, 3, "scalar"), (2, 2, "scalar"), (3, 4, "scalar"),
                                         (3, 1, "scalar"), (3, 3, "polar"), (4, 2, "polar"), (2, 4, "polar")])
 @pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 300, [300, 1, 0]),
