@@ -87,7 +87,12 @@ bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t c
 
 constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
 constexpr int kLogitsCtas = 148 * 4;   // resident CTAs of the logits kernel
-constexpr int kAttnCtas = 148 * 2;     // resident CTAs of the attention kernel
+// Resident CTAs of the attention kernel (one wave): 4 per SM, 3 for 4-bit
+// keys (more registers), 2 in polar mode.
+int attn_ctas(const tq_codebook* kcb) {
+  if (kcb->dev.mode == TQ_MODE_POLAR) return 148 * 2;
+  return kcb->dev.b1 == 3 ? 148 * 3 : 148 * 4;
+}
 
 template <class T>
 tq_status upload(tq_codebook* cb, const std::vector<T>& h, const T** out) {
@@ -525,7 +530,7 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
   if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, kAttnCtas, &nchunks, &tpc);
+  chunking(B, Hkv, capacity, attn_ctas(kcb), &nchunks, &tpc);
   const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d));
   const int64_t parts = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d) * 4;
   (void)Hq;
@@ -554,7 +559,7 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   if (kcb->dev.mode != vcb->dev.mode)
     return fail(TQ_EUNSUPPORTED, "tq_decode_attention: keys and values must use the same stage-1 mode");
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, kAttnCtas, &nchunks, &tpc);
+  chunking(B, Hkv, capacity, attn_ctas(kcb), &nchunks, &tpc);
   const int64_t rows = (int64_t)B * Hkv * capacity;
   const float sl2 = scale * 1.4426950408889634f;
   if (kcb->dev.mode == TQ_MODE_POLAR) {
@@ -570,11 +575,17 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   }
   if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
     return st;
-  if ((st = launched("tq_decode_attention",
-                     tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                     static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens, prep,
-                                     sl2, parts, nchunks, tpc, s))) != TQ_OK)
-    return st;
+  if (capacity % 16 == 0)
+    st = launched("tq_decode_attention",
+                  tq::launch_attn_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                         static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens,
+                                         prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
+  else
+    st = launched("tq_decode_attention",
+                  tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                  static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens, prep,
+                                  sl2, parts, nchunks, tpc, s));
+  if (st != TQ_OK) return st;
   return launched("tq_decode_attention/merge",
                   tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
 }

@@ -698,6 +698,218 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode attention with bulk-copy staging (capacity a multiple of 16),
+// launched as the programmatic dependent of the query prep.  Same arithmetic
+// as k_attn; the key and value records and norms of each stage of
+// kStageTiles tiles arrive by cp.async.bulk in a ring of kRing slots (the
+// first stage is requested before the query fragments), and each warp scores
+// tiles warp and warp + 4 of every stage.
+// ---------------------------------------------------------------------------
+template <int NVK, int PK, int NVV, int PV>
+__global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev kcb, const Dev vcb,
+                                                     const uint8_t* __restrict__ kcache,
+                                                     const uint8_t* __restrict__ vcache, int Hq, int Hkv,
+                                                     int64_t capacity, int64_t cache_rows,
+                                                     const int32_t* __restrict__ seq_lens,
+                                                     const uint8_t* __restrict__ prep, float scale_log2,
+                                                     float* __restrict__ partials, int tiles_per_cta,
+                                                     int* __restrict__ status) {
+  constexpr int RBK = 16 * PK, RBV = 16 * PV;    // record bytes at d = 128
+  constexpr int kSK = kStageTiles * 16 * RBK, kSKN = kStageTiles * 16 * 4;
+  constexpr int kSV = kStageTiles * 16 * RBV, kSVN = kStageTiles * 16 * 2;
+  constexpr int kSlot = kSK + kSKN + kSV + kSVN;
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ __align__(8) uint64_t bars[kRing];
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
+  const int nt_cap = tcap > tile0 ? (int)(tcap - tile0) : 0;
+  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
+  const int64_t r0 = rowbase + tile0 * 16;
+  const uint8_t* gk = kcache + r0 * RBK;
+  const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows) + r0 * 4;
+  const uint8_t* gv = vcache + r0 * RBV;
+  const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows) + r0 * 2;
+  auto request = [&](int st, int t_n) {
+    const int slot = st % kRing;
+    const size_t t_a = (size_t)st * kStageTiles * 16;    // first row of the stage
+    const uint32_t nk = (uint32_t)(t_n * 16 * RBK), nkn = (uint32_t)(t_n * 16 * 4);
+    const uint32_t nv = (uint32_t)(t_n * 16 * RBV), nvn = (uint32_t)(t_n * 16 * 2);
+    const uint32_t bar = su32(&bars[slot]);
+    uint8_t* base = sm + (size_t)slot * kSlot;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(nk + nkn + nv + nvn)
+                 : "memory");
+    bulk_g2s(su32(base), gk + t_a * RBK, nk, bar);
+    bulk_g2s(su32(base + kSK), gkn + t_a * 4, nkn, bar);
+    bulk_g2s(su32(base + kSK + kSKN), gv + t_a * RBV, nv, bar);
+    bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + t_a * 2, nvn, bar);
+  };
+  if (tid == 0) {
+    for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (nt_cap > 0) request(0, min(kStageTiles, nt_cap));
+  }
+  const int64_t L = seq_lens[b];
+  const int64_t tend = min(tcap, (L + 15) / 16);
+  const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
+  const int nst = (nt + kStageTiles - 1) / kStageTiles;
+  // query fragments come from the preceding prep grid: wait for it only now
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  QK16<NVK, PK> qk;
+  qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, kcb);
+  __syncthreads();
+  if (tid == 0)
+    for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
+  int issued = nt_cap > 0 ? max(1, min(nst, kRing)) : 0;
+
+  float m_run = -INFINITY, l_run = 0.f, wsum = 0.f;
+  float acc[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  float vcn[NVV];
+#pragma unroll
+  for (int u = 0; u < NVV; ++u) vcn[u] = -2.f * vcb.vcoef[u];
+  const float kq = kcb.qjl_const;
+  const uint32_t vsel = (g & 1) ? 0x7632u : 0x5410u;
+  const int hh = g >> 1, pc = g & 1;    // B-fragment column: head slot, piece
+  const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
+  const int vword = g >> 1;
+  bool ok = true;
+  int pending_from = 0;
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kRing;
+    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1)))) {
+      ok = false;
+      pending_from = st;
+      break;
+    }
+    const uint8_t* base = sm + (size_t)slot * kSlot;
+    const uint8_t* sk = base;
+    const uint32_t* skn = reinterpret_cast<const uint32_t*>(base + kSK);
+    const uint8_t* sv = base + kSK + kSKN;
+    const __half* svn = reinterpret_cast<const __half*>(base + kSK + kSKN + kSV);
+    const int t_a = st * kStageTiles, n_here = min(kStageTiles, nt - t_a);
+    for (int lt = warp; lt < n_here; lt += 4) {
+      const int64_t t0 = (tile0 + t_a + lt) * 16;       // first token of the tile
+      const int64_t ta = t0 + g, tb = ta + 8;
+      // keys g and g+8: column c words
+      uint32_t wa[1][PK], wb[1][PK];
+      {
+        const uint32_t* ka = reinterpret_cast<const uint32_t*>(sk + ((size_t)lt * 16 + g) * RBK) + c * PK;
+        const uint32_t* kb2 = reinterpret_cast<const uint32_t*>(sk + ((size_t)lt * 16 + g + 8) * RBK) + c * PK;
+#pragma unroll
+        for (int p = 0; p < PK; ++p) {
+          wa[0][p] = ka[p];
+          wb[0][p] = kb2[p];
+        }
+      }
+      float s1[1][2], s2[1][2];
+      qk.template score<1>(wa, wb, s1, s2);
+      // scores in log2 units
+      const float sa = ta < L ? est_from(skn[lt * 16 + g], s1[0][0], s2[0][0], kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L ? est_from(skn[lt * 16 + g + 8], s1[0][1], s2[0][1], kq) * scale_log2 : -INFINITY;
+      float mx = fmaxf(sa, sb);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (__any_sync(kFull, mx > m_run)) {
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+        l_run *= alpha;
+        wsum *= alpha;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        m_run = m_new;
+      }
+      const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
+      const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_run);
+      const float vn0 = ta < L ? __half2float(svn[lt * 16 + g]) : 0.f;
+      const float vn1 = tb < L ? __half2float(svn[lt * 16 + g + 8]) : 0.f;
+      const float wA = pa * vn0, wB = pb * vn1;
+      float ps = pa + pb, ws = wA + wB;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        ps += __shfl_xor_sync(kFull, ps, o);
+        ws += __shfl_xor_sync(kFull, ws, o);
+      }
+      l_run += ps;
+      wsum += ws;
+      // weights of tokens 2c, 2c+1, 2c+8, 2c+9 for head slot hh, in B-fragment order
+      const float w0 = __shfl_sync(kFull, wA, src0);
+      const float w1 = __shfl_sync(kFull, wA, src1);
+      const float w8 = __shfl_sync(kFull, wB, src0);
+      const float w9 = __shfl_sync(kFull, wB, src1);
+      // value words (word column g/2) of tokens 2c, 2c+1, 2c+8, 2c+9
+      uint32_t vw[4][PV];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tok = 2 * c + (j & 1) + 8 * (j >> 1);
+        const uint32_t* vp = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV) + vword * PV;
+#pragma unroll
+        for (int p = 0; p < PV; ++p) vw[j][p] = vp[p];
+      }
+#pragma unroll
+      for (int u = 0; u < NVV; ++u) {
+        const float cu = vcn[u];
+        const uint32_t b0 = pack_half2(piece16(cu * w0, pc), piece16(cu * w1, pc));
+        const uint32_t b1 = pack_half2(piece16(cu * w8, pc), piece16(cu * w9, pc));
+        uint32_t x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r = 0;
+#pragma unroll
+          for (int p = 0; p < PV; ++p)
+            if (kOddMask[u] >> p & 1u) r ^= vw[j][p];
+          x[j] = r;
+        }
+        uint32_t r01[16], r89[16];
+        expand16_v(__byte_perm(x[0], x[1], vsel), r01);
+        expand16_v(__byte_perm(x[2], x[3], vsel), r89);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+          mma_f16(acc[mt], r01[2 * mt], r01[2 * mt + 1], r89[2 * mt], r89[2 * mt + 1], b0, b1);
+      }
+    }
+    // every warp is done with this ring slot: refill it with stage st + kRing
+    if (st + kRing < nst) {
+      __syncthreads();
+      if (tid == 0) request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
+      issued = st + kRing + 1;
+    }
+  }
+  if (!ok) {
+    if (tid == 0) atomicExch(status, 2);
+    for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
+  } else if (nst == 0 && issued) {
+    bar_wait(su32(&bars[0]), 0);             // the speculative first stage
+  }
+  // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
+  // acc = C0 * wsum + value_factor(beta) * D
+  float c0 = 0.f;
+#pragma unroll
+  for (int u = 0; u < NVV; ++u) c0 += vcb.vcoef[u];
+  const int nchunks = gridDim.x;
+  float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
+  float* ph = part + c * (2 + 128);
+  if (g == 0) {
+    ph[0] = m_run;
+    ph[1] = l_run;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int b0 = 2 * mt, b1 = 2 * mt + 1;
+    const float f0 = value_factor(b0), f1 = value_factor(b1);
+    ph[2 + 16 * g + b0] = fmaf(f0, acc[mt][0] + acc[mt][1], c0 * wsum);
+    ph[2 + 16 * g + b1] = fmaf(f1, acc[mt][2] + acc[mt][3], c0 * wsum);
+  }
+}
+
 // Merge the split partials of one (b, query head) and rotate back once:
 // M = max m_p, o_rot = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,
 // out = Pi_v^T o_rot.
@@ -809,6 +1021,55 @@ cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq
     case 1: return logits_staged_t<1, 2>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
     case 2: return logits_staged_t<2, 3>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
     default: return logits_staged_t<4, 4>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
+  }
+}
+
+template <int NVK, int PK, int NVV, int PV>
+static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
+                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const int32_t* sl,
+                                 const uint8_t* prep, float sl2, float* parts, int tpc, int* status) {
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 + 16 * PV + 2);
+  static cudaError_t configured = [] {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_staged<NVK, PK, NVV, PV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_attn_staged<NVK, PK, NVV, PV>));
+    return e;
+  }();
+  if (configured != cudaSuccess) return configured;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn_staged<NVK, PK, NVV, PV>, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2,
+                            parts, tpc, status);
+}
+
+template <int NVK, int PK>
+static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
+                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const int32_t* sl,
+                                 const uint8_t* prep, float sl2, float* parts, int tpc, int* status) {
+  switch (b1v) {
+    case 1: return attn_staged_t<NVK, PK, 1, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    case 2: return attn_staged_t<NVK, PK, 2, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    case 3: return attn_staged_t<NVK, PK, 4, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    default: return attn_staged_t<NVK, PK, 8, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+  }
+}
+
+cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq,
+                               int Hkv, int64_t capacity, int64_t rows, const int32_t* seq_lens, const uint8_t* prep,
+                               float scale_log2, float* parts, int nchunks, int tpc, int* status, cudaStream_t s) {
+  const dim3 grid(nchunks, Hkv, B);
+  switch (kcb.b1) {
+    case 1: return attn_staged_v<1, 2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
+    case 2: return attn_staged_v<2, 3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
+    default: return attn_staged_v<4, 4>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
   }
 }
 

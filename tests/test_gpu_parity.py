@@ -225,6 +225,35 @@ def test_attention_parity(kb, vb, mode, B, Hq, Hkv, cap, lens):
             rowwise_ok(got[b], ref[b])
 
 
+def test_attention_long_context_ring_refill():
+    """2 sequences x 8 kv heads at context 16384: chunks of more tiles than
+    the staging ring holds.  Keys and values repeat 4096 oracle-coded rows;
+    the oracle attends over the repeated codes in full."""
+    B, Hq, Hkv, cap, lens = 2, 32, 8, 16384, [16384, 12001]
+    okc, gkc = pair(128, 3, "prod")
+    ovc, gvc = pair(128, 3, "mse", seed_pi=1)
+    K = wl.llama_kv_slice(0, 0, 0, 4096, which="keys")
+    V = wl.llama_kv_slice(0, 0, 0, 4096, which="values")
+    reps = B * Hkv * cap // 4096
+    kcode = tiled_code(quant.quantize(okc, K.astype(np.float64)), reps)
+    vcode = tiled_code(quant.quantize(ovc, V.astype(np.float64)), reps)
+    rows = B * Hkv * cap
+    kimg = layout.write_cache(okc, rows, kcode)
+    vimg = layout.write_cache(ovc, rows, vcode)
+    q = wl.queries((B, Hq, 128))
+    scale = 1.0 / math.sqrt(128)
+    ref = estimate.attention(okc, ovc, kcode, vcode, q.astype(np.float64), lens, Hkv, cap, scale)
+    ws = torch.empty(tq.tq_decode_attention_workspace(gkc, B, Hq, Hkv, cap), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    tq.tq_decode_attention(gkc, gvc, torch.from_numpy(kimg).cuda(), torch.from_numpy(vimg).cuda(), B, Hq, Hkv, cap,
+                           torch.tensor(lens, dtype=torch.int32, device="cuda"), torch.from_numpy(q).cuda(), scale,
+                           out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        rowwise_ok(got[b], ref[b])
+
+
 def test_invalid_arguments_return_status_without_launch():
     _, gcb = pair(128, 3)
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
