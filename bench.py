@@ -359,7 +359,7 @@ def run_attention(args, dist, rank, steps, mode="scalar"):
     from decode_attention_21_b300 import tq
     from decode_attention_21_b300 import workloads as wl
     c = ATTN
-    B, Hq, Hkv, d, T = c["B"], c["Hq"], c["Hkv"], c["d"], c["T"]
+    B, Hq, Hkv, d, T = args.attn_batch, c["Hq"], c["Hkv"], c["d"], c["T"]
     rows = B * Hkv * T
     md = tq.MODE_POLAR if mode == "polar" else tq.MODE_SCALAR
     kcb = tq.Codebook(d, c["kbits"], tq.KIND_PROD, md)
@@ -404,7 +404,7 @@ def run_attention(args, dist, rank, steps, mode="scalar"):
                        max(steps, 5))
     pk = peaks()
     achieved = packed / (k_ms / 1e3) / 1e9
-    return {"workload": f"fused decode attention ({mode} stage 1): batch 8, 32/8 heads, d 128, context 131072, "
+    return {"workload": f"fused decode attention ({mode} stage 1): batch {B}, 32/8 heads, d 128, context 131072, "
                         "keys 3-bit, values 3-bit",
             "keys_per_s": steps * rows * args.world / (ms / 1e3), "ms_per_step": ms / steps,
             "packed_bytes_per_step": packed,
@@ -522,6 +522,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="all", choices=["all", "logits", "attention", "quantize", "search"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--attn-batch", type=int, default=ATTN["B"],
+                    help="sequences in the attention workload (smaller batches for profiling)")
+    ap.add_argument("--attn-modes", default="scalar,polar", help="comma list of stage-1 modes for attention")
     args = ap.parse_args()
     world, rank, local = dist_env()
     args.world = world
@@ -539,8 +542,9 @@ def main():
     secondary = {}
     sec_steps = max(3, args.steps // 5)
     if args.workload in ("all", "attention"):
-        secondary["attention"] = run_attention(args, dist, rank, sec_steps)
-        secondary["attention_polar"] = run_attention(args, dist, rank, sec_steps, mode="polar")
+        for mode in args.attn_modes.split(","):
+            key = "attention" if mode == "scalar" else "attention_" + mode
+            secondary[key] = run_attention(args, dist, rank, sec_steps, mode=mode)
     if args.workload in ("all", "quantize"):
         secondary["quantize"] = run_quantize(args, dist, rank, sec_steps)
     if args.workload in ("all", "search"):

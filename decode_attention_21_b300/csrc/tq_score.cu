@@ -912,28 +912,54 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
 
 // Merge the split partials of one (b, query head) and rotate back once:
 // M = max m_p, o_rot = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,
-// out = Pi_v^T o_rot.
+// out = Pi_v^T o_rot.  The maximum, the weights and L are computed by the
+// whole CTA (parts strided over threads); thread i then sums coordinate i.
+constexpr int kMergeMaxParts = 4096;
 __global__ void __launch_bounds__(128) k_attn_merge(const Dev vcb, const float* __restrict__ partials, int Hq, int Hkv,
                                                     int nparts, float* __restrict__ out) {
   const int h = blockIdx.x, b = blockIdx.y;
   const int G = Hq / Hkv, kvh = h / G, slot = h % G;
   constexpr int d = 128;
-  __shared__ float so[d];
-  const float* base = partials + ((size_t)b * Hkv + kvh) * nparts * partial_floats(d) + slot * (2 + d);
-  const int i = threadIdx.x;
-  float M = -INFINITY;
-  for (int p = 0; p < nparts; ++p) M = fmaxf(M, base[(size_t)p * partial_floats(d)]);
-  float Lsum = 0.f, a = 0.f;
-  if (M != -INFINITY) {
-    for (int p = 0; p < nparts; ++p) {
-      const float* ph = base + (size_t)p * partial_floats(d);
-      const float mp = ph[0];
-      if (mp == -INFINITY) continue;
-      const float w = exp2f(mp - M);
-      Lsum = fmaf(w, ph[1], Lsum);
-      a = fmaf(w, ph[2 + i], a);
-    }
+  constexpr int64_t PF = 4 * (2 + d);        // partial_floats(d)
+  __shared__ float so[d], red[4], wts[kMergeMaxParts];
+  const float* base = partials + ((size_t)b * Hkv + kvh) * nparts * PF + slot * (2 + d);
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const bool cache_w = nparts <= kMergeMaxParts;
+  float mloc = -INFINITY;
+  for (int p = i; p < nparts; p += 128) mloc = fmaxf(mloc, base[(size_t)p * PF]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
+  if (lane == 0) red[warp] = mloc;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float lloc = 0.f;
+  for (int p = i; p < nparts; p += 128) {
+    const float mp = base[(size_t)p * PF];
+    const float w = (M == -INFINITY || mp == -INFINITY) ? 0.f : exp2f(mp - M);
+    if (cache_w) wts[p] = w;
+    lloc = fmaf(w, base[(size_t)p * PF + 1], lloc);
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) lloc += __shfl_xor_sync(kFull, lloc, o);
+  if (lane == 0) red[warp] = lloc;
+  __syncthreads();
+  const float Lsum = (red[0] + red[1]) + (red[2] + red[3]);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int p = 0;
+  auto weight = [&](int q) {
+    if (cache_w) return wts[q];
+    const float mp = base[(size_t)q * PF];
+    return (M == -INFINITY || mp == -INFINITY) ? 0.f : exp2f(mp - M);
+  };
+  for (; p + 4 <= nparts; p += 4) {
+    a0 = fmaf(weight(p), base[(size_t)p * PF + 2 + i], a0);
+    a1 = fmaf(weight(p + 1), base[(size_t)(p + 1) * PF + 2 + i], a1);
+    a2 = fmaf(weight(p + 2), base[(size_t)(p + 2) * PF + 2 + i], a2);
+    a3 = fmaf(weight(p + 3), base[(size_t)(p + 3) * PF + 2 + i], a3);
+  }
+  for (; p < nparts; ++p) a0 = fmaf(weight(p), base[(size_t)p * PF + 2 + i], a0);
+  const float a = (a0 + a1) + (a2 + a3);
   so[i] = Lsum > 0.f ? a / Lsum : 0.f;
   __syncthreads();
   float o = 0.f;
