@@ -57,6 +57,9 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
                                                        const float* __restrict__ y_in,
                                                        const float* __restrict__ n_in,
                                                        const int64_t* __restrict__ dst_rows) {
+  // a programmatic dependent (the query prep) may start now: it reads none of
+  // the rows written here and waits for this grid before it completes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int K = D / 32;
   constexpr int LOGD = D == 128 ? 7 : 8;
   __shared__ float s_y[8][D];
@@ -301,6 +304,9 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
                                                         const void* __restrict__ x, int x_dtype, int64_t n, int d_in,
                                                         const float* __restrict__ y_in, const float* __restrict__ n_in,
                                                         const int64_t* __restrict__ dst_rows) {
+  // a programmatic dependent (the query prep) may start now: it reads none of
+  // the rows written here and waits for this grid before it completes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int NW = D / 32;
   __shared__ float xs[D];
   __shared__ float part[4][D];

@@ -132,6 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_pilo, const __grid_constant__ CUtensorMap tm_s, const Dev cb,
                   uint8_t* __restrict__ cache, int64_t cache_rows, int64_t n, const int64_t* __restrict__ dst_rows,
                   int* __restrict__ status) {
+  // a programmatic dependent (the query prep) may start now: it reads none of
+  // the rows written here and waits for this grid before it completes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);

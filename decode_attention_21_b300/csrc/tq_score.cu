@@ -78,8 +78,11 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   const int unit = blockIdx.x >> 2;               // kv head * 4 + slot
   const int kvh = unit >> 2, slot = unit & 3, b = blockIdx.y;
   const bool live = slot < G;
-  // The scoring kernel that follows may start now: it only reads the key
-  // cache (written before this kernel started) until it waits for this grid.
+  // This grid may run alongside the kernel before it (a cache append), since
+  // it reads only the queries and the codebook; it waits for that kernel at
+  // its end, so its completion implies the append's.  The scoring kernel
+  // that follows may start now: it touches no cache row before it waits for
+  // this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float sq[d], part[2][4][32], sv[2][32];
   __shared__ float red[4][4];   // [source rank][max |q'|, max |2 q''|, sum q', sum q'']
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
     }
     frag[(v * 8 + kb) * 32 + g * 4 + r] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -354,12 +358,12 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
 // ---------------------------------------------------------------------------
 // Logits with bulk-copy staging (capacity a multiple of 16), launched as the
 // programmatic dependent of the query prep.  Grid (chunks, Hkv, B); each CTA
+//   * sets up a ring of kRing stages of kStageTiles tiles (one mbarrier per
+//     stage) while the prep runs, then waits for the prep grid;
 //   * requests the first stage of its chunk's key records and norms
-//     (cp.async.bulk into a ring of kRing stages of kStageTiles tiles, one
-//     mbarrier per stage) before the sequence length or the query arrive;
-//   * waits for the prep grid and loads the query fragments while only that
-//     first stage is in flight (a whole chunk in flight would queue these
-//     small loads behind it), then requests the next stages;
+//     (cp.async.bulk), loads the query fragments while only that stage is in
+//     flight (a whole chunk in flight would queue these small loads behind
+//     it), then requests the next stages;
 //   * scores its tiles as the stages land, refilling each ring slot once all
 //     warps are done with it.
 // Every wait is bounded; on a timeout the CTA records an error, waits
@@ -408,11 +412,10 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   const int g = lane >> 2, c = lane & 3;
   uint8_t* srec = sm;
   uint8_t* snrm = sm + (size_t)kRing * kStageRec;
-  // ---- chunk bounds; the first stage is requested before the length arrives
+  // ---- chunk bounds
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
   if (tile0 >= tcap) return;
-  const int nt_cap = (int)(tcap - tile0);
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
   const uint8_t* grec = kcache + (rowbase + tile0 * 16) * RB;
   const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows) + (rowbase + tile0 * 16) * 4;
@@ -429,21 +432,24 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    request(0, min(kStageTiles, nt_cap));
   }
   const int64_t L = seq_lens[b];
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
-  // query fragments come from the preceding prep grid (launched as its
-  // programmatic dependent): wait for it only now
+  // The query fragments come from the preceding prep grid, launched as its
+  // programmatic dependent; the prep's completion also implies that of any
+  // cache append before it, so no cache row is read before this wait.  The
+  // first stage goes out right after it, the fragment loads queue behind
+  // only that stage, and the other stages follow.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
   QK16<NV, P> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, cb);
   __syncthreads();                           // the barriers are initialised; the fragments are in
   if (tid == 0)
     for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
-  int issued = max(1, min(nst, kRing));      // stages requested so far
+  int issued = min(nst, kRing);              // stages requested so far
   // ---- scoring
   const float kq = cb.qjl_const;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
@@ -525,8 +531,6 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     if (tid == 0) atomicExch(status, 2);
     // let the copies still in flight land (bounded) before the shared memory is released
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
-  } else if (nst == 0) {
-    bar_wait(su32(&bars[0]), 0);             // the speculative first stage
   }
 }
 
@@ -703,8 +707,9 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
 // launched as the programmatic dependent of the query prep.  Same arithmetic
 // as k_attn; the key and value records and norms of each stage of
 // kStageTiles tiles arrive by cp.async.bulk in a ring of kRing slots (the
-// first stage is requested before the query fragments), and each warp scores
-// tiles warp and warp + 4 of every stage.
+// first stage is requested right after the wait for the prep, before the
+// query fragments are loaded), and each warp scores tiles warp and warp + 4
+// of every stage.
 // ---------------------------------------------------------------------------
 template <int NVK, int PK, int NVV, int PV>
 __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev kcb, const Dev vcb,
@@ -726,7 +731,6 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   const int g = lane >> 2, c = lane & 3;
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
-  const int nt_cap = tcap > tile0 ? (int)(tcap - tile0) : 0;
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
   const int64_t r0 = rowbase + tile0 * 16;
   const uint8_t* gk = kcache + r0 * RBK;
@@ -750,20 +754,22 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (nt_cap > 0) request(0, min(kStageTiles, nt_cap));
   }
   const int64_t L = seq_lens[b];
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
-  // query fragments come from the preceding prep grid: wait for it only now
+  // query fragments come from the preceding prep grid (whose completion also
+  // implies that of any cache append before it): no cache row is read before
+  // this wait; the first stage goes out right after it
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
   QK16<NVK, PK> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, kcb);
   __syncthreads();
   if (tid == 0)
     for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
-  int issued = nt_cap > 0 ? max(1, min(nst, kRing)) : 0;
+  int issued = min(nst, kRing);
 
   float m_run = -INFINITY, l_run = 0.f, wsum = 0.f;
   float acc[8][4];
@@ -886,8 +892,6 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   if (!ok) {
     if (tid == 0) atomicExch(status, 2);
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
-  } else if (nst == 0 && issued) {
-    bar_wait(su32(&bars[0]), 0);             // the speculative first stage
   }
   // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
   // acc = C0 * wsum + value_factor(beta) * D
@@ -993,13 +997,15 @@ cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, u
   cfg.gridDim = dim3(Hkv * 16, B);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 4;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_prep, cb, q, Hq, Hkv, prep);
 }
 
