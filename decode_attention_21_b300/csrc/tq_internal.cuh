@@ -36,6 +36,26 @@ struct Dev {
 
 inline __host__ __device__ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
+// L2 residency hints.  The packed caches are streamed once per call
+// (evict-first); the small codebook tables (Pi, S Pi, S) are read by every
+// query prep and cache append and should stay in L2 (evict-last).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Read-only load of a table entry with an L2 cache policy.
+__device__ __forceinline__ float ld_table(const float* p, uint64_t policy) {
+  float v;
+  asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
+  return v;
+}
+
 // Byte offset of the norm region of a cache holding `rows` rows.
 inline __host__ __device__ int64_t norm_offset(const Dev& cb, int64_t rows) {
   return align256(rows * cb.W * 4);

@@ -288,8 +288,9 @@ struct Quarter {
   // column slice i, rows q*D/4 .. (q+1)*D/4 - 1 of the transposed matrix MT
   __device__ __forceinline__ void load(const float* __restrict__ MT, int i, int q) {
     const float* col = MT + (size_t)(q * (D / 4)) * D + i;
+    const uint64_t keep = l2_policy_evict_last();
 #pragma unroll
-    for (int j = 0; j < D / 4; ++j) m[j] = __ldg(col + (size_t)j * D);
+    for (int j = 0; j < D / 4; ++j) m[j] = ld_table(col + (size_t)j * D, keep);
   }
   __device__ __forceinline__ float dot(const float* xs, int q) const {
     float acc = 0.f;

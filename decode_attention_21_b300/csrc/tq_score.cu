@@ -79,8 +79,8 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   const int kvh = unit >> 2, slot = unit & 3, b = blockIdx.y;
   const bool live = slot < G;
   // This grid may run alongside the kernel before it (a cache append), since
-  // it reads only the queries and the codebook; it waits for that kernel at
-  // its end, so its completion implies the append's.  The scoring kernel
+  // it reads only the queries and the codebook; one of its CTAs waits for
+  // that kernel at its end, so the grid's completion implies the append's.  The scoring kernel
   // that follows may start now: it touches no cache row before it waits for
   // this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   // these loads do not depend on q, so they are issued before waiting for it
   const float* col = (mat == 0 ? cb.PiT : cb.SPT) + (size_t)(32 * qt) * d + 32 * r + o;
   float m[32];
+  const uint64_t keep = l2_policy_evict_last();
 #pragma unroll
-  for (int j = 0; j < 32; ++j) m[j] = __ldg(col + (size_t)j * d);
+  for (int j = 0; j < 32; ++j) m[j] = ld_table(col + (size_t)j * d, keep);
   if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
   float acc = 0.f;
@@ -156,7 +157,10 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
     }
     frag[(v * 8 + kb) * 32 + g * 4 + r] = make_uint2(pack_half2(vals[0], vals[1]), pack_half2(vals[2], vals[3]));
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // One CTA waiting for the kernel before this grid is enough for the grid's
+  // completion to imply that kernel's; the others leave now and free their
+  // SMs for the scoring kernel.
+  if (blockIdx.x == 0 && blockIdx.y == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -372,14 +376,25 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
 namespace {
 constexpr int kStageTiles = 8;
 constexpr int kRing = 4;
+constexpr int kPrefetchStages = 8;    // stages per CTA prefetched into L2 before the prep completes
 constexpr long long kWaitLimit = 1ll << 26;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
+// Bulk copy of streamed cache bytes (L2 evict-first: read once per call).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(l2_policy_evict_first())
+      : "memory");
+}
+
+// Prefetch into L2 (no shared-memory copy): safe before the wait for the
+// cache's writer, since L2 is where the writer's stores land; the bulk copies
+// after the wait then hit L2 instead of HBM.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
@@ -437,11 +452,19 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
+  // Stream the first kPrefetchStages stages of the chunk from HBM into L2
+  // while the prep (and any cache append before it) still runs.
+  if (tid == 0)
+    for (int st = 0; st < min(nst, kPrefetchStages); ++st) {
+      const int t_n = min(kStageTiles, nt - st * kStageTiles);
+      prefetch_l2(grec + (size_t)st * kStageTiles * 16 * RB, (uint32_t)(t_n * 16 * RB));
+      prefetch_l2(gnrm + (size_t)st * kStageTiles * 16 * 4, (uint32_t)(t_n * 16 * 4));
+    }
   // The query fragments come from the preceding prep grid, launched as its
   // programmatic dependent; the prep's completion also implies that of any
-  // cache append before it, so no cache row is read before this wait.  The
-  // first stage goes out right after it, the fragment loads queue behind
-  // only that stage, and the other stages follow.
+  // cache append before it, so no cache row is read into the SM before this
+  // wait.  The first stage goes out right after it, the fragment loads queue
+  // behind only that stage, and the other stages follow.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
   QK16<NV, P> qk;
@@ -759,9 +782,19 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
+  // the first stages stream from HBM into L2 while the prep still runs
+  if (tid == 0)
+    for (int st = 0; st < min(nst, kRing); ++st) {
+      const size_t t_a = (size_t)st * kStageTiles * 16;
+      const int t_n = min(kStageTiles, nt - st * kStageTiles);
+      prefetch_l2(gk + t_a * RBK, (uint32_t)(t_n * 16 * RBK));
+      prefetch_l2(gkn + t_a * 4, (uint32_t)(t_n * 16 * 4));
+      prefetch_l2(gv + t_a * RBV, (uint32_t)(t_n * 16 * RBV));
+      prefetch_l2(gvn + t_a * 2, (uint32_t)(t_n * 16 * 2));
+    }
   // query fragments come from the preceding prep grid (whose completion also
-  // implies that of any cache append before it): no cache row is read before
-  // this wait; the first stage goes out right after it
+  // implies that of any cache append before it): no cache row is read into
+  // the SM before this wait; the first stage goes out right after it
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
   QK16<NVK, PK> qk;
@@ -967,7 +1000,8 @@ __global__ void __launch_bounds__(128) k_attn_merge(const Dev vcb, const float* 
   so[i] = Lsum > 0.f ? a / Lsum : 0.f;
   __syncthreads();
   float o = 0.f;
-  for (int k = 0; k < d; ++k) o = fmaf(vcb.Pi[(size_t)k * d + i], so[k], o);
+  const uint64_t keep = l2_policy_evict_last();
+  for (int k = 0; k < d; ++k) o = fmaf(ld_table(vcb.Pi + (size_t)k * d + i, keep), so[k], o);
   out[((size_t)b * Hq + h) * d + i] = o;
 }
 
