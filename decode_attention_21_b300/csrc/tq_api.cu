@@ -565,11 +565,17 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   if (kcb->dev.mode == TQ_MODE_POLAR) {
     if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
       return st;
-    if ((st = launched("tq_decode_attention",
-                       tq::launch_attn_polar(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                             static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
-                                             seq_lens, prep, sl2, parts, nchunks, tpc, s))) != TQ_OK)
-      return st;
+    if (capacity % 16 == 0)
+      st = launched("tq_decode_attention",
+                    tq::launch_attn_polar_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                                 static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
+                                                 seq_lens, prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
+    else
+      st = launched("tq_decode_attention",
+                    tq::launch_attn_polar(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                          static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens,
+                                          prep, sl2, parts, nchunks, tpc, s));
+    if (st != TQ_OK) return st;
     return launched("tq_decode_attention/merge",
                     tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
   }

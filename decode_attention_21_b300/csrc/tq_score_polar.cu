@@ -14,10 +14,12 @@
 
 #include "tq_internal.cuh"
 #include "tq_mma.cuh"
+#include "tq_stage.cuh"
 
 namespace tq {
 
 using namespace mma;
+using namespace stage;
 
 namespace {
 
@@ -192,6 +194,18 @@ struct PKey {
       w6[p] = __ldg(r + (1 + (c >> 1)) * P + p);
     }
     nrm = __ldg(nrm_p + row);
+  }
+  // the same words from a record already in shared memory (r = record start)
+  __device__ __forceinline__ void load_row(const uint32_t* r, uint32_t nrm_bits, int c, bool valid) {
+    constexpr int P = B + 1;
+#pragma unroll
+    for (int p = 0; p < P; ++p) ws[p] = valid ? r[c * P + p] : 0u;
+#pragma unroll
+    for (int p = 0; p < B; ++p) {
+      w0[p] = valid ? r[p] : 0u;
+      w6[p] = valid ? r[(1 + (c >> 1)) * P + p] : 0u;
+    }
+    nrm = valid ? nrm_bits : 0u;
   }
   // the 32 leaves of subtree c (unit row)
   __device__ __forceinline__ void decode(const PolarTab& tab, int c, float (&y)[32]) const {
@@ -423,6 +437,237 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
   for (int mt = 0; mt < 8; ++mt) {
     ph[2 + 16 * g + 2 * mt] = acc[mt][0] + acc[mt][1];
     ph[2 + 16 * g + 2 * mt + 1] = acc[mt][2] + acc[mt][3];
+  }
+}
+
+// Polar-mode decode attention with bulk-copy staging (capacity a multiple of
+// 16): the key and value records and norms of each stage of kStageTiles
+// tiles arrive by cp.async.bulk in a ring of kRing slots, so the tree decode
+// reads shared memory instead of waiting on global loads.  Arithmetic as in
+// k_attn_polar.
+template <int BK, int BV>
+__global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, const Dev vcb,
+                                                           const uint8_t* __restrict__ kcache,
+                                                           const uint8_t* __restrict__ vcache, int Hq, int Hkv,
+                                                           int64_t capacity, int64_t cache_rows,
+                                                           const int32_t* __restrict__ seq_lens,
+                                                           const uint8_t* __restrict__ prep, float scale_log2,
+                                                           float* __restrict__ partials, int tiles_per_cta,
+                                                           int* __restrict__ status) {
+  constexpr int PK = BK + 1, PV = BV;
+  constexpr int RBK = 16 * PK, RBV = 16 * PV;    // record bytes at d = 128
+  constexpr int kSK = kStageTiles * 16 * RBK, kSKN = kStageTiles * 16 * 4;
+  constexpr int kSV = kStageTiles * 16 * RBV, kSVN = kStageTiles * 16 * 2;
+  constexpr int kSlot = kSK + kSKN + kSV + kSVN;
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ __align__(8) uint64_t bars[kRing];
+  __shared__ PolarTab ktab, vtab;
+  load_tab(kcb, ktab);
+  load_tab(vcb, vtab);
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
+  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
+  const int64_t r0 = rowbase + tile0 * 16;
+  const uint8_t* gk = kcache + r0 * RBK;
+  const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows) + r0 * 4;
+  const uint8_t* gv = vcache + r0 * RBV;
+  const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows) + r0 * 2;
+  auto request = [&](int st, int t_n) {
+    const int slot = st % kRing;
+    const size_t t_a = (size_t)st * kStageTiles * 16;
+    const uint32_t nk = (uint32_t)(t_n * 16 * RBK), nkn = (uint32_t)(t_n * 16 * 4);
+    const uint32_t nv = (uint32_t)(t_n * 16 * RBV), nvn = (uint32_t)(t_n * 16 * 2);
+    const uint32_t bar = su32(&bars[slot]);
+    uint8_t* base = sm + (size_t)slot * kSlot;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(nk + nkn + nv + nvn)
+                 : "memory");
+    bulk_g2s(su32(base), gk + t_a * RBK, nk, bar);
+    bulk_g2s(su32(base + kSK), gkn + t_a * 4, nkn, bar);
+    bulk_g2s(su32(base + kSK + kSKN), gv + t_a * RBV, nv, bar);
+    bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + t_a * 2, nvn, bar);
+  };
+  if (tid == 0) {
+    for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const int64_t L = seq_lens[b];
+  const int64_t tend = min(tcap, (L + 15) / 16);
+  const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
+  const int nst = (nt + kStageTiles - 1) / kStageTiles;
+  if (tid == 0)
+    for (int st = 0; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
+  int issued = min(nst, kRing);
+  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
+  const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
+  uint2 bq[2][8];
+#pragma unroll
+  for (int v = 0; v < 2; ++v)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) bq[v][k] = frag[(v * 8 + k) * 32 + lane];
+  const float* hdr = reinterpret_cast<const float*>(blk);
+  const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
+  __syncthreads();                           // tables and barriers ready
+
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  const float kq = kcb.qjl_const;
+  const int hh = g >> 1, pc = g & 1;
+  const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
+  const int vs = g >> 1, vh = g & 1;   // value subtree and half of this thread's 16 coordinates
+  bool ok = true;
+  int pending_from = 0;
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kRing;
+    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1)))) {
+      ok = false;
+      pending_from = st;
+      break;
+    }
+    const uint8_t* base = sm + (size_t)slot * kSlot;
+    const uint32_t* skn = reinterpret_cast<const uint32_t*>(base + kSK);
+    const uint8_t* sv = base + kSK + kSKN;
+    const __half* svn = reinterpret_cast<const __half*>(base + kSK + kSKN + kSV);
+    const int t_a = st * kStageTiles, n_here = min(kStageTiles, nt - t_a);
+    for (int lt = warp; lt < n_here; lt += 4) {
+      const int64_t t0 = (tile0 + t_a + lt) * 16;
+      const int64_t ta = t0 + g, tb = ta + 8;
+      PKey<BK> ka, kb_;
+      ka.load_row(reinterpret_cast<const uint32_t*>(base + ((size_t)lt * 16 + g) * RBK), skn[lt * 16 + g], c, ta < L);
+      kb_.load_row(reinterpret_cast<const uint32_t*>(base + ((size_t)lt * 16 + g + 8) * RBK), skn[lt * 16 + g + 8], c,
+                   tb < L);
+      float s1a, s1b, s2a, s2b;
+      polar_qk<BK>(ktab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
+      const float sa = ta < L ? est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L ? est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq) * scale_log2 : -INFINITY;
+      float mx = fmaxf(sa, sb);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (__any_sync(kFull, mx > m_run)) {
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+        l_run *= alpha;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        m_run = m_new;
+      }
+      const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
+      const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_run);
+      const float vn0 = ta < L ? __half2float(svn[lt * 16 + g]) : 0.f;
+      const float vn1 = tb < L ? __half2float(svn[lt * 16 + g + 8]) : 0.f;
+      const float wA = pa * vn0, wB = pb * vn1;
+      float ps = pa + pb;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) ps += __shfl_xor_sync(kFull, ps, o);
+      l_run += ps;
+      const float w0 = __shfl_sync(kFull, wA, src0);
+      const float w1 = __shfl_sync(kFull, wA, src1);
+      const float w8 = __shfl_sync(kFull, wB, src0);
+      const float w9 = __shfl_sync(kFull, wB, src1);
+      const uint32_t b0 = pack_half2(piece16(w0, pc), piece16(w1, pc));
+      const uint32_t b1 = pack_half2(piece16(w8, pc), piece16(w9, pc));
+      // decode this thread's 16 value coordinates of tokens 2c, 2c+1, 2c+8, 2c+9
+      float yv[4][16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tok = 2 * c + (j & 1) + 8 * (j >> 1);
+        if (t0 + tok < L) {
+          const uint32_t* r = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV);
+          uint32_t wsv[BV], w0v[BV], w6v[BV];
+#pragma unroll
+          for (int p = 0; p < BV; ++p) {
+            wsv[p] = r[vs * BV + p];
+            w0v[p] = r[p];
+            w6v[p] = r[(1 + (vs >> 1)) * BV + p];
+          }
+          const float rho5 = subtree_radius<BV>(vtab, w0v, w6v, vs);
+          decode_half<BV>(vtab, wsv, rho5, vh, yv[j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) yv[j][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int pv = 0; pv < 2; ++pv) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int q0 = 2 * mt, q1 = 2 * mt + 1;
+          const uint32_t a0 = pack_half2(piece16(yv[0][q0], pv), piece16(yv[1][q0], pv));
+          const uint32_t a1 = pack_half2(piece16(yv[0][q1], pv), piece16(yv[1][q1], pv));
+          const uint32_t a2 = pack_half2(piece16(yv[2][q0], pv), piece16(yv[3][q0], pv));
+          const uint32_t a3 = pack_half2(piece16(yv[2][q1], pv), piece16(yv[3][q1], pv));
+          mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+    }
+    if (st + kRing < nst) {
+      __syncthreads();
+      if (tid == 0) request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
+      issued = st + kRing + 1;
+    }
+  }
+  if (!ok) {
+    if (tid == 0) atomicExch(status, 2);
+    for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
+  }
+  const int nchunks = gridDim.x;
+  float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
+  float* ph = part + c * (2 + 128);
+  if (g == 0) {
+    ph[0] = m_run;
+    ph[1] = l_run;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    ph[2 + 16 * g + 2 * mt] = acc[mt][0] + acc[mt][1];
+    ph[2 + 16 * g + 2 * mt + 1] = acc[mt][2] + acc[mt][3];
+  }
+}
+
+template <int BK, int BV>
+static cudaError_t attn_polar_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
+                                       const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows,
+                                       const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
+                                       int* status) {
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * (BK + 1) + 4 + 16 * BV + 2);
+  static cudaError_t configured = cudaFuncSetAttribute(k_attn_polar_staged<BK, BV>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (configured != cudaSuccess) return configured;
+  k_attn_polar_staged<BK, BV><<<grid, 128, smem, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc,
+                                                      status);
+  return cudaGetLastError();
+}
+
+template <int BK>
+static cudaError_t attn_polar_staged_v(int bv, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v,
+                                       const uint8_t* kc, const uint8_t* vc, int Hq, int Hkv, int64_t cap,
+                                       int64_t rows, const int32_t* sl, const uint8_t* prep, float sl2, float* parts,
+                                       int tpc, int* status) {
+  switch (bv) {
+    case 1: return attn_polar_staged_t<BK, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    case 2: return attn_polar_staged_t<BK, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    case 3: return attn_polar_staged_t<BK, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    default: return attn_polar_staged_t<BK, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+  }
+}
+
+cudaError_t launch_attn_polar_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B,
+                                     int Hq, int Hkv, int64_t capacity, int64_t rows, const int32_t* seq_lens,
+                                     const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc,
+                                     int* status, cudaStream_t s) {
+  const dim3 grid(nchunks, Hkv, B);
+  switch (kcb.b1) {
+    case 1: return attn_polar_staged_v<1>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
+    case 2: return attn_polar_staged_v<2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
+    default: return attn_polar_staged_v<3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
   }
 }
 

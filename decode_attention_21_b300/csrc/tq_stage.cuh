@@ -1,0 +1,47 @@
+// Bulk-copy staging shared by the scoring kernels: cp.async.bulk copies of
+// cache bytes into shared memory, completed on mbarriers, waited on with
+// bounded spins, and L2 prefetches.
+#pragma once
+#include <cstdint>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace stage {
+constexpr int kStageTiles = 8;
+constexpr int kRing = 4;
+constexpr int kPrefetchStages = 8;    // stages per CTA prefetched into L2 before the prep completes
+constexpr long long kWaitLimit = 1ll << 26;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// Bulk copy of streamed cache bytes (L2 evict-first: read once per call).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(l2_policy_evict_first())
+      : "memory");
+}
+
+// Prefetch into L2 (no shared-memory copy): safe before the wait for the
+// cache's writer, since L2 is where the writer's stores land; the bulk copies
+// after the wait then hit L2 instead of HBM.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+}  // namespace stage
+}  // namespace tq
