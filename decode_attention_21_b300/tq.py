@@ -18,7 +18,7 @@ KIND_PROD, KIND_MSE = 0, 1
 F32, BF16 = 0, 1
 
 EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_host_tables", "tq_record_bytes", "tq_cache_bytes",
-           "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits",
+           "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits", "tq_logits_dense",
            "tq_decode_attention_workspace", "tq_decode_attention", "tq_decode_attention_static",
            "tq_search_workspace", "tq_search",
            "tq_check_device", "tq_last_error"]
@@ -62,6 +62,7 @@ def lib():
         L.tq_logits_workspace.argtypes = [vp, i32, i32, i32]
         L.tq_logits_workspace.restype = sz
         L.tq_logits.argtypes = [vp, vp, i32, i32, i32, i64, vp, vp, vp, vp, sz, vp]
+        L.tq_logits_dense.argtypes = [vp, i32, i32, i32, i32, i32, i64, vp, vp, vp, vp]
         L.tq_decode_attention_workspace.argtypes = [vp, i32, i32, i32, i64]
         L.tq_decode_attention_workspace.restype = sz
         L.tq_decode_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i64, vp, vp, ctypes.c_float, vp, vp, sz, vp]
@@ -186,6 +187,13 @@ def tq_logits_workspace(kcb, B, Hq, Hkv):
 def tq_logits(kcb, kcache, B, Hq, Hkv, capacity, seq_lens, q, logits, workspace, stream=None):
     _check(lib().tq_logits(kcb.handle, _ptr(kcache), B, Hq, Hkv, capacity, _ptr(seq_lens), _ptr(q), _ptr(logits),
                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_logits_dense(keys, B, Hq, Hkv, capacity, seq_lens, q, logits, stream=None):
+    """Unquantized comparator: keys [B, Hkv, capacity, 128] fp32 or bf16."""
+    dt = {torch.float32: F32, torch.bfloat16: BF16}[keys.dtype]
+    _check(lib().tq_logits_dense(_ptr(keys), dt, keys.shape[-1], B, Hq, Hkv, capacity, _ptr(seq_lens), _ptr(q),
+                                 _ptr(logits), _stream(stream)))
 
 
 def tq_decode_attention_workspace(kcb, B, Hq, Hkv, capacity):

@@ -147,6 +147,22 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
                     int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q,
                     float* logits, void* workspace, size_t ws_bytes, void* stream);
 
+/* Unquantized comparator of tq_logits: the same logits from uncompressed
+ * keys ([xujun] 常见问题: TurboQuant's attention-logit speed-up is quoted
+ * against 32-bit unquantized keys):
+ *   logits[b, h, t] = <q[b, h], keys[b, h / G, t]>   for t < seq_lens[b];
+ * entries t >= seq_lens[b] are left untouched.
+ *   keys       device [B, Hkv, capacity, d], fp32 or bf16 (key_dtype TQ_F32 /
+ *              TQ_BF16), row-major
+ *   d          128 (TQ_EUNSUPPORTED otherwise)
+ *   seq_lens   device int32[B], each <= capacity
+ *   q          device fp32 [B, Hq, d] (G = Hq / Hkv <= 4)
+ *   logits     device fp32 [B, Hq, capacity]
+ * fp32 accumulation; no workspace.                                          */
+tq_status tq_logits_dense(const void* keys, int32_t key_dtype, int32_t d, int32_t B, int32_t Hq,
+                          int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q,
+                          float* logits, void* stream);
+
 /* Workspace bytes of tq_decode_attention. */
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq,
                                      int32_t Hkv, int64_t capacity);

@@ -64,6 +64,24 @@ def logits(cb_k, kcode, q, seq_lens, Hkv, capacity):
     return out
 
 
+def dense_logits(K, q, seq_lens, Hkv, capacity):
+    """Unquantized logits <q[b, h], K[b, h // G, t]> [B, Hq, capacity]; NaN for
+    t >= seq_len[b].  The comparator that the attention-logit speed-up of
+    TurboQuant keys is stated against ([xujun] 常见问题: 32-bit unquantized
+    keys).  K [B, Hkv, capacity, d] holds the key values exactly as stored
+    (fp32, or bf16 widened)."""
+    K = np.asarray(K, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, _ = q.shape
+    G = Hq // Hkv
+    out = np.full((B, Hq, capacity), np.nan)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(Hq):
+            out[b, h, :L] = K[b, h // G, :L] @ q[b, h]
+    return out
+
+
 def attention(cb_k, cb_v, kcode, vcode, q, seq_lens, Hkv, capacity, scale, chunk=1 << 16):
     """Decode attention output [B, Hq, d] (fp64), chunked over tokens."""
     B, Hq, d = q.shape

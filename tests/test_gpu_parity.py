@@ -254,6 +254,32 @@ def test_attention_long_context_ring_refill():
         rowwise_ok(got[b], ref[b])
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 32, 8, 4096, [4096]), (3, 6, 3, 333, [333, 17, 0]),
+                                               (2, 4, 4, 1001, [1000, 1001])])
+def test_logits_dense_comparator(dtype, B, Hq, Hkv, cap, lens):
+    """Unquantized logits (fp32 or bf16 keys) against the oracle's plain dot products."""
+    from oracle import rng as orng
+    K = np.stack([np.stack([wl.llama_kv_slice(0, h, 0, cap, which="keys") for h in range(Hkv)])
+                  for _ in range(B)]).astype(np.float64)
+    Kt = torch.from_numpy(K.astype(np.float32))
+    if dtype == "bf16":
+        Kt = Kt.to(torch.bfloat16)
+        K = orng.round_bf16(K)
+    q = wl.queries((B, Hq, 128))
+    ref = estimate.dense_logits(K, q.astype(np.float64), lens, Hkv, cap)
+    out = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    tq.tq_logits_dense(Kt.cuda(), B, Hq, Hkv, cap, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                       torch.from_numpy(q).cuda(), out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        L = lens[b]
+        assert np.all(np.isnan(got[b, :, L:]))
+        if L:
+            rowwise_ok(got[b, :, :L], ref[b, :, :L], tol=1e-4, med=1e-4)
+
+
 def test_invalid_arguments_return_status_without_launch():
     _, gcb = pair(128, 3)
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")

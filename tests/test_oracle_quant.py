@@ -317,3 +317,24 @@ def test_search_recall_high_bits():
     ids, _ = estimate.search(cb, quant.quantize(cb, x), q, 10)
     true = np.argmax(q.astype(np.float64) @ x.astype(np.float64).T, axis=1)
     assert estimate.recall_1_at_k(true, ids)[10] >= 0.98
+
+
+def test_dense_logits_brute_force():
+    """The unquantized comparator against a plain Python triple loop (tiny case,
+    GQA group 2, a short sequence)."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, cap, d = 2, 4, 2, 5, 8
+    K = rng.standard_normal((B, Hkv, cap, d))
+    q = rng.standard_normal((B, Hq, d))
+    lens = [5, 3]
+    got = estimate.dense_logits(K, q, lens, Hkv, cap)
+    for b in range(B):
+        for h in range(Hq):
+            for t in range(cap):
+                if t >= lens[b]:
+                    assert np.isnan(got[b, h, t])
+                    continue
+                want = 0.0
+                for i in range(d):
+                    want += float(q[b, h, i]) * float(K[b, h // 2, t, i])
+                assert abs(got[b, h, t] - want) <= 1e-12 * (1 + abs(want))
