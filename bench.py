@@ -395,18 +395,37 @@ def dense_comparator(tq, wl, B, Hq, Hkv, d, T, cache, kcb, seq, q, ws, tq_call_m
         res[name] = {"ms_per_call": ms, "gbs": nbytes / (ms / 1e3) / 1e9, "frac": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
                      "turboquant_speedup": ms / tq_call_ms}
         del copies
-    # accuracy of the 4-bit estimate against the exact logits of the same keys
+    # accuracy against the exact logits of the same keys: relative RMS error
+    # and least-squares slope of estimate on exact (1 = unbiased; MSE-only
+    # keys shrink inner products)
     exact = torch.empty(B, Hq, T, device="cuda")
     tq.tq_logits_dense(keys.to(torch.float32), B, Hq, Hkv, T, seq, q, exact)
-    fresh = torch.empty_like(cache)           # the same keys, freshly compressed (no appended rows)
-    for h in range(Hkv):
-        dst = torch.arange(h * T, (h + 1) * T, dtype=torch.int64, device="cuda")
-        tq.tq_quantize(kcb, fresh, B * Hkv * T, keys[0, h], T, d, dst_rows=dst)
-    est = torch.empty(B, Hq, T, device="cuda")
-    tq.tq_logits(kcb, fresh, B, Hq, Hkv, T, seq, q, est, ws)
-    torch.cuda.synchronize()
-    rel = ((est - exact).norm(dim=-1) / exact.norm(dim=-1)).flatten()
-    res["turboquant_rel_rms_error"] = {"median_over_heads": float(rel.median()), "max": float(rel.max())}
+    variants = {}
+    for name, bits, kind in (("prod_b4", 4, tq.KIND_PROD), ("mse_b4", 4, tq.KIND_MSE), ("mse_b3", 3, tq.KIND_MSE)):
+        cb = kcb if name == "prod_b4" else tq.Codebook(d, bits, kind)
+        fresh = torch.empty(tq.cache_bytes(cb, B * Hkv * T), dtype=torch.uint8, device="cuda")
+        for h in range(Hkv):
+            dst = torch.arange(h * T, (h + 1) * T, dtype=torch.int64, device="cuda")
+            tq.tq_quantize(cb, fresh, B * Hkv * T, keys[0, h], T, d, dst_rows=dst)
+        wsv = torch.empty(tq.tq_logits_workspace(cb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+        est = torch.empty(B, Hq, T, device="cuda")
+        tq.tq_logits(cb, fresh, B, Hq, Hkv, T, seq, q, est, wsv)
+        torch.cuda.synchronize()
+        rel = ((est - exact).norm(dim=-1) / exact.norm(dim=-1)).flatten()
+        slope = float((est * exact).sum() / (exact * exact).sum())
+        v = {"bytes_per_key": tq.record_bytes(cb) + (4 if kind == tq.KIND_PROD else 2),
+             "rel_rms_error_median": float(rel.median()), "rel_rms_error_max": float(rel.max()),
+             "slope_vs_exact": slope}
+        if name != "prod_b4":
+            nc = max(2, math.ceil(2.2 * L2_BYTES / fresh.numel()))
+            copies = [fresh] + [fresh.clone() for _ in range(nc - 1)]
+            v["ms_per_call"] = per_call_ms(
+                lambda i: tq.tq_logits(cb, copies[i % nc], B, Hq, Hkv, T, seq, q, est, wsv), 20)
+            del copies
+        else:
+            v["ms_per_call"] = tq_call_ms
+        variants[name] = v
+    res["turboquant_variants"] = variants
     res["note"] = ("the pages quote up to 8x for 4-bit keys vs 32-bit keys on H100 (attention logits only); "
                    "here both arms are measured on one B300")
     return res

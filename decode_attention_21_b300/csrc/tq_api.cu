@@ -500,7 +500,12 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
                     const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
                     void* stream) {
   tq_status st;
-  if ((st = check_scoring_codebook(kcb, TQ_KIND_PROD, "tq_logits")) != TQ_OK) return st;
+  // keys with the QJL term (PROD), or MSE-only keys in scalar mode
+  if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD,
+                                   "tq_logits")) != TQ_OK)
+    return st;
+  if (kcb->dev.kind == TQ_KIND_MSE && kcb->dev.mode != TQ_MODE_SCALAR)
+    return fail(TQ_EUNSUPPORTED, "tq_logits: MSE-only keys are scored in scalar mode only");
   if ((st = check_heads("tq_logits", B, Hq, Hkv, capacity)) != TQ_OK) return st;
   if (capacity == 0) return ok();
   if (!kcache || !seq_lens || !q || !logits || !workspace)

@@ -92,11 +92,13 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   const int mat = tid >> 7, qt = (tid >> 5) & 3, o = tid & 31;
   // Pi^T (mat 0) or (S Pi)^T (mat 1): rows 32 qt .. 32 qt + 31, column 32 r + o;
   // these loads do not depend on q, so they are issued before waiting for it
+  // (MSE-only keys have no sketch: the second matrix is absent and q'' = 0)
+  const bool has_s = cb.kind == 0;
   const float* col = (mat == 0 ? cb.PiT : cb.SPT) + (size_t)(32 * qt) * d + 32 * r + o;
   float m[32];
   const uint64_t keep = l2_policy_evict_last();
 #pragma unroll
-  for (int j = 0; j < 32; ++j) m[j] = ld_table(col + (size_t)j * d, keep);
+  for (int j = 0; j < 32; ++j) m[j] = (mat == 0 || has_s) ? ld_table(col + (size_t)j * d, keep) : 0.f;
   if (tid < d) sq[tid] = live ? q[((size_t)b * Hq + kvh * G + slot) * d + tid] : 0.f;
   __syncthreads();
   float acc = 0.f;
@@ -171,10 +173,12 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
 // (odd XOR-products of the code planes) share the query operand and keep one
 // accumulator each; the coefficients -2 coef_v S1 are applied to the sums.
 // ---------------------------------------------------------------------------
-template <int NV, int P>
+template <int NV, int P, bool QJL = true>
 struct QK16 {
   static constexpr int C1 = NV == 1 ? 2 : 1;   // accumulator chains per virtual plane
-  uint2 bq[2][8];
+  static constexpr int PS = QJL ? P - 1 : P;   // stage-1 code planes (the QJL sign plane is last)
+  static constexpr int NQ = QJL ? 1 : 0;
+  uint2 bq[1 + NQ][8];
   float S2, K1, K2;
   float cv[NV];
 
@@ -182,7 +186,7 @@ struct QK16 {
     const float* hdr = reinterpret_cast<const float*>(blk);
     const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
 #pragma unroll
-    for (int v = 0; v < 2; ++v)
+    for (int v = 0; v <= NQ; ++v)
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb) bq[v][kb] = frag[(v * 8 + kb) * 32 + lane];
     const int c = lane & 3;
@@ -195,19 +199,20 @@ struct QK16 {
   }
 
   // wa[t], wb[t]: the P plane words (column c) of keys g and g+8 of tile t.
-  // s1[t][0/1], s2[t][0/1]: stage-1 and QJL inner products of keys g, g+8.
+  // s1[t][0/1], s2[t][0/1]: stage-1 and QJL inner products of keys g, g+8
+  // (s2 = 0 without the QJL plane).
   template <int T>
   __device__ __forceinline__ void score(const uint32_t (&wa)[T][P], const uint32_t (&wb)[T][P], float (&s1)[T][2],
                                         float (&s2)[T][2]) const {
     float a1[T][NV][C1][4], a2[T][2][4];
-    uint32_t xa[T][NV + 1], xb[T][NV + 1], ya[T][NV + 1], yb[T][NV + 1];
+    uint32_t xa[T][NV + NQ], xb[T][NV + NQ], ya[T][NV + NQ], yb[T][NV + NQ];
 #pragma unroll
     for (int t = 0; t < T; ++t) {
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         uint32_t pa = 0, pb = 0;
 #pragma unroll
-        for (int p = 0; p < P - 1; ++p)
+        for (int p = 0; p < PS; ++p)
           if (kOddMask[v] >> p & 1u) {
             pa ^= wa[t][p];
             pb ^= wb[t][p];
@@ -219,10 +224,12 @@ struct QK16 {
 #pragma unroll
           for (int e = 0; e < 4; ++e) a1[t][v][ch][e] = 0.f;
       }
-      xa[t][NV] = wa[t][P - 1];
-      xb[t][NV] = wb[t][P - 1];
+      if constexpr (QJL) {
+        xa[t][NV] = wa[t][P - 1];
+        xb[t][NV] = wb[t][P - 1];
+      }
 #pragma unroll
-      for (int v = 0; v <= NV; ++v) {
+      for (int v = 0; v < NV + NQ; ++v) {
         ya[t][v] = xa[t][v] >> 4;
         yb[t][v] = xb[t][v] >> 4;
       }
@@ -236,9 +243,10 @@ struct QK16 {
       const int b0 = 2 * kb, b1 = 2 * kb + 1;
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        mma_f16(a2[t][kb & 1], bit_operand(xa[t][NV], ya[t][NV], b0), bit_operand(xb[t][NV], yb[t][NV], b0),
-                bit_operand(xa[t][NV], ya[t][NV], b1), bit_operand(xb[t][NV], yb[t][NV], b1), bq[1][kb].x,
-                bq[1][kb].y);
+        if constexpr (QJL)
+          mma_f16(a2[t][kb & 1], bit_operand(xa[t][NV], ya[t][NV], b0), bit_operand(xb[t][NV], yb[t][NV], b0),
+                  bit_operand(xa[t][NV], ya[t][NV], b1), bit_operand(xb[t][NV], yb[t][NV], b1), bq[NQ][kb].x,
+                  bq[NQ][kb].y);
 #pragma unroll
         for (int v = 0; v < NV; ++v)
           mma_f16(a1[t][v][kb % C1], bit_operand(xa[t][v], ya[t][v], b0), bit_operand(xb[t][v], yb[t][v], b0),
@@ -258,8 +266,12 @@ struct QK16 {
         }
       s1[t][0] = ra;
       s1[t][1] = rb;
-      s2[t][0] = fmaf(S2, (a2[t][0][0] + a2[t][0][1]) + (a2[t][1][0] + a2[t][1][1]), K2);
-      s2[t][1] = fmaf(S2, (a2[t][0][2] + a2[t][0][3]) + (a2[t][1][2] + a2[t][1][3]), K2);
+      if constexpr (QJL) {
+        s2[t][0] = fmaf(S2, (a2[t][0][0] + a2[t][0][1]) + (a2[t][1][0] + a2[t][1][1]), K2);
+        s2[t][1] = fmaf(S2, (a2[t][0][2] + a2[t][0][3]) + (a2[t][1][2] + a2[t][1][3]), K2);
+      } else {
+        s2[t][0] = s2[t][1] = 0.f;
+      }
     }
   }
 };
@@ -279,17 +291,22 @@ __device__ __forceinline__ void load_words(const uint32_t* __restrict__ rec, int
   }
 }
 
-// Key words and norms of one 16-key tile for thread (g, c).
-template <int P>
+// Key words and norms of one 16-key tile for thread (g, c).  The norm entry
+// is 4 bytes (n, gamma) with the QJL term, 2 bytes (n) without.
+template <int P, bool QJL = true>
 struct KTile {
   uint32_t wa[P], wb[P];
   uint32_t na, nb;
+  __device__ __forceinline__ static uint32_t norm_at(const uint32_t* nrm, int64_t row) {
+    if constexpr (QJL) return __ldg(nrm + row);
+    else return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(nrm) + row);
+  }
   __device__ __forceinline__ void load(const uint32_t* recs, const uint32_t* nrm, int W, int64_t rowbase, int64_t ta,
                                        int64_t L, int c) {
     const int64_t tb = ta + 8;
     if (ta < L) {
       load_words<P>(recs + (rowbase + ta) * W, c, wa);
-      na = __ldg(nrm + rowbase + ta);
+      na = norm_at(nrm, rowbase + ta);
     } else {
 #pragma unroll
       for (int p = 0; p < P; ++p) wa[p] = 0;
@@ -297,7 +314,7 @@ struct KTile {
     }
     if (tb < L) {
       load_words<P>(recs + (rowbase + tb) * W, c, wb);
-      nb = __ldg(nrm + rowbase + tb);
+      nb = norm_at(nrm, rowbase + tb);
     } else {
 #pragma unroll
       for (int p = 0; p < P; ++p) wb[p] = 0;
@@ -306,16 +323,30 @@ struct KTile {
   }
 };
 
+// Estimate from the norm entry: fp16 (n, gamma) for keys with the QJL term,
+// fp16 n (low half) for MSE-only keys.
+template <bool QJL>
+__device__ __forceinline__ float est_key(uint32_t nrm_bits, float s1, float s2, float kq);
+
 __device__ __forceinline__ float est_from(uint32_t nrm_bits, float s1, float s2, float kq) {
   const __half2 h = *reinterpret_cast<const __half2*>(&nrm_bits);
   return __low2float(h) * fmaf(__high2float(h) * kq, s2, s1);
+}
+
+template <bool QJL>
+__device__ __forceinline__ float est_key(uint32_t nrm_bits, float s1, float s2, float kq) {
+  if constexpr (QJL) {
+    return est_from(nrm_bits, s1, s2, kq);
+  } else {
+    return __half2float(__ushort_as_half((unsigned short)(nrm_bits & 0xffffu))) * s1;
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Logits: grid (chunks, Hkv, B), 4 warps; each warp scores 16-key tiles,
 // prefetching its next tile while scoring the current one.
 // ---------------------------------------------------------------------------
-template <int NV, int P>
+template <int NV, int P, bool QJL>
 __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
                                                 int64_t capacity, int64_t cache_rows,
                                                 const int32_t* __restrict__ seq_lens,
@@ -330,7 +361,7 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
   if (tile0 + warp >= tend) return;
-  QK16<NV, P> qk;
+  QK16<NV, P, QJL> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, cb);
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
@@ -338,7 +369,7 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
   const float kq = cb.qjl_const;
   const int W = cb.W;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
-  KTile<P> cur, nxt;
+  KTile<P, QJL> cur, nxt;
   int64_t tile = tile0 + warp;
   cur.load(recs, nrm, W, rowbase, tile * 16 + g, L, c);
   for (; tile < tend; tile += 4) {
@@ -354,8 +385,8 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
     qk.template score<1>(wa, wb, s1, s2);
     const int64_t ta = tile * 16 + g, tb = ta + 8;
     if (c < G) {
-      if (ta < L) out[ta] = est_from(cur.na, s1[0][0], s2[0][0], kq);
-      if (tb < L) out[tb] = est_from(cur.nb, s1[0][1], s2[0][1], kq);
+      if (ta < L) out[ta] = est_key<QJL>(cur.na, s1[0][0], s2[0][0], kq);
+      if (tb < L) out[tb] = est_key<QJL>(cur.nb, s1[0][1], s2[0][1], kq);
     }
     cur = nxt;
   }
@@ -376,14 +407,16 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
 // (bounded) for its copies in flight and returns.
 // ---------------------------------------------------------------------------
 
-template <int NV, int P>
+template <int NV, int P, bool QJL>
 __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
                                                        int Hkv, int64_t capacity, int64_t cache_rows,
                                                        const int32_t* __restrict__ seq_lens,
                                                        const uint8_t* __restrict__ prep, float* __restrict__ logits,
                                                        int tiles_per_cta, int* __restrict__ status) {
   constexpr int RB = 16 * P;                 // record bytes at d = 128
-  constexpr int kStageRec = kStageTiles * 16 * RB, kStageNrm = kStageTiles * 16 * 4;
+  constexpr int NB = QJL ? 4 : 2;            // norm entry bytes
+  constexpr int kPairs = NV <= 4;            // two tiles per warp step (registers permitting)
+  constexpr int kStageRec = kStageTiles * 16 * RB, kStageNrm = kStageTiles * 16 * NB;
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ __align__(8) uint64_t bars[kRing];
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -398,16 +431,16 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   if (tile0 >= tcap) return;
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
   const uint8_t* grec = kcache + (rowbase + tile0 * 16) * RB;
-  const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows) + (rowbase + tile0 * 16) * 4;
+  const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows) + (rowbase + tile0 * 16) * NB;
   // stage st (tiles st*kStageTiles ..) into ring slot st % kRing
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
     const int t_a = st * kStageTiles;
-    const uint32_t rb = (uint32_t)(t_n * 16 * RB), nb = (uint32_t)(t_n * 16 * 4);
+    const uint32_t rb = (uint32_t)(t_n * 16 * RB), nb = (uint32_t)(t_n * 16 * NB);
     const uint32_t bar = su32(&bars[slot]);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(rb + nb) : "memory");
     bulk_g2s(su32(srec + (size_t)slot * kStageRec), grec + (size_t)t_a * 16 * RB, rb, bar);
-    bulk_g2s(su32(snrm + (size_t)slot * kStageNrm), gnrm + (size_t)t_a * 16 * 4, nb, bar);
+    bulk_g2s(su32(snrm + (size_t)slot * kStageNrm), gnrm + (size_t)t_a * 16 * NB, nb, bar);
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -423,7 +456,7 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     for (int st = 0; st < min(nst, kPrefetchStages); ++st) {
       const int t_n = min(kStageTiles, nt - st * kStageTiles);
       prefetch_l2(grec + (size_t)st * kStageTiles * 16 * RB, (uint32_t)(t_n * 16 * RB));
-      prefetch_l2(gnrm + (size_t)st * kStageTiles * 16 * 4, (uint32_t)(t_n * 16 * 4));
+      prefetch_l2(gnrm + (size_t)st * kStageTiles * 16 * NB, (uint32_t)(t_n * 16 * NB));
     }
   // The query fragments come from the preceding prep grid, launched as its
   // programmatic dependent; the prep's completion also implies that of any
@@ -432,7 +465,7 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   // behind only that stage, and the other stages follow.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
-  QK16<NV, P> qk;
+  QK16<NV, P, QJL> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, cb);
   __syncthreads();                           // the barriers are initialised; the fragments are in
   if (tid == 0)
@@ -459,8 +492,13 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
         wb[p] = reinterpret_cast<const uint32_t*>(rbp)[p];
       }
     }
-    na = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g];
-    nb = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g + 8];
+    if constexpr (QJL) {
+      na = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g];
+      nb = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g + 8];
+    } else {
+      na = reinterpret_cast<const unsigned short*>(nrm)[lt * 16 + g];
+      nb = reinterpret_cast<const unsigned short*>(nrm)[lt * 16 + g + 8];
+    }
     const int64_t ta = tg * 16 + g;
     if (ta >= L) {
 #pragma unroll
@@ -474,8 +512,8 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   auto emit = [&](int64_t tg, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
     const int64_t ta = tg * 16 + g, tb = ta + 8;
     if (c < G) {
-      if (ta < L) out[ta] = est_from(na, s1a, s2a, kq);
-      if (tb < L) out[tb] = est_from(nb, s1b, s2b, kq);
+      if (ta < L) out[ta] = est_key<QJL>(na, s1a, s2a, kq);
+      if (tb < L) out[tb] = est_key<QJL>(nb, s1b, s2b, kq);
     }
   };
   for (int st = 0; st < nst; ++st) {
@@ -492,7 +530,7 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     // a lone last tile is scored on its own
     for (int lt = warp; lt < n_here; lt += 8) {
       const int lt2 = lt + 4;
-      if (lt2 < n_here) {
+      if (kPairs && lt2 < n_here) {
         uint32_t wa[2][P], wb[2][P], na, nb, ma, mb;
         tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb);
         tile_words(rec, nrm, lt2, tile0 + t_a + lt2, wa[1], wb[1], ma, mb);
@@ -506,6 +544,12 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
         float s1[1][2], s2[1][2];
         qk.template score<1>(wa, wb, s1, s2);
         emit(tile0 + t_a + lt, na, nb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
+        if (!kPairs && lt2 < n_here) {
+          uint32_t xa[1][P], xb[1][P], ma, mb;
+          tile_words(rec, nrm, lt2, tile0 + t_a + lt2, xa[0], xb[0], ma, mb);
+          qk.template score<1>(xa, xb, s1, s2);
+          emit(tile0 + t_a + lt2, ma, mb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
+        }
       }
     }
     // every warp is done with this ring slot: refill it with stage st + kRing
@@ -1008,26 +1052,43 @@ cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, u
   return cudaLaunchKernelEx(&cfg, k_prep, cb, q, Hq, Hkv, prep);
 }
 
+// Key caches with the QJL term (PROD) use b' = 1..3 code planes + the sign
+// plane; MSE-only key caches use b = 1..4 code planes.
+#define TQ_LOGITS_DISPATCH(CALL)                          \
+  if (cb.kind == 0) {                                     \
+    switch (cb.b1) {                                      \
+      case 1: CALL(1, 2, true);                           \
+      case 2: CALL(2, 3, true);                           \
+      default: CALL(4, 4, true);                          \
+    }                                                     \
+  }                                                       \
+  switch (cb.b1) {                                        \
+    case 1: CALL(1, 1, false);                            \
+    case 2: CALL(2, 2, false);                            \
+    case 3: CALL(4, 3, false);                            \
+    default: CALL(8, 4, false);                           \
+  }
+
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks,
                           int tpc, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
-  switch (cb.b1) {
-    case 1: k_logits<1, 2><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
-    case 2: k_logits<2, 3><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
-    default: k_logits<4, 4><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
-  }
-  return cudaGetLastError();
+#define TQ_CALL(NV, P, Q)                                                                                 \
+  k_logits<NV, P, Q><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); \
+  return cudaGetLastError()
+  TQ_LOGITS_DISPATCH(TQ_CALL)
+#undef TQ_CALL
 }
 
-template <int NV, int P>
+template <int NV, int P, bool QJL>
 static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                                    int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                                    int nchunks, int tpc, int* status, cudaStream_t s) {
-  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + 4);
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + (QJL ? 4 : 2));
   static cudaError_t configured = [] {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_staged<NV, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_logits_staged<NV, P>));
+    cudaError_t e =
+        cudaFuncSetAttribute(k_logits_staged<NV, P, QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_logits_staged<NV, P, QJL>));
     return e;
   }();
   if (configured != cudaSuccess) return configured;
@@ -1041,19 +1102,19 @@ static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc,
-                            status);
+  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P, QJL>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep,
+                            logits, tpc, status);
 }
 
 cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                                  int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                                  int nchunks, int tpc, int* status, cudaStream_t s) {
-  switch (cb.b1) {
-    case 1: return logits_staged_t<1, 2>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
-    case 2: return logits_staged_t<2, 3>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
-    default: return logits_staged_t<4, 4>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s);
-  }
+#define TQ_CALL(NV, P, Q) \
+  return logits_staged_t<NV, P, Q>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s)
+  TQ_LOGITS_DISPATCH(TQ_CALL)
+#undef TQ_CALL
 }
+#undef TQ_LOGITS_DISPATCH
 
 template <int NVK, int PK, int NVV, int PV>
 static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,

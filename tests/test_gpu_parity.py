@@ -159,6 +159,30 @@ def test_logits_parity(bits, B, Hq, Hkv, cap, lens, mode):
             rowwise_ok(got[b, :, :L], ref[b, :, :L])
 
 
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 8, 2, 4096, [4096]), (3, 6, 3, 333, [333, 17, 0]),
+                                               (2, 4, 1, 1000, [1000, 1])])
+def test_logits_parity_mse_only_keys(bits, B, Hq, Hkv, cap, lens):
+    """TurboQuant-MSE keys (b-bit stage 1, no QJL term): est = n <q', yhat>."""
+    ocb, gcb = pair(128, bits, kind="mse")
+    rows = B * Hkv * cap
+    x = wl.gaussian_outlier_keys(rows, 128)
+    code, img = oracle_cache(ocb, rows, x.astype(np.float64))
+    q = wl.queries((B, Hq, 128), name="tiny_q")
+    ref = estimate.logits(ocb, code, q.astype(np.float64), lens, Hkv, cap)
+    ws = torch.empty(tq.tq_logits_workspace(gcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    tq.tq_logits(gcb, torch.from_numpy(img).cuda(), B, Hq, Hkv, cap, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                 torch.from_numpy(q).cuda(), out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        L = lens[b]
+        assert np.all(np.isnan(got[b, :, L:]))
+        if L:
+            rowwise_ok(got[b, :, :L], ref[b, :, :L])
+
+
 def tiled_code(code, reps):
     """The oracle's code arrays repeated ``reps`` times along the rows."""
     n = code["n"].shape[0]
@@ -300,9 +324,13 @@ def test_invalid_arguments_return_status_without_launch():
     with pytest.raises(tq.TqError) as e:
         tq.tq_quantize(gcb, kc, 64, q.view(-1, 128), 4, 129)     # d_in > d
     assert e.value.status == tq.TQ_EINVAL
-    _, vcb = pair(128, 3, "mse")
+    _, pcb = pair(128, 3, "mse", mode="polar")
     with pytest.raises(tq.TqError) as e:
-        tq.tq_logits(vcb, kc, 1, 4, 1, 64, sl, q, out, ws)       # values codebook for keys
+        tq.tq_logits(pcb, kc, 1, 4, 1, 64, sl, q, out, ws)       # MSE-only keys in polar mode
+    assert e.value.status == tq.TQ_EUNSUPPORTED
+    _, vcb = pair(128, 3, "mse")
+    with pytest.raises(tq.TqError) as e:                         # MSE-only keys in attention
+        tq.tq_decode_attention(vcb, vcb, kc, kc, 1, 4, 1, 64, sl, q, 0.1, out, ws)
     assert e.value.status == tq.TQ_EINVAL
     torch.cuda.synchronize()
 
