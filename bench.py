@@ -401,8 +401,10 @@ def dense_comparator(tq, wl, B, Hq, Hkv, d, T, cache, kcb, seq, q, ws, tq_call_m
     exact = torch.empty(B, Hq, T, device="cuda")
     tq.tq_logits_dense(keys.to(torch.float32), B, Hq, Hkv, T, seq, q, exact)
     variants = {}
-    for name, bits, kind in (("prod_b4", 4, tq.KIND_PROD), ("mse_b4", 4, tq.KIND_MSE), ("mse_b3", 3, tq.KIND_MSE)):
-        cb = kcb if name == "prod_b4" else tq.Codebook(d, bits, kind)
+    for name, bits, kind, extra in (("prod_b4", 4, tq.KIND_PROD, 0), ("prod_b3.5", 3, tq.KIND_PROD, 32),
+                                    ("prod_b2.5", 2, tq.KIND_PROD, 32), ("mse_b4", 4, tq.KIND_MSE, 0),
+                                    ("mse_b3", 3, tq.KIND_MSE, 0)):
+        cb = kcb if name == "prod_b4" else tq.Codebook(d, bits, kind, extra=extra)
         fresh = torch.empty(tq.cache_bytes(cb, B * Hkv * T), dtype=torch.uint8, device="cuda")
         for h in range(Hkv):
             dst = torch.arange(h * T, (h + 1) * T, dtype=torch.int64, device="cuda")

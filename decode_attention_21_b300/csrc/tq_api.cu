@@ -136,11 +136,13 @@ void chunking(int B, int Hkv, int64_t capacity, int target, int* nchunks, int* t
   *nchunks = (int)((tiles + tpc - 1) / tpc);
 }
 
-tq_status check_scoring_codebook(const tq_codebook* cb, int kind, const char* what) {
+tq_status check_scoring_codebook(const tq_codebook* cb, int kind, const char* what, bool mixed_ok = false) {
   if (!cb) return fail(TQ_EINVAL, "%s: codebook is NULL", what);
   if (cb->dev.kind != kind) return fail(TQ_EINVAL, "%s: codebook has the wrong kind", what);
   if (cb->dev.d != 128) return fail(TQ_EUNSUPPORTED, "%s: only d = 128 is implemented", what);
-  if (cb->dev.extra != 0) return fail(TQ_EUNSUPPORTED, "%s: mixed-bit caches are not scored yet", what);
+  if (cb->dev.extra != 0 && !(mixed_ok && cb->dev.kind == TQ_KIND_PROD && cb->dev.mode == TQ_MODE_SCALAR &&
+                              cb->dev.extra <= 64))
+    return fail(TQ_EUNSUPPORTED, "%s: this mixed-bit cache is not scored here", what);
   int dev = -1;
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
@@ -270,6 +272,33 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
       }
       dv.vmask[v] = mask;
       dv.vcoef[v] = (float)(a / L);
+    }
+    // extended codebook: idx_x = (top << 1) | extra bit, plane p (p <= b1) is
+    // bit b1 - p of idx_x
+    dv.nvx = D.extra ? L : 0;
+    for (int v = 0; v < dv.nvx; ++v) {
+      const uint32_t mask = kOddMaskHost[v];
+      double a = 0.0;
+      for (int idx = 0; idx < 2 * L; ++idx) {
+        int par = 0;
+        for (int p = 0; p <= b1; ++p)
+          if (mask >> p & 1u) par ^= (idx >> (b1 - p)) & 1;
+        a += (par ? -1.0 : 1.0) * (double)dv.cent_x[idx];
+      }
+      dv.vcoef_x[v] = (float)(a / (2 * L));
+    }
+    for (int idx = 0; idx < (D.extra ? 2 * L : 0); ++idx) {
+      double r = 0.0;
+      for (int v = 0; v < dv.nvx; ++v) {
+        int par = 0;
+        for (int p = 0; p <= b1; ++p)
+          if (kOddMaskHost[v] >> p & 1u) par ^= (idx >> (b1 - p)) & 1;
+        r += (par ? -1.0 : 1.0) * dv.vcoef_x[v];
+      }
+      if (std::fabs(r - dv.cent_x[idx]) > 1e-6 * std::fabs(dv.cent_x[2 * L - 1])) {
+        delete cb;
+        return fail(TQ_EINVAL, "tq_make_codebook: extended centroid table is not symmetric");
+      }
     }
     // the expansion must reproduce every centroid (even subsets vanish for a
     // symmetric table)
@@ -502,7 +531,7 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
   tq_status st;
   // keys with the QJL term (PROD), or MSE-only keys in scalar mode
   if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD,
-                                   "tq_logits")) != TQ_OK)
+                                   "tq_logits", true)) != TQ_OK)
     return st;
   if (kcb->dev.kind == TQ_KIND_MSE && kcb->dev.mode != TQ_MODE_SCALAR)
     return fail(TQ_EUNSUPPORTED, "tq_logits: MSE-only keys are scored in scalar mode only");

@@ -20,6 +20,11 @@ struct Dev {
   float vcoef[kMaxL];     // yhat = sum_v vcoef[v] * (-1)^(xor of the subset's bits)
   float cent[kMaxL], bound[kMaxL];
   float cent_x[2 * kMaxL], bound_x[2 * kMaxL];
+  // extended (b' + 1)-bit codebook of the first `extra` coordinates: the
+  // Walsh-Hadamard coefficients of cent_x over the odd subsets of its b' + 1
+  // planes (plane b' = the extra bit), nvx = 2 nv of them
+  int nvx;
+  float vcoef_x[kMaxL];
   float qjl_const;        // sqrt(pi/2) / m
   // polar mode, per level l = 1..D (index l): boundary and centroid (cos, sin)
   float pb_cos[kMaxLevels][kMaxL], pb_sin[kMaxLevels][kMaxL];

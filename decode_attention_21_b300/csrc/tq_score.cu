@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   // this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float sq[d], part[2][4][32], sv[2][32];
-  __shared__ float red[4][4];   // [source rank][max |q'|, max |2 q''|, sum q', sum q'']
+  // [source rank][max |q'|, max |2 q''|, sum q', sum q'', sum of q' over extended-codebook coordinates]
+  __shared__ float red[4][5];
   const int tid = threadIdx.x;
   const int mat = tid >> 7, qt = (tid >> 5) & 3, o = tid & 31;
   // Pi^T (mat 0) or (S Pi)^T (mat 1): rows 32 qt .. 32 qt + 31, column 32 r + o;
@@ -121,20 +122,23 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
     if (o < 4) {
       cluster_st(&red[r][mm], (uint32_t)o, mx);
       cluster_st(&red[r][2 + mm], (uint32_t)o, sm);
+      if (mm == 0) cluster_st(&red[r][4], (uint32_t)o, (int)r < cb.extra / 32 ? sm : 0.f);
     }
   }
   cluster_sync();
   // every CTA combines the four partials in rank order (identical results)
-  float mx1 = 0.f, mx2 = 0.f, sm1 = 0.f, sm2 = 0.f;
+  float mx1 = 0.f, mx2 = 0.f, sm1 = 0.f, sm2 = 0.f, sm1x = 0.f;
   for (int k = 0; k < 4; ++k) {
     mx1 = fmaxf(mx1, red[k][0]);
     mx2 = fmaxf(mx2, red[k][1]);
     sm1 += red[k][2];
     sm2 += red[k][3];
+    sm1x += red[k][4];
   }
   const int nv = cb.nv;
-  float csum = 0.f;
+  float csum = 0.f, csumx = 0.f;
   for (int v = 0; v < nv; ++v) csum += cb.vcoef[v];
+  for (int u = 0; u < cb.nvx; ++u) csumx += cb.vcoef_x[u];
   // keep |B| <= 2^14 at the largest bit factor
   const float S1 = pow2_scale(mx1 * kMaxBitFactor, 16384.f), S2 = pow2_scale(mx2 * kMaxBitFactor, 16384.f);
   uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(d);
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   if (r == 0 && tid == 0) {
     hdr[slot] = live ? S1 : 0.f;
     hdr[4 + slot] = live ? S2 : 0.f;
-    hdr[8 + slot] = live ? csum * sm1 : 0.f;
+    hdr[8 + slot] = live ? fmaf(csumx - csum, sm1x, csum * sm1) : 0.f;
     hdr[12 + slot] = live ? -sm2 : 0.f;
   }
   // fragments of this word column (c = r) for this slot's lanes g = 2 slot + piece
@@ -181,6 +185,8 @@ struct QK16 {
   uint2 bq[1 + NQ][8];
   float S2, K1, K2;
   float cv[NV];
+  float cvx[2 * NV];   // coefficients of the extended (mixed-bit) codebook's planes
+  int c_;
 
   __device__ __forceinline__ void load(const uint8_t* blk, int lane, const Dev& cb) {
     const float* hdr = reinterpret_cast<const float*>(blk);
@@ -196,6 +202,9 @@ struct QK16 {
     K2 = hdr[12 + c];
 #pragma unroll
     for (int v = 0; v < NV; ++v) cv[v] = -2.f * cb.vcoef[v] * S1;
+#pragma unroll
+    for (int u = 0; u < 2 * NV; ++u) cvx[u] = -2.f * cb.vcoef_x[u] * S1;
+    c_ = c;
   }
 
   // wa[t], wb[t]: the P plane words (column c) of keys g and g+8 of tile t.
@@ -204,10 +213,47 @@ struct QK16 {
   template <int T>
   __device__ __forceinline__ void score(const uint32_t (&wa)[T][P], const uint32_t (&wb)[T][P], float (&s1)[T][2],
                                         float (&s2)[T][2]) const {
-    float a1[T][NV][C1][4], a2[T][2][4];
+    uint32_t z[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) z[t] = 0u;
+    score_mixed<T, 0>(wa, wb, z, z, s1, s2);
+  }
+
+  // Mixed-bit keys: the first EXT word columns (32 EXT coordinates) use the
+  // (b' + 1)-bit codebook, whose low bit is the extra word ea/eb of the
+  // column.  Lanes of those columns feed the 2 NV extended virtual planes and
+  // zeros to the main ones; the other lanes do the opposite.
+  template <int T, int EXT>
+  __device__ __forceinline__ void score_mixed(const uint32_t (&wa)[T][P], const uint32_t (&wb)[T][P],
+                                              const uint32_t (&ea)[T], const uint32_t (&eb)[T], float (&s1)[T][2],
+                                              float (&s2)[T][2]) const {
+    constexpr int NX = EXT ? 2 * NV : 0;
+    const bool xl = EXT > 0 && c_ < EXT;
+    float a1[T][NV][C1][4], a2[T][2][4], ax[T][NX > 0 ? NX : 1][4];
     uint32_t xa[T][NV + NQ], xb[T][NV + NQ], ya[T][NV + NQ], yb[T][NV + NQ];
+    uint32_t za[T][NX > 0 ? NX : 1], zb[T][NX > 0 ? NX : 1], wza[T][NX > 0 ? NX : 1], wzb[T][NX > 0 ? NX : 1];
 #pragma unroll
     for (int t = 0; t < T; ++t) {
+#pragma unroll
+      for (int u = 0; u < NX; ++u) {
+        uint32_t pa = 0, pb = 0;
+#pragma unroll
+        for (int p = 0; p < PS; ++p)
+          if (kOddMask[u] >> p & 1u) {
+            pa ^= wa[t][p];
+            pb ^= wb[t][p];
+          }
+        if (kOddMask[u] >> PS & 1u) {
+          pa ^= ea[t];
+          pb ^= eb[t];
+        }
+        za[t][u] = xl ? pa : 0u;
+        zb[t][u] = xl ? pb : 0u;
+        wza[t][u] = za[t][u] >> 4;
+        wzb[t][u] = zb[t][u] >> 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ax[t][u][e] = 0.f;
+      }
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         uint32_t pa = 0, pb = 0;
@@ -217,8 +263,8 @@ struct QK16 {
             pa ^= wa[t][p];
             pb ^= wb[t][p];
           }
-        xa[t][v] = pa;
-        xb[t][v] = pb;
+        xa[t][v] = xl ? 0u : pa;
+        xb[t][v] = xl ? 0u : pb;
 #pragma unroll
         for (int ch = 0; ch < C1; ++ch)
 #pragma unroll
@@ -252,6 +298,11 @@ struct QK16 {
           mma_f16(a1[t][v][kb % C1], bit_operand(xa[t][v], ya[t][v], b0), bit_operand(xb[t][v], yb[t][v], b0),
                   bit_operand(xa[t][v], ya[t][v], b1), bit_operand(xb[t][v], yb[t][v], b1), bq[0][kb].x,
                   bq[0][kb].y);
+#pragma unroll
+        for (int u = 0; u < NX; ++u)
+          mma_f16(ax[t][u], bit_operand(za[t][u], wza[t][u], b0), bit_operand(zb[t][u], wzb[t][u], b0),
+                  bit_operand(za[t][u], wza[t][u], b1), bit_operand(zb[t][u], wzb[t][u], b1), bq[0][kb].x,
+                  bq[0][kb].y);
       }
     }
 #pragma unroll
@@ -264,6 +315,11 @@ struct QK16 {
           ra = fmaf(cv[v], a1[t][v][ch][0] + a1[t][v][ch][1], ra);
           rb = fmaf(cv[v], a1[t][v][ch][2] + a1[t][v][ch][3], rb);
         }
+#pragma unroll
+      for (int u = 0; u < NX; ++u) {
+        ra = fmaf(cvx[u], ax[t][u][0] + ax[t][u][1], ra);
+        rb = fmaf(cvx[u], ax[t][u][2] + ax[t][u][3], rb);
+      }
       s1[t][0] = ra;
       s1[t][1] = rb;
       if constexpr (QJL) {
@@ -276,13 +332,16 @@ struct QK16 {
   }
 };
 
-template <int P>
+// The P plane words of word column c of a record.  Vector loads need the
+// record start aligned to 4 P bytes (records of exactly 4 P words); records
+// with extra-bit words (VEC = false) are read word by word.
+template <int P, bool VEC = true>
 __device__ __forceinline__ void load_words(const uint32_t* __restrict__ rec, int c, uint32_t (&w)[P]) {
   const uint32_t* p = rec + c * P;
-  if constexpr (P == 4) {
+  if constexpr (VEC && P == 4) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else if constexpr (P == 2) {
+  } else if constexpr (VEC && P == 2) {
     const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
     w[0] = v.x; w[1] = v.y;
   } else {
@@ -293,9 +352,10 @@ __device__ __forceinline__ void load_words(const uint32_t* __restrict__ rec, int
 
 // Key words and norms of one 16-key tile for thread (g, c).  The norm entry
 // is 4 bytes (n, gamma) with the QJL term, 2 bytes (n) without.
-template <int P, bool QJL = true>
+template <int P, bool QJL = true, int EXT = 0>
 struct KTile {
   uint32_t wa[P], wb[P];
+  uint32_t ea = 0, eb = 0;   // extra-bit words (word columns < EXT of mixed-bit keys)
   uint32_t na, nb;
   __device__ __forceinline__ static uint32_t norm_at(const uint32_t* nrm, int64_t row) {
     if constexpr (QJL) return __ldg(nrm + row);
@@ -305,7 +365,8 @@ struct KTile {
                                        int64_t L, int c) {
     const int64_t tb = ta + 8;
     if (ta < L) {
-      load_words<P>(recs + (rowbase + ta) * W, c, wa);
+      load_words<P, EXT == 0>(recs + (rowbase + ta) * W, c, wa);
+      if (EXT && c < EXT) ea = __ldg(recs + (rowbase + ta) * W + 4 * P + c);
       na = norm_at(nrm, rowbase + ta);
     } else {
 #pragma unroll
@@ -313,7 +374,8 @@ struct KTile {
       na = 0;
     }
     if (tb < L) {
-      load_words<P>(recs + (rowbase + tb) * W, c, wb);
+      load_words<P, EXT == 0>(recs + (rowbase + tb) * W, c, wb);
+      if (EXT && c < EXT) eb = __ldg(recs + (rowbase + tb) * W + 4 * P + c);
       nb = norm_at(nrm, rowbase + tb);
     } else {
 #pragma unroll
@@ -346,7 +408,7 @@ __device__ __forceinline__ float est_key(uint32_t nrm_bits, float s1, float s2, 
 // Logits: grid (chunks, Hkv, B), 4 warps; each warp scores 16-key tiles,
 // prefetching its next tile while scoring the current one.
 // ---------------------------------------------------------------------------
-template <int NV, int P, bool QJL>
+template <int NV, int P, bool QJL, int EXT>
 __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
                                                 int64_t capacity, int64_t cache_rows,
                                                 const int32_t* __restrict__ seq_lens,
@@ -369,7 +431,7 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
   const float kq = cb.qjl_const;
   const int W = cb.W;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
-  KTile<P, QJL> cur, nxt;
+  KTile<P, QJL, EXT> cur, nxt;
   int64_t tile = tile0 + warp;
   cur.load(recs, nrm, W, rowbase, tile * 16 + g, L, c);
   for (; tile < tend; tile += 4) {
@@ -382,7 +444,8 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
       wb[0][p] = cur.wb[p];
     }
     float s1[1][2], s2[1][2];
-    qk.template score<1>(wa, wb, s1, s2);
+    const uint32_t ea[1] = {cur.ea}, eb[1] = {cur.eb};
+    qk.template score_mixed<1, EXT>(wa, wb, ea, eb, s1, s2);
     const int64_t ta = tile * 16 + g, tb = ta + 8;
     if (c < G) {
       if (ta < L) out[ta] = est_key<QJL>(cur.na, s1[0][0], s2[0][0], kq);
@@ -407,15 +470,15 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
 // (bounded) for its copies in flight and returns.
 // ---------------------------------------------------------------------------
 
-template <int NV, int P, bool QJL>
+template <int NV, int P, bool QJL, int EXT>
 __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
                                                        int Hkv, int64_t capacity, int64_t cache_rows,
                                                        const int32_t* __restrict__ seq_lens,
                                                        const uint8_t* __restrict__ prep, float* __restrict__ logits,
                                                        int tiles_per_cta, int* __restrict__ status) {
-  constexpr int RB = 16 * P;                 // record bytes at d = 128
+  constexpr int RB = 16 * P + 4 * EXT;       // record bytes at d = 128 (+ extra-bit words)
   constexpr int NB = QJL ? 4 : 2;            // norm entry bytes
-  constexpr int kPairs = NV <= 4;            // two tiles per warp step (registers permitting)
+  constexpr int kPairs = NV <= 4 && EXT == 0;  // two tiles per warp step (registers permitting)
   constexpr int kStageRec = kStageTiles * 16 * RB, kStageNrm = kStageTiles * 16 * NB;
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ __align__(8) uint64_t bars[kRing];
@@ -477,10 +540,15 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   bool ok = true;
   int pending_from = 0;                      // first stage whose copy may still be in flight
   auto tile_words = [&](const uint8_t* rec, const uint8_t* nrm, int lt, int64_t tg, uint32_t(&wa)[P],
-                        uint32_t(&wb)[P], uint32_t& na, uint32_t& nb) {
+                        uint32_t(&wb)[P], uint32_t& na, uint32_t& nb, uint32_t& ea, uint32_t& eb) {
     const uint8_t* ra = rec + ((size_t)lt * 16 + g) * RB + c * P * 4;
     const uint8_t* rbp = ra + 8 * RB;
-    if constexpr (P == 4) {
+    ea = eb = 0u;
+    if (EXT && c < EXT) {
+      ea = reinterpret_cast<const uint32_t*>(rec + ((size_t)lt * 16 + g) * RB + 16 * P)[c];
+      eb = reinterpret_cast<const uint32_t*>(rec + ((size_t)lt * 16 + g + 8) * RB + 16 * P)[c];
+    }
+    if constexpr (P == 4 && EXT == 0) {
       const uint4 x = *reinterpret_cast<const uint4*>(ra);
       const uint4 y = *reinterpret_cast<const uint4*>(rbp);
       wa[0] = x.x; wa[1] = x.y; wa[2] = x.z; wa[3] = x.w;
@@ -503,10 +571,12 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     if (ta >= L) {
 #pragma unroll
       for (int p = 0; p < P; ++p) wa[p] = 0;
+      ea = 0u;
     }
     if (ta + 8 >= L) {
 #pragma unroll
       for (int p = 0; p < P; ++p) wb[p] = 0;
+      eb = 0u;
     }
   };
   auto emit = [&](int64_t tg, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
@@ -531,23 +601,23 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     for (int lt = warp; lt < n_here; lt += 8) {
       const int lt2 = lt + 4;
       if (kPairs && lt2 < n_here) {
-        uint32_t wa[2][P], wb[2][P], na, nb, ma, mb;
-        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb);
-        tile_words(rec, nrm, lt2, tile0 + t_a + lt2, wa[1], wb[1], ma, mb);
+        uint32_t wa[2][P], wb[2][P], na, nb, ma, mb, ea[2], eb[2];
+        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb, ea[0], eb[0]);
+        tile_words(rec, nrm, lt2, tile0 + t_a + lt2, wa[1], wb[1], ma, mb, ea[1], eb[1]);
         float s1[2][2], s2[2][2];
-        qk.template score<2>(wa, wb, s1, s2);
+        qk.template score_mixed<2, EXT>(wa, wb, ea, eb, s1, s2);
         emit(tile0 + t_a + lt, na, nb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
         emit(tile0 + t_a + lt2, ma, mb, s1[1][0], s1[1][1], s2[1][0], s2[1][1]);
       } else {
-        uint32_t wa[1][P], wb[1][P], na, nb;
-        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb);
+        uint32_t wa[1][P], wb[1][P], na, nb, ea[1], eb[1];
+        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb, ea[0], eb[0]);
         float s1[1][2], s2[1][2];
-        qk.template score<1>(wa, wb, s1, s2);
+        qk.template score_mixed<1, EXT>(wa, wb, ea, eb, s1, s2);
         emit(tile0 + t_a + lt, na, nb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
         if (!kPairs && lt2 < n_here) {
           uint32_t xa[1][P], xb[1][P], ma, mb;
-          tile_words(rec, nrm, lt2, tile0 + t_a + lt2, xa[0], xb[0], ma, mb);
-          qk.template score<1>(xa, xb, s1, s2);
+          tile_words(rec, nrm, lt2, tile0 + t_a + lt2, xa[0], xb[0], ma, mb, ea[0], eb[0]);
+          qk.template score_mixed<1, EXT>(xa, xb, ea, eb, s1, s2);
           emit(tile0 + t_a + lt2, ma, mb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
         }
       }
@@ -1053,42 +1123,50 @@ cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, u
 }
 
 // Key caches with the QJL term (PROD) use b' = 1..3 code planes + the sign
-// plane; MSE-only key caches use b = 1..4 code planes.
+// plane, optionally with 1 or 2 extra-bit word columns (mixed-bit caches);
+// MSE-only key caches use b = 1..4 code planes.
 #define TQ_LOGITS_DISPATCH(CALL)                          \
   if (cb.kind == 0) {                                     \
-    switch (cb.b1) {                                      \
-      case 1: CALL(1, 2, true);                           \
-      case 2: CALL(2, 3, true);                           \
-      default: CALL(4, 4, true);                          \
+    const int ext = cb.extra / 32;                        \
+    switch (cb.b1 * 4 + ext) {                            \
+      case 4: CALL(1, 2, true, 0);                        \
+      case 5: CALL(1, 2, true, 1);                        \
+      case 6: CALL(1, 2, true, 2);                        \
+      case 8: CALL(2, 3, true, 0);                        \
+      case 9: CALL(2, 3, true, 1);                        \
+      case 10: CALL(2, 3, true, 2);                       \
+      case 13: CALL(4, 4, true, 1);                       \
+      case 14: CALL(4, 4, true, 2);                       \
+      default: CALL(4, 4, true, 0);                       \
     }                                                     \
   }                                                       \
   switch (cb.b1) {                                        \
-    case 1: CALL(1, 1, false);                            \
-    case 2: CALL(2, 2, false);                            \
-    case 3: CALL(4, 3, false);                            \
-    default: CALL(8, 4, false);                           \
+    case 1: CALL(1, 1, false, 0);                         \
+    case 2: CALL(2, 2, false, 0);                         \
+    case 3: CALL(4, 3, false, 0);                         \
+    default: CALL(8, 4, false, 0);                        \
   }
 
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks,
                           int tpc, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
-#define TQ_CALL(NV, P, Q)                                                                                 \
-  k_logits<NV, P, Q><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); \
+#define TQ_CALL(NV, P, Q, X)                                                                                 \
+  k_logits<NV, P, Q, X><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); \
   return cudaGetLastError()
   TQ_LOGITS_DISPATCH(TQ_CALL)
 #undef TQ_CALL
 }
 
-template <int NV, int P, bool QJL>
+template <int NV, int P, bool QJL, int EXT>
 static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                                    int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                                    int nchunks, int tpc, int* status, cudaStream_t s) {
-  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + (QJL ? 4 : 2));
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + 4 * EXT + (QJL ? 4 : 2));
   static cudaError_t configured = [] {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_logits_staged<NV, P, QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_logits_staged<NV, P, QJL>));
+    cudaError_t e = cudaFuncSetAttribute(k_logits_staged<NV, P, QJL, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_logits_staged<NV, P, QJL, EXT>));
     return e;
   }();
   if (configured != cudaSuccess) return configured;
@@ -1102,15 +1180,15 @@ static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P, QJL>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep,
+  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P, QJL, EXT>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep,
                             logits, tpc, status);
 }
 
 cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                                  int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                                  int nchunks, int tpc, int* status, cudaStream_t s) {
-#define TQ_CALL(NV, P, Q) \
-  return logits_staged_t<NV, P, Q>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s)
+#define TQ_CALL(NV, P, Q, X) \
+  return logits_staged_t<NV, P, Q, X>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s)
   TQ_LOGITS_DISPATCH(TQ_CALL)
 #undef TQ_CALL
 }

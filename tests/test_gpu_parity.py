@@ -183,6 +183,30 @@ def test_logits_parity_mse_only_keys(bits, B, Hq, Hkv, cap, lens):
             rowwise_ok(got[b, :, :L], ref[b, :, :L])
 
 
+@pytest.mark.parametrize("bits,extra", [(2, 32), (3, 32), (2, 64), (3, 64), (4, 32)])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 8, 2, 4096, [4096]), (3, 6, 3, 333, [333, 17, 0])])
+def test_logits_parity_mixed_bits(bits, extra, B, Hq, Hkv, cap, lens):
+    """Mixed-bit keys (2.5 / 3.5-bit points): the first `extra` rotated
+    coordinates carry one more stage-1 bit."""
+    ocb, gcb = pair(128, bits, extra=extra)
+    rows = B * Hkv * cap
+    x = wl.gaussian_outlier_keys(rows, 128)
+    code, img = oracle_cache(ocb, rows, x.astype(np.float64))
+    q = wl.queries((B, Hq, 128), name="tiny_q")
+    ref = estimate.logits(ocb, code, q.astype(np.float64), lens, Hkv, cap)
+    ws = torch.empty(tq.tq_logits_workspace(gcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    tq.tq_logits(gcb, torch.from_numpy(img).cuda(), B, Hq, Hkv, cap, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                 torch.from_numpy(q).cuda(), out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        L = lens[b]
+        assert np.all(np.isnan(got[b, :, L:]))
+        if L:
+            rowwise_ok(got[b, :, :L], ref[b, :, :L])
+
+
 def tiled_code(code, reps):
     """The oracle's code arrays repeated ``reps`` times along the rows."""
     n = code["n"].shape[0]
