@@ -27,6 +27,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kD = 256;
 constexpr int kMaxK = 32;
+constexpr int kRound = 4;   // 16-row tiles per exchange between the two coordinate halves
 __device__ constexpr uint32_t kOddMask[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -159,20 +160,20 @@ __global__ void __launch_bounds__(1024) k_search_prep(const Dev cb, const float*
 // Scan: 8 warps = 4 query groups x 2 coordinate halves.  Warp (grp_local,
 // half) holds the fragments of k-blocks 8 half .. 8 half + 7 (word c + 4 half).
 template <int NV, int P>
-__global__ void __launch_bounds__(256, 1) k_search(const Dev cb, const uint8_t* __restrict__ db, int64_t n_db,
+__global__ void __launch_bounds__(256, P <= 3 ? 2 : 1) k_search(const Dev cb, const uint8_t* __restrict__ db, int64_t n_db,
                                                    const uint8_t* __restrict__ prep, int nq, int k,
                                                    int32_t* __restrict__ ids, float* __restrict__ scores) {
-  __shared__ float xch[4][4][32];             // [group][acc element][lane]
-  __shared__ float top_s[16][kMaxK];
-  __shared__ int32_t top_i[16][kMaxK];
-  __shared__ int top_n[16];
+  __shared__ float xch[2][4][kRound][4][32];  // [buffer][group][tile of the round][acc element][lane]
+  __shared__ float top_s[2][16][kMaxK];       // [coordinate half][query slot][rank]
+  __shared__ int32_t top_i[2][16][kMaxK];
+  __shared__ int top_n[2][16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gl = warp >> 1, half = warp & 1;
   const int grp = blockIdx.x * 4 + gl;
   const int ngroups = (nq + 3) / 4;
   const int g = lane >> 2, c = lane & 3;
   const bool live = grp < ngroups;
-  if (threadIdx.x < 16) top_n[threadIdx.x] = 0;
+  if (threadIdx.x < 32) top_n[threadIdx.x >> 4][threadIdx.x & 15] = 0;
   uint2 bq[NV + 1][8];
   float S1 = 0.f, S2 = 0.f, K1 = 0.f, K2 = 0.f;
   if (live) {
@@ -196,101 +197,156 @@ __global__ void __launch_bounds__(256, 1) k_search(const Dev cb, const uint8_t* 
   const int word = c + 4 * half;
   const int qslot = gl * 4 + c;               // this thread's query (shared-memory list index)
   const int64_t ntiles = (n_db + 15) / 16;
-  for (int64_t tile = 0; tile < ntiles; ++tile) {
+  // words and norms of one tile, loaded one tile ahead of use
+  uint32_t nwa[P], nwb[P], nna = 0u, nnb = 0u;
+  auto fetch = [&](int64_t tile) {
     const int64_t ta = tile * 16 + g, tb = ta + 8;
-    float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-    if (live) {
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      nwa[p] = (live && ta < n_db) ? __ldg(recs + ta * W + word * P + p) : 0u;
+      nwb[p] = (live && tb < n_db) ? __ldg(recs + tb * W + word * P + p) : 0u;
+    }
+    nna = (live && ta < n_db) ? __ldg(nrm + ta) : 0u;
+    nnb = (live && tb < n_db) ? __ldg(nrm + tb) : 0u;
+  };
+  fetch(0);
+  // rounds of kRound tiles: each half scores its coordinates of the round's
+  // tiles, the two halves of a group meet once per round
+  for (int64_t t0 = 0; t0 < ntiles; t0 += kRound) {
+    float part[kRound][4];
+    uint32_t nra[kRound], nrb[kRound];
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+      const int64_t tile = t0 + u;
       uint32_t wa[P], wb[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) {
-        wa[p] = ta < n_db ? __ldg(recs + ta * W + word * P + p) : 0u;
-        wb[p] = tb < n_db ? __ldg(recs + tb * W + word * P + p) : 0u;
+        wa[p] = nwa[p];
+        wb[p] = nwb[p];
       }
+      nra[u] = nna;
+      nrb[u] = nnb;
+      if (tile + 1 < ntiles) fetch(tile + 1);
+      float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      if (live && tile < ntiles) {
 #pragma unroll
-      for (int v = 0; v <= NV; ++v) {
-        uint32_t xa = 0, xb = 0;
-        if (v < NV) {
+        for (int v = 0; v <= NV; ++v) {
+          uint32_t xa = 0, xb = 0;
+          if (v < NV) {
 #pragma unroll
-          for (int p = 0; p < P - 1; ++p)
-            if (kOddMask[v] >> p & 1u) {
-              xa ^= wa[p];
-              xb ^= wb[p];
-            }
-        } else {
-          xa = wa[P - 1];
-          xb = wb[P - 1];
-        }
-        uint32_t ra[16], rb[16];
-        expand16(xa, ra);
-        expand16(xb, rb);
-        float(&acc)[4] = v < NV ? acc1 : acc2;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb)
-          mma_f16(acc, ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
-      }
-    }
-    // combine the two coordinate halves of the group
-    if (half == 1) {
-      xch[gl][0][lane] = (acc1[0] + acc1[1]);
-      xch[gl][1][lane] = (acc1[2] + acc1[3]);
-      xch[gl][2][lane] = (acc2[0] + acc2[1]);
-      xch[gl][3][lane] = (acc2[2] + acc2[3]);
-    }
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + gl));
-    if (half == 0 && live) {
-      const float m1a = (acc1[0] + acc1[1]) + xch[gl][0][lane];
-      const float m1b = (acc1[2] + acc1[3]) + xch[gl][1][lane];
-      const float m2a = (acc2[0] + acc2[1]) + xch[gl][2][lane];
-      const float m2b = (acc2[2] + acc2[3]) + xch[gl][3][lane];
-      const uint32_t na = ta < n_db ? __ldg(nrm + ta) : 0u, nb = tb < n_db ? __ldg(nrm + tb) : 0u;
-      const __half2 ha = *reinterpret_cast<const __half2*>(&na);
-      const __half2 hb = *reinterpret_cast<const __half2*>(&nb);
-      const float sa = __low2float(ha) * fmaf(__high2float(ha) * kq, fmaf(S2, m2a, K2), fmaf(S1, m1a, K1));
-      const float sb = __low2float(hb) * fmaf(__high2float(hb) * kq, fmaf(S2, m2b, K2), fmaf(S1, m1b, K1));
-      const bool qok = grp * 4 + c < nq;
-      // candidates: beat the current k-th score of their query
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float sc = h == 0 ? sa : sb;
-        const int64_t id = h == 0 ? ta : tb;
-        const int cnt = top_n[qslot];
-        const bool cand = qok && id < n_db && (cnt < k || sc > top_s[qslot][k - 1]);
-        unsigned mask = __ballot_sync(kFull, cand);
-        while (mask) {
-          const int src = __ffs(mask) - 1;
-          mask &= mask - 1;
-          const float s_new = __shfl_sync(kFull, sc, src);
-          const int id_new = (int)__shfl_sync(kFull, (int)id, src);
-          const int qs = __shfl_sync(kFull, qslot, src);
-          if (lane == 0) {
-            // insert into the sorted list of query qs (decreasing score, ties keep the earlier id first)
-            int n0 = top_n[qs];
-            if (n0 < k || s_new > top_s[qs][k - 1]) {
-              int pos = n0 < k ? n0 : k - 1;
-              while (pos > 0 && top_s[qs][pos - 1] < s_new) {
-                top_s[qs][pos] = top_s[qs][pos - 1];
-                top_i[qs][pos] = top_i[qs][pos - 1];
-                --pos;
+            for (int p = 0; p < P - 1; ++p)
+              if (kOddMask[v] >> p & 1u) {
+                xa ^= wa[p];
+                xb ^= wb[p];
               }
-              top_s[qs][pos] = s_new;
-              top_i[qs][pos] = id_new;
-              if (n0 < k) top_n[qs] = n0 + 1;
-            }
+          } else {
+            xa = wa[P - 1];
+            xb = wb[P - 1];
           }
-          __syncwarp();
+          uint32_t ra[16], rb[16];
+          expand16(xa, ra);
+          expand16(xb, rb);
+          float(&acc)[4] = v < NV ? acc1 : acc2;
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb)
+            mma_f16(acc, ra[2 * kb], rb[2 * kb], ra[2 * kb + 1], rb[2 * kb + 1], bq[v][kb].x, bq[v][kb].y);
+        }
+      }
+      part[u][0] = acc1[0] + acc1[1];
+      part[u][1] = acc1[2] + acc1[3];
+      part[u][2] = acc2[0] + acc2[1];
+      part[u][3] = acc2[2] + acc2[3];
+    }
+    // combine the two coordinate halves of the group: half h finishes tiles
+    // u with u / (kRound / 2) == h of the round, using the other half's
+    // partials from the exchange buffer (double-buffered: one barrier per round)
+    const int buf = (int)((t0 / kRound) & 1);
+#pragma unroll
+    for (int u = 0; u < kRound; ++u)
+      if (u / (kRound / 2) != half)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xch[buf][gl][u][e][lane] = part[u][e];
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + gl));
+    if (live) {
+      const bool qok = grp * 4 + c < nq;
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        if (u / (kRound / 2) != half) continue;
+        const int64_t ta = (t0 + u) * 16 + g, tb = ta + 8;
+        const float m1a = part[u][0] + xch[buf][gl][u][0][lane];
+        const float m1b = part[u][1] + xch[buf][gl][u][1][lane];
+        const float m2a = part[u][2] + xch[buf][gl][u][2][lane];
+        const float m2b = part[u][3] + xch[buf][gl][u][3][lane];
+        const __half2 ha = *reinterpret_cast<const __half2*>(&nra[u]);
+        const __half2 hb = *reinterpret_cast<const __half2*>(&nrb[u]);
+        const float sa = __low2float(ha) * fmaf(__high2float(ha) * kq, fmaf(S2, m2a, K2), fmaf(S1, m1a, K1));
+        const float sb = __low2float(hb) * fmaf(__high2float(hb) * kq, fmaf(S2, m2b, K2), fmaf(S1, m1b, K1));
+        float* ls = top_s[half][0];
+        int32_t* li = top_i[half][0];
+        int* ln = top_n[half];
+        // candidates: beat the current k-th score of their query in this half's list
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float sc = h == 0 ? sa : sb;
+          const int64_t id = h == 0 ? ta : tb;
+          const int cnt = ln[qslot];
+          const bool cand = qok && id < n_db && (cnt < k || sc > ls[qslot * kMaxK + k - 1]);
+          unsigned mask = __ballot_sync(kFull, cand);
+          while (mask) {
+            const int src = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const float s_new = __shfl_sync(kFull, sc, src);
+            const int id_new = (int)__shfl_sync(kFull, (int)id, src);
+            const int qs = __shfl_sync(kFull, qslot, src);
+            if (lane == 0) {
+              // insert into the sorted list of query qs (decreasing score; the
+              // list receives increasing ids, so ties keep the earlier id first)
+              float* sq = ls + qs * kMaxK;
+              int32_t* iq = li + qs * kMaxK;
+              int n0 = ln[qs];
+              if (n0 < k || s_new > sq[k - 1]) {
+                int pos = n0 < k ? n0 : k - 1;
+                while (pos > 0 && sq[pos - 1] < s_new) {
+                  sq[pos] = sq[pos - 1];
+                  iq[pos] = iq[pos - 1];
+                  --pos;
+                }
+                sq[pos] = s_new;
+                iq[pos] = id_new;
+                if (n0 < k) ln[qs] = n0 + 1;
+              }
+            }
+            __syncwarp();
+          }
         }
       }
     }
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + gl));
   }
   __syncthreads();
+  // merge the two halves' lists of each query (decreasing score, ties to the smaller id)
   if (half == 0 && live && lane < 4) {
     const int qi = grp * 4 + lane;
     if (qi < nq) {
       const int qs = gl * 4 + lane;
+      const int na = top_n[0][qs], nb = top_n[1][qs];
+      int ia = 0, ib = 0;
       for (int j = 0; j < k; ++j) {
-        ids[(size_t)qi * k + j] = j < top_n[qs] ? top_i[qs][j] : -1;
-        scores[(size_t)qi * k + j] = j < top_n[qs] ? top_s[qs][j] : -INFINITY;
+        bool take_a;
+        if (ia < na && ib < nb) {
+          const float sa = top_s[0][qs][ia], sb = top_s[1][qs][ib];
+          take_a = sa > sb || (sa == sb && top_i[0][qs][ia] < top_i[1][qs][ib]);
+        } else {
+          take_a = ia < na;
+        }
+        const bool have = ia < na || ib < nb;
+        const float sc = !have ? -INFINITY : take_a ? top_s[0][qs][ia] : top_s[1][qs][ib];
+        const int32_t id = !have ? -1 : take_a ? top_i[0][qs][ia] : top_i[1][qs][ib];
+        if (have) {
+          if (take_a) ++ia;
+          else ++ib;
+        }
+        ids[(size_t)qi * k + j] = id;
+        scores[(size_t)qi * k + j] = sc;
       }
     }
   }
