@@ -440,7 +440,10 @@ tq_status tq_check_device(const tq_codebook* cb) {
   if (flag) {
     const int zero = 0;
     cudaMemcpy(cb->d_status, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    return fail(TQ_ETIMEOUT, "tq_check_device: a kernel's bounded wait on its copies or MMAs gave up");
+    if (flag & ~tq::kBadRow)
+      return fail(TQ_ETIMEOUT, "tq_check_device: a kernel's bounded wait on its copies or MMAs gave up");
+    return fail(TQ_EINVAL, "tq_check_device: an append destination or a block-table entry lay outside the cache "
+                           "(those writes were skipped; reads of such a page went to page 0)");
   }
   return ok();
 }
@@ -469,12 +472,13 @@ size_t tq_cache_bytes(const tq_codebook* cb, int64_t rows) {
 
 static tq_status quantize_common(const char* what, const tq_codebook* cb, void* cache, int64_t cache_rows,
                                  const void* x, int32_t x_dtype, int64_t n, int32_t d_in, const float* y,
-                                 const float* norms, const int64_t* dst_rows, void* stream) {
+                                 const float* norms, const int64_t* dst_rows, void* stream,
+                                 const tq::AppendDst* paged = nullptr) {
   if (!cb) return fail(TQ_EINVAL, "%s: codebook is NULL", what);
   if (n < 0 || cache_rows < 0) return fail(TQ_EINVAL, "%s: negative size", what);
   if (n == 0) return ok();
   if (!cache || !aligned16(cache)) return fail(TQ_EINVAL, "%s: cache must be a 16-byte aligned device pointer", what);
-  if (!dst_rows && n > cache_rows) return fail(TQ_EINVAL, "%s: n = %lld rows exceed cache_rows = %lld", what, (long long)n, (long long)cache_rows);
+  if (!dst_rows && !paged && n > cache_rows) return fail(TQ_EINVAL, "%s: n = %lld rows exceed cache_rows = %lld", what, (long long)n, (long long)cache_rows);
   if (!y) {
     if (!x) return fail(TQ_EINVAL, "%s: x is NULL", what);
     if (x_dtype != TQ_F32 && x_dtype != TQ_BF16) return fail(TQ_EINVAL, "%s: bad dtype %d", what, x_dtype);
@@ -487,15 +491,19 @@ static tq_status quantize_common(const char* what, const tq_codebook* cb, void* 
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // bf16 batches in scalar mode: tensor-core rotation and sketch
-  if (!y && x_dtype == TQ_BF16 && cb->tc_ready && n >= 2048 && d_in % 8 == 0 && aligned16(x) && n < (1ll << 31)) {
+  if (!paged && !y && x_dtype == TQ_BF16 && cb->tc_ready && n >= 2048 && d_in % 8 == 0 && aligned16(x) &&
+      n < (1ll << 31)) {
     CUtensorMap tm_x;
     if (encode_bf16_rows(&tm_x, x, n, d_in))
       return launched(what, tq::launch_quantize_tc(tm_x, cb->tm_pihi, cb->tm_pilo, cb->tm_s, cb->dev,
                                                    static_cast<uint8_t*>(cache), cache_rows, n, dst_rows,
                                                    cb->d_status, cb->sms, s));
   }
+  tq::AppendDst dst = {};
+  dst.rows = dst_rows;
+  if (paged) dst = *paged;
   return launched(what, tq::launch_quantize_simt(cb->dev, static_cast<uint8_t*>(cache), cache_rows, x, x_dtype, n,
-                                                 d_in, y, norms, dst_rows, s));
+                                                 d_in, y, norms, dst, cb->d_status, s));
 }
 
 tq_status tq_quantize(const tq_codebook* cb, void* cache, int64_t cache_rows, const void* x, int32_t x_dtype,
@@ -525,40 +533,95 @@ static tq_status check_heads(const char* what, int32_t B, int32_t Hq, int32_t Hk
   return TQ_OK;
 }
 
-tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
-                    const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
-                    void* stream) {
+static tq_status logits_common(const char* what, const tq_codebook* kcb, const void* kcache, int64_t rows,
+                               const tq::RowMap& map, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
+                               const int32_t* seq_lens, const float* q, float* logits, void* workspace,
+                               size_t ws_bytes, void* stream) {
   tq_status st;
   // keys with the QJL term (PROD), or MSE-only keys in scalar mode
-  if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD,
-                                   "tq_logits", true)) != TQ_OK)
+  if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD, what,
+                                   true)) != TQ_OK)
     return st;
   if (kcb->dev.kind == TQ_KIND_MSE && kcb->dev.mode != TQ_MODE_SCALAR)
-    return fail(TQ_EUNSUPPORTED, "tq_logits: MSE-only keys are scored in scalar mode only");
-  if ((st = check_heads("tq_logits", B, Hq, Hkv, capacity)) != TQ_OK) return st;
+    return fail(TQ_EUNSUPPORTED, "%s: MSE-only keys are scored in scalar mode only", what);
+  if (map.table && kcb->dev.mode != TQ_MODE_SCALAR)
+    return fail(TQ_EUNSUPPORTED, "%s: paged logits are implemented for scalar-mode keys only", what);
+  if ((st = check_heads(what, B, Hq, Hkv, capacity)) != TQ_OK) return st;
   if (capacity == 0) return ok();
-  if (!kcache || !seq_lens || !q || !logits || !workspace)
-    return fail(TQ_EINVAL, "tq_logits: NULL device pointer");
+  if (!kcache || !seq_lens || !q || !logits || !workspace) return fail(TQ_EINVAL, "%s: NULL device pointer", what);
   if (!aligned16(kcache) || !aligned16(q) || !aligned16(logits) || !aligned16(workspace))
-    return fail(TQ_EINVAL, "tq_logits: device pointers must be 16-byte aligned");
-  if (ws_bytes < tq_logits_workspace(kcb, B, Hq, Hkv)) return fail(TQ_ENOMEM, "tq_logits: workspace too small");
+    return fail(TQ_EINVAL, "%s: device pointers must be 16-byte aligned", what);
+  if (ws_bytes < tq_logits_workspace(kcb, B, Hq, Hkv)) return fail(TQ_ENOMEM, "%s: workspace too small", what);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   int nchunks, tpc;
   chunking(B, Hkv, capacity, kLogitsCtas, &nchunks, &tpc);
-  const int64_t rows = (int64_t)B * Hkv * capacity;
   if (kcb->dev.mode == TQ_MODE_POLAR) {
-    if ((st = launched("tq_logits/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
-    return launched("tq_logits", tq::launch_logits_polar(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
-                                                         capacity, rows, seq_lens, prep, logits, nchunks, tpc, s));
+    if ((st = launched(what, tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+    return launched(what, tq::launch_logits_polar(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                  capacity, rows, seq_lens, prep, logits, nchunks, tpc, s));
   }
-  if ((st = launched("tq_logits/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+  if ((st = launched(what, tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
   if (capacity % 16 == 0)
-    return launched("tq_logits", tq::launch_logits_staged(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
-                                                          capacity, rows, seq_lens, prep, logits, nchunks, tpc,
-                                                          kcb->d_status, s));
-  return launched("tq_logits", tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
-                                                 rows, seq_lens, prep, logits, nchunks, tpc, s));
+    return launched(what, tq::launch_logits_staged(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                   capacity, rows, map, seq_lens, prep, logits, nchunks, tpc,
+                                                   kcb->d_status, s));
+  return launched(what, tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
+                                          rows, seq_lens, prep, logits, nchunks, tpc, s));
+}
+
+tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
+                    const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  return logits_common("tq_logits", kcb, kcache, (int64_t)B * Hkv * capacity, tq::RowMap{}, B, Hq, Hkv, capacity,
+                       seq_lens, q, logits, workspace, ws_bytes, stream);
+}
+
+// Paged layout arguments shared by the *_paged entry points.
+static tq_status check_paged(const char* what, int32_t num_pages, int32_t page_size, const int32_t* block_table,
+                             int32_t max_pages, int32_t Hkv, tq::RowMap* map) {
+  if (!block_table) return fail(TQ_EINVAL, "%s: block_table is NULL", what);
+  if (page_size < 16 || page_size % 16 || page_size > (1 << 20))
+    return fail(TQ_EINVAL, "%s: page_size = %d must be a positive multiple of 16 (at most 2^20)", what, page_size);
+  if (num_pages < 1 || max_pages < 1) return fail(TQ_EINVAL, "%s: num_pages and max_pages must be positive", what);
+  if (Hkv < 1 || (int64_t)num_pages * Hkv * page_size >= (1ll << 40))
+    return fail(TQ_EINVAL, "%s: cache too large", what);
+  map->table = block_table;
+  map->page = page_size;
+  map->max_pages = max_pages;
+  map->num_pages = num_pages;
+  return TQ_OK;
+}
+
+tq_status tq_logits_paged(const tq_codebook* kcb, const void* kcache, int32_t num_pages, int32_t page_size,
+                          const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq, int32_t Hkv,
+                          const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  tq::RowMap map;
+  tq_status st = check_paged("tq_logits_paged", num_pages, page_size, block_table, max_pages, Hkv, &map);
+  if (st != TQ_OK) return st;
+  return logits_common("tq_logits_paged", kcb, kcache, (int64_t)num_pages * Hkv * page_size, map, B, Hq, Hkv,
+                       (int64_t)max_pages * page_size, seq_lens, q, logits, workspace, ws_bytes, stream);
+}
+
+tq_status tq_append_paged(const tq_codebook* cb, void* cache, int32_t num_pages, int32_t page_size,
+                          const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hkv,
+                          const int32_t* seq_lens, const void* x, int32_t x_dtype, int32_t d_in, void* stream) {
+  tq::AppendDst dst = {};
+  tq_status st = check_paged("tq_append_paged", num_pages, page_size, block_table, max_pages, Hkv, &dst.map);
+  if (st != TQ_OK) return st;
+  if (!cb) return fail(TQ_EINVAL, "tq_append_paged: codebook is NULL");
+  if (B < 1 || B > 65535) return fail(TQ_EINVAL, "tq_append_paged: bad B = %d", B);
+  if (!seq_lens) return fail(TQ_EINVAL, "tq_append_paged: seq_lens is NULL");
+  dst.seq_lens = seq_lens;
+  dst.Hkv = Hkv;
+  return quantize_common("tq_append_paged", cb, cache, (int64_t)num_pages * Hkv * page_size, x, x_dtype,
+                         (int64_t)B * Hkv, d_in, nullptr, nullptr, nullptr, stream, &dst);
+}
+
+tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* stream) {
+  if (!seq_lens || B < 1) return fail(TQ_EINVAL, "tq_advance_lengths: bad arguments");
+  return launched("tq_advance_lengths", tq::launch_advance_lengths(seq_lens, B, delta, static_cast<cudaStream_t>(stream)));
 }
 
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
@@ -571,39 +634,38 @@ size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t 
   return (size_t)(prep + parts);
 }
 
-tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache, const void* vcache,
-                              int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
-                              const float* q, float scale, float* out, void* workspace, size_t ws_bytes,
-                              void* stream) {
+static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache,
+                             const void* vcache, int64_t rows, const tq::RowMap& map, int32_t B, int32_t Hq,
+                             int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q, float scale,
+                             float* out, void* workspace, size_t ws_bytes, void* stream) {
   tq_status st;
   if ((st = check_scoring_codebook(kcb, TQ_KIND_PROD, "tq_decode_attention(keys)")) != TQ_OK) return st;
   if ((st = check_scoring_codebook(vcb, TQ_KIND_MSE, "tq_decode_attention(values)")) != TQ_OK) return st;
-  if ((st = check_heads("tq_decode_attention", B, Hq, Hkv, capacity)) != TQ_OK) return st;
+  if ((st = check_heads(what, B, Hq, Hkv, capacity)) != TQ_OK) return st;
   if (!kcache || !vcache || !seq_lens || !q || !out || !workspace)
-    return fail(TQ_EINVAL, "tq_decode_attention: NULL device pointer");
+    return fail(TQ_EINVAL, "%s: NULL device pointer", what);
   if (!aligned16(kcache) || !aligned16(vcache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
-    return fail(TQ_EINVAL, "tq_decode_attention: device pointers must be 16-byte aligned");
-  if (!std::isfinite(scale)) return fail(TQ_EINVAL, "tq_decode_attention: scale must be finite");
+    return fail(TQ_EINVAL, "%s: device pointers must be 16-byte aligned", what);
+  if (!std::isfinite(scale)) return fail(TQ_EINVAL, "%s: scale must be finite", what);
   if (ws_bytes < tq_decode_attention_workspace(kcb, B, Hq, Hkv, capacity))
-    return fail(TQ_ENOMEM, "tq_decode_attention: workspace too small");
+    return fail(TQ_ENOMEM, "%s: workspace too small", what);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   float* parts = reinterpret_cast<float*>(
       prep + tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d)));
   if (kcb->dev.mode != vcb->dev.mode)
-    return fail(TQ_EUNSUPPORTED, "tq_decode_attention: keys and values must use the same stage-1 mode");
+    return fail(TQ_EUNSUPPORTED, "%s: keys and values must use the same stage-1 mode", what);
   int nchunks, tpc;
   chunking(B, Hkv, capacity, attn_ctas(kcb), &nchunks, &tpc);
-  const int64_t rows = (int64_t)B * Hkv * capacity;
   const float sl2 = scale * 1.4426950408889634f;
   if (kcb->dev.mode == TQ_MODE_POLAR) {
     if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
       return st;
-    if (capacity % 16 == 0)
+    if (capacity % 16 == 0 || map.table)
       st = launched("tq_decode_attention",
                     tq::launch_attn_polar_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
                                                  static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
-                                                 seq_lens, prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
+                                                 map, seq_lens, prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
     else
       st = launched("tq_decode_attention",
                     tq::launch_attn_polar(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
@@ -615,11 +677,11 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   }
   if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
     return st;
-  if (capacity % 16 == 0)
+  if (capacity % 16 == 0 || map.table)
     st = launched("tq_decode_attention",
                   tq::launch_attn_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                         static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens,
-                                         prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
+                                         static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, map,
+                                         seq_lens, prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
   else
     st = launched("tq_decode_attention",
                   tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
@@ -628,6 +690,27 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
   if (st != TQ_OK) return st;
   return launched("tq_decode_attention/merge",
                   tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
+}
+
+tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache, const void* vcache,
+                              int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
+                              const float* q, float scale, float* out, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  return attn_common("tq_decode_attention", kcb, vcb, kcache, vcache, (int64_t)B * Hkv * capacity, tq::RowMap{}, B,
+                     Hq, Hkv, capacity, seq_lens, q, scale, out, workspace, ws_bytes, stream);
+}
+
+tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache,
+                                    const void* vcache, int32_t num_pages, int32_t page_size,
+                                    const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq,
+                                    int32_t Hkv, const int32_t* seq_lens, const float* q, float scale, float* out,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  tq::RowMap map;
+  tq_status st = check_paged("tq_decode_attention_paged", num_pages, page_size, block_table, max_pages, Hkv, &map);
+  if (st != TQ_OK) return st;
+  return attn_common("tq_decode_attention_paged", kcb, vcb, kcache, vcache, (int64_t)num_pages * Hkv * page_size,
+                     map, B, Hq, Hkv, (int64_t)max_pages * page_size, seq_lens, q, scale, out, workspace, ws_bytes,
+                     stream);
 }
 
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k) {

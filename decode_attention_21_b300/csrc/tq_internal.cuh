@@ -77,10 +77,58 @@ inline __host__ __device__ int64_t partial_floats(int d) { return 4 * (2 + d); }
 
 constexpr int kAttnWarps = 4;     // warps per attention / logits CTA
 
+// Where the cache row of token t of sequence b, kv head kvh lives.
+//   contiguous (table == nullptr): row (b*Hkv + kvh)*capacity + t;
+//   paged: block table entry table[b*max_pages + t/page] names a page that
+//   holds `page` consecutive rows per kv head: row (entry*Hkv + kvh)*page + t%page.
+// page is a multiple of 16, so a 16-token tile never straddles two pages.
+struct RowMap {
+  const int32_t* table;
+  int32_t page;        // tokens per page
+  int32_t max_pages;   // entries per table row (capacity = max_pages * page)
+  int32_t num_pages;   // pages in the cache; other entries are rejected
+};
+
+// Destination rows of a cache append: rows 0..n-1, an explicit list, or for a
+// paged cache the last token (seq_lens[b] - 1) of each (b, kvh) of a batch of
+// B*Hkv rows in (b, kvh) order; sequences with seq_lens[b] <= 0 are skipped.
+struct AppendDst {
+  const int64_t* rows;      // explicit list, or nullptr
+  RowMap map;               // paged when map.table != nullptr
+  const int32_t* seq_lens;  // paged: lengths including the appended token
+  int32_t Hkv;
+};
+
+// Status word bits set by the kernels (the codebook's device status word):
+// low bits = a bounded wait gave up (1 quantize, 2 scoring); kBadRow = an
+// append destination or a block-table entry lay outside the cache (the
+// access was skipped, or for a scoring read redirected to page 0).
+constexpr int kBadRow = 0x100;
+
+// Destination row of append row `row`: >= 0, or -1 (skip: empty sequence),
+// or -2 (skip: outside the cache).
+__device__ __forceinline__ int64_t append_row(const AppendDst& a, int64_t row, int64_t cache_rows) {
+  int64_t dst;
+  if (a.map.table) {
+    const int b = (int)(row / a.Hkv), kvh = (int)(row - (int64_t)b * a.Hkv);
+    const int64_t t = (int64_t)a.seq_lens[b] - 1;
+    if (t < 0) return -1;
+    const int64_t pi = t / a.map.page;
+    if (pi >= a.map.max_pages) return -2;
+    const int32_t pg = a.map.table[(int64_t)b * a.map.max_pages + pi];
+    if (pg < 0 || pg >= a.map.num_pages) return -2;
+    dst = ((int64_t)pg * a.Hkv + kvh) * a.map.page + (t - pi * a.map.page);
+  } else {
+    dst = a.rows ? a.rows[row] : row;
+  }
+  return (dst >= 0 && dst < cache_rows) ? dst : -2;
+}
+
 // Host-side launchers (one per kernel family); each returns the launch error.
 cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int x_dtype,
-                                 int64_t n, int d_in, const float* y, const float* norms, const int64_t* dst_rows,
-                                 cudaStream_t s);
+                                 int64_t n, int d_in, const float* y, const float* norms, const AppendDst& dst,
+                                 int* status, cudaStream_t s);
+cudaError_t launch_advance_lengths(int32_t* seq_lens, int B, int32_t delta, cudaStream_t s);
 cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
                                const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
                                const int64_t* dst_rows, int* status, int sms, cudaStream_t s);
@@ -89,17 +137,17 @@ cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, i
                           int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                           int nchunks, int tiles_per_cta, cudaStream_t s);
 cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
-                                 int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
-                                 int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
+                                 int64_t cache_rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
+                                 float* logits, int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache, int B, int Hq,
                         int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep,
                         float scale_log2, float* partials, int nchunks, int tiles_per_cta, cudaStream_t s);
 cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache, int B,
-                               int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens,
-                               const uint8_t* prep, float scale_log2, float* partials, int nchunks, int tiles_per_cta,
-                               int* status, cudaStream_t s);
+                               int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const RowMap& map,
+                               const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* partials,
+                               int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_attn_polar_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache,
-                                     int B, int Hq, int Hkv, int64_t capacity, int64_t cache_rows,
+                                     int B, int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const RowMap& map,
                                      const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* partials,
                                      int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_prep_polar(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s);

@@ -55,8 +55,8 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
                                                        int64_t cache_rows, const void* __restrict__ x,
                                                        int x_dtype, int64_t n, int d_in,
                                                        const float* __restrict__ y_in,
-                                                       const float* __restrict__ n_in,
-                                                       const int64_t* __restrict__ dst_rows) {
+                                                       const float* __restrict__ n_in, const AppendDst dmap,
+                                                       int* __restrict__ status) {
   // a programmatic dependent (the query prep) may start now: it reads none of
   // the rows written here and waits for this grid before it completes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -263,16 +263,19 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
     }
     __syncwarp();
 
-    // ---- store
-    const int64_t dst = dst_rows ? dst_rows[row] : row;
-    uint32_t* rec = recs + dst * W;
-    if (lane < W) rec[lane] = mine0;
-    if (lane + 32 < W) rec[lane + 32] = mine1;
-    if (lane == 0) {
-      if (prod)
-        reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
-      else
-        reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+    // ---- store (a destination outside the cache is skipped and flagged)
+    const int64_t dst = append_row(dmap, row, cache_rows);
+    if (dst == -2 && lane == 0) atomicOr(status, kBadRow);
+    if (dst >= 0) {
+      uint32_t* rec = recs + dst * W;
+      if (lane < W) rec[lane] = mine0;
+      if (lane + 32 < W) rec[lane + 32] = mine1;
+      if (lane == 0) {
+        if (prod)
+          reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
+        else
+          reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+      }
     }
   }
 }
@@ -304,7 +307,7 @@ template <int D>
 __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* __restrict__ cache, int64_t cache_rows,
                                                         const void* __restrict__ x, int x_dtype, int64_t n, int d_in,
                                                         const float* __restrict__ y_in, const float* __restrict__ n_in,
-                                                        const int64_t* __restrict__ dst_rows) {
+                                                        const AppendDst dmap, int* __restrict__ status) {
   // a programmatic dependent (the query prep) may start now: it reads none of
   // the rows written here and waits for this grid before it completes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -415,35 +418,51 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
       }
     }
     __syncthreads();
-    const int64_t dst = dst_rows ? dst_rows[row] : row;
-    if (t < cb.W) recs[dst * cb.W + t] = words[t];
-    if (t == 0) {
-      if (prod)
-        reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
-      else
-        reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+    // a destination outside the cache is skipped and flagged
+    const int64_t dst = append_row(dmap, row, cache_rows);
+    if (dst == -2 && t == 0) atomicOr(status, kBadRow);
+    if (dst >= 0) {
+      if (t < cb.W) recs[dst * cb.W + t] = words[t];
+      if (t == 0) {
+        if (prod)
+          reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
+        else
+          reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+      }
     }
     __syncthreads();
   }
 }
 
 cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int x_dtype,
-                                 int64_t n, int d_in, const float* y, const float* norms, const int64_t* dst_rows,
-                                 cudaStream_t s) {
+                                 int64_t n, int d_in, const float* y, const float* norms, const AppendDst& dst,
+                                 int* status, cudaStream_t s) {
   if (cb.mode == 0 && n <= 16384) {
     const int blocks = (int)(n < 148 * 16 ? n : 148 * 16);
     if (cb.d == 128)
-      k_quantize_row<128><<<blocks, 512, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+      k_quantize_row<128><<<blocks, 512, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst, status);
     else
-      k_quantize_row<256><<<blocks, 1024, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+      k_quantize_row<256><<<blocks, 1024, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst, status);
     return cudaGetLastError();
   }
   const int64_t blocks64 = (n + 7) / 8;
   const int blocks = (int)(blocks64 < 148 * 16 ? (blocks64 > 0 ? blocks64 : 1) : 148 * 16);
   if (cb.d == 128)
-    k_quantize_simt<128><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+    k_quantize_simt<128><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst, status);
   else
-    k_quantize_simt<256><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst_rows);
+    k_quantize_simt<256><<<blocks, 256, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst, status);
+  return cudaGetLastError();
+}
+
+// Decode-loop bookkeeping on the device: seq_lens[b] += delta, so a captured
+// step (advance, append, attend) can be replayed without host updates.
+__global__ void k_advance_lengths(int32_t* __restrict__ seq_lens, int B, int32_t delta) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) seq_lens[b] += delta;
+}
+
+cudaError_t launch_advance_lengths(int32_t* seq_lens, int B, int32_t delta, cudaStream_t s) {
+  k_advance_lengths<<<(B + 255) / 256, 256, 0, s>>>(seq_lens, B, delta);
   return cudaGetLastError();
 }
 

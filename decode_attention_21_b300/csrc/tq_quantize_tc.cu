@@ -322,8 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- store
     const int64_t row = tile * kRows + m;
-    if (row < n) {
-      const int64_t dst = dst_rows ? dst_rows[row] : row;
+    const int64_t dst = row < n ? (dst_rows ? dst_rows[row] : row) : -1;
+    if (row < n && (dst < 0 || dst >= cache_rows) && cg == 0) atomicOr(status, kBadRow);  // skipped
+    if (dst >= 0 && dst < cache_rows) {
       uint32_t* rec = reinterpret_cast<uint32_t*>(cache) + dst * W;
       if constexpr (PROD) word[b1] = sword;
       if constexpr (P == 4 && !EXT) {
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
   }
   if (!ok) {
-    if (tid == 0) atomicExch(status, 1);
+    if (tid == 0) atomicOr(status, 1);
     // let our own copies and MMAs drain (bounded waits) before freeing TMEM
     if (pending_stage >= 0) mbar_wait(bar_full0 + 8 * pending_stage, ((it + 1) >> 1) & 1);
     mbar_wait(bar_mma1, it & 1);

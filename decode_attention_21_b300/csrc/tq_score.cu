@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
 template <int NV, int P, bool QJL, int EXT>
 __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
                                                        int Hkv, int64_t capacity, int64_t cache_rows,
-                                                       const int32_t* __restrict__ seq_lens,
+                                                       const RowMap map, const int32_t* __restrict__ seq_lens,
                                                        const uint8_t* __restrict__ prep, float* __restrict__ logits,
                                                        int tiles_per_cta, int* __restrict__ status) {
   constexpr int RB = 16 * P + 4 * EXT;       // record bytes at d = 128 (+ extra-bit words)
@@ -492,18 +492,19 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
   if (tile0 >= tcap) return;
-  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
-  const uint8_t* grec = kcache + (rowbase + tile0 * 16) * RB;
-  const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows) + (rowbase + tile0 * 16) * NB;
-  // stage st (tiles st*kStageTiles ..) into ring slot st % kRing
+  const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows);
+  // stage st (tiles st*kStageTiles ..) into ring slot st % kRing, one copy
+  // per run of consecutive cache rows (one run unless the cache is paged)
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
-    const int t_a = st * kStageTiles;
-    const uint32_t rb = (uint32_t)(t_n * 16 * RB), nb = (uint32_t)(t_n * 16 * NB);
     const uint32_t bar = su32(&bars[slot]);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(rb + nb) : "memory");
-    bulk_g2s(su32(srec + (size_t)slot * kStageRec), grec + (size_t)t_a * 16 * RB, rb, bar);
-    bulk_g2s(su32(snrm + (size_t)slot * kStageNrm), gnrm + (size_t)t_a * 16 * NB, nb, bar);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)(t_n * 16 * (RB + NB)))
+                 : "memory");
+    for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16, t_n * 16, status,
+             [&](int64_t row, int k, int cnt) {
+               bulk_g2s(su32(srec + (size_t)slot * kStageRec + (size_t)k * RB), kcache + row * RB, (uint32_t)(cnt * RB), bar);
+               bulk_g2s(su32(snrm + (size_t)slot * kStageNrm + (size_t)k * NB), gnrm + row * NB, (uint32_t)(cnt * NB), bar);
+             });
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -516,11 +517,12 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   // Stream the first kPrefetchStages stages of the chunk from HBM into L2
   // while the prep (and any cache append before it) still runs.
   if (tid == 0)
-    for (int st = 0; st < min(nst, kPrefetchStages); ++st) {
-      const int t_n = min(kStageTiles, nt - st * kStageTiles);
-      prefetch_l2(grec + (size_t)st * kStageTiles * 16 * RB, (uint32_t)(t_n * 16 * RB));
-      prefetch_l2(gnrm + (size_t)st * kStageTiles * 16 * NB, (uint32_t)(t_n * 16 * NB));
-    }
+    for (int st = 0; st < min(nst, kPrefetchStages); ++st)
+      for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16,
+               min(kStageTiles, nt - st * kStageTiles) * 16, status, [&](int64_t row, int, int cnt) {
+                 prefetch_l2(kcache + row * RB, (uint32_t)(cnt * RB));
+                 prefetch_l2(gnrm + row * NB, (uint32_t)(cnt * NB));
+               });
   // The query fragments come from the preceding prep grid, launched as its
   // programmatic dependent; the prep's completion also implies that of any
   // cache append before it, so no cache row is read into the SM before this
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     }
   }
   if (!ok) {
-    if (tid == 0) atomicExch(status, 2);
+    if (tid == 0) atomicOr(status, 2);
     // let the copies still in flight land (bounded) before the shared memory is released
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
   }
@@ -817,7 +819,7 @@ template <int NVK, int PK, int NVV, int PV>
 __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev kcb, const Dev vcb,
                                                      const uint8_t* __restrict__ kcache,
                                                      const uint8_t* __restrict__ vcache, int Hq, int Hkv,
-                                                     int64_t capacity, int64_t cache_rows,
+                                                     int64_t capacity, int64_t cache_rows, const RowMap map,
                                                      const int32_t* __restrict__ seq_lens,
                                                      const uint8_t* __restrict__ prep, float scale_log2,
                                                      float* __restrict__ partials, int tiles_per_cta,
@@ -833,25 +835,24 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   const int g = lane >> 2, c = lane & 3;
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
-  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
-  const int64_t r0 = rowbase + tile0 * 16;
-  const uint8_t* gk = kcache + r0 * RBK;
-  const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows) + r0 * 4;
-  const uint8_t* gv = vcache + r0 * RBV;
-  const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows) + r0 * 2;
+  const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows);
+  const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows);
+  // stage st into ring slot st % kRing, one copy per run of consecutive cache
+  // rows (one run unless the cache is paged)
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
-    const size_t t_a = (size_t)st * kStageTiles * 16;    // first row of the stage
-    const uint32_t nk = (uint32_t)(t_n * 16 * RBK), nkn = (uint32_t)(t_n * 16 * 4);
-    const uint32_t nv = (uint32_t)(t_n * 16 * RBV), nvn = (uint32_t)(t_n * 16 * 2);
     const uint32_t bar = su32(&bars[slot]);
     uint8_t* base = sm + (size_t)slot * kSlot;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(nk + nkn + nv + nvn)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
                  : "memory");
-    bulk_g2s(su32(base), gk + t_a * RBK, nk, bar);
-    bulk_g2s(su32(base + kSK), gkn + t_a * 4, nkn, bar);
-    bulk_g2s(su32(base + kSK + kSKN), gv + t_a * RBV, nv, bar);
-    bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + t_a * 2, nvn, bar);
+    for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16, t_n * 16, status,
+             [&](int64_t row, int k, int cnt) {
+               bulk_g2s(su32(base + k * RBK), kcache + row * RBK, (uint32_t)(cnt * RBK), bar);
+               bulk_g2s(su32(base + kSK + k * 4), gkn + row * 4, (uint32_t)(cnt * 4), bar);
+               bulk_g2s(su32(base + kSK + kSKN + k * RBV), vcache + row * RBV, (uint32_t)(cnt * RBV), bar);
+               bulk_g2s(su32(base + kSK + kSKN + kSV + k * 2), gvn + row * 2, (uint32_t)(cnt * 2), bar);
+             });
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -863,14 +864,14 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
   // the first stages stream from HBM into L2 while the prep still runs
   if (tid == 0)
-    for (int st = 0; st < min(nst, kRing); ++st) {
-      const size_t t_a = (size_t)st * kStageTiles * 16;
-      const int t_n = min(kStageTiles, nt - st * kStageTiles);
-      prefetch_l2(gk + t_a * RBK, (uint32_t)(t_n * 16 * RBK));
-      prefetch_l2(gkn + t_a * 4, (uint32_t)(t_n * 16 * 4));
-      prefetch_l2(gv + t_a * RBV, (uint32_t)(t_n * 16 * RBV));
-      prefetch_l2(gvn + t_a * 2, (uint32_t)(t_n * 16 * 2));
-    }
+    for (int st = 0; st < min(nst, kRing); ++st)
+      for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16,
+               min(kStageTiles, nt - st * kStageTiles) * 16, status, [&](int64_t row, int, int cnt) {
+                 prefetch_l2(kcache + row * RBK, (uint32_t)(cnt * RBK));
+                 prefetch_l2(gkn + row * 4, (uint32_t)(cnt * 4));
+                 prefetch_l2(vcache + row * RBV, (uint32_t)(cnt * RBV));
+                 prefetch_l2(gvn + row * 2, (uint32_t)(cnt * 2));
+               });
   // query fragments come from the preceding prep grid (whose completion also
   // implies that of any cache append before it): no cache row is read into
   // the SM before this wait; the first stage goes out right after it
@@ -1002,7 +1003,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
     }
   }
   if (!ok) {
-    if (tid == 0) atomicExch(status, 2);
+    if (tid == 0) atomicOr(status, 2);
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
   }
   // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
@@ -1160,8 +1161,8 @@ cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int H
 
 template <int NV, int P, bool QJL, int EXT>
 static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
-                                   int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
-                                   int nchunks, int tpc, int* status, cudaStream_t s) {
+                                   int64_t rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
+                                   float* logits, int nchunks, int tpc, int* status, cudaStream_t s) {
   constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + 4 * EXT + (QJL ? 4 : 2));
   static cudaError_t configured = [] {
     cudaError_t e = cudaFuncSetAttribute(k_logits_staged<NV, P, QJL, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1180,15 +1181,16 @@ static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P, QJL, EXT>, cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep,
-                            logits, tpc, status);
+  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P, QJL, EXT>, cb, kc, Hq, Hkv, capacity, rows, map, seq_lens,
+                            prep, logits, tpc, status);
 }
 
 cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
-                                 int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
-                                 int nchunks, int tpc, int* status, cudaStream_t s) {
-#define TQ_CALL(NV, P, Q, X) \
-  return logits_staged_t<NV, P, Q, X>(cb, kc, B, Hq, Hkv, capacity, rows, seq_lens, prep, logits, nchunks, tpc, status, s)
+                                 int64_t rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
+                                 float* logits, int nchunks, int tpc, int* status, cudaStream_t s) {
+#define TQ_CALL(NV, P, Q, X)                                                                                      \
+  return logits_staged_t<NV, P, Q, X>(cb, kc, B, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, nchunks, tpc, \
+                                      status, s)
   TQ_LOGITS_DISPATCH(TQ_CALL)
 #undef TQ_CALL
 }
@@ -1196,7 +1198,7 @@ cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq
 
 template <int NVK, int PK, int NVV, int PV>
 static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
-                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const int32_t* sl,
+                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map, const int32_t* sl,
                                  const uint8_t* prep, float sl2, float* parts, int tpc, int* status) {
   constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 + 16 * PV + 2);
   static cudaError_t configured = [] {
@@ -1216,30 +1218,30 @@ static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_attn_staged<NVK, PK, NVV, PV>, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2,
+  return cudaLaunchKernelEx(&cfg, k_attn_staged<NVK, PK, NVV, PV>, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2,
                             parts, tpc, status);
 }
 
 template <int NVK, int PK>
 static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
-                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const int32_t* sl,
+                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map, const int32_t* sl,
                                  const uint8_t* prep, float sl2, float* parts, int tpc, int* status) {
   switch (b1v) {
-    case 1: return attn_staged_t<NVK, PK, 1, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
-    case 2: return attn_staged_t<NVK, PK, 2, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
-    case 3: return attn_staged_t<NVK, PK, 4, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
-    default: return attn_staged_t<NVK, PK, 8, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    case 1: return attn_staged_t<NVK, PK, 1, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+    case 2: return attn_staged_t<NVK, PK, 2, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+    case 3: return attn_staged_t<NVK, PK, 4, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+    default: return attn_staged_t<NVK, PK, 8, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
   }
 }
 
 cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq,
-                               int Hkv, int64_t capacity, int64_t rows, const int32_t* seq_lens, const uint8_t* prep,
-                               float scale_log2, float* parts, int nchunks, int tpc, int* status, cudaStream_t s) {
+                               int Hkv, int64_t capacity, int64_t rows, const RowMap& map, const int32_t* seq_lens,
+                               const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc, int* status, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
   switch (kcb.b1) {
-    case 1: return attn_staged_v<1, 2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
-    case 2: return attn_staged_v<2, 3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
-    default: return attn_staged_v<4, 4>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
+    case 1: return attn_staged_v<1, 2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
+    case 2: return attn_staged_v<2, 3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
+    default: return attn_staged_v<4, 4>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
   }
 }
 

@@ -449,7 +449,7 @@ template <int BK, int BV>
 __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, const Dev vcb,
                                                            const uint8_t* __restrict__ kcache,
                                                            const uint8_t* __restrict__ vcache, int Hq, int Hkv,
-                                                           int64_t capacity, int64_t cache_rows,
+                                                           int64_t capacity, int64_t cache_rows, const RowMap map,
                                                            const int32_t* __restrict__ seq_lens,
                                                            const uint8_t* __restrict__ prep, float scale_log2,
                                                            float* __restrict__ partials, int tiles_per_cta,
@@ -469,25 +469,24 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   const int g = lane >> 2, c = lane & 3;
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
-  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
-  const int64_t r0 = rowbase + tile0 * 16;
-  const uint8_t* gk = kcache + r0 * RBK;
-  const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows) + r0 * 4;
-  const uint8_t* gv = vcache + r0 * RBV;
-  const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows) + r0 * 2;
+  const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows);
+  const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows);
+  // stage st into ring slot st % kRing, one copy per run of consecutive cache
+  // rows (one run unless the cache is paged)
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
-    const size_t t_a = (size_t)st * kStageTiles * 16;
-    const uint32_t nk = (uint32_t)(t_n * 16 * RBK), nkn = (uint32_t)(t_n * 16 * 4);
-    const uint32_t nv = (uint32_t)(t_n * 16 * RBV), nvn = (uint32_t)(t_n * 16 * 2);
     const uint32_t bar = su32(&bars[slot]);
     uint8_t* base = sm + (size_t)slot * kSlot;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(nk + nkn + nv + nvn)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
                  : "memory");
-    bulk_g2s(su32(base), gk + t_a * RBK, nk, bar);
-    bulk_g2s(su32(base + kSK), gkn + t_a * 4, nkn, bar);
-    bulk_g2s(su32(base + kSK + kSKN), gv + t_a * RBV, nv, bar);
-    bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + t_a * 2, nvn, bar);
+    for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16, t_n * 16, status,
+             [&](int64_t row, int k, int cnt) {
+               bulk_g2s(su32(base + k * RBK), kcache + row * RBK, (uint32_t)(cnt * RBK), bar);
+               bulk_g2s(su32(base + kSK + k * 4), gkn + row * 4, (uint32_t)(cnt * 4), bar);
+               bulk_g2s(su32(base + kSK + kSKN + k * RBV), vcache + row * RBV, (uint32_t)(cnt * RBV), bar);
+               bulk_g2s(su32(base + kSK + kSKN + kSV + k * 2), gvn + row * 2, (uint32_t)(cnt * 2), bar);
+             });
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -615,7 +614,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
     }
   }
   if (!ok) {
-    if (tid == 0) atomicExch(status, 2);
+    if (tid == 0) atomicOr(status, 2);
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
   }
   const int nchunks = gridDim.x;
@@ -635,13 +634,13 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
 template <int BK, int BV>
 static cudaError_t attn_polar_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
                                        const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows,
-                                       const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
+                                       const RowMap& map, const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
                                        int* status) {
   constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * (BK + 1) + 4 + 16 * BV + 2);
   static cudaError_t configured = cudaFuncSetAttribute(k_attn_polar_staged<BK, BV>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (configured != cudaSuccess) return configured;
-  k_attn_polar_staged<BK, BV><<<grid, 128, smem, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc,
+  k_attn_polar_staged<BK, BV><<<grid, 128, smem, s>>>(k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc,
                                                       status);
   return cudaGetLastError();
 }
@@ -649,25 +648,25 @@ static cudaError_t attn_polar_staged_t(dim3 grid, cudaStream_t s, const Dev& k, 
 template <int BK>
 static cudaError_t attn_polar_staged_v(int bv, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v,
                                        const uint8_t* kc, const uint8_t* vc, int Hq, int Hkv, int64_t cap,
-                                       int64_t rows, const int32_t* sl, const uint8_t* prep, float sl2, float* parts,
-                                       int tpc, int* status) {
+                                       int64_t rows, const RowMap& map, const int32_t* sl, const uint8_t* prep, float sl2,
+                                       float* parts, int tpc, int* status) {
   switch (bv) {
-    case 1: return attn_polar_staged_t<BK, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
-    case 2: return attn_polar_staged_t<BK, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
-    case 3: return attn_polar_staged_t<BK, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
-    default: return attn_polar_staged_t<BK, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, sl, prep, sl2, parts, tpc, status);
+    case 1: return attn_polar_staged_t<BK, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+    case 2: return attn_polar_staged_t<BK, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+    case 3: return attn_polar_staged_t<BK, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+    default: return attn_polar_staged_t<BK, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
   }
 }
 
 cudaError_t launch_attn_polar_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B,
-                                     int Hq, int Hkv, int64_t capacity, int64_t rows, const int32_t* seq_lens,
-                                     const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc,
+                                     int Hq, int Hkv, int64_t capacity, int64_t rows, const RowMap& map,
+                                     const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc,
                                      int* status, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
   switch (kcb.b1) {
-    case 1: return attn_polar_staged_v<1>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
-    case 2: return attn_polar_staged_v<2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
-    default: return attn_polar_staged_v<3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, seq_lens, prep, scale_log2, parts, tpc, status);
+    case 1: return attn_polar_staged_v<1>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
+    case 2: return attn_polar_staged_v<2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
+    default: return attn_polar_staged_v<3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
   }
 }
 

@@ -31,6 +31,33 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Visit the runs of consecutive cache rows holding tokens t0 .. t0 + n - 1 of
+// (b, kvh) (t0 and n multiples of 16, t0 + n <= capacity): f(row, k, count)
+// for tokens t0 + k .. t0 + k + count - 1 starting at cache row `row`.  A
+// block-table entry outside the cache sets kBadRow in *status and reads
+// page 0 instead, so every copy stays inside the cache.
+template <class F>
+__device__ __forceinline__ void for_runs(const RowMap& map, int b, int kvh, int Hkv, int64_t capacity, int64_t t0,
+                                         int n, int* status, F&& f) {
+  if (!map.table) {
+    f(((int64_t)b * Hkv + kvh) * capacity + t0, 0, n);
+    return;
+  }
+  for (int k = 0; k < n;) {
+    const int64_t t = t0 + k;
+    const int64_t pi = t / map.page;
+    const int off = (int)(t - pi * map.page);
+    const int cnt = min(n - k, map.page - off);
+    int32_t pg = __ldg(map.table + (int64_t)b * map.max_pages + pi);
+    if (pg < 0 || pg >= map.num_pages) {
+      atomicOr(status, kBadRow);
+      pg = 0;
+    }
+    f(((int64_t)pg * Hkv + kvh) * map.page + off, k, cnt);
+    k += cnt;
+  }
+}
+
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
   for (long long i = 0; i < kWaitLimit; ++i) {
     uint32_t done;

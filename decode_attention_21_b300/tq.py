@@ -21,6 +21,7 @@ EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_hos
            "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits", "tq_logits_dense",
            "tq_decode_attention_workspace", "tq_decode_attention", "tq_decode_attention_static",
            "tq_search_workspace", "tq_search",
+           "tq_append_paged", "tq_logits_paged", "tq_decode_attention_paged", "tq_advance_lengths",
            "tq_check_device", "tq_last_error"]
 
 
@@ -71,6 +72,11 @@ def lib():
         L.tq_search_workspace.argtypes = [vp, i64, i32, i32]
         L.tq_search_workspace.restype = sz
         L.tq_search.argtypes = [vp, vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.tq_append_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, vp, vp, i32, i32, vp]
+        L.tq_logits_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.tq_decode_attention_paged.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp,
+                                                ctypes.c_float, vp, vp, sz, vp]
+        L.tq_advance_lengths.argtypes = [vp, i32, i32, vp]
         L.tq_check_device.argtypes = [vp]
         L.tq_last_error.argtypes = []
         L.tq_last_error.restype = ctypes.c_char_p
@@ -222,6 +228,33 @@ def tq_search_workspace(cb, n_db, nq, k):
 def tq_search(cb, db_cache, n_db, q, nq, d_in, k, ids, scores, workspace, stream=None):
     _check(lib().tq_search(cb.handle, _ptr(db_cache), n_db, _ptr(q), nq, d_in, k, _ptr(ids), _ptr(scores),
                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_append_paged(cb, cache, num_pages, page_size, block_table, B, Hkv, seq_lens, x, d_in, stream=None):
+    """Append x [B, Hkv, d_in] at token seq_lens[b] - 1 of each sequence of a
+    paged cache; block_table is int32 [B, max_pages]."""
+    dt = BF16 if x.dtype == torch.bfloat16 else F32
+    _check(lib().tq_append_paged(cb.handle, _ptr(cache), num_pages, page_size, _ptr(block_table),
+                                 block_table.shape[1], B, Hkv, _ptr(seq_lens), _ptr(x), dt, d_in, _stream(stream)))
+
+
+def tq_logits_paged(kcb, kcache, num_pages, page_size, block_table, B, Hq, Hkv, seq_lens, q, logits, workspace,
+                    stream=None):
+    _check(lib().tq_logits_paged(kcb.handle, _ptr(kcache), num_pages, page_size, _ptr(block_table),
+                                 block_table.shape[1], B, Hq, Hkv, _ptr(seq_lens), _ptr(q), _ptr(logits),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_decode_attention_paged(kcb, vcb, kcache, vcache, num_pages, page_size, block_table, B, Hq, Hkv, seq_lens, q,
+                              scale, out, workspace, stream=None):
+    _check(lib().tq_decode_attention_paged(kcb.handle, vcb.handle, _ptr(kcache), _ptr(vcache), num_pages, page_size,
+                                           _ptr(block_table), block_table.shape[1], B, Hq, Hkv, _ptr(seq_lens),
+                                           _ptr(q), float(scale), _ptr(out), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_advance_lengths(seq_lens, B, delta=1, stream=None):
+    _check(lib().tq_advance_lengths(_ptr(seq_lens), B, delta, _stream(stream)))
 
 
 def tq_check_device(cb):

@@ -14,6 +14,10 @@ Workloads (shapes of the pages' own cases):
   log-normal(0,1) scale, with 2% of the channels (3 of 128, seeded, without
   replacement) scaled x10.
 * ``queries``: fp32 ~N(0, I).
+* ``block_table``: a paged cache's page assignment: the pages of all
+  sequences are a seeded random permutation of the pool (so consecutive
+  pages of a sequence are scattered), entries past each sequence's last page
+  are -1.
 * ``search_mixture``: database and held-out queries from a Gaussian mixture
   (1000 centres ~N(0, I) in d=200, within-cluster sigma 0.3), unit-normalised;
   a synthetic stand-in for the 200-dimensional GloVe vectors.
@@ -23,7 +27,7 @@ import numpy as np
 DATA_SEED = 20261202
 
 _NAMES = {"keys": 1, "values": 2, "queries": 3, "scale": 4, "outliers": 5,
-          "centres": 6, "db": 7, "search_q": 8, "tiny_keys": 9, "tiny_q": 10, "append": 11}
+          "centres": 6, "db": 7, "search_q": 8, "tiny_keys": 9, "tiny_q": 10, "append": 11, "pages": 12}
 
 
 def _rng(seed, name, *idx):
@@ -104,3 +108,18 @@ def llama_kv_torch(n, d, kv_head, seed=DATA_SEED, which="keys", device="cuda", g
     s = torch.from_numpy(llama_channel_scale(kv_head, d, seed, which)).to(device=device, dtype=torch.float32)
     x = torch.randn(n, d, generator=g, device=device, dtype=torch.float32) * s
     return x.to(torch.bfloat16)
+
+
+def block_table(B, max_pages, num_pages, page_size, lens, seed=DATA_SEED):
+    """int32 [B, max_pages] page ids: sequence b's pages 0..ceil(lens[b] /
+    page_size) - 1 are distinct pages drawn from a seeded permutation of
+    range(num_pages); the other entries are -1."""
+    need = [-(-int(L) // page_size) for L in lens]
+    assert max(need) <= max_pages and sum(need) <= num_pages
+    perm = _rng(seed, "pages", B, max_pages, num_pages).permutation(num_pages)
+    t = np.full((B, max_pages), -1, dtype=np.int32)
+    k = 0
+    for b in range(B):
+        t[b, : need[b]] = perm[k: k + need[b]]
+        k += need[b]
+    return t

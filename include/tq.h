@@ -114,8 +114,9 @@ size_t tq_cache_bytes(const tq_codebook* cb, int64_t rows);
  *   cache      device, tq_cache_bytes(cb, cache_rows) bytes
  *   x          device, n x d_in row-major, dtype TQ_F32 or TQ_BF16; d_in <= d
  *              and columns d_in..d-1 are taken as zero
- *   dst_rows   device int64[n] target rows (each < cache_rows, distinct), or
- *              NULL for rows 0..n-1
+ *   dst_rows   device int64[n] target rows (distinct), or NULL for rows
+ *              0..n-1; a row outside 0..cache_rows-1 is skipped and flagged
+ *              for tq_check_device (TQ_EINVAL)
  * Each row: n = ||x||, y = Pi x / n, stage-1 codes, r = y - yhat, gamma =
  * ||r||, sign(S r); n and gamma stored as fp16 (round to nearest even).    */
 tq_status tq_quantize(const tq_codebook* cb, void* cache, int64_t cache_rows,
@@ -197,6 +198,66 @@ tq_status tq_decode_attention_static(const tq_codebook* kcb, const tq_codebook* 
                                      int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
                                      const float* q, float scale, float* out, void* stream);
 
+/* ---- Paged caches and the in-place decode loop --------------------------
+ * The per-token, calibration-free use of the method ([suzuke] 為什麼這個方法
+ * 特別聰明: each new key or value is compressed the moment it arrives) fills
+ * a cache one token per step.  The pages fix no memory layout for this; the
+ * entry points below add the usual one, a pool of fixed-size pages named by a
+ * per-sequence block table, so sequences grow without reserving their full
+ * capacity.  The arithmetic is that of the contiguous entry points, bit for
+ * bit: a paged call returns exactly what the contiguous call returns on a
+ * cache holding the same rows.
+ *
+ * Paged layout (shared by keys and values):
+ *   cache        tq_cache_bytes(cb, num_pages * Hkv * page_size) bytes; page
+ *                p holds, for each kv head h, page_size consecutive rows
+ *                starting at row (p*Hkv + h)*page_size (records, then the
+ *                norm region, as in any cache)
+ *   page_size    tokens per page, a positive multiple of 16
+ *   block_table  device int32 [B, max_pages]: token t of sequence b lives in
+ *                page block_table[b*max_pages + t/page_size], slot
+ *                t % page_size; entries for pages past seq_lens[b] are not read
+ *   capacity     max_pages * page_size tokens per sequence
+ * The kernels read the table and seq_lens without validating them against the
+ * host: a table entry outside 0..num_pages-1 is never dereferenced (a read
+ * goes to page 0 instead, a write is skipped) and sets a flag that the next
+ * tq_check_device reports as TQ_EINVAL.                                      */
+
+/* Append one token per (sequence, kv head): x device [B, Hkv, d_in] (TQ_F32
+ * or TQ_BF16) is compressed as by tq_quantize and written at token
+ * seq_lens[b] - 1 of sequence b (seq_lens counts the appended token);
+ * sequences with seq_lens[b] <= 0 are skipped, and a token past the capacity
+ * is skipped and flagged.                                                    */
+tq_status tq_append_paged(const tq_codebook* cb, void* cache, int32_t num_pages, int32_t page_size,
+                          const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hkv,
+                          const int32_t* seq_lens, const void* x, int32_t x_dtype, int32_t d_in,
+                          void* stream);
+
+/* tq_logits over a paged key cache (scalar mode; PROD or MSE-only keys):
+ *   logits  device fp32 [B, Hq, max_pages * page_size]
+ *   workspace >= tq_logits_workspace(kcb, B, Hq, Hkv) bytes
+ * Polar-mode keys return TQ_EUNSUPPORTED.                                    */
+tq_status tq_logits_paged(const tq_codebook* kcb, const void* kcache, int32_t num_pages, int32_t page_size,
+                          const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq, int32_t Hkv,
+                          const int32_t* seq_lens, const float* q, float* logits, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/* tq_decode_attention over paged key and value caches (same block table and
+ * page size for both; scalar or polar mode):
+ *   workspace >= tq_decode_attention_workspace(kcb, B, Hq, Hkv,
+ *                max_pages * page_size) bytes                                */
+tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache,
+                                    const void* vcache, int32_t num_pages, int32_t page_size,
+                                    const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq,
+                                    int32_t Hkv, const int32_t* seq_lens, const float* q, float scale, float* out,
+                                    void* workspace, size_t ws_bytes, void* stream);
+
+/* seq_lens[b] += delta for b < B, on the stream.  With it one decode step
+ * (tq_advance_lengths by 1, tq_append_paged of the new keys and values,
+ * tq_decode_attention_paged) reads and updates only device state, so the step
+ * can be captured once in a CUDA graph and replayed step after step.        */
+tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* stream);
+
 /* Workspace bytes of tq_search. */
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k);
 
@@ -210,9 +271,11 @@ tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, c
                     int32_t nq, int32_t d_in, int32_t k, int32_t* ids, float* scores,
                     void* workspace, size_t ws_bytes, void* stream);
 
-/* Synchronise the device and report whether any kernel of this codebook
- * gave up a bounded wait on its own copies or tensor-core operations since
- * the last check (TQ_ETIMEOUT, flag cleared), else TQ_OK.  Not a hot call.  */
+/* Synchronise the device and report, since the last check, whether any
+ * kernel of this codebook gave up a bounded wait on its own copies or
+ * tensor-core operations (TQ_ETIMEOUT), or met an append destination or a
+ * block-table entry outside the cache (TQ_EINVAL); the flag is cleared.
+ * TQ_OK otherwise.  Not a hot call.                                          */
 tq_status tq_check_device(const tq_codebook* cb);
 
 /* Message of the calling thread's last failed call ("" if none). */
