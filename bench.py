@@ -345,9 +345,12 @@ def run_logits(args, dist, rank):
     e2e_value = args.steps * keys * args.world / (e_ms / 1e3)
 
     comparator = dense_comparator(tq, wl, B, Hq, Hkv, d, T, caches[0], kcb, seq, qs[0], ws, k_ms)
+    paged = {f"page_{ps}": paged_logits(tq, wl, kcb, base, B, Hq, Hkv, d, T, NC, ps, seq, qs, outs, ws, n_k, k_ms)
+             for ps in (16, 256)}
 
     res = {
         "comparator": comparator,
+        "paged": paged,
         "metric": "keys scored per second (decode logits, 4-bit TurboQuant keys)",
         "value": value,
         "unit": "keys/s",
@@ -376,6 +379,32 @@ def run_logits(args, dist, rank):
                                "sample": f"1 of 8 kv heads: append 1 key + score {T} keys x 4 query heads, "
                                          f"{n} repetitions in {el:.1f} s"}
     return res
+
+
+def paged_logits(tq, wl, kcb, base, B, Hq, Hkv, d, T, NC, ps, seq, qs, outs, ws, n, k_ms):
+    """tq_logits_paged on the same keys scattered over pages: one pool of NC
+    copies (larger than L2, like the contiguous rotation), copy j reached
+    through block-table row j; event-timed per call like the contiguous one."""
+    max_pages = T // ps
+    num_pages = NC * max_pages
+    table = torch.from_numpy(wl.block_table(NC, max_pages, num_pages, ps, [T] * NC)).cuda()
+    rows = B * Hkv * T
+    pool_rows = num_pages * Hkv * ps
+    pool = torch.empty(tq.cache_bytes(kcb, pool_rows), dtype=torch.uint8, device="cuda")
+    rb, nb = tq.record_bytes(kcb), 4
+    src_off = (rows * rb + 255) // 256 * 256
+    dst_off = (pool_rows * rb + 255) // 256 * 256
+    h = torch.arange(Hkv, device="cuda")[:, None]
+    t = torch.arange(T, device="cuda")[None, :]
+    for j in range(NC):
+        phys = ((table[j, t // ps].long() * Hkv + h) * ps + t % ps).reshape(-1)
+        pool[: pool_rows * rb].view(pool_rows, rb)[phys] = base[: rows * rb].view(rows, rb)
+        pool[dst_off: dst_off + pool_rows * nb].view(pool_rows, nb)[phys] = base[src_off: src_off + rows * nb].view(rows, nb)
+    tables = [table[j: j + 1].contiguous() for j in range(NC)]
+    ms = per_call_ms(lambda i: tq.tq_logits_paged(kcb, pool, num_pages, ps, tables[i % NC], B, Hq, Hkv, seq,
+                                                  qs[i % NC], outs[i % NC], ws), n)
+    tq.tq_check_device(kcb)
+    return {"page_size": ps, "ms_per_call": ms, "vs_contiguous": ms / k_ms}
 
 
 def dense_comparator(tq, wl, B, Hq, Hkv, d, T, cache, kcb, seq, q, ws, tq_call_ms):
@@ -486,13 +515,73 @@ def run_attention(args, dist, rank, steps, mode="scalar"):
                        max(steps, 5))
     pk = peaks()
     achieved = packed / (k_ms / 1e3) / 1e9
-    return {"workload": f"fused decode attention ({mode} stage 1): batch {B}, 32/8 heads, d 128, context 131072, "
-                        "keys 3-bit, values 3-bit",
-            "keys_per_s": steps * rows * args.world / (ms / 1e3), "ms_per_step": ms / steps,
-            "packed_bytes_per_step": packed,
-            "roofline": {"kernel": "tq_decode_attention (prep + fused kernel + merge)", "bound": "hbm",
-                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / pk["hbm_gbs"], "launch_ms": k_ms}}
+    res = {"workload": f"fused decode attention ({mode} stage 1): batch {B}, 32/8 heads, d 128, context 131072, "
+                       "keys 3-bit, values 3-bit",
+           "keys_per_s": steps * rows * args.world / (ms / 1e3), "ms_per_step": ms / steps,
+           "packed_bytes_per_step": packed,
+           "roofline": {"kernel": "tq_decode_attention (prep + fused kernel + merge)", "bound": "hbm",
+                        "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / pk["hbm_gbs"], "launch_ms": k_ms}}
+    if mode == "scalar":
+        res["paged_decode_loop"] = {
+            f"page_{ps}": run_paged_loop(dist, tq, kcb, vcb, kc, vc, B, Hq, Hkv, T, q, knew, vnew, ps, steps)
+            for ps in (16, 64, 256)}
+    return res
+
+
+def run_paged_loop(dist, tq, kcb, vcb, kc, vc, B, Hq, Hkv, T, q, knew, vnew, ps, steps):
+    """The same caches scattered over pages (seeded random page order), and a
+    decode step that reads and updates only device state: advance the lengths,
+    append one key and value per (sequence, kv head) at the new last token,
+    attend over the pages.  Captured once as a CUDA graph of `steps` steps."""
+    from decode_attention_21_b300 import workloads as wl
+    d = 128
+    rows = B * Hkv * T
+    max_pages = T // ps
+    num_pages = B * max_pages
+    table = torch.from_numpy(wl.block_table(B, max_pages, num_pages, ps, [T] * B)).cuda()
+    # logical row (b*Hkv + h)*T + t  ->  physical row (page*Hkv + h)*ps + t % ps
+    b = torch.arange(B, device="cuda")[:, None, None]
+    h = torch.arange(Hkv, device="cuda")[None, :, None]
+    t = torch.arange(T, device="cuda")[None, None, :]
+    phys = ((table[b, t // ps].long() * Hkv + h) * ps + t % ps).reshape(-1)
+    pages = []
+    for cb, src in ((kcb, kc), (vcb, vc)):
+        rb = tq.record_bytes(cb)
+        nb = 4 if cb is kcb else 2
+        dst = torch.empty_like(src)
+        off = (rows * rb + 255) // 256 * 256
+        dst[: rows * rb].view(rows, rb)[phys] = src[: rows * rb].view(rows, rb)
+        dst[off: off + rows * nb].view(rows, nb)[phys] = src[off: off + rows * nb].view(rows, nb)
+        pages.append(dst)
+    kp, vp = pages
+    # lengths start low enough for every step this function runs
+    runs = 3 + 2 * steps
+    seq = torch.full((B,), T - runs - 1, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, Hq, d, device="cuda")
+    ws = torch.empty(tq.tq_decode_attention_workspace(kcb, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    kin, vin = knew.view(B, Hkv, d), vnew.view(B, Hkv, d)
+
+    def step(i):
+        tq.tq_advance_lengths(seq, B, 1)
+        tq.tq_append_paged(kcb, kp, num_pages, ps, table, B, Hkv, seq, kin, d)
+        tq.tq_append_paged(vcb, vp, num_pages, ps, table, B, Hkv, seq, vin, d)
+        tq.tq_decode_attention_paged(kcb, vcb, kp, vp, num_pages, ps, table, B, Hq, Hkv, seq, q, scale, out, ws)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    graph = capture(step, steps)
+    graph.replay()
+    torch.cuda.synchronize()
+    ms = timed(dist, graph.replay)
+    tq.tq_check_device(kcb)
+    tq.tq_check_device(vcb)
+    del kp, vp, pages
+    return {"page_size": ps, "ms_per_step": ms / steps, "keys_per_s": steps * rows / (ms / 1e3),
+            "step": "advance lengths + append 1 key and 1 value per (sequence, kv head) + paged attention, "
+                    "one CUDA graph"}
 
 
 # --------------------------------------------------------- quantize (config)
@@ -637,7 +726,7 @@ def main():
             "vs_baseline": None, "dtype": res.get("dtype", "f32"), "data": "synthetic (seeded)",
             "impl": "ours"}
     for k in ("config", "query_head_scores_per_s", "packed_gbs", "roofline", "cpu_baseline", "e2e", "gpu_launches",
-              "comparator",
+              "comparator", "paged",
               "clocks"):
         if k in res:
             line[k] = res[k]

@@ -586,10 +586,15 @@ static tq_status check_paged(const char* what, int32_t num_pages, int32_t page_s
   if (num_pages < 1 || max_pages < 1) return fail(TQ_EINVAL, "%s: num_pages and max_pages must be positive", what);
   if (Hkv < 1 || (int64_t)num_pages * Hkv * page_size >= (1ll << 40))
     return fail(TQ_EINVAL, "%s: cache too large", what);
+  if ((int64_t)max_pages * page_size >= (1ll << 31))
+    return fail(TQ_EINVAL, "%s: max_pages * page_size must be below 2^31 tokens", what);
   map->table = block_table;
   map->page = page_size;
   map->max_pages = max_pages;
   map->num_pages = num_pages;
+  map->page_shift = -1;
+  for (int k = 4; k <= 20; ++k)
+    if (page_size == (1 << k)) map->page_shift = k;
   return TQ_OK;
 }
 

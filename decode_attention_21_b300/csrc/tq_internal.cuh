@@ -85,9 +85,21 @@ constexpr int kAttnWarps = 4;     // warps per attention / logits CTA
 struct RowMap {
   const int32_t* table;
   int32_t page;        // tokens per page
-  int32_t max_pages;   // entries per table row (capacity = max_pages * page)
+  int32_t max_pages;   // entries per table row (capacity = max_pages * page < 2^31)
   int32_t num_pages;   // pages in the cache; other entries are rejected
+  int32_t page_shift;  // log2(page) for a power-of-two page, else -1
 };
+
+// Page index and offset within the page of token t.
+__device__ __forceinline__ void split_token(const RowMap& m, uint32_t t, uint32_t& pi, uint32_t& off) {
+  if (m.page_shift >= 0) {
+    pi = t >> m.page_shift;
+    off = t & (uint32_t)(m.page - 1);
+  } else {
+    pi = t / (uint32_t)m.page;
+    off = t - pi * (uint32_t)m.page;
+  }
+}
 
 // Destination rows of a cache append: rows 0..n-1, an explicit list, or for a
 // paged cache the last token (seq_lens[b] - 1) of each (b, kvh) of a batch of
@@ -111,13 +123,14 @@ __device__ __forceinline__ int64_t append_row(const AppendDst& a, int64_t row, i
   int64_t dst;
   if (a.map.table) {
     const int b = (int)(row / a.Hkv), kvh = (int)(row - (int64_t)b * a.Hkv);
-    const int64_t t = (int64_t)a.seq_lens[b] - 1;
+    const int32_t t = a.seq_lens[b] - 1;
     if (t < 0) return -1;
-    const int64_t pi = t / a.map.page;
-    if (pi >= a.map.max_pages) return -2;
+    uint32_t pi, off;
+    split_token(a.map, (uint32_t)t, pi, off);
+    if (pi >= (uint32_t)a.map.max_pages) return -2;
     const int32_t pg = a.map.table[(int64_t)b * a.map.max_pages + pi];
     if (pg < 0 || pg >= a.map.num_pages) return -2;
-    dst = ((int64_t)pg * a.Hkv + kvh) * a.map.page + (t - pi * a.map.page);
+    dst = ((int64_t)pg * a.Hkv + kvh) * a.map.page + off;
   } else {
     dst = a.rows ? a.rows[row] : row;
   }

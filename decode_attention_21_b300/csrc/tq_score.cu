@@ -493,18 +493,38 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
   if (tile0 >= tcap) return;
   const uint8_t* gnrm = kcache + norm_offset(cb, cache_rows);
-  // stage st (tiles st*kStageTiles ..) into ring slot st % kRing, one copy
-  // per run of consecutive cache rows (one run unless the cache is paged)
+  // Stage st (tiles st*kStageTiles ..) into ring slot st % kRing; every
+  // thread calls this and warp 0 issues the copies: one per array for a
+  // contiguous cache, one per array and page touched for a paged one.
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
     const uint32_t bar = su32(&bars[slot]);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)(t_n * 16 * (RB + NB)))
-                 : "memory");
-    for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16, t_n * 16, status,
-             [&](int64_t row, int k, int cnt) {
-               bulk_g2s(su32(srec + (size_t)slot * kStageRec + (size_t)k * RB), kcache + row * RB, (uint32_t)(cnt * RB), bar);
-               bulk_g2s(su32(snrm + (size_t)slot * kStageNrm + (size_t)k * NB), gnrm + row * NB, (uint32_t)(cnt * NB), bar);
-             });
+    if (warp == 0) {
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(t_n * 16 * (RB + NB)))
+                     : "memory");
+      const int64_t t0 = (tile0 + (int64_t)st * kStageTiles) * 16;
+      if (map.table == nullptr) {
+        if (lane == 0) {
+          const int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
+          bulk_g2s(su32(srec + (size_t)slot * kStageRec), kcache + row * RB, (uint32_t)(t_n * 16 * RB), bar);
+          bulk_g2s(su32(snrm + (size_t)slot * kStageNrm), gnrm + row * NB, (uint32_t)(t_n * 16 * NB), bar);
+        }
+      } else {
+        // paged: lane 2r + a copies array a (records, norms) of the stage's
+        // run r (its tokens in one page), so the runs' table lookups and
+        // copies are issued in parallel
+        int k, cnt;
+        int64_t row;
+        if (lane < 2 * kStageTiles && page_run(map, b, kvh, Hkv, t0, t_n * 16, lane >> 1, status, k, cnt, row)) {
+          if (lane & 1)
+            bulk_g2s(su32(snrm + (size_t)slot * kStageNrm + (size_t)k * NB), gnrm + row * NB, (uint32_t)(cnt * NB), bar);
+          else
+            bulk_g2s(su32(srec + (size_t)slot * kStageRec + (size_t)k * RB), kcache + row * RB, (uint32_t)(cnt * RB), bar);
+        }
+      }
+    }
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -516,25 +536,31 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
   // Stream the first kPrefetchStages stages of the chunk from HBM into L2
   // while the prep (and any cache append before it) still runs.
-  if (tid == 0)
-    for (int st = 0; st < min(nst, kPrefetchStages); ++st)
-      for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16,
-               min(kStageTiles, nt - st * kStageTiles) * 16, status, [&](int64_t row, int, int cnt) {
-                 prefetch_l2(kcache + row * RB, (uint32_t)(cnt * RB));
-                 prefetch_l2(gnrm + row * NB, (uint32_t)(cnt * NB));
-               });
+  if (warp == 0)
+    for (int st = 0; st < min(nst, kPrefetchStages); ++st) {
+      const int64_t t0 = (tile0 + (int64_t)st * kStageTiles) * 16;
+      const int n = min(kStageTiles, nt - st * kStageTiles) * 16;
+      int k = 0, cnt = n;
+      int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
+      if (map.table ? (lane < 2 * kStageTiles && page_run(map, b, kvh, Hkv, t0, n, lane >> 1, status, k, cnt, row))
+                    : lane < 2) {
+        if (lane & 1)
+          prefetch_l2(gnrm + row * NB, (uint32_t)(cnt * NB));
+        else
+          prefetch_l2(kcache + row * RB, (uint32_t)(cnt * RB));
+      }
+    }
   // The query fragments come from the preceding prep grid, launched as its
   // programmatic dependent; the prep's completion also implies that of any
   // cache append before it, so no cache row is read into the SM before this
   // wait.  The first stage goes out right after it, the fragment loads queue
   // behind only that stage, and the other stages follow.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
+  if (nst > 0) request(0, min(kStageTiles, nt));
   QK16<NV, P, QJL> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, cb);
   __syncthreads();                           // the barriers are initialised; the fragments are in
-  if (tid == 0)
-    for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
+  for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
   int issued = min(nst, kRing);              // stages requested so far
   // ---- scoring
   const float kq = cb.qjl_const;
@@ -627,7 +653,7 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     // every warp is done with this ring slot: refill it with stage st + kRing
     if (st + kRing < nst) {
       __syncthreads();
-      if (tid == 0) request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
+      request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
       issued = st + kRing + 1;
     }
   }
@@ -837,22 +863,43 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
   const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows);
   const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows);
-  // stage st into ring slot st % kRing, one copy per run of consecutive cache
-  // rows (one run unless the cache is paged)
+  // Stage st into ring slot st % kRing.  Every thread calls this and warp 0
+  // issues the copies: one per array for a contiguous cache, one per array
+  // and page touched for a paged one.
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
     const uint32_t bar = su32(&bars[slot]);
     uint8_t* base = sm + (size_t)slot * kSlot;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                 "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
-                 : "memory");
-    for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16, t_n * 16, status,
-             [&](int64_t row, int k, int cnt) {
-               bulk_g2s(su32(base + k * RBK), kcache + row * RBK, (uint32_t)(cnt * RBK), bar);
-               bulk_g2s(su32(base + kSK + k * 4), gkn + row * 4, (uint32_t)(cnt * 4), bar);
-               bulk_g2s(su32(base + kSK + kSKN + k * RBV), vcache + row * RBV, (uint32_t)(cnt * RBV), bar);
-               bulk_g2s(su32(base + kSK + kSKN + kSV + k * 2), gvn + row * 2, (uint32_t)(cnt * 2), bar);
-             });
+    if (warp == 0) {
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
+                     : "memory");
+      const int64_t t0 = (tile0 + (int64_t)st * kStageTiles) * 16;
+      if (map.table == nullptr) {
+        if (lane == 0) {
+          const int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
+          const uint32_t n = (uint32_t)(t_n * 16);
+          bulk_g2s(su32(base), kcache + row * RBK, n * RBK, bar);
+          bulk_g2s(su32(base + kSK), gkn + row * 4, n * 4, bar);
+          bulk_g2s(su32(base + kSK + kSKN), vcache + row * RBV, n * RBV, bar);
+          bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + row * 2, n * 2, bar);
+        }
+      } else {
+        // paged: lane 4r + a copies array a (key records, key norms, value
+        // records, value norms) of the stage's run r (its tokens in one page),
+        // so the runs' table lookups and copies are issued in parallel
+        int k, cnt;
+        int64_t row;
+        if (page_run(map, b, kvh, Hkv, t0, t_n * 16, lane >> 2, status, k, cnt, row)) {
+          const int a = lane & 3;
+          const int rb = a == 0 ? RBK : a == 1 ? 4 : a == 2 ? RBV : 2;
+          const int off = a == 0 ? 0 : a == 1 ? kSK : a == 2 ? kSK + kSKN : kSK + kSKN + kSV;
+          const uint8_t* g = a == 0 ? kcache : a == 1 ? gkn : a == 2 ? vcache : gvn;
+          bulk_g2s(su32(base + off + k * rb), g + row * rb, (uint32_t)(cnt * rb), bar);
+        }
+      }
+    }
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -863,25 +910,28 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
   // the first stages stream from HBM into L2 while the prep still runs
-  if (tid == 0)
-    for (int st = 0; st < min(nst, kRing); ++st)
-      for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16,
-               min(kStageTiles, nt - st * kStageTiles) * 16, status, [&](int64_t row, int, int cnt) {
-                 prefetch_l2(kcache + row * RBK, (uint32_t)(cnt * RBK));
-                 prefetch_l2(gkn + row * 4, (uint32_t)(cnt * 4));
-                 prefetch_l2(vcache + row * RBV, (uint32_t)(cnt * RBV));
-                 prefetch_l2(gvn + row * 2, (uint32_t)(cnt * 2));
-               });
+  if (warp == 0)
+    for (int st = 0; st < min(nst, kRing); ++st) {
+      const int64_t t0 = (tile0 + (int64_t)st * kStageTiles) * 16;
+      const int n = min(kStageTiles, nt - st * kStageTiles) * 16;
+      int k = 0, cnt = n;
+      int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
+      if (map.table ? page_run(map, b, kvh, Hkv, t0, n, lane >> 2, status, k, cnt, row) : lane < 4) {
+        const int a = lane & 3;
+        const int rb = a == 0 ? RBK : a == 1 ? 4 : a == 2 ? RBV : 2;
+        const uint8_t* g = a == 0 ? kcache : a == 1 ? gkn : a == 2 ? vcache : gvn;
+        prefetch_l2(g + row * rb, (uint32_t)(cnt * rb));
+      }
+    }
   // query fragments come from the preceding prep grid (whose completion also
   // implies that of any cache append before it): no cache row is read into
   // the SM before this wait; the first stage goes out right after it
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0 && nst > 0) request(0, min(kStageTiles, nt));
+  if (nst > 0) request(0, min(kStageTiles, nt));
   QK16<NVK, PK> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, kcb);
   __syncthreads();
-  if (tid == 0)
-    for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
+  for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
   int issued = min(nst, kRing);
 
   float m_run = -INFINITY, l_run = 0.f, wsum = 0.f;
@@ -998,7 +1048,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
     // every warp is done with this ring slot: refill it with stage st + kRing
     if (st + kRing < nst) {
       __syncthreads();
-      if (tid == 0) request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
+      request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
       issued = st + kRing + 1;
     }
   }
@@ -1236,7 +1286,8 @@ static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& 
 
 cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq,
                                int Hkv, int64_t capacity, int64_t rows, const RowMap& map, const int32_t* seq_lens,
-                               const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc, int* status, cudaStream_t s) {
+                               const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc, int* status,
+                               cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
   switch (kcb.b1) {
     case 1: return attn_staged_v<1, 2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);

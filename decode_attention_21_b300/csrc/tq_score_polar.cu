@@ -471,22 +471,43 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   const int64_t tcap = min(tile0 + tiles_per_cta, capacity / 16);
   const uint8_t* gkn = kcache + norm_offset(kcb, cache_rows);
   const uint8_t* gvn = vcache + norm_offset(vcb, cache_rows);
-  // stage st into ring slot st % kRing, one copy per run of consecutive cache
-  // rows (one run unless the cache is paged)
+  // Stage st into ring slot st % kRing.  Every thread calls this and warp 0
+  // issues the copies: one per array for a contiguous cache, one per array
+  // and page touched for a paged one.
   auto request = [&](int st, int t_n) {
     const int slot = st % kRing;
     const uint32_t bar = su32(&bars[slot]);
     uint8_t* base = sm + (size_t)slot * kSlot;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                 "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
-                 : "memory");
-    for_runs(map, b, kvh, Hkv, capacity, (tile0 + (int64_t)st * kStageTiles) * 16, t_n * 16, status,
-             [&](int64_t row, int k, int cnt) {
-               bulk_g2s(su32(base + k * RBK), kcache + row * RBK, (uint32_t)(cnt * RBK), bar);
-               bulk_g2s(su32(base + kSK + k * 4), gkn + row * 4, (uint32_t)(cnt * 4), bar);
-               bulk_g2s(su32(base + kSK + kSKN + k * RBV), vcache + row * RBV, (uint32_t)(cnt * RBV), bar);
-               bulk_g2s(su32(base + kSK + kSKN + kSV + k * 2), gvn + row * 2, (uint32_t)(cnt * 2), bar);
-             });
+    if (warp == 0) {
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
+                     : "memory");
+      const int64_t t0 = (tile0 + (int64_t)st * kStageTiles) * 16;
+      if (map.table == nullptr) {
+        if (lane == 0) {
+          const int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
+          const uint32_t n = (uint32_t)(t_n * 16);
+          bulk_g2s(su32(base), kcache + row * RBK, n * RBK, bar);
+          bulk_g2s(su32(base + kSK), gkn + row * 4, n * 4, bar);
+          bulk_g2s(su32(base + kSK + kSKN), vcache + row * RBV, n * RBV, bar);
+          bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + row * 2, n * 2, bar);
+        }
+      } else {
+        // paged: lane 4r + a copies array a (key records, key norms, value
+        // records, value norms) of the stage's run r (its tokens in one page),
+        // so the runs' table lookups and copies are issued in parallel
+        int k, cnt;
+        int64_t row;
+        if (page_run(map, b, kvh, Hkv, t0, t_n * 16, lane >> 2, status, k, cnt, row)) {
+          const int a = lane & 3;
+          const int rb = a == 0 ? RBK : a == 1 ? 4 : a == 2 ? RBV : 2;
+          const int off = a == 0 ? 0 : a == 1 ? kSK : a == 2 ? kSK + kSKN : kSK + kSKN + kSV;
+          const uint8_t* g = a == 0 ? kcache : a == 1 ? gkn : a == 2 ? vcache : gvn;
+          bulk_g2s(su32(base + off + k * rb), g + row * rb, (uint32_t)(cnt * rb), bar);
+        }
+      }
+    }
   };
   if (tid == 0) {
     for (int k = 0; k < kRing; ++k) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bars[k])));
@@ -496,8 +517,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
-  if (tid == 0)
-    for (int st = 0; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
+  for (int st = 0; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
   int issued = min(nst, kRing);
   const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
   const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
@@ -609,7 +629,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
     }
     if (st + kRing < nst) {
       __syncthreads();
-      if (tid == 0) request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
+      request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
       issued = st + kRing + 1;
     }
   }
@@ -660,8 +680,8 @@ static cudaError_t attn_polar_staged_v(int bv, dim3 grid, cudaStream_t s, const 
 
 cudaError_t launch_attn_polar_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B,
                                      int Hq, int Hkv, int64_t capacity, int64_t rows, const RowMap& map,
-                                     const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc,
-                                     int* status, cudaStream_t s) {
+                                     const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* parts,
+                                     int nchunks, int tpc, int* status, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
   switch (kcb.b1) {
     case 1: return attn_polar_staged_v<1>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);

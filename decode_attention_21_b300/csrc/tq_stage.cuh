@@ -31,31 +31,26 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// Visit the runs of consecutive cache rows holding tokens t0 .. t0 + n - 1 of
-// (b, kvh) (t0 and n multiples of 16, t0 + n <= capacity): f(row, k, count)
-// for tokens t0 + k .. t0 + k + count - 1 starting at cache row `row`.  A
-// block-table entry outside the cache sets kBadRow in *status and reads
-// page 0 instead, so every copy stays inside the cache.
-template <class F>
-__device__ __forceinline__ void for_runs(const RowMap& map, int b, int kvh, int Hkv, int64_t capacity, int64_t t0,
-                                         int n, int* status, F&& f) {
-  if (!map.table) {
-    f(((int64_t)b * Hkv + kvh) * capacity + t0, 0, n);
-    return;
+// Run r (r = 0, 1, ..) of the tokens t0 .. t0 + n - 1 of (b, kvh) in a paged
+// cache, i.e. the part of them in their (r+1)-th page: false if there is no
+// such run; else its first token k (relative to t0), its token count and its
+// first cache row.  Runs are independent, so the lanes of a warp can each
+// look up and copy one.
+__device__ __forceinline__ bool page_run(const RowMap& map, int b, int kvh, int Hkv, int64_t t0, int n, int r,
+                                         int* status, int& k, int& cnt, int64_t& row) {
+  uint32_t p0, o0;
+  split_token(map, (uint32_t)t0, p0, o0);
+  const int first = min(n, map.page - (int)o0);
+  k = r == 0 ? 0 : first + (r - 1) * map.page;
+  if (k >= n) return false;
+  cnt = r == 0 ? first : min(n - k, map.page);
+  int32_t pg = __ldg(map.table + (int64_t)b * map.max_pages + p0 + r);
+  if (pg < 0 || pg >= map.num_pages) {
+    atomicOr(status, kBadRow);
+    pg = 0;
   }
-  for (int k = 0; k < n;) {
-    const int64_t t = t0 + k;
-    const int64_t pi = t / map.page;
-    const int off = (int)(t - pi * map.page);
-    const int cnt = min(n - k, map.page - off);
-    int32_t pg = __ldg(map.table + (int64_t)b * map.max_pages + pi);
-    if (pg < 0 || pg >= map.num_pages) {
-      atomicOr(status, kBadRow);
-      pg = 0;
-    }
-    f(((int64_t)pg * Hkv + kvh) * map.page + off, k, cnt);
-    k += cnt;
-  }
+  row = ((int64_t)pg * Hkv + kvh) * map.page + (r == 0 ? o0 : 0);
+  return true;
 }
 
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {

@@ -217,7 +217,7 @@ tq_status tq_decode_attention_static(const tq_codebook* kcb, const tq_codebook* 
  *   block_table  device int32 [B, max_pages]: token t of sequence b lives in
  *                page block_table[b*max_pages + t/page_size], slot
  *                t % page_size; entries for pages past seq_lens[b] are not read
- *   capacity     max_pages * page_size tokens per sequence
+ *   capacity     max_pages * page_size tokens per sequence (below 2^31)
  * The kernels read the table and seq_lens without validating them against the
  * host: a table entry outside 0..num_pages-1 is never dereferenced (a read
  * goes to page 0 instead, a write is skipped) and sets a flag that the next
