@@ -87,11 +87,12 @@ bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t c
 
 constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
 constexpr int kLogitsCtas = 148 * 4;   // resident CTAs of the logits kernel
-// Resident CTAs of the attention kernel (one wave): 4 per SM, 3 for 4-bit
-// keys (more registers), 2 in polar mode.
+// Resident CTAs of the attention kernel (one wave): 4 per SM, 3 for keys
+// with four or more stage-1 virtual planes or extra-bit words (more
+// registers), 2 in polar mode.
 int attn_ctas(const tq_codebook* kcb) {
   if (kcb->dev.mode == TQ_MODE_POLAR) return 148 * 2;
-  return kcb->dev.b1 == 3 ? 148 * 3 : 148 * 4;
+  return kcb->dev.nv >= 4 || kcb->dev.extra > 0 ? 148 * 3 : 148 * 4;
 }
 
 template <class T>
@@ -644,8 +645,19 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
                              int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q, float scale,
                              float* out, void* workspace, size_t ws_bytes, void* stream) {
   tq_status st;
-  if ((st = check_scoring_codebook(kcb, TQ_KIND_PROD, "tq_decode_attention(keys)")) != TQ_OK) return st;
+  // keys: with the QJL term (PROD, 2.5 / 3.5-bit mixed included) or MSE-only
+  if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD,
+                                   "tq_decode_attention(keys)", true)) != TQ_OK)
+    return st;
   if ((st = check_scoring_codebook(vcb, TQ_KIND_MSE, "tq_decode_attention(values)")) != TQ_OK) return st;
+  if (kcb->dev.kind == TQ_KIND_MSE || kcb->dev.extra != 0) {
+    if (kcb->dev.mode != TQ_MODE_SCALAR || vcb->dev.mode != TQ_MODE_SCALAR)
+      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit keys are attended in scalar mode only", what);
+    if (!tq::attn_staged_supports(kcb->dev, vcb->dev))
+      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit keys are paired with 3- or 4-bit values only", what);
+    if (capacity % 16 != 0 && !map.table)
+      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit keys need a capacity that is a multiple of 16", what);
+  }
   if ((st = check_heads(what, B, Hq, Hkv, capacity)) != TQ_OK) return st;
   if (!kcache || !vcache || !seq_lens || !q || !out || !workspace)
     return fail(TQ_EINVAL, "%s: NULL device pointer", what);

@@ -159,6 +159,8 @@ cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc
                                int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const RowMap& map,
                                const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* partials,
                                int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
+// Key / value codebook pairs the staged scalar attention kernel is built for.
+bool attn_staged_supports(const Dev& kcb, const Dev& vcb);
 cudaError_t launch_attn_polar_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache,
                                      int B, int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const RowMap& map,
                                      const int32_t* seq_lens, const uint8_t* prep, float scale_log2, float* partials,

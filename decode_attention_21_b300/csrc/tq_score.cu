@@ -832,6 +832,11 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
   }
 }
 
+// Resident CTAs per SM of the staged attention kernel: 4, or 3 where the key
+// side needs more registers (4 virtual planes, or extra-bit words).  The host
+// sizes the grid to one wave of the same count.
+constexpr int attn_min_blocks(int nvk, int extk) { return nvk >= 4 || extk > 0 ? 3 : 4; }
+
 // ---------------------------------------------------------------------------
 // Fused decode attention with bulk-copy staging (capacity a multiple of 16),
 // launched as the programmatic dependent of the query prep.  Same arithmetic
@@ -841,8 +846,8 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
 // query fragments are loaded), and each warp scores tiles warp and warp + 4
 // of every stage.
 // ---------------------------------------------------------------------------
-template <int NVK, int PK, int NVV, int PV>
-__global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev kcb, const Dev vcb,
+template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK>
+__global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged(const Dev kcb, const Dev vcb,
                                                      const uint8_t* __restrict__ kcache,
                                                      const uint8_t* __restrict__ vcache, int Hq, int Hkv,
                                                      int64_t capacity, int64_t cache_rows, const RowMap map,
@@ -850,8 +855,10 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
                                                      const uint8_t* __restrict__ prep, float scale_log2,
                                                      float* __restrict__ partials, int tiles_per_cta,
                                                      int* __restrict__ status) {
-  constexpr int RBK = 16 * PK, RBV = 16 * PV;    // record bytes at d = 128
-  constexpr int kSK = kStageTiles * 16 * RBK, kSKN = kStageTiles * 16 * 4;
+  constexpr int RBK = 16 * PK + 4 * EXTK;       // key record bytes at d = 128 (+ extra-bit words)
+  constexpr int RBV = 16 * PV;                  // value record bytes
+  constexpr int NBK = QJLK ? 4 : 2;             // key norm entry bytes
+  constexpr int kSK = kStageTiles * 16 * RBK, kSKN = kStageTiles * 16 * NBK;
   constexpr int kSV = kStageTiles * 16 * RBV, kSVN = kStageTiles * 16 * 2;
   constexpr int kSlot = kSK + kSKN + kSV + kSVN;
   extern __shared__ __align__(16) uint8_t sm[];
@@ -873,7 +880,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
     if (warp == 0) {
       if (lane == 0)
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"((uint32_t)(t_n * 16 * (RBK + 4 + RBV + 2)))
+                     "r"((uint32_t)(t_n * 16 * (RBK + NBK + RBV + 2)))
                      : "memory");
       const int64_t t0 = (tile0 + (int64_t)st * kStageTiles) * 16;
       if (map.table == nullptr) {
@@ -881,7 +888,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
           const int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
           const uint32_t n = (uint32_t)(t_n * 16);
           bulk_g2s(su32(base), kcache + row * RBK, n * RBK, bar);
-          bulk_g2s(su32(base + kSK), gkn + row * 4, n * 4, bar);
+          bulk_g2s(su32(base + kSK), gkn + row * NBK, n * NBK, bar);
           bulk_g2s(su32(base + kSK + kSKN), vcache + row * RBV, n * RBV, bar);
           bulk_g2s(su32(base + kSK + kSKN + kSV), gvn + row * 2, n * 2, bar);
         }
@@ -893,7 +900,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
         int64_t row;
         if (page_run(map, b, kvh, Hkv, t0, t_n * 16, lane >> 2, status, k, cnt, row)) {
           const int a = lane & 3;
-          const int rb = a == 0 ? RBK : a == 1 ? 4 : a == 2 ? RBV : 2;
+          const int rb = a == 0 ? RBK : a == 1 ? NBK : a == 2 ? RBV : 2;
           const int off = a == 0 ? 0 : a == 1 ? kSK : a == 2 ? kSK + kSKN : kSK + kSKN + kSV;
           const uint8_t* g = a == 0 ? kcache : a == 1 ? gkn : a == 2 ? vcache : gvn;
           bulk_g2s(su32(base + off + k * rb), g + row * rb, (uint32_t)(cnt * rb), bar);
@@ -918,7 +925,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
       int64_t row = ((int64_t)b * Hkv + kvh) * capacity + t0;
       if (map.table ? page_run(map, b, kvh, Hkv, t0, n, lane >> 2, status, k, cnt, row) : lane < 4) {
         const int a = lane & 3;
-        const int rb = a == 0 ? RBK : a == 1 ? 4 : a == 2 ? RBV : 2;
+        const int rb = a == 0 ? RBK : a == 1 ? NBK : a == 2 ? RBV : 2;
         const uint8_t* g = a == 0 ? kcache : a == 1 ? gkn : a == 2 ? vcache : gvn;
         prefetch_l2(g + row * rb, (uint32_t)(cnt * rb));
       }
@@ -928,7 +935,7 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
   // the SM before this wait; the first stage goes out right after it
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (nst > 0) request(0, min(kStageTiles, nt));
-  QK16<NVK, PK> qk;
+  QK16<NVK, PK, QJLK> qk;
   qk.load(prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128), lane, kcb);
   __syncthreads();
   for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
@@ -959,29 +966,41 @@ __global__ void __launch_bounds__(128, NVK == 4 ? 3 : 4) k_attn_staged(const Dev
     }
     const uint8_t* base = sm + (size_t)slot * kSlot;
     const uint8_t* sk = base;
-    const uint32_t* skn = reinterpret_cast<const uint32_t*>(base + kSK);
+    const uint8_t* skn = base + kSK;
     const uint8_t* sv = base + kSK + kSKN;
     const __half* svn = reinterpret_cast<const __half*>(base + kSK + kSKN + kSV);
     const int t_a = st * kStageTiles, n_here = min(kStageTiles, nt - t_a);
     for (int lt = warp; lt < n_here; lt += 4) {
       const int64_t t0 = (tile0 + t_a + lt) * 16;       // first token of the tile
       const int64_t ta = t0 + g, tb = ta + 8;
-      // keys g and g+8: column c words
-      uint32_t wa[1][PK], wb[1][PK];
+      // keys g and g+8: column c words (+ the extra-bit word of column c)
+      uint32_t wa[1][PK], wb[1][PK], ea[1] = {0u}, eb[1] = {0u};
       {
-        const uint32_t* ka = reinterpret_cast<const uint32_t*>(sk + ((size_t)lt * 16 + g) * RBK) + c * PK;
-        const uint32_t* kb2 = reinterpret_cast<const uint32_t*>(sk + ((size_t)lt * 16 + g + 8) * RBK) + c * PK;
+        const uint32_t* ka = reinterpret_cast<const uint32_t*>(sk + ((size_t)lt * 16 + g) * RBK);
+        const uint32_t* kb2 = reinterpret_cast<const uint32_t*>(sk + ((size_t)lt * 16 + g + 8) * RBK);
 #pragma unroll
         for (int p = 0; p < PK; ++p) {
-          wa[0][p] = ka[p];
-          wb[0][p] = kb2[p];
+          wa[0][p] = ka[c * PK + p];
+          wb[0][p] = kb2[c * PK + p];
+        }
+        if (EXTK > 0 && c < EXTK) {
+          ea[0] = ka[4 * PK + c];
+          eb[0] = kb2[4 * PK + c];
         }
       }
       float s1[1][2], s2[1][2];
-      qk.template score<1>(wa, wb, s1, s2);
+      qk.template score_mixed<1, EXTK>(wa, wb, ea, eb, s1, s2);
+      uint32_t na, nb;
+      if constexpr (QJLK) {
+        na = reinterpret_cast<const uint32_t*>(skn)[lt * 16 + g];
+        nb = reinterpret_cast<const uint32_t*>(skn)[lt * 16 + g + 8];
+      } else {
+        na = reinterpret_cast<const unsigned short*>(skn)[lt * 16 + g];
+        nb = reinterpret_cast<const unsigned short*>(skn)[lt * 16 + g + 8];
+      }
       // scores in log2 units
-      const float sa = ta < L ? est_from(skn[lt * 16 + g], s1[0][0], s2[0][0], kq) * scale_log2 : -INFINITY;
-      const float sb = tb < L ? est_from(skn[lt * 16 + g + 8], s1[0][1], s2[0][1], kq) * scale_log2 : -INFINITY;
+      const float sa = ta < L ? est_key<QJLK>(na, s1[0][0], s2[0][0], kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L ? est_key<QJLK>(nb, s1[0][1], s2[0][1], kq) * scale_log2 : -INFINITY;
       float mx = fmaxf(sa, sb);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
@@ -1246,15 +1265,16 @@ cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq
 }
 #undef TQ_LOGITS_DISPATCH
 
-template <int NVK, int PK, int NVV, int PV>
+template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK>
 static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
-                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map, const int32_t* sl,
-                                 const uint8_t* prep, float sl2, float* parts, int tpc, int* status) {
-  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 + 16 * PV + 2);
-  static cudaError_t configured = [] {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_staged<NVK, PK, NVV, PV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_attn_staged<NVK, PK, NVV, PV>));
+                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map,
+                                 const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
+                                 int* status) {
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 * EXTK + (QJLK ? 4 : 2) + 16 * PV + 2);
+  auto kern = k_attn_staged<NVK, PK, NVV, PV, QJLK, EXTK>;
+  static cudaError_t configured = [&] {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(kern));
     return e;
   }();
   if (configured != cudaSuccess) return configured;
@@ -1268,20 +1288,41 @@ static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_attn_staged<NVK, PK, NVV, PV>, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2,
-                            parts, tpc, status);
+  return cudaLaunchKernelEx(&cfg, kern, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
 }
 
-template <int NVK, int PK>
+// Value codebooks: every b' for keys with the QJL term and no extra bits;
+// b = 3 and 4 for MSE-only and mixed-bit keys (other pairs are rejected by
+// the host before launch).
+template <int NVK, int PK, bool QJLK, int EXTK>
 static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
-                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map, const int32_t* sl,
-                                 const uint8_t* prep, float sl2, float* parts, int tpc, int* status) {
-  switch (b1v) {
-    case 1: return attn_staged_t<NVK, PK, 1, 1>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
-    case 2: return attn_staged_t<NVK, PK, 2, 2>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
-    case 3: return attn_staged_t<NVK, PK, 4, 3>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
-    default: return attn_staged_t<NVK, PK, 8, 4>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, sl2, parts, tpc, status);
+                                 const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map,
+                                 const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
+                                 int* status) {
+#define TQ_ATTN_V(NVV, PV)                                                                                      \
+  return attn_staged_t<NVK, PK, NVV, PV, QJLK, EXTK>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, \
+                                                     sl2, parts, tpc, status)
+  if constexpr (QJLK && EXTK == 0) {
+    switch (b1v) {
+      case 1: TQ_ATTN_V(1, 1);
+      case 2: TQ_ATTN_V(2, 2);
+      case 3: TQ_ATTN_V(4, 3);
+      default: TQ_ATTN_V(8, 4);
+    }
+  } else {
+    switch (b1v) {
+      case 3: TQ_ATTN_V(4, 3);
+      case 4: TQ_ATTN_V(8, 4);
+      default: return cudaErrorInvalidValue;
+    }
   }
+#undef TQ_ATTN_V
+}
+
+bool attn_staged_supports(const Dev& kcb, const Dev& vcb) {
+  if (kcb.mode != 0 || vcb.mode != 0 || vcb.extra != 0) return false;
+  const bool plain_keys = kcb.kind == 0 && kcb.extra == 0;
+  return plain_keys || vcb.b1 == 3 || vcb.b1 == 4;
 }
 
 cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq,
@@ -1289,11 +1330,29 @@ cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc
                                const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc, int* status,
                                cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
-  switch (kcb.b1) {
-    case 1: return attn_staged_v<1, 2>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
-    case 2: return attn_staged_v<2, 3>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
-    default: return attn_staged_v<4, 4>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, prep, scale_log2, parts, tpc, status);
+#define TQ_ATTN_K(NVK, PK, Q, X)                                                                                  \
+  return attn_staged_v<NVK, PK, Q, X>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, \
+                                      prep, scale_log2, parts, tpc, status)
+  if (kcb.kind == 0) {
+    switch (kcb.b1 * 4 + kcb.extra / 32) {
+      case 4: TQ_ATTN_K(1, 2, true, 0);
+      case 5: TQ_ATTN_K(1, 2, true, 1);
+      case 6: TQ_ATTN_K(1, 2, true, 2);
+      case 8: TQ_ATTN_K(2, 3, true, 0);
+      case 9: TQ_ATTN_K(2, 3, true, 1);
+      case 10: TQ_ATTN_K(2, 3, true, 2);
+      case 13: TQ_ATTN_K(4, 4, true, 1);
+      case 14: TQ_ATTN_K(4, 4, true, 2);
+      default: TQ_ATTN_K(4, 4, true, 0);
+    }
   }
+  switch (kcb.b1) {
+    case 1: TQ_ATTN_K(1, 1, false, 0);
+    case 2: TQ_ATTN_K(2, 2, false, 0);
+    case 3: TQ_ATTN_K(4, 3, false, 0);
+    default: TQ_ATTN_K(8, 4, false, 0);
+  }
+#undef TQ_ATTN_K
 }
 
 cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const uint8_t* vc, int B, int Hq, int Hkv,

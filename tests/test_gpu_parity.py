@@ -273,6 +273,59 @@ def test_attention_parity(kb, vb, mode, B, Hq, Hkv, cap, lens):
             rowwise_ok(got[b], ref[b])
 
 
+@pytest.mark.parametrize("kkind,kbits,kextra", [("mse", 3, 0), ("mse", 4, 0), ("mse", 2, 0), ("prod", 3, 32),
+                                                ("prod", 4, 32), ("prod", 2, 64), ("prod", 4, 64)])
+@pytest.mark.parametrize("vb", [3, 4])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 304, [300, 1, 0])])
+def test_attention_parity_key_variants(kkind, kbits, kextra, vb, B, Hq, Hkv, cap, lens):
+    """Decode attention over MSE-only keys (no QJL term) and over mixed-bit
+    keys (the first `extra` rotated coordinates carry one more stage-1 bit),
+    with 3- or 4-bit values."""
+    okc, gkc = pair(128, kbits, kkind, extra=kextra)
+    ovc, gvc = pair(128, vb, "mse", seed_pi=1)
+    rows = B * Hkv * cap
+    K = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="keys") for h in range(B * Hkv)])
+    V = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="values") for h in range(B * Hkv)])
+    kcode, kimg = oracle_cache(okc, rows, K.astype(np.float64))
+    vcode, vimg = oracle_cache(ovc, rows, V.astype(np.float64))
+    q = wl.queries((B, Hq, 128))
+    scale = 1.0 / math.sqrt(128)
+    ref = estimate.attention(okc, ovc, kcode, vcode, q.astype(np.float64), lens, Hkv, cap, scale)
+    ws = torch.empty(tq.tq_decode_attention_workspace(gkc, B, Hq, Hkv, cap), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    tq.tq_decode_attention(gkc, gvc, torch.from_numpy(kimg).cuda(), torch.from_numpy(vimg).cuda(), B, Hq, Hkv, cap,
+                           torch.tensor(lens, dtype=torch.int32, device="cuda"), torch.from_numpy(q).cuda(), scale,
+                           out, ws)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gkc)
+    got = out.cpu().numpy()
+    for b in range(B):
+        if lens[b] == 0:
+            assert np.all(got[b] == 0)
+        else:
+            rowwise_ok(got[b], ref[b])
+
+
+def test_attention_key_variants_unsupported_pairs():
+    """MSE-only or mixed-bit keys with 1- or 2-bit values, in polar mode, or at
+    a capacity that is not a multiple of 16 are rejected before any launch."""
+    _, gk = pair(128, 3, "mse")
+    _, gm = pair(128, 3, "prod", extra=32)
+    _, gv2 = pair(128, 2, "mse", seed_pi=1)
+    _, gv3 = pair(128, 3, "mse", seed_pi=1)
+    B, Hq, Hkv = 1, 4, 1
+    sl = torch.tensor([10], dtype=torch.int32, device="cuda")
+    q = torch.zeros((B, Hq, 128), device="cuda")
+    out = torch.zeros((B, Hq, 128), device="cuda")
+    for kcb, vcb, cap in ((gk, gv2, 64), (gm, gv2, 64), (gk, gv3, 40), (gm, gv3, 40)):
+        kc = torch.zeros(tq.cache_bytes(kcb, cap), dtype=torch.uint8, device="cuda")
+        vc = torch.zeros(tq.cache_bytes(vcb, cap), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(tq.tq_decode_attention_workspace(kcb, B, Hq, Hkv, cap), dtype=torch.uint8, device="cuda")
+        with pytest.raises(tq.TqError) as e:
+            tq.tq_decode_attention(kcb, vcb, kc, vc, B, Hq, Hkv, cap, sl, q, 0.1, out, ws)
+        assert e.value.status == tq.TQ_EUNSUPPORTED
+
+
 def test_attention_long_context_ring_refill():
     """2 sequences x 8 kv heads at context 16384: chunks of more tiles than
     the staging ring holds.  Keys and values repeat 4096 oracle-coded rows;
@@ -352,9 +405,8 @@ def test_invalid_arguments_return_status_without_launch():
     with pytest.raises(tq.TqError) as e:
         tq.tq_logits(pcb, kc, 1, 4, 1, 64, sl, q, out, ws)       # MSE-only keys in polar mode
     assert e.value.status == tq.TQ_EUNSUPPORTED
-    _, vcb = pair(128, 3, "mse")
-    with pytest.raises(tq.TqError) as e:                         # MSE-only keys in attention
-        tq.tq_decode_attention(vcb, vcb, kc, kc, 1, 4, 1, 64, sl, q, 0.1, out, ws)
+    with pytest.raises(tq.TqError) as e:                         # values of kind PROD
+        tq.tq_decode_attention(gcb, gcb, kc, kc, 1, 4, 1, 64, sl, q, 0.1, out, ws)
     assert e.value.status == tq.TQ_EINVAL
     torch.cuda.synchronize()
 
