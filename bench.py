@@ -523,9 +523,40 @@ def run_attention(args, dist, rank, steps, mode="scalar"):
                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                         "frac": achieved / pk["hbm_gbs"], "launch_ms": k_ms}}
     if mode == "scalar":
+        res["key_variants"] = attention_key_variants(tq, wl, dist, vcb, vc, B, Hq, Hkv, T, q, seq, out, max(steps, 5))
         res["paged_decode_loop"] = {
             f"page_{ps}": run_paged_loop(dist, tq, kcb, vcb, kc, vc, B, Hq, Hkv, T, q, knew, vnew, ps, steps)
             for ps in (16, 64, 256)}
+    return res
+
+
+def attention_key_variants(tq, wl, dist, vcb, vc, B, Hq, Hkv, T, q, seq, out, n):
+    """The attention call of the same workload with other key caches (same
+    synthetic keys, same 3-bit values): 3.5-bit keys (3 bits with the QJL
+    term + one more stage-1 bit on 32 of 128 rotated coordinates) and
+    MSE-only keys at 3 and 4 bits."""
+    d = 128
+    rows = B * Hkv * T
+    res = {}
+    for name, bits, kind, extra in (("prod_b3.5", 3, tq.KIND_PROD, 32), ("mse_b3", 3, tq.KIND_MSE, 0),
+                                    ("mse_b4", 4, tq.KIND_MSE, 0)):
+        kcb = tq.Codebook(d, bits, kind, tq.MODE_SCALAR, extra=extra)
+        kc = torch.empty(tq.cache_bytes(kcb, rows), dtype=torch.uint8, device="cuda")
+        chunk = 1 << 20
+        for u in range(B * Hkv):
+            h = u % Hkv
+            for a in range(0, T, chunk):
+                m = min(chunk, T - a)
+                dst = torch.arange(u * T + a, u * T + a + m, dtype=torch.int64, device="cuda")
+                tq.tq_quantize(kcb, kc, rows, wl.llama_kv_torch(m, d, h, which="keys",
+                                                                 generator_offset=u * 64 + a // chunk), m, d,
+                               dst_rows=dst)
+        ws = torch.empty(tq.tq_decode_attention_workspace(kcb, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+        scale = 1.0 / math.sqrt(d)
+        ms = per_call_ms(lambda i: tq.tq_decode_attention(kcb, vcb, kc, vc, B, Hq, Hkv, T, seq, q, scale, out, ws), n)
+        packed = rows * (tq.record_bytes(kcb) + (4 if kind == tq.KIND_PROD else 2) + tq.record_bytes(vcb) + 2)
+        res[name] = {"ms_per_call": ms, "packed_bytes": packed, "gbs": packed / (ms / 1e3) / 1e9}
+        del kc
     return res
 
 
