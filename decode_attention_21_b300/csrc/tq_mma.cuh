@@ -73,6 +73,38 @@ __device__ __forceinline__ void expand16_v(uint32_t w, uint32_t (&r)[16]) {
     r[beta] = beta < 6 ? (w6 & (0x00010001u << (beta + 6))) : bit_operand(w, w4, beta);
 }
 
+// Two-level sum of the PV products of a warp.  An mma.sync chain adds each
+// tile's products into its fp32 accumulator inside the tensor core, which
+// drops low-order bits of small addends against a large running sum; over a
+// long context (thousands of tiles per warp) that drifts by ~1e-4 relative.
+// So the chain runs over a few tiles only, and flush() moves its sum into
+// fp32 registers with ordinary adds.  t[mt][0/1] = the two coordinates of the
+// thread's C fragment, hi and lo weight pieces already combined.
+struct PvTotal {
+  float t[8][2];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) t[mt][0] = t[mt][1] = 0.f;
+  }
+  __device__ __forceinline__ void scale(float a) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      t[mt][0] *= a;
+      t[mt][1] *= a;
+    }
+  }
+  __device__ __forceinline__ void flush(float (&acc)[8][4]) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      t[mt][0] += acc[mt][0] + acc[mt][1];
+      t[mt][1] += acc[mt][2] + acc[mt][3];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+    }
+  }
+};
+constexpr int kPvFlushStages = 4;   // stages (2 tiles per warp each) per mma chain
+
 // Power of two s with amax / s <= target (1 for amax = 0).
 __device__ __forceinline__ float pow2_scale(float amax, float target) {
   if (!(amax > 0.f)) return 1.f;

@@ -715,6 +715,8 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  PvTotal tot;
+  tot.zero();
 
   if (tile0 + warp < tend) {
     QK16<NVK, PK> qk;
@@ -738,6 +740,7 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
     int64_t tile = tile0 + warp;
     kcur.load(krec, knrm, KW, rowbase, tile * 16 + g, L, c);
     vcur.load(vrec, vnrm, VW, rowbase, tile * 16, L, g, c);
+    int chain = 0;    // tiles in the current mma chain
     for (; tile < tend; tile += 4) {
       const int64_t tn = tile + 4;
       if (tn < tend) {
@@ -768,6 +771,7 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        tot.scale(alpha);
         m_run = m_new;
       }
       const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
@@ -809,8 +813,13 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
       }
       kcur = knxt;
       vcur = vnxt;
+      if (++chain == 2 * kPvFlushStages) {
+        tot.flush(acc);
+        chain = 0;
+      }
     }
   }
+  tot.flush(acc);
   // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
   // acc = C0 * wsum + value_factor(beta) * D
   float c0 = 0.f;
@@ -827,8 +836,8 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
   for (int mt = 0; mt < 8; ++mt) {
     const int b0 = 2 * mt, b1 = 2 * mt + 1;
     const float f0 = value_factor(b0), f1 = value_factor(b1);
-    ph[2 + 16 * g + b0] = fmaf(f0, acc[mt][0] + acc[mt][1], c0 * wsum);
-    ph[2 + 16 * g + b1] = fmaf(f1, acc[mt][2] + acc[mt][3], c0 * wsum);
+    ph[2 + 16 * g + b0] = fmaf(f0, tot.t[mt][0], c0 * wsum);
+    ph[2 + 16 * g + b1] = fmaf(f1, tot.t[mt][1], c0 * wsum);
   }
 }
 
@@ -947,6 +956,8 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  PvTotal tot;
+  tot.zero();
   float vcn[NVV];
 #pragma unroll
   for (int u = 0; u < NVV; ++u) vcn[u] = -2.f * vcb.vcoef[u];
@@ -1013,6 +1024,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        tot.scale(alpha);
         m_run = m_new;
       }
       const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
@@ -1064,6 +1076,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
           mma_f16(acc[mt], r01[2 * mt], r01[2 * mt + 1], r89[2 * mt], r89[2 * mt + 1], b0, b1);
       }
     }
+    if (st % kPvFlushStages == kPvFlushStages - 1) tot.flush(acc);
     // every warp is done with this ring slot: refill it with stage st + kRing
     if (st + kRing < nst) {
       __syncthreads();
@@ -1075,6 +1088,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
     if (tid == 0) atomicOr(status, 2);
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
   }
+  tot.flush(acc);
   // this warp's partial: head slot c, coordinates 16g + 2mt (+1);
   // acc = C0 * wsum + value_factor(beta) * D
   float c0 = 0.f;
@@ -1091,8 +1105,8 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
   for (int mt = 0; mt < 8; ++mt) {
     const int b0 = 2 * mt, b1 = 2 * mt + 1;
     const float f0 = value_factor(b0), f1 = value_factor(b1);
-    ph[2 + 16 * g + b0] = fmaf(f0, acc[mt][0] + acc[mt][1], c0 * wsum);
-    ph[2 + 16 * g + b1] = fmaf(f1, acc[mt][2] + acc[mt][3], c0 * wsum);
+    ph[2 + 16 * g + b0] = fmaf(f0, tot.t[mt][0], c0 * wsum);
+    ph[2 + 16 * g + b1] = fmaf(f1, tot.t[mt][1], c0 * wsum);
   }
 }
 

@@ -335,6 +335,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  PvTotal tot;
+  tot.zero();
   if (tile0 + warp < tend) {
     const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
     const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
@@ -354,6 +356,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
     const int hh = g >> 1, pc = g & 1;
     const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
     const int vs = g >> 1, vh = g & 1;   // value subtree and half of this thread's 16 coordinates
+    int chain = 0;    // tiles in the current mma chain
     for (int64_t tile = tile0 + warp; tile < tend; tile += 4) {
       const int64_t t0 = tile * 16, ta = t0 + g, tb = ta + 8;
       PKey<BK> ka, kb_;
@@ -374,6 +377,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        tot.scale(alpha);
         m_run = m_new;
       }
       const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
@@ -424,8 +428,13 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
           mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
         }
       }
+      if (++chain == 2 * kPvFlushStages) {
+        tot.flush(acc);
+        chain = 0;
+      }
     }
   }
+  tot.flush(acc);
   const int nchunks = gridDim.x;
   float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
   float* ph = part + c * (2 + 128);
@@ -435,8 +444,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
   }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    ph[2 + 16 * g + 2 * mt] = acc[mt][0] + acc[mt][1];
-    ph[2 + 16 * g + 2 * mt + 1] = acc[mt][2] + acc[mt][3];
+    ph[2 + 16 * g + 2 * mt] = tot.t[mt][0];
+    ph[2 + 16 * g + 2 * mt + 1] = tot.t[mt][1];
   }
 }
 
@@ -536,6 +545,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  PvTotal tot;
+  tot.zero();
   const float kq = kcb.qjl_const;
   const int hh = g >> 1, pc = g & 1;
   const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
@@ -576,6 +587,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+        tot.scale(alpha);
         m_run = m_new;
       }
       const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
@@ -627,6 +639,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
         }
       }
     }
+    if (st % kPvFlushStages == kPvFlushStages - 1) tot.flush(acc);
     if (st + kRing < nst) {
       __syncthreads();
       request(st + kRing, min(kStageTiles, nt - (st + kRing) * kStageTiles));
@@ -637,6 +650,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
     if (tid == 0) atomicOr(status, 2);
     for (int st = pending_from; st < issued; ++st) bar_wait(su32(&bars[st % kRing]), (uint32_t)((st / kRing) & 1));
   }
+  tot.flush(acc);
   const int nchunks = gridDim.x;
   float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
   float* ph = part + c * (2 + 128);
@@ -646,8 +660,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    ph[2 + 16 * g + 2 * mt] = acc[mt][0] + acc[mt][1];
-    ph[2 + 16 * g + 2 * mt + 1] = acc[mt][2] + acc[mt][3];
+    ph[2 + 16 * g + 2 * mt] = tot.t[mt][0];
+    ph[2 + 16 * g + 2 * mt + 1] = tot.t[mt][1];
   }
 }
 

@@ -1,0 +1,132 @@
+"""GPU parity at the benchmark's full sizes, in the launch configurations the
+benchmark times (same batch, heads and context, so the same grid and the same
+split of the context over CTAs).
+
+* logits, 4-bit keys, B=1, 32/8 heads, context 32768: every output against
+  the oracle on the oracle's own packed cache;
+* decode attention, 3-bit keys and values, B=8, 32/8 heads, context 131072:
+  each (sequence, kv head) holds 4096 distinct oracle-coded rows repeated 32
+  times in order.  Attention is unchanged when the whole key/value set is
+  repeated (every softmax weight is scaled by the same count), so the
+  full-size output must equal the oracle's attention over one copy;
+* quantize, 2^20 bf16 rows in one call (the persistent tcgen05 kernel, one CTA
+  per SM, ~55 tiles each): a seeded sample of 8192 rows (first and last
+  included) against the oracle, with the bar of the smaller tensor-core tests.
+
+Bars as in test_gpu_parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_21_b300 import tq
+from decode_attention_21_b300 import workloads as wl
+from oracle import estimate, layout, quant
+
+pytestmark = pytest.mark.gpu
+
+
+def pair(bits, kind="prod", seed_pi=1, seed_s=2):
+    ocb = quant.Codebook(128, bits, kind=kind, seed_pi=seed_pi, seed_s=seed_s)
+    gcb = tq.Codebook(128, bits, tq.KIND_PROD if kind == "prod" else tq.KIND_MSE, tq.MODE_SCALAR, seed_pi, seed_s)
+    return ocb, gcb
+
+
+def rowwise_ok(got, ref, tol=1e-3, med=1e-4):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.max(np.abs(ref), axis=-1, keepdims=True)
+    assert np.all(np.abs(got - ref) <= tol * scale + 1e-30), float(np.max(np.abs(got - ref) / scale))
+    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3 * scale)
+    assert np.median(rel) <= med, float(np.median(rel))
+
+
+def test_logits_full_size():
+    B, Hq, Hkv, T = 1, 32, 8, 32768
+    ocb, gcb = pair(4)
+    rows = B * Hkv * T
+    x = np.concatenate([wl.llama_kv_slice(0, h, 0, T, which="keys") for h in range(B * Hkv)])
+    code = quant.quantize(ocb, x.astype(np.float64))
+    img = layout.write_cache(ocb, rows, code)
+    q = wl.queries((B, Hq, 128))
+    lens = [T]
+    ref = estimate.logits(ocb, code, q.astype(np.float64), lens, Hkv, T)
+    ws = torch.empty(tq.tq_logits_workspace(gcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, T), float("nan"), device="cuda")
+    tq.tq_logits(gcb, torch.from_numpy(img).cuda(), B, Hq, Hkv, T, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                 torch.from_numpy(q).cuda(), out, ws)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gcb)
+    rowwise_ok(out.cpu().numpy()[0], ref[0])
+
+
+def replicate(ocb, gcb, img_u, rows_u, rows, src):
+    """Cache of `rows` rows whose row r holds row src[r] of a `rows_u`-row
+    cache image (records and norm entries copied byte for byte)."""
+    rb = tq.record_bytes(gcb)
+    nb = 4 if ocb.kind == "prod" else 2
+    u = torch.from_numpy(img_u).cuda()
+    full = torch.zeros(tq.cache_bytes(gcb, rows), dtype=torch.uint8, device="cuda")
+    off_u = (rows_u * rb + 255) // 256 * 256
+    off = (rows * rb + 255) // 256 * 256
+    full[: rows * rb].view(rows, rb)[:] = u[: rows_u * rb].view(rows_u, rb)[src]
+    full[off: off + rows * nb].view(rows, nb)[:] = u[off_u: off_u + rows_u * nb].view(rows_u, nb)[src]
+    return full
+
+
+def test_attention_full_size_repeated_rows():
+    B, Hq, Hkv, T, U = 8, 32, 8, 131072, 4096
+    okc, gkc = pair(3)
+    ovc, gvc = pair(3, "mse", seed_pi=1)
+    units = B * Hkv
+    K = np.concatenate([wl.llama_kv_slice(0, u, 0, U, which="keys") for u in range(units)])
+    V = np.concatenate([wl.llama_kv_slice(0, u, 0, U, which="values") for u in range(units)])
+    kcode = quant.quantize(okc, K.astype(np.float64))
+    vcode = quant.quantize(ovc, V.astype(np.float64))
+    q = wl.queries((B, Hq, 128))
+    scale = 1.0 / math.sqrt(128)
+    ref = estimate.attention(okc, ovc, kcode, vcode, q.astype(np.float64), [U] * B, Hkv, U, scale)
+    rows_u, rows = units * U, units * T
+    r = torch.arange(rows, device="cuda", dtype=torch.int64)
+    src = (r // T) * U + (r % T) % U
+    kc = replicate(okc, gkc, layout.write_cache(okc, rows_u, kcode), rows_u, rows, src)
+    vc = replicate(ovc, gvc, layout.write_cache(ovc, rows_u, vcode), rows_u, rows, src)
+    del r, src
+    ws = torch.empty(tq.tq_decode_attention_workspace(gkc, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    tq.tq_decode_attention(gkc, gvc, kc, vc, B, Hq, Hkv, T, torch.full((B,), T, dtype=torch.int32, device="cuda"),
+                           torch.from_numpy(q).cuda(), scale, out, ws)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gkc)
+    got = out.cpu().numpy()
+    for b in range(B):
+        rowwise_ok(got[b], ref[b])
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantize_full_size_sampled(bits):
+    N = 1 << 20
+    ocb, gcb = pair(bits)
+    x = np.concatenate([wl.llama_kv_slice(0, h, 0, N // 8, which="keys") for h in range(8)])
+    cache = torch.zeros(tq.cache_bytes(gcb, N), dtype=torch.uint8, device="cuda")
+    tq.tq_quantize(gcb, cache, N, torch.from_numpy(x).cuda().to(torch.bfloat16), N, 128)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gcb)
+    rng = np.random.default_rng(bits)
+    sample = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 8190, replace=False)]))
+    code = quant.quantize(ocb, x[sample].astype(np.float64))
+    got = layout.read_cache(ocb, N, cache.cpu().numpy(), row_ids=sample)
+    code_bits = got["idx"] != code["idx"]
+    flips = code_bits.sum() + (got["sigma"] != code["sigma"]).sum()
+    nbits = code["idx"].size * ocb.b1 + code["sigma"].size
+    assert flips <= 1e-3 * nbits, flips / nbits
+    if code_bits.any():
+        y, _ = quant.rotate(ocb, x[sample].astype(np.float64))
+        t = ocb.t.astype(np.float64)
+        dist = np.min(np.abs(y[code_bits][:, None] - t[None, :]), axis=1)
+        assert np.all(dist < 1e-4 / math.sqrt(128))
+    n_ref = np.linalg.norm(x[sample].astype(np.float64), axis=1)
+    assert np.allclose(got["n16"].astype(np.float64), n_ref, rtol=1e-3)
+    assert np.allclose(got["g16"].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
