@@ -11,7 +11,9 @@ split of the context over CTAs).
   full-size output must equal the oracle's attention over one copy;
 * quantize, 2^20 bf16 rows in one call (the persistent tcgen05 kernel, one CTA
   per SM, ~55 tiles each): a seeded sample of 8192 rows (first and last
-  included) against the oracle, with the bar of the smaller tensor-core tests.
+  included) against the oracle, with the bar of the smaller tensor-core tests;
+* search, 10^6 database rows, 10^4 queries, top-10: 16 sampled queries
+  against the oracle's top-k over all rows.
 
 Bars as in test_gpu_parity.py.
 """
@@ -130,3 +132,59 @@ def test_quantize_full_size_sampled(bits):
     n_ref = np.linalg.norm(x[sample].astype(np.float64), axis=1)
     assert np.allclose(got["n16"].astype(np.float64), n_ref, rtol=1e-3)
     assert np.allclose(got["g16"].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
+
+
+def test_search_full_size_sampled_queries():
+    """Top-10 over 10^6 rows (d 200 -> 256, b = 2) for all 10^4 queries, as
+    the benchmark runs it, on the oracle's own packed database; 16 sampled
+    queries (first and last included) against the oracle's blocked top-k:
+    identical ids except swaps among near-tied scores, scores equal to the
+    estimator of the returned rows."""
+    n_db, nq, k, blk = 1000000, 10000, 10, 1 << 17
+    ocb = quant.Codebook(256, 2, kind="prod")
+    gcb = tq.Codebook(256, 2, tq.KIND_PROD, tq.MODE_SCALAR)
+    x = wl.search_rows(n_db, "db")
+    q = wl.search_rows(nq, "search_q")
+    keep = ("idx", "sigma", "n16", "g16")
+    parts = []
+    for a in range(0, n_db, blk):
+        c = quant.quantize(ocb, x[a: a + blk].astype(np.float64))
+        parts.append({key: c[key] for key in keep})
+    del x
+    code = {key: np.concatenate([p[key] for p in parts]) for key in keep}
+    del parts
+    img = torch.from_numpy(layout.write_cache(ocb, n_db, code)).cuda()
+    ws = torch.empty(tq.tq_search_workspace(gcb, n_db, nq, k), dtype=torch.uint8, device="cuda")
+    ids = torch.full((nq, k), -7, dtype=torch.int32, device="cuda")
+    sc = torch.full((nq, k), float("nan"), device="cuda")
+    tq.tq_search(gcb, img, n_db, torch.from_numpy(q).cuda(), nq, q.shape[1], k, ids, sc, ws)
+    torch.cuda.synchronize()
+    gi, gs = ids.cpu().numpy(), sc.cpu().numpy()
+    rng = np.random.default_rng(5)
+    sample = np.unique(np.concatenate([[0, nq - 1], rng.choice(nq, 14, replace=False)]))
+    qs = q[sample].astype(np.float64)
+    # oracle: blocked top-k of the estimator over all rows (ties to the smaller id)
+    best_s = np.full((len(sample), 0), -np.inf)
+    best_i = np.zeros((len(sample), 0), dtype=np.int64)
+    full_g = np.zeros((len(sample), k))
+    for a in range(0, n_db, blk):
+        rows = np.arange(a, min(a + blk, n_db))
+        cb_rows = quant.decode_codes(ocb, {key: code[key][rows] for key in keep})
+        s = estimate.estimate(ocb, qs, cb_rows)
+        for r in range(len(sample)):
+            inb = (gi[sample[r]] >= a) & (gi[sample[r]] < a + blk)
+            full_g[r, inb] = s[r, gi[sample[r]][inb] - a]
+        cand_s = np.concatenate([best_s, s], axis=1)
+        cand_i = np.concatenate([best_i, np.broadcast_to(rows, s.shape)], axis=1)
+        order = np.lexsort((cand_i, -cand_s), axis=1)[:, :k]
+        best_s = np.take_along_axis(cand_s, order, axis=1)
+        best_i = np.take_along_axis(cand_i, order, axis=1)
+    tol = 1e-5 * np.max(np.abs(best_s))
+    for r, qi in enumerate(sample):
+        g_ids = gi[qi]
+        assert len(set(g_ids.tolist())) == k and np.all(g_ids >= 0) and np.all(g_ids < n_db)
+        assert np.all(np.abs(gs[qi] - full_g[r]) <= tol)
+        assert np.all(np.abs(np.sort(full_g[r])[::-1] - best_s[r]) <= tol)
+        for j in np.nonzero(g_ids != best_i[r])[0]:
+            assert abs(full_g[r, j] - best_s[r, j]) <= tol
+        assert np.all(np.diff(gs[qi]) <= tol)

@@ -10,8 +10,10 @@ pages named by a block table.  The arithmetic is unchanged, so:
 * table entries past a sequence's last page are -1 here: reading one would
   raise the out-of-cache flag, which every test checks is clear;
 * a decode loop captured once in a CUDA graph (advance the lengths, append
-  the step's key and value, attend) and replayed step after step matches the
-  contiguous path and, on the codes it wrote, the oracle.
+  the step's key and value, attend) and replayed step after step writes the
+  same packed rows as the contiguous path, attends bit-identically to it, and
+  matches the oracle's attention over the oracle's own codes of the same
+  keys and values.
 """
 import math
 
@@ -234,15 +236,18 @@ def test_decode_loop_in_a_cuda_graph(mode):
     li = torch.from_numpy(live_log).cuda()
     tq.tq_quantize(gkc, kcc, rows_c, Kd[li].contiguous(), len(live_log), 128, dst_rows=li)
     tq.tq_quantize(gvc, vcc, rows_c, Vd[li].contiguous(), len(live_log), 128, dst_rows=li)
-    # codes the loop wrote, read back by the oracle's decoder, in logical order;
-    # the contiguous cache holds the same packed rows
-    kcode = quant.decode_codes(okc, layout.read_cache(okc, rows_total, kc.cpu().numpy(), row_ids=live_phys))
-    vcode = quant.decode_codes(ovc, layout.read_cache(ovc, rows_total, vc.cpu().numpy(), row_ids=live_phys))
-    kcode_c = layout.read_cache(okc, rows_c, kcc.cpu().numpy(), row_ids=live_log)
-    for key in ("idx", "sigma", "n16", "g16"):
-        assert np.array_equal(kcode_c[key], kcode[key]), key
-    kcode_l = scatter_logical(kcode, live_log, rows_c)
-    vcode_l = scatter_logical(vcode, live_log, rows_c)
+    # the pages hold exactly the packed rows of the contiguous cache
+    for gcb, paged, contig, nb in ((gkc, kc, kcc, 4), (gvc, vc, vcc, 2)):
+        assert torch.equal(packed_rows(gcb, paged, rows_total, live_phys, nb),
+                           packed_rows(gcb, contig, rows_c, live_log, nb))
+    # the oracle codes the same keys and values itself; the loop's codes
+    # differ from them at most in rare boundary cases (fp32 vs fp64 rotation)
+    kcode = quant.quantize(okc, K.astype(np.float64))
+    vcode = quant.quantize(ovc, V.astype(np.float64))
+    for ocb, paged in ((okc, kc), (ovc, vc)):
+        got = layout.read_cache(ocb, rows_total, paged.cpu().numpy(), row_ids=live_phys)
+        ref_idx = (kcode if ocb is okc else vcode)["idx"][live_log]
+        assert (got["idx"] != ref_idx).sum() <= 1e-3 * ref_idx.size
     wsc = torch.empty_like(ws)
     outc = torch.zeros_like(out)
     for i in range(steps):
@@ -252,25 +257,20 @@ def test_decode_loop_in_a_cuda_graph(mode):
                                wsc)
         torch.cuda.synchronize()
         assert torch.equal(outs[i], outc), i
-        ref = estimate.attention(okc, ovc, kcode_l, vcode_l, Q[i].astype(np.float64), lens_i, Hkv, cap, scale)
+        ref = estimate.attention(okc, ovc, kcode, vcode, Q[i].astype(np.float64), lens_i, Hkv, cap, scale)
         got = outs[i].cpu().numpy()
         for b in range(B):
             rowwise_ok(got[b], ref[b])
 
 
-def scatter_logical(code, log, rows):
-    """Code arrays of the live rows placed at logical rows ``log`` of a
-    contiguous [rows] layout (other rows: copies of row 0, never attended)."""
-    n = len(log)
-    out = {}
-    for k, v in code.items():
-        if isinstance(v, np.ndarray) and v.shape[:1] == (n,):
-            full = np.repeat(v[:1], rows, axis=0)
-            full[log] = v
-            out[k] = full
-        else:
-            out[k] = v
-    return out
+def packed_rows(gcb, buf, rows_total, ids, nb):
+    """Records and norm entries of rows ``ids`` of a cache buffer, as bytes."""
+    rb = tq.record_bytes(gcb)
+    off = (rows_total * rb + 255) // 256 * 256
+    ids = torch.from_numpy(np.asarray(ids, dtype=np.int64)).cuda()
+    rec = buf[: rows_total * rb].view(rows_total, rb)[ids]
+    nrm = buf[off: off + rows_total * nb].view(rows_total, nb)[ids]
+    return torch.cat([rec, nrm], dim=1)
 
 
 def test_paged_table_entry_outside_the_cache_is_flagged():
