@@ -731,10 +731,8 @@ tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* v
 }
 
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k) {
-  (void)n_db;
-  (void)k;
-  if (!cb || nq <= 0) return 0;
-  return (size_t)tq::search_workspace_bytes(cb->dev, nq);
+  if (!cb || nq <= 0 || n_db <= 0 || k < 1) return 0;
+  return (size_t)tq::search_workspace_bytes(cb->dev, n_db, nq, k, cb->sms);
 }
 
 tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, const float* q, int32_t nq,
@@ -755,7 +753,7 @@ tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, c
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "tq_search: codebook lives on another device");
   return launched("tq_search", tq::launch_search(cb->dev, static_cast<const uint8_t*>(db_cache), n_db, q, nq, d_in, k,
-                                                ids, scores, static_cast<uint8_t*>(workspace),
+                                                ids, scores, static_cast<uint8_t*>(workspace), cb->sms,
                                                 static_cast<cudaStream_t>(stream)));
 }
 

@@ -173,9 +173,9 @@ cudaError_t launch_attn_polar(const Dev& kcb, const Dev& vcb, const uint8_t* kca
                               int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens,
                               const uint8_t* prep, float scale_log2, float* partials, int nchunks, int tiles_per_cta,
                               cudaStream_t s);
-int64_t search_workspace_bytes(const Dev& cb, int nq);
+int64_t search_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, int sms);
 cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
-                          int32_t* ids, float* scores, uint8_t* prep, cudaStream_t s);
+                          int32_t* ids, float* scores, uint8_t* prep, int sms, cudaStream_t s);
 cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts, float* out,
                               cudaStream_t s);
 

@@ -16,7 +16,12 @@
 //     accumulators through shared memory, and the first half updates a
 //     per-query top-k list in shared memory (a candidate enters only if it
 //     beats the current k-th score).
+//   * the database is split into chunks (a second grid dimension) so that
+//     the scan fills whole waves of resident CTAs; a merge kernel combines
+//     the per-chunk lists.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "tq_internal.cuh"
 
@@ -28,6 +33,9 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kD = 256;
 constexpr int kMaxK = 32;
 constexpr int kRound = 4;   // 16-row tiles per exchange between the two coordinate halves
+constexpr int kMaxChunks = 16;
+// Resident scan CTAs per SM (registers): 2 for databases of up to 3 planes.
+__host__ __device__ constexpr int search_ctas_per_sm(int P) { return P <= 3 ? 2 : 1; }
 __device__ constexpr uint32_t kOddMask[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -159,10 +167,16 @@ __global__ void __launch_bounds__(1024) k_search_prep(const Dev cb, const float*
 
 // Scan: 8 warps = 4 query groups x 2 coordinate halves.  Warp (grp_local,
 // half) holds the fragments of k-blocks 8 half .. 8 half + 7 (word c + 4 half).
+//
+// Grid (query CTAs, database chunks): CTA (x, y) scans tiles
+// y * tiles_per_chunk .. of the database and writes its queries' top-k to
+// ids / scores + (y * nq + query) * k (with one chunk: the final lists; with
+// several: per-chunk lists that k_search_merge combines).
 template <int NV, int P>
-__global__ void __launch_bounds__(256, P <= 3 ? 2 : 1) k_search(const Dev cb, const uint8_t* __restrict__ db, int64_t n_db,
-                                                   const uint8_t* __restrict__ prep, int nq, int k,
-                                                   int32_t* __restrict__ ids, float* __restrict__ scores) {
+__global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev cb, const uint8_t* __restrict__ db,
+                                                   int64_t n_db, const uint8_t* __restrict__ prep, int nq, int k,
+                                                   int tiles_per_chunk, int32_t* __restrict__ ids,
+                                                   float* __restrict__ scores) {
   __shared__ float xch[2][4][kRound][4][32];  // [buffer][group][tile of the round][acc element][lane]
   __shared__ float top_s[2][16][kMaxK];       // [coordinate half][query slot][rank]
   __shared__ int32_t top_i[2][16][kMaxK];
@@ -196,7 +210,8 @@ __global__ void __launch_bounds__(256, P <= 3 ? 2 : 1) k_search(const Dev cb, co
   const float kq = cb.qjl_const;
   const int word = c + 4 * half;
   const int qslot = gl * 4 + c;               // this thread's query (shared-memory list index)
-  const int64_t ntiles = (n_db + 15) / 16;
+  const int64_t c0 = (int64_t)blockIdx.y * tiles_per_chunk;
+  const int64_t ntiles = min((n_db + 15) / 16, c0 + tiles_per_chunk);   // end of this chunk
   // words and norms of one tile, loaded one tile ahead of use
   uint32_t nwa[P], nwb[P], nna = 0u, nnb = 0u;
   auto fetch = [&](int64_t tile) {
@@ -209,10 +224,10 @@ __global__ void __launch_bounds__(256, P <= 3 ? 2 : 1) k_search(const Dev cb, co
     nna = (live && ta < n_db) ? __ldg(nrm + ta) : 0u;
     nnb = (live && tb < n_db) ? __ldg(nrm + tb) : 0u;
   };
-  fetch(0);
+  if (c0 < ntiles) fetch(c0);
   // rounds of kRound tiles: each half scores its coordinates of the round's
   // tiles, the two halves of a group meet once per round
-  for (int64_t t0 = 0; t0 < ntiles; t0 += kRound) {
+  for (int64_t t0 = c0; t0 < ntiles; t0 += kRound) {
     float part[kRound][4];
     uint32_t nra[kRound], nrb[kRound];
 #pragma unroll
@@ -260,7 +275,7 @@ __global__ void __launch_bounds__(256, P <= 3 ? 2 : 1) k_search(const Dev cb, co
     // combine the two coordinate halves of the group: half h finishes tiles
     // u with u / (kRound / 2) == h of the round, using the other half's
     // partials from the exchange buffer (double-buffered: one barrier per round)
-    const int buf = (int)((t0 / kRound) & 1);
+    const int buf = (int)(((t0 - c0) / kRound) & 1);
 #pragma unroll
     for (int u = 0; u < kRound; ++u)
       if (u / (kRound / 2) != half)
@@ -345,27 +360,134 @@ __global__ void __launch_bounds__(256, P <= 3 ? 2 : 1) k_search(const Dev cb, co
           if (take_a) ++ia;
           else ++ib;
         }
-        ids[(size_t)qi * k + j] = id;
-        scores[(size_t)qi * k + j] = sc;
+        ids[((size_t)blockIdx.y * nq + qi) * k + j] = id;
+        scores[((size_t)blockIdx.y * nq + qi) * k + j] = sc;
       }
     }
   }
 }
 
-int64_t search_workspace_bytes(const Dev& cb, int nq) { return align256((int64_t)((nq + 3) / 4) * search_block_bytes(cb.nv)); }
+
+// Merge of the per-chunk top-k lists: one warp per query takes the k best of
+// its chunks * k candidates (decreasing score, ties to the smaller id; a
+// missing entry is id -1 with score -inf and ranks last).
+__global__ void __launch_bounds__(128) k_search_merge(const int32_t* __restrict__ pid, const float* __restrict__ psc,
+                                                      int chunks, int nq, int k, int32_t* __restrict__ ids,
+                                                      float* __restrict__ scores) {
+  constexpr int kPer = kMaxChunks * kMaxK / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qi = blockIdx.x * 4 + warp;
+  if (qi >= nq) return;
+  const int n = chunks * k;
+  float s[kPer];
+  int32_t id[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = lane + 32 * j;
+    const int ch = e / k, r = e - ch * k;
+    const bool v = e < n;
+    id[j] = v ? pid[((size_t)ch * nq + qi) * k + r] : -1;
+    s[j] = (v && id[j] >= 0) ? psc[((size_t)ch * nq + qi) * k + r] : -INFINITY;
+    if (s[j] == -INFINITY) id[j] = -1;
+  }
+  // (score, id) order: higher score first, then the smaller valid id
+  auto better = [](float sa, int32_t ia, float sb, int32_t ib) {
+    if (ia < 0) return false;
+    if (ib < 0) return true;
+    return sa > sb || (sa == sb && ia < ib);
+  };
+  for (int out = 0; out < k; ++out) {
+    float bs = -INFINITY;
+    int32_t bi = -1;
+    int bj = -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (better(s[j], id[j], bs, bi)) {
+        bs = s[j];
+        bi = id[j];
+        bj = j;
+      }
+    float ws = bs;
+    int32_t wi = bi;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float os = __shfl_xor_sync(kFull, ws, o);
+      const int32_t oi = __shfl_xor_sync(kFull, wi, o);
+      if (better(os, oi, ws, wi)) {
+        ws = os;
+        wi = oi;
+      }
+    }
+    // the lane holding the winner drops it (ids are distinct across chunks)
+    if (wi >= 0 && bi == wi) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (j == bj) {
+          s[j] = -INFINITY;
+          id[j] = -1;
+        }
+    }
+    if (lane == 0) {
+      ids[(size_t)qi * k + out] = wi;
+      scores[(size_t)qi * k + out] = wi >= 0 ? ws : -INFINITY;
+    }
+  }
+}
+
+// Database chunks of the scan: enough that the grid fills its last wave of
+// resident CTAs (>= 95% of the slots busy, else the best count up to 16),
+// with at least 256 tiles per chunk.
+int search_chunks(const Dev& cb, int64_t n_db, int nq, int sms) {
+  const int64_t base = ((nq + 3) / 4 + 3) / 4;
+  const int64_t per_wave = (int64_t)sms * search_ctas_per_sm(cb.P);
+  const int64_t ntiles = (n_db + 15) / 16;
+  const int max_s = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxChunks, ntiles / 256));
+  int best = 1;
+  double best_eff = 0.0;
+  for (int sch = 1; sch <= max_s; ++sch) {
+    const int64_t units = base * sch;
+    const double eff = (double)units / (double)(((units + per_wave - 1) / per_wave) * per_wave);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = sch;
+    }
+    if (eff >= 0.95) break;
+  }
+  return best;
+}
+
+int64_t search_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, int sms) {
+  const int64_t prep = align256((int64_t)((nq + 3) / 4) * search_block_bytes(cb.nv));
+  const int chunks = search_chunks(cb, n_db, nq, sms);
+  return chunks > 1 ? prep + align256((int64_t)chunks * nq * k * 8) : prep;
+}
 
 cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
-                          int32_t* ids, float* scores, uint8_t* prep, cudaStream_t s) {
+                          int32_t* ids, float* scores, uint8_t* prep, int sms, cudaStream_t s) {
   const int ngroups = (nq + 3) / 4;
   k_search_prep<<<dim3(ngroups, 4), 1024, 0, s>>>(cb, q, nq, d_in, prep);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int grid = (ngroups + 3) / 4;
-  switch (cb.b1) {
-    case 1: k_search<1, 2><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, ids, scores); break;
-    case 2: k_search<2, 3><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, ids, scores); break;
-    default: k_search<4, 4><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, ids, scores); break;
+  const int chunks = search_chunks(cb, n_db, nq, sms);
+  const int64_t ntiles = (n_db + 15) / 16;
+  int64_t tpc = (ntiles + chunks - 1) / chunks;
+  tpc = (tpc + kRound - 1) / kRound * kRound;
+  int32_t* oid = ids;
+  float* osc = scores;
+  if (chunks > 1) {
+    uint8_t* part = prep + align256((int64_t)ngroups * search_block_bytes(cb.nv));
+    oid = reinterpret_cast<int32_t*>(part);
+    osc = reinterpret_cast<float*>(part + (size_t)chunks * nq * k * 4);
   }
+  const dim3 grid((ngroups + 3) / 4, chunks);
+  switch (cb.b1) {
+    case 1: k_search<1, 2><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc); break;
+    case 2: k_search<2, 3><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc); break;
+    default: k_search<4, 4><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc); break;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || chunks == 1) return e;
+  k_search_merge<<<(nq + 3) / 4, 128, 0, s>>>(oid, osc, chunks, nq, k, ids, scores);
   return cudaGetLastError();
 }
 

@@ -258,7 +258,8 @@ tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* v
  * can be captured once in a CUDA graph and replayed step after step.        */
 tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* stream);
 
-/* Workspace bytes of tq_search. */
+/* Workspace bytes of tq_search: query fragments, plus per-chunk top-k lists
+ * when the scan is split over database chunks (depends on n_db, nq, k). */
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k);
 
 /* Top-k inner-product search over a compressed database ([xujun] 常见问题,
