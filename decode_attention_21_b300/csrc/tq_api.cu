@@ -545,8 +545,6 @@ static tq_status logits_common(const char* what, const tq_codebook* kcb, const v
     return st;
   if (kcb->dev.kind == TQ_KIND_MSE && kcb->dev.mode != TQ_MODE_SCALAR)
     return fail(TQ_EUNSUPPORTED, "%s: MSE-only keys are scored in scalar mode only", what);
-  if (map.table && kcb->dev.mode != TQ_MODE_SCALAR)
-    return fail(TQ_EUNSUPPORTED, "%s: paged logits are implemented for scalar-mode keys only", what);
   if ((st = check_heads(what, B, Hq, Hkv, capacity)) != TQ_OK) return st;
   if (capacity == 0) return ok();
   if (!kcache || !seq_lens || !q || !logits || !workspace) return fail(TQ_EINVAL, "%s: NULL device pointer", what);
@@ -560,7 +558,8 @@ static tq_status logits_common(const char* what, const tq_codebook* kcb, const v
   if (kcb->dev.mode == TQ_MODE_POLAR) {
     if ((st = launched(what, tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
     return launched(what, tq::launch_logits_polar(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
-                                                  capacity, rows, seq_lens, prep, logits, nchunks, tpc, s));
+                                                  capacity, rows, map, seq_lens, prep, logits, nchunks, tpc,
+                                                  kcb->d_status, s));
   }
   if ((st = launched(what, tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
   if (capacity % 16 == 0)

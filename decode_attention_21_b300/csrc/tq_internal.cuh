@@ -167,8 +167,8 @@ cudaError_t launch_attn_polar_staged(const Dev& kcb, const Dev& vcb, const uint8
                                      int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_prep_polar(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s);
 cudaError_t launch_logits_polar(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
-                                int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
-                                int nchunks, int tiles_per_cta, cudaStream_t s);
+                                int64_t cache_rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
+                                float* logits, int nchunks, int tiles_per_cta, int* status, cudaStream_t s);
 cudaError_t launch_attn_polar(const Dev& kcb, const Dev& vcb, const uint8_t* kcache, const uint8_t* vcache, int B,
                               int Hq, int Hkv, int64_t capacity, int64_t cache_rows, const int32_t* seq_lens,
                               const uint8_t* prep, float scale_log2, float* partials, int nchunks, int tiles_per_cta,

@@ -267,10 +267,10 @@ __device__ __forceinline__ float est_polar(uint32_t nrm_bits, float s1, float s2
 
 template <int B>
 __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
-                                                      int Hkv, int64_t capacity, int64_t cache_rows,
+                                                      int Hkv, int64_t capacity, int64_t cache_rows, const RowMap map,
                                                       const int32_t* __restrict__ seq_lens,
                                                       const uint8_t* __restrict__ prep, float* __restrict__ logits,
-                                                      int tiles_per_cta) {
+                                                      int tiles_per_cta, int* __restrict__ status) {
   __shared__ PolarTab tab;
   load_tab(cb, tab);
   __syncthreads();
@@ -294,14 +294,14 @@ __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_
   const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
-  const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
   const float kq = cb.qjl_const;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
   for (int64_t tile = tile0 + warp; tile < tend; tile += 4) {
     const int64_t ta = tile * 16 + g, tb = ta + 8;
+    const int64_t row0 = tile_row(map, b, kvh, Hkv, capacity, tile * 16, status);   // cache row of the tile's token 0
     PKey<B> ka, kb_;
-    ka.load(recs, nrm, rowbase + ta, cb.W, c, ta < L);
-    kb_.load(recs, nrm, rowbase + tb, cb.W, c, tb < L);
+    ka.load(recs, nrm, row0 + g, cb.W, c, ta < L);
+    kb_.load(recs, nrm, row0 + g + 8, cb.W, c, tb < L);
     float s1a, s1b, s2a, s2b;
     polar_qk<B>(tab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
     if (c < G) {
@@ -710,13 +710,13 @@ cudaError_t launch_prep_polar(const Dev& cb, const float* q, int B, int Hq, int 
 }
 
 cudaError_t launch_logits_polar(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
-                                int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks,
-                                int tpc, cudaStream_t s) {
+                                int64_t rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
+                                float* logits, int nchunks, int tpc, int* status, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
   switch (cb.b1) {
-    case 1: k_logits_polar<1><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
-    case 2: k_logits_polar<2><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
-    default: k_logits_polar<3><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); break;
+    case 1: k_logits_polar<1><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, tpc, status); break;
+    case 2: k_logits_polar<2><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, tpc, status); break;
+    default: k_logits_polar<3><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, tpc, status); break;
   }
   return cudaGetLastError();
 }

@@ -53,6 +53,22 @@ __device__ __forceinline__ bool page_run(const RowMap& map, int b, int kvh, int 
   return true;
 }
 
+// First cache row of the 16-token tile starting at token t0 of (b, kvh):
+// contiguous, or through the block table (an entry outside the cache sets
+// kBadRow in *status and yields page 0's row).
+__device__ __forceinline__ int64_t tile_row(const RowMap& map, int b, int kvh, int Hkv, int64_t capacity, int64_t t0,
+                                            int* status) {
+  if (!map.table) return ((int64_t)b * Hkv + kvh) * capacity + t0;
+  uint32_t pi, off;
+  split_token(map, (uint32_t)t0, pi, off);
+  int32_t pg = __ldg(map.table + (int64_t)b * map.max_pages + pi);
+  if (pg < 0 || pg >= map.num_pages) {
+    atomicOr(status, kBadRow);
+    pg = 0;
+  }
+  return ((int64_t)pg * Hkv + kvh) * map.page + off;
+}
+
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
   for (long long i = 0; i < kWaitLimit; ++i) {
     uint32_t done;

@@ -233,10 +233,10 @@ tq_status tq_append_paged(const tq_codebook* cb, void* cache, int32_t num_pages,
                           const int32_t* seq_lens, const void* x, int32_t x_dtype, int32_t d_in,
                           void* stream);
 
-/* tq_logits over a paged key cache (scalar mode; PROD or MSE-only keys):
+/* tq_logits over a paged key cache (keys as for tq_logits: scalar or polar
+ * mode with the QJL term, or MSE-only keys in scalar mode):
  *   logits  device fp32 [B, Hq, max_pages * page_size]
- *   workspace >= tq_logits_workspace(kcb, B, Hq, Hkv) bytes
- * Polar-mode keys return TQ_EUNSUPPORTED.                                    */
+ *   workspace >= tq_logits_workspace(kcb, B, Hq, Hkv) bytes                  */
 tq_status tq_logits_paged(const tq_codebook* kcb, const void* kcache, int32_t num_pages, int32_t page_size,
                           const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq, int32_t Hkv,
                           const int32_t* seq_lens, const float* q, float* logits, void* workspace,

@@ -76,15 +76,16 @@ def check_clear(gcb):
     tq.tq_check_device(gcb)   # raises on a bounded-wait timeout or an out-of-cache access
 
 
-@pytest.mark.parametrize("bits,kind", [(3, "prod"), (4, "prod"), (2, "prod"), (3, "mse")])
+@pytest.mark.parametrize("bits,kind,mode", [(3, "prod", "scalar"), (4, "prod", "scalar"), (2, "prod", "scalar"),
+                                             (3, "mse", "scalar"), (3, "prod", "polar"), (4, "prod", "polar")])
 @pytest.mark.parametrize("ps", [16, 48, 128, 256])
-def test_logits_paged_equals_contiguous_and_oracle(bits, kind, ps):
+def test_logits_paged_equals_contiguous_and_oracle(bits, kind, mode, ps):
     B, Hq, Hkv = 3, 6, 3
     max_pages = -(-1100 // ps)
     cap = max_pages * ps
     lens = [cap, 517, 0]
     num_pages = B * max_pages + 5
-    ocb, gcb = pair(bits, kind)
+    ocb, gcb = pair(bits, kind, mode)
     rows = B * Hkv * cap
     x = wl.gaussian_outlier_keys(rows, 128)
     code = quant.quantize(ocb, x.astype(np.float64))
@@ -302,7 +303,7 @@ def test_paged_table_entry_outside_the_cache_is_flagged():
 
 def test_paged_invalid_arguments_return_status_without_launch():
     ocb, gcb = pair(3)
-    ocp, gcp = pair(3, mode="polar")
+    ocp, gcp = pair(3, "mse", mode="polar")     # MSE-only keys are scored in scalar mode only
     kc = torch.zeros(tq.cache_bytes(gcb, 64), dtype=torch.uint8, device="cuda")
     bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
     sl = torch.tensor([10], dtype=torch.int32, device="cuda")
