@@ -90,9 +90,10 @@ constexpr int kLogitsCtas = 148 * 4;   // resident CTAs of the logits kernel
 // Resident CTAs of the attention kernel (one wave): 4 per SM, 3 for keys
 // with four or more stage-1 virtual planes or extra-bit words (more
 // registers), 2 in polar mode.
-int attn_ctas(const tq_codebook* kcb) {
+int attn_ctas(const tq_codebook* kcb, const tq_codebook* vcb = nullptr) {
   if (kcb->dev.mode == TQ_MODE_POLAR) return 148 * 2;
-  return kcb->dev.nv >= 4 || kcb->dev.extra > 0 ? 148 * 3 : 148 * 4;
+  const bool heavy = kcb->dev.nv >= 4 || kcb->dev.extra > 0 || (vcb && vcb->dev.extra > 0);
+  return heavy ? 148 * 3 : 148 * 4;
 }
 
 template <class T>
@@ -648,14 +649,26 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
   if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD,
                                    "tq_decode_attention(keys)", true)) != TQ_OK)
     return st;
-  if ((st = check_scoring_codebook(vcb, TQ_KIND_MSE, "tq_decode_attention(values)")) != TQ_OK) return st;
-  if (kcb->dev.kind == TQ_KIND_MSE || kcb->dev.extra != 0) {
+  // values: MSE kind; mixed-bit (an extra bit on d/4 coordinates) in scalar mode
+  const bool mixed_values = vcb && vcb->dev.extra != 0;
+  if (mixed_values) {
+    if (vcb->dev.kind != TQ_KIND_MSE) return fail(TQ_EINVAL, "%s: the value codebook must be of kind MSE", what);
+  } else if ((st = check_scoring_codebook(vcb, TQ_KIND_MSE, "tq_decode_attention(values)")) != TQ_OK) {
+    return st;
+  }
+  if (kcb->dev.kind == TQ_KIND_MSE || kcb->dev.extra != 0 || mixed_values) {
     if (kcb->dev.mode != TQ_MODE_SCALAR || vcb->dev.mode != TQ_MODE_SCALAR)
-      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit keys are attended in scalar mode only", what);
+      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit caches are attended in scalar mode only", what);
     if (!tq::attn_staged_supports(kcb->dev, vcb->dev))
-      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit keys are paired with 3- or 4-bit values only", what);
+      return fail(TQ_EUNSUPPORTED,
+                  "%s: this key/value pair is not implemented (MSE-only or mixed-bit keys take 3- or 4-bit values; "
+                  "mixed-bit values take 2 or 3 bits, extra = d/4, with keys that have the QJL term)",
+                  what);
     if (capacity % 16 != 0 && !map.table)
-      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit keys need a capacity that is a multiple of 16", what);
+      return fail(TQ_EUNSUPPORTED, "%s: MSE-only and mixed-bit caches need a capacity that is a multiple of 16", what);
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != vcb->device) return fail(TQ_EINVAL, "%s: value codebook lives on another device", what);
   }
   if ((st = check_heads(what, B, Hq, Hkv, capacity)) != TQ_OK) return st;
   if (!kcache || !vcache || !seq_lens || !q || !out || !workspace)
@@ -672,7 +685,7 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
   if (kcb->dev.mode != vcb->dev.mode)
     return fail(TQ_EUNSUPPORTED, "%s: keys and values must use the same stage-1 mode", what);
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, attn_ctas(kcb), &nchunks, &tpc);
+  chunking(B, Hkv, capacity, attn_ctas(kcb, vcb), &nchunks, &tpc);
   const float sl2 = scale * 1.4426950408889634f;
   if (kcb->dev.mode == TQ_MODE_POLAR) {
     if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)

@@ -841,9 +841,9 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
   }
 }
 
-// Resident CTAs per SM of the staged attention kernel: 4, or 3 where the key
-// side needs more registers (4 virtual planes, or extra-bit words).  The host
-// sizes the grid to one wave of the same count.
+// Resident CTAs per SM of the staged attention kernel: 4, or 3 where it needs
+// more registers (4 key virtual planes, or extra-bit words in keys or values).
+// The host sizes the grid to one wave of the same count.
 constexpr int attn_min_blocks(int nvk, int extk) { return nvk >= 4 || extk > 0 ? 3 : 4; }
 
 // ---------------------------------------------------------------------------
@@ -855,8 +855,8 @@ constexpr int attn_min_blocks(int nvk, int extk) { return nvk >= 4 || extk > 0 ?
 // query fragments are loaded), and each warp scores tiles warp and warp + 4
 // of every stage.
 // ---------------------------------------------------------------------------
-template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK>
-__global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged(const Dev kcb, const Dev vcb,
+template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK, int EXTV>
+__global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn_staged(const Dev kcb, const Dev vcb,
                                                      const uint8_t* __restrict__ kcache,
                                                      const uint8_t* __restrict__ vcache, int Hq, int Hkv,
                                                      int64_t capacity, int64_t cache_rows, const RowMap map,
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
                                                      float* __restrict__ partials, int tiles_per_cta,
                                                      int* __restrict__ status) {
   constexpr int RBK = 16 * PK + 4 * EXTK;       // key record bytes at d = 128 (+ extra-bit words)
-  constexpr int RBV = 16 * PV;                  // value record bytes
+  constexpr int RBV = 16 * PV + 4 * EXTV;       // value record bytes (+ extra-bit words)
   constexpr int NBK = QJLK ? 4 : 2;             // key norm entry bytes
   constexpr int kSK = kStageTiles * 16 * RBK, kSKN = kStageTiles * 16 * NBK;
   constexpr int kSV = kStageTiles * 16 * RBV, kSVN = kStageTiles * 16 * 2;
@@ -958,14 +958,19 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
     for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
   PvTotal tot;
   tot.zero();
-  float vcn[NVV];
+  float vcn[NVV], vcnx[EXTV ? 2 * NVV : 1];
 #pragma unroll
   for (int u = 0; u < NVV; ++u) vcn[u] = -2.f * vcb.vcoef[u];
+#pragma unroll
+  for (int u = 0; u < (EXTV ? 2 * NVV : 1); ++u) vcnx[u] = EXTV ? -2.f * vcb.vcoef_x[u] : 0.f;
   const float kq = kcb.qjl_const;
   const uint32_t vsel = (g & 1) ? 0x7632u : 0x5410u;
   const int hh = g >> 1, pc = g & 1;    // B-fragment column: head slot, piece
   const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
   const int vword = g >> 1;
+  // mixed-bit values: the first EXTV word columns use the extended codebook,
+  // whose low bit is the column's extra word
+  const bool vxl = EXTV > 0 && vword < EXTV;
   bool ok = true;
   int pending_from = 0;
   for (int st = 0; st < nst; ++st) {
@@ -1046,13 +1051,14 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
       const float w8 = __shfl_sync(kFull, wB, src0);
       const float w9 = __shfl_sync(kFull, wB, src1);
       // value words (word column g/2) of tokens 2c, 2c+1, 2c+8, 2c+9
-      uint32_t vw[4][PV];
+      uint32_t vw[4][PV], ve[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tok = 2 * c + (j & 1) + 8 * (j >> 1);
-        const uint32_t* vp = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV) + vword * PV;
+        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV);
 #pragma unroll
-        for (int p = 0; p < PV; ++p) vw[j][p] = vp[p];
+        for (int p = 0; p < PV; ++p) vw[j][p] = vrow[vword * PV + p];
+        ve[j] = vxl ? vrow[4 * PV + vword] : 0u;
       }
 #pragma unroll
       for (int u = 0; u < NVV; ++u) {
@@ -1066,7 +1072,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
 #pragma unroll
           for (int p = 0; p < PV; ++p)
             if (kOddMask[u] >> p & 1u) r ^= vw[j][p];
-          x[j] = r;
+          x[j] = vxl ? 0u : r;                    // extended-codebook columns take the planes below
         }
         uint32_t r01[16], r89[16];
         expand16_v(__byte_perm(x[0], x[1], vsel), r01);
@@ -1074,6 +1080,31 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
           mma_f16(acc[mt], r01[2 * mt], r01[2 * mt + 1], r89[2 * mt], r89[2 * mt + 1], b0, b1);
+      }
+      if constexpr (EXTV > 0) {
+        // the extended codebook's 2 NVV virtual planes (plane PV = extra
+        // word), fed only by the extra-bit columns' lanes
+#pragma unroll
+        for (int u = 0; u < 2 * NVV; ++u) {
+          const float cu = vcnx[u];
+          const uint32_t b0 = pack_half2(piece16(cu * w0, pc), piece16(cu * w1, pc));
+          const uint32_t b1 = pack_half2(piece16(cu * w8, pc), piece16(cu * w9, pc));
+          uint32_t x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r = (kOddMask[u] >> PV & 1u) ? ve[j] : 0u;
+#pragma unroll
+            for (int p = 0; p < PV; ++p)
+              if (kOddMask[u] >> p & 1u) r ^= vw[j][p];
+            x[j] = vxl ? r : 0u;
+          }
+          uint32_t r01[16], r89[16];
+          expand16_v(__byte_perm(x[0], x[1], vsel), r01);
+          expand16_v(__byte_perm(x[2], x[3], vsel), r89);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+            mma_f16(acc[mt], r01[2 * mt], r01[2 * mt + 1], r89[2 * mt], r89[2 * mt + 1], b0, b1);
+        }
       }
     }
     if (st % kPvFlushStages == kPvFlushStages - 1) tot.flush(acc);
@@ -1094,6 +1125,11 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK)) k_attn_staged
   float c0 = 0.f;
 #pragma unroll
   for (int u = 0; u < NVV; ++u) c0 += vcb.vcoef[u];
+  if (EXTV > 0 && vxl) {
+    c0 = 0.f;
+#pragma unroll
+    for (int u = 0; u < (EXTV ? 2 * NVV : 0); ++u) c0 += vcb.vcoef_x[u];
+  }
   const int nchunks = gridDim.x;
   float* part = partials + ((((size_t)b * Hkv + kvh) * nchunks + blockIdx.x) * kAttnWarps + warp) * partial_floats(128);
   float* ph = part + c * (2 + 128);
@@ -1279,13 +1315,14 @@ cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq
 }
 #undef TQ_LOGITS_DISPATCH
 
-template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK>
+template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK, int EXTV>
 static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
                                  const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map,
                                  const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
                                  int* status) {
-  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 * EXTK + (QJLK ? 4 : 2) + 16 * PV + 2);
-  auto kern = k_attn_staged<NVK, PK, NVV, PV, QJLK, EXTK>;
+  constexpr size_t smem =
+      (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 * EXTK + (QJLK ? 4 : 2) + 16 * PV + 4 * EXTV + 2);
+  auto kern = k_attn_staged<NVK, PK, NVV, PV, QJLK, EXTK, EXTV>;
   static cudaError_t configured = [&] {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(kern));
@@ -1306,27 +1343,38 @@ static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const 
 }
 
 // Value codebooks: every b' for keys with the QJL term and no extra bits;
-// b = 3 and 4 for MSE-only and mixed-bit keys (other pairs are rejected by
-// the host before launch).
+// b = 3 and 4 for MSE-only and mixed-bit keys; mixed-bit values (extra bit on
+// d/4 coordinates) at b = 2 and 3 for keys with the QJL term and no or d/4
+// extra bits (other pairs are rejected by the host before launch).
 template <int NVK, int PK, bool QJLK, int EXTK>
 static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
                                  const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map,
                                  const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
                                  int* status) {
-#define TQ_ATTN_V(NVV, PV)                                                                                      \
-  return attn_staged_t<NVK, PK, NVV, PV, QJLK, EXTK>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, \
-                                                     sl2, parts, tpc, status)
+#define TQ_ATTN_V(NVV, PV, XV)                                                                                     \
+  return attn_staged_t<NVK, PK, NVV, PV, QJLK, EXTK, XV>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, \
+                                                         sl2, parts, tpc, status)
+  if (v.extra != 0) {
+    if constexpr (QJLK && EXTK <= 1) {
+      switch (b1v) {
+        case 2: TQ_ATTN_V(2, 2, 1);
+        case 3: TQ_ATTN_V(4, 3, 1);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    return cudaErrorInvalidValue;
+  }
   if constexpr (QJLK && EXTK == 0) {
     switch (b1v) {
-      case 1: TQ_ATTN_V(1, 1);
-      case 2: TQ_ATTN_V(2, 2);
-      case 3: TQ_ATTN_V(4, 3);
-      default: TQ_ATTN_V(8, 4);
+      case 1: TQ_ATTN_V(1, 1, 0);
+      case 2: TQ_ATTN_V(2, 2, 0);
+      case 3: TQ_ATTN_V(4, 3, 0);
+      default: TQ_ATTN_V(8, 4, 0);
     }
   } else {
     switch (b1v) {
-      case 3: TQ_ATTN_V(4, 3);
-      case 4: TQ_ATTN_V(8, 4);
+      case 3: TQ_ATTN_V(4, 3, 0);
+      case 4: TQ_ATTN_V(8, 4, 0);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -1334,7 +1382,9 @@ static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& 
 }
 
 bool attn_staged_supports(const Dev& kcb, const Dev& vcb) {
-  if (kcb.mode != 0 || vcb.mode != 0 || vcb.extra != 0) return false;
+  if (kcb.mode != 0 || vcb.mode != 0) return false;
+  if (vcb.extra != 0)
+    return vcb.d == 128 && vcb.extra == 32 && (vcb.b1 == 2 || vcb.b1 == 3) && kcb.kind == 0 && kcb.extra <= 32;
   const bool plain_keys = kcb.kind == 0 && kcb.extra == 0;
   return plain_keys || vcb.b1 == 3 || vcb.b1 == 4;
 }

@@ -306,18 +306,54 @@ def test_attention_parity_key_variants(kkind, kbits, kextra, vb, B, Hq, Hkv, cap
             rowwise_ok(got[b], ref[b])
 
 
+@pytest.mark.parametrize("kbits,kextra,vbits", [(3, 32, 3), (3, 0, 3), (2, 32, 2), (4, 0, 2), (4, 32, 3), (2, 0, 3)])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 304, [300, 1, 0])])
+def test_attention_parity_mixed_bit_values(kbits, kextra, vbits, B, Hq, Hkv, cap, lens):
+    """Decode attention over mixed-bit value caches (the first d/4 rotated
+    coordinates carry one more stage-1 bit: the 2.5 / 3.5-bit points), with
+    keys that carry the QJL term, mixed-bit or not."""
+    okc, gkc = pair(128, kbits, "prod", extra=kextra)
+    ovc, gvc = pair(128, vbits, "mse", extra=32, seed_pi=1)
+    rows = B * Hkv * cap
+    K = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="keys") for h in range(B * Hkv)])
+    V = np.concatenate([wl.llama_kv_slice(0, h, 0, cap, which="values") for h in range(B * Hkv)])
+    kcode, kimg = oracle_cache(okc, rows, K.astype(np.float64))
+    vcode, vimg = oracle_cache(ovc, rows, V.astype(np.float64))
+    q = wl.queries((B, Hq, 128))
+    scale = 1.0 / math.sqrt(128)
+    ref = estimate.attention(okc, ovc, kcode, vcode, q.astype(np.float64), lens, Hkv, cap, scale)
+    ws = torch.empty(tq.tq_decode_attention_workspace(gkc, B, Hq, Hkv, cap), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    tq.tq_decode_attention(gkc, gvc, torch.from_numpy(kimg).cuda(), torch.from_numpy(vimg).cuda(), B, Hq, Hkv, cap,
+                           torch.tensor(lens, dtype=torch.int32, device="cuda"), torch.from_numpy(q).cuda(), scale,
+                           out, ws)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gkc)
+    got = out.cpu().numpy()
+    for b in range(B):
+        if lens[b] == 0:
+            assert np.all(got[b] == 0)
+        else:
+            rowwise_ok(got[b], ref[b])
+
+
 def test_attention_key_variants_unsupported_pairs():
-    """MSE-only or mixed-bit keys with 1- or 2-bit values, in polar mode, or at
-    a capacity that is not a multiple of 16 are rejected before any launch."""
+    """MSE-only or mixed-bit keys with 1- or 2-bit values, mixed-bit values with
+    MSE-only keys or at 1 bit, and any of these at a capacity that is not a
+    multiple of 16 are rejected before any launch."""
     _, gk = pair(128, 3, "mse")
     _, gm = pair(128, 3, "prod", extra=32)
     _, gv2 = pair(128, 2, "mse", seed_pi=1)
     _, gv3 = pair(128, 3, "mse", seed_pi=1)
+    _, gvx = pair(128, 3, "mse", extra=32, seed_pi=1)
+    _, gvx1 = pair(128, 1, "mse", extra=32, seed_pi=1)
+    _, gk3 = pair(128, 3, "prod")
     B, Hq, Hkv = 1, 4, 1
     sl = torch.tensor([10], dtype=torch.int32, device="cuda")
     q = torch.zeros((B, Hq, 128), device="cuda")
     out = torch.zeros((B, Hq, 128), device="cuda")
-    for kcb, vcb, cap in ((gk, gv2, 64), (gm, gv2, 64), (gk, gv3, 40), (gm, gv3, 40)):
+    for kcb, vcb, cap in ((gk, gv2, 64), (gm, gv2, 64), (gk, gv3, 40), (gm, gv3, 40), (gk, gvx, 64),
+                          (gk3, gvx1, 64), (gk3, gvx, 40)):
         kc = torch.zeros(tq.cache_bytes(kcb, cap), dtype=torch.uint8, device="cuda")
         vc = torch.zeros(tq.cache_bytes(vcb, cap), dtype=torch.uint8, device="cuda")
         ws = torch.empty(tq.tq_decode_attention_workspace(kcb, B, Hq, Hkv, cap), dtype=torch.uint8, device="cuda")
