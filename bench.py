@@ -531,32 +531,43 @@ def run_attention(args, dist, rank, steps, mode="scalar"):
 
 
 def attention_key_variants(tq, wl, dist, vcb, vc, B, Hq, Hkv, T, q, seq, out, n):
-    """The attention call of the same workload with other key caches (same
-    synthetic keys, same 3-bit values): 3.5-bit keys (3 bits with the QJL
-    term + one more stage-1 bit on 32 of 128 rotated coordinates) and
-    MSE-only keys at 3 and 4 bits."""
+    """The attention call of the same workload with other caches (same
+    synthetic keys and values): 3.5-bit keys (3 bits with the QJL term + one
+    more stage-1 bit on 32 of 128 rotated coordinates) with the 3-bit values,
+    MSE-only keys at 3 and 4 bits with the 3-bit values, and 3.5-bit keys with
+    3.5-bit values (3-bit MSE + one more bit on 32 coordinates)."""
     d = 128
     rows = B * Hkv * T
-    res = {}
-    for name, bits, kind, extra in (("prod_b3.5", 3, tq.KIND_PROD, 32), ("mse_b3", 3, tq.KIND_MSE, 0),
-                                    ("mse_b4", 4, tq.KIND_MSE, 0)):
-        kcb = tq.Codebook(d, bits, kind, tq.MODE_SCALAR, extra=extra)
-        kc = torch.empty(tq.cache_bytes(kcb, rows), dtype=torch.uint8, device="cuda")
+
+    def fill(cb, which):
+        c = torch.empty(tq.cache_bytes(cb, rows), dtype=torch.uint8, device="cuda")
         chunk = 1 << 20
         for u in range(B * Hkv):
             h = u % Hkv
             for a in range(0, T, chunk):
                 m = min(chunk, T - a)
                 dst = torch.arange(u * T + a, u * T + a + m, dtype=torch.int64, device="cuda")
-                tq.tq_quantize(kcb, kc, rows, wl.llama_kv_torch(m, d, h, which="keys",
-                                                                 generator_offset=u * 64 + a // chunk), m, d,
+                tq.tq_quantize(cb, c, rows, wl.llama_kv_torch(m, d, h, which=which,
+                                                               generator_offset=u * 64 + a // chunk), m, d,
                                dst_rows=dst)
+        return c
+
+    res = {}
+    for name, bits, kind, extra, vextra in (("prod_b3.5", 3, tq.KIND_PROD, 32, 0), ("mse_b3", 3, tq.KIND_MSE, 0, 0),
+                                            ("mse_b4", 4, tq.KIND_MSE, 0, 0), ("kv_b3.5", 3, tq.KIND_PROD, 32, 32)):
+        kcb = tq.Codebook(d, bits, kind, tq.MODE_SCALAR, extra=extra)
+        kc = fill(kcb, "keys")
+        vcb_i, vc_i = vcb, vc
+        if vextra:
+            vcb_i = tq.Codebook(d, 3, tq.KIND_MSE, tq.MODE_SCALAR, extra=vextra)
+            vc_i = fill(vcb_i, "values")
         ws = torch.empty(tq.tq_decode_attention_workspace(kcb, B, Hq, Hkv, T), dtype=torch.uint8, device="cuda")
         scale = 1.0 / math.sqrt(d)
-        ms = per_call_ms(lambda i: tq.tq_decode_attention(kcb, vcb, kc, vc, B, Hq, Hkv, T, seq, q, scale, out, ws), n)
-        packed = rows * (tq.record_bytes(kcb) + (4 if kind == tq.KIND_PROD else 2) + tq.record_bytes(vcb) + 2)
+        ms = per_call_ms(lambda i: tq.tq_decode_attention(kcb, vcb_i, kc, vc_i, B, Hq, Hkv, T, seq, q, scale, out,
+                                                          ws), n)
+        packed = rows * (tq.record_bytes(kcb) + (4 if kind == tq.KIND_PROD else 2) + tq.record_bytes(vcb_i) + 2)
         res[name] = {"ms_per_call": ms, "packed_bytes": packed, "gbs": packed / (ms / 1e3) / 1e9}
-        del kc
+        del kc, vc_i
     return res
 
 
