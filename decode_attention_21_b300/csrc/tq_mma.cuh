@@ -35,6 +35,18 @@ __device__ __forceinline__ float piece16(float x, int which) {
   return which == 0 ? hi : x - hi;
 }
 
+// fp16 hi and lo pieces of two floats, packed: hi = pack(round(x0), round(x1)),
+// lo = pack(round(x0 - hi0), round(x1 - hi1)); the same bits as
+// pack_half2(piece16(x0, w), piece16(x1, w)) for w = 0, 1, in three
+// conversions instead of six.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 f = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - f.x, x1 - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // Packed bits as fp16 tensor-core operands.  A half whose only set bit is
 // bit p <= 11 is exactly 2^(p - 24) (bits 0..9 are subnormal mantissa bits,
 // bits 10 and 11 the two lowest exponent bits).  Operand register beta holds

@@ -243,16 +243,15 @@ __device__ __forceinline__ void polar_qk(const PolarTab& tab, const uint2 (&bq)[
       mma_f16(acc2[k & 1], ra[2 * k], rb[2 * k], ra[2 * k + 1], rb[2 * k + 1], bq[1][k].x, bq[1][k].y);
   }
 #pragma unroll
-  for (int pc = 0; pc < 2; ++pc) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int be = 2 * k;
-      const uint32_t a0 = pack_half2(piece16(ya[be], pc), piece16(ya[be + 16], pc));
-      const uint32_t a1 = pack_half2(piece16(yb[be], pc), piece16(yb[be + 16], pc));
-      const uint32_t a2 = pack_half2(piece16(ya[be + 1], pc), piece16(ya[be + 17], pc));
-      const uint32_t a3 = pack_half2(piece16(yb[be + 1], pc), piece16(yb[be + 17], pc));
-      mma_f16(acc1[pc], a0, a1, a2, a3, bq[0][k].x, bq[0][k].y);
-    }
+  for (int k = 0; k < 8; ++k) {
+    const int be = 2 * k;
+    uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+    split2(ya[be], ya[be + 16], h0, l0);
+    split2(yb[be], yb[be + 16], h1, l1);
+    split2(ya[be + 1], ya[be + 17], h2, l2);
+    split2(yb[be + 1], yb[be + 17], h3, l3);
+    mma_f16(acc1[0], h0, h1, h2, h3, bq[0][k].x, bq[0][k].y);
+    mma_f16(acc1[1], l0, l1, l2, l3, bq[0][k].x, bq[0][k].y);
   }
   s1a = (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]);
   s1b = (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]);
@@ -417,16 +416,15 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
         }
       }
 #pragma unroll
-      for (int pv = 0; pv < 2; ++pv) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int r0 = 2 * mt, r1 = 2 * mt + 1;
-          const uint32_t a0 = pack_half2(piece16(yv[0][r0], pv), piece16(yv[1][r0], pv));
-          const uint32_t a1 = pack_half2(piece16(yv[0][r1], pv), piece16(yv[1][r1], pv));
-          const uint32_t a2 = pack_half2(piece16(yv[2][r0], pv), piece16(yv[3][r0], pv));
-          const uint32_t a3 = pack_half2(piece16(yv[2][r1], pv), piece16(yv[3][r1], pv));
-          mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
-        }
+      for (int mt = 0; mt < 8; ++mt) {
+        const int r0 = 2 * mt, r1 = 2 * mt + 1;
+        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+        split2(yv[0][r0], yv[1][r0], h0, l0);
+        split2(yv[0][r1], yv[1][r1], h1, l1);
+        split2(yv[2][r0], yv[3][r0], h2, l2);
+        split2(yv[2][r1], yv[3][r1], h3, l3);
+        mma_f16(acc[mt], h0, h1, h2, h3, b0, b1);     // value hi pieces, then lo (same order per accumulator)
+        mma_f16(acc[mt], l0, l1, l2, l3, b0, b1);
       }
       if (++chain == 2 * kPvFlushStages) {
         tot.flush(acc);
@@ -627,16 +625,15 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
         }
       }
 #pragma unroll
-      for (int pv = 0; pv < 2; ++pv) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int q0 = 2 * mt, q1 = 2 * mt + 1;
-          const uint32_t a0 = pack_half2(piece16(yv[0][q0], pv), piece16(yv[1][q0], pv));
-          const uint32_t a1 = pack_half2(piece16(yv[0][q1], pv), piece16(yv[1][q1], pv));
-          const uint32_t a2 = pack_half2(piece16(yv[2][q0], pv), piece16(yv[3][q0], pv));
-          const uint32_t a3 = pack_half2(piece16(yv[2][q1], pv), piece16(yv[3][q1], pv));
-          mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
-        }
+      for (int mt = 0; mt < 8; ++mt) {
+        const int q0 = 2 * mt, q1 = 2 * mt + 1;
+        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+        split2(yv[0][q0], yv[1][q0], h0, l0);
+        split2(yv[0][q1], yv[1][q1], h1, l1);
+        split2(yv[2][q0], yv[3][q0], h2, l2);
+        split2(yv[2][q1], yv[3][q1], h3, l3);
+        mma_f16(acc[mt], h0, h1, h2, h3, b0, b1);     // value hi pieces, then lo (same order per accumulator)
+        mma_f16(acc[mt], l0, l1, l2, l3, b0, b1);
       }
     }
     if (st % kPvFlushStages == kPvFlushStages - 1) tot.flush(acc);
