@@ -7,15 +7,16 @@ batch 1, 32 query heads / 8 KV heads, head_dim 128, context 32768, 4-bit keys
 cache (tq_quantize) and score all 32768 x 8 cached keys against the 32
 full-precision query heads (tq_logits).  Metric: keys scored per second
 (one key = one (sequence, kv head, token) triple, scored for its 4 query
-heads).  The packed cache is 17.8 MB, so steps rotate over 16 cache copies
-(285 MB, more than twice the 126 MB L2).
+heads).  The packed cache is 17.8 MB, so steps rotate over enough cache
+copies (with their logits) to hold more than twice the 126 MB L2.
 
 Secondary workloads in the same line: fused decode attention (batch 8,
-context 131072, 3-bit keys and values) and cache-append quantization of
-1,048,576 vectors at b = 2, 3, 4 and the 2.5/3.5-bit mixes.
+context 131072, 3-bit keys and values; other key and value caches; the paged
+decode loop), cache-append quantization of 1,048,576 vectors at b = 2, 3, 4
+and the 2.5/3.5-bit mixes, and top-10 search over 10^6 rows.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload all|logits|attention|quantize]
+                    [--workload all|logits|attention|quantize|search]
 """
 import argparse
 import hashlib
