@@ -168,12 +168,17 @@ tq_status tq_logits_dense(const void* keys, int32_t key_dtype, int32_t d, int32_
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq,
                                      int32_t Hkv, int64_t capacity);
 
-/* Fused decode attention over compressed keys (PROD) and values (MSE):
+/* Fused decode attention over compressed keys and values (MSE kind):
  *   s_t = scale * logits[b, h, t], p = softmax over t < seq_lens[b],
  *   out[b, h] = Pi_v^T sum_t p_t n_v,t yhat_v,t
  * (weighted sum in the rotated domain, rotated back once per head; fp32
  * throughout).  seq_lens[b] == 0 gives a zero row.  Split-KV partials live
- * in the caller's workspace and are merged by a second kernel.              */
+ * in the caller's workspace and are merged by a second kernel.
+ * Key / value pairs: keys with the QJL term (PROD) at any width with values
+ * at 1-4 bits, in scalar or polar mode; in scalar mode and with a capacity
+ * that is a multiple of 16 also MSE-only keys or 2.5 / 3.5-bit keys (extra
+ * bits) with 3- or 4-bit values, and 2.5 / 3.5-bit values (extra = d/4, 2 or
+ * 3 bits) with keys that have the QJL term.  Other pairs: TQ_EUNSUPPORTED. */
 tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb,
                               const void* kcache, const void* vcache, int32_t B, int32_t Hq,
                               int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
