@@ -338,3 +338,21 @@ def test_dense_logits_brute_force():
                 for i in range(d):
                     want += float(q[b, h, i]) * float(K[b, h // 2, t, i])
                 assert abs(got[b, h, t] - want) <= 1e-12 * (1 + abs(want))
+
+
+def test_block_table_generator_assigns_distinct_pages():
+    """The paged-cache inputs: each sequence's first ceil(len / page) entries
+    are distinct pages of the pool (no page shared between sequences), the
+    rest are -1, and the same seed gives the same table."""
+    B, max_pages, num_pages, ps = 4, 9, 40, 16
+    lens = [144, 1, 0, 77]
+    t = wl.block_table(B, max_pages, num_pages, ps, lens)
+    assert t.shape == (B, max_pages) and t.dtype == np.int32
+    used = []
+    for b, L in enumerate(lens):
+        n = -(-L // ps)
+        assert np.all(t[b, n:] == -1)
+        assert np.all((t[b, :n] >= 0) & (t[b, :n] < num_pages))
+        used.extend(t[b, :n].tolist())
+    assert len(used) == len(set(used))
+    assert np.array_equal(t, wl.block_table(B, max_pages, num_pages, ps, lens))
