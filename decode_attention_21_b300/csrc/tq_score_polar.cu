@@ -57,31 +57,57 @@ __device__ __forceinline__ float subtree_radius(const PolarTab& tab, const uint3
   return rho6 * ((s & 1) ? r6.y : r6.x);
 }
 
+// Codes at bit positions pos .. pos + 7 of the B plane words (plane 0 = the
+// code's most significant bit), gathered into the nibbles of one word:
+// nibble i = the code at position pos + i.  Each plane's byte is spread to
+// nibble spacing by three shift-and-mask steps, so eight codes cost about
+// 8 B instructions instead of about 3 B each.
+template <int B>
+__device__ __forceinline__ uint32_t codes_x8(const uint32_t (&w)[B], int pos) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int p = 0; p < B; ++p) {
+    uint32_t x = (w[p] >> pos) & 0xFFu;
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    x = (x | (x << 3)) & 0x11111111u;
+    r = (r << 1) | x;
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint32_t nib(uint32_t r, int i) { return (r >> (4 * i)) & 0xFu; }
+
 // The 16 leaves of half h of subtree s, starting from the subtree radius.
+// Angle codes of a subtree word: level 1 at bits 0..15, level 2 at 16..23,
+// level 3 at 24..27, level 4 at 28..29, level 5 at 30.
 template <int B>
 __device__ __forceinline__ void decode_half(const PolarTab& tab, const uint32_t (&ws)[B], float rho5, int h,
                                             float (&y)[16]) {
-  const float2 a5 = tab.t[5][code_at<B>(ws, 30)];
+  const uint32_t n1 = codes_x8<B>(ws, 8 * h);        // level 1: codes 8h .. 8h + 7
+  const uint32_t n2 = codes_x8<B>(ws, 16 + 4 * h);   // level 2: nibbles 0..3
+  const uint32_t n3 = codes_x8<B>(ws, 24);           // level 3: nibbles 0..3, level 4: 4, 5, level 5: 6
+  const float2 a5 = tab.t[5][nib(n3, 6)];
   const float rho4 = rho5 * (h ? a5.y : a5.x);
-  const float2 a4 = tab.t[4][code_at<B>(ws, 28 + h)];
+  const float2 a4 = tab.t[4][nib(n3, 4 + h)];
   float r3[2] = {rho4 * a4.x, rho4 * a4.y};
   float r2[4];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const float2 a = tab.t[3][code_at<B>(ws, 24 + 2 * h + i)];
+    const float2 a = tab.t[3][nib(n3, 2 * h + i)];
     r2[2 * i] = r3[i] * a.x;
     r2[2 * i + 1] = r3[i] * a.y;
   }
   float r1[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 a = tab.t[2][code_at<B>(ws, 16 + 4 * h + i)];
+    const float2 a = tab.t[2][nib(n2, i)];
     r1[2 * i] = r2[i] * a.x;
     r1[2 * i + 1] = r2[i] * a.y;
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float2 a = tab.t[1][code_at<B>(ws, 8 * h + i)];
+    const float2 a = tab.t[1][nib(n1, i)];
     y[2 * i] = r1[i] * a.x;
     y[2 * i + 1] = r1[i] * a.y;
   }
