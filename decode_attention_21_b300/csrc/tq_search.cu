@@ -224,6 +224,9 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
     nna = (live && ta < n_db) ? __ldg(nrm + ta) : 0u;
     nnb = (live && tb < n_db) ? __ldg(nrm + tb) : 0u;
   };
+  // score a row must beat to enter this lane's query list (its k-th score
+  // once the list is full), kept in a register and refreshed after insertions
+  float thr = -INFINITY;
   if (c0 < ntiles) fetch(c0);
   // rounds of kRound tiles: each half scores its coordinates of the round's
   // tiles, the two halves of a group meet once per round
@@ -304,9 +307,9 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
         for (int h = 0; h < 2; ++h) {
           const float sc = h == 0 ? sa : sb;
           const int64_t id = h == 0 ? ta : tb;
-          const int cnt = ln[qslot];
-          const bool cand = qok && id < n_db && (cnt < k || sc > ls[qslot * kMaxK + k - 1]);
+          const bool cand = qok && id < n_db && sc > thr;
           unsigned mask = __ballot_sync(kFull, cand);
+          const bool any = mask != 0u;
           while (mask) {
             const int src = __ffs(mask) - 1;
             mask &= mask - 1;
@@ -333,6 +336,8 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
             }
             __syncwarp();
           }
+          // a list changed: refresh this lane's entry threshold
+          if (any) thr = ln[qslot] < k ? -INFINITY : ls[qslot * kMaxK + k - 1];
         }
       }
     }
