@@ -47,6 +47,14 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Piece `which` (0 = hi, 1 = lo) of two floats, packed: the same bits as
+// pack_half2(piece16(x0, which), piece16(x1, which)).
+__device__ __forceinline__ uint32_t piece2(float x0, float x1, int which) {
+  uint32_t hi, lo;
+  split2(x0, x1, hi, lo);
+  return which ? lo : hi;
+}
+
 // Packed bits as fp16 tensor-core operands.  A half whose only set bit is
 // bit p <= 11 is exactly 2^(p - 24) (bits 0..9 are subnormal mantissa bits,
 // bits 10 and 11 the two lowest exponent bits).  Operand register beta holds

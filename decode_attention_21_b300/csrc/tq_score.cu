@@ -793,8 +793,8 @@ __global__ void __launch_bounds__(128, 2) k_attn(const Dev kcb, const Dev vcb, c
 #pragma unroll
       for (int u = 0; u < NVV; ++u) {
         const float cu = vcn[u];
-        const uint32_t b0 = pack_half2(piece16(cu * w0, pc), piece16(cu * w1, pc));
-        const uint32_t b1 = pack_half2(piece16(cu * w8, pc), piece16(cu * w9, pc));
+        const uint32_t b0 = piece2(cu * w0, cu * w1, pc);
+        const uint32_t b1 = piece2(cu * w8, cu * w9, pc);
         uint32_t x[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -1063,8 +1063,8 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
 #pragma unroll
       for (int u = 0; u < NVV; ++u) {
         const float cu = vcn[u];
-        const uint32_t b0 = pack_half2(piece16(cu * w0, pc), piece16(cu * w1, pc));
-        const uint32_t b1 = pack_half2(piece16(cu * w8, pc), piece16(cu * w9, pc));
+        const uint32_t b0 = piece2(cu * w0, cu * w1, pc);
+        const uint32_t b1 = piece2(cu * w8, cu * w9, pc);
         uint32_t x[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -1087,8 +1087,8 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
 #pragma unroll
         for (int u = 0; u < 2 * NVV; ++u) {
           const float cu = vcnx[u];
-          const uint32_t b0 = pack_half2(piece16(cu * w0, pc), piece16(cu * w1, pc));
-          const uint32_t b1 = pack_half2(piece16(cu * w8, pc), piece16(cu * w9, pc));
+          const uint32_t b0 = piece2(cu * w0, cu * w1, pc);
+          const uint32_t b1 = piece2(cu * w8, cu * w9, pc);
           uint32_t x[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {

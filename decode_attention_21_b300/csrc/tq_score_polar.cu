@@ -418,8 +418,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
       const float w1 = __shfl_sync(kFull, wA, src1);
       const float w8 = __shfl_sync(kFull, wB, src0);
       const float w9 = __shfl_sync(kFull, wB, src1);
-      const uint32_t b0 = pack_half2(piece16(w0, pc), piece16(w1, pc));
-      const uint32_t b1 = pack_half2(piece16(w8, pc), piece16(w9, pc));
+      const uint32_t b0 = piece2(w0, w1, pc);
+      const uint32_t b1 = piece2(w8, w9, pc);
       // decode this thread's 16 value coordinates of tokens 2c, 2c+1, 2c+8, 2c+9
       float yv[4][16];
 #pragma unroll
@@ -627,8 +627,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
       const float w1 = __shfl_sync(kFull, wA, src1);
       const float w8 = __shfl_sync(kFull, wB, src0);
       const float w9 = __shfl_sync(kFull, wB, src1);
-      const uint32_t b0 = pack_half2(piece16(w0, pc), piece16(w1, pc));
-      const uint32_t b1 = pack_half2(piece16(w8, pc), piece16(w9, pc));
+      const uint32_t b0 = piece2(w0, w1, pc);
+      const uint32_t b1 = piece2(w8, w9, pc);
       // decode this thread's 16 value coordinates of tokens 2c, 2c+1, 2c+8, 2c+9
       float yv[4][16];
 #pragma unroll
