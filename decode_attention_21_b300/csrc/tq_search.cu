@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
   __syncthreads();
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(db);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(db + norm_offset(cb, n_db));
-  const int W = cb.W;
+  constexpr int W = (kD / 32) * P;            // record words (d = 256, no extra-bit words)
   const float kq = cb.qjl_const;
   const int word = c + 4 * half;
   const int qslot = gl * 4 + c;               // this thread's query (shared-memory list index)
