@@ -180,6 +180,60 @@ def test_polar_error_decreases_with_bits():
     assert all(errs[i + 1] < errs[i] for i in range(3))
 
 
+def _centroid_angles(tab, idx):
+    """Level-ordered centroid angles of codes idx, each level from its own table."""
+    out, off = [], 0
+    for lev in range(1, tab.D + 1):
+        n = tab.n_angles(lev)
+        out.append(tab.cent32[lev].astype(np.float64)[idx[:, off:off + n]])
+        off += n
+    return np.concatenate(out, axis=1)
+
+
+@pytest.mark.parametrize("d,bits", [(8, 1), (8, 3), (128, 2), (256, 3)])
+def test_polar_decode_is_the_tree_walk_of_the_centroid_angles(d, bits):
+    # [xujun] 第一步 / [suzuke] 第二步: decoding replaces every angle by its
+    # cell's centroid and walks the radius tree back down; decode_angles is
+    # pinned separately by the exact arctan2 round trip, so a swapped cos/sin
+    # or a level read from the wrong table in polar_decode shows up here
+    tab = polar.PolarTables(d, bits)
+    rng = np.random.default_rng(21 + d + bits)
+    idx = rng.integers(0, tab.L, size=(300, d - 1))
+    got = polar.polar_decode(tab, idx)
+    want = polar.decode_angles(d, _centroid_angles(tab, idx))
+    assert np.max(np.abs(got - want)) < 1e-12
+    roots = rng.uniform(0.5, 2.0, size=300)
+    got = polar.polar_decode(tab, idx, root=roots)
+    want = polar.decode_angles(d, _centroid_angles(tab, idx), root=roots)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_polar_decode_d8_written_out_by_hand(bits):
+    # d = 8: four level-1 angles t0..t3 (pairs (y0,y1) .. (y6,y7)), two level-2
+    # angles a (over the radii of pairs 0,1) and b (pairs 2,3), one level-3
+    # angle c (over the two level-2 radii); root radius 1.  Every code word.
+    tab = polar.PolarTables(8, bits)
+    L = tab.L
+    words = np.array(list(itertools.product(range(L), repeat=7)))
+    th = tab.cent32[1].astype(np.float64)[words[:, 0:4]]
+    a = tab.cent32[2].astype(np.float64)[words[:, 4]]
+    b = tab.cent32[2].astype(np.float64)[words[:, 5]]
+    c = tab.cent32[3].astype(np.float64)[words[:, 6]]
+    cos, sin = np.cos, np.sin
+    want = np.stack([
+        cos(c) * cos(a) * cos(th[:, 0]), cos(c) * cos(a) * sin(th[:, 0]),
+        cos(c) * sin(a) * cos(th[:, 1]), cos(c) * sin(a) * sin(th[:, 1]),
+        sin(c) * cos(b) * cos(th[:, 2]), sin(c) * cos(b) * sin(th[:, 2]),
+        sin(c) * sin(b) * cos(th[:, 3]), sin(c) * sin(b) * sin(th[:, 3]),
+    ], axis=1)
+    got = polar.polar_decode(tab, words)
+    assert np.max(np.abs(got - want)) < 1e-12
+    # the level-2 and level-3 laws differ (sin^1(2 psi) vs sin^3(2 psi)), so a
+    # level decoded with another level's table would not match
+    assert not np.allclose(tab.cent32[2], tab.cent32[3])
+
+
 def test_polar_quadrant_rule():
     tab = polar.PolarTables(8, 3)
     # points on the axes and at 45 degrees: ties go to the upper cell; the zero
