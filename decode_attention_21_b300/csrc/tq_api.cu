@@ -630,14 +630,26 @@ tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* 
   return launched("tq_advance_lengths", tq::launch_advance_lengths(seq_lens, B, delta, static_cast<cudaStream_t>(stream)));
 }
 
-size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
-  if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
+// Split of the context of a decode-attention launch and the workspace it
+// writes: the query fragments, then one partial per (sequence, kv head,
+// chunk, warp).  The launch and every workspace bound use this one helper;
+// without a value codebook it gives the largest split any value codebook
+// can get (a value codebook only ever lowers the resident-CTA target).
+static int64_t attn_workspace_bytes(const tq_codebook* kcb, const tq_codebook* vcb, int32_t B, int32_t Hkv,
+                                    int64_t capacity, int* nchunks_out = nullptr, int* tpc_out = nullptr) {
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, attn_ctas(kcb), &nchunks, &tpc);
+  chunking(B, Hkv, capacity, attn_ctas(kcb, vcb), &nchunks, &tpc);
+  if (nchunks_out) *nchunks_out = nchunks;
+  if (tpc_out) *tpc_out = tpc;
   const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d));
   const int64_t parts = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d) * 4;
+  return prep + parts;
+}
+
+size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
+  if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
   (void)Hq;
-  return (size_t)(prep + parts);
+  return (size_t)attn_workspace_bytes(kcb, nullptr, B, Hkv, capacity);
 }
 
 static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache,
@@ -676,7 +688,8 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
   if (!aligned16(kcache) || !aligned16(vcache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
     return fail(TQ_EINVAL, "%s: device pointers must be 16-byte aligned", what);
   if (!std::isfinite(scale)) return fail(TQ_EINVAL, "%s: scale must be finite", what);
-  if (ws_bytes < tq_decode_attention_workspace(kcb, B, Hq, Hkv, capacity))
+  int nchunks, tpc;
+  if (ws_bytes < (size_t)attn_workspace_bytes(kcb, vcb, B, Hkv, capacity, &nchunks, &tpc))
     return fail(TQ_ENOMEM, "%s: workspace too small", what);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
@@ -684,8 +697,6 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
       prep + tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d)));
   if (kcb->dev.mode != vcb->dev.mode)
     return fail(TQ_EUNSUPPORTED, "%s: keys and values must use the same stage-1 mode", what);
-  int nchunks, tpc;
-  chunking(B, Hkv, capacity, attn_ctas(kcb, vcb), &nchunks, &tpc);
   const float sl2 = scale * 1.4426950408889634f;
   if (kcb->dev.mode == TQ_MODE_POLAR) {
     if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)

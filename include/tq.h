@@ -168,7 +168,13 @@ tq_status tq_logits_dense(const void* keys, int32_t key_dtype, int32_t d, int32_
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq,
                                      int32_t Hkv, int64_t capacity);
 
-/* Fused decode attention over compressed keys and values (MSE kind):
+/* Fused decode attention over compressed keys and values (MSE kind).
+ * [xujun] 常见问题: the attention step over the compressed cache is where the
+ * quoted speed-up over unquantized keys comes from (not end to end);
+ * [suzuke] 為什麼這個方法特別聰明: keys and values are compressed online, one
+ * token at a time, so each decode step attends over the compressed cache as
+ * it stands; [cnyes] 1 bit 掃尾: the logits inside are the estimator of
+ * tq_logits (full-precision query, compressed keys).
  *   s_t = scale * logits[b, h, t], p = softmax over t < seq_lens[b],
  *   out[b, h] = Pi_v^T sum_t p_t n_v,t yhat_v,t
  * (weighted sum in the rotated domain, rotated back once per head; fp32
