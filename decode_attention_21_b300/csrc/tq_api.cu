@@ -755,6 +755,7 @@ tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* v
 
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k) {
   if (!cb || nq <= 0 || n_db <= 0 || k < 1) return 0;
+  if (tq::search_tc_applies(cb->dev, k)) return (size_t)tq::search_tc_workspace_bytes(cb->dev, n_db, nq, k, cb->sms);
   return (size_t)tq::search_workspace_bytes(cb->dev, n_db, nq, k, cb->sms);
 }
 
@@ -775,9 +776,27 @@ tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, c
   int dev = -1;
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "tq_search: codebook lives on another device");
+  if (tq::search_tc_applies(cb->dev, k))
+    return launched("tq_search", tq::launch_search_tc(cb->dev, static_cast<const uint8_t*>(db_cache), n_db, q, nq, d_in,
+                                                      k, ids, scores, static_cast<uint8_t*>(workspace), cb->sms,
+                                                      cb->d_status, static_cast<cudaStream_t>(stream)));
   return launched("tq_search", tq::launch_search(cb->dev, static_cast<const uint8_t*>(db_cache), n_db, q, nq, d_in, k,
                                                 ids, scores, static_cast<uint8_t*>(workspace), cb->sms,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_search_fallbacks(const tq_codebook* cb, const void* workspace, int32_t k, int32_t* count) {
+  if (!cb || !workspace || !count) return fail(TQ_EINVAL, "tq_search_fallbacks: NULL argument");
+  if (!tq::search_tc_applies(cb->dev, k)) {
+    *count = -1;
+    return ok();
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  unsigned v = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, static_cast<const unsigned*>(workspace) + 2, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(TQ_ECUDA, "tq_search_fallbacks: %s", cudaGetErrorString(e));
+  *count = (int32_t)v;
+  return ok();
 }
 
 }  // extern "C"

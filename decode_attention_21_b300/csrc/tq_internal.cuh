@@ -176,6 +176,16 @@ cudaError_t launch_attn_polar(const Dev& kcb, const Dev& vcb, const uint8_t* kca
 int64_t search_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, int sms);
 cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
                           int32_t* ids, float* scores, uint8_t* prep, int sms, cudaStream_t s);
+cudaError_t launch_search_subset(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in,
+                                 int k, int32_t* ids, float* scores, uint8_t* prep, int sms, const int32_t* qmap,
+                                 const unsigned* qcount, cudaStream_t s);
+// Tensor-core search (tcgen05 candidates + exact re-ranking), for d = 256
+// scalar-mode databases without extra bits and k <= 16.  Its workspace starts
+// with 64 status words; word 2 counts the queries sent to the exact scan.
+bool search_tc_applies(const Dev& cb, int k);
+int64_t search_tc_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, int sms);
+cudaError_t launch_search_tc(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
+                             int32_t* ids, float* scores, uint8_t* ws, int sms, int* status, cudaStream_t s);
 cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts, float* out,
                               cudaStream_t s);
 

@@ -94,11 +94,17 @@ __host__ __device__ inline int64_t search_block_bytes(int nv) { return kPrepHead
 
 // Fragment layout: [plane][kb (16)][lane] uint2; k-block kb covers word
 // c + 4 (kb / 8) of thread c, bit positions beta = 2 (kb % 8) (+1 for b1).
+// With a query map (qmap, *qcount), query slot v of the scan is query
+// qmap[v] for v < *qcount, and the rest of the grid does nothing.
 __global__ void __launch_bounds__(1024) k_search_prep(const Dev cb, const float* __restrict__ q, int nq, int d_in,
-                                                      uint8_t* __restrict__ prep) {
+                                                      uint8_t* __restrict__ prep, const int32_t* __restrict__ qmap,
+                                                      const unsigned* __restrict__ qcount) {
   const int grp = blockIdx.x, slot = blockIdx.y;
-  const int qi = grp * 4 + slot;
-  const bool live = qi < nq;
+  const int v = grp * 4 + slot;
+  const int nv_live = qmap ? (int)min(*qcount, (unsigned)nq) : nq;
+  if (grp * 4 >= nv_live) return;           // no live query in this group
+  const bool live = v < nv_live;
+  const int qi = live && qmap ? qmap[v] : v;
   __shared__ float sq[kD], sq1[kD], sq2[kD], part[4][kD], part2[4][kD];
   __shared__ float red[4];
   const int tid = threadIdx.x;
@@ -176,7 +182,8 @@ template <int NV, int P>
 __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev cb, const uint8_t* __restrict__ db,
                                                    int64_t n_db, const uint8_t* __restrict__ prep, int nq, int k,
                                                    int tiles_per_chunk, int32_t* __restrict__ ids,
-                                                   float* __restrict__ scores) {
+                                                   float* __restrict__ scores, const int32_t* __restrict__ qmap,
+                                                   const unsigned* __restrict__ qcount) {
   __shared__ float xch[2][4][kRound][4][32];  // [buffer][group][tile of the round][acc element][lane]
   __shared__ float top_s[2][16][kMaxK];       // [coordinate half][query slot][rank]
   __shared__ int32_t top_i[2][16][kMaxK];
@@ -184,7 +191,9 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gl = warp >> 1, half = warp & 1;
   const int grp = blockIdx.x * 4 + gl;
-  const int ngroups = (nq + 3) / 4;
+  const int nv_live = qmap ? (int)min(*qcount, (unsigned)nq) : nq;
+  if (blockIdx.x * 16 >= nv_live) return;   // no live query in this CTA (uniform)
+  const int ngroups = (nv_live + 3) / 4;
   const int g = lane >> 2, c = lane & 3;
   const bool live = grp < ngroups;
   if (threadIdx.x < 32) top_n[threadIdx.x >> 4][threadIdx.x & 15] = 0;
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
         for (int e = 0; e < 4; ++e) xch[buf][gl][u][e][lane] = part[u][e];
     asm volatile("bar.sync %0, 64;" ::"r"(1 + gl));
     if (live) {
-      const bool qok = grp * 4 + c < nq;
+      const bool qok = grp * 4 + c < nv_live;
 #pragma unroll
       for (int u = 0; u < kRound; ++u) {
         if (u / (kRound / 2) != half) continue;
@@ -345,8 +354,10 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
   __syncthreads();
   // merge the two halves' lists of each query (decreasing score, ties to the smaller id)
   if (half == 0 && live && lane < 4) {
-    const int qi = grp * 4 + lane;
-    if (qi < nq) {
+    const int qi = grp * 4 + lane;            // query slot
+    // final lists (one chunk) go to the query's own row; per-chunk lists stay in slot order
+    const int qo = (gridDim.y == 1 && qmap) ? (qi < nv_live ? qmap[qi] : 0) : qi;
+    if (qi < nv_live) {
       const int qs = gl * 4 + lane;
       const int na = top_n[0][qs], nb = top_n[1][qs];
       int ia = 0, ib = 0;
@@ -365,8 +376,8 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
           if (take_a) ++ia;
           else ++ib;
         }
-        ids[((size_t)blockIdx.y * nq + qi) * k + j] = id;
-        scores[((size_t)blockIdx.y * nq + qi) * k + j] = sc;
+        ids[((size_t)blockIdx.y * nq + qo) * k + j] = id;
+        scores[((size_t)blockIdx.y * nq + qo) * k + j] = sc;
       }
     }
   }
@@ -378,11 +389,14 @@ __global__ void __launch_bounds__(256, search_ctas_per_sm(P)) k_search(const Dev
 // missing entry is id -1 with score -inf and ranks last).
 __global__ void __launch_bounds__(128) k_search_merge(const int32_t* __restrict__ pid, const float* __restrict__ psc,
                                                       int chunks, int nq, int k, int32_t* __restrict__ ids,
-                                                      float* __restrict__ scores) {
+                                                      float* __restrict__ scores, const int32_t* __restrict__ qmap,
+                                                      const unsigned* __restrict__ qcount) {
   constexpr int kPer = kMaxChunks * kMaxK / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qi = blockIdx.x * 4 + warp;
-  if (qi >= nq) return;
+  const int qi = blockIdx.x * 4 + warp;     // query slot
+  const int nv_live = qmap ? (int)min(*qcount, (unsigned)nq) : nq;
+  if (qi >= nv_live) return;
+  const int qo = qmap ? qmap[qi] : qi;      // output row
   const int n = chunks * k;
   float s[kPer];
   int32_t id[kPer];
@@ -433,8 +447,8 @@ __global__ void __launch_bounds__(128) k_search_merge(const int32_t* __restrict_
         }
     }
     if (lane == 0) {
-      ids[(size_t)qi * k + out] = wi;
-      scores[(size_t)qi * k + out] = wi >= 0 ? ws : -INFINITY;
+      ids[(size_t)qo * k + out] = wi;
+      scores[(size_t)qo * k + out] = wi >= 0 ? ws : -INFINITY;
     }
   }
 }
@@ -467,10 +481,13 @@ int64_t search_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, int s
   return chunks > 1 ? prep + align256((int64_t)chunks * nq * k * 8) : prep;
 }
 
-cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
-                          int32_t* ids, float* scores, uint8_t* prep, int sms, cudaStream_t s) {
+// The exact scan over all queries (qmap == nullptr) or over the queries
+// qmap[0 .. *qcount - 1] (grids sized for nq; slots past *qcount exit).
+cudaError_t launch_search_subset(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in,
+                                 int k, int32_t* ids, float* scores, uint8_t* prep, int sms, const int32_t* qmap,
+                                 const unsigned* qcount, cudaStream_t s) {
   const int ngroups = (nq + 3) / 4;
-  k_search_prep<<<dim3(ngroups, 4), 1024, 0, s>>>(cb, q, nq, d_in, prep);
+  k_search_prep<<<dim3(ngroups, 4), 1024, 0, s>>>(cb, q, nq, d_in, prep, qmap, qcount);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int chunks = search_chunks(cb, n_db, nq, sms);
@@ -486,14 +503,19 @@ cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const 
   }
   const dim3 grid((ngroups + 3) / 4, chunks);
   switch (cb.b1) {
-    case 1: k_search<1, 2><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc); break;
-    case 2: k_search<2, 3><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc); break;
-    default: k_search<4, 4><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc); break;
+    case 1: k_search<1, 2><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc, qmap, qcount); break;
+    case 2: k_search<2, 3><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc, qmap, qcount); break;
+    default: k_search<4, 4><<<grid, 256, 0, s>>>(cb, db, n_db, prep, nq, k, (int)tpc, oid, osc, qmap, qcount); break;
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || chunks == 1) return e;
-  k_search_merge<<<(nq + 3) / 4, 128, 0, s>>>(oid, osc, chunks, nq, k, ids, scores);
+  k_search_merge<<<(nq + 3) / 4, 128, 0, s>>>(oid, osc, chunks, nq, k, ids, scores, qmap, qcount);
   return cudaGetLastError();
+}
+
+cudaError_t launch_search(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
+                          int32_t* ids, float* scores, uint8_t* prep, int sms, cudaStream_t s) {
+  return launch_search_subset(cb, db, n_db, q, nq, d_in, k, ids, scores, prep, sms, nullptr, nullptr, s);
 }
 
 }  // namespace tq

@@ -20,7 +20,7 @@ F32, BF16 = 0, 1
 EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_host_tables", "tq_record_bytes", "tq_cache_bytes",
            "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits", "tq_logits_dense",
            "tq_decode_attention_workspace", "tq_decode_attention", "tq_decode_attention_static",
-           "tq_search_workspace", "tq_search",
+           "tq_search_workspace", "tq_search", "tq_search_fallbacks",
            "tq_append_paged", "tq_logits_paged", "tq_decode_attention_paged", "tq_advance_lengths",
            "tq_check_device", "tq_last_error"]
 
@@ -72,6 +72,7 @@ def lib():
         L.tq_search_workspace.argtypes = [vp, i64, i32, i32]
         L.tq_search_workspace.restype = sz
         L.tq_search.argtypes = [vp, vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.tq_search_fallbacks.argtypes = [vp, vp, i32, ctypes.POINTER(i32)]
         L.tq_append_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, vp, vp, i32, i32, vp]
         L.tq_logits_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
         L.tq_decode_attention_paged.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp,
@@ -228,6 +229,14 @@ def tq_search_workspace(cb, n_db, nq, k):
 def tq_search(cb, db_cache, n_db, q, nq, d_in, k, ids, scores, workspace, stream=None):
     _check(lib().tq_search(cb.handle, _ptr(db_cache), n_db, _ptr(q), nq, d_in, k, _ptr(ids), _ptr(scores),
                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_search_fallbacks(cb, workspace, k):
+    """Queries of the last tq_search on ``workspace`` that the exact scan re-ran
+    (-1: that call used the exact scan only).  Synchronises the device."""
+    n = ctypes.c_int32()
+    _check(lib().tq_search_fallbacks(cb.handle, _ptr(workspace), k, ctypes.byref(n)))
+    return n.value
 
 
 def tq_append_paged(cb, cache, num_pages, page_size, block_table, B, Hkv, seq_lens, x, d_in, stream=None):

@@ -269,8 +269,9 @@ tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* v
  * can be captured once in a CUDA graph and replayed step after step.        */
 tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* stream);
 
-/* Workspace bytes of tq_search: query fragments, plus per-chunk top-k lists
- * when the scan is split over database chunks (depends on n_db, nq, k). */
+/* Workspace bytes of tq_search (depends on n_db, nq, k): query operands and
+ * candidate lists of the tensor-core scan, plus the exact scan's query
+ * fragments and per-chunk top-k lists. */
 size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int32_t k);
 
 /* Top-k inner-product search over a compressed database ([xujun] 常见问题,
@@ -278,10 +279,25 @@ size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int3
  * query, the k best rows by decreasing score, ties to the smaller id.
  *   db_cache   device, rows 0..n_db-1, PROD kind
  *   q          device fp32 [nq, d_in], d_in <= d (zero-padded)
- *   ids        device int32 [nq, k];  scores  device fp32 [nq, k]           */
+ *   ids        device int32 [nq, k];  scores  device fp32 [nq, k]; entries
+ *              past n_db are id -1, score -inf
+ *   k          1..32
+ * Scores are the fp32 estimator of the returned rows.  With d = 256 (scalar
+ * mode, no extra bits) and k <= 16, candidates come from fp16 tensor-core
+ * scores (tcgen05, queries held in tensor memory) whose error against the
+ * estimator is bounded per query; the candidates are re-scored exactly, and a
+ * query whose candidate lists cannot prove its top k (the bound is too wide
+ * for its score gaps, e.g. many equal rows) is re-run by the exact scan, so
+ * the result is that of the exact scan either way.  Other shapes run the
+ * exact scan (fp16 bit-plane products on mma.sync) directly.                */
 tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, const float* q,
                     int32_t nq, int32_t d_in, int32_t k, int32_t* ids, float* scores,
                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Test and diagnostic use (synchronises the device): *count = the number of
+ * queries of the last tq_search on `workspace` that the exact scan re-ran, or
+ * -1 when that call (this codebook, this k) used the exact scan only.       */
+tq_status tq_search_fallbacks(const tq_codebook* cb, const void* workspace, int32_t k, int32_t* count);
 
 /* Synchronise the device and report, since the last check, whether any
  * kernel of this codebook gave up a bounded wait on its own copies or

@@ -476,23 +476,22 @@ def test_quantize_tensor_core_path(bits, kind, extra, n):
         assert np.allclose(got["g16"][perm].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4])
-@pytest.mark.parametrize("n_db,nq,k", [(20013, 37, 10), (7, 5, 10), (4096, 8, 1)])
-def test_search_parity(bits, n_db, nq, k):
+def check_search(ocb, gcb, x, q, k, expect_fallbacks=None):
     """Top-k ids equal to the oracle's on the oracle's own packed database,
-    except swaps among near-tied scores (oracle scores within 1e-5 relative)."""
-    ocb, gcb = pair(256, bits)
-    x = wl.search_rows(n_db, "db")
-    q = wl.search_rows(nq, "search_q")
+    except swaps among near-tied scores (oracle scores within 1e-5 relative);
+    returns the number of queries the exact scan re-ran (-1: exact scan only)."""
+    n_db, nq = x.shape[0], q.shape[0]
     code = quant.quantize(ocb, x.astype(np.float64))
     img = torch.from_numpy(layout.write_cache(ocb, n_db, code)).cuda()
     ref_ids, ref_sc = estimate.search(ocb, code, q.astype(np.float64), min(k, n_db))
     full = estimate.estimate(ocb, q.astype(np.float64), code)
-    ws = torch.empty(tq.tq_search_workspace(gcb, n_db, nq, k), dtype=torch.uint8, device="cuda")
+    ws = torch.full((tq.tq_search_workspace(gcb, n_db, nq, k),), 0xFF, dtype=torch.uint8, device="cuda")
     ids = torch.full((nq, k), -7, dtype=torch.int32, device="cuda")
     sc = torch.full((nq, k), float("nan"), device="cuda")
     tq.tq_search(gcb, img, n_db, torch.from_numpy(q).cuda(), nq, q.shape[1], k, ids, sc, ws)
     torch.cuda.synchronize()
+    fallbacks = tq.tq_search_fallbacks(gcb, ws, k)
+    assert tq.tq_check_device(gcb) is None
     gi, gs = ids.cpu().numpy(), sc.cpu().numpy()
     kk = min(k, n_db)
     assert np.all(gi[:, kk:] == -1)
@@ -510,3 +509,39 @@ def test_search_parity(bits, n_db, nq, k):
             assert abs(full[r, g_ids[j]] - ref_sc[r, j]) <= tol
         # sorted by decreasing score
         assert np.all(np.diff(gs[r, :kk]) <= tol)
+    if expect_fallbacks is not None:
+        assert fallbacks == expect_fallbacks, fallbacks
+    return fallbacks
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("n_db,nq,k", [(20013, 37, 10), (7, 5, 10), (4096, 8, 1), (50000, 300, 16)])
+def test_search_parity(bits, n_db, nq, k):
+    """d = 256, k <= 16: tensor-core candidates and exact re-ranking; on this
+    data every query's top k is certified, so the exact scan re-runs none."""
+    ocb, gcb = pair(256, bits)
+    check_search(ocb, gcb, wl.search_rows(n_db, "db"), wl.search_rows(nq, "search_q"), k, expect_fallbacks=0)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_search_parity_exact_scan_for_large_k(bits):
+    """k > 16 runs the exact scan for every query."""
+    ocb, gcb = pair(256, bits)
+    check_search(ocb, gcb, wl.search_rows(6000, "db"), wl.search_rows(19, "search_q"), 20, expect_fallbacks=-1)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_search_uncertified_queries_fall_back_to_the_exact_scan(bits):
+    """40 consecutive copies of a query's best-scoring row inside one 128-row
+    tile put 40 equal scores at the top of one scan part: its list of 32
+    candidates is all ties, so it cannot prove the top 10 and the query is
+    re-run by the exact scan; the result is still the oracle's."""
+    ocb, gcb = pair(256, bits)
+    x = wl.search_rows(9000, "db")
+    q = wl.search_rows(12, "search_q")
+    est = estimate.estimate(ocb, q.astype(np.float64), quant.quantize(ocb, x.astype(np.float64)))
+    for j, tile in enumerate((8, 20, 40, 60)):   # queries 0..3
+        best = int(np.argmax(est[j]))
+        x[128 * tile + 10:128 * tile + 50] = x[best]
+    n = check_search(ocb, gcb, x, q, 10)
+    assert n >= 4, n
