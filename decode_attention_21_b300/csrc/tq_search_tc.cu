@@ -54,27 +54,37 @@ constexpr int kQ = 128;              // queries per block (TMEM lanes, MMA M)
 constexpr int kR = 128;              // database rows per tile (MMA N)
 constexpr int kCand = 32;            // candidates kept per (query, part)
 constexpr int kMaxKTc = 16;          // largest k served by this path
-constexpr int kSlots = 8;            // B ring slots
 constexpr int kStg = 2;              // staging slots of packed records (bulk copies)
-constexpr int kStgBytes = kR * 128 + kR * 4;   // records (<= 128 B each) + norm entries
+// Per stage-1 width b': record bytes, staging slot bytes (records + norm
+// entries) and B ring slots (as many 16 KB K-blocks as shared memory holds).
+__host__ __device__ constexpr int rec_bytes(int b1) { return 32 * (b1 + 1); }
+__host__ __device__ constexpr int stg_bytes(int b1) { return kR * rec_bytes(b1) + kR * 4; }
+__host__ __device__ constexpr int ring_slots(int b1) { return b1 == 3 ? 9 : 10; }
 constexpr int kSlotBytes = kR * 128; // 128 rows x 64 fp16 (one K-block)
-constexpr int kThreads = 384;        // warps: 0 MMA, 1 loader, 2-3 idle, 4-7 epilogue, 8-11 decoders
+constexpr int kDecWarps = 4;         // decoder warps (4: both word columns of a round per thread)
+constexpr int kThreads = 256 + 32 * kDecWarps;   // warps: 0 MMA, 1 loader, 2-3 idle, 4-7 epilogue, 8.. decoders
 constexpr int kPrepQ = 32;           // queries per prep CTA
 constexpr long long kSpin = 1ll << 26;
 constexpr uint32_t kTmemCols = 512;  // A: 0..255, D0: 256..383, D1: 384..511
 // D = F32, A = B = F16, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-// shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kOffRing = 0;
-constexpr uint32_t kOffStg = kOffRing + kSlots * kSlotBytes;        // kStg x (records, norms)
-constexpr uint32_t kOffLsc = kOffStg + kStg * kStgBytes;            // float [kCand][kQ]
-constexpr uint32_t kOffLid = kOffLsc + kCand * kQ * 4;              // int   [kCand][kQ]
-constexpr uint32_t kOffScr = kOffLid + kCand * kQ * 4;              // float [4 warps][32][33] candidate scores
-constexpr uint32_t kOffNrm = kOffScr + 4 * 32 * 33 * 4;             // float [2][kR]
-constexpr uint32_t kOffBar = kOffNrm + 2 * kR * 4;                  // mbarriers
-constexpr int kNumBars = 2 * kSlots + 8 + 2 * kStg;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;               // tmem base, abort flag
-constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+// shared memory map (offsets from a 1024-aligned base): B ring, staging,
+// candidate lists (float / int [kCand][kQ]), tile norms [2][kR], mbarriers,
+// then the TMEM base address and the abort flag
+template <int B1>
+struct Smem {
+  static constexpr int kSlots = ring_slots(B1);
+  static constexpr uint32_t kOffRing = 0;
+  static constexpr uint32_t kOffStg = kOffRing + kSlots * kSlotBytes;
+  static constexpr uint32_t kOffLsc = kOffStg + kStg * stg_bytes(B1);
+  static constexpr uint32_t kOffLid = kOffLsc + kCand * kQ * 4;
+  static constexpr uint32_t kOffNrm = kOffLid + kCand * kQ * 4;
+  static constexpr uint32_t kOffBar = kOffNrm + 2 * kR * 4;
+  static constexpr int kNumBars = 2 * kSlots + 8 + 2 * kStg;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kOffMisc + 16 + 1024;         // + alignment slack
+  static_assert(kBytes <= 232448, "shared memory of the scan exceeds 227 KB");
+};
 // misc words of the workspace: [0] n_max bits, [1] (n gamma)_max bits, [2] fallback count
 constexpr int kMiscWords = 64;
 
@@ -101,6 +111,20 @@ __device__ __forceinline__ uint32_t half_masks(uint32_t x) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, 0xBB99;" : "=r"(r) : "r"(x), "r"(0u));
   return r;
+}
+
+// r[j] for a run-time j without dynamic register indexing (a select tree).
+__device__ __forceinline__ uint32_t pick32(const uint32_t (&r)[32], int j) {
+  uint32_t a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a[k] = (j & 16) ? r[k + 16] : r[k];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) b[k] = (j & 8) ? a[k + 8] : a[k];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) c[k] = (j & 4) ? b[k + 4] : b[k];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) d[k] = (j & 2) ? c[k + 2] : c[k];
+  return (j & 1) ? d[1] : d[0];
 }
 
 // Bounded wait on an mbarrier phase; gives up early once another role of the
@@ -262,6 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                int* __restrict__ status) {
   constexpr int P = B1 + 1;               // planes per word column (stage 1 + signs)
   constexpr int W = 8 * P;                // words per record
+  using SM = Smem<B1>;
+  constexpr int kSlots = SM::kSlots;
+  constexpr uint32_t kOffRing = SM::kOffRing, kOffStg = SM::kOffStg, kOffLsc = SM::kOffLsc, kOffLid = SM::kOffLid,
+                     kOffNrm = SM::kOffNrm, kOffBar = SM::kOffBar, kOffMisc = SM::kOffMisc;
+  constexpr int kStgBytes = stg_bytes(B1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = su32(smem);
@@ -285,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(blk_full(s)));      // 4 decoder warps
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(blk_full(s)), "r"(kDecWarps));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(blk_empty(s)));     // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -298,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(nrm_rdy0 + 8u * b)); // 4 epilogue warps
     for (int b = 0; b < kStg; ++b) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(stg_full0 + 8u * b));  // loader: bytes + norms
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(stg_empty0 + 8u * b)); // 4 decoder warps
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(stg_empty0 + 8u * b), "r"(kDecWarps));
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -391,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             "l"(db + row0 * RB), "r"((uint32_t)(valid * RB)), "r"(bar)
             : "memory");
       }
-      uint32_t* sn = reinterpret_cast<uint32_t*>(stg + kR * 128);
+      uint32_t* sn = reinterpret_cast<uint32_t*>(stg + kR * RB);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int rr = 4 * lane + e;
@@ -411,7 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* Lsc = reinterpret_cast<float*>(smem + kOffLsc);
     int32_t* Lid = reinterpret_cast<int32_t*>(smem + kOffLid);
     float* nrm_s = reinterpret_cast<float*>(smem + kOffNrm);
-    float* scr = reinterpret_cast<float*>(smem + kOffScr) + (warp & 3) * 32 * 33;
     const uint32_t* nrm = reinterpret_cast<const uint32_t*>(db + norm_offset(cb, n_db));
     float thr = -INFINITY, inv_scale = 0.f;
     int filled = 0, mpos = 0;                    // entries in the list, slot of its minimum
@@ -490,14 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           cand |= (uint32_t)(32 * cbk + j < valid && sj > thr) << j;
         }
         if (__any_sync(0xffffffffu, cand != 0u)) {
-          // park the chunk's scores, then take the candidates one by one
-          // (a compact loop: the unsorted list's minimum is replaced and found again)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = __uint_as_float(r[j]);
+          // take the candidates one by one (a compact loop: the score is
+          // picked from the registers by a select tree, the unsorted list's
+          // minimum is replaced and found again)
           while (cand) {
             const int j = __ffs(cand) - 1;
             cand &= cand - 1;
-            const float sj = scr[lane * 33 + j];
+            const float sj = __uint_as_float(pick32(r, j));
             if (!(sj > thr)) continue;
             Lsc[mpos * kQ + ql] = sj;
             Lid[mpos * kQ + ql] = (int32_t)(row0 + 32 * cbk + j);
@@ -552,8 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ decoders
-    // thread r: row r of the tile, word columns 2 kb and 2 kb + 1 in round kb
-    const int r = tid - 256;
+    // thread (r, h): row r of the tile, word column 2 kb + h in round kb (8
+    // decoder warps), or both word columns (4 decoder warps)
+    constexpr int kHalves = kDecWarps == 8 ? 1 : 2;
+    const int r = (tid - 256) & 127, h0 = kDecWarps == 8 ? (tid - 256) >> 7 : 0;
     constexpr int L = 1 << B1;
     constexpr int RB = 32 * P;                   // record bytes
     // fp16 magnitudes of the upper half of the (symmetric) centroid table, in both halves
@@ -571,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* stg = smem + kOffStg + sidx * kStgBytes;
       const uint8_t* rec = stg + r * RB;
       // sigma slab value of this row: fp16(gamma kq), negative pattern in both halves
-      const uint32_t ne = reinterpret_cast<const uint32_t*>(stg + kR * 128)[r];
+      const uint32_t ne = reinterpret_cast<const uint32_t*>(stg + kR * RB)[r];
       const float gam = __high2float(*reinterpret_cast<const __half2*>(&ne));
       const uint32_t gk = f16_bits(gam * kq) | 0x8000u;
       const uint32_t neg_g = gk | (gk << 16);
@@ -589,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < kHalves; ++hh) {
+          const int half = h0 + hh;
           uint32_t w[P];
           const uint8_t* pw = rec + (2 * kb + half) * P * 4;
           if constexpr (P == 4) {
@@ -833,6 +863,7 @@ int64_t search_tc_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, in
 template <int B1>
 static cudaError_t scan_t(const TcPlan& pl, const Dev& cb, const uint8_t* db, int64_t n_db, int nq, uint8_t* ws,
                           int* status, cudaStream_t s) {
+  constexpr uint32_t kSmemBytes = Smem<B1>::kBytes;
   static cudaError_t configured = cudaFuncSetAttribute(k_stc_scan<B1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        (int)kSmemBytes);
   if (configured != cudaSuccess) return configured;
