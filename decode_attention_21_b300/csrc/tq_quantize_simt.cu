@@ -418,6 +418,12 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
       }
     }
     __syncthreads();
+    // Launched as a programmatic dependent, this CTA may have computed its
+    // rows while the kernel before it (a scoring kernel reading this cache)
+    // was still running: nothing is written, and no destination is looked up,
+    // before that kernel has completed (a no-op after the first row, and for
+    // an ordinary launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // a destination outside the cache is skipped and flagged
     const int64_t dst = append_row(dmap, row, cache_rows);
     if (dst == -2 && t == 0) atomicOr(status, kBadRow);
@@ -438,12 +444,24 @@ cudaError_t launch_quantize_simt(const Dev& cb, uint8_t* cache, int64_t cache_ro
                                  int64_t n, int d_in, const float* y, const float* norms, const AppendDst& dst,
                                  int* status, cudaStream_t s) {
   if (cb.mode == 0 && n <= 16384) {
+    // short batches (a decode step's appends): launched as a programmatic
+    // dependent, so the rows are rotated and coded while the previous kernel
+    // finishes; the stores wait for it (griddepcontrol.wait in the kernel)
     const int blocks = (int)(n < 148 * 16 ? n : 148 * 16);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(cb.d == 128 ? 512 : 1024);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (cb.d == 128)
-      k_quantize_row<128><<<blocks, 512, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst, status);
-    else
-      k_quantize_row<256><<<blocks, 1024, 0, s>>>(cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst, status);
-    return cudaGetLastError();
+      return cudaLaunchKernelEx(&cfg, k_quantize_row<128>, cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst,
+                                status);
+    return cudaLaunchKernelEx(&cfg, k_quantize_row<256>, cb, cache, cache_rows, x, x_dtype, n, d_in, y, norms, dst,
+                              status);
   }
   const int64_t blocks64 = (n + 7) / 8;
   const int blocks = (int)(blocks64 < 148 * 16 ? (blocks64 > 0 ? blocks64 : 1) : 148 * 16);

@@ -650,6 +650,11 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
         }
       }
     }
+    // The query fragments have been used (the first stage is scored), so
+    // the next call's query prep, which rewrites the workspace they came
+    // from, may start on SMs this grid frees; it waits for this grid before
+    // its own dependent reads any cache row or writes any output.
+    if (st == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // every warp is done with this ring slot: refill it with stage st + kRing
     if (st + kRing < nst) {
       __syncthreads();
@@ -1108,6 +1113,11 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
       }
     }
     if (st % kPvFlushStages == kPvFlushStages - 1) tot.flush(acc);
+    // The query fragments have been used (the first stage is scored), so
+    // the next call's query prep, which rewrites the workspace they came
+    // from, may start on SMs this grid frees; it waits for this grid before
+    // its own dependent reads any cache row or writes any output.
+    if (st == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // every warp is done with this ring slot: refill it with stage st + kRing
     if (st + kRing < nst) {
       __syncthreads();
