@@ -86,6 +86,7 @@ bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t c
 }
 
 constexpr uint32_t kOddMaskHost[8] = {1u, 2u, 4u, 7u, 8u, 11u, 13u, 14u};
+constexpr long long kDefaultWaitPolls = 1ll << 26;   // polls of a bounded device-side wait
 constexpr int kLogitsCtas = 148 * 4;   // resident CTAs of the logits kernel
 // Resident CTAs of the attention kernel (one wave): 4 per SM, 3 for keys
 // with four or more stage-1 virtual planes or extra-bit words (more
@@ -247,6 +248,7 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   dv.W = (d / 32) * dv.P + D.extra / 32;
   dv.nb = D.kind == TQ_KIND_PROD ? 4 : 2;
   dv.qjl_const = (float)(std::sqrt(M_PI / 2.0) / d);
+  dv.first_wait = kDefaultWaitPolls;
   const int L = 1 << b1;
 
   if (D.mode == TQ_MODE_SCALAR) {
@@ -429,6 +431,13 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
     cb->tc_ready = good;
   }
   *out = cb;
+  return ok();
+}
+
+tq_status tq_set_first_wait_limit(tq_codebook* cb, int64_t polls) {
+  if (!cb) return fail(TQ_EINVAL, "tq_set_first_wait_limit: NULL codebook");
+  if (polls < -1) return fail(TQ_EINVAL, "tq_set_first_wait_limit: polls must be >= -1");
+  cb->dev.first_wait = polls < 0 ? kDefaultWaitPolls : (long long)polls;
   return ok();
 }
 

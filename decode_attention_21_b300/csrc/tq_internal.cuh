@@ -26,6 +26,9 @@ struct Dev {
   int nvx;
   float vcoef_x[kMaxL];
   float qjl_const;        // sqrt(pi/2) / m
+  // polls of the first bounded wait of every launch (the others use the
+  // full limit); lowered only by tq_set_first_wait_limit, for tests
+  long long first_wait;
   // polar mode, per level l = 1..D (index l): boundary and centroid (cos, sin)
   float pb_cos[kMaxLevels][kMaxL], pb_sin[kMaxLevels][kMaxL];
   float pc_cos[kMaxLevels][kMaxL], pc_sin[kMaxLevels][kMaxL];

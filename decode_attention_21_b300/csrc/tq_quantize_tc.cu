@@ -70,8 +70,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Bounded wait for the phase with parity `parity` to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kSpinLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit = kSpinLimit) {
+  for (long long i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
@@ -195,7 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sbase + kOffX + kb * kBlockBytes, &tm_x, 64 * kb, (int)(first * kRows), bar_full0);
   }
   if (first < ntiles) pending_stage = 0;
-  if (first < ntiles) ok = __syncthreads_and(mbar_wait(bar_const, 0)) != 0;
+  bool const_pending = first < ntiles;   // Pi / S loads not yet waited for
+  if (first < ntiles) ok = __syncthreads_and(mbar_wait(bar_const, 0, cb.first_wait)) != 0;
+  if (ok) const_pending = false;
+  // commits of the two MMA groups not yet waited for (drained on a timeout)
+  bool pend1 = false, pend2 = false;
 
   int it = 0;
   for (int64_t tile = first; tile < ntiles && ok; tile += gridDim.x, ++it) {
@@ -224,10 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tm_y, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffPiLo + kb * kBlockBytes + 32 * ks), 1);
       mma_commit(bar_mma1);
     }
+    pend1 = true;
     if (!__syncthreads_and(mbar_wait(bar_mma1, it & 1))) {
       ok = false;
       break;
     }
+    pend1 = false;
     fence_after();
     // ---- epilogue 1: norm, codes, residual
     float v[32];
@@ -310,10 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                      sw128_desc(sbase + kOffS + kb * kBlockBytes + 32 * ks), 1);
         mma_commit(bar_mma2);
       }
+      pend2 = true;
       if (!__syncthreads_and(mbar_wait(bar_mma2, it & 1))) {
         ok = false;
         break;
       }
+      pend2 = false;
       fence_after();
       tmem_ld32(tm_z + ((uint32_t)(32 * q) << 16) + 32 * cg, v);
 #pragma unroll
@@ -351,9 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok) {
     if (tid == 0) atomicOr(status, 1);
     // let our own copies and MMAs drain (bounded waits) before freeing TMEM
+    if (const_pending) mbar_wait(bar_const, 0);
     if (pending_stage >= 0) mbar_wait(bar_full0 + 8 * pending_stage, ((it + 1) >> 1) & 1);
-    mbar_wait(bar_mma1, it & 1);
-    if (prod) mbar_wait(bar_mma2, it & 1);
+    if (pend1) mbar_wait(bar_mma1, it & 1);
+    if (pend2) mbar_wait(bar_mma2, it & 1);
   }
   fence_before();
   __syncthreads();

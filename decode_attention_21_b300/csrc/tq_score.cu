@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   };
   for (int st = 0; st < nst; ++st) {
     const int slot = st % kRing;
-    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1)))) {
+    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1), st == 0 ? cb.first_wait : kWaitLimit))) {
       ok = false;
       pending_from = st;
       break;
@@ -980,7 +980,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
   int pending_from = 0;
   for (int st = 0; st < nst; ++st) {
     const int slot = st % kRing;
-    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1)))) {
+    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1), st == 0 ? kcb.first_wait : kWaitLimit))) {
       ok = false;
       pending_from = st;
       break;

@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   int pending_from = 0;
   for (int st = 0; st < nst; ++st) {
     const int slot = st % kRing;
-    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1)))) {
+    if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1), st == 0 ? kcb.first_wait : kWaitLimit))) {
       ok = false;
       pending_from = st;
       break;

@@ -69,8 +69,8 @@ __device__ __forceinline__ int64_t tile_row(const RowMap& map, int b, int kvh, i
   return ((int64_t)pg * Hkv + kvh) * map.page + off;
 }
 
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i) {
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, long long limit = kWaitLimit) {
+  for (long long i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"

@@ -306,6 +306,18 @@ tq_status tq_search_fallbacks(const tq_codebook* cb, const void* workspace, int3
  * TQ_OK otherwise.  Not a hot call.                                          */
 tq_status tq_check_device(const tq_codebook* cb);
 
+/* Test use: from the next launch on, the first bounded device-side wait of
+ * every kernel that uses this codebook (the first bulk-copy stage of the
+ * logits and attention kernels, the Pi / S loads of the tensor-core
+ * quantize kernel) gives up after `polls` polls (0: at once; -1: back to the
+ * default of 2^26).  A kernel that gives up records TQ_ETIMEOUT for
+ * tq_check_device, waits (with the full limit) for the copies and tensor-core
+ * operations it has already issued, frees its tensor memory and returns; its
+ * outputs are then incomplete.  It lets a test drive the timeout path without
+ * faulting or hanging anything.  Not thread-safe against calls running on
+ * this codebook.                                                             */
+tq_status tq_set_first_wait_limit(tq_codebook* cb, int64_t polls);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* tq_last_error(void);
 
