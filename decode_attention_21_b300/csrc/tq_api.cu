@@ -539,7 +539,9 @@ size_t tq_logits_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_
 static tq_status check_heads(const char* what, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || capacity < 0) return fail(TQ_EINVAL, "%s: bad sizes", what);
   if (Hq % Hkv) return fail(TQ_EINVAL, "%s: Hq = %d is not a multiple of Hkv = %d", what, Hq, Hkv);
-  if (Hq / Hkv > 4) return fail(TQ_EUNSUPPORTED, "%s: GQA groups larger than 4 are not implemented", what);
+  const int G = Hq / Hkv;
+  if (G > 4 && (G % 4 != 0 || G > 16))
+    return fail(TQ_EUNSUPPORTED, "%s: a GQA group of %d query heads is not implemented (1..4, 8, 12 or 16)", what, G);
   if (B > 65535 || Hkv > 65535 || Hq > 65535) return fail(TQ_EINVAL, "%s: too many heads or sequences", what);
   return TQ_OK;
 }
@@ -565,19 +567,32 @@ static tq_status logits_common(const char* what, const tq_codebook* kcb, const v
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   int nchunks, tpc;
   chunking(B, Hkv, capacity, kLogitsCtas, &nchunks, &tpc);
-  if (kcb->dev.mode == TQ_MODE_POLAR) {
-    if ((st = launched(what, tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
-    return launched(what, tq::launch_logits_polar(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
-                                                  capacity, rows, map, seq_lens, prep, logits, nchunks, tpc,
+  // The kernels score 4 query heads per kv head (fp16 hi / lo of each in
+  // the 8 tensor-core columns); a larger group (a multiple of 4) is scored
+  // 4 heads at a time: with Hq and Hkv unchanged, queries and logits offset
+  // by 4 g heads address heads 4 g .. 4 g + 3 of every kv head.
+  const int ngroups = (Hq / Hkv + 3) / 4;
+  for (int g = 0; g < ngroups; ++g) {
+    const float* qg = q + (size_t)4 * g * kcb->dev.d;
+    float* lg = logits + (size_t)4 * g * capacity;
+    if (kcb->dev.mode == TQ_MODE_POLAR) {
+      if ((st = launched(what, tq::launch_prep_polar(kcb->dev, qg, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+      st = launched(what, tq::launch_logits_polar(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                  capacity, rows, map, seq_lens, prep, lg, nchunks, tpc,
                                                   kcb->d_status, s));
+    } else {
+      if ((st = launched(what, tq::launch_prep(kcb->dev, qg, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+      if (capacity % 16 == 0)
+        st = launched(what, tq::launch_logits_staged(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
+                                                     capacity, rows, map, seq_lens, prep, lg, nchunks, tpc,
+                                                     kcb->d_status, s));
+      else
+        st = launched(what, tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
+                                              rows, seq_lens, prep, lg, nchunks, tpc, s));
+    }
+    if (st != TQ_OK) return st;
   }
-  if ((st = launched(what, tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
-  if (capacity % 16 == 0)
-    return launched(what, tq::launch_logits_staged(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
-                                                   capacity, rows, map, seq_lens, prep, logits, nchunks, tpc,
-                                                   kcb->d_status, s));
-  return launched(what, tq::launch_logits(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv, capacity,
-                                          rows, seq_lens, prep, logits, nchunks, tpc, s));
+  return ok();
 }
 
 tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
@@ -644,21 +659,25 @@ tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* 
 // chunk, warp).  The launch and every workspace bound use this one helper;
 // without a value codebook it gives the largest split any value codebook
 // can get (a value codebook only ever lowers the resident-CTA target).
-static int64_t attn_workspace_bytes(const tq_codebook* kcb, const tq_codebook* vcb, int32_t B, int32_t Hkv,
-                                    int64_t capacity, int* nchunks_out = nullptr, int* tpc_out = nullptr) {
+// Groups of more than 4 query heads per kv head keep one partial region per
+// 4-head group (group_stride floats apart).
+static int64_t attn_workspace_bytes(const tq_codebook* kcb, const tq_codebook* vcb, int32_t B, int32_t Hq,
+                                    int32_t Hkv, int64_t capacity, int* nchunks_out = nullptr,
+                                    int* tpc_out = nullptr, int64_t* group_stride_out = nullptr) {
   int nchunks, tpc;
   chunking(B, Hkv, capacity, attn_ctas(kcb, vcb), &nchunks, &tpc);
   if (nchunks_out) *nchunks_out = nchunks;
   if (tpc_out) *tpc_out = tpc;
+  const int64_t ngroups = (Hq / std::max(Hkv, 1) + 3) / 4;
   const int64_t prep = tq::align256((int64_t)B * Hkv * tq::prep_block_bytes(kcb->dev.d));
-  const int64_t parts = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d) * 4;
-  return prep + parts;
+  const int64_t stride = (int64_t)B * Hkv * nchunks * tq::kAttnWarps * tq::partial_floats(kcb->dev.d);
+  if (group_stride_out) *group_stride_out = stride;
+  return prep + std::max<int64_t>(1, ngroups) * stride * 4;
 }
 
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity) {
-  if (!kcb || B <= 0 || Hkv <= 0 || capacity < 0) return 0;
-  (void)Hq;
-  return (size_t)attn_workspace_bytes(kcb, nullptr, B, Hkv, capacity);
+  if (!kcb || B <= 0 || Hkv <= 0 || Hq <= 0 || capacity < 0) return 0;
+  return (size_t)attn_workspace_bytes(kcb, nullptr, B, Hq, Hkv, capacity);
 }
 
 static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache,
@@ -698,7 +717,8 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
     return fail(TQ_EINVAL, "%s: device pointers must be 16-byte aligned", what);
   if (!std::isfinite(scale)) return fail(TQ_EINVAL, "%s: scale must be finite", what);
   int nchunks, tpc;
-  if (ws_bytes < (size_t)attn_workspace_bytes(kcb, vcb, B, Hkv, capacity, &nchunks, &tpc))
+  int64_t gstride;
+  if (ws_bytes < (size_t)attn_workspace_bytes(kcb, vcb, B, Hq, Hkv, capacity, &nchunks, &tpc, &gstride))
     return fail(TQ_ENOMEM, "%s: workspace too small", what);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
@@ -707,38 +727,44 @@ static tq_status attn_common(const char* what, const tq_codebook* kcb, const tq_
   if (kcb->dev.mode != vcb->dev.mode)
     return fail(TQ_EUNSUPPORTED, "%s: keys and values must use the same stage-1 mode", what);
   const float sl2 = scale * 1.4426950408889634f;
-  if (kcb->dev.mode == TQ_MODE_POLAR) {
-    if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
-      return st;
-    if (capacity % 16 == 0 || map.table)
-      st = launched("tq_decode_attention",
-                    tq::launch_attn_polar_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                                 static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
-                                                 map, seq_lens, prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
-    else
-      st = launched("tq_decode_attention",
-                    tq::launch_attn_polar(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                          static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens,
-                                          prep, sl2, parts, nchunks, tpc, s));
+  // 4 query heads per kv head per launch (see logits_common); head group g
+  // writes its partials gstride floats after group g - 1's
+  const int ngroups = (Hq / Hkv + 3) / 4;
+  for (int g = 0; g < ngroups; ++g) {
+    const float* qg = q + (size_t)4 * g * kcb->dev.d;
+    float* pg = parts + (size_t)g * gstride;
+    if (kcb->dev.mode == TQ_MODE_POLAR) {
+      if ((st = launched("tq_decode_attention/prep", tq::launch_prep_polar(kcb->dev, qg, B, Hq, Hkv, prep, s))) !=
+          TQ_OK)
+        return st;
+      if (capacity % 16 == 0 || map.table)
+        st = launched("tq_decode_attention",
+                      tq::launch_attn_polar_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                                   static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
+                                                   map, seq_lens, prep, sl2, pg, nchunks, tpc, kcb->d_status, s));
+      else
+        st = launched("tq_decode_attention",
+                      tq::launch_attn_polar(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                            static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows,
+                                            seq_lens, prep, sl2, pg, nchunks, tpc, s));
+    } else {
+      if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, qg, B, Hq, Hkv, prep, s))) != TQ_OK)
+        return st;
+      if (capacity % 16 == 0 || map.table)
+        st = launched("tq_decode_attention",
+                      tq::launch_attn_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                             static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, map,
+                                             seq_lens, prep, sl2, pg, nchunks, tpc, kcb->d_status, s));
+      else
+        st = launched("tq_decode_attention",
+                      tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
+                                      static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens,
+                                      prep, sl2, pg, nchunks, tpc, s));
+    }
     if (st != TQ_OK) return st;
-    return launched("tq_decode_attention/merge",
-                    tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
   }
-  if ((st = launched("tq_decode_attention/prep", tq::launch_prep(kcb->dev, q, B, Hq, Hkv, prep, s))) != TQ_OK)
-    return st;
-  if (capacity % 16 == 0 || map.table)
-    st = launched("tq_decode_attention",
-                  tq::launch_attn_staged(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                         static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, map,
-                                         seq_lens, prep, sl2, parts, nchunks, tpc, kcb->d_status, s));
-  else
-    st = launched("tq_decode_attention",
-                  tq::launch_attn(kcb->dev, vcb->dev, static_cast<const uint8_t*>(kcache),
-                                  static_cast<const uint8_t*>(vcache), B, Hq, Hkv, capacity, rows, seq_lens, prep,
-                                  sl2, parts, nchunks, tpc, s));
-  if (st != TQ_OK) return st;
   return launched("tq_decode_attention/merge",
-                  tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, out, s));
+                  tq::launch_attn_merge(vcb->dev, parts, B, Hq, Hkv, nchunks * tq::kAttnWarps, gstride, out, s));
 }
 
 tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, const void* kcache, const void* vcache,

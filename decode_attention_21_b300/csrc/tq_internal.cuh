@@ -189,7 +189,8 @@ bool search_tc_applies(const Dev& cb, int k);
 int64_t search_tc_workspace_bytes(const Dev& cb, int64_t n_db, int nq, int k, int sms);
 cudaError_t launch_search_tc(const Dev& cb, const uint8_t* db, int64_t n_db, const float* q, int nq, int d_in, int k,
                              int32_t* ids, float* scores, uint8_t* ws, int sms, int* status, cudaStream_t s);
-cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts, float* out,
-                              cudaStream_t s);
+// group_stride: floats between the partials of consecutive 4-head groups.
+cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts,
+                              int64_t group_stride, float* out, cudaStream_t s);
 
 }  // namespace tq

@@ -1160,15 +1160,18 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
 // M = max m_p, o_rot = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,
 // out = Pi_v^T o_rot.  The maximum, the weights and L are computed by the
 // whole CTA (parts strided over threads); thread i then sums coordinate i.
+// Groups larger than 4 heads per kv head are scored 4 heads at a time; the
+// partials of head group g start at partials + g * group_stride floats.
 constexpr int kMergeMaxParts = 4096;
 __global__ void __launch_bounds__(128) k_attn_merge(const Dev vcb, const float* __restrict__ partials, int Hq, int Hkv,
-                                                    int nparts, float* __restrict__ out) {
+                                                    int nparts, int64_t group_stride, float* __restrict__ out) {
   const int h = blockIdx.x, b = blockIdx.y;
   const int G = Hq / Hkv, kvh = h / G, slot = h % G;
   constexpr int d = 128;
   constexpr int64_t PF = 4 * (2 + d);        // partial_floats(d)
   __shared__ float so[d], red[4], wts[kMergeMaxParts];
-  const float* base = partials + ((size_t)b * Hkv + kvh) * nparts * PF + slot * (2 + d);
+  const float* base =
+      partials + (slot / 4) * group_stride + ((size_t)b * Hkv + kvh) * nparts * PF + (slot % 4) * (2 + d);
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
   const bool cache_w = nparts <= kMergeMaxParts;
   float mloc = -INFINITY;
@@ -1441,9 +1444,9 @@ cudaError_t launch_attn(const Dev& kcb, const Dev& vcb, const uint8_t* kc, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts, float* out,
-                              cudaStream_t s) {
-  k_attn_merge<<<dim3(Hq, B), 128, 0, s>>>(vcb, partials, Hq, Hkv, nparts, out);
+cudaError_t launch_attn_merge(const Dev& vcb, const float* partials, int B, int Hq, int Hkv, int nparts,
+                              int64_t group_stride, float* out, cudaStream_t s) {
+  k_attn_merge<<<dim3(Hq, B), 128, 0, s>>>(vcb, partials, Hq, Hkv, nparts, group_stride, out);
   return cudaGetLastError();
 }
 

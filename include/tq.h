@@ -140,8 +140,9 @@ size_t tq_logits_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq, int32_
  * for t < seq_lens[b]; entries t >= seq_lens[b] are left untouched.
  *   kcache     device, rows (b*Hkv + kvh)*capacity + t, PROD kind
  *   seq_lens   device int32[B], each <= capacity
- *   q          device fp32 [B, Hq, d] (Hq = G*Hkv, G <= 4; head h uses kv
- *              head h / G)
+ *   q          device fp32 [B, Hq, d] (Hq = G*Hkv with G = 1..4, 8, 12 or
+ *              16; head h uses kv head h / G; groups above 4 are scored four
+ *              heads per launch)
  *   logits     device fp32 [B, Hq, capacity]
  *   workspace  device, >= tq_logits_workspace(kcb, B, Hq, Hkv) bytes        */
 tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq,
@@ -164,7 +165,8 @@ tq_status tq_logits_dense(const void* keys, int32_t key_dtype, int32_t d, int32_
                           int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q,
                           float* logits, void* stream);
 
-/* Workspace bytes of tq_decode_attention. */
+/* Workspace bytes of tq_decode_attention (the query prep, and split-KV
+ * partials per 4-head group of each kv head). */
 size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t Hq,
                                      int32_t Hkv, int64_t capacity);
 
@@ -184,7 +186,8 @@ size_t tq_decode_attention_workspace(const tq_codebook* kcb, int32_t B, int32_t 
  * at 1-4 bits, in scalar or polar mode; in scalar mode and with a capacity
  * that is a multiple of 16 also MSE-only keys or 2.5 / 3.5-bit keys (extra
  * bits) with 3- or 4-bit values, and 2.5 / 3.5-bit values (extra = d/4, 2 or
- * 3 bits) with keys that have the QJL term.  Other pairs: TQ_EUNSUPPORTED. */
+ * 3 bits) with keys that have the QJL term.  Other pairs: TQ_EUNSUPPORTED.
+ * Heads as for tq_logits (G = 1..4, 8, 12 or 16).                          */
 tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb,
                               const void* kcache, const void* vcache, int32_t B, int32_t Hq,
                               int32_t Hkv, int64_t capacity, const int32_t* seq_lens,

@@ -137,7 +137,9 @@ def rowwise_ok(got, ref, tol=1e-3, med=1e-4):
 @pytest.mark.parametrize("mode", ["scalar", "polar"])
 @pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 8, 2, 4096, [4096]), (2, 4, 1, 1000, [1000, 1]),
-                                               (3, 6, 3, 333, [333, 17, 0]), (1, 2, 2, 64, [49])])
+                                               (3, 6, 3, 333, [333, 17, 0]), (1, 2, 2, 64, [49]),
+                                               (2, 16, 2, 1000, [1000, 513]), (1, 12, 1, 336, [336]),
+                                               (1, 32, 2, 256, [250])])
 def test_logits_parity(bits, B, Hq, Hkv, cap, lens, mode):
     ocb, gcb = pair(128, bits, mode=mode)
     rows = B * Hkv * cap
@@ -157,6 +159,28 @@ def test_logits_parity(bits, B, Hq, Hkv, cap, lens, mode):
         assert np.all(np.isnan(got[b, :, L:]))
         if L:
             rowwise_ok(got[b, :, :L], ref[b, :, :L])
+
+
+@pytest.mark.parametrize("mode", ["scalar", "polar"])
+def test_logits_tiny_estimator_config_all_pairs(mode):
+    """The tiny estimator check as the configuration states it: 4096 fp32 keys
+    ~N(0, I) with 4 outlier channels x20, 8 fp32 queries, b = 3 (2-bit stage 1
+    + 1-bit QJL, m = 128), logits for all 8 x 4096 pairs: one kv head shared by
+    the 8 query heads (a group of 8, scored 4 heads per launch)."""
+    ocb, gcb = pair(128, 3, mode=mode)
+    T = 4096
+    x = wl.gaussian_outlier_keys(T, 128)
+    code, img = oracle_cache(ocb, T, x.astype(np.float64))
+    q = wl.queries((1, 8, 128), name="tiny_q")
+    ref = estimate.estimate(ocb, q[0].astype(np.float64), code)           # [8, 4096]: every pair
+    ws = torch.empty(tq.tq_logits_workspace(gcb, 1, 8, 1), dtype=torch.uint8, device="cuda")
+    out = torch.full((1, 8, T), float("nan"), device="cuda")
+    tq.tq_logits(gcb, torch.from_numpy(img).cuda(), 1, 8, 1, T, torch.tensor([T], dtype=torch.int32, device="cuda"),
+                 torch.from_numpy(q).cuda(), out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()[0]
+    assert np.all(np.isfinite(got))
+    rowwise_ok(got, ref)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
@@ -247,7 +271,8 @@ def test_logits_long_context_every_position(bits):
 @pytest.mark.parametrize("kb,vb,mode", [(3, 3, "scalar"), (4, 3, "scalar"), (2, 2, "scalar"), (3, 4, "scalar"),
                                         (3, 1, "scalar"), (3, 3, "polar"), (4, 2, "polar"), (2, 4, "polar")])
 @pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 300, [300, 1, 0]),
-                                               (1, 4, 4, 5000, [4999])])
+                                               (1, 4, 4, 5000, [4999]), (2, 16, 2, 1024, [1024, 700]),
+                                               (1, 8, 1, 300, [299])])
 def test_attention_parity(kb, vb, mode, B, Hq, Hkv, cap, lens):
     okc, gkc = pair(128, kb, "prod", mode=mode)
     ovc, gvc = pair(128, vb, "mse", mode=mode, seed_pi=1)
@@ -429,7 +454,10 @@ def test_invalid_arguments_return_status_without_launch():
     assert e.value.status == tq.TQ_ENOMEM
     ws = torch.empty(tq.tq_logits_workspace(gcb, 1, 4, 1), dtype=torch.uint8, device="cuda")
     with pytest.raises(tq.TqError) as e:
-        tq.tq_logits(gcb, kc, 1, 12, 1, 64, sl, q, out, ws)      # G = 12 > 4
+        tq.tq_logits(gcb, kc, 1, 6, 1, 64, sl, q, out, ws)       # G = 6: above 4, not a multiple of 4
+    assert e.value.status == tq.TQ_EUNSUPPORTED
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_logits(gcb, kc, 1, 20, 1, 64, sl, q, out, ws)      # G = 20 > 16
     assert e.value.status == tq.TQ_EUNSUPPORTED
     with pytest.raises(tq.TqError) as e:
         tq.tq_logits(gcb, kc, 1, 6, 4, 64, sl, q, out, ws)       # Hq not a multiple of Hkv
