@@ -12,8 +12,13 @@ split of the context over CTAs).
 * quantize, 2^20 bf16 rows in one call (the persistent tcgen05 kernel, one CTA
   per SM, ~55 tiles each): a seeded sample of 8192 rows (first and last
   included) against the oracle, with the bar of the smaller tensor-core tests;
-* search, 10^6 database rows, 10^4 queries, top-10: 16 sampled queries
-  against the oracle's top-k over all rows.
+* the same attention with recursive-polar keys and values (the benchmark's
+  polar line), by the same repeated-rows argument;
+* search, 10^6 database rows, 10^4 queries, top-10, b = 2 and 4: 16 sampled
+  queries against the oracle's top-k over all rows;
+* the search database's own compression: 10^6 fp32 rows, d_in = 200 zero-
+  padded to 256, b = 2 and 4, in one call: 8192 sampled rows against the
+  oracle.
 
 Bars as in test_gpu_parity.py.
 """
@@ -30,9 +35,10 @@ from oracle import estimate, layout, quant
 pytestmark = pytest.mark.gpu
 
 
-def pair(bits, kind="prod", seed_pi=1, seed_s=2):
-    ocb = quant.Codebook(128, bits, kind=kind, seed_pi=seed_pi, seed_s=seed_s)
-    gcb = tq.Codebook(128, bits, tq.KIND_PROD if kind == "prod" else tq.KIND_MSE, tq.MODE_SCALAR, seed_pi, seed_s)
+def pair(bits, kind="prod", seed_pi=1, seed_s=2, mode="scalar", d=128):
+    ocb = quant.Codebook(d, bits, kind=kind, seed_pi=seed_pi, seed_s=seed_s, mode=mode)
+    gcb = tq.Codebook(d, bits, tq.KIND_PROD if kind == "prod" else tq.KIND_MSE,
+                      tq.MODE_POLAR if mode == "polar" else tq.MODE_SCALAR, seed_pi, seed_s)
     return ocb, gcb
 
 
@@ -78,10 +84,11 @@ def replicate(ocb, gcb, img_u, rows_u, rows, src):
     return full
 
 
-def test_attention_full_size_repeated_rows():
+@pytest.mark.parametrize("mode", ["scalar", "polar"])
+def test_attention_full_size_repeated_rows(mode):
     B, Hq, Hkv, T, U = 8, 32, 8, 131072, 4096
-    okc, gkc = pair(3)
-    ovc, gvc = pair(3, "mse", seed_pi=1)
+    okc, gkc = pair(3, mode=mode)
+    ovc, gvc = pair(3, "mse", seed_pi=1, mode=mode)
     units = B * Hkv
     K = np.concatenate([wl.llama_kv_slice(0, u, 0, U, which="keys") for u in range(units)])
     V = np.concatenate([wl.llama_kv_slice(0, u, 0, U, which="values") for u in range(units)])
@@ -134,15 +141,16 @@ def test_quantize_full_size_sampled(bits):
     assert np.allclose(got["g16"].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
 
 
-def test_search_full_size_sampled_queries():
-    """Top-10 over 10^6 rows (d 200 -> 256, b = 2) for all 10^4 queries, as
-    the benchmark runs it, on the oracle's own packed database; 16 sampled
+@pytest.mark.parametrize("bits", [2, 4])
+def test_search_full_size_sampled_queries(bits):
+    """Top-10 over 10^6 rows (d 200 -> 256) for all 10^4 queries, as the
+    benchmark runs it, on the oracle's own packed database; 16 sampled
     queries (first and last included) against the oracle's blocked top-k:
     identical ids except swaps among near-tied scores, scores equal to the
-    estimator of the returned rows."""
+    estimator of the returned rows; no query needs the exact re-scan."""
     n_db, nq, k, blk = 1000000, 10000, 10, 1 << 17
-    ocb = quant.Codebook(256, 2, kind="prod")
-    gcb = tq.Codebook(256, 2, tq.KIND_PROD, tq.MODE_SCALAR)
+    ocb = quant.Codebook(256, bits, kind="prod")
+    gcb = tq.Codebook(256, bits, tq.KIND_PROD, tq.MODE_SCALAR)
     x = wl.search_rows(n_db, "db")
     q = wl.search_rows(nq, "search_q")
     keep = ("idx", "sigma", "n16", "g16")
@@ -159,6 +167,8 @@ def test_search_full_size_sampled_queries():
     sc = torch.full((nq, k), float("nan"), device="cuda")
     tq.tq_search(gcb, img, n_db, torch.from_numpy(q).cuda(), nq, q.shape[1], k, ids, sc, ws)
     torch.cuda.synchronize()
+    assert tq.tq_search_fallbacks(gcb, ws, k) == 0
+    tq.tq_check_device(gcb)
     gi, gs = ids.cpu().numpy(), sc.cpu().numpy()
     rng = np.random.default_rng(5)
     sample = np.unique(np.concatenate([[0, nq - 1], rng.choice(nq, 14, replace=False)]))
@@ -188,3 +198,34 @@ def test_search_full_size_sampled_queries():
         for j in np.nonzero(g_ids != best_i[r])[0]:
             assert abs(full_g[r, j] - best_s[r, j]) <= tol
         assert np.all(np.diff(gs[qi]) <= tol)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_search_database_quantize_full_size_sampled(bits):
+    """The search database compressed as the benchmark does it: 10^6 fp32
+    rows of the Gaussian mixture, d_in = 200 zero-padded to d = 256, in one
+    tq_quantize call; 8192 sampled rows (first and last included) against
+    the oracle's encoding of the same rows."""
+    N, d_in = 1000000, 200
+    ocb, gcb = pair(bits, d=256)
+    x = wl.search_rows(N, "db")
+    cache = torch.zeros(tq.cache_bytes(gcb, N), dtype=torch.uint8, device="cuda")
+    tq.tq_quantize(gcb, cache, N, torch.from_numpy(x).cuda(), N, d_in)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gcb)
+    rng = np.random.default_rng(100 + bits)
+    sample = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 8190, replace=False)]))
+    code = quant.quantize(ocb, x[sample].astype(np.float64))
+    got = layout.read_cache(ocb, N, cache.cpu().numpy(), row_ids=sample)
+    code_bits = got["idx"] != code["idx"]
+    flips = code_bits.sum() + (got["sigma"] != code["sigma"]).sum()
+    nbits = code["idx"].size * ocb.b1 + code["sigma"].size
+    assert flips <= 1e-3 * nbits, flips / nbits
+    if code_bits.any():
+        y, _ = quant.rotate(ocb, x[sample].astype(np.float64))
+        t = ocb.t.astype(np.float64)
+        dist = np.min(np.abs(y[code_bits][:, None] - t[None, :]), axis=1)
+        assert np.all(dist < 1e-4 / math.sqrt(256))
+    n_ref = np.linalg.norm(x[sample].astype(np.float64), axis=1)
+    assert np.allclose(got["n16"].astype(np.float64), n_ref, rtol=1e-3)
+    assert np.allclose(got["g16"].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
