@@ -664,7 +664,7 @@ def run_search(args, dist, rank, steps):
     queries from a Gaussian mixture; recall@1@k against exact fp32 scores."""
     from decode_attention_21_b300 import tq
     from decode_attention_21_b300 import workloads as wl
-    n_db, nq, d_in, d, k = 1000000, 10000, 200, 256, 10
+    n_db, nq, d_in, d, k = 1000000, args.search_nq, 200, 256, 10
     x = torch.from_numpy(wl.search_rows(n_db, "db")).cuda()
     q = torch.from_numpy(wl.search_rows(nq, "search_q")).cuda()
     # exact fp32 top-1 (reference for recall), in blocks
@@ -676,7 +676,7 @@ def run_search(args, dist, rank, steps):
     torch.backends.cuda.matmul.allow_tf32 = prev
     pk = peaks()
     out = {}
-    for bits in (2, 4):
+    for bits in [int(b) for b in args.search_bits.split(",")]:
         cb = tq.Codebook(d, bits, tq.KIND_PROD)
         db = torch.empty(tq.cache_bytes(cb, n_db), dtype=torch.uint8, device="cuda")
         tq.tq_quantize(cb, db, n_db, x, n_db, d_in)
@@ -707,7 +707,7 @@ def run_search(args, dist, rank, steps):
                                         "peak_note": "measured bf16 cuBLAS peak; the scan runs fp16 operands (same nominal rate)",
                                         "algorithmic_flop_per_call": flops_alg,
                                         "executed_mma_flop_per_call": flops_exec}}
-    return {"workload": "top-10 search, 10^6 rows d 200->256, 10^4 queries, b = 2 and 4", **out}
+    return {"workload": f"top-10 search, 10^6 rows d 200->256, {nq} queries, b = {args.search_bits}", **out}
 
 
 # ------------------------------------------------------------ reference arm
@@ -746,6 +746,8 @@ def main():
     ap.add_argument("--attn-batch", type=int, default=ATTN["B"],
                     help="sequences in the attention workload (smaller batches for profiling)")
     ap.add_argument("--attn-modes", default="scalar,polar", help="comma list of stage-1 modes for attention")
+    ap.add_argument("--search-nq", type=int, default=10000, help="queries of the search workload (smaller for profiling)")
+    ap.add_argument("--search-bits", default="2,4", help="comma list of database bit widths for search")
     args = ap.parse_args()
     world, rank, local = dist_env()
     args.world = world
