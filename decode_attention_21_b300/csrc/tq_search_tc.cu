@@ -25,7 +25,7 @@
 //   * k_stc_prep: q' and q'' in fp32 (kept for the re-ranking), the fp16
 //     operand words of each 128-query block, |q'|_1, |q''|_1, the scale 2^e_q;
 //   * k_stc_dbmax: n_max and (n gamma)_max of the database;
-//   * k_stc_scan: 8 decoder warps turn the packed records of each 128-row tile
+//   * k_stc_scan: 4 decoder warps turn the packed records of each 128-row tile
 //     into the B operand (one 16 KB K-block per ring slot, 128-byte swizzled,
 //     K-major), one thread issues tcgen05.mma M128 N128 K16 into one of two
 //     TMEM accumulators, and 4 epilogue warps (one query per thread) read the
