@@ -24,5 +24,6 @@ Modules:
     polar      recursive-polar stage 1
     layout     packed bit-plane cache byte layout (pack / unpack)
     estimate   inner-product estimator, logits, decode attention, top-k search
+    split      outlier-channel split: independent instances per channel group
 """
-from . import rng, codebook, rotation, quant, polar, layout, estimate  # noqa: F401
+from . import rng, codebook, rotation, quant, polar, layout, estimate, split  # noqa: F401

@@ -36,6 +36,10 @@ def prep_query(cb, q):
 
 def estimate(cb, q, code, rows=None, use_fp16_norms=True, qjl=True):
     """est(q, x) for query rows q [Q, d_in] against coded rows -> [Q, N]."""
+    if getattr(cb, "split", False):
+        # outlier-channel split: the sum of the channel groups' own estimates
+        from .split import estimate as split_estimate
+        return split_estimate(cb, q, code, rows, use_fp16_norms, qjl)
     q1, q2 = prep_query(cb, q)
     sel = slice(None) if rows is None else rows
     n = (code["n16"].astype(np.float64) if use_fp16_norms else code["n"])[sel]
