@@ -176,7 +176,44 @@ static tq_status check_desc(const tq_codebook_desc* desc, const char* what) {
     return fail(TQ_EINVAL, "%s: extra must be 0, d/4 or d/2", what);
   if (D.extra != 0 && (D.mode != TQ_MODE_SCALAR || b1 + 1 > 4))
     return fail(TQ_EINVAL, "%s: extra bits need scalar mode and b' <= 3", what);
+  if (D.outliers) {
+    if (D.d != 128 || D.kind != TQ_KIND_PROD || D.mode != TQ_MODE_SCALAR || D.extra == 0)
+      return fail(TQ_EINVAL, "%s: the outlier-channel split needs d = 128, PROD kind, scalar mode and extra = 32 or 64",
+                  what);
+    if (D.pi || D.s) return fail(TQ_EINVAL, "%s: the outlier-channel split takes no Pi or S override", what);
+    std::vector<char> seen(D.d, 0);
+    for (int e = 0; e < D.extra; ++e) {
+      const int c = D.outliers[e];
+      if (c < 0 || c >= D.d || seen[c]) return fail(TQ_EINVAL, "%s: outlier channels must be distinct, in 0..d-1", what);
+      seen[c] = 1;
+    }
+  }
   return TQ_OK;
+}
+
+// Outlier-channel split: the d x d rotation x -> (Pi_A x_A, Pi_B x_B) (rows
+// 0..E-1 from group A's channels in the listed order, the rest from group B's
+// in channel order) and the block-diagonal sketch diag(S_A, S_B), each group
+// drawn from its own seeds (A: seed_pi, seed_s; B: seed_pi + 1, seed_s + 1).
+static void split_matrices(const tq_codebook_desc& D, std::vector<double>& pi, std::vector<float>& s) {
+  const int d = D.d, E = D.extra, F = d - E;
+  std::vector<int> B;
+  std::vector<char> isA(d, 0);
+  for (int e = 0; e < E; ++e) isA[D.outliers[e]] = 1;
+  for (int c = 0; c < d; ++c)
+    if (!isA[c]) B.push_back(c);
+  const std::vector<double> pa = tqm::haar_rotation(E, D.seed_pi), pb = tqm::haar_rotation(F, D.seed_pi + 1);
+  pi.assign((size_t)d * d, 0.0);
+  for (int i = 0; i < E; ++i)
+    for (int j = 0; j < E; ++j) pi[(size_t)i * d + D.outliers[j]] = pa[(size_t)i * E + j];
+  for (int i = 0; i < F; ++i)
+    for (int j = 0; j < F; ++j) pi[(size_t)(E + i) * d + B[j]] = pb[(size_t)i * F + j];
+  const std::vector<double> sa = tqm::gaussians(D.seed_s, (size_t)E * E), sb = tqm::gaussians(D.seed_s + 1, (size_t)F * F);
+  s.assign((size_t)d * d, 0.f);
+  for (int i = 0; i < E; ++i)
+    for (int j = 0; j < E; ++j) s[(size_t)i * d + j] = tqm::round_bf16(sa[(size_t)i * E + j]);
+  for (int i = 0; i < F; ++i)
+    for (int j = 0; j < F; ++j) s[(size_t)(E + i) * d + E + j] = tqm::round_bf16(sb[(size_t)i * F + j]);
 }
 
 tq_status tq_host_tables(const tq_codebook_desc* desc, int32_t level, float* centroids, float* boundaries,
@@ -190,7 +227,7 @@ tq_status tq_host_tables(const tq_codebook_desc* desc, int32_t level, float* cen
   const int L = 1 << b1;
   const int logd = d == 128 ? 7 : 8;
   if (D.mode == TQ_MODE_SCALAR) {
-    const tqm::Quantizer q = tqm::lloyd_max_beta(d, L);
+    const tqm::Quantizer q = tqm::lloyd_max_beta(D.outliers ? d - D.extra : d, L);
     for (int k = 0; k < L && centroids; ++k) centroids[k] = (float)q.c[k];
     for (int k = 0; k < L - 1 && boundaries; ++k) boundaries[k] = (float)q.t[k];
   } else {
@@ -203,6 +240,14 @@ tq_status tq_host_tables(const tq_codebook_desc* desc, int32_t level, float* cen
       for (int k = 0; k < L && centroids; ++k) centroids[k] = (float)q.c[k];
       for (int k = 0; k < L - 1 && boundaries; ++k) boundaries[k] = (float)q.t[k];
     }
+  }
+  if (D.outliers) {
+    std::vector<double> P;
+    std::vector<float> S;
+    split_matrices(D, P, S);
+    if (pi) std::memcpy(pi, P.data(), P.size() * sizeof(double));
+    if (s) std::memcpy(s, S.data(), S.size() * sizeof(float));
+    return ok();
   }
   if (pi) {
     const std::vector<double> P = D.pi ? std::vector<double>(D.pi, D.pi + (size_t)d * d) : tqm::haar_rotation(d, D.seed_pi);
@@ -234,6 +279,7 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   cb->desc = D;
   cb->desc.pi = nullptr;
   cb->desc.s = nullptr;
+  cb->desc.outliers = nullptr;
   cb->device = device;
   tq::Dev& dv = cb->dev;
   std::memset(&dv, 0, sizeof(dv));
@@ -246,19 +292,24 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   dv.extra = D.extra;
   dv.P = b1 + (D.kind == TQ_KIND_PROD ? 1 : 0);
   dv.W = (d / 32) * dv.P + D.extra / 32;
-  dv.nb = D.kind == TQ_KIND_PROD ? 4 : 2;
-  dv.qjl_const = (float)(std::sqrt(M_PI / 2.0) / d);
+  dv.split = D.outliers != nullptr;
+  dv.nb = dv.split ? 8 : (D.kind == TQ_KIND_PROD ? 4 : 2);
+  // group B (the main codebook) and group A (the extended one) of a split
+  // are E- and (d - E)-dimensional instances: own laws and QJL constants
+  const int d_main = dv.split ? d - D.extra : d, d_ext = dv.split ? D.extra : d;
+  dv.qjl_const = (float)(std::sqrt(M_PI / 2.0) / d_main);
+  dv.qjl_const_x = (float)(std::sqrt(M_PI / 2.0) / d_ext);
   dv.first_wait = kDefaultWaitPolls;
   const int L = 1 << b1;
 
   if (D.mode == TQ_MODE_SCALAR) {
-    const tqm::Quantizer q = tqm::lloyd_max_beta(d, L);
+    const tqm::Quantizer q = tqm::lloyd_max_beta(d_main, L);
     cb->cent.resize(L);
     cb->bound.resize(L - 1);
     for (int k = 0; k < L; ++k) cb->cent[k] = dv.cent[k] = (float)q.c[k];
     for (int k = 0; k < L - 1; ++k) cb->bound[k] = dv.bound[k] = (float)q.t[k];
     if (D.extra) {
-      const tqm::Quantizer qx = tqm::lloyd_max_beta(d, 2 * L);
+      const tqm::Quantizer qx = tqm::lloyd_max_beta(d_ext, 2 * L);
       for (int k = 0; k < 2 * L; ++k) dv.cent_x[k] = (float)qx.c[k];
       for (int k = 0; k < 2 * L - 1; ++k) dv.bound_x[k] = (float)qx.t[k];
     }
@@ -355,7 +406,10 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   }
 
   // rotation
-  if (D.pi) {
+  std::vector<float> split_s;
+  if (dv.split) {
+    split_matrices(D, cb->pi, split_s);
+  } else if (D.pi) {
     cb->pi.assign(D.pi, D.pi + (size_t)d * d);
   } else {
     cb->pi = tqm::haar_rotation(d, D.seed_pi);
@@ -380,7 +434,9 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   if (D.kind == TQ_KIND_PROD) {
     const int m = D.m;
     cb->s.resize((size_t)m * d);
-    if (D.s) {
+    if (dv.split) {
+      cb->s = split_s;
+    } else if (D.s) {
       for (size_t e = 0; e < cb->s.size(); ++e) {
         if (tqm::round_bf16(D.s[e]) != D.s[e]) {
           tq_free_codebook(cb);
@@ -424,7 +480,9 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   }
   cudaDeviceGetAttribute(&cb->sms, cudaDevAttrMultiProcessorCount, cb->device);
   cb->tc_ready = false;
-  if (D.mode == TQ_MODE_SCALAR && d == 128) {
+  // (the tensor-core quantize normalises whole rows: a split codebook's
+  // per-group norms take the row-wise kernels)
+  if (D.mode == TQ_MODE_SCALAR && d == 128 && !dv.split) {
     bool good = encode_bf16_rows(&cb->tm_pihi, dv.Pi_hi, d, d) && encode_bf16_rows(&cb->tm_pilo, dv.Pi_lo, d, d);
     if (D.kind == TQ_KIND_PROD) good = good && encode_bf16_rows(&cb->tm_s, dv.S_bf, D.m, d);
     else cb->tm_s = cb->tm_pihi;

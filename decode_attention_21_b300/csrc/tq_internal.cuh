@@ -14,7 +14,7 @@ struct Dev {
   int d, m, b1, kind, mode, extra;
   int P;            // stored planes per 32-coordinate word column
   int W;            // 32-bit words per record
-  int nb;           // norm bytes per row (4 prod, 2 mse)
+  int nb;           // norm bytes per row (4 prod, 2 mse, 8 split)
   int nv;           // stage-1 virtual planes (odd subsets of the code planes)
   uint32_t vmask[kMaxL];  // plane p in subset <=> bit p set
   float vcoef[kMaxL];     // yhat = sum_v vcoef[v] * (-1)^(xor of the subset's bits)
@@ -25,7 +25,11 @@ struct Dev {
   // planes (plane b' = the extra bit), nvx = 2 nv of them
   int nvx;
   float vcoef_x[kMaxL];
-  float qjl_const;        // sqrt(pi/2) / m
+  float qjl_const;        // sqrt(pi/2) / m (split: group B's, m = d - extra)
+  // outlier-channel split: rotated coordinates 0..extra-1 are group A (the
+  // extended codebook, own norms, QJL constant sqrt(pi/2) / extra)
+  int split;
+  float qjl_const_x;
   // polls of the first bounded wait of every launch (the others use the
   // full limit); lowered only by tq_set_first_wait_limit, for tests
   long long first_wait;
@@ -70,9 +74,10 @@ inline __host__ __device__ int64_t norm_offset(const Dev& cb, int64_t rows) {
 }
 
 // Per-(sequence, kv head) block of query data prepared once per step.
-//   header: float S1[4], S2[4], K1[4], K2[4]  (per head slot)
+//   header: float S1[4], S2[4], K1[4], K2[4], K1x[4], K2x[4], pad (per head
+//           slot; K1x, K2x: the constants of a split's group A)
 //   fragments: [2][d/16][32 lanes] uint2  (plane 0 = stage 1, plane 1 = QJL)
-constexpr int kPrepHeader = 64;
+constexpr int kPrepHeader = 128;
 inline __host__ __device__ int64_t prep_block_bytes(int d) { return kPrepHeader + (int64_t)2 * (d / 16) * 32 * 8; }
 
 // Split-KV partial of one warp: per head slot (4): m, l, acc[d].

@@ -74,13 +74,21 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
   const bool prod = cb.kind == 0;
   const int64_t stride = (int64_t)gridDim.x * 8;
 
+  // outlier-channel split: word columns k < kx (coordinates 0..extra-1) are
+  // group A, with its own norms; otherwise kx = 0 and one group holds all
+  const int kx = cb.split ? cb.extra / 32 : 0;
   for (int64_t row = (int64_t)blockIdx.x * 8 + warp; row < n; row += stride) {
     float y[K];
-    float nrm;
+    float nrm, nrm_x = 0.f;
     if (y_in) {
 #pragma unroll
       for (int k = 0; k < K; ++k) y[k] = y_in[row * D + lane + 32 * k];
-      nrm = n_in[row];
+      if (kx) {
+        nrm_x = n_in[2 * row];
+        nrm = n_in[2 * row + 1];
+      } else {
+        nrm = n_in[row];
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < K; ++k) {
@@ -102,14 +110,22 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
 #pragma unroll
         for (int k = 0; k < K; ++k) y[k] = fmaf(__ldg(prow + 32 * k), xj, y[k]);
       }
-      float ss = 0.f;
+      float ss = 0.f, ssx = 0.f;
 #pragma unroll
-      for (int k = 0; k < K; ++k) ss = fmaf(y[k], y[k], ss);
+      for (int k = 0; k < K; ++k) {
+        if (k < kx) ssx = fmaf(y[k], y[k], ssx);
+        else ss = fmaf(y[k], y[k], ss);
+      }
       ss = warp_sum(ss);
       nrm = sqrtf(ss);
       const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
+      float inv_x = 0.f;
+      if (kx) {
+        nrm_x = sqrtf(warp_sum(ssx));
+        inv_x = nrm_x > 0.f ? 1.f / nrm_x : 0.f;
+      }
 #pragma unroll
-      for (int k = 0; k < K; ++k) y[k] *= inv;
+      for (int k = 0; k < K; ++k) y[k] *= k < kx ? inv_x : inv;
       __syncwarp();
     }
 
@@ -232,13 +248,17 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
       }
     }
 
-    // ---- QJL: gamma = ||r||, signs of S r
-    float gamma = 0.f;
+    // ---- QJL: gamma = ||r|| (per group for a split), signs of S r
+    float gamma = 0.f, gamma_x = 0.f;
     if (prod) {
-      float ss = 0.f;
+      float ss = 0.f, ssx = 0.f;
 #pragma unroll
-      for (int k = 0; k < K; ++k) ss = fmaf(r[k], r[k], ss);
+      for (int k = 0; k < K; ++k) {
+        if (k < kx) ssx = fmaf(r[k], r[k], ssx);
+        else ss = fmaf(r[k], r[k], ss);
+      }
       gamma = sqrtf(warp_sum(ss));
+      if (kx) gamma_x = sqrtf(warp_sum(ssx));
       __syncwarp();
 #pragma unroll
       for (int k = 0; k < K; ++k) buf[lane + 32 * k] = r[k];
@@ -271,10 +291,15 @@ __global__ void __launch_bounds__(256) k_quantize_simt(const Dev cb, uint8_t* __
       if (lane < W) rec[lane] = mine0;
       if (lane + 32 < W) rec[lane + 32] = mine1;
       if (lane == 0) {
-        if (prod)
+        if (kx) {
+          __half2* e = reinterpret_cast<__half2*>(norms) + 2 * dst;
+          e[0] = __floats2half2_rn(nrm_x, gamma_x);
+          e[1] = __floats2half2_rn(nrm, gamma);
+        } else if (prod) {
           reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
-        else
+        } else {
           reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+        }
       }
     }
   }
@@ -328,12 +353,15 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
   Quarter<kKeep ? D : 4> mpi, ms;
   if (kKeep && !y_in) mpi.load(cb.PiT, i, q);
   if (kKeep && prod) ms.load(cb.ST, i, q);
+  // outlier-channel split: warps w < kx (coordinates 0..extra-1) are group
+  // A, with its own norms; otherwise kx = 0
+  const int kx = cb.split ? cb.extra / 32 : 0;
   for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
     float y = 0.f, nrm = 0.f;
     if (y_in) {
       if (q == 0) {
         y = y_in[row * D + i];
-        nrm = n_in[row];
+        nrm = kx ? n_in[2 * row + (w < kx ? 0 : 1)] : n_in[row];
       }
     } else {
       if (q == 0) {
@@ -362,9 +390,10 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
       }
       __syncthreads();
       if (q == 0) {
+        // this thread's group: words kx.. (group B, or all), or 0..kx-1
         float ss = 0.f;
 #pragma unroll
-        for (int k = 0; k < NW; ++k) ss += red[k];
+        for (int k = 0; k < NW; ++k) ss += ((k < kx) == (w < kx)) ? red[k] : 0.f;
         nrm = sqrtf(ss);
         y *= nrm > 0.f ? 1.f / nrm : 0.f;
       }
@@ -397,7 +426,7 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
       }
     }
     __syncthreads();
-    float gamma = 0.f;
+    float gamma = 0.f, nrm_x = 0.f, gamma_x = 0.f;
     if (prod) {
       if constexpr (kKeep) {
         part[q][i] = ms.dot(xs, q);
@@ -410,7 +439,7 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
       if (q == 0) {
         float ss = 0.f;
 #pragma unroll
-        for (int k = 0; k < NW; ++k) ss += red[k];
+        for (int k = 0; k < NW; ++k) ss += ((k < kx) == (w < kx)) ? red[k] : 0.f;
         gamma = sqrtf(ss);
         const float z = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
         const uint32_t bw = __ballot_sync(kFull, z >= 0.f);
@@ -418,6 +447,19 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
       }
     }
     __syncthreads();
+    // a split's norm entry is written by thread 0 (group A) with group B's
+    // values taken from thread 32 kx (the first coordinate of group B)
+    if (kx && t == 32 * kx) {
+      xs[0] = nrm;
+      xs[1] = gamma;
+    }
+    __syncthreads();
+    if (kx && t == 0) {
+      nrm_x = nrm;
+      gamma_x = gamma;
+      nrm = xs[0];
+      gamma = xs[1];
+    }
     // Launched as a programmatic dependent, this CTA may have computed its
     // rows while the kernel before it (a scoring kernel reading this cache)
     // was still running: nothing is written, and no destination is looked up,
@@ -430,10 +472,15 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
     if (dst >= 0) {
       if (t < cb.W) recs[dst * cb.W + t] = words[t];
       if (t == 0) {
-        if (prod)
+        if (kx) {
+          __half2* e = reinterpret_cast<__half2*>(norms) + 2 * dst;
+          e[0] = __floats2half2_rn(nrm_x, gamma_x);
+          e[1] = __floats2half2_rn(nrm, gamma);
+        } else if (prod) {
           reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
-        else
+        } else {
           reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+        }
       }
     }
     __syncthreads();

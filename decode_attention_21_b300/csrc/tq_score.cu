@@ -128,12 +128,22 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   cluster_sync();
   // every CTA combines the four partials in rank order (identical results)
   float mx1 = 0.f, mx2 = 0.f, sm1 = 0.f, sm2 = 0.f, sm1x = 0.f;
+  // outlier-channel split: the sums of q' and q'' over each group's word
+  // columns (group A: columns 0 .. extra/32 - 1)
+  float ga1 = 0.f, ga2 = 0.f, gb1 = 0.f, gb2 = 0.f;
   for (int k = 0; k < 4; ++k) {
     mx1 = fmaxf(mx1, red[k][0]);
     mx2 = fmaxf(mx2, red[k][1]);
     sm1 += red[k][2];
     sm2 += red[k][3];
     sm1x += red[k][4];
+    if (k < cb.extra / 32) {
+      ga1 += red[k][2];
+      ga2 += red[k][3];
+    } else {
+      gb1 += red[k][2];
+      gb2 += red[k][3];
+    }
   }
   const int nv = cb.nv;
   float csum = 0.f, csumx = 0.f;
@@ -146,8 +156,18 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   if (r == 0 && tid == 0) {
     hdr[slot] = live ? S1 : 0.f;
     hdr[4 + slot] = live ? S2 : 0.f;
-    hdr[8 + slot] = live ? fmaf(csumx - csum, sm1x, csum * sm1) : 0.f;
-    hdr[12 + slot] = live ? -sm2 : 0.f;
+    if (cb.split) {
+      // group B's constants in K1, K2 and group A's in K1x, K2x
+      hdr[8 + slot] = live ? csum * gb1 : 0.f;
+      hdr[12 + slot] = live ? -gb2 : 0.f;
+      hdr[16 + slot] = live ? csumx * ga1 : 0.f;
+      hdr[20 + slot] = live ? -ga2 : 0.f;
+    } else {
+      hdr[8 + slot] = live ? fmaf(csumx - csum, sm1x, csum * sm1) : 0.f;
+      hdr[12 + slot] = live ? -sm2 : 0.f;
+      hdr[16 + slot] = 0.f;
+      hdr[20 + slot] = 0.f;
+    }
   }
   // fragments of this word column (c = r) for this slot's lanes g = 2 slot + piece
   uint2* frag = reinterpret_cast<uint2*>(blk + kPrepHeader);
@@ -183,7 +203,7 @@ struct QK16 {
   static constexpr int PS = QJL ? P - 1 : P;   // stage-1 code planes (the QJL sign plane is last)
   static constexpr int NQ = QJL ? 1 : 0;
   uint2 bq[1 + NQ][8];
-  float S2, K1, K2;
+  float S2, K1, K2, K1x, K2x;
   float cv[NV];
   float cvx[2 * NV];   // coefficients of the extended (mixed-bit) codebook's planes
   int c_;
@@ -200,6 +220,8 @@ struct QK16 {
     S2 = hdr[4 + c];
     K1 = hdr[8 + c];
     K2 = hdr[12 + c];
+    K1x = hdr[16 + c];
+    K2x = hdr[20 + c];
 #pragma unroll
     for (int v = 0; v < NV; ++v) cv[v] = -2.f * cb.vcoef[v] * S1;
 #pragma unroll
@@ -227,9 +249,23 @@ struct QK16 {
   __device__ __forceinline__ void score_mixed(const uint32_t (&wa)[T][P], const uint32_t (&wb)[T][P],
                                               const uint32_t (&ea)[T], const uint32_t (&eb)[T], float (&s1)[T][2],
                                               float (&s2)[T][2]) const {
+    float s1x[T][2], s2x[T][2];
+    score_groups<T, EXT, false>(wa, wb, ea, eb, s1, s2, s1x, s2x);
+  }
+
+  // SPLIT (outlier-channel split keys): the extended columns are group A,
+  // with its own norms, so its stage-1 and QJL sums come out separately
+  // (s1x, s2x) and s1, s2 hold group B's; group A's sign plane gets its own
+  // accumulator (lanes of the other group feed it zeros).
+  template <int T, int EXT, bool SPLIT>
+  __device__ __forceinline__ void score_groups(const uint32_t (&wa)[T][P], const uint32_t (&wb)[T][P],
+                                               const uint32_t (&ea)[T], const uint32_t (&eb)[T], float (&s1)[T][2],
+                                               float (&s2)[T][2], float (&s1x)[T][2], float (&s2x)[T][2]) const {
+    static_assert(!SPLIT || (QJL && EXT > 0), "a split key has the QJL plane and extended columns");
     constexpr int NX = EXT ? 2 * NV : 0;
     const bool xl = EXT > 0 && c_ < EXT;
-    float a1[T][NV][C1][4], a2[T][2][4], ax[T][NX > 0 ? NX : 1][4];
+    float a1[T][NV][C1][4], a2[T][2][4], ax[T][NX > 0 ? NX : 1][4], a2x[T][SPLIT ? 2 : 1][4];
+    uint32_t qxa[T], qxb[T], qya[T], qyb[T];    // group A's sign-plane operands (SPLIT)
     uint32_t xa[T][NV + NQ], xb[T][NV + NQ], ya[T][NV + NQ], yb[T][NV + NQ];
     uint32_t za[T][NX > 0 ? NX : 1], zb[T][NX > 0 ? NX : 1], wza[T][NX > 0 ? NX : 1], wzb[T][NX > 0 ? NX : 1];
 #pragma unroll
@@ -271,8 +307,18 @@ struct QK16 {
           for (int e = 0; e < 4; ++e) a1[t][v][ch][e] = 0.f;
       }
       if constexpr (QJL) {
-        xa[t][NV] = wa[t][P - 1];
-        xb[t][NV] = wb[t][P - 1];
+        xa[t][NV] = (SPLIT && xl) ? 0u : wa[t][P - 1];
+        xb[t][NV] = (SPLIT && xl) ? 0u : wb[t][P - 1];
+      }
+      if constexpr (SPLIT) {
+        qxa[t] = xl ? wa[t][P - 1] : 0u;
+        qxb[t] = xl ? wb[t][P - 1] : 0u;
+        qya[t] = qxa[t] >> 4;
+        qyb[t] = qxb[t] >> 4;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a2x[t][ch][e] = 0.f;
       }
 #pragma unroll
       for (int v = 0; v < NV + NQ; ++v) {
@@ -293,6 +339,9 @@ struct QK16 {
           mma_f16(a2[t][kb & 1], bit_operand(xa[t][NV], ya[t][NV], b0), bit_operand(xb[t][NV], yb[t][NV], b0),
                   bit_operand(xa[t][NV], ya[t][NV], b1), bit_operand(xb[t][NV], yb[t][NV], b1), bq[NQ][kb].x,
                   bq[NQ][kb].y);
+        if constexpr (SPLIT)
+          mma_f16(a2x[t][kb & 1], bit_operand(qxa[t], qya[t], b0), bit_operand(qxb[t], qyb[t], b0),
+                  bit_operand(qxa[t], qya[t], b1), bit_operand(qxb[t], qyb[t], b1), bq[NQ][kb].x, bq[NQ][kb].y);
 #pragma unroll
         for (int v = 0; v < NV; ++v)
           mma_f16(a1[t][v][kb % C1], bit_operand(xa[t][v], ya[t][v], b0), bit_operand(xb[t][v], yb[t][v], b0),
@@ -315,10 +364,16 @@ struct QK16 {
           ra = fmaf(cv[v], a1[t][v][ch][0] + a1[t][v][ch][1], ra);
           rb = fmaf(cv[v], a1[t][v][ch][2] + a1[t][v][ch][3], rb);
         }
+      float xa_ = SPLIT ? K1x : 0.f, xb_ = SPLIT ? K1x : 0.f;
 #pragma unroll
       for (int u = 0; u < NX; ++u) {
-        ra = fmaf(cvx[u], ax[t][u][0] + ax[t][u][1], ra);
-        rb = fmaf(cvx[u], ax[t][u][2] + ax[t][u][3], rb);
+        if constexpr (SPLIT) {
+          xa_ = fmaf(cvx[u], ax[t][u][0] + ax[t][u][1], xa_);
+          xb_ = fmaf(cvx[u], ax[t][u][2] + ax[t][u][3], xb_);
+        } else {
+          ra = fmaf(cvx[u], ax[t][u][0] + ax[t][u][1], ra);
+          rb = fmaf(cvx[u], ax[t][u][2] + ax[t][u][3], rb);
+        }
       }
       s1[t][0] = ra;
       s1[t][1] = rb;
@@ -327,6 +382,12 @@ struct QK16 {
         s2[t][1] = fmaf(S2, (a2[t][0][2] + a2[t][0][3]) + (a2[t][1][2] + a2[t][1][3]), K2);
       } else {
         s2[t][0] = s2[t][1] = 0.f;
+      }
+      if constexpr (SPLIT) {
+        s1x[t][0] = xa_;
+        s1x[t][1] = xb_;
+        s2x[t][0] = fmaf(S2, (a2x[t][0][0] + a2x[t][0][1]) + (a2x[t][1][0] + a2x[t][1][1]), K2x);
+        s2x[t][1] = fmaf(S2, (a2x[t][0][2] + a2x[t][0][3]) + (a2x[t][1][2] + a2x[t][1][3]), K2x);
       }
     }
   }
@@ -352,13 +413,15 @@ __device__ __forceinline__ void load_words(const uint32_t* __restrict__ rec, int
 
 // Key words and norms of one 16-key tile for thread (g, c).  The norm entry
 // is 4 bytes (n, gamma) with the QJL term, 2 bytes (n) without.
-template <int P, bool QJL = true, int EXT = 0>
+template <int P, bool QJL = true, int EXT = 0, bool SPLIT = false>
 struct KTile {
   uint32_t wa[P], wb[P];
   uint32_t ea = 0, eb = 0;   // extra-bit words (word columns < EXT of mixed-bit keys)
-  uint32_t na, nb;
+  uint32_t na, nb;           // norm entries (a split's group B: n_B, gamma_B)
+  uint32_t nxa = 0, nxb = 0; // a split's group A: n_A, gamma_A
   __device__ __forceinline__ static uint32_t norm_at(const uint32_t* nrm, int64_t row) {
-    if constexpr (QJL) return __ldg(nrm + row);
+    if constexpr (SPLIT) return __ldg(nrm + 2 * row + 1);
+    else if constexpr (QJL) return __ldg(nrm + row);
     else return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(nrm) + row);
   }
   __device__ __forceinline__ void load(const uint32_t* recs, const uint32_t* nrm, int W, int64_t rowbase, int64_t ta,
@@ -368,6 +431,7 @@ struct KTile {
       load_words<P, EXT == 0>(recs + (rowbase + ta) * W, c, wa);
       if (EXT && c < EXT) ea = __ldg(recs + (rowbase + ta) * W + 4 * P + c);
       na = norm_at(nrm, rowbase + ta);
+      if (SPLIT) nxa = __ldg(nrm + 2 * (rowbase + ta));
     } else {
 #pragma unroll
       for (int p = 0; p < P; ++p) wa[p] = 0;
@@ -377,6 +441,7 @@ struct KTile {
       load_words<P, EXT == 0>(recs + (rowbase + tb) * W, c, wb);
       if (EXT && c < EXT) eb = __ldg(recs + (rowbase + tb) * W + 4 * P + c);
       nb = norm_at(nrm, rowbase + tb);
+      if (SPLIT) nxb = __ldg(nrm + 2 * (rowbase + tb));
     } else {
 #pragma unroll
       for (int p = 0; p < P; ++p) wb[p] = 0;
@@ -404,11 +469,20 @@ __device__ __forceinline__ float est_key(uint32_t nrm_bits, float s1, float s2, 
   }
 }
 
+// Outlier-channel split key: group A's estimate (n_A, gamma_A in nx; sums
+// s1x, s2x; QJL constant kqx) plus group B's (n_B, gamma_B in n).
+template <bool QJL, bool SPLIT>
+__device__ __forceinline__ float est_groups(uint32_t nx, uint32_t n, float s1x, float s2x, float s1, float s2,
+                                            float kqx, float kq) {
+  if constexpr (SPLIT) return est_from(nx, s1x, s2x, kqx) + est_from(n, s1, s2, kq);
+  else return est_key<QJL>(n, s1, s2, kq);
+}
+
 // ---------------------------------------------------------------------------
 // Logits: grid (chunks, Hkv, B), 4 warps; each warp scores 16-key tiles,
 // prefetching its next tile while scoring the current one.
 // ---------------------------------------------------------------------------
-template <int NV, int P, bool QJL, int EXT>
+template <int NV, int P, bool QJL, int EXT, bool SPLIT = false>
 __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* __restrict__ kcache, int Hq, int Hkv,
                                                 int64_t capacity, int64_t cache_rows,
                                                 const int32_t* __restrict__ seq_lens,
@@ -428,10 +502,10 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
   const uint32_t* nrm = reinterpret_cast<const uint32_t*>(kcache + norm_offset(cb, cache_rows));
   const int64_t rowbase = ((int64_t)b * Hkv + kvh) * capacity;
-  const float kq = cb.qjl_const;
+  const float kq = cb.qjl_const, kqx = cb.qjl_const_x;
   const int W = cb.W;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
-  KTile<P, QJL, EXT> cur, nxt;
+  KTile<P, QJL, EXT, SPLIT> cur, nxt;
   int64_t tile = tile0 + warp;
   cur.load(recs, nrm, W, rowbase, tile * 16 + g, L, c);
   for (; tile < tend; tile += 4) {
@@ -443,13 +517,13 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
       wa[0][p] = cur.wa[p];
       wb[0][p] = cur.wb[p];
     }
-    float s1[1][2], s2[1][2];
+    float s1[1][2], s2[1][2], s1x[1][2], s2x[1][2];
     const uint32_t ea[1] = {cur.ea}, eb[1] = {cur.eb};
-    qk.template score_mixed<1, EXT>(wa, wb, ea, eb, s1, s2);
+    qk.template score_groups<1, EXT, SPLIT>(wa, wb, ea, eb, s1, s2, s1x, s2x);
     const int64_t ta = tile * 16 + g, tb = ta + 8;
     if (c < G) {
-      if (ta < L) out[ta] = est_key<QJL>(cur.na, s1[0][0], s2[0][0], kq);
-      if (tb < L) out[tb] = est_key<QJL>(cur.nb, s1[0][1], s2[0][1], kq);
+      if (ta < L) out[ta] = est_groups<QJL, SPLIT>(cur.nxa, cur.na, s1x[0][0], s2x[0][0], s1[0][0], s2[0][0], kqx, kq);
+      if (tb < L) out[tb] = est_groups<QJL, SPLIT>(cur.nxb, cur.nb, s1x[0][1], s2x[0][1], s1[0][1], s2[0][1], kqx, kq);
     }
     cur = nxt;
   }
@@ -470,14 +544,14 @@ __global__ void __launch_bounds__(128, 4) k_logits(const Dev cb, const uint8_t* 
 // (bounded) for its copies in flight and returns.
 // ---------------------------------------------------------------------------
 
-template <int NV, int P, bool QJL, int EXT>
+template <int NV, int P, bool QJL, int EXT, bool SPLIT = false>
 __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const uint8_t* __restrict__ kcache, int Hq,
                                                        int Hkv, int64_t capacity, int64_t cache_rows,
                                                        const RowMap map, const int32_t* __restrict__ seq_lens,
                                                        const uint8_t* __restrict__ prep, float* __restrict__ logits,
                                                        int tiles_per_cta, int* __restrict__ status) {
   constexpr int RB = 16 * P + 4 * EXT;       // record bytes at d = 128 (+ extra-bit words)
-  constexpr int NB = QJL ? 4 : 2;            // norm entry bytes
+  constexpr int NB = SPLIT ? 8 : QJL ? 4 : 2;  // norm entry bytes
   constexpr int kPairs = NV <= 4 && EXT == 0;  // two tiles per warp step (registers permitting)
   constexpr int kStageRec = kStageTiles * 16 * RB, kStageNrm = kStageTiles * 16 * NB;
   extern __shared__ __align__(16) uint8_t sm[];
@@ -563,10 +637,11 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
   for (int st = 1; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
   int issued = min(nst, kRing);              // stages requested so far
   // ---- scoring
-  const float kq = cb.qjl_const;
+  const float kq = cb.qjl_const, kqx = cb.qjl_const_x;
   float* out = logits + ((size_t)b * Hq + (size_t)kvh * G + c) * capacity;
   bool ok = true;
   int pending_from = 0;                      // first stage whose copy may still be in flight
+  uint32_t nxa = 0u, nxb = 0u;               // a split key's group A norms (single-tile steps only)
   auto tile_words = [&](const uint8_t* rec, const uint8_t* nrm, int lt, int64_t tg, uint32_t(&wa)[P],
                         uint32_t(&wb)[P], uint32_t& na, uint32_t& nb, uint32_t& ea, uint32_t& eb) {
     const uint8_t* ra = rec + ((size_t)lt * 16 + g) * RB + c * P * 4;
@@ -588,7 +663,14 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
         wb[p] = reinterpret_cast<const uint32_t*>(rbp)[p];
       }
     }
-    if constexpr (QJL) {
+    if constexpr (SPLIT) {
+      const uint2 x = reinterpret_cast<const uint2*>(nrm)[lt * 16 + g];
+      const uint2 y = reinterpret_cast<const uint2*>(nrm)[lt * 16 + g + 8];
+      nxa = x.x;
+      na = x.y;
+      nxb = y.x;
+      nb = y.y;
+    } else if constexpr (QJL) {
       na = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g];
       nb = reinterpret_cast<const uint32_t*>(nrm)[lt * 16 + g + 8];
     } else {
@@ -614,6 +696,15 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
       if (tb < L) out[tb] = est_key<QJL>(nb, s1b, s2b, kq);
     }
   };
+  // a split key: group A's estimate from nxa / nxb plus group B's
+  auto emit_split = [&](int64_t tg, uint32_t na, uint32_t nb, const float (&s1)[1][2], const float (&s2)[1][2],
+                        const float (&s1x)[1][2], const float (&s2x)[1][2]) {
+    const int64_t ta = tg * 16 + g, tb = ta + 8;
+    if (c < G) {
+      if (ta < L) out[ta] = est_groups<QJL, true>(nxa, na, s1x[0][0], s2x[0][0], s1[0][0], s2[0][0], kqx, kq);
+      if (tb < L) out[tb] = est_groups<QJL, true>(nxb, nb, s1x[0][1], s2x[0][1], s1[0][1], s2[0][1], kqx, kq);
+    }
+  };
   for (int st = 0; st < nst; ++st) {
     const int slot = st % kRing;
     if (!__syncthreads_and(bar_wait(su32(&bars[slot]), (uint32_t)((st / kRing) & 1), st == 0 ? cb.first_wait : kWaitLimit))) {
@@ -636,6 +727,17 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
         qk.template score_mixed<2, EXT>(wa, wb, ea, eb, s1, s2);
         emit(tile0 + t_a + lt, na, nb, s1[0][0], s1[0][1], s2[0][0], s2[0][1]);
         emit(tile0 + t_a + lt2, ma, mb, s1[1][0], s1[1][1], s2[1][0], s2[1][1]);
+      } else if constexpr (SPLIT) {
+        uint32_t wa[1][P], wb[1][P], na, nb, ea[1], eb[1];
+        float s1[1][2], s2[1][2], s1x[1][2], s2x[1][2];
+        tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb, ea[0], eb[0]);
+        qk.template score_groups<1, EXT, true>(wa, wb, ea, eb, s1, s2, s1x, s2x);
+        emit_split(tile0 + t_a + lt, na, nb, s1, s2, s1x, s2x);
+        if (lt2 < n_here) {
+          tile_words(rec, nrm, lt2, tile0 + t_a + lt2, wa[0], wb[0], na, nb, ea[0], eb[0]);
+          qk.template score_groups<1, EXT, true>(wa, wb, ea, eb, s1, s2, s1x, s2x);
+          emit_split(tile0 + t_a + lt2, na, nb, s1, s2, s1x, s2x);
+        }
       } else {
         uint32_t wa[1][P], wb[1][P], na, nb, ea[1], eb[1];
         tile_words(rec, nrm, lt, tile0 + t_a + lt, wa[0], wb[0], na, nb, ea[0], eb[0]);
@@ -860,7 +962,7 @@ constexpr int attn_min_blocks(int nvk, int extk) { return nvk >= 4 || extk > 0 ?
 // query fragments are loaded), and each warp scores tiles warp and warp + 4
 // of every stage.
 // ---------------------------------------------------------------------------
-template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK, int EXTV>
+template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK, int EXTV, bool SPLIT = false>
 __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn_staged(const Dev kcb, const Dev vcb,
                                                      const uint8_t* __restrict__ kcache,
                                                      const uint8_t* __restrict__ vcache, int Hq, int Hkv,
@@ -871,7 +973,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
                                                      int* __restrict__ status) {
   constexpr int RBK = 16 * PK + 4 * EXTK;       // key record bytes at d = 128 (+ extra-bit words)
   constexpr int RBV = 16 * PV + 4 * EXTV;       // value record bytes (+ extra-bit words)
-  constexpr int NBK = QJLK ? 4 : 2;             // key norm entry bytes
+  constexpr int NBK = SPLIT ? 8 : QJLK ? 4 : 2;  // key norm entry bytes
   constexpr int kSK = kStageTiles * 16 * RBK, kSKN = kStageTiles * 16 * NBK;
   constexpr int kSV = kStageTiles * 16 * RBV, kSVN = kStageTiles * 16 * 2;
   constexpr int kSlot = kSK + kSKN + kSV + kSVN;
@@ -968,7 +1070,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
   for (int u = 0; u < NVV; ++u) vcn[u] = -2.f * vcb.vcoef[u];
 #pragma unroll
   for (int u = 0; u < (EXTV ? 2 * NVV : 1); ++u) vcnx[u] = EXTV ? -2.f * vcb.vcoef_x[u] : 0.f;
-  const float kq = kcb.qjl_const;
+  const float kq = kcb.qjl_const, kqx = kcb.qjl_const_x;
   const uint32_t vsel = (g & 1) ? 0x7632u : 0x5410u;
   const int hh = g >> 1, pc = g & 1;    // B-fragment column: head slot, piece
   const int src0 = (2 * c) * 4 + hh, src1 = (2 * c + 1) * 4 + hh;
@@ -1009,10 +1111,17 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
           eb[0] = kb2[4 * PK + c];
         }
       }
-      float s1[1][2], s2[1][2];
-      qk.template score_mixed<1, EXTK>(wa, wb, ea, eb, s1, s2);
-      uint32_t na, nb;
-      if constexpr (QJLK) {
+      float s1[1][2], s2[1][2], s1x[1][2], s2x[1][2];
+      qk.template score_groups<1, EXTK, SPLIT>(wa, wb, ea, eb, s1, s2, s1x, s2x);
+      uint32_t na, nb, nxa = 0u, nxb = 0u;
+      if constexpr (SPLIT) {
+        const uint2 x = reinterpret_cast<const uint2*>(skn)[lt * 16 + g];
+        const uint2 y = reinterpret_cast<const uint2*>(skn)[lt * 16 + g + 8];
+        nxa = x.x;
+        na = x.y;
+        nxb = y.x;
+        nb = y.y;
+      } else if constexpr (QJLK) {
         na = reinterpret_cast<const uint32_t*>(skn)[lt * 16 + g];
         nb = reinterpret_cast<const uint32_t*>(skn)[lt * 16 + g + 8];
       } else {
@@ -1020,8 +1129,12 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
         nb = reinterpret_cast<const unsigned short*>(skn)[lt * 16 + g + 8];
       }
       // scores in log2 units
-      const float sa = ta < L ? est_key<QJLK>(na, s1[0][0], s2[0][0], kq) * scale_log2 : -INFINITY;
-      const float sb = tb < L ? est_key<QJLK>(nb, s1[0][1], s2[0][1], kq) * scale_log2 : -INFINITY;
+      const float sa =
+          ta < L ? est_groups<QJLK, SPLIT>(nxa, na, s1x[0][0], s2x[0][0], s1[0][0], s2[0][0], kqx, kq) * scale_log2
+                 : -INFINITY;
+      const float sb =
+          tb < L ? est_groups<QJLK, SPLIT>(nxb, nb, s1x[0][1], s2x[0][1], s1[0][1], s2[0][1], kqx, kq) * scale_log2
+                 : -INFINITY;
       float mx = fmaxf(sa, sb);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
@@ -1258,48 +1371,59 @@ cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, u
 // Key caches with the QJL term (PROD) use b' = 1..3 code planes + the sign
 // plane, optionally with 1 or 2 extra-bit word columns (mixed-bit caches);
 // MSE-only key caches use b = 1..4 code planes.
+// Outlier-channel split keys are mixed-bit records with per-group norms.
 #define TQ_LOGITS_DISPATCH(CALL)                          \
+  if (cb.kind == 0 && cb.split) {                         \
+    switch (cb.b1 * 4 + cb.extra / 32) {                  \
+      case 5: CALL(1, 2, true, 1, true);                  \
+      case 6: CALL(1, 2, true, 2, true);                  \
+      case 9: CALL(2, 3, true, 1, true);                  \
+      case 10: CALL(2, 3, true, 2, true);                 \
+      case 13: CALL(4, 4, true, 1, true);                 \
+      default: CALL(4, 4, true, 2, true);                 \
+    }                                                     \
+  }                                                       \
   if (cb.kind == 0) {                                     \
     const int ext = cb.extra / 32;                        \
     switch (cb.b1 * 4 + ext) {                            \
-      case 4: CALL(1, 2, true, 0);                        \
-      case 5: CALL(1, 2, true, 1);                        \
-      case 6: CALL(1, 2, true, 2);                        \
-      case 8: CALL(2, 3, true, 0);                        \
-      case 9: CALL(2, 3, true, 1);                        \
-      case 10: CALL(2, 3, true, 2);                       \
-      case 13: CALL(4, 4, true, 1);                       \
-      case 14: CALL(4, 4, true, 2);                       \
-      default: CALL(4, 4, true, 0);                       \
+      case 4: CALL(1, 2, true, 0, false);                 \
+      case 5: CALL(1, 2, true, 1, false);                 \
+      case 6: CALL(1, 2, true, 2, false);                 \
+      case 8: CALL(2, 3, true, 0, false);                 \
+      case 9: CALL(2, 3, true, 1, false);                 \
+      case 10: CALL(2, 3, true, 2, false);                \
+      case 13: CALL(4, 4, true, 1, false);                \
+      case 14: CALL(4, 4, true, 2, false);                \
+      default: CALL(4, 4, true, 0, false);                \
     }                                                     \
   }                                                       \
   switch (cb.b1) {                                        \
-    case 1: CALL(1, 1, false, 0);                         \
-    case 2: CALL(2, 2, false, 0);                         \
-    case 3: CALL(4, 3, false, 0);                         \
-    default: CALL(8, 4, false, 0);                        \
+    case 1: CALL(1, 1, false, 0, false);                  \
+    case 2: CALL(2, 2, false, 0, false);                  \
+    case 3: CALL(4, 3, false, 0, false);                  \
+    default: CALL(8, 4, false, 0, false);                 \
   }
 
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t rows, const int32_t* seq_lens, const uint8_t* prep, float* logits, int nchunks,
                           int tpc, cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
-#define TQ_CALL(NV, P, Q, X)                                                                                 \
-  k_logits<NV, P, Q, X><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); \
+#define TQ_CALL(NV, P, Q, X, S)                                                                                 \
+  k_logits<NV, P, Q, X, S><<<grid, 128, 0, s>>>(cb, kc, Hq, Hkv, capacity, rows, seq_lens, prep, logits, tpc); \
   return cudaGetLastError()
   TQ_LOGITS_DISPATCH(TQ_CALL)
 #undef TQ_CALL
 }
 
-template <int NV, int P, bool QJL, int EXT>
+template <int NV, int P, bool QJL, int EXT, bool SPLIT>
 static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                                    int64_t rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
                                    float* logits, int nchunks, int tpc, int* status, cudaStream_t s) {
-  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + 4 * EXT + (QJL ? 4 : 2));
-  static cudaError_t configured = [] {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_staged<NV, P, QJL, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(k_logits_staged<NV, P, QJL, EXT>));
+  constexpr size_t smem = (size_t)kRing * kStageTiles * 16 * (16 * P + 4 * EXT + (SPLIT ? 8 : QJL ? 4 : 2));
+  auto kern = k_logits_staged<NV, P, QJL, EXT, SPLIT>;
+  static cudaError_t configured = [&] {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(kern));
     return e;
   }();
   if (configured != cudaSuccess) return configured;
@@ -1313,29 +1437,28 @@ static cudaError_t logits_staged_t(const Dev& cb, const uint8_t* kc, int B, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_logits_staged<NV, P, QJL, EXT>, cb, kc, Hq, Hkv, capacity, rows, map, seq_lens,
-                            prep, logits, tpc, status);
+  return cudaLaunchKernelEx(&cfg, kern, cb, kc, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, tpc, status);
 }
 
 cudaError_t launch_logits_staged(const Dev& cb, const uint8_t* kc, int B, int Hq, int Hkv, int64_t capacity,
                                  int64_t rows, const RowMap& map, const int32_t* seq_lens, const uint8_t* prep,
                                  float* logits, int nchunks, int tpc, int* status, cudaStream_t s) {
-#define TQ_CALL(NV, P, Q, X)                                                                                      \
-  return logits_staged_t<NV, P, Q, X>(cb, kc, B, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, nchunks, tpc, \
-                                      status, s)
+#define TQ_CALL(NV, P, Q, X, S)                                                                                      \
+  return logits_staged_t<NV, P, Q, X, S>(cb, kc, B, Hq, Hkv, capacity, rows, map, seq_lens, prep, logits, nchunks, tpc, \
+                                         status, s)
   TQ_LOGITS_DISPATCH(TQ_CALL)
 #undef TQ_CALL
 }
 #undef TQ_LOGITS_DISPATCH
 
-template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK, int EXTV>
+template <int NVK, int PK, int NVV, int PV, bool QJLK, int EXTK, int EXTV, bool SPLIT>
 static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
                                  const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map,
                                  const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
                                  int* status) {
   constexpr size_t smem =
-      (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 * EXTK + (QJLK ? 4 : 2) + 16 * PV + 4 * EXTV + 2);
-  auto kern = k_attn_staged<NVK, PK, NVV, PV, QJLK, EXTK, EXTV>;
+      (size_t)kRing * kStageTiles * 16 * (16 * PK + 4 * EXTK + (SPLIT ? 8 : QJLK ? 4 : 2) + 16 * PV + 4 * EXTV + 2);
+  auto kern = k_attn_staged<NVK, PK, NVV, PV, QJLK, EXTK, EXTV, SPLIT>;
   static cudaError_t configured = [&] {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = prefer_max_shared(reinterpret_cast<const void*>(kern));
@@ -1359,16 +1482,16 @@ static cudaError_t attn_staged_t(dim3 grid, cudaStream_t s, const Dev& k, const 
 // b = 3 and 4 for MSE-only and mixed-bit keys; mixed-bit values (extra bit on
 // d/4 coordinates) at b = 2 and 3 for keys with the QJL term and no or d/4
 // extra bits (other pairs are rejected by the host before launch).
-template <int NVK, int PK, bool QJLK, int EXTK>
+template <int NVK, int PK, bool QJLK, int EXTK, bool SPLIT>
 static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& v, const uint8_t* kc,
                                  const uint8_t* vc, int Hq, int Hkv, int64_t cap, int64_t rows, const RowMap& map,
                                  const int32_t* sl, const uint8_t* prep, float sl2, float* parts, int tpc,
                                  int* status) {
 #define TQ_ATTN_V(NVV, PV, XV)                                                                                     \
-  return attn_staged_t<NVK, PK, NVV, PV, QJLK, EXTK, XV>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, prep, \
-                                                         sl2, parts, tpc, status)
+  return attn_staged_t<NVK, PK, NVV, PV, QJLK, EXTK, XV, SPLIT>(grid, s, k, v, kc, vc, Hq, Hkv, cap, rows, map, sl, \
+                                                                prep, sl2, parts, tpc, status)
   if (v.extra != 0) {
-    if constexpr (QJLK && EXTK <= 1) {
+    if constexpr (QJLK && EXTK <= 1 && !SPLIT) {
       switch (b1v) {
         case 2: TQ_ATTN_V(2, 2, 1);
         case 3: TQ_ATTN_V(4, 3, 1);
@@ -1397,7 +1520,8 @@ static cudaError_t attn_staged_v(int b1v, dim3 grid, cudaStream_t s, const Dev& 
 bool attn_staged_supports(const Dev& kcb, const Dev& vcb) {
   if (kcb.mode != 0 || vcb.mode != 0) return false;
   if (vcb.extra != 0)
-    return vcb.d == 128 && vcb.extra == 32 && (vcb.b1 == 2 || vcb.b1 == 3) && kcb.kind == 0 && kcb.extra <= 32;
+    return vcb.d == 128 && vcb.extra == 32 && (vcb.b1 == 2 || vcb.b1 == 3) && kcb.kind == 0 && kcb.extra <= 32 &&
+           !kcb.split;
   const bool plain_keys = kcb.kind == 0 && kcb.extra == 0;
   return plain_keys || vcb.b1 == 3 || vcb.b1 == 4;
 }
@@ -1407,27 +1531,37 @@ cudaError_t launch_attn_staged(const Dev& kcb, const Dev& vcb, const uint8_t* kc
                                const uint8_t* prep, float scale_log2, float* parts, int nchunks, int tpc, int* status,
                                cudaStream_t s) {
   const dim3 grid(nchunks, Hkv, B);
-#define TQ_ATTN_K(NVK, PK, Q, X)                                                                                  \
-  return attn_staged_v<NVK, PK, Q, X>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, \
-                                      prep, scale_log2, parts, tpc, status)
+#define TQ_ATTN_K(NVK, PK, Q, X, S)                                                                                  \
+  return attn_staged_v<NVK, PK, Q, X, S>(vcb.b1, grid, s, kcb, vcb, kc, vc, Hq, Hkv, capacity, rows, map, seq_lens, \
+                                         prep, scale_log2, parts, tpc, status)
+  if (kcb.kind == 0 && kcb.split) {
+    switch (kcb.b1 * 4 + kcb.extra / 32) {
+      case 5: TQ_ATTN_K(1, 2, true, 1, true);
+      case 6: TQ_ATTN_K(1, 2, true, 2, true);
+      case 9: TQ_ATTN_K(2, 3, true, 1, true);
+      case 10: TQ_ATTN_K(2, 3, true, 2, true);
+      case 13: TQ_ATTN_K(4, 4, true, 1, true);
+      default: TQ_ATTN_K(4, 4, true, 2, true);
+    }
+  }
   if (kcb.kind == 0) {
     switch (kcb.b1 * 4 + kcb.extra / 32) {
-      case 4: TQ_ATTN_K(1, 2, true, 0);
-      case 5: TQ_ATTN_K(1, 2, true, 1);
-      case 6: TQ_ATTN_K(1, 2, true, 2);
-      case 8: TQ_ATTN_K(2, 3, true, 0);
-      case 9: TQ_ATTN_K(2, 3, true, 1);
-      case 10: TQ_ATTN_K(2, 3, true, 2);
-      case 13: TQ_ATTN_K(4, 4, true, 1);
-      case 14: TQ_ATTN_K(4, 4, true, 2);
-      default: TQ_ATTN_K(4, 4, true, 0);
+      case 4: TQ_ATTN_K(1, 2, true, 0, false);
+      case 5: TQ_ATTN_K(1, 2, true, 1, false);
+      case 6: TQ_ATTN_K(1, 2, true, 2, false);
+      case 8: TQ_ATTN_K(2, 3, true, 0, false);
+      case 9: TQ_ATTN_K(2, 3, true, 1, false);
+      case 10: TQ_ATTN_K(2, 3, true, 2, false);
+      case 13: TQ_ATTN_K(4, 4, true, 1, false);
+      case 14: TQ_ATTN_K(4, 4, true, 2, false);
+      default: TQ_ATTN_K(4, 4, true, 0, false);
     }
   }
   switch (kcb.b1) {
-    case 1: TQ_ATTN_K(1, 1, false, 0);
-    case 2: TQ_ATTN_K(2, 2, false, 0);
-    case 3: TQ_ATTN_K(4, 3, false, 0);
-    default: TQ_ATTN_K(8, 4, false, 0);
+    case 1: TQ_ATTN_K(1, 1, false, 0, false);
+    case 2: TQ_ATTN_K(2, 2, false, 0, false);
+    case 3: TQ_ATTN_K(4, 3, false, 0, false);
+    default: TQ_ATTN_K(8, 4, false, 0, false);
   }
 #undef TQ_ATTN_K
 }

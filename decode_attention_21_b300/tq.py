@@ -35,7 +35,7 @@ class Desc(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int32), ("bits", ctypes.c_int32), ("m", ctypes.c_int32), ("mode", ctypes.c_int32),
                 ("kind", ctypes.c_int32), ("extra", ctypes.c_int32), ("seed_pi", ctypes.c_uint64),
                 ("seed_s", ctypes.c_uint64), ("pi", ctypes.POINTER(ctypes.c_double)),
-                ("s", ctypes.POINTER(ctypes.c_float))]
+                ("s", ctypes.POINTER(ctypes.c_float)), ("outliers", ctypes.POINTER(ctypes.c_int32))]
 
 
 _lib = None
@@ -115,10 +115,16 @@ class Codebook:
     """Owner of a ``tq_codebook*`` built on the current CUDA device."""
 
     def __init__(self, d=128, bits=3, kind=KIND_PROD, mode=MODE_SCALAR, seed_pi=1, seed_s=2, m=None, extra=0,
-                 pi=None, s=None):
+                 pi=None, s=None, outliers=None):
         import numpy as np
-        desc = Desc(d, bits, m if m is not None else d, mode, kind, extra, seed_pi, seed_s, None, None)
+        if outliers is not None:
+            extra = len(outliers)
+        desc = Desc(d, bits, m if m is not None else d, mode, kind, extra, seed_pi, seed_s, None, None, None)
         self._keep = []
+        if outliers is not None:
+            a = np.ascontiguousarray(outliers, dtype=np.int32)
+            self._keep.append(a)
+            desc.outliers = a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
         if pi is not None:
             a = np.ascontiguousarray(pi, dtype=np.float64)
             self._keep.append(a)
@@ -131,6 +137,7 @@ class Codebook:
         _check(lib().tq_make_codebook(ctypes.byref(desc), ctypes.byref(h)))
         self.handle = h.value
         self.d, self.bits, self.kind, self.mode, self.extra = d, bits, kind, mode, extra
+        self.split = outliers is not None
         self.b1 = bits - 1 if kind == KIND_PROD else bits
 
     def __del__(self):
@@ -154,10 +161,15 @@ def codebook_tables(cb):
     return c, t, pi, (s if cb.kind == KIND_PROD else None)
 
 
-def host_tables(d, bits, kind=KIND_PROD, mode=MODE_SCALAR, seed_pi=1, seed_s=2, level=2):
-    """(centroids, boundaries, pi, s) the library would build, computed on the host."""
+def host_tables(d, bits, kind=KIND_PROD, mode=MODE_SCALAR, seed_pi=1, seed_s=2, level=2, outliers=None):
+    """(centroids, boundaries, pi, s) the library would build, computed on the host
+    (for an outlier-channel split: group B's tables, the d x d rotation and sketch)."""
     import numpy as np
-    desc = Desc(d, bits, d, mode, kind, 0, seed_pi, seed_s, None, None)
+    desc = Desc(d, bits, d, mode, kind, 0, seed_pi, seed_s, None, None, None)
+    if outliers is not None:
+        keep = np.ascontiguousarray(outliers, dtype=np.int32)
+        desc.extra = len(keep)
+        desc.outliers = keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
     b1 = bits - 1 if kind == KIND_PROD else bits
     L = 1 << b1
     c = np.zeros(L, dtype=np.float32)

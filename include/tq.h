@@ -69,7 +69,32 @@ typedef struct {
   const double* pi;   /* host, optional: d*d row-major Pi overriding seed_pi */
   const float* s;     /* host, optional: m*d row-major S (bf16-exact values)
                          overriding seed_s                                   */
+  const int32_t* outliers;  /* host, optional: `extra` distinct input channels
+                         (0 .. d-1) forming an outlier group.  Non-NULL
+                         selects the outlier-channel split (below).          */
 } tq_codebook_desc;
+
+/* Outlier-channel split ([xujun] 社区验证 and [suzuke] 實際跑出來的數據
+ * quote 2.5- and 3.5-bit caches; the pages do not say how a fractional width
+ * arises, and this is the reading implemented): the outlier channels (group
+ * A, E = `extra` of them) and the other d - E channels (group B) are each
+ * compressed as their own vector by their own instance of the method, group
+ * A with one more bit per coordinate:
+ *   - own rotation: Pi_A (E x E, Haar, seed_pi), Pi_B ((d-E) x (d-E),
+ *     seed_pi + 1); the codebook's Pi (tq_codebook_tables) is the d x d map
+ *     x -> (Pi_A x_A, Pi_B x_B), so rotated coordinates 0..E-1 are group A's
+ *     (in the order listed) and the rest group B's (channel order);
+ *   - own Lloyd-Max tables on the law of a rotated coordinate of an E- and a
+ *     (d-E)-dimensional unit vector (B: b' bits, A: b'+1 bits);
+ *   - own sketch: S = diag(S_A, S_B) (seed_s, seed_s + 1; m_g = d_g rows)
+ *     and own QJL constant sqrt(pi/2)/d_g;
+ *   - own norms: the norm entry is four fp16 values n_A, gamma_A, n_B,
+ *     gamma_B (8 bytes);
+ *   - the estimate of <q, x> is the sum of the two groups' estimates.
+ * The record is the mixed-bit record (E extended coordinates).  Supported:
+ * d = 128, scalar mode, PROD keys, extra = 32 or 64, bits 2..4; pi and s
+ * overrides must be NULL.  Bits per coordinate: (E (b+1) + (d-E) b)/d codes
+ * + 0.5 for the norms (b = 2: 2.75 at E = 32, 3.0 at E = 64).               */
 
 typedef struct tq_codebook tq_codebook;   /* opaque; immutable once built */
 
@@ -104,7 +129,7 @@ size_t tq_record_bytes(const tq_codebook* cb);
 
 /* Bytes of a cache holding `rows` rows: the records, padding to 256 bytes,
  * then one norm entry per row (PROD: fp16 ||x|| and fp16 ||r||; MSE: fp16
- * ||x||).  Record layout: word (c, p) at word offset c*P + p (P planes, plane
+ * ||x||; outlier-channel split: fp16 n_A, gamma_A, n_B, gamma_B).  Record layout: word (c, p) at word offset c*P + p (P planes, plane
  * 0 = most significant stage-1 bit, last plane of PROD = QJL signs), bit j of
  * word c <-> coordinate 32c + j.                                             */
 size_t tq_cache_bytes(const tq_codebook* cb, int64_t rows);
@@ -124,7 +149,9 @@ tq_status tq_quantize(const tq_codebook* cb, void* cache, int64_t cache_rows,
                       const int64_t* dst_rows, void* stream);
 
 /* As tq_quantize but from already rotated unit rows: y device fp32 [n, d],
- * norms device fp32 [n] (stored as ||x||).  The stage-1 codes depend only on
+ * norms device fp32 [n] (stored as ||x||).  For an outlier-channel split
+ * codebook, y holds each group's unit vector (group A in columns 0..E-1) and
+ * norms is fp32 [n, 2] (n_A, n_B).  The stage-1 codes depend only on
  * fp32 comparisons of y, so they are reproducible bit for bit.              */
 tq_status tq_quantize_rotated(const tq_codebook* cb, void* cache, int64_t cache_rows,
                               const float* y, const float* norms, int64_t n,

@@ -79,3 +79,29 @@ def test_rotation_and_sketch_match_oracle(L, d, seed):
     P = haar_rotation(d, seed)
     assert np.max(np.abs(pi - P)) < 1e-12
     assert np.array_equal(s.astype(np.float64), qjl_matrix(d, d, seed + 1))
+
+
+@pytest.mark.parametrize("E,bits", [(32, 2), (64, 3), (32, 4)])
+def test_split_tables_match_oracle(L, E, bits):
+    # outlier-channel split: the library's d x d rotation and block-diagonal
+    # sketch, built from the two groups' own seeds and the channel list, and
+    # group B's stage-1 tables, against the oracle's two instances
+    from oracle import split
+    out = np.random.default_rng(E + bits).choice(128, size=E, replace=False)
+    c, t, pi, s = tq.host_tables(128, bits, seed_pi=5, seed_s=9, outliers=out)
+    scb = split.SplitCodebook(128, bits, out, seed_pi=5, seed_s=9)
+    assert np.max(np.abs(pi - scb.full_rotation())) < 1e-12
+    assert np.array_equal(s.astype(np.float64), scb.full_sketch())
+    assert np.array_equal(c, scb.groups[1].c) and np.array_equal(t, scb.groups[1].t)
+
+
+def test_split_descriptor_checks(L):
+    out = np.arange(32, dtype=np.int32)
+    for d, kind, mode, extra, chans in [(256, tq.KIND_PROD, tq.MODE_SCALAR, 32, out),
+                                        (128, tq.KIND_MSE, tq.MODE_SCALAR, 32, out),
+                                        (128, tq.KIND_PROD, tq.MODE_POLAR, 32, out),
+                                        (128, tq.KIND_PROD, tq.MODE_SCALAR, 32, np.r_[out[:31], 0].astype(np.int32)),
+                                        (128, tq.KIND_PROD, tq.MODE_SCALAR, 32, np.r_[out[:31], 128].astype(np.int32))]:
+        desc = tq.Desc(d, 3, d, mode, kind, extra, 1, 2, None, None, None)
+        desc.outliers = chans.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        assert L.tq_host_tables(ctypes.byref(desc), 1, None, None, None, None) == tq.TQ_EINVAL
