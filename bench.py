@@ -434,10 +434,18 @@ def dense_comparator(tq, wl, B, Hq, Hkv, d, T, cache, kcb, seq, q, ws, tq_call_m
     exact = torch.empty(B, Hq, T, device="cuda")
     tq.tq_logits_dense(keys.to(torch.float32), B, Hq, Hkv, T, seq, q, exact)
     variants = {}
+    # split<E>_b<b>: outlier-channel split, the layer's E channels of largest
+    # RMS scale one bit wider, each group with its own rotation and norms
     for name, bits, kind, extra in (("prod_b4", 4, tq.KIND_PROD, 0), ("prod_b3.5", 3, tq.KIND_PROD, 32),
-                                    ("prod_b2.5", 2, tq.KIND_PROD, 32), ("mse_b4", 4, tq.KIND_MSE, 0),
-                                    ("mse_b3", 3, tq.KIND_MSE, 0)):
-        cb = kcb if name == "prod_b4" else tq.Codebook(d, bits, kind, extra=extra)
+                                    ("prod_b2.5", 2, tq.KIND_PROD, 32), ("split32_b3", 3, tq.KIND_PROD, 32),
+                                    ("split32_b2", 2, tq.KIND_PROD, 32), ("split64_b2", 2, tq.KIND_PROD, 64),
+                                    ("mse_b4", 4, tq.KIND_MSE, 0), ("mse_b3", 3, tq.KIND_MSE, 0)):
+        if name == "prod_b4":
+            cb = kcb
+        elif name.startswith("split"):
+            cb = tq.Codebook(d, bits, kind, outliers=wl.layer_outlier_channels(Hkv, extra, d))
+        else:
+            cb = tq.Codebook(d, bits, kind, extra=extra)
         fresh = torch.empty(tq.cache_bytes(cb, B * Hkv * T), dtype=torch.uint8, device="cuda")
         for h in range(Hkv):
             dst = torch.arange(h * T, (h + 1) * T, dtype=torch.int64, device="cuda")
@@ -448,7 +456,8 @@ def dense_comparator(tq, wl, B, Hq, Hkv, d, T, cache, kcb, seq, q, ws, tq_call_m
         torch.cuda.synchronize()
         rel = ((est - exact).norm(dim=-1) / exact.norm(dim=-1)).flatten()
         slope = float((est * exact).sum() / (exact * exact).sum())
-        v = {"bytes_per_key": tq.record_bytes(cb) + (4 if kind == tq.KIND_PROD else 2),
+        nbytes = tq.record_bytes(cb) + (8 if name.startswith("split") else 4 if kind == tq.KIND_PROD else 2)
+        v = {"bytes_per_key": nbytes, "bits_per_coord": nbytes * 8 / d,
              "rel_rms_error_median": float(rel.median()), "rel_rms_error_max": float(rel.max()),
              "slope_vs_exact": slope}
         if name != "prod_b4":
@@ -538,8 +547,10 @@ def attention_key_variants(tq, wl, dist, vcb, vc, B, Hq, Hkv, T, q, seq, out, n)
     """The attention call of the same workload with other caches (same
     synthetic keys and values): 3.5-bit keys (3 bits with the QJL term + one
     more stage-1 bit on 32 of 128 rotated coordinates) with the 3-bit values,
-    MSE-only keys at 3 and 4 bits with the 3-bit values, and 3.5-bit keys with
-    3.5-bit values (3-bit MSE + one more bit on 32 coordinates)."""
+    MSE-only keys at 3 and 4 bits with the 3-bit values, 3.5-bit keys with
+    3.5-bit values (3-bit MSE + one more bit on 32 coordinates), and
+    outlier-channel split keys (the layer's 32 largest channels at 4 bits, the
+    rest at 3, each group with its own rotation and norms)."""
     d = 128
     rows = B * Hkv * T
 
@@ -558,8 +569,12 @@ def attention_key_variants(tq, wl, dist, vcb, vc, B, Hq, Hkv, T, q, seq, out, n)
 
     res = {}
     for name, bits, kind, extra, vextra in (("prod_b3.5", 3, tq.KIND_PROD, 32, 0), ("mse_b3", 3, tq.KIND_MSE, 0, 0),
-                                            ("mse_b4", 4, tq.KIND_MSE, 0, 0), ("kv_b3.5", 3, tq.KIND_PROD, 32, 32)):
-        kcb = tq.Codebook(d, bits, kind, tq.MODE_SCALAR, extra=extra)
+                                            ("mse_b4", 4, tq.KIND_MSE, 0, 0), ("kv_b3.5", 3, tq.KIND_PROD, 32, 32),
+                                            ("split32_b3", 3, tq.KIND_PROD, 32, 0)):
+        if name.startswith("split"):
+            kcb = tq.Codebook(d, bits, kind, outliers=wl.layer_outlier_channels(Hkv, extra, d))
+        else:
+            kcb = tq.Codebook(d, bits, kind, tq.MODE_SCALAR, extra=extra)
         kc = fill(kcb, "keys")
         vcb_i, vc_i = vcb, vc
         if vextra:
@@ -569,7 +584,8 @@ def attention_key_variants(tq, wl, dist, vcb, vc, B, Hq, Hkv, T, q, seq, out, n)
         scale = 1.0 / math.sqrt(d)
         ms = per_call_ms(lambda i: tq.tq_decode_attention(kcb, vcb_i, kc, vc_i, B, Hq, Hkv, T, seq, q, scale, out,
                                                           ws), n)
-        packed = rows * (tq.record_bytes(kcb) + (4 if kind == tq.KIND_PROD else 2) + tq.record_bytes(vcb_i) + 2)
+        knorm = 8 if name.startswith("split") else 4 if kind == tq.KIND_PROD else 2
+        packed = rows * (tq.record_bytes(kcb) + knorm + tq.record_bytes(vcb_i) + 2)
         res[name] = {"ms_per_call": ms, "packed_bytes": packed, "gbs": packed / (ms / 1e3) / 1e9}
         del kc, vc_i
     return res

@@ -448,17 +448,20 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
     }
     __syncthreads();
     // a split's norm entry is written by thread 0 (group A) with group B's
-    // values taken from thread 32 kx (the first coordinate of group B)
-    if (kx && t == 32 * kx) {
-      xs[0] = nrm;
-      xs[1] = gamma;
-    }
-    __syncthreads();
-    if (kx && t == 0) {
-      nrm_x = nrm;
-      gamma_x = gamma;
-      nrm = xs[0];
-      gamma = xs[1];
+    // values taken from thread 32 kx (the first coordinate of group B); kx
+    // is the same for the whole block
+    if (kx) {
+      if (t == 32 * kx) {
+        xs[0] = nrm;
+        xs[1] = gamma;
+      }
+      __syncthreads();
+      if (t == 0) {
+        nrm_x = nrm;
+        gamma_x = gamma;
+        nrm = xs[0];
+        gamma = xs[1];
+      }
     }
     // Launched as a programmatic dependent, this CTA may have computed its
     // rows while the kernel before it (a scoring kernel reading this cache)

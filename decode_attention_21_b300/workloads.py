@@ -64,6 +64,13 @@ def llama_channel_scale(h, d=128, seed=DATA_SEED, which="keys", outlier_frac=0.0
     return s
 
 
+def layer_outlier_channels(Hkv, E, d=128, seed=DATA_SEED, which="keys"):
+    """The E channels of largest RMS scale over the layer's Hkv kv heads (a
+    caller's calibration of the channel groups for an outlier-channel split)."""
+    rms = np.sqrt(np.mean([llama_channel_scale(h, d, seed, which) ** 2 for h in range(Hkv)], axis=0))
+    return np.argsort(-rms, kind="stable")[:E].astype(np.int32)
+
+
 def llama_kv_slice(b, h, t0, t1, d=128, seed=DATA_SEED, which="keys"):
     """bf16-valued rows t0..t1-1 of sequence b, kv head h (fp32 array [t1-t0, d]).
 
