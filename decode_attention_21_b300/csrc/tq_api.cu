@@ -480,9 +480,7 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   }
   cudaDeviceGetAttribute(&cb->sms, cudaDevAttrMultiProcessorCount, cb->device);
   cb->tc_ready = false;
-  // (the tensor-core quantize normalises whole rows: a split codebook's
-  // per-group norms take the row-wise kernels)
-  if (D.mode == TQ_MODE_SCALAR && d == 128 && !dv.split) {
+  if (D.mode == TQ_MODE_SCALAR && d == 128) {
     bool good = encode_bf16_rows(&cb->tm_pihi, dv.Pi_hi, d, d) && encode_bf16_rows(&cb->tm_pilo, dv.Pi_lo, d, d);
     if (D.kind == TQ_KIND_PROD) good = good && encode_bf16_rows(&cb->tm_s, dv.S_bf, D.m, d);
     else cb->tm_s = cb->tm_pihi;

@@ -12,10 +12,11 @@
 //        S once per CTA.
 //   MMA (one thread): Y = X Pi_hi^T + X Pi_lo^T into TMEM columns 0..127
 //        (Pi = Pi_hi + Pi_lo, both bf16: fp32-accurate rotation of bf16 x).
-//   epilogue 1 (warp w: TMEM lanes 32 (w%4).., columns 32 (w/4)..): n = ||y||,
-//        codes by compare-count against the boundaries, code-plane words,
-//        residual r = y/n - yhat written to shared memory as bf16 hi + lo in
-//        the MMA's swizzled K-major layout.
+//   epilogue 1 (warp w: TMEM lanes 32 (w%4).., columns 32 (w/4)..): n = ||y||
+//        (an outlier-channel split: each group's own norm), codes by
+//        bisection over the boundaries (each level one comparison, setting
+//        that level's code-plane bit), residual r = y/n - yhat written to
+//        shared memory as bf16 hi + lo in the MMA's swizzled K-major layout.
 //   MMA: Z = R_hi S^T + R_lo S^T into TMEM columns 128..255.
 //   epilogue 2: sign words of Z, gamma = ||r||, record and fp16 norms.
 // Every wait on an mbarrier is bounded; on a timeout the kernel records an
@@ -120,8 +121,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+// Two fp32 values rounded to bf16 in one instruction: a in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// Stage-1 cell of y among the 2^L - 1 sorted boundaries: bisection, each
+// level one comparison y >= t (so the cell equals #{k : y >= t_k}); level l
+// sets bit j of w[l] (most significant bit first).  The first boundary
+// compared is t_mid (a register), the others come from shared memory.
+template <int L>
+__device__ __forceinline__ int cell_bisect(float y, float t_mid, const float* s_bnd, uint32_t* w, int j) {
+  int idx = 0;
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    const int half = 1 << (L - 1 - l);
+    const float t = l == 0 ? t_mid : s_bnd[idx + half - 1];
+    if (y >= t) {
+      idx += half;
+      w[l] |= 1u << j;
+    }
+  }
+  return idx;
 }
 
 }  // namespace
@@ -151,15 +174,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool prod = PROD;
   constexpr int NB = (1 << B1) - 1, NBX = (2 << B1) - 1;
   const int W = cb.W;
-  // stage-1 tables in registers (boundaries) and shared memory (centroids)
-  __shared__ float s_cent[16], s_centx[32];
-  float bnd[NB], bndx[EXT ? NBX : 1];
-#pragma unroll
-  for (int t = 0; t < NB; ++t) bnd[t] = cb.bound[t];
-#pragma unroll
-  for (int t = 0; t < (EXT ? NBX : 1); ++t) bndx[t] = EXT ? cb.bound_x[t] : 0.f;
-  if (tid < 16) s_cent[tid] = cb.cent[tid];
-  if (tid < 32) s_centx[tid] = cb.cent_x[tid];
+  // stage-1 tables in shared memory (the middle boundaries also in registers)
+  __shared__ float s_cent[16], s_centx[32], s_bnd[16], s_bndx[32];
+  const float t_mid = cb.bound[NB / 2], t_midx = EXT ? cb.bound_x[NBX / 2] : 0.f;
+  if (tid < 16) {
+    s_cent[tid] = cb.cent[tid];
+    s_bnd[tid] = cb.bound[tid];
+  }
+  if (tid < 32) {
+    s_centx[tid] = cb.cent_x[tid];
+    s_bndx[tid] = cb.bound_x[tid];
+  }
+  // outlier-channel split: word columns cg < kx are group A, with its own norms
+  const int kx = cb.split ? cb.extra / 32 : 0;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -243,46 +270,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
     red1[cg * kRows + m] = ss;
     __syncthreads();
-    const float tot = (red1[m] + red1[kRows + m]) + (red1[2 * kRows + m] + red1[3 * kRows + m]);
+    // the row's norm (a split: this column group's group's norm)
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tot += ((k < kx) == (cg < kx)) ? red1[k * kRows + m] : 0.f;
     const float nrm = sqrtf(tot);
     const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
-    const bool ext = EXT && (32 * cg < cb.extra);
-    uint32_t word[P];
+    const bool ext = EXT && (32 * cg < cb.extra);   // the same for the whole warp
+    // word[0..b1-1]: code planes; word[b1] (EXT columns): the extra low bit
+    uint32_t word[P + 1];
 #pragma unroll
-    for (int p = 0; p < P; ++p) word[p] = 0u;
-    uint32_t xword = 0u;
+    for (int p = 0; p <= P; ++p) word[p] = 0u;
     float gs = 0.f;
     uint32_t rh[16], rl[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float y = v[j] * inv;
-      int idx = 0;
-      float r;
-      if (EXT && ext) {
+    for (int j = 0; j < 32; j += 2) {
+      float r2[2];
 #pragma unroll
-        for (int t = 0; t < (EXT ? NBX : 1); ++t) idx += (y >= bndx[t]) ? 1 : 0;
-        r = y - s_centx[idx];
-      } else {
-#pragma unroll
-        for (int t = 0; t < NB; ++t) idx += (y >= bnd[t]) ? 1 : 0;
-        r = y - s_cent[idx];
+      for (int e = 0; e < 2; ++e) {
+        const float y = v[j + e] * inv;
+        float r;
+        if (EXT && ext) {
+          const int idx = cell_bisect<B1 + 1>(y, t_midx, s_bndx, word, j + e);
+          r = y - s_centx[idx];
+        } else {
+          const int idx = cell_bisect<B1>(y, t_mid, s_bnd, word, j + e);
+          r = y - s_cent[idx];
+        }
+        gs = fmaf(r, r, gs);
+        r2[e] = r;
       }
-      gs = fmaf(r, r, gs);
-      const int top = (EXT && ext) ? idx >> 1 : idx;
-#pragma unroll
-      for (int p = 0; p < b1; ++p) word[p] |= (uint32_t)((top >> (b1 - 1 - p)) & 1) << j;
-      if (EXT && ext) xword |= (uint32_t)(idx & 1) << j;
-      const uint32_t hb = bf16_bits(r);
-      const float hi = __uint_as_float(hb << 16);
-      const uint32_t lb = bf16_bits(r - hi);
-      if (j & 1) {
-        rh[j >> 1] |= hb << 16;
-        rl[j >> 1] |= lb << 16;
-      } else {
-        rh[j >> 1] = hb;
-        rl[j >> 1] = lb;
-      }
+      // bf16 hi + lo pieces of the residual pair
+      const uint32_t h = bf16x2(r2[0], r2[1]);
+      rh[j >> 1] = h;
+      rl[j >> 1] = bf16x2(r2[0] - __uint_as_float(h << 16), r2[1] - __uint_as_float(h & 0xFFFF0000u));
     }
+    const uint32_t xword = (EXT && ext) ? word[b1] : 0u;
     red2[cg * kRows + m] = gs;
     if (prod) {
       // residual rows into the swizzled K-major operand layout: coordinate
@@ -326,7 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tm_z + ((uint32_t)(32 * q) << 16) + 32 * cg, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) sword |= (v[j] >= 0.f ? 1u : 0u) << j;
-      gamma = sqrtf((red2[m] + red2[kRows + m]) + (red2[2 * kRows + m] + red2[3 * kRows + m]));
+      float g2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) g2 += ((k < kx) == (cg < kx)) ? red2[k * kRows + m] : 0.f;
+      gamma = sqrtf(g2);
     }
     // ---- store
     const int64_t row = tile * kRows + m;
@@ -346,10 +372,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EXT && ext) rec[(128 / 32) * P + cg] = xword;
       if (cg == 0) {
         uint8_t* norms = cache + norm_offset(cb, cache_rows);
-        if (prod)
+        if (kx) {
+          // group A's (this thread's) and group B's norms
+          float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k >= kx) {
+              t1 += red1[k * kRows + m];
+              t2 += red2[k * kRows + m];
+            }
+          __half2* e = reinterpret_cast<__half2*>(norms) + 2 * dst;
+          e[0] = __floats2half2_rn(nrm, gamma);
+          e[1] = __floats2half2_rn(sqrtf(t1), sqrtf(t2));
+        } else if (prod) {
           reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
-        else
+        } else {
           reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+        }
       }
     }
     fence_before();
