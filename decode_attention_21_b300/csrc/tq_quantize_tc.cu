@@ -33,20 +33,25 @@ namespace tq {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;                          // two groups of 8 warps
+constexpr int kStages = 3;                             // X tiles in flight
 constexpr uint32_t kBlockBytes = kRows * 128;          // 64 bf16 columns x 128 rows
 constexpr uint32_t kTileBytes = 2 * kBlockBytes;       // 128 columns
 // shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kOffX = 0;                          // 2 stages x kTileBytes (R_hi reuses the stage)
-constexpr uint32_t kOffPiHi = 2 * kTileBytes;
+constexpr uint32_t kOffX = 0;                          // kStages x kTileBytes
+constexpr uint32_t kOffPiHi = kStages * kTileBytes;
 constexpr uint32_t kOffPiLo = kOffPiHi + kTileBytes;
 constexpr uint32_t kOffS = kOffPiLo + kTileBytes;
-constexpr uint32_t kOffRlo = kOffS + kTileBytes;
-constexpr uint32_t kOffRed = kOffRlo + kTileBytes;     // float red1[4][128], red2[4][128]
-constexpr uint32_t kOffBar = kOffRed + 2 * 4 * kRows * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + alignment slack
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kOffRed = kOffS + kTileBytes;       // float red1[2][4][128], red2[2][4][128]
+constexpr uint32_t kOffBar = kOffRed + 2 * 2 * 4 * kRows * 4;
+// mbarriers: full[kStages], const, y[2], z[2]; then the TMEM base and the
+// per-stage counts of issued and consumed loads
+constexpr uint32_t kOffTmem = kOffBar + 8 * (kStages + 5);
+constexpr uint32_t kOffCnt = kOffTmem + 8;
+constexpr uint32_t kSmemBytes = kOffCnt + 8 * kStages + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 512;                    // per group: Y / Z 128, R_hi 64, R_lo 64
 constexpr long long kSpinLimit = 1ll << 26;
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 // kind::f16 instruction descriptor: D = F32, A = B = BF16, both K-major,
 // N = 128, M = 128.
@@ -118,6 +123,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// A from tensor memory (lane = row, two bf16 per 32-bit column along K).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Named barrier of one 8-warp tile group (ids 1, 2; id 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int g) { asm volatile("bar.sync %0, 256;" ::"r"(1 + g) : "memory"); }
+
+// The same barrier, returning whether v holds in every thread of the group.
+__device__ __forceinline__ bool group_and(int g, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred q, %2, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + g)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -162,13 +198,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q = warp & 3, cg = warp >> 2;
+  const int g = warp >> 3;                           // tile group: local tiles g, g + 2, ...
+  const bool leader = (tid & 255) == 0;              // the group's MMA and TMA issuer
+  const int q = warp & 3;                            // TMEM lane quarter
+  const int wh = (warp >> 2) & 1;                    // column groups 2 wh, 2 wh + 1
   const int m = 32 * q + lane;                       // tile row = TMEM lane
-  float* red1 = reinterpret_cast<float*>(smem + kOffRed);
-  float* red2 = red1 + 4 * kRows;
-  const uint32_t bar_full0 = sbase + kOffBar, bar_const = bar_full0 + 16, bar_mma1 = bar_full0 + 24,
-                 bar_mma2 = bar_full0 + 32;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 48);
+  float* red1 = reinterpret_cast<float*>(smem + kOffRed) + g * 4 * kRows;
+  float* red2 = reinterpret_cast<float*>(smem + kOffRed) + (2 + g) * 4 * kRows;
+  const uint32_t bar0 = sbase + kOffBar;
+  auto bar_full = [&](int st) { return bar0 + 8u * st; };
+  const uint32_t bar_const = bar0 + 8u * kStages;
+  const uint32_t bar_y = bar0 + 8u * (kStages + 1 + g), bar_z = bar0 + 8u * (kStages + 3 + g);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  int* n_issued = reinterpret_cast<int*>(smem + kOffCnt);        // loads issued into each stage
+  int* n_taken = n_issued + kStages;                              // loads waited for
   const int64_t ntiles = (n + kRows - 1) / kRows;
   constexpr int b1 = B1, P = B1 + (PROD ? 1 : 0);
   constexpr bool prod = PROD;
@@ -194,22 +237,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    mbar_init(bar_full0, 1);
-    mbar_init(bar_full0 + 8, 1);
-    mbar_init(bar_const, 1);
-    mbar_init(bar_mma1, 1);
-    mbar_init(bar_mma2, 1);
+    for (int k = 0; k < kStages + 5; ++k) mbar_init(bar0 + 8u * k, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (tid < 2 * kStages) n_issued[tid] = 0;
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_y = tmem, tm_z = tmem + 128;
+  const uint32_t tg = tmem + 256u * g;               // Y, then Z: columns +0..127
+  const uint32_t t_rhi = tg + 128, t_rlo = tg + 192; // residual operand (bf16 pairs)
+  const uint32_t lane_off = (uint32_t)(32 * q) << 16;
 
-  bool ok = true;
-  int pending_stage = -1;  // stage with a TMA load in flight that nobody waited for
-  const int64_t first = blockIdx.x;
+  // local tile it of this CTA is tile blockIdx.x + it * gridDim.x, staged in
+  // X stage it % kStages; its load is issued by the prologue (it < kStages)
+  // or by the group that ran tile it - kStages, once that tile's rotation
+  // has consumed the stage
+  const int64_t first = blockIdx.x, step = gridDim.x;
+  auto load_x = [&](int64_t it) {
+    const int st = (int)(it % kStages);
+    const uint32_t dst = sbase + kOffX + st * kTileBytes;
+    mbar_expect_tx(bar_full(st), kTileBytes);
+    for (int kb = 0; kb < 2; ++kb)
+      tma_load_2d(dst + kb * kBlockBytes, &tm_x, 64 * kb, (int)((first + it * step) * kRows), bar_full(st));
+    atomicAdd(&n_issued[st], 1);
+  };
   if (tid == 0 && first < ntiles) {
     mbar_expect_tx(bar_const, (prod ? 3 : 2) * kTileBytes);
     for (int kb = 0; kb < 2; ++kb) {
@@ -217,163 +269,174 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sbase + kOffPiLo + kb * kBlockBytes, &tm_pilo, 64 * kb, 0, bar_const);
       if (prod) tma_load_2d(sbase + kOffS + kb * kBlockBytes, &tm_s, 64 * kb, 0, bar_const);
     }
-    mbar_expect_tx(bar_full0, kTileBytes);
-    for (int kb = 0; kb < 2; ++kb)
-      tma_load_2d(sbase + kOffX + kb * kBlockBytes, &tm_x, 64 * kb, (int)(first * kRows), bar_full0);
+    for (int it = 0; it < kStages && first + it * step < ntiles; ++it) load_x(it);
   }
-  if (first < ntiles) pending_stage = 0;
+  bool ok = true;
   bool const_pending = first < ntiles;   // Pi / S loads not yet waited for
   if (first < ntiles) ok = __syncthreads_and(mbar_wait(bar_const, 0, cb.first_wait)) != 0;
   if (ok) const_pending = false;
-  // commits of the two MMA groups not yet waited for (drained on a timeout)
-  bool pend1 = false, pend2 = false;
+  // this group's MMA commits not yet waited for (drained on a timeout)
+  bool pend_y = false, pend_z = false;
+  int j = 0;                              // this group's tile count (mbarrier phases)
 
-  int it = 0;
-  for (int64_t tile = first; tile < ntiles && ok; tile += gridDim.x, ++it) {
-    const int s = it & 1;
-    const uint32_t xs = sbase + kOffX + s * kTileBytes;
-    const int64_t next = tile + gridDim.x;
-    if (tid == 0 && next < ntiles) {
-      const uint32_t xn = sbase + kOffX + (s ^ 1) * kTileBytes;
-      mbar_expect_tx(bar_full0 + 8 * (s ^ 1), kTileBytes);
-      for (int kb = 0; kb < 2; ++kb) tma_load_2d(xn + kb * kBlockBytes, &tm_x, 64 * kb, (int)(next * kRows), bar_full0 + 8 * (s ^ 1));
-    }
-    // ---- rotation on the tensor cores
-    if (!__syncthreads_and(mbar_wait(bar_full0 + 8 * s, (it >> 1) & 1))) {
-      ok = false;
-      break;
-    }
-    pending_stage = next < ntiles ? (s ^ 1) : -1;
-    if (tid == 0) {
-      fence_after();
-      for (int kb = 0; kb < 2; ++kb)
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tm_y, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffPiHi + kb * kBlockBytes + 32 * ks),
-                   (kb | ks) != 0);
-      for (int kb = 0; kb < 2; ++kb)
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tm_y, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffPiLo + kb * kBlockBytes + 32 * ks), 1);
-      mma_commit(bar_mma1);
-    }
-    pend1 = true;
-    if (!__syncthreads_and(mbar_wait(bar_mma1, it & 1))) {
-      ok = false;
-      break;
-    }
-    pend1 = false;
-    fence_after();
-    // ---- epilogue 1: norm, codes, residual
-    float v[32];
-    tmem_ld32(tm_y + ((uint32_t)(32 * q) << 16) + 32 * cg, v);
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
-    red1[cg * kRows + m] = ss;
-    __syncthreads();
-    // the row's norm (a split: this column group's group's norm)
-    float tot = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) tot += ((k < kx) == (cg < kx)) ? red1[k * kRows + m] : 0.f;
-    const float nrm = sqrtf(tot);
-    const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
-    const bool ext = EXT && (32 * cg < cb.extra);   // the same for the whole warp
-    // word[0..b1-1]: code planes; word[b1] (EXT columns): the extra low bit
-    uint32_t word[P + 1];
-#pragma unroll
-    for (int p = 0; p <= P; ++p) word[p] = 0u;
-    float gs = 0.f;
-    uint32_t rh[16], rl[16];
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      float r2[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float y = v[j + e] * inv;
-        float r;
-        if (EXT && ext) {
-          const int idx = cell_bisect<B1 + 1>(y, t_midx, s_bndx, word, j + e);
-          r = y - s_centx[idx];
-        } else {
-          const int idx = cell_bisect<B1>(y, t_mid, s_bnd, word, j + e);
-          r = y - s_cent[idx];
-        }
-        gs = fmaf(r, r, gs);
-        r2[e] = r;
-      }
-      // bf16 hi + lo pieces of the residual pair
-      const uint32_t h = bf16x2(r2[0], r2[1]);
-      rh[j >> 1] = h;
-      rl[j >> 1] = bf16x2(r2[0] - __uint_as_float(h << 16), r2[1] - __uint_as_float(h & 0xFFFF0000u));
-    }
-    const uint32_t xword = (EXT && ext) ? word[b1] : 0u;
-    red2[cg * kRows + m] = gs;
-    if (prod) {
-      // residual rows into the swizzled K-major operand layout: coordinate
-      // block cg/2, 16-byte chunks (cg%2)*4 + c at chunk position ^ (m % 8)
-      const uint32_t blk = (uint32_t)(cg >> 1) * kBlockBytes + (uint32_t)m * 128;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const uint32_t chunk = (uint32_t)(((cg & 1) * 4 + c4) ^ (m & 7)) * 16;
-        uint8_t* ph = smem + (xs - sbase) + blk + chunk;
-        uint8_t* pl = smem + kOffRlo + blk + chunk;
-        *reinterpret_cast<uint4*>(ph) = make_uint4(rh[4 * c4], rh[4 * c4 + 1], rh[4 * c4 + 2], rh[4 * c4 + 3]);
-        *reinterpret_cast<uint4*>(pl) = make_uint4(rl[4 * c4], rl[4 * c4 + 1], rl[4 * c4 + 2], rl[4 * c4 + 3]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    fence_before();
-    __syncthreads();
-    // ---- QJL projection on the tensor cores
-    uint32_t sword = 0u;
-    float gamma = 0.f;
-    if (prod) {
-      if (tid == 0) {
+  for (int64_t it = g; ok && first + it * step < ntiles; it += 2, ++j) {
+    const int64_t tile = first + it * step;
+    const int st = (int)(it % kStages);
+    const uint32_t xs = sbase + kOffX + st * kTileBytes;
+    // ---- rotation on the tensor cores: Y = X Pi_hi^T + X Pi_lo^T
+    bool good = true;
+    if (leader) {
+      good = mbar_wait(bar_full(st), (uint32_t)((it / kStages) & 1));
+      if (good) {
+        atomicAdd(&n_taken[st], 1);
         fence_after();
         for (int kb = 0; kb < 2; ++kb)
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tm_z, sw128_desc(xs + kb * kBlockBytes + 32 * ks), sw128_desc(sbase + kOffS + kb * kBlockBytes + 32 * ks),
-                     (kb | ks) != 0);
+            mma_bf16(tg, sw128_desc(xs + kb * kBlockBytes + 32 * ks),
+                     sw128_desc(sbase + kOffPiHi + kb * kBlockBytes + 32 * ks), (kb | ks) != 0);
         for (int kb = 0; kb < 2; ++kb)
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tm_z, sw128_desc(sbase + kOffRlo + kb * kBlockBytes + 32 * ks),
-                     sw128_desc(sbase + kOffS + kb * kBlockBytes + 32 * ks), 1);
-        mma_commit(bar_mma2);
+            mma_bf16(tg, sw128_desc(xs + kb * kBlockBytes + 32 * ks),
+                     sw128_desc(sbase + kOffPiLo + kb * kBlockBytes + 32 * ks), 1);
+        mma_commit(bar_y);
       }
-      pend2 = true;
-      if (!__syncthreads_and(mbar_wait(bar_mma2, it & 1))) {
+    }
+    if (!group_and(g, good)) {
+      ok = false;
+      break;
+    }
+    pend_y = true;
+    if (!group_and(g, mbar_wait(bar_y, j & 1))) {
+      ok = false;
+      break;
+    }
+    pend_y = false;
+    fence_after();
+    // the stage is consumed: fetch local tile it + kStages into it
+    if (leader && first + (it + kStages) * step < ntiles) load_x(it + kStages);
+
+    // ---- epilogue 1: norms (pass 1), codes and the residual operand (pass 2)
+    float v[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cg = 2 * wh + h;
+      tmem_ld32(tg + lane_off + 32 * cg, v);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ss = fmaf(v[e], v[e], ss);
+      red1[cg * kRows + m] = ss;
+    }
+    group_sync(g);
+    uint32_t words[2][P + 1];   // per column group: code planes, then the extra low bit (EXT columns)
+    float nrm0 = 0.f;           // column group 2 wh's norm (the norm entry's writer uses it)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cg = 2 * wh + h;
+      float tot = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tot += ((k < kx) == (cg < kx)) ? red1[k * kRows + m] : 0.f;
+      const float nrm = sqrtf(tot);
+      if (h == 0) nrm0 = nrm;
+      const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
+      const bool ext = EXT && (32 * cg < cb.extra);   // the same for the whole warp
+      uint32_t* word = words[h];
+#pragma unroll
+      for (int p = 0; p <= P; ++p) word[p] = 0u;
+      tmem_ld32(tg + lane_off + 32 * cg, v);
+      float gs = 0.f;
+      uint32_t rh[16], rl[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float r2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float y = v[e + u] * inv;
+          float r;
+          if (EXT && ext) {
+            const int idx = cell_bisect<B1 + 1>(y, t_midx, s_bndx, word, e + u);
+            r = y - s_centx[idx];
+          } else {
+            const int idx = cell_bisect<B1>(y, t_mid, s_bnd, word, e + u);
+            r = y - s_cent[idx];
+          }
+          gs = fmaf(r, r, gs);
+          r2[u] = r;
+        }
+        // bf16 hi + lo pieces of the residual pair
+        const uint32_t hb = bf16x2(r2[0], r2[1]);
+        rh[e >> 1] = hb;
+        rl[e >> 1] = bf16x2(r2[0] - __uint_as_float(hb << 16), r2[1] - __uint_as_float(hb & 0xFFFF0000u));
+      }
+      red2[cg * kRows + m] = gs;
+      if (prod) {
+        // A operand of the sketch in tensor memory: lane = row, column
+        // 16 cg + i holds coordinates 32 cg + 2i (low half) and 2i + 1
+        tmem_st16(t_rhi + lane_off + 16 * cg, rh);
+        tmem_st16(t_rlo + lane_off + 16 * cg, rl);
+      }
+    }
+    if (prod) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    fence_before();
+    group_sync(g);
+    // ---- QJL projection on the tensor cores: Z = R_hi S^T + R_lo S^T (into
+    // the columns of Y, which every thread of the group has read)
+    uint32_t sword[2] = {0u, 0u};
+    float gam[2] = {0.f, 0.f};
+    if (prod) {
+      if (leader) {
+        fence_after();
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_ta(tg, t_rhi + 8 * ks, sw128_desc(sbase + kOffS + (ks >> 2) * kBlockBytes + 32 * (ks & 3)),
+                      ks != 0);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_ta(tg, t_rlo + 8 * ks, sw128_desc(sbase + kOffS + (ks >> 2) * kBlockBytes + 32 * (ks & 3)), 1);
+        mma_commit(bar_z);
+      }
+      pend_z = true;
+      if (!group_and(g, mbar_wait(bar_z, j & 1))) {
         ok = false;
         break;
       }
-      pend2 = false;
+      pend_z = false;
       fence_after();
-      tmem_ld32(tm_z + ((uint32_t)(32 * q) << 16) + 32 * cg, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) sword |= (v[j] >= 0.f ? 1u : 0u) << j;
-      float g2 = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        const int cg = 2 * wh + h;
+        tmem_ld32(tg + lane_off + 32 * cg, v);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) g2 += ((k < kx) == (cg < kx)) ? red2[k * kRows + m] : 0.f;
-      gamma = sqrtf(g2);
+        for (int e = 0; e < 32; ++e) sword[h] |= (v[e] >= 0.f ? 1u : 0u) << e;
+        float g2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) g2 += ((k < kx) == (cg < kx)) ? red2[k * kRows + m] : 0.f;
+        gam[h] = sqrtf(g2);
+      }
     }
     // ---- store
     const int64_t row = tile * kRows + m;
     const int64_t dst = row < n ? (dst_rows ? dst_rows[row] : row) : -1;
-    if (row < n && (dst < 0 || dst >= cache_rows) && cg == 0) atomicOr(status, kBadRow);  // skipped
+    if (row < n && (dst < 0 || dst >= cache_rows) && wh == 0) atomicOr(status, kBadRow);  // skipped
     if (dst >= 0 && dst < cache_rows) {
       uint32_t* rec = reinterpret_cast<uint32_t*>(cache) + dst * W;
-      if constexpr (PROD) word[b1] = sword;
-      if constexpr (P == 4 && !EXT) {
-        *reinterpret_cast<uint4*>(rec + cg * P) = make_uint4(word[0], word[1], word[2], word[3]);
-      } else if constexpr (P == 2 && !EXT) {
-        *reinterpret_cast<uint2*>(rec + cg * P) = make_uint2(word[0], word[1]);
-      } else {
 #pragma unroll
-        for (int p = 0; p < P; ++p) rec[cg * P + p] = word[p];
+      for (int h = 0; h < 2; ++h) {
+        const int cg = 2 * wh + h;
+        const bool ext = EXT && (32 * cg < cb.extra);
+        const uint32_t xword = ext ? words[h][b1] : 0u;
+        if constexpr (PROD) words[h][b1] = sword[h];
+        if constexpr (P == 4 && !EXT) {
+          *reinterpret_cast<uint4*>(rec + cg * P) = make_uint4(words[h][0], words[h][1], words[h][2], words[h][3]);
+        } else if constexpr (P == 2 && !EXT) {
+          *reinterpret_cast<uint2*>(rec + cg * P) = make_uint2(words[h][0], words[h][1]);
+        } else {
+#pragma unroll
+          for (int p = 0; p < P; ++p) rec[cg * P + p] = words[h][p];
+        }
+        if (EXT && ext) rec[(128 / 32) * P + cg] = xword;
       }
-      if (EXT && ext) rec[(128 / 32) * P + cg] = xword;
-      if (cg == 0) {
+      if (wh == 0) {
         uint8_t* norms = cache + norm_offset(cb, cache_rows);
         if (kx) {
-          // group A's (this thread's) and group B's norms
+          // group A's (column group 0) and group B's norms
           float t1 = 0.f, t2 = 0.f;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -382,28 +445,34 @@ __global__ void __launch_bounds__(kThreads, 1)
               t2 += red2[k * kRows + m];
             }
           __half2* e = reinterpret_cast<__half2*>(norms) + 2 * dst;
-          e[0] = __floats2half2_rn(nrm, gamma);
+          e[0] = __floats2half2_rn(nrm0, gam[0]);
           e[1] = __floats2half2_rn(sqrtf(t1), sqrtf(t2));
         } else if (prod) {
-          reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
+          reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm0, gam[0]);
         } else {
-          reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+          reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm0);
         }
       }
     }
+    // every thread of the group has read Z (and its red entries) before the
+    // group's next rotation overwrites them
     fence_before();
-    __syncthreads();
-    fence_after();
+    group_sync(g);
   }
   if (!ok) {
     if (tid == 0) atomicOr(status, 1);
-    // let our own copies and MMAs drain (bounded waits) before freeing TMEM
-    if (const_pending) mbar_wait(bar_const, 0);
-    if (pending_stage >= 0) mbar_wait(bar_full0 + 8 * pending_stage, ((it + 1) >> 1) & 1);
-    if (pend1) mbar_wait(bar_mma1, it & 1);
-    if (pend2) mbar_wait(bar_mma2, it & 1);
+    // this group's own MMAs in flight finish (bounded waits)
+    if (leader && pend_y) mbar_wait(bar_y, j & 1);
+    if (leader && pend_z) mbar_wait(bar_z, j & 1);
   }
+  // every load issued lands (bounded) before the shared memory is released
   fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    if (const_pending) mbar_wait(bar_const, 0);
+    for (int st = 0; st < kStages; ++st)
+      for (int k = n_taken[st]; k < n_issued[st]; ++k) mbar_wait(bar_full(st), (uint32_t)(k & 1));
+  }
   __syncthreads();
   if (warp == 0) {
     fence_after();
