@@ -131,13 +131,22 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b), "r"(kIdesc), "r"(acc));
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 
 // Named barrier of one 8-warp tile group (ids 1, 2; id 0 is __syncthreads).
@@ -164,23 +173,47 @@ __device__ __forceinline__ uint32_t bf16x2(float a, float b) {
   return r;
 }
 
-// Stage-1 cell of y among the 2^L - 1 sorted boundaries: bisection, each
-// level one comparison y >= t (so the cell equals #{k : y >= t_k}); level l
-// sets bit j of w[l] (most significant bit first).  The first boundary
-// compared is t_mid (a register), the others come from shared memory.
+// Stage-1 cell of y among the 2^L - 1 sorted boundaries b: bisection, each
+// level one comparison y >= t (so the cell equals #{k : y >= b_k}); level l
+// sets bit j of w[l] (most significant bit first).  lt holds the boundaries
+// of the first levels in heap order (lt[0] = b[2^(L-1) - 1], then each
+// level's candidates left to right).
 template <int L>
-__device__ __forceinline__ int cell_bisect(float y, float t_mid, const float* s_bnd, uint32_t* w, int j) {
-  int idx = 0;
+__device__ __forceinline__ int cell_heap(float y, const float (&lt)[7], const float* s_bnd, uint32_t* w, int j) {
+  if constexpr (L <= 2) {
+    // one or two levels: the boundaries from registers
+    const bool p0 = y >= lt[0];
+    if (p0) w[0] |= 1u << j;
+    if constexpr (L == 1) return p0 ? 1 : 0;
+    const bool p1 = y >= (p0 ? lt[2] : lt[1]);
+    if (p1) w[1] |= 1u << j;
+    return (p0 ? 2 : 0) | (p1 ? 1 : 0);
+  } else {
+    // deeper tables: the first level from a register, the others from shared
+    // memory (a register select tree was measured slower here)
+    int idx = 0;
 #pragma unroll
-  for (int l = 0; l < L; ++l) {
-    const int half = 1 << (L - 1 - l);
-    const float t = l == 0 ? t_mid : s_bnd[idx + half - 1];
-    if (y >= t) {
-      idx += half;
-      w[l] |= 1u << j;
+    for (int l = 0; l < L; ++l) {
+      const int half = 1 << (L - 1 - l);
+      const float t = l == 0 ? lt[0] : s_bnd[idx + half - 1];
+      if (y >= t) {
+        idx += half;
+        w[l] |= 1u << j;
+      }
     }
+    return idx;
   }
-  return idx;
+}
+
+// Heap-ordered boundaries of the first three bisection levels of a 2^L-cell
+// table (node n at level l, position k: boundary (2k + 1) 2^(L-1-l) - 1).
+template <int L>
+__device__ __forceinline__ void heap_levels(const float* bnd, float (&lt)[7]) {
+#pragma unroll
+  for (int nd = 0; nd < 7; ++nd) {
+    const int l = nd == 0 ? 0 : nd < 3 ? 1 : 2, k = nd - ((1 << l) - 1);
+    lt[nd] = l < L ? bnd[(2 * k + 1) * (1 << (L - 1 - l)) - 1] : 0.f;
+  }
 }
 
 }  // namespace
@@ -215,11 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t ntiles = (n + kRows - 1) / kRows;
   constexpr int b1 = B1, P = B1 + (PROD ? 1 : 0);
   constexpr bool prod = PROD;
-  constexpr int NB = (1 << B1) - 1, NBX = (2 << B1) - 1;
   const int W = cb.W;
   // stage-1 tables in shared memory (the middle boundaries also in registers)
   __shared__ float s_cent[16], s_centx[32], s_bnd[16], s_bndx[32];
-  const float t_mid = cb.bound[NB / 2], t_midx = EXT ? cb.bound_x[NBX / 2] : 0.f;
+  float lt[7], ltx[7];
+  heap_levels<B1>(cb.bound, lt);
+  heap_levels<EXT ? B1 + 1 : 1>(cb.bound_x, ltx);
   if (tid < 16) {
     s_cent[tid] = cb.cent[tid];
     s_bnd[tid] = cb.bound[tid];
@@ -316,10 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (leader && first + (it + kStages) * step < ntiles) load_x(it + kStages);
 
     // ---- epilogue 1: norms (pass 1), codes and the residual operand (pass 2)
-    float v[32];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int cg = 2 * wh + h;
+      float v[32];
       tmem_ld32(tg + lane_off + 32 * cg, v);
       float ss = 0.f;
 #pragma unroll
@@ -342,38 +376,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t* word = words[h];
 #pragma unroll
       for (int p = 0; p <= P; ++p) word[p] = 0u;
-      tmem_ld32(tg + lane_off + 32 * cg, v);
       float gs = 0.f;
-      uint32_t rh[16], rl[16];
+      // two halves of 16 coordinates: fewer live registers
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float r2[2];
+      for (int half = 0; half < 2; ++half) {
+        float v[16];
+        tmem_ld16(tg + lane_off + 32 * cg + 16 * half, v);
+        uint32_t rh[8], rl[8];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float y = v[e + u] * inv;
-          float r;
-          if (EXT && ext) {
-            const int idx = cell_bisect<B1 + 1>(y, t_midx, s_bndx, word, e + u);
-            r = y - s_centx[idx];
-          } else {
-            const int idx = cell_bisect<B1>(y, t_mid, s_bnd, word, e + u);
-            r = y - s_cent[idx];
+        for (int e = 0; e < 16; e += 2) {
+          float r2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float y = v[e + u] * inv;
+            const int jb = 16 * half + e + u;       // bit of the column group's words
+            float r;
+            if (EXT && ext) {
+              const int idx = cell_heap<B1 + 1>(y, ltx, s_bndx, word, jb);
+              r = y - s_centx[idx];
+            } else {
+              const int idx = cell_heap<B1>(y, lt, s_bnd, word, jb);
+              r = y - s_cent[idx];
+            }
+            gs = fmaf(r, r, gs);
+            r2[u] = r;
           }
-          gs = fmaf(r, r, gs);
-          r2[u] = r;
+          // bf16 hi + lo pieces of the residual pair
+          const uint32_t hb = bf16x2(r2[0], r2[1]);
+          rh[e >> 1] = hb;
+          rl[e >> 1] = bf16x2(r2[0] - __uint_as_float(hb << 16), r2[1] - __uint_as_float(hb & 0xFFFF0000u));
         }
-        // bf16 hi + lo pieces of the residual pair
-        const uint32_t hb = bf16x2(r2[0], r2[1]);
-        rh[e >> 1] = hb;
-        rl[e >> 1] = bf16x2(r2[0] - __uint_as_float(hb << 16), r2[1] - __uint_as_float(hb & 0xFFFF0000u));
+        if (prod) {
+          // A operand of the sketch in tensor memory: lane = row, column
+          // 16 cg + i holds coordinates 32 cg + 2i (low half) and 2i + 1
+          tmem_st8(t_rhi + lane_off + 16 * cg + 8 * half, rh);
+          tmem_st8(t_rlo + lane_off + 16 * cg + 8 * half, rl);
+        }
       }
       red2[cg * kRows + m] = gs;
-      if (prod) {
-        // A operand of the sketch in tensor memory: lane = row, column
-        // 16 cg + i holds coordinates 32 cg + 2i (low half) and 2i + 1
-        tmem_st16(t_rhi + lane_off + 16 * cg, rh);
-        tmem_st16(t_rlo + lane_off + 16 * cg, rl);
-      }
     }
     if (prod) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     fence_before();
@@ -402,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int cg = 2 * wh + h;
+        float v[32];
         tmem_ld32(tg + lane_off + 32 * cg, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) sword[h] |= (v[e] >= 0.f ? 1u : 0u) << e;
