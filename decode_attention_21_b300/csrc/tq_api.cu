@@ -73,12 +73,13 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 row-major [rows, cols] matrix, 128-byte swizzled boxes of 64 columns x 128 rows.
-bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t cols) {
+// Row-major bf16 matrix, tiles of 64 columns x box_rows rows, 128-byte swizzle.
+bool encode_bf16_rows(CUtensorMap* tm, const void* base, int64_t rows, int64_t cols, uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t es[2] = {1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -480,9 +481,12 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   }
   cudaDeviceGetAttribute(&cb->sms, cudaDevAttrMultiProcessorCount, cb->device);
   cb->tc_ready = false;
-  if (D.mode == TQ_MODE_SCALAR && d == 128) {
-    bool good = encode_bf16_rows(&cb->tm_pihi, dv.Pi_hi, d, d) && encode_bf16_rows(&cb->tm_pilo, dv.Pi_lo, d, d);
-    if (D.kind == TQ_KIND_PROD) good = good && encode_bf16_rows(&cb->tm_s, dv.S_bf, D.m, d);
+  // tensor maps of Pi_hi, Pi_lo and S for the tensor-core quantize kernels:
+  // 64-column blocks of all d rows (d = 128: with extra-bit coordinates too;
+  // d = 256: without)
+  if (D.mode == TQ_MODE_SCALAR && (d == 128 || D.extra == 0)) {
+    bool good = encode_bf16_rows(&cb->tm_pihi, dv.Pi_hi, d, d, d) && encode_bf16_rows(&cb->tm_pilo, dv.Pi_lo, d, d, d);
+    if (D.kind == TQ_KIND_PROD) good = good && encode_bf16_rows(&cb->tm_s, dv.S_bf, D.m, d, d);
     else cb->tm_s = cb->tm_pihi;
     cb->tc_ready = good;
   }
@@ -557,9 +561,15 @@ static tq_status quantize_common(const char* what, const tq_codebook* cb, void* 
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // bf16 batches in scalar mode: tensor-core rotation and sketch
-  if (!paged && !y && x_dtype == TQ_BF16 && cb->tc_ready && n >= 2048 && d_in % 8 == 0 && aligned16(x) &&
-      n < (1ll << 31)) {
+  // d = 256 batches (bf16 or fp32) in scalar mode: tensor-core rotation and sketch
+  if (!paged && !y && cb->dev.d == 256 && cb->tc_ready && n >= 2048 && d_in % (x_dtype == TQ_BF16 ? 8 : 4) == 0 &&
+      aligned16(x) && n < (1ll << 31))
+    return launched(what, tq::launch_quantize_tc256(cb->tm_pihi, cb->tm_pilo, cb->tm_s, cb->dev,
+                                                    static_cast<uint8_t*>(cache), cache_rows, x, x_dtype == TQ_F32,
+                                                    n, d_in, dst_rows, cb->d_status, cb->sms, s));
+  // d = 128 bf16 batches in scalar mode: tensor-core rotation and sketch
+  if (!paged && !y && cb->dev.d == 128 && x_dtype == TQ_BF16 && cb->tc_ready && n >= 2048 && d_in % 8 == 0 &&
+      aligned16(x) && n < (1ll << 31)) {
     CUtensorMap tm_x;
     if (encode_bf16_rows(&tm_x, x, n, d_in))
       return launched(what, tq::launch_quantize_tc(tm_x, cb->tm_pihi, cb->tm_pilo, cb->tm_s, cb->dev,
