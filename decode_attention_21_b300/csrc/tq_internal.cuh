@@ -153,9 +153,9 @@ cudaError_t launch_advance_lengths(int32_t* seq_lens, int B, int32_t delta, cuda
 cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
                                const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
                                const int64_t* dst_rows, int* status, int sms, cudaStream_t s);
-cudaError_t launch_quantize_tc256(const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo, const CUtensorMap& tm_s,
-                                  const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, bool f32,
-                                  int64_t n, int d_in, const int64_t* dst_rows, int* status, int sms, cudaStream_t s);
+cudaError_t launch_quantize_tcx(const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo, const CUtensorMap& tm_s,
+                                const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, bool f32, int64_t n,
+                                int d_in, const int64_t* dst_rows, int* status, int sms, cudaStream_t s);
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s);
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,

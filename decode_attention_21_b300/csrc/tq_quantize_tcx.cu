@@ -1,6 +1,8 @@
-// Batch compression of d = 256 vectors on the 5th-generation tensor cores:
-// the search database (rows of 200 coordinates zero-padded to 256, fp32 or
-// bf16) and any other scalar-mode codebook of that width.
+// Batch compression on the 5th-generation tensor cores with the A operands
+// (X, then the residual) in tensor memory: d = 256 vectors (the search
+// database: rows of 200 coordinates zero-padded to 256, fp32 or bf16), and
+// d = 128 fp32 vectors (bf16 ones take the two-group kernel of
+// tq_quantize_tc.cu).
 //
 // [xujun] note-189244, 常见问题 (vector search over a compressed database);
 // [suzuke] "TurboQuant: compressing AI consciousness", 技術上怎麼做到的:
@@ -9,20 +11,20 @@
 //
 // One CTA per SM (16 warps) walks 128-row tiles.  Per tile:
 //   * the warps load their rows of X straight from global memory (thread:
-//     row 32 (w % 4) + lane, coordinates 64 (w / 4) .. + 63; the CTA's next
+//     row 32 (w % 4) + lane, coordinates d/4 (w / 4) .. + d/4 - 1; the CTA's next
 //     tile is prefetched into L2 by one bulk prefetch), split each value
 //     into bf16 hi + lo and store the pairs to tensor memory: the A operand;
 //   * thread 0 issues the rotation Y = X_hi Pi_hi^T + X_hi Pi_lo^T (+ X_lo
-//     Pi_hi^T for fp32 input) as M128 N256 K16 MMAs.  Pi_hi, Pi_lo (and S for
-//     the sketch) stream through a ring of four 32 KB shared-memory slots, one
-//     64-wide K block of one matrix per slot (TMA, 128-byte swizzle), in a
-//     fixed order the loads and the MMAs both follow;
+//     Pi_hi^T for fp32 input) as M128 N(d) K16 MMAs.  Pi_hi, Pi_lo (and S for
+//     the sketch) stream through a ring of four shared-memory slots, one
+//     64-wide K block of one matrix per slot (d x 64 bf16: TMA, 128-byte
+//     swizzle), in a fixed order the loads and the MMAs both follow;
 //   * epilogue 1: norms, stage-1 cells (bisection), residual r = y/n - yhat
 //     as bf16 hi + lo into the tensor-memory columns X used;
 //   * thread 0 issues the sketch Z = R_hi S^T + R_lo S^T into the columns of Y;
 //   * epilogue 2: sign words of Z, gamma = ||r||, record and fp16 norms.
-// TMEM: Y / Z in columns 0..255, X and then R (bf16 pairs, coordinate k in
-// column k / 2) in 256..383 (hi) and 384..511 (lo).
+// TMEM: Y / Z in columns 0..d-1, X and then R (bf16 pairs, coordinate k in
+// column k / 2) from column 256 (hi) and 384 (lo).
 // Every wait is bounded; on a timeout the kernel records an error, waits
 // (bounded) for its own copies and MMAs, frees its TMEM and returns.
 #include <cuda.h>
@@ -41,27 +43,31 @@ using namespace tc;
 constexpr int kRows = 128;
 constexpr int kThreads = 512;
 constexpr int kSlots = 4;                                // ring of B-operand K blocks
-constexpr uint32_t kSlotBytes = 256 * 128;               // 256 rows (N) x 64 bf16 (K)
-constexpr uint32_t kOffRing = 0;
-constexpr uint32_t kOffRed = kSlots * kSlotBytes;        // float red1[8][128], red2[8][128]
-constexpr uint32_t kOffBar = kOffRed + 2 * 8 * kRows * 4;
-// mbarriers: full[kSlots], empty[kSlots], y, z; then the TMEM base
-constexpr uint32_t kOffTmem = kOffBar + 8 * (2 * kSlots + 2);
-constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;    // + alignment slack
+// shared memory map per width: ring of d x 64 bf16 slots, then float
+// red1[d/32][128], red2[4][128], the mbarriers full[kSlots], empty[kSlots],
+// y, z, and the TMEM base
+template <int D>
+struct Map {
+  static constexpr uint32_t kSlotBytes = D * 128;
+  static constexpr uint32_t kOffRing = 0;
+  static constexpr uint32_t kOffRed = kSlots * kSlotBytes;
+  static constexpr uint32_t kOffBar = kOffRed + (D / 32 + 4) * kRows * 4;
+  static constexpr uint32_t kOffTmem = kOffBar + 8 * (2 * kSlots + 2);
+  static constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;    // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdesc = idesc_bf16(256);
-static_assert(kSmemBytes <= 232448, "shared memory");
 
-// Loads of one tile, in ring order: Pi_hi and Pi_lo of K blocks 0..3
-// (interleaved), then S of K blocks 0..3 (PROD only).
-template <bool PROD>
-__host__ __device__ constexpr int loads_per_tile() { return PROD ? 12 : 8; }
+// Loads of one tile, in ring order: Pi_hi and Pi_lo of the d/64 K blocks
+// (interleaved), then S of the K blocks (PROD only).
+template <int D, bool PROD>
+__host__ __device__ constexpr int loads_per_tile() { return (PROD ? 3 : 2) * (D / 64); }
 
 }  // namespace
 
-template <int B1, bool PROD, bool F32>
+template <int D, int B1, bool PROD, bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_quantize_tc256(const __grid_constant__ CUtensorMap tm_pihi, const __grid_constant__ CUtensorMap tm_pilo,
+    k_quantize_tcx(const __grid_constant__ CUtensorMap tm_pihi, const __grid_constant__ CUtensorMap tm_pilo,
                      const __grid_constant__ CUtensorMap tm_s, const Dev cb, uint8_t* __restrict__ cache,
                      int64_t cache_rows, const void* __restrict__ x, int64_t n, int d_in,
                      const int64_t* __restrict__ dst_rows, int* __restrict__ status) {
@@ -73,17 +79,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = warp & 3;                            // TMEM lane quarter
-  const int cq = warp >> 2;                          // coordinates 64 cq .. 64 cq + 63
+  const int cq = warp >> 2;                          // coordinates (d/4) cq .. (d/4) cq + d/4 - 1
   const int m = 32 * q + lane;                       // tile row = TMEM lane
-  float* red1 = reinterpret_cast<float*>(smem + kOffRed);
-  float* red2 = red1 + 8 * kRows;
-  const uint32_t bar0 = sbase + kOffBar;
+  using M = Map<D>;
+  constexpr int QC = D / 4;                          // coordinates per thread
+  constexpr int NCH = QC / 32;                       // 32-coordinate word columns per thread
+  constexpr int KB = D / 64;                         // K blocks
+  constexpr uint32_t kIdesc = idesc_bf16(D);
+  float* red1 = reinterpret_cast<float*>(smem + M::kOffRed);
+  float* red2 = red1 + (D / 32) * kRows;
+  const uint32_t bar0 = sbase + M::kOffBar;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
   auto bar_empty = [&](int s) { return bar0 + 8u * (kSlots + s); };
   const uint32_t bar_y = bar0 + 8u * (2 * kSlots), bar_z = bar_y + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + M::kOffTmem);
   constexpr int P = B1 + (PROD ? 1 : 0);
-  constexpr int NL = loads_per_tile<PROD>();
+  constexpr int NL = loads_per_tile<D, PROD>();
   const int W = cb.W;
   const int64_t ntiles = (n + kRows - 1) / kRows;
   __shared__ float s_cent[16], s_bnd[16];
@@ -121,10 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = (int)(g % kSlots);
     if (g >= kSlots && !mbar_wait(bar_empty(s), (uint32_t)(((g / kSlots) - 1) & 1))) return false;
     const int c = (int)(g % NL);
-    const CUtensorMap* map = c < 8 ? ((c & 1) ? &tm_pilo : &tm_pihi) : &tm_s;
-    const int kb = c < 8 ? (c >> 1) : c - 8;
-    mbar_expect_tx(bar_full(s), kSlotBytes);
-    tma_load_2d(sbase + kOffRing + s * kSlotBytes, map, 64 * kb, 0, bar_full(s));
+    const CUtensorMap* map = c < 2 * KB ? ((c & 1) ? &tm_pilo : &tm_pihi) : &tm_s;
+    const int kb = c < 2 * KB ? (c >> 1) : c - 2 * KB;
+    mbar_expect_tx(bar_full(s), M::kSlotBytes);
+    tma_load_2d(sbase + M::kOffRing + s * M::kSlotBytes, map, 64 * kb, 0, bar_full(s));
     return true;
   };
   bool ok = true;
@@ -139,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(bar_full(s), (uint32_t)((g / kSlots) & 1), first_wait ? cb.first_wait : kSpinLimit)) return false;
     first_wait = false;
     fence_after();
-    issue_mmas(sbase + kOffRing + s * kSlotBytes);
+    issue_mmas(sbase + M::kOffRing + s * M::kSlotBytes);
     mma_commit(bar_empty(s));
     g_done = g + 1;
     if (g >= 1 && g_issued < total_loads && g_issued == g - 1 + kSlots) {
@@ -165,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const int64_t row = tile * kRows + m;
 #pragma unroll
-      for (int piece = 0; piece < 4; ++piece) {
-        const int k0 = 64 * cq + 16 * piece;             // first coordinate of the piece
+      for (int piece = 0; piece < QC / 16; ++piece) {
+        const int k0 = QC * cq + 16 * piece;             // first coordinate of the piece
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = 0.f;
@@ -212,11 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_before();
     __syncthreads();
-    // ---- rotation: loads g0 .. g0 + 7 (Pi_hi, Pi_lo of K blocks 0..3)
+    // ---- rotation: loads g0 .. g0 + 2 KB - 1 (Pi_hi, Pi_lo of the K blocks)
     bool good = true;
     if (tid == 0) {
       fence_after();
-      for (int c = 0; c < 8 && good; ++c) {
+      for (int c = 0; c < 2 * KB && good; ++c) {
         const int kb = c >> 1;
         good = consume(g0 + c, [&](uint32_t slot) {
 #pragma unroll
@@ -244,30 +255,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- epilogue 1: norms (pass 1), codes and the residual operand (pass 2)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NCH; ++h) {
       float v[32];
-      tmem_ld32(tmem + lane_off + 64 * cq + 32 * h, v);
+      tmem_ld32(tmem + lane_off + QC * cq + 32 * h, v);
       float ss = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) ss = fmaf(v[e], v[e], ss);
-      red1[(2 * cq + h) * kRows + m] = ss;
+      red1[(NCH * cq + h) * kRows + m] = ss;
     }
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tot += red1[k * kRows + m];
+    for (int k = 0; k < D / 32; ++k) tot += red1[k * kRows + m];
     const float nrm = sqrtf(tot);
     const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
-    uint32_t words[2][P];
+    uint32_t words[NCH][P];
     float gs = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NCH; ++h) {
 #pragma unroll
       for (int p = 0; p < P; ++p) words[h][p] = 0u;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float v[16];
-        tmem_ld16(tmem + lane_off + 64 * cq + 32 * h + 16 * half, v);
+        tmem_ld16(tmem + lane_off + QC * cq + 32 * h + 16 * half, v);
         uint32_t rh[8], rl[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
@@ -285,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           rl[e >> 1] = bf16x2(r2[0] - __uint_as_float(hb << 16), r2[1] - __uint_as_float(hb & 0xFFFF0000u));
         }
         if (PROD) {
-          const uint32_t col = (uint32_t)(32 * cq + 16 * h + 8 * half);
+          const uint32_t col = (uint32_t)(QC / 2 * cq + 16 * h + 8 * half);
           tmem_st8(t_hi + lane_off + col, rh);
           tmem_st8(t_lo + lane_off + col, rl);
         }
@@ -295,15 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PROD) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     fence_before();
     __syncthreads();
-    // ---- sketch: loads g0 + 8 .. g0 + 11 (S of K blocks 0..3)
-    uint32_t sword[2] = {0u, 0u};
+    // ---- sketch: loads g0 + 2 KB .. g0 + 3 KB - 1 (S of the K blocks)
+    uint32_t sword[NCH];
+#pragma unroll
+    for (int h = 0; h < NCH; ++h) sword[h] = 0u;
     float gamma = 0.f;
     if (PROD) {
       good = true;
       if (tid == 0) {
         fence_after();
-        for (int c = 8; c < 12 && good; ++c) {
-          const int kb = c - 8;
+        for (int c = 2 * KB; c < 3 * KB && good; ++c) {
+          const int kb = c - 2 * KB;
           good = consume(g0 + c, [&](uint32_t slot) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -328,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend_z = false;
       fence_after();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NCH; ++h) {
         float v[32];
-        tmem_ld32(tmem + lane_off + 64 * cq + 32 * h, v);
+        tmem_ld32(tmem + lane_off + QC * cq + 32 * h, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) sword[h] |= (v[e] >= 0.f ? 1u : 0u) << e;
       }
@@ -346,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (dst >= 0 && dst < cache_rows) {
       uint32_t* rec = reinterpret_cast<uint32_t*>(cache) + dst * W;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NCH; ++h) {
         if constexpr (PROD) words[h][B1] = sword[h];
-        const int wc = 2 * cq + h;
+        const int wc = NCH * cq + h;
         if constexpr (P == 4) {
           *reinterpret_cast<uint4*>(rec + wc * P) = make_uint4(words[h][0], words[h][1], words[h][2], words[h][3]);
         } else if constexpr (P == 2) {
@@ -393,30 +406,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int B1, bool PROD, bool F32>
-static cudaError_t launch_tc256_t(const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo, const CUtensorMap& tm_s,
-                                  const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int64_t n,
-                                  int d_in, const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
-  static cudaError_t configured = cudaFuncSetAttribute(k_quantize_tc256<B1, PROD, F32>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+template <int D, int B1, bool PROD, bool F32>
+static cudaError_t launch_tcx_t(const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo, const CUtensorMap& tm_s,
+                                const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, int64_t n, int d_in,
+                                const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
+  constexpr uint32_t smem = Map<D>::kSmemBytes;
+  static cudaError_t configured =
+      cudaFuncSetAttribute(k_quantize_tcx<D, B1, PROD, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (configured != cudaSuccess) return configured;
   const int64_t ntiles = (n + kRows - 1) / kRows;
   const int grid = (int)(ntiles < sms ? ntiles : sms);
-  k_quantize_tc256<B1, PROD, F32><<<grid, kThreads, kSmemBytes, s>>>(tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows,
-                                                                     x, n, d_in, dst_rows, status);
+  k_quantize_tcx<D, B1, PROD, F32><<<grid, kThreads, smem, s>>>(tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, x, n,
+                                                                d_in, dst_rows, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_tc256(const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo, const CUtensorMap& tm_s,
-                                  const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, bool f32,
-                                  int64_t n, int d_in, const int64_t* dst_rows, int* status, int sms,
-                                  cudaStream_t s) {
-#define TQ_TC(B, PR, F)                                                                                        \
-  return launch_tc256_t<B, PR, F>(tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, x, n, d_in, dst_rows, status, \
-                                  sms, s)
-#define TQ_TC_F(B, PR) \
-  if (f32) TQ_TC(B, PR, true); \
-  TQ_TC(B, PR, false)
+// d = 256 in either input type; d = 128 for fp32 input (no extra-bit words).
+cudaError_t launch_quantize_tcx(const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo, const CUtensorMap& tm_s,
+                                const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, bool f32, int64_t n,
+                                int d_in, const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
+#define TQ_TC(DD, B, PR, F)                                                                                        \
+  return launch_tcx_t<DD, B, PR, F>(tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, x, n, d_in, dst_rows, status, \
+                                    sms, s)
+#define TQ_TC_F(B, PR)               \
+  if (cb.d == 128) TQ_TC(128, B, PR, true); \
+  if (f32) TQ_TC(256, B, PR, true); \
+  TQ_TC(256, B, PR, false)
   if (cb.kind == 0) {
     switch (cb.b1) {
       case 1: TQ_TC_F(1, true);

@@ -504,16 +504,19 @@ def test_quantize_tensor_core_path(bits, kind, extra, n):
         assert np.allclose(got["g16"][perm].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,dtype", [(256, "f32"), (256, "bf16"), (128, "f32")])
 @pytest.mark.parametrize("bits,kind", [(2, "prod"), (3, "prod"), (4, "prod"), (4, "mse")])
 @pytest.mark.parametrize("n", [2048, 4096 + 77])
-def test_quantize_tensor_core_path_d256(dtype, bits, kind, n):
-    """d = 256 batches of >= 2048 rows (the search database: 200 coordinates
-    zero-padded) take the d = 256 tcgen05 kernel, fp32 or bf16 input:
-    <= 0.1% differing bits against the oracle, each differing code near a
-    boundary, scattered destination rows, ragged last tile."""
-    ocb, gcb = pair(256, bits, kind, "scalar", 0)
-    x = wl.search_rows(n, "db")
+def test_quantize_tensor_core_path_tmem_operands(d, dtype, bits, kind, n):
+    """Batches of >= 2048 rows that take the tcgen05 kernel with X in tensor
+    memory: d = 256 (the search database, 200 coordinates zero-padded), fp32
+    or bf16, and d = 128 fp32: <= 0.1% differing bits against the oracle,
+    each differing code near a boundary, scattered destination rows, ragged
+    last tile."""
+    ocb, gcb = pair(d, bits, kind, "scalar", 0)
+    d_in = 200 if d == 256 else 128
+    x = wl.search_rows(n, "db") if d == 256 else np.concatenate(
+        [wl.llama_kv_slice(0, h, 0, 4096) for h in range(2)])[:n]
     xt = torch.from_numpy(x).cuda()
     if dtype == "bf16":
         xt = xt.to(torch.bfloat16)
@@ -522,7 +525,7 @@ def test_quantize_tensor_core_path_d256(dtype, bits, kind, n):
     rows = n + 100
     perm = np.random.default_rng(n + bits).permutation(rows)[:n]
     cache = gpu_cache(gcb, rows)
-    tq.tq_quantize(gcb, cache, rows, xt, n, 200, dst_rows=torch.from_numpy(perm.astype(np.int64)).cuda())
+    tq.tq_quantize(gcb, cache, rows, xt, n, d_in, dst_rows=torch.from_numpy(perm.astype(np.int64)).cuda())
     tq.tq_check_device(gcb)
     got = read_back(ocb, rows, cache)
     g_idx = got["idx"][perm]
@@ -537,7 +540,7 @@ def test_quantize_tensor_core_path_d256(dtype, bits, kind, n):
         y, _ = quant.rotate(ocb, x64)
         t = ocb.t.astype(np.float64)
         dist = np.min(np.abs(y[bad][:, None] - t[None, :]), axis=1)
-        assert np.all(dist < 1e-4 / math.sqrt(256))
+        assert np.all(dist < 1e-4 / math.sqrt(d))
     n_ref = np.linalg.norm(x64, axis=1)
     assert np.allclose(got["n16"][perm].astype(np.float64), n_ref, rtol=1e-3)
     if kind == "prod":
