@@ -719,7 +719,10 @@ def run_search(args, dist, rank, steps):
                            "pair_scores_per_s": steps * nq * n_db / (ms / 1e3),
                            "recall_1_at_k": recall, "db_bytes": n_db * (tq.record_bytes(cb) + 4),
                            "db_quantize": {"ms": q_ms, "vectors_per_s": n_db / (q_ms / 1e3),
-                                           "input": "fp32 rows, 200 coordinates zero-padded to 256"},
+                                           "input": "fp32 rows, 200 coordinates zero-padded to 256",
+                                           "kernel": "k_quantize_tcx (tcgen05, X and residual in TMEM)",
+                                           "hbm_frac": n_db * (4 * d_in + tq.record_bytes(cb) + 4)
+                                           / (q_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
                            "queries_rerun_by_exact_scan": fallbacks,
                            "roofline": {"kernel": "tq_search (tcgen05 candidate scan + exact re-ranking)",
                                         "bound": "tensor", "achieved": tf, "unit": "TFLOP/s",
