@@ -182,3 +182,53 @@ def test_split_keys_rejected_where_not_scored():
         tq.tq_decode_attention(gcb, gvc, kc, vc, 1, 4, 1, 100, torch.tensor([100], dtype=torch.int32, device="cuda"),
                                torch.zeros(1, 4, 128, device="cuda"), 0.1, torch.zeros(1, 4, 128, device="cuda"), ws)
     assert e.value.status == tq.TQ_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("ps", [16, 256])
+def test_split_logits_paged_equals_contiguous(ps):
+    # the paged staged kernel copies 8-byte norm entries per page run
+    B, Hq, Hkv = 2, 8, 2
+    max_pages = -(-700 // ps)
+    cap = max_pages * ps
+    lens = [cap, 333]
+    num_pages = B * max_pages + 3
+    rows = B * Hkv * cap
+    x = keys(rows)
+    scb, gcb = split_pair(3, outlier_channels(x, 32))
+    code = split.quantize(scb, x.astype(np.float64))
+    table = wl.block_table(B, max_pages, num_pages, ps, lens)
+    # physical row of every live logical row; other physical rows hold valid unrelated rows
+    rows_p = num_pages * Hkv * ps
+    filler = np.random.default_rng(5).integers(0, rows, size=rows_p)
+    log, phys = [], []
+    for b in range(B):
+        t = np.arange(lens[b])
+        for h in range(Hkv):
+            log.append((b * Hkv + h) * cap + t)
+            phys.append((table[b, t // ps].astype(np.int64) * Hkv + h) * ps + t % ps)
+    log, phys = np.concatenate(log), np.concatenate(phys)
+    pcode = {"groups": []}
+    for c in code["groups"]:
+        pc = {k: v[filler].copy() for k, v in c.items() if isinstance(v, np.ndarray) and v.shape[:1] == (rows,)}
+        for k in pc:
+            pc[k][phys] = c[k][log]
+        pcode["groups"].append(pc)
+    img_c = split.write_cache(scb, rows, code)
+    img_p = split.write_cache(scb, rows_p, pcode)
+    q = wl.queries((B, Hq, 128), name="tiny_q")
+    ref = estimate.logits(scb, code, q.astype(np.float64), lens, Hkv, cap)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    qd = torch.from_numpy(q).cuda()
+    ws = torch.empty(tq.tq_logits_workspace(gcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
+    out_c = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    out_p = torch.full((B, Hq, cap), float("nan"), device="cuda")
+    tq.tq_logits(gcb, torch.from_numpy(img_c).cuda(), B, Hq, Hkv, cap, sl, qd, out_c, ws)
+    tq.tq_logits_paged(gcb, torch.from_numpy(img_p).cuda(), num_pages, ps, torch.from_numpy(table).cuda(), B, Hq,
+                       Hkv, sl, qd, out_p, ws)
+    torch.cuda.synchronize()
+    tq.tq_check_device(gcb)
+    got_c, got_p = out_c.cpu().numpy(), out_p.cpu().numpy()
+    for b in range(B):
+        L = lens[b]
+        assert np.array_equal(got_p[b, :, :L], got_c[b, :, :L])
+        rowwise_ok(got_p[b, :, :L], ref[b, :, :L])

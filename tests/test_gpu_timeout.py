@@ -101,3 +101,25 @@ def test_staged_attention_gives_up_and_recovers():
     tq.tq_check_device(kcb)
     assert torch.equal(out, ref)
     assert np.all(np.isfinite(out.cpu().numpy()))
+
+
+def test_tensor_memory_operand_quantize_gives_up_and_recovers():
+    # the d = 256 kernel (X and the residual in tensor memory, Pi and S
+    # streamed through a TMA ring): a timeout on its first ring wait must
+    # drain the loads already issued and free its tensor memory
+    cb = tq.Codebook(256, 3, tq.KIND_PROD)
+    n = 4096
+    x = torch.from_numpy(wl.search_rows(n, "db")).cuda()
+    ref = torch.zeros(tq.cache_bytes(cb, n), dtype=torch.uint8, device="cuda")
+    tq.tq_quantize(cb, ref, n, x, n, 200)
+    tq.tq_check_device(cb)
+    cache = torch.zeros_like(ref)
+    tq.tq_set_first_wait_limit(cb, 0)
+    try:
+        tq.tq_quantize(cb, cache, n, x, n, 200)
+        _expect_timeout(cb)
+    finally:
+        tq.tq_set_first_wait_limit(cb, -1)
+    tq.tq_quantize(cb, cache, n, x, n, 200)
+    tq.tq_check_device(cb)
+    assert torch.equal(cache, ref)
