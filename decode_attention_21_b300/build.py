@@ -49,7 +49,7 @@ def build(verbose=False, out=OUT):
             if r.returncode:
                 raise RuntimeError("nvcc failed on " + s)
             objs.append(o)
-    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", out] + objs
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", out] + objs + ["-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(r.stdout + r.stderr)

@@ -9,9 +9,16 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "tq.h"
 #include "tq_internal.cuh"
 #include "tq_math.h"
+
+namespace tq {
+NvtxRange::NvtxRange(const char* name) { nvtxRangePushA(name); }
+NvtxRange::~NvtxRange() { nvtxRangePop(); }
+}  // namespace tq
 
 
 struct tq_codebook {
@@ -98,9 +105,16 @@ int attn_ctas(const tq_codebook* kcb, const tq_codebook* vcb = nullptr) {
   return heavy ? 148 * 3 : 148 * 4;
 }
 
+// Test hook (tq_fail_allocation): device allocations of tq_make_codebook
+// still to go before one fails as if the device were out of memory (-1: none).
+int g_fail_after = -1;
+
 template <class T>
 tq_status upload(tq_codebook* cb, const std::vector<T>& h, const T** out) {
   void* p = nullptr;
+  if (g_fail_after >= 0 && g_fail_after-- == 0)
+    return fail(TQ_ENOMEM, "cudaMalloc(%zu) failed: allocation failure injected by tq_fail_allocation",
+                h.size() * sizeof(T));
   cudaError_t e = cudaMalloc(&p, h.size() * sizeof(T));
   if (e != cudaSuccess) return fail(TQ_ENOMEM, "cudaMalloc(%zu) failed: %s", h.size() * sizeof(T), cudaGetErrorString(e));
   cb->allocs.push_back(p);
@@ -262,6 +276,7 @@ tq_status tq_host_tables(const tq_codebook_desc* desc, int32_t level, float* cen
 }
 
 tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
+  const tq::NvtxRange nvtx_range("tq_make_codebook");
   if (!desc || !out) return fail(TQ_EINVAL, "tq_make_codebook: NULL argument");
   *out = nullptr;
   const tq_codebook_desc& D = *desc;
@@ -494,6 +509,12 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   return ok();
 }
 
+tq_status tq_fail_allocation(int32_t nth) {
+  if (nth < -1) return fail(TQ_EINVAL, "tq_fail_allocation: nth must be >= -1");
+  g_fail_after = nth;
+  return ok();
+}
+
 tq_status tq_set_first_wait_limit(tq_codebook* cb, int64_t polls) {
   if (!cb) return fail(TQ_EINVAL, "tq_set_first_wait_limit: NULL codebook");
   if (polls < -1) return fail(TQ_EINVAL, "tq_set_first_wait_limit: polls must be >= -1");
@@ -502,6 +523,7 @@ tq_status tq_set_first_wait_limit(tq_codebook* cb, int64_t polls) {
 }
 
 tq_status tq_check_device(const tq_codebook* cb) {
+  const tq::NvtxRange nvtx_range("tq_check_device");
   if (!cb) return fail(TQ_EINVAL, "tq_check_device: NULL codebook");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(TQ_ECUDA, "tq_check_device: %s", cudaGetErrorString(e));
@@ -587,12 +609,14 @@ static tq_status quantize_common(const char* what, const tq_codebook* cb, void* 
 
 tq_status tq_quantize(const tq_codebook* cb, void* cache, int64_t cache_rows, const void* x, int32_t x_dtype,
                       int64_t n, int32_t d_in, const int64_t* dst_rows, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_quantize");
   return quantize_common("tq_quantize", cb, cache, cache_rows, x, x_dtype, n, d_in, nullptr, nullptr, dst_rows,
                          stream);
 }
 
 tq_status tq_quantize_rotated(const tq_codebook* cb, void* cache, int64_t cache_rows, const float* y,
                               const float* norms, int64_t n, const int64_t* dst_rows, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_quantize_rotated");
   if (n > 0 && !y) return fail(TQ_EINVAL, "tq_quantize_rotated: y is NULL");
   return quantize_common("tq_quantize_rotated", cb, cache, cache_rows, nullptr, TQ_F32, n, cb ? cb->dev.d : 0, y,
                          norms, dst_rows, stream);
@@ -666,6 +690,7 @@ static tq_status logits_common(const char* what, const tq_codebook* kcb, const v
 tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
                     const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
                     void* stream) {
+  const tq::NvtxRange nvtx_range("tq_logits");
   return logits_common("tq_logits", kcb, kcache, (int64_t)B * Hkv * capacity, tq::RowMap{}, B, Hq, Hkv, capacity,
                        seq_lens, q, logits, workspace, ws_bytes, stream);
 }
@@ -695,6 +720,7 @@ tq_status tq_logits_paged(const tq_codebook* kcb, const void* kcache, int32_t nu
                           const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq, int32_t Hkv,
                           const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
                           void* stream) {
+  const tq::NvtxRange nvtx_range("tq_logits_paged");
   tq::RowMap map;
   tq_status st = check_paged("tq_logits_paged", num_pages, page_size, block_table, max_pages, Hkv, &map);
   if (st != TQ_OK) return st;
@@ -705,6 +731,7 @@ tq_status tq_logits_paged(const tq_codebook* kcb, const void* kcache, int32_t nu
 tq_status tq_append_paged(const tq_codebook* cb, void* cache, int32_t num_pages, int32_t page_size,
                           const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hkv,
                           const int32_t* seq_lens, const void* x, int32_t x_dtype, int32_t d_in, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_append_paged");
   tq::AppendDst dst = {};
   tq_status st = check_paged("tq_append_paged", num_pages, page_size, block_table, max_pages, Hkv, &dst.map);
   if (st != TQ_OK) return st;
@@ -718,6 +745,7 @@ tq_status tq_append_paged(const tq_codebook* cb, void* cache, int32_t num_pages,
 }
 
 tq_status tq_advance_lengths(int32_t* seq_lens, int32_t B, int32_t delta, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_advance_lengths");
   if (!seq_lens || B < 1) return fail(TQ_EINVAL, "tq_advance_lengths: bad arguments");
   return launched("tq_advance_lengths", tq::launch_advance_lengths(seq_lens, B, delta, static_cast<cudaStream_t>(stream)));
 }
@@ -839,6 +867,7 @@ tq_status tq_decode_attention(const tq_codebook* kcb, const tq_codebook* vcb, co
                               int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
                               const float* q, float scale, float* out, void* workspace, size_t ws_bytes,
                               void* stream) {
+  const tq::NvtxRange nvtx_range("tq_decode_attention");
   return attn_common("tq_decode_attention", kcb, vcb, kcache, vcache, (int64_t)B * Hkv * capacity, tq::RowMap{}, B,
                      Hq, Hkv, capacity, seq_lens, q, scale, out, workspace, ws_bytes, stream);
 }
@@ -848,6 +877,7 @@ tq_status tq_decode_attention_paged(const tq_codebook* kcb, const tq_codebook* v
                                     const int32_t* block_table, int32_t max_pages, int32_t B, int32_t Hq,
                                     int32_t Hkv, const int32_t* seq_lens, const float* q, float scale, float* out,
                                     void* workspace, size_t ws_bytes, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_decode_attention_paged");
   tq::RowMap map;
   tq_status st = check_paged("tq_decode_attention_paged", num_pages, page_size, block_table, max_pages, Hkv, &map);
   if (st != TQ_OK) return st;
@@ -865,6 +895,7 @@ size_t tq_search_workspace(const tq_codebook* cb, int64_t n_db, int32_t nq, int3
 tq_status tq_search(const tq_codebook* cb, const void* db_cache, int64_t n_db, const float* q, int32_t nq,
                     int32_t d_in, int32_t k, int32_t* ids, float* scores, void* workspace, size_t ws_bytes,
                     void* stream) {
+  const tq::NvtxRange nvtx_range("tq_search");
   if (!cb) return fail(TQ_EINVAL, "tq_search: codebook is NULL");
   if (cb->dev.kind != TQ_KIND_PROD) return fail(TQ_EINVAL, "tq_search: the database codebook must be of kind PROD");
   if (cb->dev.mode != TQ_MODE_SCALAR || cb->dev.extra != 0)

@@ -217,6 +217,7 @@ tq_status report_error(tq_status st, const char* msg);
 extern "C" tq_status tq_logits_dense(const void* keys, int32_t key_dtype, int32_t d, int32_t B, int32_t Hq,
                                      int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q,
                                      float* logits, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_logits_dense");
   if (key_dtype != TQ_F32 && key_dtype != TQ_BF16)
     return tq::report_error(TQ_EINVAL, "tq_logits_dense: key_dtype must be TQ_F32 or TQ_BF16");
   if (d != 128) return tq::report_error(TQ_EUNSUPPORTED, "tq_logits_dense: only d = 128 is implemented");

@@ -48,6 +48,15 @@ struct Dev {
 
 inline __host__ __device__ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
+// One NVTX range per C-ABI call, named after the call (shows in profiler
+// timelines; a few nanoseconds when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name);
+  ~NvtxRange();
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // L2 residency hints.  The packed caches are streamed once per call
 // (evict-first); the small codebook tables (Pi, S Pi, S) are read by every
 // query prep and cache append and should stay in L2 (evict-last).

@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "tq.h"
+#include "tq_internal.cuh"
 
 namespace tq {
 tq_status report_error(tq_status st, const char* msg);
@@ -74,6 +75,7 @@ extern "C" tq_status tq_decode_attention_static(const tq_codebook* kcb, const tq
                                                 const void* vcache, int32_t B, int32_t Hq, int32_t Hkv,
                                                 int64_t capacity, const int32_t* seq_lens, const float* q,
                                                 float scale, float* out, void* stream) {
+  const tq::NvtxRange nvtx_range("tq_decode_attention_static");
   if (!kcb || !vcb) return tq::report_error(TQ_EINVAL, "tq_decode_attention_static: codebook is NULL");
   const size_t need = tq_decode_attention_workspace(kcb, B, Hq, Hkv, capacity);
   if (need > kStaticScratchBytes) {

@@ -20,7 +20,7 @@ F32, BF16 = 0, 1
 EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_host_tables", "tq_record_bytes", "tq_cache_bytes",
            "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits", "tq_logits_dense",
            "tq_decode_attention_workspace", "tq_decode_attention", "tq_decode_attention_static",
-           "tq_search_workspace", "tq_search", "tq_search_fallbacks", "tq_set_first_wait_limit",
+           "tq_search_workspace", "tq_search", "tq_search_fallbacks", "tq_set_first_wait_limit", "tq_fail_allocation",
            "tq_append_paged", "tq_logits_paged", "tq_decode_attention_paged", "tq_advance_lengths",
            "tq_check_device", "tq_last_error"]
 
@@ -74,6 +74,7 @@ def lib():
         L.tq_search.argtypes = [vp, vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp]
         L.tq_search_fallbacks.argtypes = [vp, vp, i32, ctypes.POINTER(i32)]
         L.tq_set_first_wait_limit.argtypes = [vp, i64]
+        L.tq_fail_allocation.argtypes = [i32]
         L.tq_append_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, vp, vp, i32, i32, vp]
         L.tq_logits_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
         L.tq_decode_attention_paged.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp,
@@ -277,6 +278,11 @@ def tq_decode_attention_paged(kcb, vcb, kcache, vcache, num_pages, page_size, bl
 
 def tq_advance_lengths(seq_lens, B, delta=1, stream=None):
     _check(lib().tq_advance_lengths(_ptr(seq_lens), B, delta, _stream(stream)))
+
+
+def tq_fail_allocation(nth):
+    """Test hook: the nth device allocation of tq_make_codebook from now on fails (-1: off)."""
+    _check(lib().tq_fail_allocation(nth))
 
 
 def tq_set_first_wait_limit(cb, polls):

@@ -336,6 +336,12 @@ tq_status tq_search_fallbacks(const tq_codebook* cb, const void* workspace, int3
  * TQ_OK otherwise.  Not a hot call.                                          */
 tq_status tq_check_device(const tq_codebook* cb);
 
+/* Test hook: the nth device allocation of tq_make_codebook from now on
+ * (0 = the next one) fails as if the device were out of memory, so that the
+ * call returns TQ_ENOMEM after freeing what it had allocated; -1 turns the
+ * hook off.  Process-wide; for tests only.  Errors: TQ_EINVAL for nth < -1. */
+tq_status tq_fail_allocation(int32_t nth);
+
 /* Test use: from the next launch on, the first bounded device-side wait of
  * every kernel that uses this codebook (the first bulk-copy stage of the
  * logits and attention kernels, the Pi / S loads of the tensor-core
