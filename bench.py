@@ -669,9 +669,31 @@ def run_quantize(args, dist, rank, steps):
         gbs = steps * bytes_moved / (ms / 1e3) / 1e9
         out[name] = {"vectors_per_s": steps * N * args.world / (ms / 1e3), "ms_per_call": ms / steps,
                      "bits_per_coord": (tq.record_bytes(cb) + 4) * 8 / d,
+                     "cpu_baseline": quantize_oracle_rate(bits, extra) if rank == 0 else None,
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                   "frac": gbs / pk["hbm_gbs"]}}
     return out
+
+
+def quantize_oracle_rate(bits, extra, n=8192):
+    """The oracle compressing a sample of the same vectors (rows 0..n-1 of the
+    bench's distribution, drawn with the numpy recipe), with all cores and
+    single-threaded."""
+    from threadpoolctl import threadpool_limits
+
+    from decode_attention_21_b300 import workloads as wl
+    from oracle import quant
+    ocb = quant.Codebook(128, bits, "prod", extra=extra)
+    x = wl.llama_kv_slice(0, 0, 0, n).astype(np.float64)
+    quant.quantize(ocb, x[:64])                       # codebook tables and imports warm
+    res = {"unit": "vectors/s", "kind": "oracle", "sample": f"{n} vectors of d 128 (same distribution)"}
+    for key, limit in (("value", None), ("single_thread_value", 1)):
+        with threadpool_limits(limits=limit):
+            t0 = time.perf_counter()
+            quant.quantize(ocb, x)
+            res[key] = n / (time.perf_counter() - t0)
+    res["cores"] = cores()
+    return res
 
 
 # ----------------------------------------------------------- search (config)
