@@ -10,7 +10,7 @@ namespace tq {
 namespace stage {
 constexpr int kStageTiles = 8;
 constexpr int kRing = 4;
-constexpr int kPrefetchStages = 8;    // stages per CTA prefetched into L2 before the prep completes
+constexpr int kPrefetchStages = 1;    // stages per CTA prefetched into L2 before the prep completes
 constexpr long long kWaitLimit = 1ll << 26;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
