@@ -131,3 +131,35 @@ def test_codebook_allocation_failure_is_reported_and_recovered():
     tq.tq_quantize(cb, cache, 64, x, 64, 128)
     tq.tq_check_device(cb)
     assert int(cache.sum()) > 0
+
+
+@pytest.mark.parametrize("d,dtype,extra", [(128, "bf16", 0), (128, "f32", 0), (256, "f32", 0), (256, "bf16", 0),
+                                           (128, "bf16", 32)])
+def test_quantize_destination_outside_the_cache_is_skipped_and_flagged(d, dtype, extra):
+    # a destination row past the cache is not written (the canary tail stays)
+    # and tq_check_device reports TQ_EINVAL; every other row is written
+    cb = tq.Codebook(d, 3, tq.KIND_PROD, extra=extra)
+    n, rows = 4096, 5000
+    d_in = 256 if d == 256 else 128
+    x = np.random.default_rng(d).standard_normal((n, d_in)).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    if dtype == "bf16":
+        xt = xt.to(torch.bfloat16)
+    dst = torch.arange(n, dtype=torch.int64, device="cuda") + 7
+    dst[1234] = rows + 5
+    nbytes = tq.cache_bytes(cb, rows)
+    buf, cache = guarded(nbytes)
+    tq.tq_quantize(cb, cache, rows, xt, n, d_in, dst_rows=dst)
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_check_device(cb)
+    assert e.value.status == tq.TQ_EINVAL
+    assert tail_intact(buf, nbytes)
+    ref = torch.zeros(tq.cache_bytes(cb, rows), dtype=torch.uint8, device="cuda")
+    ok_dst = dst.clone()
+    ok_dst[1234] = 3                                   # a row nobody else writes
+    tq.tq_quantize(cb, ref, rows, xt, n, d_in, dst_rows=ok_dst)
+    tq.tq_check_device(cb)
+    W = tq.record_bytes(cb)
+    recs, recs_ref = cache[: rows * W].view(rows, W), ref[: rows * W].view(rows, W)
+    written = torch.cat([dst[:1234], dst[1235:]])     # rows both calls wrote
+    assert torch.equal(recs[written], recs_ref[written])

@@ -138,7 +138,8 @@ def test_split_logits_parity(E, bits, B, Hq, Hkv, cap, lens):
 
 @pytest.mark.parametrize("E,bits", [(32, 2), (64, 3), (32, 4)])
 @pytest.mark.parametrize("vb", [3, 4])
-@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 304, [300, 1, 0])])
+@pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(2, 8, 2, 2048, [2048, 1500]), (3, 4, 1, 304, [300, 1, 0]),
+                                               (1, 16, 2, 512, [500])])
 def test_split_attention_parity(E, bits, vb, B, Hq, Hkv, cap, lens):
     rows = B * Hkv * cap
     K = keys(rows)
