@@ -654,8 +654,11 @@ def run_quantize(args, dist, rank, steps):
     x = wl.llama_kv_torch(N, d, 0, which="keys")
     pk = peaks()
     out = {}
-    for name, bits, extra in [("b2", 2, 0), ("b3", 3, 0), ("b4", 4, 0), ("b2.5", 2, 32), ("b3.5", 3, 32)]:
-        cb = tq.Codebook(d, bits, tq.KIND_PROD, extra=extra)
+    for name, bits, extra, mode in [("b2", 2, 0, "scalar"), ("b3", 3, 0, "scalar"), ("b4", 4, 0, "scalar"),
+                                    ("b2.5", 2, 32, "scalar"), ("b3.5", 3, 32, "scalar"), ("polar_b3", 3, 0, "polar"),
+                                    ("polar_b4", 4, 0, "polar")]:
+        md = tq.MODE_POLAR if mode == "polar" else tq.MODE_SCALAR
+        cb = tq.Codebook(d, bits, tq.KIND_PROD, md, extra=extra)
         caches = [torch.empty(tq.cache_bytes(cb, N), dtype=torch.uint8, device="cuda") for _ in range(2)]
 
         def step(i, cb=cb, caches=caches):
@@ -669,19 +672,19 @@ def run_quantize(args, dist, rank, steps):
         gbs = steps * bytes_moved / (ms / 1e3) / 1e9
         out[name] = {"vectors_per_s": steps * N * args.world / (ms / 1e3), "ms_per_call": ms / steps,
                      "bits_per_coord": (tq.record_bytes(cb) + 4) * 8 / d,
-                     "cpu_baseline": quantize_oracle_rate(bits, extra) if rank == 0 else None,
+                     "cpu_baseline": quantize_oracle_rate(bits, extra, mode) if rank == 0 else None,
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                   "frac": gbs / pk["hbm_gbs"]}}
     return out
 
 
-def quantize_oracle_rate(bits, extra, n=8192):
+def quantize_oracle_rate(bits, extra, mode="scalar", n=8192):
     """The oracle compressing a sample of the same vectors (rows 0..n-1 of the
     bench's distribution, drawn with the numpy recipe), with all cores and
     single-threaded."""
     from decode_attention_21_b300 import workloads as wl
     from oracle import quant
-    ocb = quant.Codebook(128, bits, "prod", extra=extra)
+    ocb = quant.Codebook(128, bits, "prod", mode=mode, extra=extra)
     x = wl.llama_kv_slice(0, 0, 0, n).astype(np.float64)
     quant.quantize(ocb, x[:64])                       # codebook tables and imports warm
     res = {"unit": "vectors/s", "kind": "oracle", "sample": f"{n} vectors of d 128 (same distribution)",

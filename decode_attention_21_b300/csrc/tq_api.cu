@@ -498,8 +498,8 @@ tq_status tq_make_codebook(const tq_codebook_desc* desc, tq_codebook** out) {
   cb->tc_ready = false;
   // tensor maps of Pi_hi, Pi_lo and S for the tensor-core quantize kernels:
   // 64-column blocks of all d rows (d = 128: with extra-bit coordinates too;
-  // d = 256: without)
-  if (D.mode == TQ_MODE_SCALAR && (d == 128 || D.extra == 0)) {
+  // d = 256: without; polar mode has none)
+  if (d == 128 || D.extra == 0) {
     bool good = encode_bf16_rows(&cb->tm_pihi, dv.Pi_hi, d, d, d) && encode_bf16_rows(&cb->tm_pilo, dv.Pi_lo, d, d, d);
     if (D.kind == TQ_KIND_PROD) good = good && encode_bf16_rows(&cb->tm_s, dv.S_bf, D.m, d, d);
     else cb->tm_s = cb->tm_pihi;
@@ -583,9 +583,10 @@ static tq_status quantize_common(const char* what, const tq_codebook* cb, void* 
   cudaGetDevice(&dev);
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // scalar-mode batches on the tensor cores with X in tensor memory: d = 256
-  // (bf16 or fp32), and d = 128 fp32 without extra-bit coordinates
-  const bool tcx = cb->dev.d == 256 || (x_dtype == TQ_F32 && cb->dev.extra == 0);
+  // batches on the tensor cores with X in tensor memory: d = 256 (bf16 or
+  // fp32), d = 128 fp32 without extra-bit coordinates, and polar mode
+  const bool tcx =
+      cb->dev.d == 256 || (x_dtype == TQ_F32 && cb->dev.extra == 0) || cb->dev.mode == TQ_MODE_POLAR;
   if (!paged && !y && tcx && cb->tc_ready && n >= 2048 && d_in % (x_dtype == TQ_BF16 ? 8 : 4) == 0 &&
       aligned16(x) && n < (1ll << 31))
     return launched(what, tq::launch_quantize_tcx(cb->tm_pihi, cb->tm_pilo, cb->tm_s, cb->dev,

@@ -77,6 +77,30 @@ __device__ __forceinline__ float ld_table(const float* p, uint64_t policy) {
   return v;
 }
 
+// Polar angle decisions.  "angle(ra, rb) >= t" is the exact sign of
+// rb cos t - ra sin t >= 0 for fp32 inputs (a zero determinant goes to the
+// upper cell).  The fp32 value v = fma(rb, c, -round(ra s)) is off the exact
+// determinant by at most half an ulp of round(ra s) plus the rounding of v,
+// so whenever |v| > max(2^-21 |round(ra s)|, 2^-100) its sign is the exact
+// sign; otherwise (near-ties, tiny products) both products are formed exactly
+// in fp64.  Valid for products below 2^127 in magnitude (unit rows).
+// The fp64 products sit in a function of their own so that they run only on
+// that rare branch (B300's fp64 rate is a small fraction of its fp32 rate).
+static __device__ __noinline__ int ge_exact_f64(float rb, float ra, float c, float s) {
+  return (double)rb * (double)c - (double)ra * (double)s >= 0.0 ? 1 : 0;
+}
+__device__ __forceinline__ int ge_exact(float rb, float ra, float c, float s) {
+  const float ps = ra * s;
+  const float v = fmaf(rb, c, -ps);
+  if (__builtin_expect(fabsf(v) > fmaxf(fabsf(ps) * 0x1p-21f, 0x1p-100f), 1)) return v > 0.f ? 1 : 0;
+  return ge_exact_f64(rb, ra, c, s);
+}
+
+// fp32 radius with separately rounded products, sum and square root.
+__device__ __forceinline__ float radius_rn(float a, float b) {
+  return __fsqrt_rn(__fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b)));
+}
+
 // Byte offset of the norm region of a cache holding `rows` rows.
 inline __host__ __device__ int64_t norm_offset(const Dev& cb, int64_t rows) {
   return align256(rows * cb.W * 4);

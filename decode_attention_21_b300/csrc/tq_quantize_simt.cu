@@ -25,18 +25,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Exact sign of rb*c - ra*s >= 0 for fp32 inputs: the products are exact in
-// fp64 and the sign of their difference is exact.
-__device__ __forceinline__ int ge_exact(float rb, float ra, float c, float s) {
-  const double v = (double)rb * (double)c - (double)ra * (double)s;
-  return v >= 0.0 ? 1 : 0;
-}
-
-// fp32 radius with separately rounded products, sum and square root.
-__device__ __forceinline__ float radius_rn(float a, float b) {
-  return __fsqrt_rn(__fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b)));
-}
-
 // Slot (32*word + bit) of angle j of level `lev` (see the polar layout in tq.h).
 __device__ __forceinline__ int polar_slot(int lev, int j, int logd) {
   if (lev <= 5) {

@@ -475,6 +475,45 @@ def test_invalid_arguments_return_status_without_launch():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("bits,kind,extra", [(2, "prod", 0), (3, "prod", 0), (4, "prod", 0), (4, "mse", 0),
+                                             (3, "prod", 32), (2, "prod", 64)])
+@pytest.mark.parametrize("n", [1, 8, 128])
+def test_quantize_decode_step_appends(dtype, bits, kind, extra, n):
+    """A decode step's few rows (one CTA per row, coded while the previous
+    kernel runs): the same bars as the batch paths, scattered destinations."""
+    ocb, gcb = pair(128, bits, kind, "scalar", extra)
+    x = wl.llama_kv_slice(0, 3, 0, n)
+    xt = torch.from_numpy(x).cuda()
+    if dtype == "bf16":
+        xt = xt.to(torch.bfloat16)
+    x64 = xt.float().cpu().numpy().astype(np.float64)
+    code = quant.quantize(ocb, x64)
+    rows = n + 50
+    perm = np.random.default_rng(n + bits).permutation(rows)[:n]
+    cache = gpu_cache(gcb, rows)
+    tq.tq_quantize(gcb, cache, rows, xt, n, 128, dst_rows=torch.from_numpy(perm.astype(np.int64)).cuda())
+    tq.tq_check_device(gcb)
+    got = read_back(ocb, rows, cache)
+    bad = got["idx"][perm] != code["idx"]
+    flips = bad.sum()
+    nbits = code["idx"].size * ocb.b1
+    if kind == "prod":
+        flips += (got["sigma"][perm] != code["sigma"]).sum()
+        nbits += code["sigma"].size
+    assert flips <= max(1, 1e-3 * nbits)
+    if bad.any():
+        y, _ = quant.rotate(ocb, x64)
+        t = ocb.t.astype(np.float64)
+        tx = ocb.t_x.astype(np.float64) if extra else t
+        for r, cidx in zip(*np.nonzero(bad)):
+            tt = tx if cidx < extra else t
+            assert np.min(np.abs(y[r, cidx] - tt)) < 1e-4 / math.sqrt(128)
+    assert np.allclose(got["n16"][perm].astype(np.float64), np.linalg.norm(x64, axis=1), rtol=1e-3)
+    if kind == "prod":
+        assert np.allclose(got["g16"][perm].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
+
+
 @pytest.mark.parametrize("bits,kind,extra", [(2, "prod", 0), (3, "prod", 0), (4, "prod", 0), (3, "mse", 0),
                                              (4, "mse", 0), (3, "prod", 32), (2, "prod", 64)])
 @pytest.mark.parametrize("n", [2048, 5000 + 37])
@@ -545,6 +584,145 @@ def test_quantize_tensor_core_path_tmem_operands(d, dtype, bits, kind, n):
     assert np.allclose(got["n16"][perm].astype(np.float64), n_ref, rtol=1e-3)
     if kind == "prod":
         assert np.allclose(got["g16"][perm].astype(np.float64), code["gamma"], rtol=2e-3, atol=1e-4)
+
+
+def polar_tie_distance(ocb, y):
+    """Per level-ordered angle of unit rows y: how far (in the rotated space)
+    the point sits from the nearest cell boundary of its level, i.e. the
+    angular distance to the boundary times the radius of its node."""
+    from oracle import polar
+    tab = ocb.polar
+    ang = polar.exact_angles(y)
+    a, b = y[:, 0::2], y[:, 1::2]
+    rho = np.hypot(a, b)
+    radii = [rho]
+    while rho.shape[1] > 1:
+        rho = np.hypot(rho[:, 0::2], rho[:, 1::2])
+        radii.append(rho)
+    radii = np.concatenate(radii, axis=1)
+    dist = np.empty_like(ang)
+    off = 0
+    for lev in range(1, tab.D + 1):
+        cnt = tab.d >> lev
+        bnd = tab.bound[lev].astype(np.float64)
+        if lev == 1:                                   # the full circle wraps at 0 = 2 pi
+            bnd = np.concatenate([[0.0], bnd, [2.0 * math.pi]])
+        sl = slice(off, off + cnt)
+        dist[:, sl] = np.min(np.abs(ang[:, sl, None] - bnd[None, None, :]), axis=2) * radii[:, sl]
+        off += cnt
+    return dist
+
+
+@pytest.mark.parametrize("d,dtype,bits,kind", [(128, "bf16", 2, "prod"), (128, "bf16", 3, "prod"),
+                                               (128, "bf16", 4, "prod"), (128, "f32", 3, "prod"),
+                                               (128, "bf16", 1, "mse"), (128, "bf16", 3, "mse"),
+                                               (128, "bf16", 4, "mse"), (128, "f32", 4, "mse"),
+                                               (256, "f32", 3, "prod"), (256, "bf16", 4, "prod"),
+                                               (256, "f32", 4, "mse")])
+@pytest.mark.parametrize("n", [2048, 4096 + 37])
+def test_quantize_polar_tensor_core_path(d, dtype, bits, kind, n):
+    """Polar-mode batches of >= 2048 rows (tcgen05 rotation and sketch, the
+    angle tree on the CUDA cores): <= 0.1% differing bits against the
+    oracle, each differing angle code a near-tie (its point within 1e-4 /
+    sqrt(d) of a cell boundary), scattered destinations, ragged last tile."""
+    ocb, gcb = pair(d, bits, kind, "polar", 0)
+    d_in = 200 if d == 256 else 128
+    x = wl.search_rows(n, "db") if d == 256 else np.concatenate(
+        [wl.llama_kv_slice(0, h, 0, 4096) for h in range(2)])[:n]
+    xt = torch.from_numpy(x).cuda()
+    if dtype == "bf16":
+        xt = xt.to(torch.bfloat16)
+    x64 = xt.float().cpu().numpy().astype(np.float64)
+    code = quant.quantize(ocb, x64)
+    rows = n + 100
+    perm = np.random.default_rng(n + bits).permutation(rows)[:n]
+    cache = gpu_cache(gcb, rows)
+    tq.tq_quantize(gcb, cache, rows, xt, n, d_in, dst_rows=torch.from_numpy(perm.astype(np.int64)).cuda())
+    tq.tq_check_device(gcb)
+    got = read_back(ocb, rows, cache)
+    bad = got["idx"][perm] != code["idx"]
+    flips = bad.sum()
+    nbits = code["idx"].size * ocb.b1
+    if kind == "prod":
+        flips += (got["sigma"][perm] != code["sigma"]).sum()
+        nbits += code["sigma"].size
+    assert flips <= 1e-3 * nbits, flips / nbits
+    if bad.any():
+        y, _ = quant.rotate(ocb, x64)
+        dist = polar_tie_distance(ocb, y)
+        assert np.all(dist[bad] < 1e-4 / math.sqrt(d)), float(np.max(dist[bad]))
+    n_ref = np.linalg.norm(x64, axis=1)
+    assert np.allclose(got["n16"][perm].astype(np.float64), n_ref, rtol=1e-3)
+    if kind == "prod":
+        # a flipped angle code moves a whole subtree's reproduction, so the
+        # residual norm is compared on the rows whose codes all agree
+        same = ~bad.any(axis=1)
+        assert same.mean() > 0.9
+        assert np.allclose(got["g16"][perm][same].astype(np.float64), code["gamma"][same], rtol=2e-3, atol=1e-4)
+
+
+@pytest.mark.parametrize("d,bits,kind", [(128, 4, "prod"), (128, 4, "mse"), (256, 3, "mse")])
+def test_quantize_polar_exact_ties_take_the_upper_cell(d, bits, kind):
+    """Level-1 pairs placed exactly on a boundary ray, and one ulp to either
+    side of it: the fp32 screen of the sign test cannot decide these, so the
+    exact fp64 products decide, and the codes equal the oracle's bit for bit
+    (a zero determinant goes to the upper cell)."""
+    ocb, gcb = pair(d, bits, kind, "polar", 0)
+    tab = ocb.polar
+    bc, bs = tab.bcos[1].astype(np.float32), tab.bsin[1].astype(np.float32)
+    rng = np.random.default_rng(d + bits)
+    n = 512
+    y = np.empty((n, d), dtype=np.float32)
+    for r in range(n):
+        j = rng.integers(0, len(bc), size=d // 2)
+        c, s_ = bc[j].copy(), bs[j].copy()
+        nudge = rng.integers(-1, 2, size=d // 2)       # -1, 0, +1 ulp on the sine
+        s_ = np.where(nudge > 0, np.nextafter(s_, np.float32(2)), np.where(nudge < 0, np.nextafter(s_, np.float32(-2)), s_))
+        scale = np.float32(2.0) ** rng.integers(-8, 1, size=d // 2).astype(np.float32)   # exact scaling
+        y[r, 0::2] = c * scale
+        y[r, 1::2] = s_ * scale
+    y /= np.float32(8.0)
+    nrm = np.ones(n, dtype=np.float32)
+    code = quant.encode_rotated(ocb, y.astype(np.float64), nrm.astype(np.float64))
+    cache = gpu_cache(gcb, n)
+    tq.tq_quantize_rotated(gcb, cache, n, torch.from_numpy(y).cuda(), torch.from_numpy(nrm).cuda(), n)
+    tq.tq_check_device(gcb)
+    got = read_back(ocb, n, cache)
+    assert np.array_equal(got["idx"], code["idx"])
+
+
+def kernels_of(fn):
+    """Names of the CUDA kernels one call launches."""
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    return {e.name for e in prof.events() if e.device_type.name == "CUDA"}
+
+
+@pytest.mark.parametrize("d,dtype,mode,n,kernel", [(128, "bf16", "scalar", 4096, "k_quantize_tc<"),
+                                                   (128, "f32", "scalar", 4096, "k_quantize_tcx<128"),
+                                                   (256, "f32", "scalar", 4096, "k_quantize_tcx<256"),
+                                                   (256, "bf16", "scalar", 4096, "k_quantize_tcx<256"),
+                                                   (128, "bf16", "polar", 4096, "k_quantize_tcx<128"),
+                                                   (128, "f32", "polar", 4096, "k_quantize_tcx<128"),
+                                                   (256, "f32", "polar", 4096, "k_quantize_tcx<256"),
+                                                   (128, "bf16", "scalar", 8, "k_quantize_row<128>"),
+                                                   (128, "bf16", "polar", 8, "k_quantize_simt<128>")])
+def test_quantize_batches_take_the_tensor_core_kernels(d, dtype, mode, n, kernel):
+    """Which kernel a batch takes: every batch of >= 2048 rows runs a tcgen05
+    kernel (launch list recorded by the profiler); short batches run the
+    row-wise CUDA-core kernels."""
+    gcb = tq.Codebook(d, 3, tq.KIND_PROD, MODE[mode])
+    d_in = 200 if d == 256 else 128
+    x = torch.randn(n, d_in, device="cuda", generator=torch.Generator("cuda").manual_seed(d + n))
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    cache = gpu_cache(gcb, n)
+    names = kernels_of(lambda: tq.tq_quantize(gcb, cache, n, x, n, d_in))
+    tq.tq_check_device(gcb)
+    assert any(kernel in nm for nm in names), names
 
 
 def check_search(ocb, gcb, x, q, k, expect_fallbacks=None):
