@@ -657,6 +657,8 @@ def run_quantize(args, dist, rank, steps):
     for name, bits, extra, mode in [("b2", 2, 0, "scalar"), ("b3", 3, 0, "scalar"), ("b4", 4, 0, "scalar"),
                                     ("b2.5", 2, 32, "scalar"), ("b3.5", 3, 32, "scalar"), ("polar_b3", 3, 0, "polar"),
                                     ("polar_b4", 4, 0, "polar")]:
+        if args.quantize_configs and name not in args.quantize_configs.split(","):
+            continue
         md = tq.MODE_POLAR if mode == "polar" else tq.MODE_SCALAR
         cb = tq.Codebook(d, bits, tq.KIND_PROD, md, extra=extra)
         caches = [torch.empty(tq.cache_bytes(cb, N), dtype=torch.uint8, device="cuda") for _ in range(2)]
@@ -800,6 +802,8 @@ def main():
     ap.add_argument("--attn-batch", type=int, default=ATTN["B"],
                     help="sequences in the attention workload (smaller batches for profiling)")
     ap.add_argument("--attn-modes", default="scalar,polar", help="comma list of stage-1 modes for attention")
+    ap.add_argument("--quantize-configs", default="",
+                    help="comma list of quantize lines to run (b2,b3,b4,b2.5,b3.5,polar_b3,polar_b4; default all)")
     ap.add_argument("--search-nq", type=int, default=10000, help="queries of the search workload (smaller for profiling)")
     ap.add_argument("--search-bits", default="2,4", help="comma list of database bit widths for search")
     args = ap.parse_args()

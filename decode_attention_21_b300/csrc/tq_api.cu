@@ -584,15 +584,15 @@ static tq_status quantize_common(const char* what, const tq_codebook* cb, void* 
   if (dev != cb->device) return fail(TQ_EINVAL, "%s: codebook lives on device %d, current device is %d", what, cb->device, dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // batches on the tensor cores with X in tensor memory: d = 256 (bf16 or
-  // fp32), d = 128 fp32 without extra-bit coordinates, and polar mode
-  const bool tcx =
-      cb->dev.d == 256 || (x_dtype == TQ_F32 && cb->dev.extra == 0) || cb->dev.mode == TQ_MODE_POLAR;
+  // fp32) and d = 128 fp32 without extra-bit coordinates (either mode)
+  const bool tcx = cb->dev.d == 256 || (x_dtype == TQ_F32 && cb->dev.extra == 0);
   if (!paged && !y && tcx && cb->tc_ready && n >= 2048 && d_in % (x_dtype == TQ_BF16 ? 8 : 4) == 0 &&
       aligned16(x) && n < (1ll << 31))
     return launched(what, tq::launch_quantize_tcx(cb->tm_pihi, cb->tm_pilo, cb->tm_s, cb->dev,
                                                   static_cast<uint8_t*>(cache), cache_rows, x, x_dtype == TQ_F32, n,
                                                   d_in, dst_rows, cb->d_status, cb->sms, s));
-  // d = 128 bf16 batches in scalar mode: tensor-core rotation and sketch
+  // d = 128 bf16 batches (scalar or polar mode): tensor-core rotation and
+  // sketch, X by TMA, two tile groups
   if (!paged && !y && cb->dev.d == 128 && x_dtype == TQ_BF16 && cb->tc_ready && n >= 2048 && d_in % 8 == 0 &&
       aligned16(x) && n < (1ll << 31)) {
     CUtensorMap tm_x;

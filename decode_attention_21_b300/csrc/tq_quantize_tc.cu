@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "tq_internal.cuh"
+#include "tq_polar.cuh"
 #include "tq_tc.cuh"
 
 namespace tq {
@@ -43,8 +44,8 @@ constexpr uint32_t kOffX = 0;                          // kStages x kTileBytes
 constexpr uint32_t kOffPiHi = kStages * kTileBytes;
 constexpr uint32_t kOffPiLo = kOffPiHi + kTileBytes;
 constexpr uint32_t kOffS = kOffPiLo + kTileBytes;
-constexpr uint32_t kOffRed = kOffS + kTileBytes;       // float red1[2][4][128], red2[2][4][128]
-constexpr uint32_t kOffBar = kOffRed + 2 * 2 * 4 * kRows * 4;
+constexpr uint32_t kOffRed = kOffS + kTileBytes;       // float red1[2][4][128], red2[2][4][128], red3[2][4][128]
+constexpr uint32_t kOffBar = kOffRed + 3 * 2 * 4 * kRows * 4;
 // mbarriers: full[kStages], const, y[2], z[2]; then the TMEM base and the
 // per-stage counts of issued and consumed loads
 constexpr uint32_t kOffTmem = kOffBar + 8 * (kStages + 5);
@@ -57,7 +58,9 @@ using namespace tc;
 
 }  // namespace
 
-template <int B1, bool PROD, bool EXT>
+// POLAR: the recursive-polar stage 1 (B1 bits per angle) instead of the
+// scalar one (no extra-bit words).
+template <int B1, bool PROD, bool EXT, bool POLAR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_quantize_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pihi,
                   const __grid_constant__ CUtensorMap tm_pilo, const __grid_constant__ CUtensorMap tm_s, const Dev cb,
@@ -77,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m = 32 * q + lane;                       // tile row = TMEM lane
   float* red1 = reinterpret_cast<float*>(smem + kOffRed) + g * 4 * kRows;
   float* red2 = reinterpret_cast<float*>(smem + kOffRed) + (2 + g) * 4 * kRows;
+  float* red3 = reinterpret_cast<float*>(smem + kOffRed) + (4 + g) * 4 * kRows;   // polar block radii
   const uint32_t bar0 = sbase + kOffBar;
   auto bar_full = [&](int st) { return bar0 + 8u * st; };
   const uint32_t bar_const = bar0 + 8u * kStages;
@@ -103,6 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // outlier-channel split: word columns cg < kx are group A, with its own norms
   const int kx = cb.split ? cb.extra / 32 : 0;
+  __shared__ polar::Tables tpol;                     // polar mode only
+  if constexpr (POLAR) polar::load_tables(cb, tpol, tid, kThreads);
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -202,6 +208,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     group_sync(g);
     uint32_t words[2][P + 1];   // per column group: code planes, then the extra low bit (EXT columns)
     float nrm0 = 0.f;           // column group 2 wh's norm (the norm entry's writer uses it)
+    if constexpr (POLAR) {
+      float tot = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tot += red1[k * kRows + m];
+      nrm0 = sqrtf(tot);
+      const float inv = nrm0 > 0.f ? 1.f / nrm0 : 0.f;
+      float gs = 0.f;
+      polar::epilogue<128, 2, B1, PROD>(tpol, tg + lane_off, t_rhi + lane_off, t_rlo + lane_off, 2 * wh, inv, red3, m,
+                                        words, gs, [&] { group_sync(g); });
+      red2[(2 * wh) * kRows + m] = gs;
+      red2[(2 * wh + 1) * kRows + m] = 0.f;
+    } else {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int cg = 2 * wh + h;
@@ -253,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       red2[cg * kRows + m] = gs;
+    }
     }
     if (prod) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     fence_before();
@@ -361,21 +380,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int B1, bool PROD, bool EXT>
+template <int B1, bool PROD, bool EXT, bool POLAR>
 static cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_pihi, const CUtensorMap& tm_pilo,
                                const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
                                const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_tc<B1, PROD, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_tc<B1, PROD, EXT, POLAR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t ntiles = (n + kRows - 1) / kRows;
   const int grid = (int)(ntiles < sms ? ntiles : sms);
-  k_quantize_tc<B1, PROD, EXT><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows,
-                                                                  n, dst_rows, status);
+  k_quantize_tc<B1, PROD, EXT, POLAR><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache,
+                                                                         cache_rows, n, dst_rows, status);
   return cudaGetLastError();
 }
 
@@ -383,7 +402,24 @@ cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pi
                                const CUtensorMap& tm_s, const Dev& cb, uint8_t* cache, int64_t cache_rows, int64_t n,
                                const int64_t* dst_rows, int* status, int sms, cudaStream_t s) {
 #define TQ_TC(B, PR, EX) \
-  return launch_tc_t<B, PR, EX>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, n, dst_rows, status, sms, s)
+  return launch_tc_t<B, PR, EX, false>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, n, dst_rows, status, sms, s)
+#define TQ_TCP(B, PR) \
+  return launch_tc_t<B, PR, false, true>(tm_x, tm_pihi, tm_pilo, tm_s, cb, cache, cache_rows, n, dst_rows, status, sms, s)
+  if (cb.mode != 0) {   // polar mode (no extra-bit words)
+    if (cb.kind == 0) {
+      switch (cb.b1) {
+        case 1: TQ_TCP(1, true);
+        case 2: TQ_TCP(2, true);
+        default: TQ_TCP(3, true);
+      }
+    }
+    switch (cb.b1) {
+      case 1: TQ_TCP(1, false);
+      case 2: TQ_TCP(2, false);
+      case 3: TQ_TCP(3, false);
+      default: TQ_TCP(4, false);
+    }
+  }
   const bool ext = cb.extra != 0;
   if (cb.kind == 0) {
     switch (cb.b1 * 2 + (ext ? 1 : 0)) {
@@ -404,6 +440,7 @@ cudaError_t launch_quantize_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_pi
     case 7: TQ_TC(3, false, true);
     default: TQ_TC(4, false, false);
   }
+#undef TQ_TCP
 #undef TQ_TC
 }
 

@@ -5,8 +5,8 @@ Each output (cache, logits, attention output, search ids and scores, and
 the workspaces) is the front of a larger byte buffer whose tail holds a
 canary pattern; after the call the tail must be byte-for-byte unchanged.
 The cases reach every quantize kernel (two-group tensor-core, tensor-memory
-operand at d = 128 fp32 and d = 256, row-per-warp, short-batch) and the
-scoring kernels.  The allocation hook makes the n-th device allocation of
+operand at d = 128 fp32 and d = 256, in scalar and polar mode; row-per-warp,
+short-batch) and the scoring kernels.  The allocation hook makes the n-th device allocation of
 tq_make_codebook fail: the call must return TQ_ENOMEM and leave a working
 library behind.
 """
@@ -36,11 +36,13 @@ def tail_intact(buf, nbytes):
     return bool(torch.all(buf[nbytes:] == CANARY))
 
 
-@pytest.mark.parametrize("d,dtype,n,extra", [(128, "bf16", 4096, 0), (128, "bf16", 4096, 32), (128, "f32", 4096, 0),
-                                             (256, "f32", 4096, 0), (256, "bf16", 2048 + 5, 0), (128, "bf16", 100, 0),
-                                             (128, "f32", 20000, 32)])
-def test_quantize_writes_stay_inside_the_cache(d, dtype, n, extra):
-    cb = tq.Codebook(d, 3, tq.KIND_PROD, extra=extra)
+@pytest.mark.parametrize("d,dtype,n,extra,mode", [(128, "bf16", 4096, 0, 0), (128, "bf16", 4096, 32, 0),
+                                                  (128, "f32", 4096, 0, 0), (256, "f32", 4096, 0, 0),
+                                                  (256, "bf16", 2048 + 5, 0, 0), (128, "bf16", 100, 0, 0),
+                                                  (128, "f32", 20000, 32, 0), (128, "bf16", 4096 + 7, 0, 1),
+                                                  (128, "f32", 4096, 0, 1), (256, "bf16", 2048 + 5, 0, 1)])
+def test_quantize_writes_stay_inside_the_cache(d, dtype, n, extra, mode):
+    cb = tq.Codebook(d, 3, tq.KIND_PROD, tq.MODE_POLAR if mode else tq.MODE_SCALAR, extra=extra)
     d_in = 200 if d == 256 else 128
     x = wl.search_rows(n, "db") if d == 256 else np.concatenate(
         [wl.llama_kv_slice(0, h, 0, 4096) for h in range(-(-n // 4096))])[:n]
@@ -133,12 +135,13 @@ def test_codebook_allocation_failure_is_reported_and_recovered():
     assert int(cache.sum()) > 0
 
 
-@pytest.mark.parametrize("d,dtype,extra", [(128, "bf16", 0), (128, "f32", 0), (256, "f32", 0), (256, "bf16", 0),
-                                           (128, "bf16", 32)])
-def test_quantize_destination_outside_the_cache_is_skipped_and_flagged(d, dtype, extra):
+@pytest.mark.parametrize("d,dtype,extra,mode", [(128, "bf16", 0, 0), (128, "f32", 0, 0), (256, "f32", 0, 0),
+                                                (256, "bf16", 0, 0), (128, "bf16", 32, 0), (128, "bf16", 0, 1),
+                                                (256, "f32", 0, 1)])
+def test_quantize_destination_outside_the_cache_is_skipped_and_flagged(d, dtype, extra, mode):
     # a destination row past the cache is not written (the canary tail stays)
     # and tq_check_device reports TQ_EINVAL; every other row is written
-    cb = tq.Codebook(d, 3, tq.KIND_PROD, extra=extra)
+    cb = tq.Codebook(d, 3, tq.KIND_PROD, tq.MODE_POLAR if mode else tq.MODE_SCALAR, extra=extra)
     n, rows = 4096, 5000
     d_in = 256 if d == 256 else 128
     x = np.random.default_rng(d).standard_normal((n, d_in)).astype(np.float32)

@@ -705,7 +705,7 @@ def kernels_of(fn):
                                                    (128, "f32", "scalar", 4096, "k_quantize_tcx<128"),
                                                    (256, "f32", "scalar", 4096, "k_quantize_tcx<256"),
                                                    (256, "bf16", "scalar", 4096, "k_quantize_tcx<256"),
-                                                   (128, "bf16", "polar", 4096, "k_quantize_tcx<128"),
+                                                   (128, "bf16", "polar", 4096, "k_quantize_tc<"),
                                                    (128, "f32", "polar", 4096, "k_quantize_tcx<128"),
                                                    (256, "f32", "polar", 4096, "k_quantize_tcx<256"),
                                                    (128, "bf16", "scalar", 8, "k_quantize_row<128>"),
