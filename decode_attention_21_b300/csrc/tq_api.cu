@@ -98,9 +98,9 @@ constexpr long long kDefaultWaitPolls = 1ll << 26;   // polls of a bounded devic
 constexpr int kLogitsCtas = 148 * 4;   // resident CTAs of the logits kernel
 // Resident CTAs of the attention kernel (one wave): 4 per SM, 3 for keys
 // with four or more stage-1 virtual planes or extra-bit words (more
-// registers), 2 in polar mode.
+// registers), 3 in polar mode.
 int attn_ctas(const tq_codebook* kcb, const tq_codebook* vcb = nullptr) {
-  if (kcb->dev.mode == TQ_MODE_POLAR) return 148 * 2;
+  if (kcb->dev.mode == TQ_MODE_POLAR) return 148 * 3;
   const bool heavy = kcb->dev.nv >= 4 || kcb->dev.extra > 0 || (vcb && vcb->dev.extra > 0);
   return heavy ? 148 * 3 : 148 * 4;
 }

@@ -6,10 +6,15 @@
 // in scalar mode.  d = 128, tree of 7 levels, subtrees of 32 leaves per
 // packed word (see the polar layout in tq.h).
 //
-//   logits: A = decoded keys (16 keys x 16 coordinates, hi then lo),
+//   logits: A = decoded keys (16 keys x 16 coordinates, hi then lo; a
+//           thread's k slots 2c, 2c + 1, 2c + 8, 2c + 9 of k block kb are
+//           coordinates 4 kb .. 4 kb + 3 of its subtree c, so each half of
+//           the subtree is decoded and consumed on its own),
 //           B = q' (fp16 hi/lo columns of the G <= 4 heads);
-//   attention PV: A = decoded values (16 coordinates x 16 tokens, the two
-//           tokens of a pair in the two fp16 halves), B = p_t n_v,t.
+//   attention PV: A = decoded values (16 coordinates x 8 tokens per m16n8k8,
+//           the two tokens of a pair in the two fp16 halves: tokens 2c,
+//           2c + 1, then 2c + 8, 2c + 9 of the tile), B = p_t n_v,t.
+// The query fragments are read from shared memory where they are used.
 #include <cuda_fp16.h>
 
 #include "tq_internal.cuh"
@@ -184,8 +189,11 @@ __global__ void __launch_bounds__(512) k_prep_polar(const Dev cb, const float* _
     float vals[4] = {0.f, 0.f, 0.f, 0.f};
     if (live) {
       for (int t = 0; t < 4; ++t) {
+        // stage 1: k slots 2c, 2c + 1, 2c + 8, 2c + 9 = coordinates
+        // 4 kb + t of subtree c; QJL: bits beta and beta + 16 of the sign
+        // word (the bit-operand layout of scalar mode)
         const int beta = 2 * kb + (t >> 1);
-        const int k = 32 * c + beta + 16 * (t & 1);
+        const int k = v == 0 ? 32 * c + 4 * kb + t : 32 * c + beta + 16 * (t & 1);
         const float x = v == 0 ? sq1[k] / S1 : 2.f * sq2[k] * bit_factor(beta) / S2;
         vals[t] = piece16(x, pc);
       }
@@ -233,31 +241,27 @@ struct PKey {
     }
     nrm = valid ? nrm_bits : 0u;
   }
-  // the 32 leaves of subtree c (unit row)
-  __device__ __forceinline__ void decode(const PolarTab& tab, int c, float (&y)[32]) const {
+  // leaves 16 h .. 16 h + 15 of subtree c (unit row), from its radius rho5
+  __device__ __forceinline__ void decode_h(const PolarTab& tab, float rho5, int h, float (&y)[16]) const {
     uint32_t cw[B];
 #pragma unroll
     for (int p = 0; p < B; ++p) cw[p] = ws[p];
-    const float rho5 = subtree_radius<B>(tab, w0, w6, c);
-    float lo[16], hi[16];
-    decode_half<B>(tab, cw, rho5, 0, lo);
-    decode_half<B>(tab, cw, rho5, 1, hi);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      y[i] = lo[i];
-      y[16 + i] = hi[i];
-    }
+    decode_half<B>(tab, cw, rho5, h, y);
   }
 };
 
+// The query fragments of one (sequence, kv head) from the prep block into
+// shared memory: [plane][k block][lane].
+__device__ __forceinline__ void load_frags(const uint8_t* blk, uint2* sfrag) {
+  const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
+  for (int e = threadIdx.x; e < 2 * 8 * 32; e += blockDim.x) sfrag[e] = frag[e];
+}
+
 // inner products (stage 1, QJL) of keys g and g+8 for head slot c
 template <int B>
-__device__ __forceinline__ void polar_qk(const PolarTab& tab, const uint2 (&bq)[2][8], const PKey<B>& ka,
+__device__ __forceinline__ void polar_qk(const PolarTab& tab, const uint2* sfrag, int lane, const PKey<B>& ka,
                                          const PKey<B>& kb_, int c, float& s1a, float& s1b, float& s2a,
                                          float& s2b) {
-  float ya[32], yb[32];
-  ka.decode(tab, c, ya);
-  kb_.decode(tab, c, yb);
   float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   {
@@ -265,24 +269,47 @@ __device__ __forceinline__ void polar_qk(const PolarTab& tab, const uint2 (&bq)[
     expand16(ka.ws[B], ra);
     expand16(kb_.ws[B], rb);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      mma_f16(acc2[k & 1], ra[2 * k], rb[2 * k], ra[2 * k + 1], rb[2 * k + 1], bq[1][k].x, bq[1][k].y);
+    for (int k = 0; k < 8; ++k) {
+      const uint2 bq = sfrag[(8 + k) * 32 + lane];
+      mma_f16(acc2[k & 1], ra[2 * k], rb[2 * k], ra[2 * k + 1], rb[2 * k + 1], bq.x, bq.y);
+    }
   }
+  const float rha = subtree_radius<B>(tab, ka.w0, ka.w6, c), rhb = subtree_radius<B>(tab, kb_.w0, kb_.w6, c);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int be = 2 * k;
-    uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-    split2(ya[be], ya[be + 16], h0, l0);
-    split2(yb[be], yb[be + 16], h1, l1);
-    split2(ya[be + 1], ya[be + 17], h2, l2);
-    split2(yb[be + 1], yb[be + 17], h3, l3);
-    mma_f16(acc1[0], h0, h1, h2, h3, bq[0][k].x, bq[0][k].y);
-    mma_f16(acc1[1], l0, l1, l2, l3, bq[0][k].x, bq[0][k].y);
+  for (int h = 0; h < 2; ++h) {
+    float ya[16], yb[16];
+    ka.decode_h(tab, rha, h, ya);
+    kb_.decode_h(tab, rhb, h, yb);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint2 bq = sfrag[(4 * h + kk) * 32 + lane];
+      uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+      split2(ya[4 * kk], ya[4 * kk + 1], h0, l0);
+      split2(yb[4 * kk], yb[4 * kk + 1], h1, l1);
+      split2(ya[4 * kk + 2], ya[4 * kk + 3], h2, l2);
+      split2(yb[4 * kk + 2], yb[4 * kk + 3], h3, l3);
+      mma_f16(acc1[0], h0, h1, h2, h3, bq.x, bq.y);
+      mma_f16(acc1[1], l0, l1, l2, l3, bq.x, bq.y);
+    }
   }
   s1a = (acc1[0][0] + acc1[0][1]) + (acc1[1][0] + acc1[1][1]);
   s1b = (acc1[0][2] + acc1[0][3]) + (acc1[1][2] + acc1[1][3]);
   s2a = (acc2[0][0] + acc2[0][1]) + (acc2[1][0] + acc2[1][1]);
   s2b = (acc2[0][2] + acc2[0][3]) + (acc2[1][2] + acc2[1][3]);
+}
+
+// PV of one k8 half of a tile: yv[j][i] = coordinate i of the thread's 16
+// for token 2c + j (+ 8 for the second half), bw = the weights of those two
+// tokens (this thread's fp16 piece); hi pieces, then lo, per accumulator.
+__device__ __forceinline__ void pv_pair(float (&acc)[8][4], const float (&yv)[2][16], uint32_t bw) {
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    uint32_t h0, l0, h1, l1;
+    split2(yv[0][2 * mt], yv[1][2 * mt], h0, l0);
+    split2(yv[0][2 * mt + 1], yv[1][2 * mt + 1], h1, l1);
+    mma_f16_k8(acc[mt], h0, h1, bw);
+    mma_f16_k8(acc[mt], l0, l1, bw);
+  }
 }
 
 __device__ __forceinline__ float est_polar(uint32_t nrm_bits, float s1, float s2, float kq) {
@@ -297,9 +324,12 @@ __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_
                                                       const uint8_t* __restrict__ prep, float* __restrict__ logits,
                                                       int tiles_per_cta, int* __restrict__ status) {
   __shared__ PolarTab tab;
+  __shared__ uint2 sfrag[2 * 8 * 32];
   load_tab(cb, tab);
-  __syncthreads();
   const int kvh = blockIdx.y, b = blockIdx.z;
+  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
+  load_frags(blk, sfrag);
+  __syncthreads();
   const int G = Hq / Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -308,13 +338,6 @@ __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_
   const int64_t tile0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t tend = min(tile0 + tiles_per_cta, ntiles);
   if (tile0 + warp >= tend) return;
-  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
-  const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
-  uint2 bq[2][8];
-#pragma unroll
-  for (int v = 0; v < 2; ++v)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) bq[v][k] = frag[(v * 8 + k) * 32 + lane];
   const float* hdr = reinterpret_cast<const float*>(blk);
   const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
   const uint32_t* recs = reinterpret_cast<const uint32_t*>(kcache);
@@ -328,7 +351,7 @@ __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_
     ka.load(recs, nrm, row0 + g, cb.W, c, ta < L);
     kb_.load(recs, nrm, row0 + g + 8, cb.W, c, tb < L);
     float s1a, s1b, s2a, s2b;
-    polar_qk<B>(tab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
+    polar_qk<B>(tab, sfrag, lane, ka, kb_, c, s1a, s1b, s2a, s2b);
     if (c < G) {
       if (ta < L) out[ta] = est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq);
       if (tb < L) out[tb] = est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq);
@@ -337,17 +360,20 @@ __global__ void __launch_bounds__(128) k_logits_polar(const Dev cb, const uint8_
 }
 
 template <int BK, int BV>
-__global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev vcb, const uint8_t* __restrict__ kcache,
+__global__ void __launch_bounds__(128, 3) k_attn_polar(const Dev kcb, const Dev vcb, const uint8_t* __restrict__ kcache,
                                                        const uint8_t* __restrict__ vcache, int Hq, int Hkv,
                                                        int64_t capacity, int64_t cache_rows,
                                                        const int32_t* __restrict__ seq_lens,
                                                        const uint8_t* __restrict__ prep, float scale_log2,
                                                        float* __restrict__ partials, int tiles_per_cta) {
   __shared__ PolarTab ktab, vtab;
+  __shared__ uint2 sfrag[2 * 8 * 32];
   load_tab(kcb, ktab);
   load_tab(vcb, vtab);
-  __syncthreads();
   const int kvh = blockIdx.y, b = blockIdx.z;
+  const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
+  load_frags(blk, sfrag);
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int64_t L = seq_lens[b];
@@ -363,13 +389,6 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
   PvTotal tot;
   tot.zero();
   if (tile0 + warp < tend) {
-    const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
-    const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
-    uint2 bq[2][8];
-#pragma unroll
-    for (int v = 0; v < 2; ++v)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) bq[v][k] = frag[(v * 8 + k) * 32 + lane];
     const float* hdr = reinterpret_cast<const float*>(blk);
     const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
     const uint32_t* krec = reinterpret_cast<const uint32_t*>(kcache);
@@ -388,7 +407,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
       ka.load(krec, knrm, rowbase + ta, kcb.W, c, ta < L);
       kb_.load(krec, knrm, rowbase + tb, kcb.W, c, tb < L);
       float s1a, s1b, s2a, s2b;
-      polar_qk<BK>(ktab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
+      polar_qk<BK>(ktab, sfrag, lane, ka, kb_, c, s1a, s1b, s2a, s2b);
       const float sa = ta < L ? est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq) * scale_log2 : -INFINITY;
       const float sb = tb < L ? est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq) * scale_log2 : -INFINITY;
       float mx = fmaxf(sa, sb);
@@ -420,37 +439,31 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
       const float w9 = __shfl_sync(kFull, wB, src1);
       const uint32_t b0 = piece2(w0, w1, pc);
       const uint32_t b1 = piece2(w8, w9, pc);
-      // decode this thread's 16 value coordinates of tokens 2c, 2c+1, 2c+8, 2c+9
-      float yv[4][16];
+      // this thread's 16 value coordinates of tokens 2c, 2c+1 (the first
+      // k8 half of the tile), then of tokens 2c+8, 2c+9
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t t = t0 + 2 * c + (j & 1) + 8 * (j >> 1);
-        uint32_t wsv[BV], w0v[BV], w6v[BV];
-        if (t < L) {
-          const uint32_t* r = vrec + (rowbase + t) * vcb.W;
+      for (int hk = 0; hk < 2; ++hk) {
+        float yv[2][16];
 #pragma unroll
-          for (int p = 0; p < BV; ++p) {
-            wsv[p] = __ldg(r + vs * BV + p);
-            w0v[p] = __ldg(r + p);
-            w6v[p] = __ldg(r + (1 + (vs >> 1)) * BV + p);
+        for (int j = 0; j < 2; ++j) {
+          const int64_t t = t0 + 2 * c + j + 8 * hk;
+          uint32_t wsv[BV], w0v[BV], w6v[BV];
+          if (t < L) {
+            const uint32_t* r = vrec + (rowbase + t) * vcb.W;
+#pragma unroll
+            for (int p = 0; p < BV; ++p) {
+              wsv[p] = __ldg(r + vs * BV + p);
+              w0v[p] = __ldg(r + p);
+              w6v[p] = __ldg(r + (1 + (vs >> 1)) * BV + p);
+            }
+            const float rho5 = subtree_radius<BV>(vtab, w0v, w6v, vs);
+            decode_half<BV>(vtab, wsv, rho5, vh, yv[j]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) yv[j][i] = 0.f;
           }
-          const float rho5 = subtree_radius<BV>(vtab, w0v, w6v, vs);
-          decode_half<BV>(vtab, wsv, rho5, vh, yv[j]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) yv[j][i] = 0.f;
         }
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int r0 = 2 * mt, r1 = 2 * mt + 1;
-        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-        split2(yv[0][r0], yv[1][r0], h0, l0);
-        split2(yv[0][r1], yv[1][r1], h1, l1);
-        split2(yv[2][r0], yv[3][r0], h2, l2);
-        split2(yv[2][r1], yv[3][r1], h3, l3);
-        mma_f16(acc[mt], h0, h1, h2, h3, b0, b1);     // value hi pieces, then lo (same order per accumulator)
-        mma_f16(acc[mt], l0, l1, l2, l3, b0, b1);
+        pv_pair(acc, yv, hk ? b1 : b0);
       }
       if (++chain == 2 * kPvFlushStages) {
         tot.flush(acc);
@@ -479,7 +492,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar(const Dev kcb, const Dev 
 // reads shared memory instead of waiting on global loads.  Arithmetic as in
 // k_attn_polar.
 template <int BK, int BV>
-__global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, const Dev vcb,
+__global__ void __launch_bounds__(128, 3) k_attn_polar_staged(const Dev kcb, const Dev vcb,
                                                            const uint8_t* __restrict__ kcache,
                                                            const uint8_t* __restrict__ vcache, int Hq, int Hkv,
                                                            int64_t capacity, int64_t cache_rows, const RowMap map,
@@ -495,6 +508,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ __align__(8) uint64_t bars[kRing];
   __shared__ PolarTab ktab, vtab;
+  __shared__ uint2 sfrag[2 * 8 * 32];
   load_tab(kcb, ktab);
   load_tab(vcb, vtab);
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -553,12 +567,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
   for (int st = 0; st < min(nst, kRing); ++st) request(st, min(kStageTiles, nt - st * kStageTiles));
   int issued = min(nst, kRing);
   const uint8_t* blk = prep + ((size_t)b * Hkv + kvh) * prep_block_bytes(128);
-  const uint2* frag = reinterpret_cast<const uint2*>(blk + kPrepHeader);
-  uint2 bq[2][8];
-#pragma unroll
-  for (int v = 0; v < 2; ++v)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) bq[v][k] = frag[(v * 8 + k) * 32 + lane];
+  load_frags(blk, sfrag);
   const float* hdr = reinterpret_cast<const float*>(blk);
   const float S1 = hdr[c], S2 = hdr[4 + c], K2 = hdr[12 + c];
   __syncthreads();                           // tables and barriers ready
@@ -597,7 +606,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
       kb_.load_row(reinterpret_cast<const uint32_t*>(base + ((size_t)lt * 16 + g + 8) * RBK), skn[lt * 16 + g + 8], c,
                    tb < L);
       float s1a, s1b, s2a, s2b;
-      polar_qk<BK>(ktab, bq, ka, kb_, c, s1a, s1b, s2a, s2b);
+      polar_qk<BK>(ktab, sfrag, lane, ka, kb_, c, s1a, s1b, s2a, s2b);
       const float sa = ta < L ? est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq) * scale_log2 : -INFINITY;
       const float sb = tb < L ? est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq) * scale_log2 : -INFINITY;
       float mx = fmaxf(sa, sb);
@@ -629,37 +638,31 @@ __global__ void __launch_bounds__(128, 2) k_attn_polar_staged(const Dev kcb, con
       const float w9 = __shfl_sync(kFull, wB, src1);
       const uint32_t b0 = piece2(w0, w1, pc);
       const uint32_t b1 = piece2(w8, w9, pc);
-      // decode this thread's 16 value coordinates of tokens 2c, 2c+1, 2c+8, 2c+9
-      float yv[4][16];
+      // this thread's 16 value coordinates of tokens 2c, 2c+1 (the first
+      // k8 half of the tile), then of tokens 2c+8, 2c+9
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tok = 2 * c + (j & 1) + 8 * (j >> 1);
-        if (t0 + tok < L) {
-          const uint32_t* r = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV);
-          uint32_t wsv[BV], w0v[BV], w6v[BV];
+      for (int hk = 0; hk < 2; ++hk) {
+        float yv[2][16];
 #pragma unroll
-          for (int p = 0; p < BV; ++p) {
-            wsv[p] = r[vs * BV + p];
-            w0v[p] = r[p];
-            w6v[p] = r[(1 + (vs >> 1)) * BV + p];
+        for (int j = 0; j < 2; ++j) {
+          const int tok = 2 * c + j + 8 * hk;
+          if (t0 + tok < L) {
+            const uint32_t* r = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV);
+            uint32_t wsv[BV], w0v[BV], w6v[BV];
+#pragma unroll
+            for (int p = 0; p < BV; ++p) {
+              wsv[p] = r[vs * BV + p];
+              w0v[p] = r[p];
+              w6v[p] = r[(1 + (vs >> 1)) * BV + p];
+            }
+            const float rho5 = subtree_radius<BV>(vtab, w0v, w6v, vs);
+            decode_half<BV>(vtab, wsv, rho5, vh, yv[j]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) yv[j][i] = 0.f;
           }
-          const float rho5 = subtree_radius<BV>(vtab, w0v, w6v, vs);
-          decode_half<BV>(vtab, wsv, rho5, vh, yv[j]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) yv[j][i] = 0.f;
         }
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int q0 = 2 * mt, q1 = 2 * mt + 1;
-        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-        split2(yv[0][q0], yv[1][q0], h0, l0);
-        split2(yv[0][q1], yv[1][q1], h1, l1);
-        split2(yv[2][q0], yv[3][q0], h2, l2);
-        split2(yv[2][q1], yv[3][q1], h3, l3);
-        mma_f16(acc[mt], h0, h1, h2, h3, b0, b1);     // value hi pieces, then lo (same order per accumulator)
-        mma_f16(acc[mt], l0, l1, l2, l3, b0, b1);
+        pv_pair(acc, yv, hk ? b1 : b0);
       }
     }
     if (st % kPvFlushStages == kPvFlushStages - 1) tot.flush(acc);
