@@ -36,6 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 126 * 2 ** 20
+# device time of untimed work enqueued right before each timed region (see timed)
+WARM_MS = 30.0
 FALLBACK_HBM_GBS = 6400.0
 
 
@@ -165,10 +167,25 @@ def capture(steps_fn, n):
     return g
 
 
-def timed(dist, fn):
-    """Milliseconds of fn() on the device, max over ranks."""
+def timed(dist, fn, warm_ms=WARM_MS):
+    """Milliseconds of fn() on the device, max over ranks.
+
+    After the barrier, untimed repeats of fn() worth about warm_ms of device
+    time are enqueued ahead of the first event, so that a short timed region
+    starts on a busy GPU at its working clock rather than after an idle gap;
+    the events bracket exactly one fn()."""
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 0
+    if warm_ms > 0:
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        reps = 0 if t >= warm_ms else min(2000, math.ceil(warm_ms / max(t, 1e-3)))
     barrier(dist)
+    for _ in range(reps):
+        fn()
     e0.record()
     fn()
     e1.record()
@@ -181,16 +198,12 @@ def timed(dist, fn):
 def per_call_ms(fn, n):
     """Average device duration of one fn(i): n calls captured back to back in a
     CUDA graph, timed with events around the replay on the launching stream
-    (host-side call overhead is excluded, inter-kernel gaps are included)."""
+    (host-side call overhead is excluded, inter-kernel gaps are included),
+    after untimed replays that keep the GPU busy up to the timed one."""
     g = capture(fn, n)
     g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / n
+    return timed(None, g.replay) / n
 
 
 def cores():
@@ -272,12 +285,18 @@ def run_logits(args, dist, rank):
     seq = torch.full((B,), T, dtype=torch.int32, device="cuda")
     ws = torch.empty(tq.tq_logits_workspace(kcb, B, Hq, Hkv), dtype=torch.uint8, device="cuda")
 
-    def step(i):
+    def step_separate(i):
         j = i % NC
         tq.tq_quantize(kcb, caches[j], rows, xnew[j], B * Hkv, d, dst_rows=dst_new)
         tq.tq_logits(kcb, caches[j], B, Hq, Hkv, T, seq, qs[j], outs[j], ws)
 
+    def step(i):
+        # the same step in one call: the append rides in the query-prep launch
+        j = i % NC
+        tq.tq_append_logits(kcb, caches[j], xnew[j], B * Hkv, d, dst_new, B, Hq, Hkv, T, seq, qs[j], outs[j], ws)
+
     for i in range(args.warmup):
+        step_separate(i)
         step(i)
     torch.cuda.synchronize()
     graph = capture(step, args.steps)
@@ -287,6 +306,11 @@ def run_logits(args, dist, rank):
     clocks.start()
     ms = timed(dist, graph.replay)
     clk = clocks.stop()
+    # the step as two calls (tq_quantize, then tq_logits), for comparison
+    graph_sep = capture(step_separate, args.steps)
+    graph_sep.replay()
+    torch.cuda.synchronize()
+    ms_separate = timed(dist, graph_sep.replay)
     keys = B * Hkv * T
     value = args.steps * keys * args.world / (ms / 1e3)
 
@@ -323,8 +347,7 @@ def run_logits(args, dist, rank):
                 main.wait_event(copied[i - NC])      # outs[j] has been read back
             xd.copy_(xh[j], non_blocking=True)
             qd.copy_(qh[j], non_blocking=True)
-            tq.tq_quantize(kcb, caches[j], rows, xd, B * Hkv, d, dst_rows=dst_new)
-            tq.tq_logits(kcb, caches[j], B, Hq, Hkv, T, seq, qd, outs[j], ws)
+            tq.tq_append_logits(kcb, caches[j], xd, B * Hkv, d, dst_new, B, Hq, Hkv, T, seq, qd, outs[j], ws)
             done[i].record(main)
             copy_stream.wait_event(done[i])
             with torch.cuda.stream(copy_stream):
@@ -362,7 +385,8 @@ def run_logits(args, dist, rank):
                    "stage1_bits": bits - 1, "qjl_rows": d, "packed_bytes_per_key": tq.record_bytes(kcb) + 4,
                    "l2": f"inputs larger than L2: steps rotate over {NC} cache copies "
                          f"({NC * (cbytes + out_bytes) / 2**20:.0f} MiB)",
-                   "cuda_graph": True},
+                   "cuda_graph": True, "step_call": "tq_append_logits (append fused into the query-prep launch)"},
+        "step_two_calls_ms": ms_separate / args.steps,     # tq_quantize + tq_logits, same graph timing
         "query_head_scores_per_s": value * G,
         "packed_gbs": args.steps * packed * args.world / (ms / 1e3) / 1e9,
         "roofline": {"kernel": "tq_logits (query prep + tensor-core scoring)", "bound": "hbm",
@@ -374,7 +398,7 @@ def run_logits(args, dist, rank):
                      "launch_ms": k_ms, "traffic": traffic},
         "e2e": {"value": e2e_value, "unit": "keys/s", "h2d_bytes_per_step": xnew[0].numel() * 2 + qs[0].numel() * 4,
                 "d2h_bytes_per_step": out_bytes},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,                    # k_prep_append + k_logits_staged per step
         "clocks": clk,
     }
     if rank == 0 and args.world == 1:
@@ -637,7 +661,7 @@ def run_paged_loop(dist, tq, kcb, vcb, kc, vc, B, Hq, Hkv, T, q, knew, vnew, ps,
     graph = capture(step, steps)
     graph.replay()
     torch.cuda.synchronize()
-    ms = timed(dist, graph.replay)
+    ms = timed(dist, graph.replay, warm_ms=0)     # every replay advances the lengths: no extra replays
     tq.tq_check_device(kcb)
     tq.tq_check_device(vcb)
     del kp, vp, pages
@@ -836,7 +860,7 @@ def main():
             "vs_baseline": None, "dtype": res.get("dtype", "f32"), "data": "synthetic (seeded)",
             "impl": "ours"}
     for k in ("config", "query_head_scores_per_s", "packed_gbs", "roofline", "cpu_baseline", "e2e", "gpu_launches",
-              "comparator", "paged",
+              "comparator", "paged", "step_two_calls_ms",
               "clocks"):
         if k in res:
             line[k] = res[k]

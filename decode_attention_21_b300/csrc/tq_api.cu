@@ -639,10 +639,20 @@ static tq_status check_heads(const char* what, int32_t B, int32_t Hq, int32_t Hk
   return TQ_OK;
 }
 
+// A decode step's key append carried by the first query-prep launch (see
+// tq_append_logits); n = 0: none.
+struct FusedAppend {
+  const void* x = nullptr;
+  int32_t x_dtype = 0;
+  int64_t n = 0;
+  int32_t d_in = 0;
+  const int64_t* dst_rows = nullptr;
+};
+
 static tq_status logits_common(const char* what, const tq_codebook* kcb, const void* kcache, int64_t rows,
                                const tq::RowMap& map, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
                                const int32_t* seq_lens, const float* q, float* logits, void* workspace,
-                               size_t ws_bytes, void* stream) {
+                               size_t ws_bytes, void* stream, const FusedAppend& app = FusedAppend()) {
   tq_status st;
   // keys with the QJL term (PROD), or MSE-only keys in scalar mode
   if ((st = check_scoring_codebook(kcb, kcb && kcb->dev.kind == TQ_KIND_MSE ? TQ_KIND_MSE : TQ_KIND_PROD, what,
@@ -674,7 +684,13 @@ static tq_status logits_common(const char* what, const tq_codebook* kcb, const v
                                                   capacity, rows, map, seq_lens, prep, lg, nchunks, tpc,
                                                   kcb->d_status, s));
     } else {
-      if ((st = launched(what, tq::launch_prep(kcb->dev, qg, B, Hq, Hkv, prep, s))) != TQ_OK) return st;
+      if (g == 0 && app.n > 0)
+        st = launched(what, tq::launch_prep_append(kcb->dev, qg, B, Hq, Hkv, prep,
+                                                   static_cast<uint8_t*>(const_cast<void*>(kcache)), rows, app.x,
+                                                   app.x_dtype, app.n, app.d_in, app.dst_rows, kcb->d_status, s));
+      else
+        st = launched(what, tq::launch_prep(kcb->dev, qg, B, Hq, Hkv, prep, s));
+      if (st != TQ_OK) return st;
       if (capacity % 16 == 0)
         st = launched(what, tq::launch_logits_staged(kcb->dev, static_cast<const uint8_t*>(kcache), B, Hq, Hkv,
                                                      capacity, rows, map, seq_lens, prep, lg, nchunks, tpc,
@@ -694,6 +710,39 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
   const tq::NvtxRange nvtx_range("tq_logits");
   return logits_common("tq_logits", kcb, kcache, (int64_t)B * Hkv * capacity, tq::RowMap{}, B, Hq, Hkv, capacity,
                        seq_lens, q, logits, workspace, ws_bytes, stream);
+}
+
+tq_status tq_append_logits(const tq_codebook* kcb, void* kcache, const void* x, int32_t x_dtype, int64_t n,
+                           int32_t d_in, const int64_t* dst_rows, int32_t B, int32_t Hq, int32_t Hkv, int64_t capacity,
+                           const int32_t* seq_lens, const float* q, float* logits, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  const tq::NvtxRange nvtx_range("tq_append_logits");
+  const char* what = "tq_append_logits";
+  if (!kcb) return fail(TQ_EINVAL, "%s: codebook is NULL", what);
+  if (B <= 0 || Hkv <= 0 || capacity < 0) return fail(TQ_EINVAL, "%s: bad sizes", what);
+  const int64_t rows = (int64_t)B * Hkv * capacity;
+  const bool fuse = n >= 1 && n <= 4096 && kcb->dev.mode == TQ_MODE_SCALAR && kcb->dev.d == 128 &&
+                    kcb->dev.extra == 0 && capacity > 0;
+  if (!fuse) {
+    tq_status st = quantize_common(what, kcb, kcache, rows, x, x_dtype, n, d_in, nullptr, nullptr, dst_rows, stream);
+    if (st != TQ_OK) return st;
+    return logits_common(what, kcb, kcache, rows, tq::RowMap{}, B, Hq, Hkv, capacity, seq_lens, q, logits, workspace,
+                         ws_bytes, stream);
+  }
+  // the append's own checks (as tq_quantize), then the fused launch
+  if (!kcache || !aligned16(kcache)) return fail(TQ_EINVAL, "%s: cache must be a 16-byte aligned device pointer", what);
+  if (!x) return fail(TQ_EINVAL, "%s: x is NULL", what);
+  if (x_dtype != TQ_F32 && x_dtype != TQ_BF16) return fail(TQ_EINVAL, "%s: bad dtype %d", what, x_dtype);
+  if (d_in < 1 || d_in > kcb->dev.d) return fail(TQ_EINVAL, "%s: d_in = %d must be in 1..%d", what, d_in, kcb->dev.d);
+  if (!dst_rows && n > rows) return fail(TQ_EINVAL, "%s: n = %lld rows exceed the cache", what, (long long)n);
+  FusedAppend app;
+  app.x = x;
+  app.x_dtype = x_dtype;
+  app.n = n;
+  app.d_in = d_in;
+  app.dst_rows = dst_rows;
+  return logits_common(what, kcb, kcache, rows, tq::RowMap{}, B, Hq, Hkv, capacity, seq_lens, q, logits, workspace,
+                       ws_bytes, stream, app);
 }
 
 // Paged layout arguments shared by the *_paged entry points.

@@ -190,6 +190,11 @@ cudaError_t launch_quantize_tcx(const CUtensorMap& tm_pihi, const CUtensorMap& t
                                 const Dev& cb, uint8_t* cache, int64_t cache_rows, const void* x, bool f32, int64_t n,
                                 int d_in, const int64_t* dst_rows, int* status, int sms, cudaStream_t s);
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s);
+// The query prep with a decode step's key append (n rows of x into the
+// cache at dst_rows; scalar mode, d = 128, no extra-bit words) in one grid.
+cudaError_t launch_prep_append(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, uint8_t* cache,
+                               int64_t cache_rows, const void* x, int x_dtype, int64_t n, int d_in,
+                               const int64_t* dst_rows, int* status, cudaStream_t s);
 cudaError_t launch_logits(const Dev& cb, const uint8_t* kcache, int B, int Hq, int Hkv, int64_t capacity,
                           int64_t cache_rows, const int32_t* seq_lens, const uint8_t* prep, float* logits,
                           int nchunks, int tiles_per_cta, cudaStream_t s);

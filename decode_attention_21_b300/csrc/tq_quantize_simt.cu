@@ -407,11 +407,14 @@ __global__ void __launch_bounds__(4 * D) k_quantize_row(const Dev cb, uint8_t* _
         const uint32_t bw = __ballot_sync(kFull, idx & 1);
         if (lane == 0) words[NW * P + w] = bw;
       }
-      if (prod) {
-        xs[i] = r;
-        const float ss = warp_sum(r * r);
-        if (lane == 0) red[w] = ss;
-      }
+    }
+    // every warp has read the norm partials in red before they are replaced
+    // by the residual's
+    __syncthreads();
+    if (q == 0 && prod) {
+      xs[i] = r;
+      const float ss = warp_sum(r * r);
+      if (lane == 0) red[w] = ss;
     }
     __syncthreads();
     float gamma = 0.f, nrm_x = 0.f, gamma_x = 0.f;

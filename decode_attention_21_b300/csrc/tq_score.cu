@@ -25,6 +25,7 @@
 //     fill the 8 columns.
 //   * PV: A = value bits (16 coordinates x 16 tokens), B = -2 coef_v p_t n_v,t
 //     split into fp16 hi + lo.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "tq_internal.cuh"
@@ -71,8 +72,8 @@ __device__ __forceinline__ void cluster_sync() {
 }
 }  // namespace
 
-__global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
-                                              uint8_t* __restrict__ prep) {
+__device__ __forceinline__ void prep_body(const Dev& cb, const float* __restrict__ q, int Hq, int Hkv,
+                                          uint8_t* __restrict__ prep) {
   constexpr int d = 128;
   const int G = Hq / Hkv;
   uint32_t r;
@@ -80,12 +81,6 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   const int unit = blockIdx.x >> 2;               // kv head * 4 + slot
   const int kvh = unit >> 2, slot = unit & 3, b = blockIdx.y;
   const bool live = slot < G;
-  // This grid may run alongside the kernel before it (a cache append), since
-  // it reads only the queries and the codebook; one of its CTAs waits for
-  // that kernel at its end, so the grid's completion implies the append's.  The scoring kernel
-  // that follows may start now: it touches no cache row before it waits for
-  // this grid.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float sq[d], part[2][4][32], sv[2][32];
   // [source rank][max |q'|, max |2 q''|, sum q', sum q'', sum of q' over extended-codebook coordinates]
   __shared__ float red[4][5];
@@ -189,6 +184,144 @@ __global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restr
   // completion to imply that kernel's; the others leave now and free their
   // SMs for the scoring kernel.
   if (blockIdx.x == 0 && blockIdx.y == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(256) k_prep(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
+                                              uint8_t* __restrict__ prep) {
+  // This grid may run alongside the kernel before it (a cache append), since
+  // it reads only the queries and the codebook; one of its CTAs waits for
+  // that kernel at its end, so the grid's completion implies the append's.  The scoring kernel
+  // that follows may start now: it touches no cache row before it waits for
+  // this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  prep_body(cb, q, Hq, Hkv, prep);
+}
+
+// One key row of a decode step's cache append (scalar mode, d = 128, no
+// extra-bit words), by a CTA of 256 threads: thread (i, h) owns coordinate
+// i and quarters 2h, 2h + 1 of each matrix-vector product.  The arithmetic
+// and its order are those of the short-batch append kernel (quarters of 32
+// terms, each an fma chain, summed pairwise; warp sums of squares; codes by
+// compare-count), so the stored record and norms are bit-identical.  The
+// stores wait for the kernel before this grid (griddepcontrol.wait).
+__device__ __forceinline__ void append_body(const Dev& cb, uint8_t* __restrict__ cache, int64_t cache_rows,
+                                            const void* __restrict__ x, int x_dtype, int64_t row, int d_in,
+                                            const int64_t* __restrict__ dst_rows, int* __restrict__ status) {
+  constexpr int D = 128, NW = D / 32;
+  __shared__ float xs[D], part[4][D], red[NW];
+  __shared__ uint32_t words[4 * NW];
+  const int t = threadIdx.x, i = t & (D - 1), h = t >> 7;
+  const int lane = i & 31, w = i >> 5;
+  const int b1 = cb.b1, P = cb.P;
+  const bool prod = cb.kind == 0;
+  const uint64_t keep = l2_policy_evict_last();
+  if (h == 0) {
+    float v = 0.f;
+    if (i < d_in)
+      v = x_dtype == 0 ? static_cast<const float*>(x)[row * d_in + i]
+                       : __bfloat162float(static_cast<const __nv_bfloat16*>(x)[row * d_in + i]);
+    xs[i] = v;
+  }
+  __syncthreads();
+  // quarter k of (M^T)[:, i] . xs: rows 32 k .. 32 k + 31 of column i
+  auto quarter = [&](const float* MT, int k) {
+    const float* col = MT + (size_t)(32 * k) * D + i;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc = fmaf(ld_table(col + (size_t)j * D, keep), xs[32 * k + j], acc);
+    return acc;
+  };
+  part[2 * h][i] = quarter(cb.PiT, 2 * h);
+  part[2 * h + 1][i] = quarter(cb.PiT, 2 * h + 1);
+  __syncthreads();
+  float y = 0.f, r = 0.f;
+  if (h == 0) {
+    y = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
+    float ss = y * y;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    if (lane == 0) red[w] = ss;
+  }
+  __syncthreads();
+  float nrm = 0.f;
+  if (h == 0) {
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) ss += red[k];
+    nrm = sqrtf(ss);
+    y *= nrm > 0.f ? 1.f / nrm : 0.f;
+    int idx = 0;
+    const int nbd = (1 << b1) - 1;
+    for (int k = 0; k < nbd; ++k) idx += (y >= cb.bound[k]) ? 1 : 0;
+    r = y - cb.cent[idx];
+    for (int p = 0; p < b1; ++p) {
+      const uint32_t bw = __ballot_sync(kFull, (idx >> (b1 - 1 - p)) & 1);
+      if (lane == 0) words[w * P + p] = bw;
+    }
+  }
+  __syncthreads();                         // everyone has read red and xs
+  if (prod && h == 0) {
+    xs[i] = r;
+    float ss = r * r;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    if (lane == 0) red[w] = ss;
+  }
+  __syncthreads();
+  float gamma = 0.f;
+  if (prod) {
+    part[2 * h][i] = quarter(cb.ST, 2 * h);
+    part[2 * h + 1][i] = quarter(cb.ST, 2 * h + 1);
+    __syncthreads();
+    if (h == 0) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < NW; ++k) ss += red[k];
+      gamma = sqrtf(ss);
+      const float z = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
+      const uint32_t bw = __ballot_sync(kFull, z >= 0.f);
+      if (lane == 0) words[w * P + b1] = bw;
+    }
+  }
+  __syncthreads();
+  // the kernel before this grid (a scoring kernel reading this cache) has
+  // completed before any destination is looked up or written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t dst = dst_rows ? dst_rows[row] : row;
+  if (dst < 0 || dst >= cache_rows) {
+    if (t == 0) atomicOr(status, kBadRow);
+    return;
+  }
+  uint32_t* rec = reinterpret_cast<uint32_t*>(cache) + dst * cb.W;
+  if (t < cb.W) rec[t] = words[t];
+  if (t == 0) {
+    unsigned char* norms = cache + norm_offset(cb, cache_rows);
+    if (prod)
+      reinterpret_cast<__half2*>(norms)[dst] = __floats2half2_rn(nrm, gamma);
+    else
+      reinterpret_cast<__half*>(norms)[dst] = __float2half_rn(nrm);
+  }
+}
+
+// A decode step's query prep and key append in one grid: blocks
+// 0 .. 16 Hkv - 1 of each grid row are the prep's (4-CTA clusters), blocks
+// 16 Hkv + k of grid row 0 append row k of x (k < n).  One launch instead of
+// two saves one grid-completion handoff on the step's critical path; the
+// append CTAs wait for the kernel before this grid before they store.
+__global__ void __launch_bounds__(256) k_prep_append(const Dev cb, const float* __restrict__ q, int Hq, int Hkv,
+                                                     uint8_t* __restrict__ prep, uint8_t* __restrict__ cache,
+                                                     int64_t cache_rows, const void* __restrict__ x, int x_dtype,
+                                                     int64_t n, int d_in, const int64_t* __restrict__ dst_rows,
+                                                     int* __restrict__ status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int nprep = Hkv * 16;
+  if ((int)blockIdx.x < nprep) {
+    prep_body(cb, q, Hq, Hkv, prep);
+    return;
+  }
+  const int64_t row = (int64_t)blockIdx.x - nprep;
+  if (blockIdx.y != 0 || row >= n) return;
+  append_body(cb, cache, cache_rows, x, x_dtype, row, d_in, dst_rows, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -1347,6 +1480,28 @@ static void attn_v(int b1v, dim3 grid, cudaStream_t s, const Dev& k, const Dev& 
 // shared-memory carveout, so all of them ask for the largest one.
 cudaError_t prefer_max_shared(const void* fn) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t launch_prep_append(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, uint8_t* cache,
+                               int64_t cache_rows, const void* x, int x_dtype, int64_t n, int d_in,
+                               const int64_t* dst_rows, int* status, cudaStream_t s) {
+  static cudaError_t configured = prefer_max_shared(reinterpret_cast<const void*>(k_prep_append));
+  if (configured != cudaSuccess) return configured;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(Hkv * 16 + ((n + 3) / 4) * 4), B);   // whole 4-CTA clusters
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_prep_append, cb, q, Hq, Hkv, prep, cache, cache_rows, x, x_dtype, n, d_in,
+                            dst_rows, status);
 }
 
 cudaError_t launch_prep(const Dev& cb, const float* q, int B, int Hq, int Hkv, uint8_t* prep, cudaStream_t s) {

@@ -18,7 +18,7 @@ KIND_PROD, KIND_MSE = 0, 1
 F32, BF16 = 0, 1
 
 EXPORTS = ["tq_make_codebook", "tq_free_codebook", "tq_codebook_tables", "tq_host_tables", "tq_record_bytes", "tq_cache_bytes",
-           "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits", "tq_logits_dense",
+           "tq_quantize", "tq_quantize_rotated", "tq_logits_workspace", "tq_logits", "tq_append_logits", "tq_logits_dense",
            "tq_decode_attention_workspace", "tq_decode_attention", "tq_decode_attention_static",
            "tq_search_workspace", "tq_search", "tq_search_fallbacks", "tq_set_first_wait_limit", "tq_fail_allocation",
            "tq_append_paged", "tq_logits_paged", "tq_decode_attention_paged", "tq_advance_lengths",
@@ -63,6 +63,7 @@ def lib():
         L.tq_logits_workspace.argtypes = [vp, i32, i32, i32]
         L.tq_logits_workspace.restype = sz
         L.tq_logits.argtypes = [vp, vp, i32, i32, i32, i64, vp, vp, vp, vp, sz, vp]
+        L.tq_append_logits.argtypes = [vp, vp, vp, i32, i64, i32, vp, i32, i32, i32, i64, vp, vp, vp, vp, sz, vp]
         L.tq_logits_dense.argtypes = [vp, i32, i32, i32, i32, i32, i64, vp, vp, vp, vp]
         L.tq_decode_attention_workspace.argtypes = [vp, i32, i32, i32, i64]
         L.tq_decode_attention_workspace.restype = sz
@@ -208,6 +209,16 @@ def tq_logits_workspace(kcb, B, Hq, Hkv):
 def tq_logits(kcb, kcache, B, Hq, Hkv, capacity, seq_lens, q, logits, workspace, stream=None):
     _check(lib().tq_logits(kcb.handle, _ptr(kcache), B, Hq, Hkv, capacity, _ptr(seq_lens), _ptr(q), _ptr(logits),
                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_append_logits(kcb, kcache, x, n, d_in, dst_rows, B, Hq, Hkv, capacity, seq_lens, q, logits, workspace,
+                     stream=None):
+    """tq_quantize of the step's new keys x into kcache, then tq_logits (one
+    call; the append rides in the query-prep launch where it can)."""
+    dt = BF16 if x.dtype == torch.bfloat16 else F32
+    _check(lib().tq_append_logits(kcb.handle, _ptr(kcache), _ptr(x), dt, n, d_in, _ptr(dst_rows), B, Hq, Hkv,
+                                  capacity, _ptr(seq_lens), _ptr(q), _ptr(logits), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def tq_logits_dense(keys, B, Hq, Hkv, capacity, seq_lens, q, logits, stream=None):

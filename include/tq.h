@@ -176,6 +176,29 @@ tq_status tq_logits(const tq_codebook* kcb, const void* kcache, int32_t B, int32
                     int32_t Hkv, int64_t capacity, const int32_t* seq_lens, const float* q,
                     float* logits, void* workspace, size_t ws_bytes, void* stream);
 
+/* One decode step of the logits path: the step's new keys are compressed
+ * into the cache, then every key is scored ([suzuke] 為什麼這個方法特別聰明:
+ * each token is compressed online as it arrives; [cnyes] 1 bit 掃尾: the
+ * query is rotated and sketched once per step).  Equivalent to
+ *   tq_quantize(kcb, kcache, B*Hkv*capacity, x, x_dtype, n, d_in, dst_rows)
+ *   tq_logits(kcb, kcache, B, Hq, Hkv, capacity, seq_lens, q, logits, ...)
+ * on the same stream, with bit-identical cache bytes and logits (seq_lens
+ * must already count the appended keys).  For scalar-mode codebooks with
+ * d = 128, no extra-bit words and 1 <= n <= 4096 the append runs inside the
+ * query-prep launch, which takes one kernel hand-off off the step; other
+ * codebooks, and n = 0, run the two calls as such.
+ *   kcache     device, rows (b*Hkv + kvh)*capacity + t (as tq_logits)
+ *   x          device, n x d_in row-major, TQ_F32 or TQ_BF16 (as tq_quantize)
+ *   dst_rows   device int64[n] target rows of kcache, or NULL for 0..n-1; a
+ *              row outside the cache is skipped and flagged (TQ_EINVAL at
+ *              tq_check_device)
+ * Other arguments and errors as tq_quantize and tq_logits.                  */
+tq_status tq_append_logits(const tq_codebook* kcb, void* kcache, const void* x, int32_t x_dtype,
+                           int64_t n, int32_t d_in, const int64_t* dst_rows, int32_t B,
+                           int32_t Hq, int32_t Hkv, int64_t capacity, const int32_t* seq_lens,
+                           const float* q, float* logits, void* workspace, size_t ws_bytes,
+                           void* stream);
+
 /* Unquantized comparator of tq_logits: the same logits from uncompressed
  * keys ([xujun] 常见问题: TurboQuant's attention-logit speed-up is quoted
  * against 32-bit unquantized keys):
