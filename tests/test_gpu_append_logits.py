@@ -69,7 +69,8 @@ def run_both(cb, B, Hq, Hkv, cap, lens, dtype, seed=5):
 @pytest.mark.parametrize("bits,kind", [(4, tq.KIND_PROD), (3, tq.KIND_PROD), (2, tq.KIND_PROD), (3, tq.KIND_MSE)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("B,Hq,Hkv,cap,lens", [(1, 32, 8, 4096, [4096]), (2, 8, 2, 1024, [1024, 333]),
-                                              (3, 3, 3, 512, [1, 200, 512]), (1, 16, 2, 256, [100])])
+                                              (3, 3, 3, 512, [1, 200, 512]), (1, 16, 2, 256, [100]),
+                                              (2, 12, 1, 333, [333, 20]), (5, 4, 1, 64, [64, 1, 17, 33, 2])])
 def test_fused_step_equals_separate_calls(bits, kind, dtype, B, Hq, Hkv, cap, lens):
     cb = tq.Codebook(128, bits, kind)
     c1, l1, c2, l2, _, _ = run_both(cb, B, Hq, Hkv, cap, lens, dtype)
