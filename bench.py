@@ -463,9 +463,12 @@ def dense_comparator(tq, wl, B, Hq, Hkv, d, T, cache, kcb, seq, q, ws, tq_call_m
     for name, bits, kind, extra in (("prod_b4", 4, tq.KIND_PROD, 0), ("prod_b3.5", 3, tq.KIND_PROD, 32),
                                     ("prod_b2.5", 2, tq.KIND_PROD, 32), ("split32_b3", 3, tq.KIND_PROD, 32),
                                     ("split32_b2", 2, tq.KIND_PROD, 32), ("split64_b2", 2, tq.KIND_PROD, 64),
-                                    ("mse_b4", 4, tq.KIND_MSE, 0), ("mse_b3", 3, tq.KIND_MSE, 0)):
+                                    ("mse_b4", 4, tq.KIND_MSE, 0), ("mse_b3", 3, tq.KIND_MSE, 0),
+                                    ("polar_b4", 4, tq.KIND_PROD, 0), ("polar_b3", 3, tq.KIND_PROD, 0)):
         if name == "prod_b4":
             cb = kcb
+        elif name.startswith("polar"):
+            cb = tq.Codebook(d, bits, kind, tq.MODE_POLAR)
         elif name.startswith("split"):
             cb = tq.Codebook(d, bits, kind, outliers=wl.layer_outlier_channels(Hkv, extra, d))
         else:

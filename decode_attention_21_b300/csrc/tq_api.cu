@@ -669,7 +669,9 @@ static tq_status logits_common(const char* what, const tq_codebook* kcb, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* prep = static_cast<uint8_t*>(workspace);
   int nchunks, tpc;
-  chunking(B, Hkv, capacity, kLogitsCtas, &nchunks, &tpc);
+  // the polar kernel (72 registers, no shared-memory ring) hides its global
+  // loads with more resident CTAs: 7 per SM
+  chunking(B, Hkv, capacity, kcb->dev.mode == TQ_MODE_POLAR ? 148 * 7 : kLogitsCtas, &nchunks, &tpc);
   // The kernels score 4 query heads per kv head (fp16 hi / lo of each in
   // the 8 tensor-core columns); a larger group (a multiple of 4) is scored
   // 4 heads at a time: with Hq and Hkv unchanged, queries and logits offset
