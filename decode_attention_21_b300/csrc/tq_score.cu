@@ -810,17 +810,10 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
       na = reinterpret_cast<const unsigned short*>(nrm)[lt * 16 + g];
       nb = reinterpret_cast<const unsigned short*>(nrm)[lt * 16 + g + 8];
     }
-    const int64_t ta = tg * 16 + g;
-    if (ta >= L) {
-#pragma unroll
-      for (int p = 0; p < P; ++p) wa[p] = 0;
-      ea = 0u;
-    }
-    if (ta + 8 >= L) {
-#pragma unroll
-      for (int p = 0; p < P; ++p) wb[p] = 0;
-      eb = 0u;
-    }
+    // keys at or past L are scored like the others (their bytes are staged
+    // cache rows of the same tile); an MMA output row depends only on its
+    // own key, and emit stores only keys below L
+    (void)tg;
   };
   auto emit = [&](int64_t tg, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
     const int64_t ta = tg * 16 + g, tb = ta + 8;
