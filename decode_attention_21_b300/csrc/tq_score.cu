@@ -815,11 +815,13 @@ __global__ void __launch_bounds__(128, 4) k_logits_staged(const Dev cb, const ui
     // own key, and emit stores only keys below L
     (void)tg;
   };
+  // token positions in 32 bits (capacity < 2^31)
+  const int L32 = (int)L;
   auto emit = [&](int64_t tg, uint32_t na, uint32_t nb, float s1a, float s1b, float s2a, float s2b) {
-    const int64_t ta = tg * 16 + g, tb = ta + 8;
+    const int ta = (int)tg * 16 + g, tb = ta + 8;
     if (c < G) {
-      if (ta < L) out[ta] = est_key<QJL>(na, s1a, s2a, kq);
-      if (tb < L) out[tb] = est_key<QJL>(nb, s1b, s2b, kq);
+      if (ta < L32) out[ta] = est_key<QJL>(na, s1a, s2a, kq);
+      if (tb < L32) out[tb] = est_key<QJL>(nb, s1b, s2b, kq);
     }
   };
   // a split key: group A's estimate from nxa / nxb plus group B's
