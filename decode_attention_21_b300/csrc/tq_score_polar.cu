@@ -81,7 +81,12 @@ __device__ __forceinline__ uint32_t codes_x8(const uint32_t (&w)[B], int pos) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t nib(uint32_t r, int i) { return (r >> (4 * i)) & 0xFu; }
+// (cos, sin) of the level-l centroid whose code is nibble i of r: the
+// nibble shifted straight to its byte offset in the table row (code x 8).
+__device__ __forceinline__ float2 tab_nib(const PolarTab& tab, int l, uint32_t r, int i) {
+  const uint32_t off = i == 0 ? (r << 3) & 0x78u : (r >> (4 * i - 3)) & 0x78u;
+  return *reinterpret_cast<const float2*>(reinterpret_cast<const char*>(&tab.t[l][0]) + off);
+}
 
 // The 16 leaves of half h of subtree s, starting from the subtree radius.
 // Angle codes of a subtree word: level 1 at bits 0..15, level 2 at 16..23,
@@ -92,27 +97,27 @@ __device__ __forceinline__ void decode_half(const PolarTab& tab, const uint32_t 
   const uint32_t n1 = codes_x8<B>(ws, 8 * h);        // level 1: codes 8h .. 8h + 7
   const uint32_t n2 = codes_x8<B>(ws, 16 + 4 * h);   // level 2: nibbles 0..3
   const uint32_t n3 = codes_x8<B>(ws, 24);           // level 3: nibbles 0..3, level 4: 4, 5, level 5: 6
-  const float2 a5 = tab.t[5][nib(n3, 6)];
+  const float2 a5 = tab_nib(tab, 5, n3, 6);
   const float rho4 = rho5 * (h ? a5.y : a5.x);
-  const float2 a4 = tab.t[4][nib(n3, 4 + h)];
+  const float2 a4 = tab_nib(tab, 4, n3, 4 + h);
   float r3[2] = {rho4 * a4.x, rho4 * a4.y};
   float r2[4];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const float2 a = tab.t[3][nib(n3, 2 * h + i)];
+    const float2 a = tab_nib(tab, 3, n3, 2 * h + i);
     r2[2 * i] = r3[i] * a.x;
     r2[2 * i + 1] = r3[i] * a.y;
   }
   float r1[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 a = tab.t[2][nib(n2, i)];
+    const float2 a = tab_nib(tab, 2, n2, i);
     r1[2 * i] = r2[i] * a.x;
     r1[2 * i + 1] = r2[i] * a.y;
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float2 a = tab.t[1][nib(n1, i)];
+    const float2 a = tab_nib(tab, 1, n1, i);
     y[2 * i] = r1[i] * a.x;
     y[2 * i + 1] = r1[i] * a.y;
   }
