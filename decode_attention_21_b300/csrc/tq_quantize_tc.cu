@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_cent[16], s_centx[32], s_bnd[16], s_bndx[32];
   float lt[7], ltx[7];
   heap_levels<B1>(cb.bound, lt);
+  float cr[4];                                       // centroids in registers (b' <= 2)
+#pragma unroll
+  for (int k = 0; k < 4; ++k) cr[k] = cb.cent[k];
   heap_levels<EXT ? B1 + 1 : 1>(cb.bound_x, ltx);
   if (tid < 16) {
     s_cent[tid] = cb.cent[tid];
@@ -251,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (EXT && ext) {
               const int idx = cell_heap<B1 + 1>(y, ltx, s_bndx, word, jb);
               r = y - s_centx[idx];
+            } else if constexpr (B1 <= 2 && !EXT) {   // (with extra-bit words this measured slower)
+              r = y - cell_cent<B1>(y, lt, cr, word, jb);
             } else {
               const int idx = cell_heap<B1>(y, lt, s_bnd, word, jb);
               r = y - s_cent[idx];

@@ -167,6 +167,23 @@ __device__ __forceinline__ int cell_heap(float y, const float (&lt)[7], const fl
   }
 }
 
+// As cell_heap for L <= 2, returning the centroid of the cell from the
+// registers cr[0 .. 2^L - 1] (selects instead of an index and a table load).
+template <int L>
+__device__ __forceinline__ float cell_cent(float y, const float (&lt)[7], const float (&cr)[4], uint32_t* w, int j) {
+  static_assert(L <= 2, "register centroids for one or two levels");
+  const bool p0 = y >= lt[0];
+  if (p0) w[0] |= 1u << j;
+  if constexpr (L == 1) {
+    return p0 ? cr[1] : cr[0];
+  } else {
+    const bool p1 = y >= (p0 ? lt[2] : lt[1]);
+    if (p1) w[1] |= 1u << j;
+    const float lo = p1 ? cr[1] : cr[0], hi = p1 ? cr[3] : cr[2];
+    return p0 ? hi : lo;
+  }
+}
+
 // Heap-ordered boundaries of the first three bisection levels of a 2^L-cell
 // table (node n at level l, position k: boundary (2k + 1) 2^(L-1-l) - 1).
 template <int L>
