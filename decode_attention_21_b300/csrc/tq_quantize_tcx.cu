@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ polar::Tables tpol;                   // polar mode only
   float lt[7];
   if constexpr (!POLAR) heap_levels<B1>(cb.bound, lt);
+  float cr[4];                                       // centroids in registers (b' <= 2)
+#pragma unroll
+  for (int k = 0; k < 4; ++k) cr[k] = cb.cent[k];
   if (tid < 16) {
     s_cent[tid] = cb.cent[tid];
     s_bnd[tid] = cb.bound[tid];
@@ -301,8 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const float y = v[e + u] * inv;
-            const int idx = cell_heap<B1>(y, lt, s_bnd, words[h], 16 * half + e + u);
-            const float r = y - s_cent[idx];
+            float r;
+            if constexpr (B1 <= 2) {
+              r = y - cell_cent<B1>(y, lt, cr, words[h], 16 * half + e + u);
+            } else {
+              const int idx = cell_heap<B1>(y, lt, s_bnd, words[h], 16 * half + e + u);
+              r = y - s_cent[idx];
+            }
             gs = fmaf(r, r, gs);
             r2[u] = r;
           }
