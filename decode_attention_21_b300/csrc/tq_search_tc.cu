@@ -292,7 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kOffNrm = SM::kOffNrm, kOffBar = SM::kOffBar, kOffMisc = SM::kOffMisc;
   constexpr int kStgBytes = stg_bytes(B1);
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned by pointer arithmetic on the shared array, so the
+  // compiler keeps every access through smem in the shared space
+  uint8_t* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = su32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t NT = (n_db + kR - 1) / kR, NQB = (nq + kQ - 1) / kQ, U = NQB * NT, G = gridDim.x;
