@@ -443,7 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* Lid = reinterpret_cast<int32_t*>(smem + kOffLid);
     float* nrm_s = reinterpret_cast<float*>(smem + kOffNrm);
     const uint32_t* nrm = reinterpret_cast<const uint32_t*>(db + norm_offset(cb, n_db));
-    float thr = -INFINITY, inv_scale = 0.f;
+    // thr: the list's entry threshold (scaled scores); thr_s = thr 2^e_q, the
+    // same threshold for the unscaled products (2^-e_q is a power of two, so
+    // p 2^-e_q > thr exactly when p > thr 2^e_q)
+    float thr = -INFINITY, inv_scale = 0.f, scale_q = INFINITY, thr_s = -INFINITY;
     int filled = 0, mpos = 0;                    // entries in the list, slot of its minimum
     bool ok = true;
     int seg = 0;
@@ -465,6 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         filled = mpos = 0;
         const int qi = (int)(qb * kQ + ql);
         inv_scale = qi < nq ? __ldg(qinfo + (size_t)qi * 4) : 0.f;
+        scale_q = inv_scale > 0.f ? 1.f / inv_scale : INFINITY;
+        thr_s = thr * scale_q;
         for (int c = 0; c < 8; ++c) {
           uint32_t r[32];
 #pragma unroll
@@ -511,14 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               "=r"(r[30]), "=r"(r[31])
             : "r"(dcol + lane_off + 32 * cbk));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        // scores of the chunk and the mask of those above the threshold (branch-free)
+        // unscaled scores of the chunk and the mask of those above the
+        // threshold (branch-free); rows past the database end masked once
         uint32_t cand = 0u;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float sj = __uint_as_float(r[j]) * nb[32 * cbk + j] * inv_scale;
-          r[j] = __float_as_uint(sj);
-          cand |= (uint32_t)(32 * cbk + j < valid && sj > thr) << j;
+          const float pj = __uint_as_float(r[j]) * nb[32 * cbk + j];
+          r[j] = __float_as_uint(pj);
+          cand |= (uint32_t)(pj > thr_s) << j;
         }
+        const int nvalid = valid - 32 * cbk;
+        cand &= nvalid >= 32 ? 0xffffffffu : (nvalid <= 0 ? 0u : (1u << nvalid) - 1u);
         if (__any_sync(0xffffffffu, cand != 0u)) {
           // take the candidates one by one (a compact loop: the score is
           // picked from the registers by a select tree, the unsorted list's
@@ -526,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (cand) {
             const int j = __ffs(cand) - 1;
             cand &= cand - 1;
-            const float sj = __uint_as_float(pick32(r, j));
+            const float sj = __uint_as_float(pick32(r, j)) * inv_scale;
             if (!(sj > thr)) continue;
             Lsc[mpos * kQ + ql] = sj;
             Lid[mpos * kQ + ql] = (int32_t)(row0 + 32 * cbk + j);
@@ -542,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mv = fminf(v, mv);
               }
               thr = mv;
+              thr_s = mv * scale_q;
               mpos = mp;
               filled = kCand;
             }
