@@ -518,12 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         // unscaled scores of the chunk and the mask of those above the
         // threshold (branch-free); rows past the database end masked once
+        // (thr_s - p < 0 exactly when p > thr_s: the sign bit is funnel-shifted
+        // into the mask, j = 31 first so that row j lands on bit j)
         uint32_t cand = 0u;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 31; j >= 0; --j) {
           const float pj = __uint_as_float(r[j]) * nb[32 * cbk + j];
           r[j] = __float_as_uint(pj);
-          cand |= (uint32_t)(pj > thr_s) << j;
+          cand = __funnelshift_l(__float_as_uint(thr_s - pj), cand, 1);
         }
         const int nvalid = valid - 32 * cbk;
         cand &= nvalid >= 32 ? 0xffffffffu : (nvalid <= 0 ? 0u : (1u << nvalid) - 1u);
