@@ -156,6 +156,30 @@ __device__ __forceinline__ void bar_arrive(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Min-heap of kCand (score, id) entries in the column layout [e * kQ + ql]:
+// place (v, id) at slot e and sink it below any smaller child.
+__device__ __forceinline__ void heap_sift(float* Lsc, int32_t* Lid, int ql, int e, float v, int32_t id) {
+  while (true) {
+    const int l = 2 * e + 1;
+    if (l >= kCand) break;
+    int m = l;
+    float vm = Lsc[l * kQ + ql];
+    if (l + 1 < kCand) {
+      const float vr = Lsc[(l + 1) * kQ + ql];
+      if (vr < vm) {
+        m = l + 1;
+        vm = vr;
+      }
+    }
+    if (!(vm < v)) break;
+    Lsc[e * kQ + ql] = vm;
+    Lid[e * kQ + ql] = Lid[m * kQ + ql];
+    e = m;
+  }
+  Lsc[e * kQ + ql] = v;
+  Lid[e * kQ + ql] = id;
+}
+
 // CTA c of G covers units [U c / G, U (c + 1) / G); the CTA holding unit x.
 __host__ __device__ __forceinline__ int64_t unit_cta(int64_t x, int64_t U, int64_t G) { return (G * (x + 1) - 1) / U; }
 
@@ -447,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // same threshold for the unscaled products (2^-e_q is a power of two, so
     // p 2^-e_q > thr exactly when p > thr 2^e_q)
     float thr = -INFINITY, inv_scale = 0.f, scale_q = INFINITY, thr_s = -INFINITY;
-    int filled = 0, mpos = 0;                    // entries in the list, slot of its minimum
+    int filled = 0;                              // entries in the list (a min-heap once full)
     bool ok = true;
     int seg = 0;
     // norm entry of this thread's row of tile i (prefetched one tile ahead)
@@ -465,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           Lid[j * kQ + ql] = -1;
         }
         thr = -INFINITY;
-        filled = mpos = 0;
+        filled = 0;
         const int qi = (int)(qb * kQ + ql);
         inv_scale = qi < nq ? __ldg(qinfo + (size_t)qi * 4) : 0.f;
         scale_q = inv_scale > 0.f ? 1.f / inv_scale : INFINITY;
@@ -538,23 +562,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             cand &= cand - 1;
             const float sj = __uint_as_float(pick32(r, j)) * inv_scale;
             if (!(sj > thr)) continue;
-            Lsc[mpos * kQ + ql] = sj;
-            Lid[mpos * kQ + ql] = (int32_t)(row0 + 32 * cbk + j);
-            if (++filled < kCand) {
-              mpos = filled;
-            } else {
-              float mv = Lsc[ql];
-              int mp = 0;
-#pragma unroll 4
-              for (int e = 1; e < kCand; ++e) {
-                const float v = Lsc[e * kQ + ql];
-                mp = v < mv ? e : mp;
-                mv = fminf(v, mv);
+            const int32_t id = (int32_t)(row0 + 32 * cbk + j);
+            if (filled < kCand) {
+              // filling: append; once full, order the list as a min-heap
+              Lsc[filled * kQ + ql] = sj;
+              Lid[filled * kQ + ql] = id;
+              if (++filled == kCand) {
+                for (int e = kCand / 2 - 1; e >= 0; --e) heap_sift(Lsc, Lid, ql, e, Lsc[e * kQ + ql], Lid[e * kQ + ql]);
+                thr = Lsc[ql];
+                thr_s = thr * scale_q;
               }
-              thr = mv;
-              thr_s = mv * scale_q;
-              mpos = mp;
-              filled = kCand;
+            } else {
+              // full: the new entry replaces the minimum (the root) and sinks
+              heap_sift(Lsc, Lid, ql, 0, sj, id);
+              thr = Lsc[ql];
+              thr_s = thr * scale_q;
             }
           }
           __syncwarp();
