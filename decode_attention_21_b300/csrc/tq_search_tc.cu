@@ -369,9 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seg = 0;
       bool ok = true;
       bool issued = false;
+      // tile index within the query block (u0 + i) % NT, and the ring
+      // position of K-block g = 8 i + blk: slot g % kSlots, phase
+      // (g / kSlots) & 1, all kept as running counters
+      int64_t t = u0 % NT;
+      int slot = 0;
+      uint32_t sphase = 0u;
       for (int i = 0; i < ntile && ok; ++i) {
-        const int64_t u = u0 + i;
-        if (i == 0 || u % NT == 0) {
+        if (i == 0 || t == 0) {
           ok = wait_bar(a_full, seg & 1, abort_flag);
           ++seg;
           if (!ok) break;
@@ -380,9 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after();
         const uint32_t dcol = tmem + 256 + 128 * (i & 1);
         for (int blk = 0; blk < 8 && ok; ++blk) {
-          const int64_t g = (int64_t)i * 8 + blk;
-          const int slot = (int)(g % kSlots);
-          if (!(ok = wait_bar(blk_full(slot), (uint32_t)((g / kSlots) & 1), abort_flag))) break;
+          if (!(ok = wait_bar(blk_full(slot), sphase, abort_flag))) break;
           fence_after();
           const uint32_t acol = tmem + (blk & 1) * 128 + (blk >> 1) * 32;
           const uint32_t bsm = sbase + kOffRing + slot * kSlotBytes;
@@ -398,11 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                            blk_empty(slot))
                        : "memory");
+          if (++slot == kSlots) {
+            slot = 0;
+            sphase ^= 1u;
+          }
         }
         if (!ok) break;
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                          d_full0 + 8u * (i & 1))
                      : "memory");
+        if (++t == NT) t = 0;
       }
       if (!ok) {
         atomicOr(status, 4);
@@ -431,10 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int RB = 32 * (B1 + 1);            // record bytes
     const uint32_t* nrm = reinterpret_cast<const uint32_t*>(db + norm_offset(cb, n_db));
     bool ok = true;
-    for (int i = 0; i < ntile && ok; ++i) {
+    int64_t t = u0 % NT;                         // (u0 + i) % NT, as a running counter
+    for (int i = 0; i < ntile && ok; ++i, t = t + 1 == NT ? 0 : t + 1) {
       const int sidx = i % kStg, use = i / kStg;
       if (use > 0 && !(ok = wait_bar_warp(stg_empty0 + 8u * sidx, (uint32_t)((use - 1) & 1), abort_flag))) break;
-      const int64_t row0 = ((u0 + i) % NT) * kR;
+      const int64_t row0 = t * kR;
       const int valid = (int)min((int64_t)kR, n_db - row0);
       uint8_t* stg = smem + kOffStg + sidx * kStgBytes;
       if (lane == 0) {
@@ -474,14 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int filled = 0;                              // entries in the list (a min-heap once full)
     bool ok = true;
     int seg = 0;
-    // norm entry of this thread's row of tile i (prefetched one tile ahead)
-    auto norm_of = [&](int i) -> uint32_t {
-      const int64_t row = ((u0 + i) % NT) * kR + ql;
+    // norm entry of this thread's row of tile i, whose index within its
+    // query block is tt (prefetched one tile ahead)
+    auto norm_of = [&](int i, int64_t tt) -> uint32_t {
+      const int64_t row = tt * kR + ql;
       return (i < ntile && row < n_db) ? __ldg(nrm + row) : 0u;
     };
-    uint32_t nnext = norm_of(0);
+    // query block and tile of u0 + i as running counters
+    int64_t qb = u0 / NT, t = u0 % NT;
+    uint32_t nnext = norm_of(0, t);
     for (int i = 0; i < ntile && ok; ++i) {
-      const int64_t u = u0 + i, qb = u / NT, t = u % NT;
       if (i == 0 || t == 0) {
         // new segment: reset the lists and load this query block's operand
         for (int j = 0; j < kCand; ++j) {
@@ -513,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++seg;
       }
       const uint32_t ncur = nnext;
-      nnext = norm_of(i + 1);
+      nnext = norm_of(i + 1, t + 1 == NT ? 0 : t + 1);
       if (!(ok = wait_bar_warp(d_full0 + 8u * (i & 1), (uint32_t)((i >> 1) & 1), abort_flag))) break;
       fence_after();
       // n_r of every column of the tile, shared by the 128 queries (each
@@ -585,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before();
       __syncwarp();
       if (lane == 0) bar_arrive(d_empty0 + 8u * (i & 1));
-      if (i == ntile - 1 || (u + 1) % NT == 0) {
+      if (i == ntile - 1 || t + 1 == NT) {
         // segment end: this CTA's lists for query block qb, part = CTA - first CTA of qb
         const int part = (int)(blockIdx.x - unit_cta(qb * NT, U, G));
         const size_t base = ((size_t)qb * Pmax + part) * kCand;
@@ -606,6 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           lsc[(base + j) * kQ + ql] = Lsc[j * kQ + ql];
           lid[(base + j) * kQ + ql] = Lid[j * kQ + ql];
         }
+      }
+      if (++t == NT) {
+        t = 0;
+        ++qb;
       }
     }
     if (!ok) {
@@ -629,6 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float kq = cb.qjl_const;
     bool ok = true;
+    // ring position of K-block g = 8 i + 2 kb + sl: slot g % kSlots and use
+    // g / kSlots, as running counters
+    int dslot = 0;
+    int64_t duse = 0;
     for (int i = 0; i < ntile && ok; ++i) {
       const int sidx = i % kStg;
       if (!(ok = wait_bar_warp(stg_full0 + 8u * sidx, (uint32_t)((i / kStg) & 1), abort_flag))) break;
@@ -642,13 +661,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int kb = 0; kb < 4 && ok; ++kb) {
         // ring slots of this round's two K-blocks (yhat, then sigma)
-        const int64_t g0 = (int64_t)i * 8 + 2 * kb;
         int slot[2];
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl) {
-          const int64_t g = g0 + sl;
-          slot[sl] = (int)(g % kSlots);
-          const int64_t use = g / kSlots;
+          slot[sl] = dslot;
+          const int64_t use = duse;
+          if (++dslot == kSlots) {
+            dslot = 0;
+            ++duse;
+          }
           if (use > 0 && !(ok = wait_bar_warp(blk_empty(slot[sl]), (uint32_t)((use - 1) & 1), abort_flag))) break;
         }
         if (!ok) break;
