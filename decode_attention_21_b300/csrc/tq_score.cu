@@ -1157,6 +1157,7 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const int64_t L = seq_lens[b];
+  const int L32 = (int)L;                    // token positions in 32 bits (capacity < 2^31)
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
@@ -1222,8 +1223,8 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
     const __half* svn = reinterpret_cast<const __half*>(base + kSK + kSKN + kSV);
     const int t_a = st * kStageTiles, n_here = min(kStageTiles, nt - t_a);
     for (int lt = warp; lt < n_here; lt += 4) {
-      const int64_t t0 = (tile0 + t_a + lt) * 16;       // first token of the tile
-      const int64_t ta = t0 + g, tb = ta + 8;
+      const int t0 = ((int)tile0 + t_a + lt) * 16;      // first token of the tile
+      const int ta = t0 + g, tb = ta + 8;
       // keys g and g+8: column c words (+ the extra-bit word of column c)
       uint32_t wa[1][PK], wb[1][PK], ea[1] = {0u}, eb[1] = {0u};
       {
@@ -1258,10 +1259,10 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
       }
       // scores in log2 units
       const float sa =
-          ta < L ? est_groups<QJLK, SPLIT>(nxa, na, s1x[0][0], s2x[0][0], s1[0][0], s2[0][0], kqx, kq) * scale_log2
+          ta < L32 ? est_groups<QJLK, SPLIT>(nxa, na, s1x[0][0], s2x[0][0], s1[0][0], s2[0][0], kqx, kq) * scale_log2
                  : -INFINITY;
       const float sb =
-          tb < L ? est_groups<QJLK, SPLIT>(nxb, nb, s1x[0][1], s2x[0][1], s1[0][1], s2[0][1], kqx, kq) * scale_log2
+          tb < L32 ? est_groups<QJLK, SPLIT>(nxb, nb, s1x[0][1], s2x[0][1], s1[0][1], s2[0][1], kqx, kq) * scale_log2
                  : -INFINITY;
       float mx = fmaxf(sa, sb);
 #pragma unroll
@@ -1280,8 +1281,8 @@ __global__ void __launch_bounds__(128, attn_min_blocks(NVK, EXTK + EXTV)) k_attn
       }
       const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
       const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_run);
-      const float vn0 = ta < L ? __half2float(svn[lt * 16 + g]) : 0.f;
-      const float vn1 = tb < L ? __half2float(svn[lt * 16 + g + 8]) : 0.f;
+      const float vn0 = ta < L32 ? __half2float(svn[lt * 16 + g]) : 0.f;
+      const float vn1 = tb < L32 ? __half2float(svn[lt * 16 + g + 8]) : 0.f;
       const float wA = pa * vn0, wB = pb * vn1;
       float ps = pa + pb, ws = wA + wB;
 #pragma unroll
