@@ -566,6 +566,7 @@ __global__ void __launch_bounds__(128, 3) k_attn_polar_staged(const Dev kcb, con
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const int64_t L = seq_lens[b];
+  const int L32 = (int)L;                    // token positions in 32 bits (capacity < 2^31)
   const int64_t tend = min(tcap, (L + 15) / 16);
   const int nt = tend > tile0 ? (int)(tend - tile0) : 0;
   const int nst = (nt + kStageTiles - 1) / kStageTiles;
@@ -604,16 +605,16 @@ __global__ void __launch_bounds__(128, 3) k_attn_polar_staged(const Dev kcb, con
     const __half* svn = reinterpret_cast<const __half*>(base + kSK + kSKN + kSV);
     const int t_a = st * kStageTiles, n_here = min(kStageTiles, nt - t_a);
     for (int lt = warp; lt < n_here; lt += 4) {
-      const int64_t t0 = (tile0 + t_a + lt) * 16;
-      const int64_t ta = t0 + g, tb = ta + 8;
+      const int t0 = ((int)tile0 + t_a + lt) * 16;
+      const int ta = t0 + g, tb = ta + 8;
       PKey<BK> ka, kb_;
-      ka.load_row(reinterpret_cast<const uint32_t*>(base + ((size_t)lt * 16 + g) * RBK), skn[lt * 16 + g], c, ta < L);
+      ka.load_row(reinterpret_cast<const uint32_t*>(base + ((size_t)lt * 16 + g) * RBK), skn[lt * 16 + g], c, ta < L32);
       kb_.load_row(reinterpret_cast<const uint32_t*>(base + ((size_t)lt * 16 + g + 8) * RBK), skn[lt * 16 + g + 8], c,
-                   tb < L);
+                   tb < L32);
       float s1a, s1b, s2a, s2b;
       polar_qk<BK>(ktab, sfrag, lane, ka, kb_, c, s1a, s1b, s2a, s2b);
-      const float sa = ta < L ? est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq) * scale_log2 : -INFINITY;
-      const float sb = tb < L ? est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq) * scale_log2 : -INFINITY;
+      const float sa = ta < L32 ? est_polar(ka.nrm, S1 * s1a, fmaf(S2, s2a, K2), kq) * scale_log2 : -INFINITY;
+      const float sb = tb < L32 ? est_polar(kb_.nrm, S1 * s1b, fmaf(S2, s2b, K2), kq) * scale_log2 : -INFINITY;
       float mx = fmaxf(sa, sb);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
@@ -630,8 +631,8 @@ __global__ void __launch_bounds__(128, 3) k_attn_polar_staged(const Dev kcb, con
       }
       const float pa = sa == -INFINITY ? 0.f : exp2f(sa - m_run);
       const float pb = sb == -INFINITY ? 0.f : exp2f(sb - m_run);
-      const float vn0 = ta < L ? __half2float(svn[lt * 16 + g]) : 0.f;
-      const float vn1 = tb < L ? __half2float(svn[lt * 16 + g + 8]) : 0.f;
+      const float vn0 = ta < L32 ? __half2float(svn[lt * 16 + g]) : 0.f;
+      const float vn1 = tb < L32 ? __half2float(svn[lt * 16 + g + 8]) : 0.f;
       const float wA = pa * vn0, wB = pb * vn1;
       float ps = pa + pb;
 #pragma unroll
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(128, 3) k_attn_polar_staged(const Dev kcb, con
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int tok = 2 * c + j + 8 * hk;
-          if (t0 + tok < L) {
+          if (t0 + tok < L32) {
             const uint32_t* r = reinterpret_cast<const uint32_t*>(sv + ((size_t)lt * 16 + tok) * RBV);
             uint32_t wsv[BV], w0v[BV], w6v[BV];
 #pragma unroll
