@@ -53,6 +53,8 @@ def test_descriptor_validation_on_host(L):
     assert L.tq_cache_bytes(None, 10) == 0 and L.tq_record_bytes(None) == 0
     assert L.tq_quantize(None, None, 0, None, 0, 0, 0, None, None) == tq.TQ_EINVAL
     assert L.tq_logits(None, None, 1, 1, 1, 1, None, None, None, None, 0, None) == tq.TQ_EINVAL
+    assert L.tq_append_logits(None, None, None, 0, 1, 128, None, 1, 1, 1, 1, None, None, None, None, 0,
+                              None) == tq.TQ_EINVAL
     assert L.tq_decode_attention(None, None, None, None, 1, 1, 1, 1, None, None, 1.0, None, None, 0, None) == tq.TQ_EINVAL
 
 
