@@ -309,7 +309,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                const float* __restrict__ qinfo, float* __restrict__ lsc, int32_t* __restrict__ lid, int Pmax,
                int* __restrict__ status) {
   constexpr int P = B1 + 1;               // planes per word column (stage 1 + signs)
-  constexpr int W = 8 * P;                // words per record
   using SM = Smem<B1>;
   constexpr int kSlots = SM::kSlots;
   constexpr uint32_t kOffRing = SM::kOffRing, kOffStg = SM::kOffStg, kOffLsc = SM::kOffLsc, kOffLid = SM::kOffLid,
