@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "tq_internal.cuh"
 #include "tq_polar.cuh"
 #include "tq_tc.cuh"
@@ -237,44 +239,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int p = 0; p <= P; ++p) word[p] = 0u;
       float gs = 0.f;
-      // two halves of 16 coordinates: fewer live registers
+      // the column group's 32 coordinates in two halves of 16 (fewer live
+      // registers); XC: the extended (b' + 1)-bit codebook of extra-bit
+      // columns.  The choice is made once per column group, outside the
+      // element loops.
+      auto column_group = [&](auto xc) {
+        constexpr bool XC = decltype(xc)::value;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[16];
-        tmem_ld16(tg + lane_off + 32 * cg + 16 * half, v);
-        uint32_t rh[8], rl[8];
+        for (int half = 0; half < 2; ++half) {
+          float v[16];
+          tmem_ld16(tg + lane_off + 32 * cg + 16 * half, v);
+          uint32_t rh[8], rl[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float r2[2];
+          for (int e = 0; e < 16; e += 2) {
+            float r2[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float y = v[e + u] * inv;
-            const int jb = 16 * half + e + u;       // bit of the column group's words
-            float r;
-            if (EXT && ext) {
-              const int idx = cell_heap<B1 + 1>(y, ltx, s_bndx, word, jb);
-              r = y - s_centx[idx];
-            } else if constexpr (B1 <= 2 && !EXT) {   // (with extra-bit words this measured slower)
-              r = y - cell_cent<B1>(y, lt, cr, word, jb);
-            } else {
-              const int idx = cell_heap<B1>(y, lt, s_bnd, word, jb);
-              r = y - s_cent[idx];
+            for (int u = 0; u < 2; ++u) {
+              const float y = v[e + u] * inv;
+              const int jb = 16 * half + e + u;       // bit of the column group's words
+              float r;
+              if constexpr (XC) {
+                const int idx = cell_heap<B1 + 1>(y, ltx, s_bndx, word, jb);
+                r = y - s_centx[idx];
+              } else if constexpr (B1 <= 2) {
+                r = y - cell_cent<B1>(y, lt, cr, word, jb);
+              } else {
+                const int idx = cell_heap<B1>(y, lt, s_bnd, word, jb);
+                r = y - s_cent[idx];
+              }
+              gs = fmaf(r, r, gs);
+              r2[u] = r;
             }
-            gs = fmaf(r, r, gs);
-            r2[u] = r;
+            // bf16 hi + lo pieces of the residual pair
+            const uint32_t hb = bf16x2(r2[0], r2[1]);
+            rh[e >> 1] = hb;
+            rl[e >> 1] = bf16x2(r2[0] - __uint_as_float(hb << 16), r2[1] - __uint_as_float(hb & 0xFFFF0000u));
           }
-          // bf16 hi + lo pieces of the residual pair
-          const uint32_t hb = bf16x2(r2[0], r2[1]);
-          rh[e >> 1] = hb;
-          rl[e >> 1] = bf16x2(r2[0] - __uint_as_float(hb << 16), r2[1] - __uint_as_float(hb & 0xFFFF0000u));
+          if (prod) {
+            // A operand of the sketch in tensor memory: lane = row, column
+            // 16 cg + i holds coordinates 32 cg + 2i (low half) and 2i + 1
+            tmem_st8(t_rhi + lane_off + 16 * cg + 8 * half, rh);
+            tmem_st8(t_rlo + lane_off + 16 * cg + 8 * half, rl);
+          }
         }
-        if (prod) {
-          // A operand of the sketch in tensor memory: lane = row, column
-          // 16 cg + i holds coordinates 32 cg + 2i (low half) and 2i + 1
-          tmem_st8(t_rhi + lane_off + 16 * cg + 8 * half, rh);
-          tmem_st8(t_rlo + lane_off + 16 * cg + 8 * half, rl);
-        }
-      }
+      };
+      if (EXT && ext)
+        column_group(std::integral_constant<bool, EXT>{});
+      else
+        column_group(std::integral_constant<bool, false>{});
       red2[cg * kRows + m] = gs;
     }
     }
